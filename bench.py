@@ -1,0 +1,474 @@
+#!/usr/bin/env python3
+"""Benchmark: paged decode attention, KV-read HBM GB/s, D=256 GQA 6:1.
+
+Workload (the decode benchmark of opengfx1030/vllm-rdna pull request #33,
+"Test Plan" step 3, at the D=256 6:1 geometry of its results comment): Hq=24,
+Hkv=4, D=256, qlen=1, fp16 Q/K/V ~ N(0,1), block_size 16, seq_len 4096 for
+every sequence, random-permuted block tables, balanced split. The headline
+step is one decode_paged call over B=32 sequences; the batch sweep B in
+{1,2,3,8,32} is reported beside it.
+
+One step = one call of the whole path (page translation, KV gather, scores,
+masking, online softmax, P.V, split combine: one kernel launch). KV bytes are
+the algorithmic K+V bytes of the visible keys. Cold L2: every step reads its
+KV through a different block table over a pool at least 4x the L2 size, so no
+step finds the previous step's KV in L2. The K timed steps are captured in a
+CUDA graph and replayed once between CUDA events on the launching stream
+(removes host launch overhead only).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores instead (the
+only other implementation available); under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from paged_split_decode_gb300 import inputs  # noqa: E402
+
+METRIC = "paged decode attn: KV-read HBM GB/s (% of GB300 peak), us/call, D=256 GQA 6:1"
+UNIT = "GB/s"
+HEADLINE_B = 32
+SWEEP_B = (1, 2, 3, 8, 32)
+HQ, HKV, D, SEQ_LEN, BS = 24, 4, 256, 4096, 16
+KERNEL_SOURCES = ["paged_split_decode_gb300/csrc/decode_kernel.cuh",
+                  "paged_split_decode_gb300/csrc/ptx.cuh",
+                  "paged_split_decode_gb300/csrc/decode_f16_d256.cu",
+                  "paged_split_decode_gb300/csrc/launch.h",
+                  "paged_split_decode_gb300/csrc/pdecode_api.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_f16_d256_gqa6_b32_traffic.md")
+
+
+def kv_bytes_of(seq_lens, qlen, window, Hkv, Dh, elem):
+    """Algorithmic KV bytes: each visible key once per (sequence, KV head), K and V."""
+    total = 0
+    for L in seq_lens:
+        if L <= 0:
+            continue
+        first = max(0, L - qlen - window + 1) if window > 0 else 0
+        total += L - first
+    return total * Hkv * Dh * elem * 2
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def traffic_per_launch():
+    """dram read+write bytes per launch from the committed ncu summary, or None
+    when the summary is missing or was taken on other kernel sources."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    txt = open(TRAFFIC_FILE).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", txt)
+    hsh = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
+    if not m or not hsh or hsh.group(1) != kernel_hash():
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples (every 50 ms) stamped on arrival; the
+    summary keeps the samples that arrived during the timed region (plus 100 ms
+    of slack for nvidia-smi's own reporting delay)."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.samples = []
+        self.t0 = self.t1 = None
+
+    def _reader(self):
+        for ln in self.proc.stdout:
+            if ln.strip():
+                self.samples.append((time.monotonic(), ln.strip()))
+
+    def __enter__(self):
+        import threading
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._reader, daemon=True)
+            self.th.start()
+            t_wait = time.monotonic()
+            while not self.samples and time.monotonic() - t_wait < 5:
+                time.sleep(0.01)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def mark_start(self):
+        self.t0 = time.monotonic()
+
+    def mark_end(self):
+        self.t1 = time.monotonic()
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.th.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons, n_in = [], None, set(), 0
+        t0 = self.t0 or 0.0
+        t1 = (self.t1 or t0) + 0.1
+        rows = [(t, ln) for t, ln in self.samples if t0 <= t <= t1]
+        if not rows and self.samples:  # region shorter than one period: nearest sample after it
+            after = [(t, ln) for t, ln in self.samples if t >= t0]
+            rows = after[:1]
+        for _, ln in rows:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            n_in += 1
+            for n, v in zip(self.NAMES, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": n_in, "region_ms": round(((self.t1 or t0) - t0) * 1e3, 2)}
+
+
+def gpu_smi_id(device):
+    props = torch.cuda.get_device_properties(device)
+    u = getattr(props, "uuid", None)
+    if u is not None:
+        u = str(u)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    return str(device.index or 0)
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+class Rotation:
+    """n_rot disjoint block tables over one device pool (cold L2 per step)."""
+
+    def __init__(self, B, device, l2_bytes, seed):
+        gen = torch.Generator().manual_seed(seed)
+        nblk = (SEQ_LEN + BS - 1) // BS
+        per_table = B * nblk
+        blk_bytes = BS * HKV * D * 2
+        footprint = per_table * blk_bytes * 2
+        self.n_rot = max(2, -(-4 * l2_bytes // footprint))
+        pool = self.n_rot * per_table
+        ids = torch.randperm(pool, generator=gen).to(torch.int32)
+        self.tables = [ids[r * per_table:(r + 1) * per_table].view(B, nblk).contiguous().to(device)
+                       for r in range(self.n_rot)]
+        # pool values: N(0,1) fp16 drawn on the device from a seeded generator
+        dg = torch.Generator(device=device).manual_seed(seed + 1)
+        self.k = torch.randn((pool, BS, HKV, D), generator=dg, device=device,
+                             dtype=torch.float32).to(torch.float16)
+        self.v = torch.randn((pool, BS, HKV, D), generator=dg, device=device,
+                             dtype=torch.float32).to(torch.float16)
+        self.q = torch.randn((B, HQ, D), generator=dg, device=device,
+                             dtype=torch.float32).to(torch.float16)
+        self.seq_lens = torch.full((B,), SEQ_LEN, dtype=torch.int32, device=device)
+        self.out = torch.empty_like(self.q)
+        self.B = B
+
+
+def time_device(B, steps, warmup, device, l2_bytes, seed, world):
+    import paged_split_decode_gb300 as pd
+    rot = Rotation(B, device, l2_bytes, seed)
+    scale = 1.0 / D ** 0.5
+    stream = torch.cuda.Stream(device)
+    dims = pd.dims_of(rot.q, rot.k, rot.tables[0], 1)
+    ws = pd.get_workspace(device, pd.workspace_bytes(dims, 1, 0))
+    flag = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def call(r):
+        pd.decode_paged(rot.q, rot.k, rot.v, rot.tables[r % rot.n_rot], rot.seq_lens, scale, 0, 1,
+                        0, out=rot.out, workspace=ws, error_flag=flag)
+
+    with torch.cuda.stream(stream):
+        for r in range(warmup):
+            call(r)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for r in range(steps):
+            call(warmup + r)
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    with ClockSampler(gpu_smi_id(device)) as clk, torch.cuda.stream(stream):
+        clk.mark_start()
+        start.record(stream)
+        graph.replay()  # launches on the current stream, i.e. `stream`
+        end.record(stream)
+        end.synchronize()
+        clk.mark_end()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    ms = start.elapsed_time(end)
+    if int(flag.item()) != 0:
+        raise RuntimeError(f"device error flag {int(flag.item())}")
+    del graph
+    return ms, clk.summary(), rot
+
+
+def time_e2e(B, steps, warmup, device, seed, world):
+    """Public API with host buffers: H2D of the step's inputs (pinned), the
+    call, D2H of the output, all inside the timed region."""
+    import paged_split_decode_gb300 as pd
+    gen = torch.Generator().manual_seed(seed)
+    nblk = (SEQ_LEN + BS - 1) // BS
+    pool = B * nblk
+    table = torch.randperm(pool, generator=gen).to(torch.int32).view(B, nblk).pin_memory()
+    k = torch.randn((pool, BS, HKV, D), generator=gen).to(torch.float16).pin_memory()
+    v = torch.randn((pool, BS, HKV, D), generator=gen).to(torch.float16).pin_memory()
+    q = torch.randn((B, HQ, D), generator=gen).to(torch.float16).pin_memory()
+    lens = torch.full((B,), SEQ_LEN, dtype=torch.int32).pin_memory()
+    out_h = torch.empty((B, HQ, D), dtype=torch.float16).pin_memory()
+    dq, dk, dv = (torch.empty_like(x, device=device) for x in (q, k, v))
+    dt, dl = torch.empty_like(table, device=device), torch.empty_like(lens, device=device)
+    dout = torch.empty_like(dq)
+    scale = 1.0 / D ** 0.5
+    h2d = sum(x.numel() * x.element_size() for x in (q, k, v, table, lens))
+    d2h = out_h.numel() * out_h.element_size()
+
+    def step():
+        for dst, src in ((dq, q), (dk, k), (dv, v), (dt, table), (dl, lens)):
+            dst.copy_(src, non_blocking=True)
+        pd.decode_paged(dq, dk, dv, dt, dl, scale, 0, 1, 0, out=dout)
+        out_h.copy_(dout, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        step()
+    e.record()
+    e.synchronize()
+    barrier(world)
+    return s.elapsed_time(e), h2d, d2h
+
+
+def cpu_oracle_rate(B, budget_s=10.0, seed=777, max_seqs=None):
+    """Time the fp64 oracle on the host cores over whole sequences of the
+    workload; returns (GB/s of KV, cores, sample description, seconds/step)."""
+    import oracle
+    n = B if max_seqs is None else min(B, max_seqs)
+    w = inputs.gqa_d256(n, seed=seed)
+    args = (w.q.numpy(), w.k_cache.numpy(), w.v_cache.numpy(), w.block_table.numpy(),
+            w.seq_lens.numpy(), w.scale)
+    cores = oracle.default_threads()
+    oracle.decode_paged(*args, threads=cores)  # warm (builds if needed)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.decode_paged(*args, threads=cores)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    kvb = kv_bytes_of(w.seq_lens.tolist(), 1, 0, HKV, D, 2)
+    return kvb / dt / 1e9, cores, f"{n} of {B} sequences x all 24 heads, {reps} runs", dt
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    B = HEADLINE_B
+    # bounded sample per step: 4 sequences of the B=32 batch
+    nseq = 4
+    w = inputs.gqa_d256(nseq, seed=4242)
+    cores = oracle.default_threads()
+    a = (w.q.numpy(), w.k_cache.numpy(), w.v_cache.numpy(), w.block_table.numpy(),
+         w.seq_lens.numpy(), w.scale)
+    for _ in range(args.warmup):
+        oracle.decode_paged(*a, threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode_paged(*a, threads=cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    kvb = kv_bytes_of(w.seq_lens.tolist(), 1, 0, HKV, D, 2)
+    val = kvb / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(B),
+        "cpu_baseline": {"value": round(val, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{nseq} of {B} sequences x all 24 heads per step"},
+        "e2e": {"value": round(val, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(B):
+    return {"workload": f"gqa6_d256_L{SEQ_LEN}_b{B}", "B": B, "Hq": HQ, "Hkv": HKV, "D": D,
+            "qlen": 1, "seq_len": SEQ_LEN, "block_size": BS, "block_table": "random-permuted",
+            "num_splits": "auto (balanced)", "kv_dtype": "fp16",
+            "l2": "inputs larger than L2: each step reads its KV through a different block table "
+                  "over a pool >= 4x L2", "launch": "CUDA graph of the K steps, replayed once",
+            "parallelism": "replicas (one per GPU, no collective)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    from paged_split_decode_gb300 import build as pkg_build
+    import paged_split_decode_gb300 as pd
+    if rank == 0 or world == 1:
+        pkg_build.build()
+    barrier(world)
+    pd.load()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    peak, peak_kind = measured_peaks()
+
+    sweep = []
+    Bs = [HEADLINE_B] if args.no_sweep else list(SWEEP_B)
+    head = None
+    for B in Bs:
+        ms, clk, rot = time_device(B, args.steps, args.warmup, device, l2, 1000 + B + 17 * rank, world)
+        ms = max_over_ranks(ms, world, device)
+        per = ms / args.steps
+        kvb = kv_bytes_of([SEQ_LEN] * B, 1, 0, HKV, D, 2)
+        gbs = kvb / (per * 1e-3) / 1e9
+        ent = {"B": B, "us_per_call": round(per * 1e3, 3), "kv_gbs": round(gbs, 1),
+               "frac_of_peak": round(gbs / peak, 4), "kv_bytes": kvb,
+               "grid_ctas": pd.grid_ctas(pd.dims_of(rot.q, rot.k, rot.tables[0], 1), 1, 0)}
+        sweep.append(ent)
+        if B == HEADLINE_B:
+            head = (ms, per, kvb, gbs, clk)
+        del rot
+        torch.cuda.empty_cache()
+    ms, per, kvb, gbs, clk = head
+    total_bytes = kvb * world
+    value = total_bytes / (ms / args.steps * 1e-3) / 1e9
+
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 10))
+    e_ms, h2d, d2h = time_e2e(HEADLINE_B, e2e_steps, 2, device, 99 + rank, world)
+    e_ms = max_over_ranks(e_ms, world, device)
+    e2e_val = kvb * world / (e_ms / e2e_steps * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        rate, cores, sample, _ = cpu_oracle_rate(HEADLINE_B, budget_s=10.0, max_seqs=4)
+        cpu = {"value": round(rate, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": sample + " (D=256 GQA 6:1, L=4096)"}
+    traffic = traffic_per_launch()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5),
+            "us_per_call": round(per * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": workload_config(HEADLINE_B),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                         "traffic": traffic,
+                         "algorithmic_bytes_per_launch": kvb,
+                         "kernel": "decode_paged_kernel<D=256,f16,NT=1>"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_val, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": args.steps,
+            "clocks": clk,
+            "sweep": sweep,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

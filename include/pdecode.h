@@ -1,0 +1,160 @@
+/*
+ * pdecode.h -- C ABI of libpdecode: paged split-K decode attention on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes follows opengfx1030/vllm-rdna pull request #33
+ * ("Paged split-K decode"):
+ *   - "Purpose": a per-head decode over a paged KV cache -- page lookups
+ *     through a block table, scores scale * q . k, online softmax, P.V, and
+ *     split-K partials merged by a combine; fp16 and fp8 KV share the body;
+ *     every launch runs on the caller's current stream;
+ *   - "What changed vs the old #33 diff": an empty key range never enters the
+ *     P.V loop (empty rows are zero);
+ *   - "Test Plan" step 2: the decode cells -- writer layout, empty rows are
+ *     zero, a custom scale written into a caller-owned `out`, a paged sliding
+ *     window, multi-token (speculative verify) queries, split decode;
+ *   - "Test Result": the split-K schedule must agree with a one-shot fp64
+ *     reference.
+ *
+ * Readings where the page is silent:
+ *   - seq_lens[b] counts every cached key of sequence b, including its qlen
+ *     query tokens; query token i sits at position p = seq_lens[b] - qlen + i
+ *     and sees keys j <= p (causal among the query tokens);
+ *   - window W > 0 keeps keys p - W + 1 <= j <= p; W <= 0 disables it;
+ *   - query head h reads KV head h / (Hq / Hkv);
+ *   - a row with no visible key is written as zeros.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous
+ *     and row-major, on the device that is current when the call is made. The
+ *     library never allocates, frees or synchronises; it launches on `stream`
+ *     (a cudaStream_t; NULL = the legacy default stream) and returns at once.
+ *   - Host-checkable problems are reported through the return value before
+ *     anything is launched. PD_ERR_CUDA means a launch or runtime call failed;
+ *     cudaGetLastError() then holds the CUDA error.
+ *   - Data errors that only the device can see (a block id outside
+ *     [0, num_blocks), a seq_len outside [0, max_blocks_per_seq*block_size],
+ *     a pipeline wait that ran past its time limit) never trap: the kernel
+ *     sets a bit of *error_flag (if error_flag is not NULL) with atomicOr and
+ *     carries on; the affected rows are then unspecified. The caller clears
+ *     the flag.
+ *   - There is no CPU fallback and no alternative back end: shapes the
+ *     kernels do not implement return PD_ERR_UNSUPPORTED.
+ */
+#ifndef PDECODE_H
+#define PDECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PD_API __attribute__((visibility("default")))
+#else
+#define PD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PD_OK = 0,
+  PD_ERR_NULL = 1,        /* a required pointer is NULL */
+  PD_ERR_SHAPE = 2,       /* sizes are inconsistent or out of range */
+  PD_ERR_DTYPE = 3,       /* unknown KV dtype */
+  PD_ERR_UNSUPPORTED = 4, /* legal, but no kernel here implements it */
+  PD_ERR_ALIGN = 5,       /* a pointer is not 16-byte aligned */
+  PD_ERR_WORKSPACE = 6,   /* workspace missing or smaller than pd_workspace_bytes */
+  PD_ERR_CUDA = 7         /* a CUDA runtime call or launch failed */
+} pd_status;
+
+typedef enum {
+  PD_KV_F16 = 0,      /* K and V caches hold IEEE binary16 */
+  PD_KV_FP8_E4M3 = 1  /* K and V caches hold OCP e4m3fn codes; value = code * scale */
+} pd_kv_dtype;
+
+/* Bits written into *error_flag by the device. */
+#define PD_DEVERR_BLOCK_ID 1u /* a block_table entry used by the call is outside [0, num_blocks) */
+#define PD_DEVERR_SEQ_LEN 2u  /* a seq_len is negative or above max_blocks_per_seq*block_size */
+#define PD_DEVERR_TIMEOUT 4u  /* a pipeline wait ran past its limit; the call gave up */
+
+/* Shapes of one call.
+ *   B                  number of sequences (rows of block_table / seq_lens)
+ *   Hq, Hkv            query and KV heads; Hq % Hkv == 0
+ *   D                  head size; the kernels implement 128 and 256
+ *   block_size         keys per cache block; a multiple of 16
+ *   num_blocks         blocks in each of the K and V caches
+ *   max_blocks_per_seq columns of block_table
+ *   kv_dtype           pd_kv_dtype
+ *   k_scale, v_scale   fp8 only: per-cache dequantisation scales (ignored for fp16) */
+typedef struct {
+  int32_t B, Hq, Hkv, D;
+  int32_t block_size, num_blocks, max_blocks_per_seq;
+  int32_t kv_dtype;
+  float k_scale, v_scale;
+} pd_dims;
+
+/* Workspace bytes that decode_paged needs for these shapes, qlen and
+ * num_splits (0 = balanced automatic split) on a device with sm_count SMs
+ * (sm_count <= 0: the current device's). 0 means no workspace is needed (the
+ * pointer may then be NULL). Layout: a fixed 64 KiB header of split tickets,
+ * then the fp32 split partials. The header must be zero-filled once before the
+ * buffer's first use; every call that completes leaves it zero again, whatever
+ * the shapes of the call, so one buffer serves any sequence of calls on one
+ * stream. Calls that may run at the same time must not share a workspace.
+ * With num_splits > 1, B*Hkv may be at most 16384. Returns 0 for invalid dims. */
+PD_API size_t pd_workspace_bytes(const pd_dims* dims, int qlen, int num_splits, int sm_count);
+
+/* Number of CTAs decode_paged launches for these arguments (persistent grid),
+ * or 0 for invalid dims. Host-only; no device work. */
+PD_API int pd_grid_ctas(const pd_dims* dims, int qlen, int num_splits, int sm_count);
+
+/* Paged decode attention, split-K over keys, GQA heads packed per CTA.
+ *
+ *   q            fp16 [B*qlen, Hq, D]; row b*qlen + i is query token i of sequence b
+ *   k_cache      [num_blocks, block_size, Hkv, D] fp16 or e4m3fn (dims->kv_dtype)
+ *   v_cache      same layout and dtype as k_cache
+ *   block_table  int32 [B, max_blocks_per_seq]; entry [b][n] is the physical
+ *                block holding keys n*block_size .. n*block_size+block_size-1 of
+ *                sequence b. Only the entries of blocks holding visible keys are read.
+ *   seq_lens     int32 [B]; keys cached for each sequence, query tokens included
+ *   scale        multiplies q . k (e.g. 1/sqrt(D))
+ *   window       sliding window in keys (<= 0: none)
+ *   qlen         query tokens per sequence, 1..8; Hq/Hkv*qlen must be <= 32
+ *   num_splits   0: balanced split of all visible key tiles over the SMs;
+ *                >= 1: each sequence's visible tiles cut into num_splits
+ *                contiguous chunks (1 = no split)
+ *   out          fp16 [B*qlen, Hq, D], written in full (rows without a visible
+ *                key are zeros); must not overlap the inputs
+ *   workspace    device buffer of >= pd_workspace_bytes(...) bytes, zero-filled
+ *                before its first use (see pd_workspace_bytes)
+ *   error_flag   device uint32 or NULL (see PD_DEVERR_*)
+ *   stream       cudaStream_t to launch on
+ * All pointers must be 16-byte aligned. */
+PD_API pd_status decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_table, const int32_t* seq_lens, float scale,
+                       int window, int qlen, int num_splits, void* out, const pd_dims* dims,
+                       void* workspace, size_t workspace_bytes, uint32_t* error_flag,
+                       void* stream);
+
+/* Split-K combine on its own (the combine step of "Purpose" and of the
+ * schedule model in "Test Result"). For each of `rows` rows and S partials:
+ *   part_m  fp32 [rows, S]     largest score of the chunk, natural-log units
+ *                              (-inf for an empty chunk)
+ *   part_l  fp32 [rows, S]     sum over the chunk of exp(s_j - m)
+ *   part_o  fp32 [rows, S, D]  sum over the chunk of exp(s_j - m) * V_j
+ *   out     fp16 [rows, D]     sum_s w_s O_s / sum_s w_s l_s with
+ *                              w_s = exp(m_s - max_s m_s); zeros when every
+ *                              chunk is empty
+ * D is 1..1024 and a multiple of 8. */
+PD_API pd_status decode_paged_combine(const float* part_m, const float* part_l, const float* part_o,
+                               int rows, int num_splits, int D, void* out, void* stream);
+
+/* Human-readable name of a status. */
+PD_API const char* pd_status_str(pd_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PDECODE_H */

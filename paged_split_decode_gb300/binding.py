@@ -1,0 +1,187 @@
+"""Thin ctypes binding over libpdecode (C ABI in include/pdecode.h).
+
+Argument marshalling only: tensors become device pointers, the current torch
+stream becomes the launch stream, a status other than PD_OK becomes an
+exception. Every step of the computation runs in the library's CUDA kernels;
+there is no CPU or PyTorch fallback, and a missing library is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpdecode.so")
+_lib = None
+_lock = threading.Lock()
+
+PD_KV_F16 = 0
+PD_KV_FP8_E4M3 = 1
+DEVERR_BLOCK_ID = 1
+DEVERR_SEQ_LEN = 2
+DEVERR_TIMEOUT = 4
+
+EXPORTS = ("decode_paged", "decode_paged_combine", "pd_workspace_bytes", "pd_grid_ctas",
+           "pd_status_str")
+
+
+class PdDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_blocks", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float)]
+
+
+class DecodeError(RuntimeError):
+    pass
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libpdecode.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(f"{_LIB_PATH} is missing: build it first "
+                                   "(paged_split_decode_gb300.build.build())")
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            lib.pd_status_str.argtypes = [ctypes.c_int]
+            lib.pd_status_str.restype = ctypes.c_char_p
+            lib.pd_workspace_bytes.argtypes = [ctypes.POINTER(PdDims), ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int]
+            lib.pd_workspace_bytes.restype = ctypes.c_size_t
+            lib.pd_grid_ctas.argtypes = [ctypes.POINTER(PdDims), ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int]
+            lib.pd_grid_ctas.restype = ctypes.c_int
+            lib.decode_paged.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, P, ctypes.POINTER(PdDims), P,
+                                         ctypes.c_size_t, P, P]
+            lib.decode_paged.restype = ctypes.c_int
+            lib.decode_paged_combine.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                 P, P]
+            lib.decode_paged_combine.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def status_str(code: int) -> str:
+    return load().pd_status_str(code).decode()
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise DecodeError(f"{what}: {status_str(code)} (status {code})")
+
+
+def make_dims(B, Hq, Hkv, D, block_size, num_blocks, max_blocks_per_seq, kv_fp8=False,
+              k_scale=1.0, v_scale=1.0) -> PdDims:
+    return PdDims(int(B), int(Hq), int(Hkv), int(D), int(block_size), int(num_blocks),
+                  int(max_blocks_per_seq), PD_KV_FP8_E4M3 if kv_fp8 else PD_KV_F16,
+                  float(k_scale), float(v_scale))
+
+
+def dims_of(q, k_cache, block_table, qlen, kv_fp8=False, k_scale=1.0, v_scale=1.0) -> PdDims:
+    num_blocks, bs, Hkv, D = k_cache.shape
+    return make_dims(block_table.shape[0], q.shape[1], Hkv, D, bs, num_blocks,
+                     block_table.shape[1], kv_fp8, k_scale, v_scale)
+
+
+def workspace_bytes(dims: PdDims, qlen: int, num_splits: int, sm_count: int = 0) -> int:
+    return int(load().pd_workspace_bytes(ctypes.byref(dims), int(qlen), int(num_splits),
+                                         int(sm_count)))
+
+
+def grid_ctas(dims: PdDims, qlen: int, num_splits: int, sm_count: int = 0) -> int:
+    return int(load().pd_grid_ctas(ctypes.byref(dims), int(qlen), int(num_splits), int(sm_count)))
+
+
+_workspaces: dict = {}
+
+
+def get_workspace(device: torch.device, nbytes: int) -> torch.Tensor | None:
+    """A zero-filled, reusable workspace per device, grown on demand.
+
+    The kernels leave it zero-filled after every completed call, so one buffer
+    serves every call made on one stream. Pass your own buffer to
+    decode_paged for calls that may overlap on different streams."""
+    if nbytes == 0:
+        return None
+    key = (device.type, device.index)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def _dev_ptr(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    return t.data_ptr()
+
+
+def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, qlen=1,
+                 num_splits=0, out=None, *, k_scale=1.0, v_scale=1.0, workspace=None,
+                 error_flag=None, stream=None):
+    """Paged decode attention on the GPU; returns ``out`` (fp16 [B*qlen, Hq, D]).
+
+    ``k_cache``/``v_cache`` are fp16, or uint8 / float8_e4m3fn holding e4m3fn
+    codes (then ``k_scale``/``v_scale`` apply). ``num_splits`` 0 = balanced.
+    """
+    lib = load()
+    kv_fp8 = k_cache.dtype in (torch.uint8, torch.float8_e4m3fn)
+    kv_dt = (torch.uint8, torch.float8_e4m3fn) if kv_fp8 else torch.float16
+    dims = dims_of(q, k_cache, block_table, qlen, kv_fp8, k_scale, v_scale)
+    if out is None:
+        out = torch.empty_like(q)
+    if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype:
+        raise ValueError("v_cache must match k_cache in shape and dtype")
+    if q.dim() != 3 or q.shape[0] != block_table.shape[0] * qlen or seq_lens.numel() != block_table.shape[0]:
+        raise ValueError("q must be [B*qlen, Hq, D] with B = rows of block_table and seq_lens")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    need = workspace_bytes(dims, qlen, num_splits)
+    if workspace is None:
+        workspace = get_workspace(q.device, need)
+    ws_ptr = 0 if workspace is None else _dev_ptr(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    flag_ptr = None if error_flag is None else _dev_ptr(error_flag, "error_flag", (torch.int32, torch.uint32))
+    rc = lib.decode_paged(_dev_ptr(q, "q", torch.float16), _dev_ptr(k_cache, "k_cache", kv_dt),
+                          _dev_ptr(v_cache, "v_cache", kv_dt),
+                          _dev_ptr(block_table, "block_table", torch.int32),
+                          _dev_ptr(seq_lens, "seq_lens", torch.int32), float(scale), int(window),
+                          int(qlen), int(num_splits), _dev_ptr(out, "out", torch.float16),
+                          ctypes.byref(dims), ws_ptr or None, ws_bytes, flag_ptr, stream)
+    _check(rc, "decode_paged")
+    return out
+
+
+def decode_paged_combine(part_m, part_l, part_o, out=None, *, stream=None):
+    """Split-K combine: part_m/part_l fp32 [rows, S] (natural-log m), part_o fp32
+    [rows, S, D] -> fp16 [rows, D]."""
+    lib = load()
+    rows, S, D = part_o.shape
+    if out is None:
+        out = torch.empty((rows, D), dtype=torch.float16, device=part_o.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(part_o.device).cuda_stream
+    rc = lib.decode_paged_combine(_dev_ptr(part_m, "part_m", torch.float32),
+                                  _dev_ptr(part_l, "part_l", torch.float32),
+                                  _dev_ptr(part_o, "part_o", torch.float32), int(rows), int(S),
+                                  int(D), _dev_ptr(out, "out", torch.float16), stream)
+    _check(rc, "decode_paged_combine")
+    return out

@@ -1,0 +1,37 @@
+// decode_f16_d256.cu -- instantiations of the decode kernel for f16 KV, D=256.
+// NT = row tiles of 8 query rows (rows per unit = Hq/Hkv * qlen <= 8*NT);
+// KG = key groups; the ring takes as many stages as shared memory allows.
+#include "launch.h"
+
+namespace pd {
+namespace {
+constexpr bool kFp8 = false;
+constexpr int kD = 256;
+using C1 = Cfg<kD, kFp8, 1, 4, ring_stages<kD, kFp8, 1, 4>()>;
+using C2 = Cfg<kD, kFp8, 2, 2, ring_stages<kD, kFp8, 2, 2>()>;
+using C3 = Cfg<kD, kFp8, 3, 2, ring_stages<kD, kFp8, 3, 2>()>;
+using C4 = Cfg<kD, kFp8, 4, 2, ring_stages<kD, kFp8, 4, 2>()>;
+}  // namespace
+
+bool shape_f16_d256(int nt, KernelShape* out) {
+  switch (nt) {
+    case 1: return shape_of<C1>(out);
+    case 2: return shape_of<C2>(out);
+    case 3: return shape_of<C3>(out);
+    case 4: return shape_of<C4>(out);
+    default: return false;
+  }
+}
+
+cudaError_t launch_f16_d256(int nt, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const DecodeParams& p, int grid, cudaStream_t s) {
+  switch (nt) {
+    case 1: return launch_cfg<C1>(tk, tv, p, grid, s);
+    case 2: return launch_cfg<C2>(tk, tv, p, grid, s);
+    case 3: return launch_cfg<C3>(tk, tv, p, grid, s);
+    case 4: return launch_cfg<C4>(tk, tv, p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pd

@@ -1,0 +1,741 @@
+// decode_kernel.cuh -- paged split-K decode attention for sm_103a.
+//
+// Computes, for every sequence b, query token i and query head h, the softmax
+// of scale * q . k over the keys the token sees, weighted over V (the per-head
+// paged decode of opengfx1030/vllm-rdna pull request #33, "Purpose"), reading
+// K and V through an int32 block table from caches laid out
+// [num_blocks, block_size, Hkv, D].
+//
+// GB300 design (the pull request's RDNA2 schedule is prior art only):
+//  * Work unit = (sequence b, KV head kh). All G*qlen query rows that read kh
+//    are packed into one CTA, so each K/V byte crosses HBM once.
+//  * Persistent grid, one CTA per SM. The visible key tiles (16 keys each) of
+//    all units are laid end to end and cut into equal contiguous ranges, one
+//    per CTA (balanced split-K). A fixed num_splits instead cuts each unit
+//    into num_splits chunks handed out round robin.
+//  * One producer warp walks the CTA's tiles, reads block-table entries 32 at
+//    a time (the next group is prefetched while the current one is issued)
+//    and issues TMA bulk-tensor loads of the K and V tiles into an NS-stage
+//    ring of 128B-swizzled shared-memory slabs, completed on mbarriers.
+//  * Consumer warps are (row tile nt, key group kg): warp (nt, kg) takes the
+//    ring's tiles kg, kg+KG, ... for query rows 8nt..8nt+7. Per tile it forms
+//    S^T = K Q^T with mma.sync m16n8k16 (keys on M, query rows on N, Q held in
+//    registers), masks, runs the online softmax with warp shuffles, turns P
+//    into the B operand with movmatrix and accumulates O^T = V^T P^T.
+//    fp8 e4m3 tiles are widened to fp16 in registers (cvt.f16x2.e4m3x2); the
+//    K scale is folded into the score scale and the V scale into the output.
+//  * At the end of a unit piece the KG key groups merge (m, l, O) through
+//    shared memory. A unit covered by one piece is normalised and written as
+//    fp16; otherwise the piece writes an fp32 partial and bumps the unit's
+//    ticket; the piece that arrives last merges all partials in a fixed
+//    order (deterministic) and writes the row, then resets the ticket.
+//  * Every mbarrier wait is bounded in wall time; on expiry the kernel raises
+//    an error bit and runs the rest of its control flow without waiting, so
+//    named barriers and tickets stay consistent and the CTA always exits.
+#pragma once
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace pd {
+
+constexpr int kTileKeys = 16;      // keys per pipeline tile
+constexpr int kMaxAutoB = 2048;    // sequences handled by the balanced split
+// The workspace opens with a fixed header of split tickets that every call
+// layout shares and leaves at zero; partials follow it and never overlap it.
+constexpr int kTickets = 16384;
+constexpr uint32_t kErrBlockId = 1u, kErrSeqLen = 2u, kErrTimeout = 4u;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DecodeParams {
+  const __half* q;            // [B*qlen, Hq, D]
+  __half* out;                // [B*qlen, Hq, D]
+  const int32_t* block_table; // [B, max_blocks]
+  const int32_t* seq_lens;    // [B]
+  float* ws_o;                // [slots, RP, D]   partial O (log2-domain weights)
+  float* ws_ml;               // [slots, RP, 2]   partial (m, l), m in log2 units
+  int* ws_count;              // [kTickets]       split tickets (zero between calls)
+  uint32_t* error_flag;       // may be null
+  int B, qlen, Hq, Hkv, G, R;
+  int max_blocks, block_size, num_blocks, tiles_per_block;
+  int window;                 // <= 0: none
+  int num_splits;             // 0: balanced
+  float sl2;                  // scale * log2(e) * k_scale
+  float out_scale;            // v_scale (1 for fp16)
+  unsigned long long timeout_ns;
+};
+
+template <int D_, bool FP8_, int NT_, int KG_, int NS_>
+struct Cfg {
+  static constexpr int D = D_, NT = NT_, KG = KG_, NS = NS_;
+  static constexpr bool FP8 = FP8_;
+  static constexpr int kElem = FP8 ? 1 : 2;
+  static constexpr int kSlabElems = 128 / kElem;        // one 128-byte swizzle row
+  static constexpr int kSlabs = D / kSlabElems;
+  static constexpr int kSlabBytes = kTileKeys * 128;    // 2 KB, 1024-aligned
+  static constexpr int kTileBytes = kSlabs * kSlabBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;    // K tile then V tile
+  static constexpr int kConsumerWarps = NT * KG;
+  static constexpr int kConsumerThreads = kConsumerWarps * 32;
+  static constexpr int kThreads = kConsumerThreads + 32;
+  static constexpr int RP = NT * 8;
+  static constexpr int kDP = D + 4;                     // merge row pitch (floats)
+  static constexpr int kMergeOBytes = NT * 8 * kDP * 4;        // one buffer per row tile
+  static constexpr int kMergeMLBytes = kConsumerWarps * 8 * 2 * 4;
+  static constexpr int kOffMergeO = NS * kStageBytes;
+  static constexpr int kOffMergeML = kOffMergeO + kMergeOBytes;
+  static constexpr int kOffBars = (kOffMergeML + kMergeMLBytes + 15) / 16 * 16;
+  static constexpr int kOffPre = kOffBars + 2 * NS * 8;
+  static constexpr int kOffMisc = kOffPre + (kMaxAutoB + 1) * 4;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+  static_assert(D % kSlabElems == 0, "D must be a multiple of the slab width");
+  static_assert(D % 32 == 0, "D must be a multiple of 32");
+};
+
+// ---------------------------------------------------------------------------
+// Work decomposition shared by the producer and the consumers. Both walk the
+// same sequence of pieces, so the ring's tile order matches on both sides.
+struct Piece {
+  int b, kh, L;
+  int first_tile;   // tile index (within the sequence) of the piece's first tile
+  int ntiles;       // tiles in this piece (0: a zero-fill piece for an empty unit)
+  int npieces;      // pieces the unit was cut into (1: write the output directly)
+  int slot;         // workspace slot of this piece's partial (npieces > 1)
+  int ticket;       // ticket of the unit (npieces > 1): balanced mode the CTA that
+                    // holds its first piece (each CTA starts at most one split unit),
+                    // fixed mode the unit index
+  int unit_t0;      // first visible tile of the unit (within the sequence)
+  int unit;         // b * Hkv + kh
+  int first_slot_cta;  // balanced mode: the first CTA covering the unit
+  int unit_start;      // balanced mode: global tile index where the unit begins
+};
+
+__device__ __forceinline__ void raise_error(uint32_t* flag, uint32_t bit) {
+  if (flag) atomicOr(flag, bit);
+}
+
+// Visible tile span of sequence b: tiles [t0, t0 + n). Validates seq_len.
+__device__ __forceinline__ void seq_span(const DecodeParams& p, int b, bool report, int& L, int& t0,
+                                         int& n) {
+  L = p.seq_lens[b];
+  const int cap = p.max_blocks * p.block_size;
+  if (L < 0 || L > cap) {
+    if (report) raise_error(p.error_flag, kErrSeqLen);
+    L = L < 0 ? 0 : cap;
+  }
+  if (L == 0) { t0 = 0; n = 0; return; }
+  int lo = 0;
+  if (p.window > 0) {
+    const int first = L - p.qlen - p.window + 1;  // token 0's first visible key
+    lo = first > 0 ? first : 0;
+  }
+  t0 = lo / kTileKeys;
+  n = (L - 1) / kTileKeys - t0 + 1;
+}
+
+struct WorkIter {
+  // balanced mode: the CTA's tile range [g_begin, g_end) out of T, with
+  // C = min(gridDim.x, T) CTAs holding non-empty ranges
+  long long g, g_end, g_begin, T;
+  int C;
+  int b;
+  int zero_b;       // next sequence to test for zero-fill, stepping by gridDim.x
+  int zero_kh;
+  // fixed-split mode
+  long long piece;
+};
+
+__device__ __forceinline__ int owner_cta(long long x, long long T, int C) {
+  return static_cast<int>(((x + 1) * C - 1) / T);
+}
+
+__device__ __forceinline__ void work_init(const DecodeParams& p, const int* s_pre, WorkIter& it) {
+  const int c = blockIdx.x;
+  if (p.num_splits == 0) {
+    it.T = s_pre[p.B];
+    it.C = it.T < gridDim.x ? static_cast<int>(it.T) : static_cast<int>(gridDim.x);
+    if (c < it.C) {
+      it.g_begin = it.T * c / it.C;
+      it.g_end = it.T * (c + 1) / it.C;
+    } else {
+      it.g_begin = it.g_end = 0;
+    }
+    it.g = it.g_begin;
+    // largest b with s_pre[b] <= g
+    int lo = 0, hi = p.B - 1;
+    while (lo < hi) {
+      int mid = (lo + hi + 1) >> 1;
+      if (s_pre[mid] <= it.g) lo = mid; else hi = mid - 1;
+    }
+    it.b = lo;
+    it.zero_b = c;
+    it.zero_kh = 0;
+  } else {
+    it.piece = c;
+  }
+}
+
+// Produces the next piece; returns false when the CTA has no more work.
+__device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pre, WorkIter& it,
+                                          Piece& pc) {
+  const int C = gridDim.x, c = blockIdx.x;
+  if (p.num_splits == 0) {
+    if (it.g < it.g_end) {
+      while (s_pre[it.b + 1] <= it.g) ++it.b;
+      const int b = it.b;
+      const int n = (s_pre[b + 1] - s_pre[b]) / p.Hkv;
+      const long long off = it.g - s_pre[b];
+      const int kh = static_cast<int>(off / n);
+      const long long us = s_pre[b] + static_cast<long long>(kh) * n;
+      const long long ue = us + n;
+      const long long pe = ue < it.g_end ? ue : it.g_end;
+      int L, t0, nn;
+      seq_span(p, b, false, L, t0, nn);
+      pc.b = b; pc.kh = kh; pc.L = L; pc.unit_t0 = t0; pc.unit = b * p.Hkv + kh;
+      pc.first_tile = t0 + static_cast<int>(it.g - us);
+      pc.ntiles = static_cast<int>(pe - it.g);
+      const int cf = owner_cta(us, it.T, it.C), cl = owner_cta(ue - 1, it.T, it.C);
+      pc.npieces = cl - cf + 1;
+      pc.slot = 2 * c + (it.g_begin < us ? 1 : 0);
+      pc.ticket = cf;
+      pc.first_slot_cta = cf;
+      pc.unit_start = static_cast<int>(us);
+      it.g = pe;
+      return true;
+    }
+    // afterwards: zero rows of empty sequences b = c, c + C, ...
+    while (it.zero_b < p.B) {
+      const int b = it.zero_b;
+      if (s_pre[b + 1] == s_pre[b]) {
+        pc.b = b; pc.kh = it.zero_kh; pc.L = 0; pc.unit_t0 = 0; pc.unit = b * p.Hkv + it.zero_kh;
+        pc.first_tile = 0; pc.ntiles = 0; pc.npieces = 1; pc.slot = 0; pc.ticket = 0;
+        pc.first_slot_cta = c; pc.unit_start = 0;
+        if (++it.zero_kh == p.Hkv) { it.zero_kh = 0; it.zero_b += C; }
+        return true;
+      }
+      it.zero_b += C;
+    }
+    return false;
+  }
+  const int S = p.num_splits;
+  const long long total = static_cast<long long>(p.B) * p.Hkv * S;
+  while (it.piece < total) {
+    const long long pi = it.piece;
+    it.piece += C;
+    const int u = static_cast<int>(pi / S), s = static_cast<int>(pi % S);
+    const int b = u / p.Hkv, kh = u % p.Hkv;
+    int L, t0, n;
+    seq_span(p, b, s == 0 && kh == 0, L, t0, n);
+    const int chunk = (n + S - 1) / S;
+    const int c0 = s * chunk;
+    const int c1 = (c0 + chunk < n) ? c0 + chunk : n;
+    if (n == 0) {
+      if (s != 0) continue;
+      pc.b = b; pc.kh = kh; pc.L = 0; pc.unit_t0 = 0; pc.unit = u;
+      pc.first_tile = 0; pc.ntiles = 0; pc.npieces = 1; pc.slot = 0; pc.ticket = 0;
+      pc.first_slot_cta = 0; pc.unit_start = 0;
+      return true;
+    }
+    if (c0 >= c1) continue;
+    pc.b = b; pc.kh = kh; pc.L = L; pc.unit_t0 = t0; pc.unit = u;
+    pc.first_tile = t0 + c0;
+    pc.ntiles = c1 - c0;
+    pc.npieces = (n + chunk - 1) / chunk;
+    pc.slot = u * S + s;
+    pc.ticket = u;
+    pc.first_slot_cta = 0; pc.unit_start = 0;
+    return true;
+  }
+  return false;
+}
+
+// ---------------------------------------------------------------------------
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
+    decode_paged_kernel(const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+  constexpr int D = Cfg::D, NT = Cfg::NT, KG = Cfg::KG, NS = Cfg::NS;
+  constexpr bool FP8 = Cfg::FP8;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float* merge_o = reinterpret_cast<float*>(smem + Cfg::kOffMergeO);
+  float* merge_ml = reinterpret_cast<float*>(smem + Cfg::kOffMergeML);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBars);  // full[NS], empty[NS]
+  int* s_pre = reinterpret_cast<int*>(smem + Cfg::kOffPre);
+  int* s_misc = reinterpret_cast<int*>(smem + Cfg::kOffMisc);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool is_producer = warp == Cfg::kConsumerWarps;
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + NS);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, NT);
+    }
+    fence_mbar_init();
+  }
+  if (is_producer && lane == 0) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  // Balanced mode: prefix over sequences of Hkv * (visible tiles), by warp 0.
+  if (p.num_splits == 0 && warp == 0) {
+    int carry = 0;
+    if (lane == 0) s_pre[0] = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int b = base + lane;
+      int v = 0;
+      if (b < p.B) {
+        int L, t0, n;
+        seq_span(p, b, blockIdx.x == 0, L, t0, n);
+        v = n * p.Hkv;
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      if (b < p.B) s_pre[b + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+
+  WorkIter it;
+  work_init(p, s_pre, it);
+  const long long T_total = (p.num_splits == 0) ? s_pre[p.B] : 0;
+  Piece pc;
+
+  if (is_producer) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = l2_policy_evict_first();
+    uint32_t q = 0, issued = 0;
+    bool ok = true;
+    while (work_next(p, s_pre, it, pc)) {
+      if (pc.ntiles == 0) continue;
+      const int32_t* row = p.block_table + static_cast<long long>(pc.b) * p.max_blocks;
+      auto load_group = [&](int t) -> int {
+        // lane i: physical block of tile t + i of this piece (0 past its end).
+        // Validated where it is used, so the load stays in flight meanwhile.
+        int blk = 0;
+        if (t + lane < pc.ntiles) {
+          const int tile = pc.first_tile + t + lane;
+          blk = __ldg(row + tile / p.tiles_per_block);
+        }
+        return blk;
+      };
+      int cur = load_group(0);
+      for (int t = 0; t < pc.ntiles; t += 32) {
+        const int nxt = (t + 32 < pc.ntiles) ? load_group(t + 32) : -1;
+        const int n = min(32, pc.ntiles - t);
+        for (int i = 0; i < n; ++i, ++q) {
+          int blk = __shfl_sync(0xffffffffu, cur, i);
+          if (lane == 0) {
+            if (blk < 0 || blk >= p.num_blocks) {
+              raise_error(p.error_flag, kErrBlockId);
+              blk = 0;
+            }
+            const int stage = q % NS;
+            if (ok && q >= NS) ok = mbar_wait(empty0 + 8 * stage, ((q / NS) - 1) & 1, p.timeout_ns);
+            if (!ok) continue;
+            const int tile = pc.first_tile + t + i;
+            const int z = blk * p.block_size + (tile % p.tiles_per_block) * kTileKeys;
+            const uint32_t dst = smem_u32(smem + stage * Cfg::kStageBytes);
+            const uint32_t fb = full0 + 8 * stage;
+            mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
+#pragma unroll
+            for (int s = 0; s < Cfg::kSlabs; ++s)
+              tma_load_3d(dst + s * Cfg::kSlabBytes, &tm_k, fb, s * Cfg::kSlabElems, pc.kh, z, pol);
+#pragma unroll
+            for (int s = 0; s < Cfg::kSlabs; ++s)
+              tma_load_3d(dst + Cfg::kTileBytes + s * Cfg::kSlabBytes, &tm_v, fb,
+                          s * Cfg::kSlabElems, pc.kh, z, pol);
+            issued = q + 1;
+          }
+        }
+        cur = nxt;
+      }
+    }
+    if (lane == 0) {
+      if (!ok) raise_error(p.error_flag, kErrTimeout);
+      // Drain: every issued load must land before the CTA's shared memory is
+      // released. Loads past the consumers' last wait are none in a normal
+      // run; after a timeout, wait (bounded) for whatever is still in flight.
+      const uint32_t first = issued > NS ? issued - NS : 0;
+      for (uint32_t k = first; k < issued; ++k) {
+        if (!mbar_wait(full0 + 8 * (k % NS), (k / NS) & 1, p.timeout_ns)) break;
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int nt = warp / KG, kg = warp % KG;
+  const int g = lane >> 2, t4 = lane & 3;
+  constexpr int KSTEPS = D / 16;
+  uint32_t qf[KSTEPS][2];
+  float o[D / 16][4];
+  uint32_t q = 0;      // ring sequence number of the piece's first tile
+  bool ok = true;
+
+  while (work_next(p, s_pre, it, pc)) {
+    // ---- per-piece setup: Q fragments (B operand) and per-row visible key limits
+    {
+      const int r = nt * 8 + g;
+      const __half* qrow = nullptr;
+      if (r < p.R && pc.ntiles > 0) {
+        const int i = r / p.G, hl = r % p.G;
+        qrow = p.q + (static_cast<long long>(pc.b * p.qlen + i) * p.Hq + pc.kh * p.G + hl) * D;
+      }
+#pragma unroll
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        int d0, d1;
+        if constexpr (FP8) {
+          // k-step ks = (slab, super-step ss, j): dims slab*128 + 16*(2*t4+ss) + 4j + {0,1},{2,3}
+          const int slab = ks / 8, ss = (ks / 4) & 1, j = ks & 3;
+          d0 = slab * 128 + 16 * (2 * t4 + ss) + 4 * j;
+          d1 = d0 + 2;
+        } else {
+          d0 = ks * 16 + 2 * t4;
+          d1 = d0 + 8;
+        }
+        qf[ks][0] = qrow ? __ldg(reinterpret_cast<const uint32_t*>(qrow + d0)) : 0u;
+        qf[ks][1] = qrow ? __ldg(reinterpret_cast<const uint32_t*>(qrow + d1)) : 0u;
+      }
+    }
+    int lo_r[2], hi_r[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int r = nt * 8 + 2 * t4 + c;
+      if (r < p.R) {
+        const int i = r / p.G;
+        const int pos = pc.L - p.qlen + i;
+        hi_r[c] = pos;
+        lo_r[c] = (p.window > 0) ? max(0, pos - p.window + 1) : 0;
+      } else {
+        hi_r[c] = -1;
+        lo_r[c] = 0;
+      }
+    }
+    float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    // ---- this warp's tiles of the piece: ring numbers q + k with k % KG == kg
+    const int first_k = ((kg - static_cast<int>(q % KG)) % KG + KG) % KG;
+    for (int k = first_k; k < pc.ntiles; k += KG) {
+      const uint32_t qq = q + k;
+      const int stage = qq % NS;
+      if (ok) ok = mbar_wait(full0 + 8 * stage, (qq / NS) & 1, p.timeout_ns);
+      if (!ok) continue;
+      const uint32_t kb = smem_u32(smem + stage * Cfg::kStageBytes);
+      const uint32_t vb = kb + Cfg::kTileBytes;
+      const int key0 = (pc.first_tile + k) * kTileKeys;
+
+      // S^T = K Q^T  (16 keys x 8 rows), two accumulation chains
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (!FP8) {
+        const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const uint32_t rowb = kb + key * 128;
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+          const int slab = ks >> 2, chunk = (ks & 3) * 2 + (lane >> 4);
+          uint32_t a[4];
+          ldsm_x4(rowb + slab * Cfg::kSlabBytes + ((chunk ^ (key & 7)) << 4), a);
+          if (ks & 1) mma_16816(sb, a, qf[ks][0], qf[ks][1]);
+          else mma_16816(sa, a, qf[ks][0], qf[ks][1]);
+        }
+      } else {
+        const uint32_t r0 = kb + g * 128, r8 = kb + (g + 8) * 128;
+#pragma unroll
+        for (int slab = 0; slab < Cfg::kSlabs; ++slab) {
+#pragma unroll
+          for (int ss = 0; ss < 2; ++ss) {
+            const int chunk = (2 * t4 + ss) ^ (g & 7);
+            uint4 w0, w8;
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(w0.x), "=r"(w0.y), "=r"(w0.z), "=r"(w0.w)
+                         : "r"(r0 + slab * Cfg::kSlabBytes + (chunk << 4)));
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(w8.x), "=r"(w8.y), "=r"(w8.z), "=r"(w8.w)
+                         : "r"(r8 + slab * Cfg::kSlabBytes + (chunk << 4)));
+            const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w};
+            const uint32_t wb[4] = {w8.x, w8.y, w8.z, w8.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int ks = slab * 8 + ss * 4 + j;
+              uint32_t a[4];
+              a[0] = e4m3x2_to_half2(static_cast<uint16_t>(wa[j] & 0xffffu));
+              a[1] = e4m3x2_to_half2(static_cast<uint16_t>(wb[j] & 0xffffu));
+              a[2] = e4m3x2_to_half2(static_cast<uint16_t>(wa[j] >> 16));
+              a[3] = e4m3x2_to_half2(static_cast<uint16_t>(wb[j] >> 16));
+              if (j & 1) mma_16816(sb, a, qf[ks][0], qf[ks][1]);
+              else mma_16816(sa, a, qf[ks][0], qf[ks][1]);
+            }
+          }
+        }
+      }
+      // scores in log2 units, masked; C layout: [0]=(key g,row 2t4) [1]=(key g,row 2t4+1)
+      //                                          [2]=(key g+8,row 2t4) [3]=(key g+8,row 2t4+1)
+      float x[4];
+      {
+        const int j0 = key0 + g, j1 = j0 + 8;
+        x[0] = (j0 >= lo_r[0] && j0 <= hi_r[0]) ? (sa[0] + sb[0]) * p.sl2 : -INFINITY;
+        x[1] = (j0 >= lo_r[1] && j0 <= hi_r[1]) ? (sa[1] + sb[1]) * p.sl2 : -INFINITY;
+        x[2] = (j1 >= lo_r[0] && j1 <= hi_r[0]) ? (sa[2] + sb[2]) * p.sl2 : -INFINITY;
+        x[3] = (j1 >= lo_r[1] && j1 <= hi_r[1]) ? (sa[3] + sb[3]) * p.sl2 : -INFINITY;
+      }
+      float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m_r[0], mx0), mn1 = fmaxf(m_r[1], mx1);
+      const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
+      const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
+      const float a0 = ex2(m_r[0] - base0), a1 = ex2(m_r[1] - base1);
+      const float p00 = ex2(x[0] - base0), p01 = ex2(x[1] - base1);
+      const float p10 = ex2(x[2] - base0), p11 = ex2(x[3] - base1);
+      m_r[0] = mn0;
+      m_r[1] = mn1;
+      l_r[0] = l_r[0] * a0 + (p00 + p10);
+      l_r[1] = l_r[1] * a1 + (p01 + p11);
+      if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
+        }
+      }
+      // P^T as the B operand: transpose the (key x row) fp16 pairs
+      const uint32_t pb0 = movmatrix_trans(pack_half2(p00, p01));
+      const uint32_t pb1 = movmatrix_trans(pack_half2(p10, p11));
+
+      // O^T += V^T P^T
+      if constexpr (!FP8) {
+        const int key = (lane & 7) + (lane >> 4) * 8;
+        const uint32_t rowb = vb + key * 128;
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          const int slab = mt >> 2, chunk = (mt & 3) * 2 + ((lane >> 3) & 1);
+          uint32_t a[4];
+          ldsm_x4_trans(rowb + slab * Cfg::kSlabBytes + ((chunk ^ (key & 7)) << 4), a);
+          mma_16816(o[mt], a, pb0, pb1);
+        }
+      } else {
+        // 32-dim group P32: lane reads 4 codes at dims 32*P32 + 4g .. +3 of keys
+        // 2t4, 2t4+1, 2t4+8, 2t4+9; m-tile 2*P32 takes dims 4g (m=g) and 4g+1
+        // (m=g+8), m-tile 2*P32+1 takes 4g+2 and 4g+3.
+        const int kA = 2 * t4, kB = kA + 1, kC = kA + 8, kD = kA + 9;
+#pragma unroll
+        for (int P32 = 0; P32 < D / 32; ++P32) {
+          const int slab = P32 >> 2;
+          const int chunk = (P32 & 3) * 2 + (g >> 2);
+          const int byte = (4 * g) & 15;
+          const uint32_t sb0 = vb + slab * Cfg::kSlabBytes + byte;
+          uint32_t wA, wB, wC, wD;
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wA) : "r"(sb0 + kA * 128 + ((chunk ^ (kA & 7)) << 4)));
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wB) : "r"(sb0 + kB * 128 + ((chunk ^ (kB & 7)) << 4)));
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wC) : "r"(sb0 + kC * 128 + ((chunk ^ (kC & 7)) << 4)));
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wD) : "r"(sb0 + kD * 128 + ((chunk ^ (kD & 7)) << 4)));
+          const uint32_t ab01 = prmt(wA, wB, 0x5140u), ab23 = prmt(wA, wB, 0x7362u);
+          const uint32_t cd01 = prmt(wC, wD, 0x5140u), cd23 = prmt(wC, wD, 0x7362u);
+          uint32_t a[4];
+          a[0] = e4m3x2_to_half2(static_cast<uint16_t>(ab01 & 0xffffu));
+          a[1] = e4m3x2_to_half2(static_cast<uint16_t>(ab01 >> 16));
+          a[2] = e4m3x2_to_half2(static_cast<uint16_t>(cd01 & 0xffffu));
+          a[3] = e4m3x2_to_half2(static_cast<uint16_t>(cd01 >> 16));
+          mma_16816(o[2 * P32], a, pb0, pb1);
+          a[0] = e4m3x2_to_half2(static_cast<uint16_t>(ab23 & 0xffffu));
+          a[1] = e4m3x2_to_half2(static_cast<uint16_t>(ab23 >> 16));
+          a[2] = e4m3x2_to_half2(static_cast<uint16_t>(cd23 & 0xffffu));
+          a[3] = e4m3x2_to_half2(static_cast<uint16_t>(cd23 >> 16));
+          mma_16816(o[2 * P32 + 1], a, pb0, pb1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+    }
+    q += pc.ntiles;
+
+    // ---- merge the KG key groups of each row tile through shared memory
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l_r[0] += __shfl_xor_sync(0xffffffffu, l_r[0], off);
+      l_r[1] += __shfl_xor_sync(0xffffffffu, l_r[1], off);
+    }
+    if (g == 0) {
+      float* ml = merge_ml + warp * 16;
+      ml[(2 * t4) * 2 + 0] = m_r[0];
+      ml[(2 * t4) * 2 + 1] = l_r[0];
+      ml[(2 * t4 + 1) * 2 + 0] = m_r[1];
+      ml[(2 * t4 + 1) * 2 + 1] = l_r[1];
+    }
+    named_bar_sync(1, Cfg::kConsumerThreads);
+    {
+      // this warp's weight per row: exp2(m_own - max over the key groups)
+      float f_r[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int row = 2 * t4 + c;
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < KG; ++k) M = fmaxf(M, merge_ml[((nt * KG + k) * 8 + row) * 2]);
+        f_r[c] = (m_r[c] == -INFINITY) ? 0.f : ex2(m_r[c] - M);
+      }
+      // the row tile's buffer accumulates f * O one key group at a time
+      float* mo = merge_o + nt * 8 * Cfg::kDP;
+      const int r0 = 2 * t4, r1 = r0 + 1;
+#pragma unroll 1
+      for (int k = 0; k < KG; ++k) {
+        if (kg == k) {
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            int d0, d1;  // output dims of C rows g and g+8 of m-tile mt
+            if constexpr (FP8) {
+              d0 = (mt >> 1) * 32 + 4 * g + 2 * (mt & 1);
+              d1 = d0 + 1;
+            } else {
+              d0 = mt * 16 + g;
+              d1 = d0 + 8;
+            }
+            float* a00 = mo + r0 * Cfg::kDP + d0;
+            float* a10 = mo + r1 * Cfg::kDP + d0;
+            float* a01 = mo + r0 * Cfg::kDP + d1;
+            float* a11 = mo + r1 * Cfg::kDP + d1;
+            if (k == 0) {
+              *a00 = f_r[0] * o[mt][0]; *a10 = f_r[1] * o[mt][1];
+              *a01 = f_r[0] * o[mt][2]; *a11 = f_r[1] * o[mt][3];
+            } else {
+              *a00 += f_r[0] * o[mt][0]; *a10 += f_r[1] * o[mt][1];
+              *a01 += f_r[0] * o[mt][2]; *a11 += f_r[1] * o[mt][3];
+            }
+          }
+        }
+        named_bar_sync(1, Cfg::kConsumerThreads);
+      }
+    }
+
+    const int tid = threadIdx.x;
+    constexpr int DCH = D / 8;  // 8-dim chunks per row
+    const bool direct = pc.npieces == 1;
+    for (int item = tid; item < p.R * DCH; item += Cfg::kConsumerThreads) {
+      const int r = item / DCH, dc = item % DCH;
+      const int rnt = r >> 3, rr = r & 7;
+      float M = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < KG; ++k) M = fmaxf(M, merge_ml[((rnt * KG + k) * 8 + rr) * 2]);
+      float Ls = 0.f;
+#pragma unroll
+      for (int k = 0; k < KG; ++k) {
+        const float mk = merge_ml[((rnt * KG + k) * 8 + rr) * 2];
+        if (mk != -INFINITY) Ls += ex2(mk - M) * merge_ml[((rnt * KG + k) * 8 + rr) * 2 + 1];
+      }
+      const float* src = merge_o + (rnt * 8 + rr) * Cfg::kDP + dc * 8;
+      const float4 v0 = *reinterpret_cast<const float4*>(src);
+      const float4 v1 = *reinterpret_cast<const float4*>(src + 4);
+      if (direct) {
+        const int i = r / p.G, hl = r % p.G;
+        __half* dst = p.out + (static_cast<long long>(pc.b * p.qlen + i) * p.Hq + pc.kh * p.G + hl) * D + dc * 8;
+        const float inv = (Ls > 0.f) ? p.out_scale / Ls : 0.f;
+        uint4 v;
+        v.x = pack_half2(v0.x * inv, v0.y * inv);
+        v.y = pack_half2(v0.z * inv, v0.w * inv);
+        v.z = pack_half2(v1.x * inv, v1.y * inv);
+        v.w = pack_half2(v1.z * inv, v1.w * inv);
+        *reinterpret_cast<uint4*>(dst) = v;
+      } else {
+        float* dst = p.ws_o + (static_cast<long long>(pc.slot) * Cfg::RP + r) * D + dc * 8;
+        __stcg(reinterpret_cast<float4*>(dst), v0);
+        __stcg(reinterpret_cast<float4*>(dst + 4), v1);
+        if (dc == 0)
+          __stcg(reinterpret_cast<float2*>(p.ws_ml + (static_cast<long long>(pc.slot) * Cfg::RP + r) * 2),
+                 make_float2(M, Ls));
+      }
+    }
+    if (!direct) {
+      // publish this piece; the last of the unit's pieces merges them all
+      __threadfence();
+      named_bar_sync(1, Cfg::kConsumerThreads);
+      if (tid == 0) {
+        const int prev = atomicAdd(p.ws_count + pc.ticket, 1);
+        const int last = prev == pc.npieces - 1;
+        if (last) p.ws_count[pc.ticket] = 0;
+        s_misc[0] = last;
+      }
+      named_bar_sync(1, Cfg::kConsumerThreads);
+      if (s_misc[0]) {
+        __threadfence();
+        // slot of partial k (key order): balanced mode 2*cta for the CTAs
+        // after the first, fixed mode unit*S + k
+        int slot0, slot_base, slot_step;
+        if (p.num_splits == 0) {
+          const int cf = pc.first_slot_cta;
+          const long long start = T_total * cf / it.C;
+          slot0 = 2 * cf + (start < pc.unit_start ? 1 : 0);
+          slot_base = 2 * cf;
+          slot_step = 2;
+        } else {
+          slot0 = slot_base = pc.unit * p.num_splits;
+          slot_step = 1;
+        }
+        for (int item = tid; item < p.R * DCH; item += Cfg::kConsumerThreads) {
+          const int r = item / DCH, dc = item % DCH;
+          // one pass in key order with a running max; loads four partials ahead
+          float m_run = -INFINITY, l_run = 0.f;
+          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          for (int k0 = 0; k0 < pc.npieces; k0 += 4) {
+            float2 ml[4];
+            float4 va[4], vb[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int k = k0 + j;
+              if (k < pc.npieces) {
+                const long long slot = (k == 0) ? slot0 : slot_base + slot_step * k;
+                ml[j] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (slot * Cfg::RP + r) * 2));
+                const float* src = p.ws_o + (slot * Cfg::RP + r) * D + dc * 8;
+                va[j] = __ldcg(reinterpret_cast<const float4*>(src));
+                vb[j] = __ldcg(reinterpret_cast<const float4*>(src + 4));
+              } else {
+                ml[j] = make_float2(-INFINITY, 0.f);
+                va[j] = vb[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float mk = ml[j].x;
+              if (mk == -INFINITY) continue;
+              if (mk > m_run) {
+                const float sc = (m_run == -INFINITY) ? 0.f : ex2(m_run - mk);
+                l_run *= sc;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] *= sc;
+                m_run = mk;
+              }
+              const float w = ex2(mk - m_run);
+              l_run += w * ml[j].y;
+              acc[0] += w * va[j].x; acc[1] += w * va[j].y; acc[2] += w * va[j].z; acc[3] += w * va[j].w;
+              acc[4] += w * vb[j].x; acc[5] += w * vb[j].y; acc[6] += w * vb[j].z; acc[7] += w * vb[j].w;
+            }
+          }
+          const int i = r / p.G, hl = r % p.G;
+          __half* dst = p.out + (static_cast<long long>(pc.b * p.qlen + i) * p.Hq + pc.kh * p.G + hl) * D + dc * 8;
+          const float inv = (l_run > 0.f) ? p.out_scale / l_run : 0.f;
+          uint4 v;
+          v.x = pack_half2(acc[0] * inv, acc[1] * inv);
+          v.y = pack_half2(acc[2] * inv, acc[3] * inv);
+          v.z = pack_half2(acc[4] * inv, acc[5] * inv);
+          v.w = pack_half2(acc[6] * inv, acc[7] * inv);
+          *reinterpret_cast<uint4*>(dst) = v;
+        }
+      }
+    }
+    named_bar_sync(1, Cfg::kConsumerThreads);  // merge buffers free again
+  }
+  if (!ok && lane == 0) raise_error(p.error_flag, kErrTimeout);
+}
+
+}  // namespace pd

@@ -1,0 +1,77 @@
+// launch.h -- internal interface between the host layer and the kernel
+// instantiation units (one translation unit per head size and KV dtype, so
+// they compile in parallel).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "decode_kernel.cuh"
+
+namespace pd {
+
+struct KernelShape {
+  int threads;     // threads per CTA
+  int smem_bytes;  // dynamic shared memory per CTA
+  int rows_padded; // RP: query rows per unit rounded up to the row-tile size
+};
+
+// Returns false when no instantiation covers (D, fp8, nt).
+bool kernel_shape(int D, bool fp8, int nt, KernelShape* out);
+
+// Launch the instantiation for (D, fp8, nt) on `grid` CTAs.
+cudaError_t launch_decode(int D, bool fp8, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const DecodeParams& p, int grid, cudaStream_t stream);
+
+// Per-dtype/head-size entry points defined in decode_*.cu.
+bool shape_f16_d128(int nt, KernelShape* out);
+bool shape_f16_d256(int nt, KernelShape* out);
+bool shape_fp8_d128(int nt, KernelShape* out);
+bool shape_fp8_d256(int nt, KernelShape* out);
+cudaError_t launch_f16_d128(int nt, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
+                            cudaStream_t);
+cudaError_t launch_f16_d256(int nt, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
+                            cudaStream_t);
+cudaError_t launch_fp8_d128(int nt, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
+                            cudaStream_t);
+cudaError_t launch_fp8_d256(int nt, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
+                            cudaStream_t);
+
+// Launch one configuration; sets the shared-memory opt-in once per device.
+template <class Cfg>
+cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
+                       cudaStream_t stream) {
+  static unsigned long long attr_done = 0;  // bit per device ordinal (< 64)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
+    e = cudaFuncSetAttribute(decode_paged_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);
+  }
+  decode_paged_kernel<Cfg><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+// Largest ring (stage count, capped at 32) whose shared-memory plan fits the
+// 227 KiB a CTA may use on sm_103a.
+constexpr int kSmemLimit = 227 * 1024;
+template <int D, bool FP8, int NT, int KG, int NS = 32>
+constexpr int ring_stages() {
+  if constexpr (NS <= 2 || Cfg<D, FP8, NT, KG, NS>::kSmemBytes <= kSmemLimit)
+    return NS;
+  else
+    return ring_stages<D, FP8, NT, KG, NS - 1>();
+}
+
+template <class Cfg>
+bool shape_of(KernelShape* out) {
+  out->threads = Cfg::kThreads;
+  out->smem_bytes = Cfg::kSmemBytes;
+  out->rows_padded = Cfg::RP;
+  return true;
+}
+
+}  // namespace pd

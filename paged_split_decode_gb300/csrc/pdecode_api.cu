@@ -1,0 +1,244 @@
+// pdecode_api.cu -- host side of libpdecode: argument validation, the split
+// plan, TMA descriptors for the paged caches, and launches on the caller's
+// stream. The C ABI is declared in include/pdecode.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "launch.h"
+#include "pdecode.h"
+
+namespace pd {
+
+bool kernel_shape(int D, bool fp8, int nt, KernelShape* out) {
+  if (D == 128) return fp8 ? shape_fp8_d128(nt, out) : shape_f16_d128(nt, out);
+  if (D == 256) return fp8 ? shape_fp8_d256(nt, out) : shape_f16_d256(nt, out);
+  return false;
+}
+
+cudaError_t launch_decode(int D, bool fp8, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const DecodeParams& p, int grid, cudaStream_t s) {
+  if (D == 128) return fp8 ? launch_fp8_d128(nt, tk, tv, p, grid, s) : launch_f16_d128(nt, tk, tv, p, grid, s);
+  return fp8 ? launch_fp8_d256(nt, tk, tv, p, grid, s) : launch_f16_d256(nt, tk, tv, p, grid, s);
+}
+
+namespace {
+
+constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
+
+// Resolved work decomposition of one call.
+struct Plan {
+  int splits;       // 0 = balanced, >= 1 fixed
+  int grid;         // CTAs launched
+  int nt;           // row tiles
+  long long slots;  // partial slots in the workspace
+  long long units;  // B * Hkv tickets
+  int rows_padded;
+  size_t off_ml, off_o, bytes;  // workspace layout
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pd_status check_dims(const pd_dims* d, int qlen) {
+  if (!d) return PD_ERR_NULL;
+  if (d->B < 0 || d->Hq < 1 || d->Hkv < 1 || d->D < 1 || d->block_size < 1 || d->num_blocks < 0 ||
+      d->max_blocks_per_seq < 0 || qlen < 1)
+    return PD_ERR_SHAPE;
+  if (d->Hq % d->Hkv != 0) return PD_ERR_SHAPE;
+  if (d->kv_dtype != PD_KV_F16 && d->kv_dtype != PD_KV_FP8_E4M3) return PD_ERR_DTYPE;
+  if (d->kv_dtype == PD_KV_FP8_E4M3 &&
+      (!std::isfinite(d->k_scale) || !std::isfinite(d->v_scale)))
+    return PD_ERR_SHAPE;
+  if (d->D != 128 && d->D != 256) return PD_ERR_UNSUPPORTED;
+  if (d->block_size % kTileKeys != 0) return PD_ERR_UNSUPPORTED;
+  if (qlen > 8) return PD_ERR_UNSUPPORTED;
+  const int R = d->Hq / d->Hkv * qlen;
+  if (R > 32) return PD_ERR_UNSUPPORTED;
+  // 32-bit index headroom: tiles, keys and cache rows
+  const long long cap_keys = static_cast<long long>(d->max_blocks_per_seq) * d->block_size;
+  if (cap_keys > (1ll << 30)) return PD_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d->B) * d->Hkv * (cap_keys / kTileKeys + 1) > (1ll << 31) - 1)
+    return PD_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d->num_blocks) * d->block_size > (1ll << 31) - 1) return PD_ERR_UNSUPPORTED;
+  if (static_cast<long long>(d->B) * qlen * d->Hq > (1ll << 31) - 1) return PD_ERR_UNSUPPORTED;
+  return PD_OK;
+}
+
+int device_sm_count(int sm_count) {
+  if (sm_count > 0) return sm_count;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Plan* pl) {
+  pd_status st = check_dims(d, qlen);
+  if (st != PD_OK) return st;
+  if (num_splits < 0) return PD_ERR_SHAPE;
+  const int sms = device_sm_count(sm_count);
+  if (sms <= 0) return PD_ERR_CUDA;
+  const int R = d->Hq / d->Hkv * qlen;
+  pl->nt = (R + 7) / 8;
+  KernelShape ks;
+  if (!kernel_shape(d->D, d->kv_dtype == PD_KV_FP8_E4M3, pl->nt, &ks)) return PD_ERR_UNSUPPORTED;
+  pl->rows_padded = ks.rows_padded;
+  pl->units = static_cast<long long>(d->B) * d->Hkv;
+  int splits = num_splits;
+  if (splits == 0 && d->B > kMaxAutoB) splits = 1;  // plenty of units: one piece each
+  if (splits > 1 && pl->units > kTickets) return PD_ERR_UNSUPPORTED;
+  pl->splits = splits;
+  if (splits == 0) {
+    pl->grid = sms;
+    pl->slots = 2ll * sms;
+  } else {
+    const long long pieces = pl->units * splits;
+    pl->grid = static_cast<int>(pieces < sms ? (pieces > 0 ? pieces : 1) : sms);
+    pl->slots = splits > 1 ? pieces : 0;
+  }
+  if (pl->slots == 0) {
+    pl->off_ml = pl->off_o = pl->bytes = 0;
+  } else {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t cnt = static_cast<size_t>(kTickets) * 4;
+    const size_t ml = up(static_cast<size_t>(pl->slots) * pl->rows_padded * 2 * 4);
+    const size_t o = static_cast<size_t>(pl->slots) * pl->rows_padded * d->D * 4;
+    pl->off_ml = cnt;
+    pl->off_o = cnt + ml;
+    pl->bytes = cnt + ml + o;
+  }
+  return PD_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a paged cache viewed as [num_blocks*block_size][Hkv][D]:
+// box = one 128-byte row slab x one head x 16 keys, 128B swizzle.
+bool encode_cache_map(CUtensorMap* m, const void* base, const pd_dims* d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const bool fp8 = d->kv_dtype == PD_KV_FP8_E4M3;
+  const cuuint64_t elem = fp8 ? 1 : 2;
+  const cuuint64_t rows = static_cast<cuuint64_t>(d->num_blocks) * d->block_size;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d->D), static_cast<cuuint64_t>(d->Hkv),
+                        rows > 0 ? rows : 1};
+  cuuint64_t strides[2] = {d->D * elem, static_cast<cuuint64_t>(d->Hkv) * d->D * elem};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem), 1, static_cast<cuuint32_t>(kTileKeys)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace pd
+
+using namespace pd;
+
+extern "C" {
+
+const char* pd_status_str(pd_status s) {
+  switch (s) {
+    case PD_OK: return "ok";
+    case PD_ERR_NULL: return "a required pointer is NULL";
+    case PD_ERR_SHAPE: return "inconsistent or out-of-range sizes";
+    case PD_ERR_DTYPE: return "unknown KV dtype";
+    case PD_ERR_UNSUPPORTED: return "shape not implemented by these kernels";
+    case PD_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case PD_ERR_WORKSPACE: return "workspace missing or too small";
+    case PD_ERR_CUDA: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+size_t pd_workspace_bytes(const pd_dims* dims, int qlen, int num_splits, int sm_count) {
+  Plan pl;
+  if (make_plan(dims, qlen, num_splits, sm_count, &pl) != PD_OK) return 0;
+  return pl.bytes;
+}
+
+int pd_grid_ctas(const pd_dims* dims, int qlen, int num_splits, int sm_count) {
+  Plan pl;
+  if (make_plan(dims, qlen, num_splits, sm_count, &pl) != PD_OK) return 0;
+  return pl.grid;
+}
+
+pd_status decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_table, const int32_t* seq_lens, float scale,
+                       int window, int qlen, int num_splits, void* out, const pd_dims* dims,
+                       void* workspace, size_t workspace_bytes, uint32_t* error_flag,
+                       void* stream) {
+  pd_status st = check_dims(dims, qlen);
+  if (st != PD_OK) return st;
+  if (num_splits < 0 || !std::isfinite(scale)) return PD_ERR_SHAPE;
+  if (dims->B == 0) return PD_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return PD_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(error_flag) & 3u))
+    return PD_ERR_ALIGN;
+  if (dims->num_blocks == 0) return PD_ERR_SHAPE;
+  Plan pl;
+  st = make_plan(dims, qlen, num_splits, 0, &pl);
+  if (st != PD_OK) return st;
+  if (pl.bytes > 0) {
+    if (!workspace || workspace_bytes < pl.bytes) return PD_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PD_ERR_ALIGN;
+  }
+
+  CUtensorMap tk, tv;
+  if (!encode_cache_map(&tk, k_cache, dims) || !encode_cache_map(&tv, v_cache, dims)) return PD_ERR_CUDA;
+
+  const bool fp8 = dims->kv_dtype == PD_KV_FP8_E4M3;
+  DecodeParams p;
+  p.q = static_cast<const __half*>(q);
+  p.out = static_cast<__half*>(out);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.ws_count = pl.bytes ? reinterpret_cast<int*>(ws) : nullptr;
+  p.ws_ml = pl.bytes ? reinterpret_cast<float*>(ws + pl.off_ml) : nullptr;
+  p.ws_o = pl.bytes ? reinterpret_cast<float*>(ws + pl.off_o) : nullptr;
+  p.error_flag = error_flag;
+  p.B = dims->B;
+  p.qlen = qlen;
+  p.Hq = dims->Hq;
+  p.Hkv = dims->Hkv;
+  p.G = dims->Hq / dims->Hkv;
+  p.R = p.G * qlen;
+  p.max_blocks = dims->max_blocks_per_seq;
+  p.block_size = dims->block_size;
+  p.num_blocks = dims->num_blocks;
+  p.tiles_per_block = dims->block_size / kTileKeys;
+  p.window = window > 0 ? window : 0;
+  p.num_splits = pl.splits;
+  const double ks = fp8 ? static_cast<double>(dims->k_scale) : 1.0;
+  p.sl2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 * ks);
+  p.out_scale = fp8 ? dims->v_scale : 1.0f;
+  p.timeout_ns = kTimeoutNs;
+
+  cudaError_t e = launch_decode(dims->D, fp8, pl.nt, tk, tv, p, pl.grid,
+                                static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PD_OK : PD_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,238 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs. Tolerance: max abs error <= 2e-3 on every element for
+fp16 KV, and for fp8 KV against the oracle run on the identically decoded
+codes; rows with no visible key must be exact zeros.
+
+Workloads follow the decode benchmarks and cells of opengfx1030/vllm-rdna pull
+request #33 ("Test Plan", results comment): the tiny two-sequence case, D=256
+GQA 6:1 at L=4096 over the batch sweep, D=128 with ragged lengths and dense or
+permuted tables, L=32768 with and without a 4096-key window across split
+counts, and qlen=3 speculative verify over e4m3 KV.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_split_decode_gb300 import inputs
+
+TOL = 2e-3
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pd():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import paged_split_decode_gb300 as pd
+    pd.load()  # raises when the library is missing: no fallback
+    return pd
+
+
+DEV = "cuda:0"
+
+
+def gpu_run(pd, w, num_splits=None, out=None, flag=None, workspace=None):
+    S = w.num_splits if num_splits is None else num_splits
+    res = pd.decode_paged(w.q.to(DEV), w.k_cache.to(DEV), w.v_cache.to(DEV), w.block_table.to(DEV),
+                          w.seq_lens.to(DEV), w.scale, w.window, w.qlen, S, out=out,
+                          k_scale=w.k_scale, v_scale=w.v_scale, error_flag=flag, workspace=workspace)
+    torch.cuda.synchronize()
+    return res
+
+
+def ref_run(w):
+    return oracle.decode_paged(w.q.numpy(), w.k_cache.numpy(), w.v_cache.numpy(),
+                               w.block_table.numpy(), w.seq_lens.numpy(), w.scale, w.window, w.qlen,
+                               w.k_scale, w.v_scale, w.kv_fp8)
+
+
+def empty_rows(w):
+    """[B*qlen*Hq] bool: rows whose query token sees no key."""
+    rows = []
+    for b, L in enumerate(w.seq_lens.tolist()):
+        for i in range(w.qlen):
+            rows += [L - w.qlen + i < 0 or L == 0] * w.Hq
+    return np.array(rows)
+
+
+def check(w, got, ref, tol=TOL):
+    g = got.float().cpu().numpy().reshape(-1, w.D)
+    r = ref.reshape(-1, w.D)
+    assert np.all(np.isfinite(g)), f"{w.name}: non-finite output"
+    err = float(np.max(np.abs(g - r))) if g.size else 0.0
+    assert err <= tol, f"{w.name}: max abs err {err:.3e}"
+    e = empty_rows(w)
+    assert np.all(g[e] == 0.0), f"{w.name}: empty rows not zero"
+    return err
+
+
+def test_tiny_two_sequences_one_empty(pd):
+    w = inputs.tiny()
+    ref = ref_run(w)
+    for S in (1, 0, 2, 5):
+        check(w, gpu_run(pd, w, S), ref)
+
+
+@pytest.mark.parametrize("B", [1, 2, 3, 8, 32])
+def test_gqa6_d256_batch_sweep_balanced(pd, B):
+    w = inputs.gqa_d256(B)
+    check(w, gpu_run(pd, w), ref_run(w))
+
+
+@pytest.mark.parametrize("heads", [(32, 8), (28, 4)])
+@pytest.mark.parametrize("layout", ["dense", "permuted"])
+def test_d128_ragged_lengths(pd, heads, layout):
+    w = inputs.gqa_d128(heads, layout)
+    check(w, gpu_run(pd, w), ref_run(w))
+
+
+@pytest.mark.parametrize("B", [1, 2])
+@pytest.mark.parametrize("window", [4096, 0])
+def test_long_context_window_across_splits(pd, B, window):
+    w = inputs.long_window(B, window, 0)
+    ref = ref_run(w)
+    outs = []
+    for S in (1, 3, 8, 0):
+        got = gpu_run(pd, w, S)
+        check(w, got, ref)
+        outs.append(got.float().cpu())
+    for o in outs[1:]:
+        assert torch.max(torch.abs(o - outs[0])).item() <= TOL
+
+
+def test_speculative_verify_fp8(pd):
+    w = inputs.verify_fp8()
+    ref = ref_run(w)
+    for S in (0, 1, 4):
+        check(w, gpu_run(pd, w, S), ref)
+
+
+EDGE = [
+    # (name, kwargs)
+    ("ragged_tail_and_short", dict(B=4, Hq=8, Hkv=2, D=128, seq_lens=[1, 15, 17, 333])),
+    ("seq_shorter_than_qlen", dict(B=3, Hq=8, Hkv=2, D=128, qlen=3, seq_lens=[1, 2, 40])),
+    ("all_empty", dict(B=3, Hq=8, Hkv=2, D=256, seq_lens=[0, 0, 0], pool_blocks=2)),
+    ("window_one_key", dict(B=2, Hq=6, Hkv=1, D=256, seq_lens=[100, 16], window=1)),
+    ("window_inside_a_tile", dict(B=2, Hq=4, Hkv=2, D=128, seq_lens=[97, 300], window=5, qlen=2)),
+    ("mha_g1", dict(B=3, Hq=4, Hkv=4, D=128, seq_lens=[50, 700, 1])),
+    ("rows_32", dict(B=2, Hq=8, Hkv=1, D=256, qlen=4, seq_lens=[600, 35])),
+    ("rows_7", dict(B=5, Hq=28, Hkv=4, D=128, seq_lens=[10, 2000, 0, 64, 65])),
+    ("block_size_32", dict(B=3, Hq=24, Hkv=4, D=256, block_size=32, seq_lens=[31, 33, 1000])),
+    ("block_size_64_fp8", dict(B=2, Hq=16, Hkv=2, D=128, block_size=64, kv="fp8", qlen=2,
+                               seq_lens=[129, 700])),
+    ("fp8_d128_rows_24", dict(B=3, Hq=8, Hkv=1, D=128, kv="fp8", qlen=3, seq_lens=[5, 300, 1500])),
+    ("fp8_d256_rows_6", dict(B=2, Hq=24, Hkv=4, D=256, kv="fp8", seq_lens=[4000, 17])),
+    ("many_sequences", dict(B=300, Hq=8, Hkv=2, D=128, seq_lens=list(range(0, 3000, 10)))),
+]
+
+
+@pytest.mark.parametrize("S", [0, 1, 3, 17])
+@pytest.mark.parametrize("name,kw", EDGE, ids=[e[0] for e in EDGE])
+def test_edge_cases(pd, name, kw, S):
+    w = inputs.make_workload(seed=zlib.crc32(name.encode()) % 10000, name=name, **kw)
+    check(w, gpu_run(pd, w, S), ref_run(w))
+
+
+def test_one_workspace_across_changing_shapes(pd):
+    """One workspace buffer serves calls of different shapes back to back: the
+    split tickets sit in a fixed header that every call leaves at zero."""
+    import paged_split_decode_gb300 as P
+    ws = torch.zeros(64 << 20, dtype=torch.uint8, device=DEV)
+    ws_list = [inputs.make_workload(B=2, Hq=8, Hkv=8, D=128, seq_lens=[5000, 16384], seed=21),
+               inputs.make_workload(B=32, Hq=32, Hkv=8, D=128, seq_lens=[4096] * 32, seed=22),
+               inputs.make_workload(B=3, Hq=24, Hkv=4, D=256, seq_lens=[9000, 1, 700], seed=23,
+                                    qlen=3, kv="fp8"),
+               inputs.make_workload(B=32, Hq=32, Hkv=8, D=256, seq_lens=[8192] * 32, seed=24)]
+    refs = [ref_run(w) for w in ws_list]
+    for rep in range(2):
+        for w, r in zip(ws_list, refs):
+            for S in (0, 3):
+                check(w, gpu_run(pd, w, S, workspace=ws), r)
+    hdr = ws[:16384 * 4].view(torch.int32)
+    assert int(torch.count_nonzero(hdr).item()) == 0
+
+
+def test_custom_scale_writes_into_out_only(pd):
+    """A caller-owned out is written in full; bytes around it are untouched."""
+    w = inputs.make_workload(B=2, Hq=24, Hkv=4, D=256, seq_lens=[1000, 0], seed=5, scale=0.37)
+    n = w.q.numel()
+    buf = torch.full((n + 2 * 4096,), 7.0, dtype=torch.float16, device=DEV)
+    out = buf[4096:4096 + n].view_as(w.q)
+    gpu_run(pd, w, 0, out=out)
+    check(w, out, ref_run(w))
+    assert torch.all(buf[:4096] == 7.0) and torch.all(buf[4096 + n:] == 7.0)
+
+
+def test_scale_zero_is_mean_of_v(pd):
+    w = inputs.make_workload(B=2, Hq=8, Hkv=2, D=128, seq_lens=[333, 64], seed=6, scale=0.0)
+    check(w, gpu_run(pd, w), ref_run(w))
+
+
+def test_writer_layout_per_head_constants(pd):
+    """V rows hold a constant per (KV head, dim): every query head must return
+    the constant of the KV head h // G (the cache layout and GQA mapping)."""
+    w = inputs.make_workload(B=3, Hq=24, Hkv=4, D=256, seq_lens=[77, 1000, 16], seed=8)
+    c = torch.arange(4, dtype=torch.float32)[:, None] * 0.5 - 1 + torch.linspace(0, 0.25, 256)[None]
+    w.v_cache[:] = c.to(torch.float16)[None, None]
+    got = gpu_run(pd, w).float().cpu()
+    for h in range(24):
+        assert torch.max(torch.abs(got[:, h] - c.to(torch.float16).float()[h // 6])).item() <= 1e-3
+
+
+def test_block_permutation_invariance_and_determinism(pd):
+    w = inputs.gqa_d256(2)
+    a = gpu_run(pd, w).clone()
+    b = gpu_run(pd, w).clone()
+    assert torch.equal(a, b), "same inputs, same workspace: results must be bitwise equal"
+    pool = w.k_cache.shape[0]
+    perm = torch.randperm(pool, generator=torch.Generator().manual_seed(3))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(pool)
+    w2 = inputs.Workload(**{**w.__dict__})
+    w2.k_cache = w.k_cache[perm].contiguous()
+    w2.v_cache = w.v_cache[perm].contiguous()
+    t = w.block_table.clone()
+    ok = t >= 0
+    t[ok] = inv[t[ok].long()].to(torch.int32)
+    w2.block_table = t
+    c = gpu_run(pd, w2)
+    assert torch.equal(a, c), "a physical block permutation must not change the result"
+
+
+def test_device_errors_are_flagged_not_trapped(pd):
+    w = inputs.make_workload(B=2, Hq=8, Hkv=2, D=128, seq_lens=[100, 50], seed=9)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    bad = inputs.Workload(**{**w.__dict__})
+    bad.block_table = w.block_table.clone()
+    bad.block_table[0, 2] = 1 << 20            # outside the pool
+    gpu_run(pd, bad, 0, flag=flag)
+    assert int(flag.item()) & 1
+    flag.zero_()
+    bad2 = inputs.Workload(**{**w.__dict__})
+    bad2.seq_lens = torch.tensor([100, 10_000], dtype=torch.int32)  # above the table's capacity
+    gpu_run(pd, bad2, 1, flag=flag)
+    assert int(flag.item()) & 2
+    flag.zero_()
+    out = gpu_run(pd, w, 0, flag=flag)          # the context is still healthy
+    assert int(flag.item()) == 0
+    check(w, out, ref_run(w))
+
+
+def test_combine_entry_point_matches_oracle(pd):
+    w = inputs.make_workload(B=3, Hq=8, Hkv=2, D=128, seq_lens=[500, 0, 77], qlen=2, seed=10)
+    _, m, l, O = oracle.decode_paged_split(w.q.numpy(), w.k_cache.numpy(), w.v_cache.numpy(),
+                                           w.block_table.numpy(), w.seq_lens.numpy(), w.scale,
+                                           num_splits=5, qlen=w.qlen, return_partials=True)
+    want = oracle.combine(m, l, O)
+    mt = torch.tensor(m, dtype=torch.float32, device=DEV)
+    lt = torch.tensor(l, dtype=torch.float32, device=DEV)
+    Ot = torch.tensor(O, dtype=torch.float32, device=DEV)
+    got = pd.decode_paged_combine(mt, lt, Ot)
+    torch.cuda.synchronize()
+    g = got.float().cpu().numpy()
+    assert np.max(np.abs(g - want)) <= TOL
+    assert np.all(g[np.all(want == 0, axis=1)] == 0)

@@ -1,0 +1,111 @@
+"""Host-side checks that need no GPU: the library builds for sm_103a, loads,
+exports exactly what include/pdecode.h declares, and its pure host functions
+(planning, workspace sizing, argument validation) behave as documented."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from paged_split_decode_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "pdecode.h")).read()
+    src = re.sub(r"#define PD_API.*", "", src)
+    return sorted(set(re.findall(r"^PD_API\s+[\w\s\*]*?\b(\w+)\s*\(", src, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.lib_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = sorted(line.split()[-1] for line in out.splitlines() if line.strip())
+    assert exported == declared_functions()
+
+
+def test_build_targets_sm_103a_only():
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert binding.status_str(code)
+    assert binding.status_str(0) == "ok"
+
+
+def _dims(**kw):
+    base = dict(B=32, Hq=24, Hkv=4, D=256, block_size=16, num_blocks=10000, max_blocks_per_seq=256)
+    base.update(kw)
+    return binding.make_dims(**base)
+
+
+def test_workspace_and_grid_plans(lib):
+    d = _dims()
+    # balanced: one CTA per SM, two partial slots per CTA, 8 padded rows of D floats
+    assert binding.grid_ctas(d, 1, 0, sm_count=152) == 152
+    ws = binding.workspace_bytes(d, 1, 0, sm_count=152)
+    cnt = 16384 * 4  # fixed ticket header
+    ml = ((304 * 8 * 2 * 4 + 255) // 256) * 256
+    assert ws == cnt + ml + 304 * 8 * 256 * 4
+    # no split: no workspace at all
+    assert binding.workspace_bytes(d, 1, 1, sm_count=152) == 0
+    assert binding.grid_ctas(d, 1, 1, sm_count=152) == 128
+    # fixed split: B*Hkv*S slots
+    assert binding.workspace_bytes(d, 1, 3, sm_count=152) == \
+        cnt + ((384 * 8 * 2 * 4 + 255) // 256) * 256 + 384 * 8 * 256 * 4
+    assert binding.grid_ctas(d, 1, 3, sm_count=152) == 152
+    # qlen 3 x G 6 = 18 rows -> three row tiles of 8
+    ws3 = binding.workspace_bytes(_dims(B=8), 3, 0, sm_count=152)
+    assert ws3 == cnt + ((304 * 24 * 2 * 4 + 255) // 256) * 256 + 304 * 24 * 256 * 4
+
+
+@pytest.mark.parametrize("kw,qlen", [
+    (dict(D=64), 1), (dict(D=96), 1), (dict(block_size=8), 1), (dict(Hq=24, Hkv=5), 1),
+    (dict(Hq=40, Hkv=1), 1), (dict(), 9), (dict(Hq=24, Hkv=4), 6),
+])
+def test_unsupported_or_bad_shapes_are_rejected(lib, kw, qlen):
+    assert binding.workspace_bytes(_dims(**kw), qlen, 0, sm_count=152) == 0
+    assert binding.grid_ctas(_dims(**kw), qlen, 0, sm_count=152) == 0
+
+
+def _call(lib, dims, q=16, k=16, v=16, bt=16, sl=16, out=16, qlen=1, splits=0, ws=None, wsb=0, flag=None):
+    return lib.decode_paged(q, k, v, bt, sl, 0.1, 0, qlen, splits, out, ctypes.byref(dims), ws, wsb,
+                            flag, None)
+
+
+def test_decode_paged_validates_before_touching_the_device(lib):
+    d = _dims()
+    assert _call(lib, _dims(D=64)) == 4          # unsupported head size
+    assert _call(lib, _dims(Hkv=5)) == 2         # Hq % Hkv
+    bad = _dims()
+    bad.kv_dtype = 7
+    assert _call(lib, bad) == 3                  # dtype
+    assert _call(lib, d, q=None) == 1            # null pointer
+    assert _call(lib, d, out=None) == 1
+    assert _call(lib, d, q=0x1008) == 5          # misaligned (not 16 B)
+    assert _call(lib, d, bt=0x1002) == 5
+    assert _call(lib, d, splits=-1) == 2
+    assert _call(lib, _dims(B=0)) == 0           # nothing to do
+
+
+def test_combine_validates(lib):
+    assert lib.decode_paged_combine(16, 16, 16, 4, 0, 256, 16, None) == 2   # S = 0
+    assert lib.decode_paged_combine(16, 16, 16, 4, 2, 100, 16, None) == 2   # D % 8
+    assert lib.decode_paged_combine(None, 16, 16, 4, 2, 256, 16, None) == 1
+    assert lib.decode_paged_combine(16, 16, 0x1004, 4, 2, 256, 16, None) == 5
+    assert lib.decode_paged_combine(16, 16, 16, 0, 2, 256, 16, None) == 0   # no rows

@@ -1,0 +1,150 @@
+"""CPU model of the kernel's work decomposition (no GPU needed).
+
+The decode kernel hands each CTA a list of unit pieces: in balanced mode the
+visible 16-key tiles of all (sequence, KV head) units are laid end to end and
+cut into equal contiguous ranges; with a fixed split count each unit is cut
+into that many chunks, dealt round robin. This model restates those index
+rules and checks the properties the kernel relies on: every visible tile is
+processed exactly once, each unit's piece count equals the number of pieces
+that bump its ticket, partial slots are distinct and inside the workspace the
+host sizes, and each empty unit gets exactly one zero-fill piece.
+"""
+import itertools
+import random
+
+import pytest
+
+TILE = 16
+
+
+def seq_span(L, qlen, window, cap):
+    L = min(max(L, 0), cap)
+    if L == 0:
+        return L, 0, 0
+    lo = max(0, L - qlen - window + 1) if window > 0 else 0
+    t0 = lo // TILE
+    return L, t0, (L - 1) // TILE - t0 + 1
+
+
+def pieces_for_cta(c, grid, B, Hkv, lens, qlen, window, cap, S):
+    spans = [seq_span(L, qlen, window, cap) for L in lens]
+    out = []
+    if S == 0:
+        pre = [0]
+        for _, _, n in spans:
+            pre.append(pre[-1] + n * Hkv)
+        T = pre[B]
+        C = min(grid, T)
+        gb, ge = (T * c // C, T * (c + 1) // C) if c < C else (0, 0)
+        owner = lambda x: ((x + 1) * C - 1) // T
+        g = gb
+        b = max([i for i in range(B) if pre[i] <= g] or [0])
+        while g < ge:
+            while pre[b + 1] <= g:
+                b += 1
+            n = (pre[b + 1] - pre[b]) // Hkv
+            kh = (g - pre[b]) // n
+            us = pre[b] + kh * n
+            ue = us + n
+            pe = min(ue, ge)
+            L, t0, _ = spans[b]
+            npieces = owner(ue - 1) - owner(us) + 1
+            slot = 2 * c + (1 if gb < us else 0)
+            slots = [2 * cc + (1 if T * cc // C < us else 0) for cc in range(owner(us), owner(us) + npieces)]
+            out.append(dict(unit=b * Hkv + kh, tiles=list(range(t0 + g - us, t0 + pe - us)),
+                            npieces=npieces, slot=slot, all_slots=slots, ticket=owner(us)))
+            g = pe
+        for b in range(c, B, grid):
+            if pre[b + 1] == pre[b]:
+                for kh in range(Hkv):
+                    out.append(dict(unit=b * Hkv + kh, tiles=[], npieces=1, slot=None, all_slots=[]))
+        return out, 2 * grid
+    total = B * Hkv * S
+    for p in range(c, total, grid):
+        u, s = divmod(p, S)
+        b, kh = divmod(u, Hkv)
+        L, t0, n = spans[b]
+        chunk = (n + S - 1) // S
+        c0, c1 = s * chunk, min(s * chunk + chunk, n)
+        if n == 0:
+            if s == 0:
+                out.append(dict(unit=u, tiles=[], npieces=1, slot=None, all_slots=[]))
+            continue
+        if c0 >= c1:
+            continue
+        npieces = (n + chunk - 1) // chunk
+        out.append(dict(unit=u, tiles=list(range(t0 + c0, t0 + c1)), npieces=npieces, slot=u * S + s,
+                        all_slots=[u * S + k for k in range(npieces)], ticket=u))
+    return out, (B * Hkv * S if S > 1 else 0)
+
+
+def check(B, Hkv, lens, qlen, window, cap, S, grid):
+    seen = {}
+    slots_used = []
+    units_pieces = {}
+    for c in range(grid):
+        pcs, nslots = pieces_for_cta(c, grid, B, Hkv, lens, qlen, window, cap, S)
+        for pc in pcs:
+            u = pc["unit"]
+            units_pieces.setdefault(u, []).append(pc)
+            for t in pc["tiles"]:
+                assert (u, t) not in seen, "tile processed twice"
+                seen[(u, t)] = c
+            if pc["npieces"] > 1:
+                assert 0 <= pc["slot"] < nslots
+                slots_used.append(pc["slot"])
+    assert len(slots_used) == len(set(slots_used)), "two pieces share a slot"
+    tickets = {}
+    for u, pcs in units_pieces.items():
+        if pcs[0]["npieces"] > 1:
+            t = {pc["ticket"] for pc in pcs}
+            assert len(t) == 1, "pieces of one unit disagree on the ticket"
+            t = t.pop()
+            assert 0 <= t < 16384
+            assert tickets.setdefault(t, u) == u, "two split units share a ticket"
+    for b, L in enumerate(lens):
+        _, t0, n = seq_span(L, qlen, window, cap)
+        for kh in range(Hkv):
+            u = b * Hkv + kh
+            pcs = units_pieces.get(u, [])
+            got = sorted(t for pc in pcs for t in pc["tiles"])
+            assert got == list(range(t0, t0 + n)), "tiles missing"
+            if n == 0:
+                assert len(pcs) == 1 and pcs[0]["tiles"] == [], "empty unit needs one zero piece"
+                continue
+            assert all(pc["npieces"] == len(pcs) for pc in pcs), "ticket count mismatch"
+            if len(pcs) > 1:
+                assert sorted(pcs[0]["all_slots"]) == sorted(pc["slot"] for pc in pcs)
+                # the combiner visits partials in key order
+                order = [pc["slot"] for pc in sorted(pcs, key=lambda p: p["tiles"][0])]
+                assert pcs[0]["all_slots"] == order
+
+
+CASES = [
+    (1, 4, [4096], 1, 0), (2, 4, [4096, 4096], 1, 0), (32, 4, [4096] * 32, 1, 0),
+    (2, 2, [100, 0], 1, 0), (3, 2, [0, 0, 0], 1, 0), (4, 2, [1, 15, 17, 333], 1, 0),
+    (3, 2, [1, 2, 40], 3, 0), (2, 1, [100, 16], 1, 1), (2, 2, [97, 300], 2, 5),
+    (2, 4, [32768, 32768], 1, 4096), (8, 4, [8192] * 8, 3, 0),
+]
+
+
+@pytest.mark.parametrize("grid", [1, 3, 7, 152])
+@pytest.mark.parametrize("S", [0, 1, 3, 8, 17])
+@pytest.mark.parametrize("case", CASES)
+def test_schedule_covers_each_tile_once(case, S, grid):
+    B, Hkv, lens, qlen, window = case
+    cap = 1 << 20
+    check(B, Hkv, lens, qlen, window, cap, S, grid)
+
+
+def test_schedule_random():
+    rng = random.Random(0)
+    for _ in range(200):
+        B = rng.randint(1, 40)
+        Hkv = rng.randint(1, 8)
+        lens = [rng.choice([0, rng.randint(1, 20), rng.randint(1, 3000)]) for _ in range(B)]
+        qlen = rng.randint(1, 4)
+        window = rng.choice([0, 0, rng.randint(1, 500)])
+        S = rng.choice([0, 0, 1, 2, 5, 9])
+        grid = rng.choice([1, 2, 5, 16, 152])
+        check(B, Hkv, lens, qlen, window, 1 << 20, S, grid)
