@@ -1,16 +1,18 @@
 // decode_f16_d256.cu -- instantiations of the decode kernel for f16 KV, D=256.
 // NT = row tiles of 8 query rows (rows per unit = Hq/Hkv * qlen <= 8*NT);
-// KG = key groups; the ring takes as many stages as shared memory allows.
+// KG = key groups (consumer warps per row tile); two CTAs share each SM, so
+// two producers keep the SM's TMA traffic flowing; the ring takes as many
+// stages as half an SM's shared memory allows.
 #include "launch.h"
 
 namespace pd {
 namespace {
 constexpr bool kFp8 = false;
 constexpr int kD = 256;
-using C1 = Cfg<kD, kFp8, 1, 4, ring_stages<kD, kFp8, 1, 4>()>;
-using C2 = Cfg<kD, kFp8, 2, 2, ring_stages<kD, kFp8, 2, 2>()>;
-using C3 = Cfg<kD, kFp8, 3, 2, ring_stages<kD, kFp8, 3, 2>()>;
-using C4 = Cfg<kD, kFp8, 4, 2, ring_stages<kD, kFp8, 4, 2>()>;
+using C1 = CfgFor<kD, kFp8, 1, 2, 2>;
+using C2 = CfgFor<kD, kFp8, 2, 1, 2>;
+using C3 = CfgFor<kD, kFp8, 3, 1, 2>;
+using C4 = CfgFor<kD, kFp8, 4, 1, 2>;
 }  // namespace
 
 bool shape_f16_d256(int nt, KernelShape* out) {

@@ -41,7 +41,7 @@
 namespace pd {
 
 constexpr int kTileKeys = 16;      // keys per pipeline tile
-constexpr int kMaxAutoB = 2048;    // sequences handled by the balanced split
+constexpr int kMaxAutoB = 1024;    // sequences handled by the balanced split
 // The workspace opens with a fixed header of split tickets that every call
 // layout shares and leaves at zero; partials follow it and never overlap it.
 constexpr int kTickets = 16384;
@@ -66,9 +66,10 @@ struct DecodeParams {
   unsigned long long timeout_ns;
 };
 
-template <int D_, bool FP8_, int NT_, int KG_, int NS_>
+template <int D_, bool FP8_, int NT_, int KG_, int NS_, int MINB_>
 struct Cfg {
   static constexpr int D = D_, NT = NT_, KG = KG_, NS = NS_;
+  static constexpr int kMinBlocks = MINB_;              // resident CTAs per SM the plan targets
   static constexpr bool FP8 = FP8_;
   static constexpr int kElem = FP8 ? 1 : 2;
   static constexpr int kSlabElems = 128 / kElem;        // one 128-byte swizzle row
@@ -252,7 +253,7 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
 
 // ---------------------------------------------------------------------------
 template <class Cfg>
-__global__ void __launch_bounds__(Cfg::kThreads, 1)
+__global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
     decode_paged_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
   constexpr int D = Cfg::D, NT = Cfg::NT, KG = Cfg::KG, NS = Cfg::NS;
@@ -333,28 +334,29 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const int n = min(32, pc.ntiles - t);
         for (int i = 0; i < n; ++i, ++q) {
           int blk = __shfl_sync(0xffffffffu, cur, i);
+          if (blk < 0 || blk >= p.num_blocks) {
+            if (lane == 0) raise_error(p.error_flag, kErrBlockId);
+            blk = 0;
+          }
+          const int stage = q % NS;
+          const uint32_t fb = full0 + 8 * stage;
           if (lane == 0) {
-            if (blk < 0 || blk >= p.num_blocks) {
-              raise_error(p.error_flag, kErrBlockId);
-              blk = 0;
-            }
-            const int stage = q % NS;
             if (ok && q >= NS) ok = mbar_wait(empty0 + 8 * stage, ((q / NS) - 1) & 1, p.timeout_ns);
-            if (!ok) continue;
+            if (ok) mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) continue;
+          // lanes 0..kSlabs-1 load the K slabs, the next kSlabs lanes the V slabs
+          if (lane < 2 * Cfg::kSlabs) {
             const int tile = pc.first_tile + t + i;
             const int z = blk * p.block_size + (tile % p.tiles_per_block) * kTileKeys;
-            const uint32_t dst = smem_u32(smem + stage * Cfg::kStageBytes);
-            const uint32_t fb = full0 + 8 * stage;
-            mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
-#pragma unroll
-            for (int s = 0; s < Cfg::kSlabs; ++s)
-              tma_load_3d(dst + s * Cfg::kSlabBytes, &tm_k, fb, s * Cfg::kSlabElems, pc.kh, z, pol);
-#pragma unroll
-            for (int s = 0; s < Cfg::kSlabs; ++s)
-              tma_load_3d(dst + Cfg::kTileBytes + s * Cfg::kSlabBytes, &tm_v, fb,
-                          s * Cfg::kSlabElems, pc.kh, z, pol);
-            issued = q + 1;
+            const int sl = lane % Cfg::kSlabs;
+            const bool is_v = lane >= Cfg::kSlabs;
+            const uint32_t dst = smem_u32(smem + stage * Cfg::kStageBytes) +
+                                 (is_v ? Cfg::kTileBytes : 0) + sl * Cfg::kSlabBytes;
+            tma_load_3d(dst, is_v ? &tm_v : &tm_k, fb, sl * Cfg::kSlabElems, pc.kh, z, pol);
           }
+          issued = q + 1;
         }
         cur = nxt;
       }

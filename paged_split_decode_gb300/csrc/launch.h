@@ -10,9 +10,10 @@
 namespace pd {
 
 struct KernelShape {
-  int threads;     // threads per CTA
-  int smem_bytes;  // dynamic shared memory per CTA
-  int rows_padded; // RP: query rows per unit rounded up to the row-tile size
+  int threads;      // threads per CTA
+  int smem_bytes;   // dynamic shared memory per CTA
+  int rows_padded;  // RP: query rows per unit rounded up to the row-tile size
+  int ctas_per_sm;  // resident CTAs per SM the configuration is sized for
 };
 
 // Returns false when no instantiation covers (D, fp8, nt).
@@ -55,22 +56,26 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
   return cudaGetLastError();
 }
 
-// Largest ring (stage count, capped at 32) whose shared-memory plan fits the
-// 227 KiB a CTA may use on sm_103a.
-constexpr int kSmemLimit = 227 * 1024;
-template <int D, bool FP8, int NT, int KG, int NS = 32>
+// Largest ring (stage count, capped at 32) whose shared-memory plan lets
+// MINB CTAs share one SM's 228 KiB (1 KiB of it reserved per CTA; at most
+// 227 KiB for one CTA).
+constexpr int smem_limit(int minb) { return minb == 1 ? 227 * 1024 : 228 * 1024 / minb - 1024; }
+template <int D, bool FP8, int NT, int KG, int MINB, int NS = 32>
 constexpr int ring_stages() {
-  if constexpr (NS <= 2 || Cfg<D, FP8, NT, KG, NS>::kSmemBytes <= kSmemLimit)
+  if constexpr (NS <= 2 || Cfg<D, FP8, NT, KG, NS, MINB>::kSmemBytes <= smem_limit(MINB))
     return NS;
   else
-    return ring_stages<D, FP8, NT, KG, NS - 1>();
+    return ring_stages<D, FP8, NT, KG, MINB, NS - 1>();
 }
+template <int D, bool FP8, int NT, int KG, int MINB>
+using CfgFor = Cfg<D, FP8, NT, KG, ring_stages<D, FP8, NT, KG, MINB>(), MINB>;
 
 template <class Cfg>
 bool shape_of(KernelShape* out) {
   out->threads = Cfg::kThreads;
   out->smem_bytes = Cfg::kSmemBytes;
   out->rows_padded = Cfg::RP;
+  out->ctas_per_sm = Cfg::kMinBlocks;
   return true;
 }
 

@@ -92,12 +92,13 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
   if (splits == 0 && d->B > kMaxAutoB) splits = 1;  // plenty of units: one piece each
   if (splits > 1 && pl->units > kTickets) return PD_ERR_UNSUPPORTED;
   pl->splits = splits;
+  const int ctas = sms * ks.ctas_per_sm;  // persistent grid: every resident CTA slot
   if (splits == 0) {
-    pl->grid = sms;
-    pl->slots = 2ll * sms;
+    pl->grid = ctas;
+    pl->slots = 2ll * ctas;
   } else {
     const long long pieces = pl->units * splits;
-    pl->grid = static_cast<int>(pieces < sms ? (pieces > 0 ? pieces : 1) : sms);
+    pl->grid = static_cast<int>(pieces < ctas ? (pieces > 0 ? pieces : 1) : ctas);
     pl->slots = splits > 1 ? pieces : 0;
   }
   if (pl->slots == 0) {
