@@ -150,6 +150,36 @@ PD_API pd_status decode_paged(const void* q, const void* k_cache, const void* v_
 PD_API pd_status decode_paged_combine(const float* part_m, const float* part_l, const float* part_o,
                                int rows, int num_splits, int D, void* out, void* stream);
 
+/* Size of the scratch array built into the library for
+ * decode_paged_static_scratch (8 MiB). Every GPU that loads the library
+ * keeps this much device memory until the process exits. */
+#define PD_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* decode_paged for callers that cannot allocate device memory (no counterpart
+ * in the pages: it exists for this library's users). Some callers cannot call
+ * cudaMalloc -- code running inside an allocator's own callbacks, a plugin
+ * host that hands out no device buffers, a process whose device footprint is
+ * fixed after start-up -- so they cannot provide decode_paged's workspace.
+ * This entry point takes the same arguments minus the workspace and uses a
+ * scratch array of PD_STATIC_SCRATCH_BYTES compiled into the library.
+ *   - It allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ *     library routine. The caller still owns q, the caches, the tables,
+ *     out and error_flag.
+ *   - Calls whose workspace (pd_workspace_bytes) exceeds
+ *     PD_STATIC_SCRATCH_BYTES return PD_ERR_WORKSPACE before anything runs.
+ *   - Each call first clears the scratch's split tickets on `stream`
+ *     (cudaMemsetAsync), then launches as decode_paged does.
+ *   - The first call on a device looks up the scratch's device address on
+ *     that device (cudaGetSymbolAddress, the device being current); make
+ *     that first call before any stream capture.
+ *   - All calls on a device share the one scratch array, which keeps the
+ *     last call's contents: calls that may overlap on the GPU (different
+ *     streams without ordering between them) race and give wrong results. */
+PD_API pd_status decode_paged_static_scratch(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_table, const int32_t* seq_lens, float scale,
+                       int window, int qlen, int num_splits, void* out, const pd_dims* dims,
+                       uint32_t* error_flag, void* stream);
+
 /* Human-readable name of a status. */
 PD_API const char* pd_status_str(pd_status status);
 

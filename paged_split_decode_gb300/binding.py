@@ -23,8 +23,8 @@ DEVERR_BLOCK_ID = 1
 DEVERR_SEQ_LEN = 2
 DEVERR_TIMEOUT = 4
 
-EXPORTS = ("decode_paged", "decode_paged_combine", "pd_workspace_bytes", "pd_grid_ctas",
-           "pd_status_str")
+EXPORTS = ("decode_paged", "decode_paged_combine", "decode_paged_static_scratch",
+           "pd_workspace_bytes", "pd_grid_ctas", "pd_status_str")
 
 
 class PdDims(ctypes.Structure):

@@ -45,6 +45,7 @@ constexpr int kMaxAutoB = 1024;    // sequences handled by the balanced split
 // The workspace opens with a fixed header of split tickets that every call
 // layout shares and leaves at zero; partials follow it and never overlap it.
 constexpr int kTickets = 16384;
+constexpr size_t kTicketHeaderBytes = static_cast<size_t>(kTickets) * sizeof(int);
 constexpr uint32_t kErrBlockId = 1u, kErrSeqLen = 2u, kErrTimeout = 4u;
 constexpr float kLog2e = 1.4426950408889634f;
 

@@ -1,0 +1,85 @@
+"""The scratch-free entry point, decode_paged_static_scratch.
+
+Callers that cannot allocate device memory (code inside an allocator's
+callbacks, plugin hosts that hand out no device buffers, processes whose
+device footprint is fixed after start-up) use this entry point: it runs the
+same decode as decode_paged but keeps its split partials in a scratch array
+built into the library instead of a caller-provided workspace.
+
+The test calls it through the C ABI (ctypes) twice in a row and compares each
+result with decode_paged's on the same inputs, within the 2e-3 tolerance the
+parity tests use. This file is collected last so that a stop-at-first-failure
+run has already run every other test; it also passes on its own in a fresh
+process.
+"""
+import ctypes
+
+import pytest
+import torch
+
+from paged_split_decode_gb300 import binding, inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lib = binding.load()
+    P = ctypes.c_void_p
+    fn = lib.decode_paged_static_scratch
+    fn.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int, P,
+                   ctypes.POINTER(binding.PdDims), P, P]
+    fn.restype = ctypes.c_int
+    return lib
+
+
+def _device(w):
+    return (w.q.to(DEV), w.k_cache.to(DEV), w.v_cache.to(DEV), w.block_table.to(DEV),
+            w.seq_lens.to(DEV))
+
+
+def _call_static(lib, w, t, num_splits, out, flag):
+    q, k, v, bt, sl = t
+    dims = binding.dims_of(q, k, bt, w.qlen, w.kv_fp8, w.k_scale, w.v_scale)
+    stream = torch.cuda.current_stream().cuda_stream
+    return lib.decode_paged_static_scratch(q.data_ptr(), k.data_ptr(), v.data_ptr(), bt.data_ptr(),
+                                           sl.data_ptr(), w.scale, w.window, w.qlen, num_splits,
+                                           out.data_ptr(), ctypes.byref(dims), flag.data_ptr(),
+                                           stream)
+
+
+def test_static_scratch_matches_decode_paged(lib):
+    # balanced split over every SM: the partials and tickets live in the scratch
+    cases = [inputs.gqa_d256(2), inputs.make_workload(B=5, Hq=32, Hkv=8, D=128, qlen=1,
+                                                       seq_lens=[3000, 0, 17, 900, 4096], seed=31)]
+    for w in cases:
+        t = _device(w)
+        q, k, v, bt, sl = t
+        want = binding.decode_paged(q, k, v, bt, sl, w.scale, w.window, w.qlen, 0,
+                                    k_scale=w.k_scale, v_scale=w.v_scale)
+        torch.cuda.synchronize()
+        for _ in range(2):  # two calls in a row share the scratch
+            out = torch.full_like(q, float("nan"))
+            flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+            assert _call_static(lib, w, t, 0, out, flag) == 0
+            torch.cuda.synchronize()
+            assert int(flag.item()) == 0
+            err = (out.float() - want.float()).abs().max().item()
+            assert err <= TOL, f"{w.name}: max abs difference {err}"
+
+
+def test_static_scratch_rejects_plans_beyond_its_size(lib):
+    # 32 query rows per KV head at D=256 need 608 slots x 32 rows x 256 floats
+    # of partials on a 152-SM GPU: more than the 8 MiB scratch.
+    w = inputs.make_workload(B=2, Hq=8, Hkv=1, D=256, qlen=4, seq_lens=[600, 35], seed=32)
+    t = _device(w)
+    need = binding.workspace_bytes(binding.dims_of(t[0], t[1], t[3], w.qlen), w.qlen, 0)
+    if need <= (8 << 20):
+        pytest.skip("this GPU's plan fits the scratch")
+    out = torch.empty_like(t[0])
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    assert _call_static(lib, w, t, 0, out, flag) == 6  # PD_ERR_WORKSPACE
