@@ -212,45 +212,68 @@ def max_over_ranks(x, world, device):
 
 
 # ---------------------------------------------------------------------------
-class Rotation:
-    """n_rot disjoint block tables over one device pool (cold L2 per step)."""
+class DeviceWorkload:
+    """A workload resident in HBM with n_rot disjoint block tables over one
+    pool at least 4x the L2 size, so consecutive steps never find their K/V in
+    L2. Values: N(0,1) fp16 (or e4m3fn codes, NaN codes excluded) drawn on the
+    device from a seeded generator; the timed path does not look at them."""
 
-    def __init__(self, B, device, l2_bytes, seed):
+    def __init__(self, device, l2_bytes, seed, B, Hq, Hkv, Dh, seq_lens, qlen=1, window=0,
+                 kv="f16", layout="permuted", bs=BS, max_blocks=None):
         gen = torch.Generator().manual_seed(seed)
-        nblk = (SEQ_LEN + BS - 1) // BS
-        per_table = B * nblk
-        blk_bytes = BS * HKV * D * 2
-        footprint = per_table * blk_bytes * 2
-        self.n_rot = max(2, -(-4 * l2_bytes // footprint))
+        need = [(L + bs - 1) // bs for L in seq_lens]
+        self.max_blocks = max_blocks or max(need + [1])
+        per_table = max(sum(need), 1)
+        elem = 1 if kv == "fp8" else 2
+        footprint = per_table * bs * Hkv * Dh * elem * 2
+        self.n_rot = min(1024, max(2, -(-4 * l2_bytes // footprint)))
         pool = self.n_rot * per_table
-        ids = torch.randperm(pool, generator=gen).to(torch.int32)
-        self.tables = [ids[r * per_table:(r + 1) * per_table].view(B, nblk).contiguous().to(device)
-                       for r in range(self.n_rot)]
-        # pool values: N(0,1) fp16 drawn on the device from a seeded generator
+        ids = torch.randperm(pool, generator=gen).to(torch.int32) if layout == "permuted" \
+            else torch.arange(pool, dtype=torch.int32)
+        self.tables = []
+        for r in range(self.n_rot):
+            t = torch.full((B, self.max_blocks), -1, dtype=torch.int32)
+            off = r * per_table
+            for b, n in enumerate(need):
+                t[b, :n] = ids[off:off + n]
+                off += n
+            self.tables.append(t.to(device))
         dg = torch.Generator(device=device).manual_seed(seed + 1)
-        self.k = torch.randn((pool, BS, HKV, D), generator=dg, device=device,
+        shape = (pool, bs, Hkv, Dh)
+        if kv == "fp8":
+            def codes():
+                mag = torch.randint(0, 0x7E + 1, shape, generator=dg, device=device, dtype=torch.int32)
+                sign = torch.randint(0, 2, shape, generator=dg, device=device, dtype=torch.int32)
+                return (mag | (sign << 7)).to(torch.uint8)
+            self.k, self.v = codes(), codes()
+            self.k_scale = self.v_scale = 1.0 / 64
+        else:
+            self.k = torch.randn(shape, generator=dg, device=device, dtype=torch.float32).to(torch.float16)
+            self.v = torch.randn(shape, generator=dg, device=device, dtype=torch.float32).to(torch.float16)
+            self.k_scale = self.v_scale = 1.0
+        self.q = torch.randn((B * qlen, Hq, Dh), generator=dg, device=device,
                              dtype=torch.float32).to(torch.float16)
-        self.v = torch.randn((pool, BS, HKV, D), generator=dg, device=device,
-                             dtype=torch.float32).to(torch.float16)
-        self.q = torch.randn((B, HQ, D), generator=dg, device=device,
-                             dtype=torch.float32).to(torch.float16)
-        self.seq_lens = torch.full((B,), SEQ_LEN, dtype=torch.int32, device=device)
+        self.seq_lens = torch.tensor(seq_lens, dtype=torch.int32, device=device)
         self.out = torch.empty_like(self.q)
-        self.B = B
+        self.B, self.qlen, self.window, self.Dh = B, qlen, window, Dh
+        self.kv_bytes = kv_bytes_of(seq_lens, qlen, window, Hkv, Dh, elem)
+        self.scale = 1.0 / Dh ** 0.5
 
 
-def time_device(B, steps, warmup, device, l2_bytes, seed, world):
+def time_workload(wl, num_splits, steps, warmup, device, world, sample_clocks=False):
+    """K calls captured in one CUDA graph (table r % n_rot for call r), replayed
+    once between CUDA events on the launching stream."""
     import paged_split_decode_gb300 as pd
-    rot = Rotation(B, device, l2_bytes, seed)
-    scale = 1.0 / D ** 0.5
     stream = torch.cuda.Stream(device)
-    dims = pd.dims_of(rot.q, rot.k, rot.tables[0], 1)
-    ws = pd.get_workspace(device, pd.workspace_bytes(dims, 1, 0))
+    dims = pd.dims_of(wl.q, wl.k, wl.tables[0], wl.qlen, wl.k.dtype == torch.uint8, wl.k_scale,
+                      wl.v_scale)
+    ws = pd.get_workspace(device, pd.workspace_bytes(dims, wl.qlen, num_splits))
     flag = torch.zeros(1, dtype=torch.int32, device=device)
 
     def call(r):
-        pd.decode_paged(rot.q, rot.k, rot.v, rot.tables[r % rot.n_rot], rot.seq_lens, scale, 0, 1,
-                        0, out=rot.out, workspace=ws, error_flag=flag)
+        pd.decode_paged(wl.q, wl.k, wl.v, wl.tables[r % wl.n_rot], wl.seq_lens, wl.scale, wl.window,
+                        wl.qlen, num_splits, out=wl.out, k_scale=wl.k_scale, v_scale=wl.v_scale,
+                        workspace=ws, error_flag=flag)
 
     with torch.cuda.stream(stream):
         for r in range(warmup):
@@ -264,20 +287,55 @@ def time_device(B, steps, warmup, device, l2_bytes, seed, world):
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(device)
-    with ClockSampler(gpu_smi_id(device)) as clk, torch.cuda.stream(stream):
-        clk.mark_start()
+    clk = ClockSampler(gpu_smi_id(device)) if sample_clocks else None
+    if clk:
+        clk.__enter__()
+    with torch.cuda.stream(stream):
+        if clk:
+            clk.mark_start()
         start.record(stream)
         graph.replay()  # launches on the current stream, i.e. `stream`
         end.record(stream)
         end.synchronize()
-        clk.mark_end()
+        if clk:
+            clk.mark_end()
+    if clk:
+        clk.__exit__(None, None, None)
     torch.cuda.synchronize(device)
     barrier(world)
     ms = start.elapsed_time(end)
     if int(flag.item()) != 0:
         raise RuntimeError(f"device error flag {int(flag.item())}")
     del graph
-    return ms, clk.summary(), rot
+    grid = pd.grid_ctas(dims, wl.qlen, num_splits)
+    return ms, (clk.summary() if clk else None), grid
+
+
+def gqa6_workload(B, device, l2, seed):
+    return DeviceWorkload(device, l2, seed, B, HQ, HKV, D, [SEQ_LEN] * B)
+
+
+def other_workloads(device, l2, seed):
+    """The other workloads the metric covers, as (name, workload, num_splits)."""
+    out = []
+    out.append(("tiny_d128_b2_lens100_0", DeviceWorkload(device, l2, seed, 2, 8, 2, 128, [100, 0],
+                                                         max_blocks=8), 1))
+    g = torch.Generator().manual_seed(seed + 3)
+    lens = torch.randint(512, 16385, (32,), generator=g).tolist()
+    for (hq, hkv) in ((32, 8), (28, 4)):
+        for layout in ("dense", "permuted"):
+            out.append((f"gqa{hq // hkv}_d128_b32_ragged_{layout}",
+                        DeviceWorkload(device, l2, seed + hq, 32, hq, hkv, 128, lens, layout=layout,
+                                       max_blocks=1024), 0))
+    for B in (1, 2):
+        for window in (4096, 0):
+            wl = DeviceWorkload(device, l2, seed + 10 * B + window, B, 24, 4, 256, [32768] * B,
+                                window=window)
+            for S in (1, 3, 8, 0):
+                out.append((f"long_d256_L32768_b{B}_w{window or 'none'}_s{S or 'auto'}", wl, S))
+    out.append(("verify_q3_fp8_d256_L8192_b8",
+                DeviceWorkload(device, l2, seed + 99, 8, 24, 4, 256, [8192] * 8, qlen=3, kv="fp8"), 0))
+    return out
 
 
 def time_e2e(B, steps, warmup, device, seed, world):
@@ -416,23 +474,38 @@ def main():
     sweep = []
     Bs = [HEADLINE_B] if args.no_sweep else list(SWEEP_B)
     head = None
+    small_steps = min(args.steps, 200)
     for B in Bs:
-        ms, clk, rot = time_device(B, args.steps, args.warmup, device, l2, 1000 + B + 17 * rank, world)
+        wl = gqa6_workload(B, device, l2, 1000 + B + 17 * rank)
+        steps = args.steps if B == HEADLINE_B else small_steps
+        ms, clk, grid = time_workload(wl, 0, steps, args.warmup, device, world,
+                                      sample_clocks=(B == HEADLINE_B))
         ms = max_over_ranks(ms, world, device)
-        per = ms / args.steps
-        kvb = kv_bytes_of([SEQ_LEN] * B, 1, 0, HKV, D, 2)
-        gbs = kvb / (per * 1e-3) / 1e9
-        ent = {"B": B, "us_per_call": round(per * 1e3, 3), "kv_gbs": round(gbs, 1),
-               "frac_of_peak": round(gbs / peak, 4), "kv_bytes": kvb,
-               "grid_ctas": pd.grid_ctas(pd.dims_of(rot.q, rot.k, rot.tables[0], 1), 1, 0)}
-        sweep.append(ent)
+        per = ms / steps
+        gbs = wl.kv_bytes / (per * 1e-3) / 1e9
+        sweep.append({"B": B, "us_per_call": round(per * 1e3, 3), "kv_gbs": round(gbs, 1),
+                      "frac_of_peak": round(gbs / peak, 4), "kv_bytes": wl.kv_bytes,
+                      "grid_ctas": grid, "steps": steps})
         if B == HEADLINE_B:
-            head = (ms, per, kvb, gbs, clk)
-        del rot
+            head = (ms, per, wl.kv_bytes, gbs, clk)
+        del wl
         torch.cuda.empty_cache()
     ms, per, kvb, gbs, clk = head
     total_bytes = kvb * world
     value = total_bytes / (ms / args.steps * 1e-3) / 1e9
+
+    configs = []
+    if not args.no_sweep:
+        for name, wl, S in other_workloads(device, l2, 5000 + 17 * rank):
+            cms, _, grid = time_workload(wl, S, small_steps, args.warmup, device, world)
+            cms = max_over_ranks(cms, world, device)
+            cper = cms / small_steps
+            cg = wl.kv_bytes / (cper * 1e-3) / 1e9
+            configs.append({"workload": name, "num_splits": S or "auto",
+                            "us_per_call": round(cper * 1e3, 3), "kv_gbs": round(cg, 1),
+                            "frac_of_peak": round(cg / peak, 4), "kv_bytes": wl.kv_bytes,
+                            "grid_ctas": grid, "steps": small_steps})
+        torch.cuda.empty_cache()
 
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 10))
     e_ms, h2d, d2h = time_e2e(HEADLINE_B, e2e_steps, 2, device, 99 + rank, world)
@@ -463,6 +536,7 @@ def main():
             "gpu_launches": args.steps,
             "clocks": clk,
             "sweep": sweep,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -44,8 +44,9 @@ constexpr int kTileKeys = 16;      // keys per pipeline tile
 constexpr int kMaxAutoB = 1024;    // sequences handled by the balanced split
 // The workspace opens with a fixed header of split tickets that every call
 // layout shares and leaves at zero; partials follow it and never overlap it.
-constexpr int kTickets = 16384;
-constexpr size_t kTicketHeaderBytes = static_cast<size_t>(kTickets) * sizeof(int);
+constexpr int kTickets = 16384;        // tickets per tree level
+constexpr int kTicketLevels = 4;       // fan-out 8: up to 8^4 = 4096 pieces per unit
+constexpr size_t kTicketHeaderBytes = static_cast<size_t>(kTickets) * kTicketLevels * sizeof(int);
 constexpr uint32_t kErrBlockId = 1u, kErrSeqLen = 2u, kErrTimeout = 4u;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -56,7 +57,7 @@ struct DecodeParams {
   const int32_t* seq_lens;    // [B]
   float* ws_o;                // [slots, RP, D]   partial O (log2-domain weights)
   float* ws_ml;               // [slots, RP, 2]   partial (m, l), m in log2 units
-  int* ws_count;              // [kTickets]       split tickets (zero between calls)
+  int* ws_count;              // [kTicketLevels][kTickets] split tickets (zero between calls)
   uint32_t* error_flag;       // may be null
   int B, qlen, Hq, Hkv, G, R;
   int max_blocks, block_size, num_blocks, tiles_per_block;
@@ -253,6 +254,126 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
 }
 
 // ---------------------------------------------------------------------------
+// Split combine as a tree of fan-out 8 over a unit's P pieces (key order).
+// Node (level l, index j) covers pieces [j*8^l, (j+1)*8^l); its partial lives
+// in the workspace slot of its first piece (written in place over its first
+// child once the children are read), and level l's tickets are the l-th
+// array of the ticket header, indexed by that slot. Each piece publishes its
+// partial and bumps its parent's ticket; the last child to arrive merges the
+// children (running max over m, weights exp2(m_c - M)) and moves one level up,
+// until the root writes the output row. Children are merged in key order, so
+// the result does not depend on arrival order.
+template <class Cfg>
+__device__ __forceinline__ void combine_tree(const DecodeParams& p, const Piece& pc, long long T_total,
+                                             int C, float* scratch, int* s_misc) {
+  constexpr int D = Cfg::D, RP = Cfg::RP, NTH = Cfg::kConsumerThreads;
+  const int tid = threadIdx.x;
+  const int R = p.R, P = pc.npieces;
+  int s_first, s_base, s_step, k_me;
+  if (p.num_splits == 0) {
+    const int cf = pc.first_slot_cta;
+    s_first = 2 * cf + ((T_total * cf / C) < pc.unit_start ? 1 : 0);
+    s_base = 2 * cf;
+    s_step = 2;
+    k_me = blockIdx.x - cf;
+  } else {
+    s_first = s_base = pc.unit * p.num_splits;
+    s_step = 1;
+    k_me = pc.slot - s_first;
+  }
+  auto slot_of = [&](int k) -> long long { return k == 0 ? s_first : s_base + s_step * k; };
+  int level = 0, j = k_me, span = 1;
+  while (true) {
+    const int n_level = (P + span - 1) / span;
+    const int parent = j >> 3;
+    const int nchild = min(8, n_level - 8 * parent);
+    const int span_up = span * 8;
+    const bool root = span_up >= P;
+    const long long s_parent = slot_of(parent * span_up);
+    // publish: every thread's partial stores are ordered before the ticket by
+    // the barrier and thread 0's gpu-scope fence
+    named_bar_sync(1, NTH);
+    if (tid == 0) {
+      __threadfence();
+      int* t = p.ws_count + level * kTickets + s_parent;
+      const int prev = atomicAdd(t, 1);
+      const int last = prev == nchild - 1;
+      if (last) {
+        *t = 0;
+        __threadfence();
+      }
+      s_misc[0] = last;
+    }
+    named_bar_sync(1, NTH);
+    if (!s_misc[0]) break;
+    // merge the children, three 4-dim items per thread per pass; each item
+    // loads its row's (m, l) and its O slice of every child in one go
+    constexpr int DQ = D / 4, NI = (Cfg::NT >= 4) ? 1 : 3;  // fewer in flight under the 2-CTA register cap
+    const int items = R * DQ;
+    for (int base = tid; base < items; base += NI * NTH) {
+      float2 ml[NI][8];
+      float4 v[NI][8];
+#pragma unroll
+      for (int u = 0; u < NI; ++u) {
+        const int item = base + u * NTH;
+        const int r = item / DQ, dq = item % DQ;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          if (item < items && c < nchild) {
+            const long long sl = slot_of((8 * parent + c) * span);
+            ml[u][c] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (sl * RP + r) * 2));
+            v[u][c] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sl * RP + r) * D + dq * 4));
+          } else {
+            ml[u][c] = make_float2(-INFINITY, 0.f);
+            v[u][c] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < NI; ++u) {
+        const int item = base + u * NTH;
+        if (item >= items) continue;
+        const int r = item / DQ, dq = item % DQ;
+        float M = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) M = fmaxf(M, ml[u][c].x);
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float w = (ml[u][c].x == -INFINITY) ? 0.f : ex2(ml[u][c].x - M);
+          L += w * ml[u][c].y;
+          acc.x += w * v[u][c].x; acc.y += w * v[u][c].y;
+          acc.z += w * v[u][c].z; acc.w += w * v[u][c].w;
+        }
+        if (root) {
+          const float inv = (L > 0.f) ? p.out_scale / L : 0.f;
+          const int i = r / p.G, hl = r % p.G;
+          __half* dst = p.out + (static_cast<long long>(pc.b * p.qlen + i) * p.Hq + pc.kh * p.G + hl) * D + dq * 4;
+          uint2 o2;
+          o2.x = pack_half2(acc.x * inv, acc.y * inv);
+          o2.y = pack_half2(acc.z * inv, acc.w * inv);
+          *reinterpret_cast<uint2*>(dst) = o2;
+        } else {
+          // in place over the first child: every thread reads its own items
+          // before writing them, and the (m, l) of the row is written after
+          // the barrier below, once all threads have read it
+          __stcg(reinterpret_cast<float4*>(p.ws_o + (s_parent * RP + r) * D + dq * 4), acc);
+          if (dq == 0) scratch[r] = M, scratch[RP + r] = L;
+        }
+      }
+    }
+    if (root) break;
+    named_bar_sync(1, NTH);
+    for (int r = tid; r < R; r += NTH)
+      __stcg(reinterpret_cast<float2*>(p.ws_ml + (s_parent * RP + r) * 2),
+             make_float2(scratch[r], scratch[RP + r]));
+    ++level;
+    j = parent;
+    span = span_up;
+  }
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
     decode_paged_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -659,83 +780,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
                  make_float2(M, Ls));
       }
     }
-    if (!direct) {
-      // publish this piece; the last of the unit's pieces merges them all
-      __threadfence();
-      named_bar_sync(1, Cfg::kConsumerThreads);
-      if (tid == 0) {
-        const int prev = atomicAdd(p.ws_count + pc.ticket, 1);
-        const int last = prev == pc.npieces - 1;
-        if (last) p.ws_count[pc.ticket] = 0;
-        s_misc[0] = last;
-      }
-      named_bar_sync(1, Cfg::kConsumerThreads);
-      if (s_misc[0]) {
-        __threadfence();
-        // slot of partial k (key order): balanced mode 2*cta for the CTAs
-        // after the first, fixed mode unit*S + k
-        int slot0, slot_base, slot_step;
-        if (p.num_splits == 0) {
-          const int cf = pc.first_slot_cta;
-          const long long start = T_total * cf / it.C;
-          slot0 = 2 * cf + (start < pc.unit_start ? 1 : 0);
-          slot_base = 2 * cf;
-          slot_step = 2;
-        } else {
-          slot0 = slot_base = pc.unit * p.num_splits;
-          slot_step = 1;
-        }
-        for (int item = tid; item < p.R * DCH; item += Cfg::kConsumerThreads) {
-          const int r = item / DCH, dc = item % DCH;
-          // one pass in key order with a running max; loads four partials ahead
-          float m_run = -INFINITY, l_run = 0.f;
-          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          for (int k0 = 0; k0 < pc.npieces; k0 += 4) {
-            float2 ml[4];
-            float4 va[4], vb[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int k = k0 + j;
-              if (k < pc.npieces) {
-                const long long slot = (k == 0) ? slot0 : slot_base + slot_step * k;
-                ml[j] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (slot * Cfg::RP + r) * 2));
-                const float* src = p.ws_o + (slot * Cfg::RP + r) * D + dc * 8;
-                va[j] = __ldcg(reinterpret_cast<const float4*>(src));
-                vb[j] = __ldcg(reinterpret_cast<const float4*>(src + 4));
-              } else {
-                ml[j] = make_float2(-INFINITY, 0.f);
-                va[j] = vb[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-              }
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float mk = ml[j].x;
-              if (mk == -INFINITY) continue;
-              if (mk > m_run) {
-                const float sc = (m_run == -INFINITY) ? 0.f : ex2(m_run - mk);
-                l_run *= sc;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] *= sc;
-                m_run = mk;
-              }
-              const float w = ex2(mk - m_run);
-              l_run += w * ml[j].y;
-              acc[0] += w * va[j].x; acc[1] += w * va[j].y; acc[2] += w * va[j].z; acc[3] += w * va[j].w;
-              acc[4] += w * vb[j].x; acc[5] += w * vb[j].y; acc[6] += w * vb[j].z; acc[7] += w * vb[j].w;
-            }
-          }
-          const int i = r / p.G, hl = r % p.G;
-          __half* dst = p.out + (static_cast<long long>(pc.b * p.qlen + i) * p.Hq + pc.kh * p.G + hl) * D + dc * 8;
-          const float inv = (l_run > 0.f) ? p.out_scale / l_run : 0.f;
-          uint4 v;
-          v.x = pack_half2(acc[0] * inv, acc[1] * inv);
-          v.y = pack_half2(acc[2] * inv, acc[3] * inv);
-          v.z = pack_half2(acc[4] * inv, acc[5] * inv);
-          v.w = pack_half2(acc[6] * inv, acc[7] * inv);
-          *reinterpret_cast<uint4*>(dst) = v;
-        }
-      }
-    }
+    if (!direct) combine_tree<Cfg>(p, pc, T_total, it.C, merge_o, s_misc);
     named_bar_sync(1, Cfg::kConsumerThreads);  // merge buffers free again
   }
   if (!ok && lane == 0) raise_error(p.error_flag, kErrTimeout);

@@ -90,7 +90,7 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
   pl->units = static_cast<long long>(d->B) * d->Hkv;
   int splits = num_splits;
   if (splits == 0 && d->B > kMaxAutoB) splits = 1;  // plenty of units: one piece each
-  if (splits > 1 && pl->units > kTickets) return PD_ERR_UNSUPPORTED;
+  if (splits > 1 && (pl->units * splits > kTickets || splits > 4096)) return PD_ERR_UNSUPPORTED;
   pl->splits = splits;
   const int ctas = sms * ks.ctas_per_sm;  // persistent grid: every resident CTA slot
   if (splits == 0) {
@@ -105,7 +105,7 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
     pl->off_ml = pl->off_o = pl->bytes = 0;
   } else {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-    const size_t cnt = static_cast<size_t>(kTickets) * 4;
+    const size_t cnt = kTicketHeaderBytes;
     const size_t ml = up(static_cast<size_t>(pl->slots) * pl->rows_padded * 2 * 4);
     const size_t o = static_cast<size_t>(pl->slots) * pl->rows_padded * d->D * 4;
     pl->off_ml = cnt;

@@ -156,6 +156,15 @@ def test_one_workspace_across_changing_shapes(pd):
     assert int(torch.count_nonzero(hdr).item()) == 0
 
 
+@pytest.mark.parametrize("S", [0, 9, 64, 100, 500])
+def test_split_tree_with_many_pieces(pd, S):
+    """One KV head, one long sequence: the balanced split cuts it into one piece
+    per CTA (hundreds), a fixed split into S pieces; the combine tree (fan-out
+    8) then has up to three levels."""
+    w = inputs.make_workload(B=1, Hq=8, Hkv=1, D=128, seq_lens=[20000], seed=41, qlen=2)
+    check(w, gpu_run(pd, w, S), ref_run(w))
+
+
 def test_custom_scale_writes_into_out_only(pd):
     """A caller-owned out is written in full; bytes around it are untouched."""
     w = inputs.make_workload(B=2, Hq=24, Hkv=4, D=256, seq_lens=[1000, 0], seed=5, scale=0.37)
