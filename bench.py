@@ -315,27 +315,43 @@ def gqa6_workload(B, device, l2, seed):
     return DeviceWorkload(device, l2, seed, B, HQ, HKV, D, [SEQ_LEN] * B)
 
 
-def other_workloads(device, l2, seed):
-    """The other workloads the metric covers, as (name, workload, num_splits)."""
-    out = []
-    out.append(("tiny_d128_b2_lens100_0", DeviceWorkload(device, l2, seed, 2, 8, 2, 128, [100, 0],
-                                                         max_blocks=8), 1))
+def other_workloads(device, l2, seed, only=None):
+    """The other workloads the metric covers, as (name, workload, num_splits);
+    with `only`, just the one of that name (the others are not built)."""
+    full = []
+
+    def add(name, make, S):
+        full.append((name, make, S))
+
+    add("tiny_d128_b2_lens100_0", lambda: DeviceWorkload(device, l2, seed, 2, 8, 2, 128, [100, 0],
+                                                          max_blocks=8), 1)
     g = torch.Generator().manual_seed(seed + 3)
     lens = torch.randint(512, 16385, (32,), generator=g).tolist()
     for (hq, hkv) in ((32, 8), (28, 4)):
         for layout in ("dense", "permuted"):
-            out.append((f"gqa{hq // hkv}_d128_b32_ragged_{layout}",
-                        DeviceWorkload(device, l2, seed + hq, 32, hq, hkv, 128, lens, layout=layout,
-                                       max_blocks=1024), 0))
+            add(f"gqa{hq // hkv}_d128_b32_ragged_{layout}",
+                lambda hq=hq, hkv=hkv, layout=layout: DeviceWorkload(
+                    device, l2, seed + hq, 32, hq, hkv, 128, lens, layout=layout, max_blocks=1024), 0)
+    cache = {}
     for B in (1, 2):
         for window in (4096, 0):
-            wl = DeviceWorkload(device, l2, seed + 10 * B + window, B, 24, 4, 256, [32768] * B,
-                                window=window)
+            def mk(B=B, window=window):
+                key = (B, window)
+                if key not in cache:
+                    cache.clear()
+                    cache[key] = DeviceWorkload(device, l2, seed + 10 * B + window, B, 24, 4, 256,
+                                                [32768] * B, window=window)
+                return cache[key]
             for S in (1, 3, 8, 0):
-                out.append((f"long_d256_L32768_b{B}_w{window or 'none'}_s{S or 'auto'}", wl, S))
-    out.append(("verify_q3_fp8_d256_L8192_b8",
-                DeviceWorkload(device, l2, seed + 99, 8, 24, 4, 256, [8192] * 8, qlen=3, kv="fp8"), 0))
-    return out
+                add(f"long_d256_L32768_b{B}_w{window or 'none'}_s{S or 'auto'}", mk, S)
+    add("verify_q3_fp8_d256_L8192_b8",
+        lambda: DeviceWorkload(device, l2, seed + 99, 8, 24, 4, 256, [8192] * 8, qlen=3, kv="fp8"), 0)
+    add("verify_q3_f16_d256_L8192_b8",
+        lambda: DeviceWorkload(device, l2, seed + 98, 8, 24, 4, 256, [8192] * 8, qlen=3), 0)
+    for name, make, S in full:
+        if only is None or name == only:
+            yield name, make(), S
+
 
 
 def time_e2e(B, steps, warmup, device, seed, world):
@@ -452,6 +468,9 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--workload", default=None,
+                    help="time only this workload (a sweep name such as gqa6_d256_L4096_b8 or a "
+                         "name from the configs list) and print its line; for profiling")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -470,6 +489,26 @@ def main():
     props = torch.cuda.get_device_properties(device)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
     peak, peak_kind = measured_peaks()
+
+    if args.workload:
+        cands = [(f"gqa6_d256_L{SEQ_LEN}_b{B}", (lambda B=B: gqa6_workload(B, device, l2, 1000 + B)), 0)
+                 for B in SWEEP_B]
+        for name, wl, S in other_workloads(device, l2, 5000, only=args.workload):
+            cands.append((name, (lambda wl=wl: wl), S))
+        hit = [c for c in cands if c[0] == args.workload]
+        if not hit:
+            raise SystemExit(f"unknown workload {args.workload}; known: {[c[0] for c in cands]}")
+        name, make, S = hit[0]
+        wl = make()
+        ms, clk, grid = time_workload(wl, S, args.steps, args.warmup, device, world, sample_clocks=True)
+        per = ms / args.steps
+        g = wl.kv_bytes / (per * 1e-3) / 1e9
+        if rank == 0:
+            print(json.dumps({"workload": name, "num_splits": S or "auto", "us_per_call": round(per * 1e3, 3),
+                              "kv_gbs": round(g, 1), "frac_of_peak": round(g / peak, 4),
+                              "kv_bytes": wl.kv_bytes, "grid_ctas": grid, "steps": args.steps,
+                              "clocks": clk}), flush=True)
+        return
 
     sweep = []
     Bs = [HEADLINE_B] if args.no_sweep else list(SWEEP_B)

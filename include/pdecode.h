@@ -151,9 +151,9 @@ PD_API pd_status decode_paged_combine(const float* part_m, const float* part_l, 
                                int rows, int num_splits, int D, void* out, void* stream);
 
 /* Size of the scratch array built into the library for
- * decode_paged_static_scratch (8 MiB). Every GPU that loads the library
+ * decode_paged_static_scratch (32 MiB). Every GPU that loads the library
  * keeps this much device memory until the process exits. */
-#define PD_STATIC_SCRATCH_BYTES (8u << 20)
+#define PD_STATIC_SCRATCH_BYTES (32u << 20)
 
 /* decode_paged for callers that cannot allocate device memory (no counterpart
  * in the pages: it exists for this library's users). Some callers cannot call

@@ -79,18 +79,29 @@ struct Cfg {
   static constexpr int kSlabBytes = kTileKeys * 128;    // 2 KB, 1024-aligned
   static constexpr int kTileBytes = kSlabs * kSlabBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;    // K tile then V tile
-  static constexpr int kConsumerWarps = NT * KG;
+  // NT == 1: each consumer warp covers all of D for the 8 rows (DS = 1).
+  // NT >= 2: consumer warps come in pairs splitting D in halves; each warp of
+  // a pair covers all NT row tiles and converts only its half of every tile,
+  // and the pair adds their partial scores through shared memory (DS = 2).
+  // NT == 4: two row groups of two row tiles each, so a warp's fragments fit.
+  static constexpr int DS = NT == 1 ? 1 : 2;
+  static constexpr int RG = NT == 4 ? 2 : 1;
+  static constexpr int NTW = NT / RG;                    // row tiles per warp
+  static constexpr int kConsumerWarps = KG * RG * DS;
   static constexpr int kConsumerThreads = kConsumerWarps * 32;
   static constexpr int kThreads = kConsumerThreads + 32;
   static constexpr int RP = NT * 8;
   static constexpr int kDP = D + 4;                     // merge row pitch (floats)
   static constexpr int kMergeOBytes = NT * 8 * kDP * 4;        // one buffer per row tile
-  static constexpr int kMergeMLBytes = kConsumerWarps * 8 * 2 * 4;
+  static constexpr int kMergeMLBytes = KG * NT * 8 * 2 * 4;
+  static constexpr int kXchgFloats = 32 * 4 * NTW;       // one warp's partial S^T, lane-major
+  static constexpr int kXchgBytes = DS == 2 ? KG * RG * 2 * 2 * kXchgFloats * 4 : 0;
   static constexpr int kOffMergeO = NS * kStageBytes;
   static constexpr int kOffMergeML = kOffMergeO + kMergeOBytes;
-  static constexpr int kOffBars = (kOffMergeML + kMergeMLBytes + 15) / 16 * 16;
+  static constexpr int kOffXchg = (kOffMergeML + kMergeMLBytes + 15) / 16 * 16;
+  static constexpr int kOffBars = (kOffXchg + kXchgBytes + 15) / 16 * 16;
   static constexpr int kOffPre = kOffBars + 2 * NS * 8;
-  static constexpr int kOffMisc = kOffPre + (kMaxAutoB + 1) * 4;
+  static constexpr int kOffMisc = (kOffPre + (kMaxAutoB + 1) * 4 + 15) / 16 * 16;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
   static_assert(D % kSlabElems == 0, "D must be a multiple of the slab width");
   static_assert(D % 32 == 0, "D must be a multiple of 32");
@@ -105,14 +116,25 @@ struct Piece {
   int ntiles;       // tiles in this piece (0: a zero-fill piece for an empty unit)
   int npieces;      // pieces the unit was cut into (1: write the output directly)
   int slot;         // workspace slot of this piece's partial (npieces > 1)
-  int ticket;       // ticket of the unit (npieces > 1): balanced mode the CTA that
-                    // holds its first piece (each CTA starts at most one split unit),
-                    // fixed mode the unit index
+  int chunk;        // balanced mode: chunk the piece belongs to; fixed mode: split index
   int unit_t0;      // first visible tile of the unit (within the sequence)
   int unit;         // b * Hkv + kh
-  int first_slot_cta;  // balanced mode: the first CTA covering the unit
-  int unit_start;      // balanced mode: global tile index where the unit begins
+  int first_slot_cta;  // balanced mode: the first chunk covering the unit
+  long long unit_start;  // balanced mode: global tile index where the unit begins
+  int tile_lo_all;     // keys [tile_lo_all, tile_hi_all] are visible to every query
+  int tile_hi_all;     // token of the unit (empty range when hi < lo)
 };
+
+// Keys every query token of a sequence of length L sees: token 0 limits the
+// top (position L - qlen), token qlen-1 the window's start.
+__device__ __forceinline__ void common_range(const DecodeParams& p, int L, Piece& pc) {
+  const int hi = L - p.qlen;
+  const int last = L - 1;
+  int lo = 0;
+  if (p.window > 0) lo = max(0, last - p.window + 1);
+  pc.tile_lo_all = lo;
+  pc.tile_hi_all = hi;
+}
 
 __device__ __forceinline__ void raise_error(uint32_t* flag, uint32_t bit) {
   if (flag) atomicOr(flag, bit);
@@ -137,38 +159,53 @@ __device__ __forceinline__ void seq_span(const DecodeParams& p, int b, bool repo
   n = (L - 1) / kTileKeys - t0 + 1;
 }
 
+// Balanced mode: the visible 16-key tiles of all units, laid end to end (T of
+// them), are cut into Ce = min(grid, T) contiguous ranges of equal size (to
+// one tile), one per CTA; chunk k is CTA k's range. (A dynamic tail -- small
+// chunks taken from a global counter -- was measured and lost: every chunk
+// costs a key-group merge, a partial and a deeper combine tree.)
+struct ChunkPlan {
+  long long T;
+  int Ce;
+  __device__ __forceinline__ long long start(int k) const { return T * k / Ce; }
+  __device__ __forceinline__ long long end(int k) const { return T * (k + 1) / Ce; }
+  __device__ __forceinline__ int owner(long long x) const {
+    return static_cast<int>(((x + 1) * Ce - 1) / T);
+  }
+};
+
+__device__ __forceinline__ ChunkPlan make_chunk_plan(long long T, int grid) {
+  ChunkPlan cp;
+  cp.T = T;
+  cp.Ce = T <= 0 ? 0 : static_cast<int>(T < grid ? T : grid);
+  return cp;
+}
+
 struct WorkIter {
-  // balanced mode: the CTA's tile range [g_begin, g_end) out of T, with
-  // C = min(gridDim.x, T) CTAs holding non-empty ranges
-  long long g, g_end, g_begin, T;
-  int C;
+  ChunkPlan cp;
+  long long g, g_end, chunk_start;
+  int chunk;        // the CTA's range (balanced mode)
   int b;
   int zero_b;       // next sequence to test for zero-fill, stepping by gridDim.x
   int zero_kh;
-  // fixed-split mode
-  long long piece;
+  long long piece;  // fixed-split mode
 };
-
-__device__ __forceinline__ int owner_cta(long long x, long long T, int C) {
-  return static_cast<int>(((x + 1) * C - 1) / T);
-}
 
 __device__ __forceinline__ void work_init(const DecodeParams& p, const int* s_pre, WorkIter& it) {
   const int c = blockIdx.x;
   if (p.num_splits == 0) {
-    it.T = s_pre[p.B];
-    it.C = it.T < gridDim.x ? static_cast<int>(it.T) : static_cast<int>(gridDim.x);
-    if (c < it.C) {
-      it.g_begin = it.T * c / it.C;
-      it.g_end = it.T * (c + 1) / it.C;
+    it.cp = make_chunk_plan(s_pre[p.B], gridDim.x);
+    it.chunk = c;
+    if (c < it.cp.Ce) {
+      it.g = it.chunk_start = it.cp.start(c);
+      it.g_end = it.cp.end(c);
     } else {
-      it.g_begin = it.g_end = 0;
+      it.g = it.g_end = it.chunk_start = 0;
     }
-    it.g = it.g_begin;
     // largest b with s_pre[b] <= g
     int lo = 0, hi = p.B - 1;
     while (lo < hi) {
-      int mid = (lo + hi + 1) >> 1;
+      const int mid = (lo + hi + 1) >> 1;
       if (s_pre[mid] <= it.g) lo = mid; else hi = mid - 1;
     }
     it.b = lo;
@@ -182,7 +219,7 @@ __device__ __forceinline__ void work_init(const DecodeParams& p, const int* s_pr
 // Produces the next piece; returns false when the CTA has no more work.
 __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pre, WorkIter& it,
                                           Piece& pc) {
-  const int C = gridDim.x, c = blockIdx.x;
+  const int C = gridDim.x;
   if (p.num_splits == 0) {
     if (it.g < it.g_end) {
       while (s_pre[it.b + 1] <= it.g) ++it.b;
@@ -198,12 +235,13 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
       pc.b = b; pc.kh = kh; pc.L = L; pc.unit_t0 = t0; pc.unit = b * p.Hkv + kh;
       pc.first_tile = t0 + static_cast<int>(it.g - us);
       pc.ntiles = static_cast<int>(pe - it.g);
-      const int cf = owner_cta(us, it.T, it.C), cl = owner_cta(ue - 1, it.T, it.C);
+      const int cf = it.cp.owner(us), cl = it.cp.owner(ue - 1);
       pc.npieces = cl - cf + 1;
-      pc.slot = 2 * c + (it.g_begin < us ? 1 : 0);
-      pc.ticket = cf;
+      pc.slot = 2 * it.chunk + (it.chunk_start < us ? 1 : 0);
+      pc.chunk = it.chunk;
       pc.first_slot_cta = cf;
-      pc.unit_start = static_cast<int>(us);
+      pc.unit_start = us;
+      common_range(p, L, pc);
       it.g = pe;
       return true;
     }
@@ -212,8 +250,8 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
       const int b = it.zero_b;
       if (s_pre[b + 1] == s_pre[b]) {
         pc.b = b; pc.kh = it.zero_kh; pc.L = 0; pc.unit_t0 = 0; pc.unit = b * p.Hkv + it.zero_kh;
-        pc.first_tile = 0; pc.ntiles = 0; pc.npieces = 1; pc.slot = 0; pc.ticket = 0;
-        pc.first_slot_cta = c; pc.unit_start = 0;
+        pc.first_tile = 0; pc.ntiles = 0; pc.npieces = 1; pc.slot = 0; pc.chunk = 0;
+        pc.first_slot_cta = 0; pc.unit_start = 0;
         if (++it.zero_kh == p.Hkv) { it.zero_kh = 0; it.zero_b += C; }
         return true;
       }
@@ -236,7 +274,7 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
     if (n == 0) {
       if (s != 0) continue;
       pc.b = b; pc.kh = kh; pc.L = 0; pc.unit_t0 = 0; pc.unit = u;
-      pc.first_tile = 0; pc.ntiles = 0; pc.npieces = 1; pc.slot = 0; pc.ticket = 0;
+      pc.first_tile = 0; pc.ntiles = 0; pc.npieces = 1; pc.slot = 0; pc.chunk = 0;
       pc.first_slot_cta = 0; pc.unit_start = 0;
       return true;
     }
@@ -246,8 +284,9 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
     pc.ntiles = c1 - c0;
     pc.npieces = (n + chunk - 1) / chunk;
     pc.slot = u * S + s;
-    pc.ticket = u;
+    pc.chunk = s;
     pc.first_slot_cta = 0; pc.unit_start = 0;
+    common_range(p, L, pc);
     return true;
   }
   return false;
@@ -264,18 +303,18 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
 // until the root writes the output row. Children are merged in key order, so
 // the result does not depend on arrival order.
 template <class Cfg>
-__device__ __forceinline__ void combine_tree(const DecodeParams& p, const Piece& pc, long long T_total,
-                                             int C, float* scratch, int* s_misc) {
+__device__ __forceinline__ void combine_tree(const DecodeParams& p, const Piece& pc, const ChunkPlan& cp,
+                                             float* scratch, int* s_misc) {
   constexpr int D = Cfg::D, RP = Cfg::RP, NTH = Cfg::kConsumerThreads;
   const int tid = threadIdx.x;
   const int R = p.R, P = pc.npieces;
   int s_first, s_base, s_step, k_me;
   if (p.num_splits == 0) {
     const int cf = pc.first_slot_cta;
-    s_first = 2 * cf + ((T_total * cf / C) < pc.unit_start ? 1 : 0);
+    s_first = 2 * cf + (cp.start(cf) < pc.unit_start ? 1 : 0);
     s_base = 2 * cf;
     s_step = 2;
-    k_me = blockIdx.x - cf;
+    k_me = pc.chunk - cf;
   } else {
     s_first = s_base = pc.unit * p.num_splits;
     s_step = 1;
@@ -378,7 +417,7 @@ template <class Cfg>
 __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
     decode_paged_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
-  constexpr int D = Cfg::D, NT = Cfg::NT, KG = Cfg::KG, NS = Cfg::NS;
+  constexpr int D = Cfg::D, KG = Cfg::KG, NS = Cfg::NS;
   constexpr bool FP8 = Cfg::FP8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -396,7 +435,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, NT);
+      mbar_init(empty0 + 8 * s, Cfg::RG * Cfg::DS);
     }
     fence_mbar_init();
   }
@@ -429,7 +468,6 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
 
   WorkIter it;
   work_init(p, s_pre, it);
-  const long long T_total = (p.num_splits == 0) ? s_pre[p.B] : 0;
   Piece pc;
 
   if (is_producer) {
@@ -497,25 +535,34 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
   }
 
   // -------------------------------------------------------------- consumers
-  const int nt = warp / KG, kg = warp % KG;
+  constexpr int DS = Cfg::DS, NTW = Cfg::NTW, RG = Cfg::RG;
+  const int dh = warp % DS;                   // half of D (DS = 2)
+  const int rg = (warp / DS) % RG;            // row group: row tiles rg*NTW .. rg*NTW+NTW-1
+  const int kg = warp / (DS * RG);            // key group
+  const int pair = kg * RG + rg;              // the D pair this warp belongs to
   const int g = lane >> 2, t4 = lane & 3;
   constexpr int KSTEPS = D / 16;
-  uint32_t qf[KSTEPS][2];
-  float o[D / 16][4];
+  constexpr int KSW = KSTEPS / DS;             // k-steps of this warp's part of D
+  constexpr int MTW = D / 16 / DS;             // m-tiles (16 output dims) of this warp
+  float* xchg = reinterpret_cast<float*>(smem + Cfg::kOffXchg);
+  uint32_t qf[KSW][NTW][2];
+  float o[MTW][NTW][4];
   uint32_t q = 0;      // ring sequence number of the piece's first tile
   bool ok = true;
 
   while (work_next(p, s_pre, it, pc)) {
     // ---- per-piece setup: Q fragments (B operand) and per-row visible key limits
-    {
-      const int r = nt * 8 + g;
+#pragma unroll
+    for (int n = 0; n < NTW; ++n) {
+      const int r = (rg * NTW + n) * 8 + g;
       const __half* qrow = nullptr;
       if (r < p.R && pc.ntiles > 0) {
         const int i = r / p.G, hl = r % p.G;
         qrow = p.q + (static_cast<long long>(pc.b * p.qlen + i) * p.Hq + pc.kh * p.G + hl) * D;
       }
 #pragma unroll
-      for (int ks = 0; ks < KSTEPS; ++ks) {
+      for (int ksl = 0; ksl < KSW; ++ksl) {
+        const int ks = dh * KSW + ksl;
         int d0, d1;
         if constexpr (FP8) {
           // k-step ks = (slab, super-step ss, j): dims slab*128 + 16*(2*t4+ss) + 4j + {0,1},{2,3}
@@ -526,31 +573,35 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           d0 = ks * 16 + 2 * t4;
           d1 = d0 + 8;
         }
-        qf[ks][0] = qrow ? __ldg(reinterpret_cast<const uint32_t*>(qrow + d0)) : 0u;
-        qf[ks][1] = qrow ? __ldg(reinterpret_cast<const uint32_t*>(qrow + d1)) : 0u;
+        qf[ksl][n][0] = qrow ? __ldg(reinterpret_cast<const uint32_t*>(qrow + d0)) : 0u;
+        qf[ksl][n][1] = qrow ? __ldg(reinterpret_cast<const uint32_t*>(qrow + d1)) : 0u;
       }
     }
-    int lo_r[2], hi_r[2];
+    int lo_r[NTW][2], hi_r[NTW][2];
+    float m_r[NTW][2], l_r[NTW][2];
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const int r = nt * 8 + 2 * t4 + c;
-      if (r < p.R) {
-        const int i = r / p.G;
-        const int pos = pc.L - p.qlen + i;
-        hi_r[c] = pos;
-        lo_r[c] = (p.window > 0) ? max(0, pos - p.window + 1) : 0;
-      } else {
-        hi_r[c] = -1;
-        lo_r[c] = 0;
+    for (int n = 0; n < NTW; ++n) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int r = (rg * NTW + n) * 8 + 2 * t4 + c;
+        if (r < p.R) {
+          const int pos = pc.L - p.qlen + r / p.G;
+          hi_r[n][c] = pos;
+          lo_r[n][c] = (p.window > 0) ? max(0, pos - p.window + 1) : 0;
+        } else {
+          hi_r[n][c] = -1;
+          lo_r[n][c] = 0;
+        }
+        m_r[n][c] = -INFINITY;
+        l_r[n][c] = 0.f;
       }
-    }
-    float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
 #pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      for (int mt = 0; mt < MTW; ++mt) o[mt][n][0] = o[mt][n][1] = o[mt][n][2] = o[mt][n][3] = 0.f;
+    }
 
-    // ---- this warp's tiles of the piece: ring numbers q + k with k % KG == kg
-    const int first_k = ((kg - static_cast<int>(q % KG)) % KG + KG) % KG;
-    for (int k = first_k; k < pc.ntiles; k += KG) {
+    // ---- this key group's tiles of the piece: k % KG == kg (piece-local, so
+    // the split of a piece over the key groups does not depend on the ring)
+    for (int k = kg; k < pc.ntiles; k += KG) {
       const uint32_t qq = q + k;
       const int stage = qq % NS;
       if (ok) ok = mbar_wait(full0 + 8 * stage, (qq / NS) & 1, p.timeout_ns);
@@ -559,95 +610,147 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
       const uint32_t vb = kb + Cfg::kTileBytes;
       const int key0 = (pc.first_tile + k) * kTileKeys;
 
-      // S^T = K Q^T  (16 keys x 8 rows), two accumulation chains
-      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      // S^T = K Q^T over this warp's part of D (16 keys x 8 rows per row tile)
+      float sa[NTW][4], sb[NTW][4];
+#pragma unroll
+      for (int n = 0; n < NTW; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sa[n][e] = sb[n][e] = 0.f;
       if constexpr (!FP8) {
         const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
         const uint32_t rowb = kb + key * 128;
 #pragma unroll
-        for (int ks = 0; ks < KSTEPS; ++ks) {
+        for (int ksl = 0; ksl < KSW; ++ksl) {
+          const int ks = dh * KSW + ksl;
           const int slab = ks >> 2, chunk = (ks & 3) * 2 + (lane >> 4);
           uint32_t a[4];
           ldsm_x4(rowb + slab * Cfg::kSlabBytes + ((chunk ^ (key & 7)) << 4), a);
-          if (ks & 1) mma_16816(sb, a, qf[ks][0], qf[ks][1]);
-          else mma_16816(sa, a, qf[ks][0], qf[ks][1]);
+#pragma unroll
+          for (int n = 0; n < NTW; ++n) {
+            if (ksl & 1) mma_16816(sb[n], a, qf[ksl][n][0], qf[ksl][n][1]);
+            else mma_16816(sa[n], a, qf[ksl][n][0], qf[ksl][n][1]);
+          }
         }
       } else {
         const uint32_t r0 = kb + g * 128, r8 = kb + (g + 8) * 128;
+        // super-steps of 4 k-steps: (slab, ss) = ks / 4
 #pragma unroll
-        for (int slab = 0; slab < Cfg::kSlabs; ++slab) {
+        for (int sup = 0; sup < KSW / 4; ++sup) {
+          const int gsup = dh * (KSW / 4) + sup;
+          const int slab = gsup >> 1, ss = gsup & 1;
+          const int chunk = (2 * t4 + ss) ^ (g & 7);
+          uint4 w0, w8;
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(w0.x), "=r"(w0.y), "=r"(w0.z), "=r"(w0.w)
+                       : "r"(r0 + slab * Cfg::kSlabBytes + (chunk << 4)));
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(w8.x), "=r"(w8.y), "=r"(w8.z), "=r"(w8.w)
+                       : "r"(r8 + slab * Cfg::kSlabBytes + (chunk << 4)));
+          const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w};
+          const uint32_t wb[4] = {w8.x, w8.y, w8.z, w8.w};
 #pragma unroll
-          for (int ss = 0; ss < 2; ++ss) {
-            const int chunk = (2 * t4 + ss) ^ (g & 7);
-            uint4 w0, w8;
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(w0.x), "=r"(w0.y), "=r"(w0.z), "=r"(w0.w)
-                         : "r"(r0 + slab * Cfg::kSlabBytes + (chunk << 4)));
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(w8.x), "=r"(w8.y), "=r"(w8.z), "=r"(w8.w)
-                         : "r"(r8 + slab * Cfg::kSlabBytes + (chunk << 4)));
-            const uint32_t wa[4] = {w0.x, w0.y, w0.z, w0.w};
-            const uint32_t wb[4] = {w8.x, w8.y, w8.z, w8.w};
+          for (int j = 0; j < 4; ++j) {
+            const int ksl = sup * 4 + j;
+            uint32_t a[4];
+            a[0] = e4m3x2_to_half2(static_cast<uint16_t>(wa[j] & 0xffffu));
+            a[1] = e4m3x2_to_half2(static_cast<uint16_t>(wb[j] & 0xffffu));
+            a[2] = e4m3x2_to_half2(static_cast<uint16_t>(wa[j] >> 16));
+            a[3] = e4m3x2_to_half2(static_cast<uint16_t>(wb[j] >> 16));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int ks = slab * 8 + ss * 4 + j;
-              uint32_t a[4];
-              a[0] = e4m3x2_to_half2(static_cast<uint16_t>(wa[j] & 0xffffu));
-              a[1] = e4m3x2_to_half2(static_cast<uint16_t>(wb[j] & 0xffffu));
-              a[2] = e4m3x2_to_half2(static_cast<uint16_t>(wa[j] >> 16));
-              a[3] = e4m3x2_to_half2(static_cast<uint16_t>(wb[j] >> 16));
-              if (j & 1) mma_16816(sb, a, qf[ks][0], qf[ks][1]);
-              else mma_16816(sa, a, qf[ks][0], qf[ks][1]);
+            for (int n = 0; n < NTW; ++n) {
+              if (j & 1) mma_16816(sb[n], a, qf[ksl][n][0], qf[ksl][n][1]);
+              else mma_16816(sa[n], a, qf[ksl][n][0], qf[ksl][n][1]);
             }
           }
         }
       }
-      // scores in log2 units, masked; C layout: [0]=(key g,row 2t4) [1]=(key g,row 2t4+1)
-      //                                          [2]=(key g+8,row 2t4) [3]=(key g+8,row 2t4+1)
-      float x[4];
-      {
-        const int j0 = key0 + g, j1 = j0 + 8;
-        x[0] = (j0 >= lo_r[0] && j0 <= hi_r[0]) ? (sa[0] + sb[0]) * p.sl2 : -INFINITY;
-        x[1] = (j0 >= lo_r[1] && j0 <= hi_r[1]) ? (sa[1] + sb[1]) * p.sl2 : -INFINITY;
-        x[2] = (j1 >= lo_r[0] && j1 <= hi_r[0]) ? (sa[2] + sb[2]) * p.sl2 : -INFINITY;
-        x[3] = (j1 >= lo_r[1] && j1 <= hi_r[1]) ? (sa[3] + sb[3]) * p.sl2 : -INFINITY;
-      }
-      float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+      float sc[NTW][4];
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      const float mn0 = fmaxf(m_r[0], mx0), mn1 = fmaxf(m_r[1], mx1);
-      const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
-      const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
-      const float a0 = ex2(m_r[0] - base0), a1 = ex2(m_r[1] - base1);
-      const float p00 = ex2(x[0] - base0), p01 = ex2(x[1] - base1);
-      const float p10 = ex2(x[2] - base0), p11 = ex2(x[3] - base1);
-      m_r[0] = mn0;
-      m_r[1] = mn1;
-      l_r[0] = l_r[0] * a0 + (p00 + p10);
-      l_r[1] = l_r[1] * a1 + (p01 + p11);
-      if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+      for (int n = 0; n < NTW; ++n)
 #pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-          o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
+        for (int e = 0; e < 4; ++e) sc[n][e] = sa[n][e] + sb[n][e];
+      if constexpr (DS == 2) {
+        // add the other half's partial scores (a + b == b + a: both warps of the
+        // pair end up with bitwise identical scores)
+        float* mine = xchg + ((pair * 2 + (qq & 1)) * 2 + dh) * Cfg::kXchgFloats + lane * 4 * NTW;
+        float* other = xchg + ((pair * 2 + (qq & 1)) * 2 + (dh ^ 1)) * Cfg::kXchgFloats + lane * 4 * NTW;
+#pragma unroll
+        for (int n = 0; n < NTW; ++n)
+          *reinterpret_cast<float4*>(mine + 4 * n) = make_float4(sc[n][0], sc[n][1], sc[n][2], sc[n][3]);
+        named_bar_sync(2 + pair, 64);
+#pragma unroll
+        for (int n = 0; n < NTW; ++n) {
+          const float4 v = *reinterpret_cast<const float4*>(other + 4 * n);
+          sc[n][0] += v.x; sc[n][1] += v.y; sc[n][2] += v.z; sc[n][3] += v.w;
         }
       }
-      // P^T as the B operand: transpose the (key x row) fp16 pairs
-      const uint32_t pb0 = movmatrix_trans(pack_half2(p00, p01));
-      const uint32_t pb1 = movmatrix_trans(pack_half2(p10, p11));
+      // per row tile: mask, online softmax, P^T fragments; C layout of S^T:
+      // [0]=(key g,row 2t4) [1]=(key g,row 2t4+1) [2]=(key g+8,row 2t4) [3]=(key g+8,row 2t4+1)
+      uint32_t pb0[NTW], pb1[NTW];
+      float al[NTW][2];
+      bool rescale = false;
+      // a tile every real row sees in full needs no per-key mask
+      const bool interior = key0 >= pc.tile_lo_all && key0 + kTileKeys - 1 <= pc.tile_hi_all;
+#pragma unroll
+      for (int n = 0; n < NTW; ++n) {
+        const int j0 = key0 + g, j1 = j0 + 8;
+        float x[4];
+        if (interior) {
+          // padded rows (hi = -1) stay masked
+          x[0] = hi_r[n][0] >= 0 ? sc[n][0] * p.sl2 : -INFINITY;
+          x[1] = hi_r[n][1] >= 0 ? sc[n][1] * p.sl2 : -INFINITY;
+          x[2] = hi_r[n][0] >= 0 ? sc[n][2] * p.sl2 : -INFINITY;
+          x[3] = hi_r[n][1] >= 0 ? sc[n][3] * p.sl2 : -INFINITY;
+        } else {
+          x[0] = (j0 >= lo_r[n][0] && j0 <= hi_r[n][0]) ? sc[n][0] * p.sl2 : -INFINITY;
+          x[1] = (j0 >= lo_r[n][1] && j0 <= hi_r[n][1]) ? sc[n][1] * p.sl2 : -INFINITY;
+          x[2] = (j1 >= lo_r[n][0] && j1 <= hi_r[n][0]) ? sc[n][2] * p.sl2 : -INFINITY;
+          x[3] = (j1 >= lo_r[n][1] && j1 <= hi_r[n][1]) ? sc[n][3] * p.sl2 : -INFINITY;
+        }
+        float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m_r[n][0], mx0), mn1 = fmaxf(m_r[n][1], mx1);
+        const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
+        const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
+        // nothing accumulated yet (m = -inf): O and l are zero, keep factor 1
+        al[n][0] = (m_r[n][0] == -INFINITY) ? 1.f : ex2(m_r[n][0] - base0);
+        al[n][1] = (m_r[n][1] == -INFINITY) ? 1.f : ex2(m_r[n][1] - base1);
+        const float p00 = ex2(x[0] - base0), p01 = ex2(x[1] - base1);
+        const float p10 = ex2(x[2] - base0), p11 = ex2(x[3] - base1);
+        m_r[n][0] = mn0;
+        m_r[n][1] = mn1;
+        l_r[n][0] = l_r[n][0] * al[n][0] + (p00 + p10);
+        l_r[n][1] = l_r[n][1] * al[n][1] + (p01 + p11);
+        rescale |= (al[n][0] != 1.f || al[n][1] != 1.f);
+        pb0[n] = movmatrix_trans(pack_half2(p00, p01));
+        pb1[n] = movmatrix_trans(pack_half2(p10, p11));
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+        for (int mt = 0; mt < MTW; ++mt)
+#pragma unroll
+          for (int n = 0; n < NTW; ++n) {
+            o[mt][n][0] *= al[n][0]; o[mt][n][1] *= al[n][1];
+            o[mt][n][2] *= al[n][0]; o[mt][n][3] *= al[n][1];
+          }
+      }
 
-      // O^T += V^T P^T
+      // O^T += V^T P^T over this warp's m-tiles
       if constexpr (!FP8) {
         const int key = (lane & 7) + (lane >> 4) * 8;
         const uint32_t rowb = vb + key * 128;
 #pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
+        for (int mtl = 0; mtl < MTW; ++mtl) {
+          const int mt = dh * MTW + mtl;
           const int slab = mt >> 2, chunk = (mt & 3) * 2 + ((lane >> 3) & 1);
           uint32_t a[4];
           ldsm_x4_trans(rowb + slab * Cfg::kSlabBytes + ((chunk ^ (key & 7)) << 4), a);
-          mma_16816(o[mt], a, pb0, pb1);
+#pragma unroll
+          for (int n = 0; n < NTW; ++n) mma_16816(o[mtl][n], a, pb0[n], pb1[n]);
         }
       } else {
         // 32-dim group P32: lane reads 4 codes at dims 32*P32 + 4g .. +3 of keys
@@ -655,7 +758,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
         // (m=g+8), m-tile 2*P32+1 takes 4g+2 and 4g+3.
         const int kA = 2 * t4, kB = kA + 1, kC = kA + 8, kD = kA + 9;
 #pragma unroll
-        for (int P32 = 0; P32 < D / 32; ++P32) {
+        for (int pl = 0; pl < MTW / 2; ++pl) {
+          const int P32 = dh * (MTW / 2) + pl;
           const int slab = P32 >> 2;
           const int chunk = (P32 & 3) * 2 + (g >> 2);
           const int byte = (4 * g) & 15;
@@ -672,12 +776,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           a[1] = e4m3x2_to_half2(static_cast<uint16_t>(ab01 >> 16));
           a[2] = e4m3x2_to_half2(static_cast<uint16_t>(cd01 & 0xffffu));
           a[3] = e4m3x2_to_half2(static_cast<uint16_t>(cd01 >> 16));
-          mma_16816(o[2 * P32], a, pb0, pb1);
+#pragma unroll
+          for (int n = 0; n < NTW; ++n) mma_16816(o[2 * pl][n], a, pb0[n], pb1[n]);
           a[0] = e4m3x2_to_half2(static_cast<uint16_t>(ab23 & 0xffffu));
           a[1] = e4m3x2_to_half2(static_cast<uint16_t>(ab23 >> 16));
           a[2] = e4m3x2_to_half2(static_cast<uint16_t>(cd23 & 0xffffu));
           a[3] = e4m3x2_to_half2(static_cast<uint16_t>(cd23 >> 16));
-          mma_16816(o[2 * P32 + 1], a, pb0, pb1);
+#pragma unroll
+          for (int n = 0; n < NTW; ++n) mma_16816(o[2 * pl + 1][n], a, pb0[n], pb1[n]);
         }
       }
       __syncwarp();
@@ -686,56 +792,68 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
     q += pc.ntiles;
 
     // ---- merge the KG key groups of each row tile through shared memory
+    // (m and l are identical in the two warps of a D pair; warp dh = 0 posts them)
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l_r[0] += __shfl_xor_sync(0xffffffffu, l_r[0], off);
-      l_r[1] += __shfl_xor_sync(0xffffffffu, l_r[1], off);
-    }
-    if (g == 0) {
-      float* ml = merge_ml + warp * 16;
-      ml[(2 * t4) * 2 + 0] = m_r[0];
-      ml[(2 * t4) * 2 + 1] = l_r[0];
-      ml[(2 * t4 + 1) * 2 + 0] = m_r[1];
-      ml[(2 * t4 + 1) * 2 + 1] = l_r[1];
+    for (int n = 0; n < NTW; ++n)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l_r[n][0] += __shfl_xor_sync(0xffffffffu, l_r[n][0], off);
+        l_r[n][1] += __shfl_xor_sync(0xffffffffu, l_r[n][1], off);
+      }
+    if (g == 0 && dh == 0) {
+#pragma unroll
+      for (int n = 0; n < NTW; ++n) {
+        float* ml = merge_ml + ((rg * NTW + n) * KG + kg) * 16;
+        ml[(2 * t4) * 2 + 0] = m_r[n][0];
+        ml[(2 * t4) * 2 + 1] = l_r[n][0];
+        ml[(2 * t4 + 1) * 2 + 0] = m_r[n][1];
+        ml[(2 * t4 + 1) * 2 + 1] = l_r[n][1];
+      }
     }
     named_bar_sync(1, Cfg::kConsumerThreads);
     {
       // this warp's weight per row: exp2(m_own - max over the key groups)
-      float f_r[2];
+      float f_r[NTW][2];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int row = 2 * t4 + c;
-        float M = -INFINITY;
+      for (int n = 0; n < NTW; ++n)
 #pragma unroll
-        for (int k = 0; k < KG; ++k) M = fmaxf(M, merge_ml[((nt * KG + k) * 8 + row) * 2]);
-        f_r[c] = (m_r[c] == -INFINITY) ? 0.f : ex2(m_r[c] - M);
-      }
-      // the row tile's buffer accumulates f * O one key group at a time
-      float* mo = merge_o + nt * 8 * Cfg::kDP;
+        for (int c = 0; c < 2; ++c) {
+          const int row = 2 * t4 + c;
+          float M = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < KG; ++k) M = fmaxf(M, merge_ml[(((rg * NTW + n) * KG + k) * 8 + row) * 2]);
+          f_r[n][c] = (m_r[n][c] == -INFINITY) ? 0.f : ex2(m_r[n][c] - M);
+        }
+      // each row tile's buffer accumulates f * O one key group at a time
       const int r0 = 2 * t4, r1 = r0 + 1;
 #pragma unroll 1
       for (int k = 0; k < KG; ++k) {
         if (kg == k) {
 #pragma unroll
-          for (int mt = 0; mt < D / 16; ++mt) {
-            int d0, d1;  // output dims of C rows g and g+8 of m-tile mt
-            if constexpr (FP8) {
-              d0 = (mt >> 1) * 32 + 4 * g + 2 * (mt & 1);
-              d1 = d0 + 1;
-            } else {
-              d0 = mt * 16 + g;
-              d1 = d0 + 8;
-            }
-            float* a00 = mo + r0 * Cfg::kDP + d0;
-            float* a10 = mo + r1 * Cfg::kDP + d0;
-            float* a01 = mo + r0 * Cfg::kDP + d1;
-            float* a11 = mo + r1 * Cfg::kDP + d1;
-            if (k == 0) {
-              *a00 = f_r[0] * o[mt][0]; *a10 = f_r[1] * o[mt][1];
-              *a01 = f_r[0] * o[mt][2]; *a11 = f_r[1] * o[mt][3];
-            } else {
-              *a00 += f_r[0] * o[mt][0]; *a10 += f_r[1] * o[mt][1];
-              *a01 += f_r[0] * o[mt][2]; *a11 += f_r[1] * o[mt][3];
+          for (int n = 0; n < NTW; ++n) {
+            float* mo = merge_o + (rg * NTW + n) * 8 * Cfg::kDP;
+#pragma unroll
+            for (int mtl = 0; mtl < MTW; ++mtl) {
+              const int mt = dh * MTW + mtl;
+              int d0, d1;  // output dims of C rows g and g+8 of m-tile mt
+              if constexpr (FP8) {
+                d0 = (mt >> 1) * 32 + 4 * g + 2 * (mt & 1);
+                d1 = d0 + 1;
+              } else {
+                d0 = mt * 16 + g;
+                d1 = d0 + 8;
+              }
+              float* a00 = mo + r0 * Cfg::kDP + d0;
+              float* a10 = mo + r1 * Cfg::kDP + d0;
+              float* a01 = mo + r0 * Cfg::kDP + d1;
+              float* a11 = mo + r1 * Cfg::kDP + d1;
+              if (k == 0) {
+                *a00 = f_r[n][0] * o[mtl][n][0]; *a10 = f_r[n][1] * o[mtl][n][1];
+                *a01 = f_r[n][0] * o[mtl][n][2]; *a11 = f_r[n][1] * o[mtl][n][3];
+              } else {
+                *a00 += f_r[n][0] * o[mtl][n][0]; *a10 += f_r[n][1] * o[mtl][n][1];
+                *a01 += f_r[n][0] * o[mtl][n][2]; *a11 += f_r[n][1] * o[mtl][n][3];
+              }
             }
           }
         }
@@ -780,7 +898,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
                  make_float2(M, Ls));
       }
     }
-    if (!direct) combine_tree<Cfg>(p, pc, T_total, it.C, merge_o, s_misc);
+    if (!direct) combine_tree<Cfg>(p, pc, it.cp, merge_o, s_misc);
     named_bar_sync(1, Cfg::kConsumerThreads);  // merge buffers free again
   }
   if (!ok && lane == 0) raise_error(p.error_flag, kErrTimeout);

@@ -95,7 +95,7 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
   const int ctas = sms * ks.ctas_per_sm;  // persistent grid: every resident CTA slot
   if (splits == 0) {
     pl->grid = ctas;
-    pl->slots = 2ll * ctas;
+    pl->slots = 2ll * ctas;  // a CTA's range holds at most two split pieces
   } else {
     const long long pieces = pl->units * splits;
     pl->grid = static_cast<int>(pieces < ctas ? (pieces > 0 ? pieces : 1) : ctas);

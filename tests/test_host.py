@@ -58,7 +58,8 @@ def test_workspace_and_grid_plans(lib):
     d = _dims()
     cnt = 4 * 16384 * 4  # fixed ticket header: 4 tree levels x 16384 tickets
     up = lambda x: (x + 255) // 256 * 256
-    # balanced: two persistent CTAs per SM, two partial slots per CTA, 8 padded rows of D floats
+    # balanced: two persistent CTAs per SM, two partial slots per CTA, 8 padded
+    # rows of D floats
     assert binding.grid_ctas(d, 1, 0, sm_count=152) == 304
     ws = binding.workspace_bytes(d, 1, 0, sm_count=152)
     assert ws == cnt + up(608 * 8 * 2 * 4) + 608 * 8 * 256 * 4

@@ -26,41 +26,62 @@ def seq_span(L, qlen, window, cap):
     return L, t0, (L - 1) // TILE - t0 + 1
 
 
-def pieces_for_cta(c, grid, B, Hkv, lens, qlen, window, cap, S):
+def chunk_plan(T, grid):
+    """The balanced mode's cut: Ce = min(grid, T) contiguous ranges of equal
+    size (to one tile), range k belonging to CTA k."""
+    return dict(T=T, Ce=min(T, grid) if T > 0 else 0)
+
+
+def chunk_start(cp, k):
+    return cp["T"] * k // cp["Ce"]
+
+
+def chunk_end(cp, k):
+    return cp["T"] * (k + 1) // cp["Ce"]
+
+
+def owner(cp, x):
+    return ((x + 1) * cp["Ce"] - 1) // cp["T"]
+
+
+def all_pieces(grid, B, Hkv, lens, qlen, window, cap, S, rng):
+    """Every CTA's pieces."""
     spans = [seq_span(L, qlen, window, cap) for L in lens]
-    out = []
+    per_cta = {c: [] for c in range(grid)}
     if S == 0:
         pre = [0]
         for _, _, n in spans:
             pre.append(pre[-1] + n * Hkv)
-        T = pre[B]
-        C = min(grid, T)
-        gb, ge = (T * c // C, T * (c + 1) // C) if c < C else (0, 0)
-        owner = lambda x: ((x + 1) * C - 1) // T
-        g = gb
-        b = max([i for i in range(B) if pre[i] <= g] or [0])
-        while g < ge:
-            while pre[b + 1] <= g:
-                b += 1
-            n = (pre[b + 1] - pre[b]) // Hkv
-            kh = (g - pre[b]) // n
-            us = pre[b] + kh * n
-            ue = us + n
-            pe = min(ue, ge)
-            L, t0, _ = spans[b]
-            npieces = owner(ue - 1) - owner(us) + 1
-            slot = 2 * c + (1 if gb < us else 0)
-            slots = [2 * cc + (1 if T * cc // C < us else 0) for cc in range(owner(us), owner(us) + npieces)]
-            out.append(dict(unit=b * Hkv + kh, tiles=list(range(t0 + g - us, t0 + pe - us)),
-                            npieces=npieces, slot=slot, all_slots=slots, ticket=owner(us)))
-            g = pe
-        for b in range(c, B, grid):
-            if pre[b + 1] == pre[b]:
-                for kh in range(Hkv):
-                    out.append(dict(unit=b * Hkv + kh, tiles=[], npieces=1, slot=None, all_slots=[]))
-        return out, 2 * grid
+        cp = chunk_plan(pre[B], grid)
+        for k in range(cp["Ce"]):
+            cta = k
+            g, ge = chunk_start(cp, k), chunk_end(cp, k)
+            while g < ge:
+                b = max(i for i in range(B) if pre[i] <= g)
+                n = (pre[b + 1] - pre[b]) // Hkv
+                kh = (g - pre[b]) // n
+                us = pre[b] + kh * n
+                ue = us + n
+                pe = min(ue, ge)
+                L, t0, _ = spans[b]
+                cf, cl = owner(cp, us), owner(cp, ue - 1)
+                npieces = cl - cf + 1
+                slots = [2 * cf + (1 if chunk_start(cp, cf) < us else 0)] + \
+                        [2 * (cf + q) for q in range(1, npieces)]
+                per_cta[cta].append(dict(unit=b * Hkv + kh, tiles=list(range(t0 + g - us, t0 + pe - us)),
+                                         npieces=npieces, slot=2 * k + (1 if chunk_start(cp, k) < us else 0),
+                                         all_slots=slots))
+                g = pe
+        for c in range(grid):
+            for b in range(c, B, grid):
+                if pre[b + 1] == pre[b]:
+                    for kh in range(Hkv):
+                        per_cta[c].append(dict(unit=b * Hkv + kh, tiles=[], npieces=1, slot=None,
+                                               all_slots=[]))
+        return per_cta, 2 * grid
     total = B * Hkv * S
-    for p in range(c, total, grid):
+    for p in range(total):
+        c = p % grid
         u, s = divmod(p, S)
         b, kh = divmod(u, Hkv)
         L, t0, n = spans[b]
@@ -68,23 +89,23 @@ def pieces_for_cta(c, grid, B, Hkv, lens, qlen, window, cap, S):
         c0, c1 = s * chunk, min(s * chunk + chunk, n)
         if n == 0:
             if s == 0:
-                out.append(dict(unit=u, tiles=[], npieces=1, slot=None, all_slots=[]))
+                per_cta[c].append(dict(unit=u, tiles=[], npieces=1, slot=None, all_slots=[]))
             continue
         if c0 >= c1:
             continue
         npieces = (n + chunk - 1) // chunk
-        out.append(dict(unit=u, tiles=list(range(t0 + c0, t0 + c1)), npieces=npieces, slot=u * S + s,
-                        all_slots=[u * S + k for k in range(npieces)], ticket=u))
-    return out, (B * Hkv * S if S > 1 else 0)
+        per_cta[c].append(dict(unit=u, tiles=list(range(t0 + c0, t0 + c1)), npieces=npieces,
+                               slot=u * S + s, all_slots=[u * S + k for k in range(npieces)]))
+    return per_cta, (B * Hkv * S if S > 1 else 0)
 
 
-def check(B, Hkv, lens, qlen, window, cap, S, grid):
+def check(B, Hkv, lens, qlen, window, cap, S, grid, seed=0):
     seen = {}
     slots_used = []
     units_pieces = {}
+    per_cta, nslots = all_pieces(grid, B, Hkv, lens, qlen, window, cap, S, random.Random(seed))
     for c in range(grid):
-        pcs, nslots = pieces_for_cta(c, grid, B, Hkv, lens, qlen, window, cap, S)
-        for pc in pcs:
+        for pc in per_cta[c]:
             u = pc["unit"]
             units_pieces.setdefault(u, []).append(pc)
             for t in pc["tiles"]:
@@ -157,4 +178,4 @@ def test_schedule_random():
         window = rng.choice([0, 0, rng.randint(1, 500)])
         S = rng.choice([0, 0, 1, 2, 5, 9])
         grid = rng.choice([1, 2, 5, 16, 152])
-        check(B, Hkv, lens, qlen, window, 1 << 20, S, grid)
+        check(B, Hkv, lens, qlen, window, 1 << 20, S, grid, seed=rng.randrange(1 << 30))

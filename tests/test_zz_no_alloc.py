@@ -73,13 +73,12 @@ def test_static_scratch_matches_decode_paged(lib):
 
 
 def test_static_scratch_rejects_plans_beyond_its_size(lib):
-    # 32 query rows per KV head at D=256 need 608 slots x 32 rows x 256 floats
-    # of partials on a 152-SM GPU: more than the 8 MiB scratch.
-    w = inputs.make_workload(B=2, Hq=8, Hkv=1, D=256, qlen=4, seq_lens=[600, 35], seed=32)
+    # a fixed split of 8 over 64 sequences x 8 KV heads needs 4096 partial slots
+    # of 8 rows x 256 floats (32 MiB) plus the ticket header: more than the scratch
+    w = inputs.make_workload(B=64, Hq=8, Hkv=8, D=256, qlen=1, seq_lens=[64] * 64, seed=32)
     t = _device(w)
-    need = binding.workspace_bytes(binding.dims_of(t[0], t[1], t[3], w.qlen), w.qlen, 0)
-    if need <= (8 << 20):
-        pytest.skip("this GPU's plan fits the scratch")
+    need = binding.workspace_bytes(binding.dims_of(t[0], t[1], t[3], w.qlen), w.qlen, 8)
+    assert need > (32 << 20)
     out = torch.empty_like(t[0])
     flag = torch.zeros(1, dtype=torch.int32, device=DEV)
-    assert _call_static(lib, w, t, 0, out, flag) == 6  # PD_ERR_WORKSPACE
+    assert _call_static(lib, w, t, 8, out, flag) == 6  # PD_ERR_WORKSPACE
