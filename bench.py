@@ -9,7 +9,8 @@ step is one decode_paged call over B=32 sequences; the batch sweep B in
 {1,2,3,8,32} is reported beside it.
 
 One step = one call of the whole path (page translation, KV gather, scores,
-masking, online softmax, P.V, split combine: one kernel launch). KV bytes are
+masking, online softmax, P.V in the decode kernel; the split combine in a
+second kernel launched behind it with programmatic dependent launch). KV bytes are
 the algorithmic K+V bytes of the visible keys. Cold L2: every step reads its
 KV through a different block table over a pool at least 4x the L2 size, so no
 step finds the previous step's KV in L2. The K timed steps are captured in a
@@ -572,7 +573,7 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_val, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * 2,  # decode kernel + split-combine kernel per step
             "clocks": clk,
             "sweep": sweep,
             "configs": configs,

@@ -97,12 +97,11 @@ typedef struct {
 /* Workspace bytes that decode_paged needs for these shapes, qlen and
  * num_splits (0 = balanced automatic split) on a device with sm_count SMs
  * (sm_count <= 0: the current device's). 0 means no workspace is needed (the
- * pointer may then be NULL). Layout: a fixed 64 KiB header of split tickets,
- * then the fp32 split partials. The header must be zero-filled once before the
- * buffer's first use; every call that completes leaves it zero again, whatever
- * the shapes of the call, so one buffer serves any sequence of calls on one
- * stream. Calls that may run at the same time must not share a workspace.
- * With num_splits > 1, B*Hkv may be at most 16384. Returns 0 for invalid dims. */
+ * pointer may then be NULL). Layout: one 16-byte split descriptor per CTA range
+ * (balanced) or per unit (fixed split), then the fp32 split partials. Every
+ * call writes what it later reads, so the buffer needs no initialisation and
+ * one buffer serves any sequence of calls on one stream; calls that may run
+ * at the same time must not share a workspace. Returns 0 for invalid dims. */
 PD_API size_t pd_workspace_bytes(const pd_dims* dims, int qlen, int num_splits, int sm_count);
 
 /* Number of CTAs decode_paged launches for these arguments (persistent grid),
@@ -110,6 +109,9 @@ PD_API size_t pd_workspace_bytes(const pd_dims* dims, int qlen, int num_splits, 
 PD_API int pd_grid_ctas(const pd_dims* dims, int qlen, int num_splits, int sm_count);
 
 /* Paged decode attention, split-K over keys, GQA heads packed per CTA.
+ * With a split (num_splits != 1) the call is two launches on `stream`: the
+ * decode kernel, then a split-combine kernel launched with programmatic
+ * dependent launch that merges the partials of units cut into pieces.
  *
  *   q            fp16 [B*qlen, Hq, D]; row b*qlen + i is query token i of sequence b
  *   k_cache      [num_blocks, block_size, Hkv, D] fp16 or e4m3fn (dims->kv_dtype)
@@ -126,8 +128,8 @@ PD_API int pd_grid_ctas(const pd_dims* dims, int qlen, int num_splits, int sm_co
  *                contiguous chunks (1 = no split)
  *   out          fp16 [B*qlen, Hq, D], written in full (rows without a visible
  *                key are zeros); must not overlap the inputs
- *   workspace    device buffer of >= pd_workspace_bytes(...) bytes, zero-filled
- *                before its first use (see pd_workspace_bytes)
+ *   workspace    device buffer of >= pd_workspace_bytes(...) bytes (contents need
+ *                no initialisation; see pd_workspace_bytes)
  *   error_flag   device uint32 or NULL (see PD_DEVERR_*)
  *   stream       cudaStream_t to launch on
  * All pointers must be 16-byte aligned. */
@@ -167,8 +169,7 @@ PD_API pd_status decode_paged_combine(const float* part_m, const float* part_l, 
  *     out and error_flag.
  *   - Calls whose workspace (pd_workspace_bytes) exceeds
  *     PD_STATIC_SCRATCH_BYTES return PD_ERR_WORKSPACE before anything runs.
- *   - Each call first clears the scratch's split tickets on `stream`
- *     (cudaMemsetAsync), then launches as decode_paged does.
+ *   - Each call launches exactly as decode_paged does, on `stream`.
  *   - The first call on a device looks up the scratch's device address on
  *     that device (cudaGetSymbolAddress, the device being current); make
  *     that first call before any stream capture.

@@ -107,17 +107,17 @@ _workspaces: dict = {}
 
 
 def get_workspace(device: torch.device, nbytes: int) -> torch.Tensor | None:
-    """A zero-filled, reusable workspace per device, grown on demand.
+    """A reusable workspace per device, grown on demand.
 
-    The kernels leave it zero-filled after every completed call, so one buffer
-    serves every call made on one stream. Pass your own buffer to
-    decode_paged for calls that may overlap on different streams."""
+    Every call writes what it reads, so one buffer serves every call made on
+    one stream. Pass your own buffer to decode_paged for calls that may
+    overlap on different streams."""
     if nbytes == 0:
         return None
     key = (device.type, device.index)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        ws = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
 

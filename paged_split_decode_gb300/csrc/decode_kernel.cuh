@@ -42,11 +42,9 @@ namespace pd {
 
 constexpr int kTileKeys = 16;      // keys per pipeline tile
 constexpr int kMaxAutoB = 1024;    // sequences handled by the balanced split
-// The workspace opens with a fixed header of split tickets that every call
-// layout shares and leaves at zero; partials follow it and never overlap it.
-constexpr int kTickets = 16384;        // tickets per tree level
-constexpr int kTicketLevels = 4;       // fan-out 8: up to 8^4 = 4096 pieces per unit
-constexpr size_t kTicketHeaderBytes = static_cast<size_t>(kTickets) * kTicketLevels * sizeof(int);
+// Split units are merged by a second kernel: the workspace opens with one
+// descriptor per entry (balanced mode: per CTA range, fixed mode: per unit)
+// naming the split unit whose first piece it holds, then the partials.
 constexpr uint32_t kErrBlockId = 1u, kErrSeqLen = 2u, kErrTimeout = 4u;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -57,7 +55,9 @@ struct DecodeParams {
   const int32_t* seq_lens;    // [B]
   float* ws_o;                // [slots, RP, D]   partial O (log2-domain weights)
   float* ws_ml;               // [slots, RP, 2]   partial (m, l), m in log2 units
-  int* ws_count;              // [kTicketLevels][kTickets] split tickets (zero between calls)
+  int4* ws_desc;              // [n_desc] {unit, pieces, slot of piece 0, slot base} or unit -1
+  int n_desc;
+  int rows_padded;            // RP: rows per partial slot
   uint32_t* error_flag;       // may be null
   int B, qlen, Hq, Hkv, G, R;
   int max_blocks, block_size, num_blocks, tiles_per_block;
@@ -292,127 +292,6 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
   return false;
 }
 
-// ---------------------------------------------------------------------------
-// Split combine as a tree of fan-out 8 over a unit's P pieces (key order).
-// Node (level l, index j) covers pieces [j*8^l, (j+1)*8^l); its partial lives
-// in the workspace slot of its first piece (written in place over its first
-// child once the children are read), and level l's tickets are the l-th
-// array of the ticket header, indexed by that slot. Each piece publishes its
-// partial and bumps its parent's ticket; the last child to arrive merges the
-// children (running max over m, weights exp2(m_c - M)) and moves one level up,
-// until the root writes the output row. Children are merged in key order, so
-// the result does not depend on arrival order.
-template <class Cfg>
-__device__ __forceinline__ void combine_tree(const DecodeParams& p, const Piece& pc, const ChunkPlan& cp,
-                                             float* scratch, int* s_misc) {
-  constexpr int D = Cfg::D, RP = Cfg::RP, NTH = Cfg::kConsumerThreads;
-  const int tid = threadIdx.x;
-  const int R = p.R, P = pc.npieces;
-  int s_first, s_base, s_step, k_me;
-  if (p.num_splits == 0) {
-    const int cf = pc.first_slot_cta;
-    s_first = 2 * cf + (cp.start(cf) < pc.unit_start ? 1 : 0);
-    s_base = 2 * cf;
-    s_step = 2;
-    k_me = pc.chunk - cf;
-  } else {
-    s_first = s_base = pc.unit * p.num_splits;
-    s_step = 1;
-    k_me = pc.slot - s_first;
-  }
-  auto slot_of = [&](int k) -> long long { return k == 0 ? s_first : s_base + s_step * k; };
-  int level = 0, j = k_me, span = 1;
-  while (true) {
-    const int n_level = (P + span - 1) / span;
-    const int parent = j >> 3;
-    const int nchild = min(8, n_level - 8 * parent);
-    const int span_up = span * 8;
-    const bool root = span_up >= P;
-    const long long s_parent = slot_of(parent * span_up);
-    // publish: every thread's partial stores are ordered before the ticket by
-    // the barrier and thread 0's gpu-scope fence
-    named_bar_sync(1, NTH);
-    if (tid == 0) {
-      __threadfence();
-      int* t = p.ws_count + level * kTickets + s_parent;
-      const int prev = atomicAdd(t, 1);
-      const int last = prev == nchild - 1;
-      if (last) {
-        *t = 0;
-        __threadfence();
-      }
-      s_misc[0] = last;
-    }
-    named_bar_sync(1, NTH);
-    if (!s_misc[0]) break;
-    // merge the children, three 4-dim items per thread per pass; each item
-    // loads its row's (m, l) and its O slice of every child in one go
-    constexpr int DQ = D / 4, NI = (Cfg::NT >= 4) ? 1 : 3;  // fewer in flight under the 2-CTA register cap
-    const int items = R * DQ;
-    for (int base = tid; base < items; base += NI * NTH) {
-      float2 ml[NI][8];
-      float4 v[NI][8];
-#pragma unroll
-      for (int u = 0; u < NI; ++u) {
-        const int item = base + u * NTH;
-        const int r = item / DQ, dq = item % DQ;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          if (item < items && c < nchild) {
-            const long long sl = slot_of((8 * parent + c) * span);
-            ml[u][c] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (sl * RP + r) * 2));
-            v[u][c] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sl * RP + r) * D + dq * 4));
-          } else {
-            ml[u][c] = make_float2(-INFINITY, 0.f);
-            v[u][c] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < NI; ++u) {
-        const int item = base + u * NTH;
-        if (item >= items) continue;
-        const int r = item / DQ, dq = item % DQ;
-        float M = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) M = fmaxf(M, ml[u][c].x);
-        float L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float w = (ml[u][c].x == -INFINITY) ? 0.f : ex2(ml[u][c].x - M);
-          L += w * ml[u][c].y;
-          acc.x += w * v[u][c].x; acc.y += w * v[u][c].y;
-          acc.z += w * v[u][c].z; acc.w += w * v[u][c].w;
-        }
-        if (root) {
-          const float inv = (L > 0.f) ? p.out_scale / L : 0.f;
-          const int i = r / p.G, hl = r % p.G;
-          __half* dst = p.out + (static_cast<long long>(pc.b * p.qlen + i) * p.Hq + pc.kh * p.G + hl) * D + dq * 4;
-          uint2 o2;
-          o2.x = pack_half2(acc.x * inv, acc.y * inv);
-          o2.y = pack_half2(acc.z * inv, acc.w * inv);
-          *reinterpret_cast<uint2*>(dst) = o2;
-        } else {
-          // in place over the first child: every thread reads its own items
-          // before writing them, and the (m, l) of the row is written after
-          // the barrier below, once all threads have read it
-          __stcg(reinterpret_cast<float4*>(p.ws_o + (s_parent * RP + r) * D + dq * 4), acc);
-          if (dq == 0) scratch[r] = M, scratch[RP + r] = L;
-        }
-      }
-    }
-    if (root) break;
-    named_bar_sync(1, NTH);
-    for (int r = tid; r < R; r += NTH)
-      __stcg(reinterpret_cast<float2*>(p.ws_ml + (s_parent * RP + r) * 2),
-             make_float2(scratch[r], scratch[RP + r]));
-    ++level;
-    j = parent;
-    span = span_up;
-  }
-}
-
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
     decode_paged_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -426,7 +305,6 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
   float* merge_ml = reinterpret_cast<float*>(smem + Cfg::kOffMergeML);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBars);  // full[NS], empty[NS]
   int* s_pre = reinterpret_cast<int*>(smem + Cfg::kOffPre);
-  int* s_misc = reinterpret_cast<int*>(smem + Cfg::kOffMisc);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool is_producer = warp == Cfg::kConsumerWarps;
@@ -468,6 +346,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
 
   WorkIter it;
   work_init(p, s_pre, it);
+  // the split-combine kernel may be scheduled now; it waits for this grid
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0 && p.num_splits == 0 && blockIdx.x < p.n_desc)
+    p.ws_desc[blockIdx.x] = make_int4(-1, 0, 0, 0);  // no split unit starts here (yet)
   Piece pc;
 
   if (is_producer) {
@@ -898,10 +780,112 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
                  make_float2(M, Ls));
       }
     }
-    if (!direct) combine_tree<Cfg>(p, pc, it.cp, merge_o, s_misc);
+    if (tid == 0 && p.n_desc > 0) {
+      // the first piece of a unit posts its descriptor for the split combine
+      // (no descriptors -- and no workspace -- without a split)
+      const bool first = p.num_splits == 0 ? (pc.npieces > 1 && pc.chunk == pc.first_slot_cta)
+                                            : (pc.chunk == 0);
+      if (first) {
+        int4 d = make_int4(-1, 0, 0, 0);
+        if (pc.npieces > 1) {
+          d.x = pc.unit;
+          d.y = pc.npieces;
+          d.z = pc.slot;
+          d.w = p.num_splits == 0 ? 2 * pc.first_slot_cta : pc.slot;
+        }
+        p.ws_desc[p.num_splits == 0 ? pc.chunk : pc.unit] = d;
+      }
+    }
     named_bar_sync(1, Cfg::kConsumerThreads);  // merge buffers free again
   }
   if (!ok && lane == 0) raise_error(p.error_flag, kErrTimeout);
+}
+
+// ---------------------------------------------------------------------------
+// Split combine: merges the fp32 (m, l, O) partials of every unit the decode
+// kernel split into pieces (m in log2 units, O relative to m). Launched after
+// the decode kernel with programmatic dependent launch: its CTAs may start
+// while the decode grid drains and wait in griddepcontrol.wait until that grid
+// has completed and its writes are visible.
+//   grid (n_desc, D/32), 256 threads: CTA (e, c) merges descriptor e's unit
+//   for output dims [32c, 32c+32). Thread t covers item t % items (row r,
+//   4-dim slice) for pieces pg, pg+PG, ... (pg = t / items, PG = 256 / items)
+//   with a running max; the PG partial states are then merged in pg order, so
+//   the result does not depend on scheduling.
+template <int D>
+__global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ float s_m[256], s_l[256];
+  __shared__ float4 s_o[256];
+  const int4 d = __ldcg(p.ws_desc + blockIdx.x);
+  const int u = d.x, P = d.y;
+  if (u < 0 || P <= 1) return;
+  const int step = p.num_splits == 0 ? 2 : 1;
+  const int R = p.R, RP = p.rows_padded;
+  const int items = R * 8;
+  const int PG = 256 / items > 0 ? 256 / items : 1;
+  const int t = threadIdx.x;
+  const int item = t % items, pg = t / items;
+  const int r = item >> 3, dim0 = blockIdx.y * 32 + (item & 7) * 4;
+  float m_run = -INFINITY, l_run = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (pg < PG) {
+    for (int k0 = pg; k0 < P; k0 += 4 * PG) {
+      float2 ml[4];
+      float4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int k = k0 + j * PG;
+        if (k < P) {
+          const long long sl = k == 0 ? d.z : d.w + static_cast<long long>(step) * k;
+          ml[j] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (sl * RP + r) * 2));
+          v[j] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sl * RP + r) * D + dim0));
+        } else {
+          ml[j] = make_float2(-INFINITY, 0.f);
+          v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float mk = ml[j].x;
+        if (mk == -INFINITY) continue;
+        if (mk > m_run) {
+          const float sc = (m_run == -INFINITY) ? 0.f : ex2(m_run - mk);
+          l_run *= sc;
+          acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+          m_run = mk;
+        }
+        const float w = ex2(mk - m_run);
+        l_run += w * ml[j].y;
+        acc.x += w * v[j].x; acc.y += w * v[j].y; acc.z += w * v[j].z; acc.w += w * v[j].w;
+      }
+    }
+  }
+  s_m[t] = m_run;
+  s_l[t] = l_run;
+  s_o[t] = acc;
+  __syncthreads();
+  if (pg != 0 || t >= items) return;
+  float M = -INFINITY;
+  for (int g2 = 0; g2 < PG; ++g2) M = fmaxf(M, s_m[g2 * items + item]);
+  float L = 0.f;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int g2 = 0; g2 < PG; ++g2) {
+    const float mg = s_m[g2 * items + item];
+    if (mg == -INFINITY) continue;
+    const float w = ex2(mg - M);
+    L += w * s_l[g2 * items + item];
+    const float4 a = s_o[g2 * items + item];
+    o.x += w * a.x; o.y += w * a.y; o.z += w * a.z; o.w += w * a.w;
+  }
+  const float inv = (L > 0.f) ? p.out_scale / L : 0.f;
+  const int b = u / p.Hkv, kh = u % p.Hkv;
+  const int i = r / p.G, hl = r % p.G;
+  __half* dst = p.out + (static_cast<long long>(b * p.qlen + i) * p.Hq + kh * p.G + hl) * D + dim0;
+  uint2 o2;
+  o2.x = pack_half2(o.x * inv, o.y * inv);
+  o2.y = pack_half2(o.z * inv, o.w * inv);
+  *reinterpret_cast<uint2*>(dst) = o2;
 }
 
 }  // namespace pd

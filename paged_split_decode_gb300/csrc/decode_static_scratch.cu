@@ -12,7 +12,6 @@
 #include <cstdint>
 #include <mutex>
 
-#include "decode_kernel.cuh"
 #include "pdecode.h"
 
 namespace {
@@ -61,15 +60,7 @@ extern "C" pd_status decode_paged_static_scratch(const void* q, const void* k_ca
   const size_t need = pd_workspace_bytes(dims, qlen, num_splits, 0);
   if (need > kStaticScratchBytes) return PD_ERR_WORKSPACE;
   void* scratch = nullptr;
-  if (need > 0) {
-    if (scratch_address(&scratch) != cudaSuccess) return PD_ERR_CUDA;
-    // The split tickets at the front of the scratch must start at zero. A
-    // completed call leaves them at zero; clearing them on every call also
-    // covers a call that gave up part-way.
-    if (cudaMemsetAsync(scratch, 0, pd::kTicketHeaderBytes, static_cast<cudaStream_t>(stream)) !=
-        cudaSuccess)
-      return PD_ERR_CUDA;
-  }
+  if (need > 0 && scratch_address(&scratch) != cudaSuccess) return PD_ERR_CUDA;
   return decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale, window, qlen, num_splits,
                       out, dims, scratch, scratch ? kStaticScratchBytes : 0, error_flag, stream);
 }

@@ -23,6 +23,9 @@ bool kernel_shape(int D, bool fp8, int nt, KernelShape* out);
 cudaError_t launch_decode(int D, bool fp8, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
                           const DecodeParams& p, int grid, cudaStream_t stream);
 
+// Split combine behind a decode launch (split_combine.cu).
+cudaError_t launch_split_combine(int D, const DecodeParams& p, int n_desc, cudaStream_t stream);
+
 // Per-dtype/head-size entry points defined in decode_*.cu.
 bool shape_f16_d128(int nt, KernelShape* out);
 bool shape_f16_d256(int nt, KernelShape* out);

@@ -36,6 +36,7 @@ struct Plan {
   int grid;         // CTAs launched
   int nt;           // row tiles
   long long slots;  // partial slots in the workspace
+  long long n_desc; // split-combine descriptors
   long long units;  // B * Hkv tickets
   int rows_padded;
   size_t off_ml, off_o, bytes;  // workspace layout
@@ -90,22 +91,23 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
   pl->units = static_cast<long long>(d->B) * d->Hkv;
   int splits = num_splits;
   if (splits == 0 && d->B > kMaxAutoB) splits = 1;  // plenty of units: one piece each
-  if (splits > 1 && (pl->units * splits > kTickets || splits > 4096)) return PD_ERR_UNSUPPORTED;
   pl->splits = splits;
   const int ctas = sms * ks.ctas_per_sm;  // persistent grid: every resident CTA slot
   if (splits == 0) {
     pl->grid = ctas;
     pl->slots = 2ll * ctas;  // a CTA's range holds at most two split pieces
+    pl->n_desc = ctas;       // at most one split unit starts in a CTA's range
   } else {
     const long long pieces = pl->units * splits;
     pl->grid = static_cast<int>(pieces < ctas ? (pieces > 0 ? pieces : 1) : ctas);
     pl->slots = splits > 1 ? pieces : 0;
+    pl->n_desc = splits > 1 ? pl->units : 0;
   }
   if (pl->slots == 0) {
     pl->off_ml = pl->off_o = pl->bytes = 0;
   } else {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-    const size_t cnt = kTicketHeaderBytes;
+    const size_t cnt = up(static_cast<size_t>(pl->n_desc) * 16);
     const size_t ml = up(static_cast<size_t>(pl->slots) * pl->rows_padded * 2 * 4);
     const size_t o = static_cast<size_t>(pl->slots) * pl->rows_padded * d->D * 4;
     pl->off_ml = cnt;
@@ -216,7 +218,9 @@ pd_status decode_paged(const void* q, const void* k_cache, const void* v_cache,
   p.block_table = block_table;
   p.seq_lens = seq_lens;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.ws_count = pl.bytes ? reinterpret_cast<int*>(ws) : nullptr;
+  p.ws_desc = pl.bytes ? reinterpret_cast<int4*>(ws) : nullptr;
+  p.n_desc = static_cast<int>(pl.n_desc);
+  p.rows_padded = pl.rows_padded;
   p.ws_ml = pl.bytes ? reinterpret_cast<float*>(ws + pl.off_ml) : nullptr;
   p.ws_o = pl.bytes ? reinterpret_cast<float*>(ws + pl.off_o) : nullptr;
   p.error_flag = error_flag;
@@ -239,6 +243,8 @@ pd_status decode_paged(const void* q, const void* k_cache, const void* v_cache,
 
   cudaError_t e = launch_decode(dims->D, fp8, pl.nt, tk, tv, p, pl.grid,
                                 static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess && pl.n_desc > 0)
+    e = launch_split_combine(dims->D, p, static_cast<int>(pl.n_desc), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PD_OK : PD_ERR_CUDA;
 }
 

@@ -1,0 +1,28 @@
+// split_combine.cu -- launches the split-combine kernel of the balanced and
+// fixed split modes right behind the decode kernel, with programmatic
+// dependent launch so that its CTAs are scheduled while the decode grid drains.
+#include "launch.h"
+
+namespace pd {
+
+cudaError_t launch_split_combine(int D, const DecodeParams& p, int n_desc, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(n_desc), static_cast<unsigned>(D / 32), 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (D == 128)
+    e = cudaLaunchKernelEx(&cfg, split_combine_kernel<128>, p);
+  else
+    e = cudaLaunchKernelEx(&cfg, split_combine_kernel<256>, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace pd

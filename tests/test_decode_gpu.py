@@ -138,10 +138,10 @@ def test_edge_cases(pd, name, kw, S):
 
 
 def test_one_workspace_across_changing_shapes(pd):
-    """One workspace buffer serves calls of different shapes back to back: the
-    split tickets sit in a fixed header that every call leaves at zero."""
+    """One workspace buffer serves calls of different shapes back to back: every
+    call writes the descriptors and partials it reads."""
     import paged_split_decode_gb300 as P
-    ws = torch.zeros(64 << 20, dtype=torch.uint8, device=DEV)
+    ws = torch.full((64 << 20,), 0xA5, dtype=torch.uint8, device=DEV)  # garbage start
     ws_list = [inputs.make_workload(B=2, Hq=8, Hkv=8, D=128, seq_lens=[5000, 16384], seed=21),
                inputs.make_workload(B=32, Hq=32, Hkv=8, D=128, seq_lens=[4096] * 32, seed=22),
                inputs.make_workload(B=3, Hq=24, Hkv=4, D=256, seq_lens=[9000, 1, 700], seed=23,
@@ -152,8 +152,6 @@ def test_one_workspace_across_changing_shapes(pd):
         for w, r in zip(ws_list, refs):
             for S in (0, 3):
                 check(w, gpu_run(pd, w, S, workspace=ws), r)
-    hdr = ws[:16384 * 4].view(torch.int32)
-    assert int(torch.count_nonzero(hdr).item()) == 0
 
 
 @pytest.mark.parametrize("S", [0, 9, 64, 100, 500])

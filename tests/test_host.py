@@ -56,24 +56,22 @@ def _dims(**kw):
 
 def test_workspace_and_grid_plans(lib):
     d = _dims()
-    cnt = 4 * 16384 * 4  # fixed ticket header: 4 tree levels x 16384 tickets
     up = lambda x: (x + 255) // 256 * 256
-    # balanced: two persistent CTAs per SM, two partial slots per CTA, 8 padded
-    # rows of D floats
+    # balanced: two persistent CTAs per SM; one 16-byte split descriptor per CTA,
+    # two partial slots per CTA, 8 padded rows of D floats
     assert binding.grid_ctas(d, 1, 0, sm_count=152) == 304
     ws = binding.workspace_bytes(d, 1, 0, sm_count=152)
-    assert ws == cnt + up(608 * 8 * 2 * 4) + 608 * 8 * 256 * 4
+    assert ws == up(304 * 16) + up(608 * 8 * 2 * 4) + 608 * 8 * 256 * 4
     # no split: no workspace at all; one CTA per unit up to the resident CTA count
     assert binding.workspace_bytes(d, 1, 1, sm_count=152) == 0
     assert binding.grid_ctas(d, 1, 1, sm_count=152) == 128
-    # fixed split: B*Hkv*S slots
-    assert binding.workspace_bytes(d, 1, 3, sm_count=152) == cnt + up(384 * 8 * 2 * 4) + 384 * 8 * 256 * 4
+    # fixed split: one descriptor per unit, B*Hkv*S slots
+    assert binding.workspace_bytes(d, 1, 3, sm_count=152) == \
+        up(128 * 16) + up(384 * 8 * 2 * 4) + 384 * 8 * 256 * 4
     assert binding.grid_ctas(d, 1, 3, sm_count=152) == 304
     # qlen 3 x G 6 = 18 rows -> three row tiles of 8
     ws3 = binding.workspace_bytes(_dims(B=8), 3, 0, sm_count=152)
-    assert ws3 == cnt + up(608 * 24 * 2 * 4) + 608 * 24 * 256 * 4
-    # fixed split with more than 16384 units is not supported (ticket header size)
-    assert binding.workspace_bytes(_dims(B=5000, Hkv=4, Hq=8), 1, 2, sm_count=152) == 0
+    assert ws3 == up(304 * 16) + up(608 * 24 * 2 * 4) + 608 * 24 * 256 * 4
 
 
 @pytest.mark.parametrize("kw,qlen", [

@@ -115,24 +115,15 @@ def check(B, Hkv, lens, qlen, window, cap, S, grid, seed=0):
                 assert 0 <= pc["slot"] < nslots
                 slots_used.append(pc["slot"])
     assert len(slots_used) == len(set(slots_used)), "two pieces share a slot"
-    # tree combine (fan-out 8): node (l, j) of a unit is ticketed at level l by the
-    # slot of its first piece; tickets of one level must never be shared
-    tickets = {}
+    # the first piece of every split unit posts the unit's descriptor: one per
+    # CTA range (balanced) or per unit (fixed); no two split units share one
+    posts = {}
     for u, pcs in units_pieces.items():
-        P = pcs[0]["npieces"]
-        if P <= 1:
-            continue
-        order = pcs[0]["all_slots"]
-        span, level = 1, 0
-        while span < P:
-            n_up = -(-P // (span * 8))
-            for j in range(n_up):
-                t = order[j * span * 8]
-                assert 0 <= t < 16384
-                assert tickets.setdefault((level, t), u) == u, "two tree nodes share a ticket"
-            span *= 8
-            level += 1
-        assert level <= 4
+        if pcs[0]["npieces"] > 1:
+            firsts = [pc for pc in pcs if pc["slot"] == pcs[0]["all_slots"][0]]
+            assert len(firsts) == 1, "a split unit needs exactly one first piece"
+            entry = firsts[0]["slot"] // 2 if S == 0 else u
+            assert posts.setdefault(entry, u) == u, "two split units share a descriptor"
     for b, L in enumerate(lens):
         _, t0, n = seq_span(L, qlen, window, cap)
         for kh in range(Hkv):
