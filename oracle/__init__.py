@@ -42,7 +42,7 @@ class Dims(ctypes.Structure):
         ("B", ctypes.c_int), ("qlen", ctypes.c_int), ("Hq", ctypes.c_int),
         ("Hkv", ctypes.c_int), ("D", ctypes.c_int), ("block_size", ctypes.c_int),
         ("num_blocks", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int),
-        ("kv_fp8", ctypes.c_int), ("k_scale", ctypes.c_double), ("v_scale", ctypes.c_double),
+        ("kv_kind", ctypes.c_int), ("k_scale", ctypes.c_double), ("v_scale", ctypes.c_double),
     ]
 
 
@@ -72,6 +72,8 @@ def _load():
         lib.pdo_f16_to_f64.restype = ctypes.c_double
         lib.pdo_e4m3fn_to_f64.argtypes = [ctypes.c_uint8]
         lib.pdo_e4m3fn_to_f64.restype = ctypes.c_double
+        lib.pdo_i8_to_f64.argtypes = [ctypes.c_uint8]
+        lib.pdo_i8_to_f64.restype = ctypes.c_double
         lib.pdo_decode_paged.argtypes = [ctypes.POINTER(Dims), P, P, P, P, P, ctypes.c_double,
                                          ctypes.c_int, ctypes.c_long, ctypes.c_long, P]
         lib.pdo_decode_paged.restype = ctypes.c_int
@@ -91,6 +93,10 @@ def f16_to_f64(bits: int) -> float:
 
 def e4m3fn_to_f64(code: int) -> float:
     return _load().pdo_e4m3fn_to_f64(code)
+
+
+def i8_to_f64(code: int) -> float:
+    return _load().pdo_i8_to_f64(code)
 
 
 def default_threads() -> int:
@@ -113,9 +119,10 @@ def _as_bits(a, dtype):
     return a
 
 
-def _prepare(q, k_cache, v_cache, block_table, seq_lens, qlen, k_scale, v_scale, kv_fp8):
+def _prepare(q, k_cache, v_cache, block_table, seq_lens, qlen, k_scale, v_scale, kv_fp8,
+             kv_int8=False):
     q = _as_bits(q, np.uint16)
-    kdt = np.uint8 if kv_fp8 else np.uint16
+    kdt = np.uint8 if (kv_fp8 or kv_int8) else np.uint16
     k = _as_bits(k_cache, kdt)
     v = _as_bits(v_cache, kdt)
     bt = np.ascontiguousarray(block_table, dtype=np.int32)
@@ -126,7 +133,7 @@ def _prepare(q, k_cache, v_cache, block_table, seq_lens, qlen, k_scale, v_scale,
     assert bt.ndim == 2 and bt.shape[0] == B
     assert q.shape[0] == B * qlen and q.shape[2] == D
     Hq = q.shape[1]
-    dims = Dims(B, qlen, Hq, Hkv, D, bs, num_blocks, bt.shape[1], int(bool(kv_fp8)),
+    dims = Dims(B, qlen, Hq, Hkv, D, bs, num_blocks, bt.shape[1], 2 if kv_int8 else int(bool(kv_fp8)),
                 float(k_scale), float(v_scale))
     return dims, q, k, v, bt, sl
 
@@ -145,17 +152,18 @@ def _run_rows(n_rows, threads, fn):
 
 
 def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, qlen=1,
-                 k_scale=1.0, v_scale=1.0, kv_fp8=False, threads=None, rows=None):
+                 k_scale=1.0, v_scale=1.0, kv_fp8=False, threads=None, rows=None, kv_int8=False):
     """One-shot fp64 paged decode. Returns float64 [B*qlen, Hq, D].
 
     q: fp16 [B*qlen, Hq, D]; caches: fp16 (or uint8 e4m3fn codes with
-    kv_fp8=True) [num_blocks, block_size, Hkv, D]; block_table int32
+    kv_fp8=True, or int8 codes as uint8 with kv_int8=True)
+    [num_blocks, block_size, Hkv, D]; block_table int32
     [B, max_blocks]; seq_lens int32 [B]. ``rows`` = (begin, end) restricts the
     computed output rows (flattened (token, head) index); the others stay 0.
     """
     lib = _load()
     dims, q, k, v, bt, sl = _prepare(q, k_cache, v_cache, block_table, seq_lens, qlen,
-                                     k_scale, v_scale, kv_fp8)
+                                     k_scale, v_scale, kv_fp8, kv_int8)
     out = np.zeros((q.shape[0], q.shape[1], q.shape[2]), dtype=np.float64)
     r0, r1 = rows if rows is not None else (0, q.shape[0] * q.shape[1])
     fn = lambda a, b: lib.pdo_decode_paged(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(bt),
@@ -167,14 +175,14 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, ql
 
 def decode_paged_split(q, k_cache, v_cache, block_table, seq_lens, scale, num_splits, window=0,
                        qlen=1, k_scale=1.0, v_scale=1.0, kv_fp8=False, threads=None,
-                       return_partials=False):
+                       return_partials=False, kv_int8=False):
     """Split-mode fp64 paged decode (chunks + online softmax + combine).
 
     Returns out, or (out, m, l, O) with m/l [rows, S] and O [rows, S, D] when
     ``return_partials`` (rows = B*qlen*Hq, m in natural-log units)."""
     lib = _load()
     dims, q, k, v, bt, sl = _prepare(q, k_cache, v_cache, block_table, seq_lens, qlen,
-                                     k_scale, v_scale, kv_fp8)
+                                     k_scale, v_scale, kv_fp8, kv_int8)
     S = int(num_splits)
     n_rows = q.shape[0] * q.shape[1]
     D = q.shape[2]
@@ -204,7 +212,7 @@ def combine(m, l, O):
 
 
 __all__ = ["build", "decode_paged", "decode_paged_split", "combine", "f16_to_f64",
-           "e4m3fn_to_f64", "default_threads"]
+           "e4m3fn_to_f64", "i8_to_f64", "default_threads"]
 
 if __name__ == "__main__":  # pragma: no cover
     print(build(force="--force" in sys.argv))

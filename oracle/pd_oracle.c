@@ -29,7 +29,9 @@
  *   - Q and out are [B*qlen, Hq, D] with row b*qlen + i; the caches are
  *     [num_blocks, block_size, Hkv, D]; block_table is [B, max_blocks_per_seq];
  *   - fp8 KV holds OCP e4m3fn codes with one fp32 scale per cache: the value of
- *     a code c is decode(c) * k_scale (or v_scale);
+ *     a code c is decode(c) * k_scale (or v_scale); int8 KV holds signed
+ *     two's-complement codes with the same per-cache scales ("Purpose": the
+ *     fp8 and int8 decode wrappers share the body);
  *   - a row with no visible key is all zeros.
  *
  * Every value is converted to fp64 exactly and all arithmetic is fp64, in
@@ -49,8 +51,8 @@
 typedef struct {
   int B, qlen, Hq, Hkv, D;
   int block_size, num_blocks, max_blocks_per_seq;
-  int kv_fp8;       /* 0: caches hold IEEE binary16 bit patterns; 1: e4m3fn bytes */
-  double k_scale;   /* fp8 only: value = decode(code) * k_scale */
+  int kv_kind;      /* 0: IEEE binary16 bit patterns; 1: e4m3fn bytes; 2: int8 codes */
+  double k_scale;   /* fp8 / int8: value = decode(code) * k_scale */
   double v_scale;
 } pdo_dims;
 
@@ -85,11 +87,15 @@ double pdo_e4m3fn_to_f64(uint8_t c) {
   return sign ? -v : v;
 }
 
+/* Signed 8-bit two's-complement code. */
+double pdo_i8_to_f64(uint8_t c) { return (double)(int8_t)c; }
+
 /* Value of element x of (block, slot, kv head) in a K or V cache. */
 static double cache_at(const pdo_dims* d, const void* cache, double fp8_scale, long blk,
                        int slot, int kh, int x) {
   long idx = ((blk * d->block_size + slot) * (long)d->Hkv + kh) * d->D + x;
-  if (d->kv_fp8) return pdo_e4m3fn_to_f64(((const uint8_t*)cache)[idx]) * fp8_scale;
+  if (d->kv_kind == 1) return pdo_e4m3fn_to_f64(((const uint8_t*)cache)[idx]) * fp8_scale;
+  if (d->kv_kind == 2) return pdo_i8_to_f64(((const uint8_t*)cache)[idx]) * fp8_scale;
   return pdo_f16_to_f64(((const uint16_t*)cache)[idx]);
 }
 

@@ -13,6 +13,8 @@ request #33, "Test Plan" step 3, and the geometry of its results comment):
   ``amax / 448`` (448 is the largest finite e4m3fn value), clamped to
   [-448, 448] and rounded to e4m3fn by torch's CPU cast; the cache holds the
   code bytes and the scale is returned beside it.
+* int8 KV: the same draw divided by ``amax / 127``, rounded half to even,
+  clamped to [-127, 127]; the cache holds the two's-complement code bytes.
 * Block tables: ``permuted`` draws a random permutation of the physical block
   pool and hands each sequence a slice of it; ``dense`` gives sequence b the
   contiguous run of blocks after sequence b-1's. Table entries past a
@@ -44,6 +46,7 @@ class Workload:
     qlen: int = 1
     num_splits: int = 0
     kv_fp8: bool = False
+    kv_int8: bool = False
     k_scale: float = 1.0
     v_scale: float = 1.0
     meta: dict = field(default_factory=dict)
@@ -77,6 +80,13 @@ def _fp8_quantise(x: torch.Tensor):
     amax = float(x.abs().max()) if x.numel() else 1.0
     scale = torch.tensor(amax / E4M3_MAX if amax > 0 else 1.0, dtype=torch.float32)
     codes = (x / scale).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, float(scale)
+
+
+def _int8_quantise(x: torch.Tensor):
+    amax = float(x.abs().max()) if x.numel() else 1.0
+    scale = torch.tensor(amax / 127.0 if amax > 0 else 1.0, dtype=torch.float32)
+    codes = torch.round(x / scale).clamp(-127, 127).to(torch.int8).view(torch.uint8)
     return codes, float(scale)
 
 
@@ -119,20 +129,25 @@ def make_workload(*, B, Hq, Hkv, D, seq_lens, qlen=1, block_size=BLOCK_SIZE, lay
     q = _normal(gen, (B * qlen, Hq, D)).to(torch.float16)
     kf = _normal(gen, (pool, block_size, Hkv, D))
     vf = _normal(gen, (pool, block_size, Hkv, D))
+    kv_fp8 = kv_int8 = False
     if kv == "fp8":
         k_cache, k_scale = _fp8_quantise(kf)
         v_cache, v_scale = _fp8_quantise(vf)
         kv_fp8 = True
+    elif kv == "int8":
+        k_cache, k_scale = _int8_quantise(kf)
+        v_cache, v_scale = _int8_quantise(vf)
+        kv_int8 = True
     elif kv == "f16":
         k_cache, v_cache = kf.to(torch.float16), vf.to(torch.float16)
         k_scale = v_scale = 1.0
-        kv_fp8 = False
     else:
         raise ValueError(kv)
     return Workload(name=name, q=q, k_cache=k_cache, v_cache=v_cache, block_table=table,
                     seq_lens=torch.tensor(seq_lens, dtype=torch.int32),
                     scale=float(scale if scale is not None else 1.0 / math.sqrt(D)),
                     window=int(window), qlen=int(qlen), num_splits=int(num_splits), kv_fp8=kv_fp8,
+                    kv_int8=kv_int8,
                     k_scale=k_scale, v_scale=v_scale,
                     meta=dict(layout=layout, seed=int(seed), kv=kv))
 

@@ -11,7 +11,9 @@ import numpy as np
 import torch
 
 
-def decode_cache(cache, fp8, scale):
+def decode_cache(cache, fp8, scale, int8=False):
+    if int8:
+        return np.ascontiguousarray(cache).view(np.int8).astype(np.float64) * float(scale)
     if fp8:
         t = torch.from_numpy(np.ascontiguousarray(cache)).view(torch.float8_e4m3fn)
         return t.to(torch.float64).numpy() * float(scale)
@@ -37,10 +39,10 @@ def visibility(L, qlen, window):
 
 
 def attention(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, qlen=1,
-              kv_fp8=False, k_scale=1.0, v_scale=1.0):
+              kv_fp8=False, k_scale=1.0, v_scale=1.0, kv_int8=False):
     qf = np.asarray(q).astype(np.float16).astype(np.float64)
-    Kc = decode_cache(k_cache, kv_fp8, k_scale)
-    Vc = decode_cache(v_cache, kv_fp8, v_scale)
+    Kc = decode_cache(k_cache, kv_fp8, k_scale, kv_int8)
+    Vc = decode_cache(v_cache, kv_fp8, v_scale, kv_int8)
     B = len(seq_lens)
     Hq, D = qf.shape[1], qf.shape[2]
     Hkv = Kc.shape[2]

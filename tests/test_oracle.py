@@ -28,7 +28,7 @@ def _np(t):
 
 def run_oracle(oracle, w, split=None, **kw):
     args = dict(scale=w.scale, window=w.window, qlen=w.qlen, k_scale=w.k_scale,
-                v_scale=w.v_scale, kv_fp8=w.kv_fp8)
+                v_scale=w.v_scale, kv_fp8=w.kv_fp8, kv_int8=w.kv_int8)
     args.update(kw)
     if split is None:
         return oracle.decode_paged(_np(w.q), _np(w.k_cache), _np(w.v_cache), _np(w.block_table),
@@ -40,7 +40,7 @@ def run_oracle(oracle, w, split=None, **kw):
 def run_dense(w):
     return ref_dense.attention(_np(w.q), _np(w.k_cache), _np(w.v_cache), _np(w.block_table),
                                _np(w.seq_lens), w.scale, w.window, w.qlen, w.kv_fp8, w.k_scale,
-                               w.v_scale)
+                               w.v_scale, w.kv_int8)
 
 
 # ---- element decoders ----------------------------------------------------------
@@ -64,6 +64,13 @@ def test_e4m3fn_decoder_every_code(oracle_lib):
     assert np.array_equal(got[~nan], want[~nan])
 
 
+def test_int8_decoder_every_code(oracle_lib):
+    want = np.arange(256, dtype=np.uint8).view(np.int8).astype(np.float64)
+    got = np.array([oracle_lib.i8_to_f64(c) for c in range(256)])
+    assert np.array_equal(got, want)
+    assert oracle_lib.i8_to_f64(0x80) == -128.0 and oracle_lib.i8_to_f64(0x7F) == 127.0
+
+
 def test_e4m3fn_spec_points(oracle_lib):
     pts = json.load(open(os.path.join(GOLDEN, "e4m3fn_points.json")))["points"]
     for p in pts:
@@ -81,7 +88,7 @@ def _golden_workload(case):
     B, Hq, Hkv, D = case["B"], case["Hq"], case["Hkv"], case["D"]
     bs, qlen = case["block_size"], case["qlen"]
     lens = case["seq_lens"]
-    fp8 = case.get("kv") == "fp8"
+    fp8 = case.get("kv") in ("fp8", "int8")
     need = [(L + bs - 1) // bs for L in lens]
     pool = sum(need) + 1
     maxb = max(need + [1])
@@ -110,6 +117,7 @@ def test_golden_closed_forms(oracle_lib, case):
     q, K, V, table, lens = _golden_workload(case)
     fp8 = case.get("kv") == "fp8"
     kw = dict(scale=case["scale"], window=case["window"], qlen=case["qlen"], kv_fp8=fp8,
+              kv_int8=case.get("kv") == "int8",
               k_scale=case.get("k_scale", 1.0), v_scale=case.get("v_scale", 1.0))
     env = {"e": math.e, "exp": math.exp, "sqrt": math.sqrt}
     want = np.array([[eval(x, env) for x in row] for row in case["expected"]])
@@ -144,7 +152,7 @@ def _tiny(c, kv="f16", seed=7, layout="permuted", scale=None):
                                 pool_blocks=sum((L + c["bs"] - 1) // c["bs"] for L in c["lens"]) + 3)
 
 
-@pytest.mark.parametrize("kv", ["f16", "fp8"])
+@pytest.mark.parametrize("kv", ["f16", "fp8", "int8"])
 @pytest.mark.parametrize("ci", range(len(TINY)))
 def test_oracle_matches_dense_bruteforce(oracle_lib, ci, kv):
     w = _tiny(TINY[ci], kv=kv, seed=100 + ci)
@@ -234,7 +242,7 @@ def test_empty_rows_are_exact_zero(oracle_lib):
 
 # ---- invariants ------------------------------------------------------------------------
 
-@pytest.mark.parametrize("kv", ["f16", "fp8"])
+@pytest.mark.parametrize("kv", ["f16", "fp8", "int8"])
 @pytest.mark.parametrize("ci", [1, 2, 3, 4, 5, 7])
 def test_split_mode_matches_one_shot(oracle_lib, ci, kv):
     w = _tiny(TINY[ci], kv=kv, seed=300 + ci)

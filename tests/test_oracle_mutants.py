@@ -27,6 +27,8 @@ MUTANTS = [
     ("online_rescale_missing", "l *= a;", "l *= 1.0;"),
     ("v_scale_unused", "o[x] += w * cache_at(d, v_cache, d->v_scale, blk, slot, kh, x);",
      "o[x] += w * cache_at(d, v_cache, d->k_scale, blk, slot, kh, x);"),
+    ("int8_unsigned", "double pdo_i8_to_f64(uint8_t c) { return (double)(int8_t)c; }",
+     "double pdo_i8_to_f64(uint8_t c) { return (double)c; }"),
     ("split_chunk_bound", "if (cb1 > first_block + n_blocks) cb1 = first_block + n_blocks;",
      "if (cb1 > first_block + n_blocks - 1) cb1 = first_block + n_blocks - 1;"),
 ]
@@ -52,10 +54,10 @@ def _pin_calls():
     import json
     cases = json.load(open(os.path.join(pins.GOLDEN, "closed_forms.json")))["cases"]
     calls = [(pins.test_f16_decoder_every_pattern, {}), (pins.test_e4m3fn_decoder_every_code, {}),
-             (pins.test_e4m3fn_spec_points, {})]
+             (pins.test_e4m3fn_spec_points, {}), (pins.test_int8_decoder_every_code, {})]
     calls += [(pins.test_golden_closed_forms, {"case": c}) for c in cases]
     calls += [(pins.test_oracle_matches_dense_bruteforce, {"ci": ci, "kv": kv})
-              for ci in range(len(pins.TINY)) for kv in ("f16", "fp8")]
+              for ci in range(len(pins.TINY)) for kv in ("f16", "fp8", "int8")]
     calls += [(pins.test_split_mode_matches_one_shot, {"ci": ci, "kv": "f16"}) for ci in (2, 5)]
     calls += [(pins.test_combine_edge_cases, {}), (pins.test_split_partials_recombine, {})]
     return calls
