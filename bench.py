@@ -225,7 +225,7 @@ class DeviceWorkload:
         need = [(L + bs - 1) // bs for L in seq_lens]
         self.max_blocks = max_blocks or max(need + [1])
         per_table = max(sum(need), 1)
-        elem = 1 if kv == "fp8" else 2
+        elem = 1 if kv in ("fp8", "int8") else 2
         footprint = per_table * bs * Hkv * Dh * elem * 2
         self.n_rot = min(1024, max(2, -(-4 * l2_bytes // footprint)))
         pool = self.n_rot * per_table
@@ -241,7 +241,13 @@ class DeviceWorkload:
             self.tables.append(t.to(device))
         dg = torch.Generator(device=device).manual_seed(seed + 1)
         shape = (pool, bs, Hkv, Dh)
-        if kv == "fp8":
+        if kv == "int8":
+            def codes():
+                return torch.randint(-127, 128, shape, generator=dg, device=device,
+                                     dtype=torch.int32).to(torch.int8)
+            self.k, self.v = codes(), codes()
+            self.k_scale = self.v_scale = 1.0 / 64
+        elif kv == "fp8":
             def codes():
                 mag = torch.randint(0, 0x7E + 1, shape, generator=dg, device=device, dtype=torch.int32)
                 sign = torch.randint(0, 2, shape, generator=dg, device=device, dtype=torch.int32)
@@ -258,6 +264,7 @@ class DeviceWorkload:
         self.out = torch.empty_like(self.q)
         self.B, self.qlen, self.window, self.Dh = B, qlen, window, Dh
         self.kv_bytes = kv_bytes_of(seq_lens, qlen, window, Hkv, Dh, elem)
+        self.kv = kv
         self.scale = 1.0 / Dh ** 0.5
 
 
@@ -266,8 +273,7 @@ def time_workload(wl, num_splits, steps, warmup, device, world, sample_clocks=Fa
     once between CUDA events on the launching stream."""
     import paged_split_decode_gb300 as pd
     stream = torch.cuda.Stream(device)
-    dims = pd.dims_of(wl.q, wl.k, wl.tables[0], wl.qlen, wl.k.dtype == torch.uint8, wl.k_scale,
-                      wl.v_scale)
+    dims = pd.dims_of(wl.q, wl.k, wl.tables[0], wl.qlen, None, wl.k_scale, wl.v_scale)
     ws = pd.get_workspace(device, pd.workspace_bytes(dims, wl.qlen, num_splits))
     flag = torch.zeros(1, dtype=torch.int32, device=device)
 
@@ -349,6 +355,12 @@ def other_workloads(device, l2, seed, only=None):
         lambda: DeviceWorkload(device, l2, seed + 99, 8, 24, 4, 256, [8192] * 8, qlen=3, kv="fp8"), 0)
     add("verify_q3_f16_d256_L8192_b8",
         lambda: DeviceWorkload(device, l2, seed + 98, 8, 24, 4, 256, [8192] * 8, qlen=3), 0)
+    add("verify_q3_int8_d256_L8192_b8",
+        lambda: DeviceWorkload(device, l2, seed + 97, 8, 24, 4, 256, [8192] * 8, qlen=3, kv="int8"), 0)
+    add("gqa6_d256_L4096_b32_fp8",
+        lambda: DeviceWorkload(device, l2, seed + 96, 32, 24, 4, 256, [4096] * 32, kv="fp8"), 0)
+    add("gqa6_d256_L4096_b32_int8",
+        lambda: DeviceWorkload(device, l2, seed + 95, 32, 24, 4, 256, [4096] * 32, kv="int8"), 0)
     for name, make, S in full:
         if only is None or name == only:
             yield name, make(), S

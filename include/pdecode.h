@@ -6,7 +6,7 @@
  * ("Paged split-K decode"):
  *   - "Purpose": a per-head decode over a paged KV cache -- page lookups
  *     through a block table, scores scale * q . k, online softmax, P.V, and
- *     split-K partials merged by a combine; fp16 and fp8 KV share the body;
+ *     split-K partials merged by a combine; fp16, fp8 and int8 KV share the body;
  *     every launch runs on the caller's current stream;
  *   - "What changed vs the old #33 diff": an empty key range never enters the
  *     P.V loop (empty rows are zero);
@@ -69,8 +69,9 @@ typedef enum {
 } pd_status;
 
 typedef enum {
-  PD_KV_F16 = 0,      /* K and V caches hold IEEE binary16 */
-  PD_KV_FP8_E4M3 = 1  /* K and V caches hold OCP e4m3fn codes; value = code * scale */
+  PD_KV_F16 = 0,       /* K and V caches hold IEEE binary16 */
+  PD_KV_FP8_E4M3 = 1,  /* K and V caches hold OCP e4m3fn codes; value = decode(code) * scale */
+  PD_KV_INT8 = 2       /* K and V caches hold int8 two's-complement codes; value = code * scale */
 } pd_kv_dtype;
 
 /* Bits written into *error_flag by the device. */
@@ -86,7 +87,7 @@ typedef enum {
  *   num_blocks         blocks in each of the K and V caches
  *   max_blocks_per_seq columns of block_table
  *   kv_dtype           pd_kv_dtype
- *   k_scale, v_scale   fp8 only: per-cache dequantisation scales (ignored for fp16) */
+ *   k_scale, v_scale   fp8 / int8: per-cache dequantisation scales (ignored for fp16) */
 typedef struct {
   int32_t B, Hq, Hkv, D;
   int32_t block_size, num_blocks, max_blocks_per_seq;
@@ -114,7 +115,7 @@ PD_API int pd_grid_ctas(const pd_dims* dims, int qlen, int num_splits, int sm_co
  * dependent launch that merges the partials of units cut into pieces.
  *
  *   q            fp16 [B*qlen, Hq, D]; row b*qlen + i is query token i of sequence b
- *   k_cache      [num_blocks, block_size, Hkv, D] fp16 or e4m3fn (dims->kv_dtype)
+ *   k_cache      [num_blocks, block_size, Hkv, D] fp16, e4m3fn or int8 (dims->kv_dtype)
  *   v_cache      same layout and dtype as k_cache
  *   block_table  int32 [B, max_blocks_per_seq]; entry [b][n] is the physical
  *                block holding keys n*block_size .. n*block_size+block_size-1 of

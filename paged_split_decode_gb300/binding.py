@@ -19,6 +19,7 @@ _lock = threading.Lock()
 
 PD_KV_F16 = 0
 PD_KV_FP8_E4M3 = 1
+PD_KV_INT8 = 2
 DEVERR_BLOCK_ID = 1
 DEVERR_SEQ_LEN = 2
 DEVERR_TIMEOUT = 4
@@ -82,16 +83,30 @@ def _check(code: int, what: str):
 
 
 def make_dims(B, Hq, Hkv, D, block_size, num_blocks, max_blocks_per_seq, kv_fp8=False,
-              k_scale=1.0, v_scale=1.0) -> PdDims:
+              k_scale=1.0, v_scale=1.0, kv_int8=False) -> PdDims:
+    kind = PD_KV_INT8 if kv_int8 else (PD_KV_FP8_E4M3 if kv_fp8 else PD_KV_F16)
     return PdDims(int(B), int(Hq), int(Hkv), int(D), int(block_size), int(num_blocks),
-                  int(max_blocks_per_seq), PD_KV_FP8_E4M3 if kv_fp8 else PD_KV_F16,
-                  float(k_scale), float(v_scale))
+                  int(max_blocks_per_seq), kind, float(k_scale), float(v_scale))
 
 
-def dims_of(q, k_cache, block_table, qlen, kv_fp8=False, k_scale=1.0, v_scale=1.0) -> PdDims:
+def kv_kind_of(k_cache) -> int:
+    """fp16 caches -> PD_KV_F16; torch.int8 -> PD_KV_INT8; uint8 or float8_e4m3fn
+    -> PD_KV_FP8_E4M3."""
+    if k_cache.dtype == torch.float16:
+        return PD_KV_F16
+    if k_cache.dtype == torch.int8:
+        return PD_KV_INT8
+    if k_cache.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return PD_KV_FP8_E4M3
+    raise TypeError(f"unsupported KV cache dtype {k_cache.dtype}")
+
+
+def dims_of(q, k_cache, block_table, qlen, kv_fp8=None, k_scale=1.0, v_scale=1.0) -> PdDims:
     num_blocks, bs, Hkv, D = k_cache.shape
+    kind = kv_kind_of(k_cache)
     return make_dims(block_table.shape[0], q.shape[1], Hkv, D, bs, num_blocks,
-                     block_table.shape[1], kv_fp8, k_scale, v_scale)
+                     block_table.shape[1], kind == PD_KV_FP8_E4M3, k_scale, v_scale,
+                     kind == PD_KV_INT8)
 
 
 def workspace_bytes(dims: PdDims, qlen: int, num_splits: int, sm_count: int = 0) -> int:
@@ -137,13 +152,15 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, ql
                  error_flag=None, stream=None):
     """Paged decode attention on the GPU; returns ``out`` (fp16 [B*qlen, Hq, D]).
 
-    ``k_cache``/``v_cache`` are fp16, or uint8 / float8_e4m3fn holding e4m3fn
-    codes (then ``k_scale``/``v_scale`` apply). ``num_splits`` 0 = balanced.
+    ``k_cache``/``v_cache`` are fp16, uint8 / float8_e4m3fn holding e4m3fn
+    codes, or int8 codes (then ``k_scale``/``v_scale`` apply). ``num_splits``
+    0 = balanced.
     """
     lib = load()
-    kv_fp8 = k_cache.dtype in (torch.uint8, torch.float8_e4m3fn)
-    kv_dt = (torch.uint8, torch.float8_e4m3fn) if kv_fp8 else torch.float16
-    dims = dims_of(q, k_cache, block_table, qlen, kv_fp8, k_scale, v_scale)
+    kind = kv_kind_of(k_cache)
+    kv_dt = {PD_KV_F16: torch.float16, PD_KV_INT8: torch.int8,
+             PD_KV_FP8_E4M3: (torch.uint8, torch.float8_e4m3fn)}[kind]
+    dims = dims_of(q, k_cache, block_table, qlen, None, k_scale, v_scale)
     if out is None:
         out = torch.empty_like(q)
     if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype:

@@ -7,12 +7,12 @@
 
 namespace pd {
 namespace {
-constexpr bool kFp8 = true;
+constexpr int kKv = kKvFp8;
 constexpr int kD = 128;
-using C1 = CfgFor<kD, kFp8, 1, 2, 2>;
-using C2 = CfgFor<kD, kFp8, 2, 1, 2>;
-using C3 = CfgFor<kD, kFp8, 3, 1, 2>;
-using C4 = CfgFor<kD, kFp8, 4, 1, 2>;
+using C1 = CfgFor<kD, kKv, 1, 2, 2>;
+using C2 = CfgFor<kD, kKv, 2, 1, 2>;
+using C3 = CfgFor<kD, kKv, 3, 1, 2>;
+using C4 = CfgFor<kD, kKv, 4, 1, 2>;
 }  // namespace
 
 bool shape_fp8_d128(int nt, KernelShape* out) {

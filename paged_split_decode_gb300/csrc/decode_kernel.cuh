@@ -22,8 +22,9 @@
 //    S^T = K Q^T with mma.sync m16n8k16 (keys on M, query rows on N, Q held in
 //    registers), masks, runs the online softmax with warp shuffles, turns P
 //    into the B operand with movmatrix and accumulates O^T = V^T P^T.
-//    fp8 e4m3 tiles are widened to fp16 in registers (cvt.f16x2.e4m3x2); the
-//    K scale is folded into the score scale and the V scale into the output.
+//    fp8 e4m3 tiles are widened to fp16 in registers (cvt.f16x2.e4m3x2), int8
+//    tiles by an exact magic-number conversion; the K scale is folded into the
+//    score scale and the V scale into the output.
 //  * At the end of a unit piece the KG key groups merge (m, l, O) through
 //    shared memory. A unit covered by one piece is normalised and written as
 //    fp16; otherwise the piece writes an fp32 partial and bumps the unit's
@@ -68,11 +69,38 @@ struct DecodeParams {
   unsigned long long timeout_ns;
 };
 
-template <int D_, bool FP8_, int NT_, int KG_, int NS_, int MINB_>
+// KV element kinds: fp16, or one byte per element (OCP e4m3fn or int8 codes).
+constexpr int kKvF16 = 0, kKvFp8 = 1, kKvInt8 = 2;
+
+// Two byte codes of `w` (its low or high 16 bits, byte 0 / 2 the lower index)
+// widened to an fp16 pair, exactly. e4m3fn: the hardware conversion. int8:
+// `w` must be pre-biased (w ^ 0x80808080, codes + 128 as unsigned bytes); each
+// byte u is spliced under the fp16 exponent byte 0x64, giving 1024 + u exactly,
+// and 1152 = 1024 + 128 is subtracted (the magic-number integer-to-float
+// conversion; every value involved is an exactly representable integer).
+template <int KV>
+__device__ __forceinline__ uint32_t byte_pair_to_half2(uint32_t w, bool high) {
+  if constexpr (KV == kKvFp8) {
+    return e4m3x2_to_half2(static_cast<uint16_t>(high ? (w >> 16) : (w & 0xffffu)));
+  } else {
+    const uint32_t h = prmt(w, 0x64646464u, high ? 0x7362u : 0x5140u);
+    const uint32_t bias = 0x64806480u;  // fp16 1152 in both halves
+    __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), *reinterpret_cast<const __half2*>(&bias));
+    return *reinterpret_cast<uint32_t*>(&r);
+  }
+}
+template <int KV>
+__device__ __forceinline__ uint32_t byte_word_prep(uint32_t w) {
+  if constexpr (KV == kKvInt8) return w ^ 0x80808080u;
+  else return w;
+}
+
+template <int D_, int KV_, int NT_, int KG_, int NS_, int MINB_>
 struct Cfg {
   static constexpr int D = D_, NT = NT_, KG = KG_, NS = NS_;
   static constexpr int kMinBlocks = MINB_;              // resident CTAs per SM the plan targets
-  static constexpr bool FP8 = FP8_;
+  static constexpr int KV = KV_;
+  static constexpr bool FP8 = KV_ != kKvF16;   // one-byte elements (e4m3fn or int8)
   static constexpr int kElem = FP8 ? 1 : 2;
   static constexpr int kSlabElems = 128 / kElem;        // one 128-byte swizzle row
   static constexpr int kSlabs = D / kSlabElems;
@@ -534,10 +562,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           for (int j = 0; j < 4; ++j) {
             const int ksl = sup * 4 + j;
             uint32_t a[4];
-            a[0] = e4m3x2_to_half2(static_cast<uint16_t>(wa[j] & 0xffffu));
-            a[1] = e4m3x2_to_half2(static_cast<uint16_t>(wb[j] & 0xffffu));
-            a[2] = e4m3x2_to_half2(static_cast<uint16_t>(wa[j] >> 16));
-            a[3] = e4m3x2_to_half2(static_cast<uint16_t>(wb[j] >> 16));
+            const uint32_t xa = byte_word_prep<Cfg::KV>(wa[j]), xb = byte_word_prep<Cfg::KV>(wb[j]);
+            a[0] = byte_pair_to_half2<Cfg::KV>(xa, false);
+            a[1] = byte_pair_to_half2<Cfg::KV>(xb, false);
+            a[2] = byte_pair_to_half2<Cfg::KV>(xa, true);
+            a[3] = byte_pair_to_half2<Cfg::KV>(xb, true);
 #pragma unroll
             for (int n = 0; n < NTW; ++n) {
               if (j & 1) mma_16816(sb[n], a, qf[ksl][n][0], qf[ksl][n][1]);
@@ -651,19 +680,21 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wB) : "r"(sb0 + kB * 128 + ((chunk ^ (kB & 7)) << 4)));
           asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wC) : "r"(sb0 + kC * 128 + ((chunk ^ (kC & 7)) << 4)));
           asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wD) : "r"(sb0 + kD * 128 + ((chunk ^ (kD & 7)) << 4)));
+          wA = byte_word_prep<Cfg::KV>(wA); wB = byte_word_prep<Cfg::KV>(wB);
+          wC = byte_word_prep<Cfg::KV>(wC); wD = byte_word_prep<Cfg::KV>(wD);
           const uint32_t ab01 = prmt(wA, wB, 0x5140u), ab23 = prmt(wA, wB, 0x7362u);
           const uint32_t cd01 = prmt(wC, wD, 0x5140u), cd23 = prmt(wC, wD, 0x7362u);
           uint32_t a[4];
-          a[0] = e4m3x2_to_half2(static_cast<uint16_t>(ab01 & 0xffffu));
-          a[1] = e4m3x2_to_half2(static_cast<uint16_t>(ab01 >> 16));
-          a[2] = e4m3x2_to_half2(static_cast<uint16_t>(cd01 & 0xffffu));
-          a[3] = e4m3x2_to_half2(static_cast<uint16_t>(cd01 >> 16));
+          a[0] = byte_pair_to_half2<Cfg::KV>(ab01, false);
+          a[1] = byte_pair_to_half2<Cfg::KV>(ab01, true);
+          a[2] = byte_pair_to_half2<Cfg::KV>(cd01, false);
+          a[3] = byte_pair_to_half2<Cfg::KV>(cd01, true);
 #pragma unroll
           for (int n = 0; n < NTW; ++n) mma_16816(o[2 * pl][n], a, pb0[n], pb1[n]);
-          a[0] = e4m3x2_to_half2(static_cast<uint16_t>(ab23 & 0xffffu));
-          a[1] = e4m3x2_to_half2(static_cast<uint16_t>(ab23 >> 16));
-          a[2] = e4m3x2_to_half2(static_cast<uint16_t>(cd23 & 0xffffu));
-          a[3] = e4m3x2_to_half2(static_cast<uint16_t>(cd23 >> 16));
+          a[0] = byte_pair_to_half2<Cfg::KV>(ab23, false);
+          a[1] = byte_pair_to_half2<Cfg::KV>(ab23, true);
+          a[2] = byte_pair_to_half2<Cfg::KV>(cd23, false);
+          a[3] = byte_pair_to_half2<Cfg::KV>(cd23, true);
 #pragma unroll
           for (int n = 0; n < NTW; ++n) mma_16816(o[2 * pl + 1][n], a, pb0[n], pb1[n]);
         }

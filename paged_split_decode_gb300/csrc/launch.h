@@ -16,11 +16,11 @@ struct KernelShape {
   int ctas_per_sm;  // resident CTAs per SM the configuration is sized for
 };
 
-// Returns false when no instantiation covers (D, fp8, nt).
-bool kernel_shape(int D, bool fp8, int nt, KernelShape* out);
+// Returns false when no instantiation covers (D, kv kind, nt).
+bool kernel_shape(int D, int kv, int nt, KernelShape* out);
 
-// Launch the instantiation for (D, fp8, nt) on `grid` CTAs.
-cudaError_t launch_decode(int D, bool fp8, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
+// Launch the instantiation for (D, kv kind, nt) on `grid` CTAs.
+cudaError_t launch_decode(int D, int kv, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
                           const DecodeParams& p, int grid, cudaStream_t stream);
 
 // Split combine behind a decode launch (split_combine.cu).
@@ -31,6 +31,8 @@ bool shape_f16_d128(int nt, KernelShape* out);
 bool shape_f16_d256(int nt, KernelShape* out);
 bool shape_fp8_d128(int nt, KernelShape* out);
 bool shape_fp8_d256(int nt, KernelShape* out);
+bool shape_i8_d128(int nt, KernelShape* out);
+bool shape_i8_d256(int nt, KernelShape* out);
 cudaError_t launch_f16_d128(int nt, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
                             cudaStream_t);
 cudaError_t launch_f16_d256(int nt, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
@@ -39,6 +41,10 @@ cudaError_t launch_fp8_d128(int nt, const CUtensorMap&, const CUtensorMap&, cons
                             cudaStream_t);
 cudaError_t launch_fp8_d256(int nt, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
                             cudaStream_t);
+cudaError_t launch_i8_d128(int nt, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
+                           cudaStream_t);
+cudaError_t launch_i8_d256(int nt, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
+                           cudaStream_t);
 
 // Launch one configuration; sets the shared-memory opt-in once per device.
 template <class Cfg>
@@ -63,15 +69,15 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
 // MINB CTAs share one SM's 228 KiB (1 KiB of it reserved per CTA; at most
 // 227 KiB for one CTA).
 constexpr int smem_limit(int minb) { return minb == 1 ? 227 * 1024 : 228 * 1024 / minb - 1024; }
-template <int D, bool FP8, int NT, int KG, int MINB, int NS = 32>
+template <int D, int KV, int NT, int KG, int MINB, int NS = 32>
 constexpr int ring_stages() {
-  if constexpr (NS <= 2 || Cfg<D, FP8, NT, KG, NS, MINB>::kSmemBytes <= smem_limit(MINB))
+  if constexpr (NS <= 2 || Cfg<D, KV, NT, KG, NS, MINB>::kSmemBytes <= smem_limit(MINB))
     return NS;
   else
-    return ring_stages<D, FP8, NT, KG, MINB, NS - 1>();
+    return ring_stages<D, KV, NT, KG, MINB, NS - 1>();
 }
-template <int D, bool FP8, int NT, int KG, int MINB>
-using CfgFor = Cfg<D, FP8, NT, KG, ring_stages<D, FP8, NT, KG, MINB>(), MINB>;
+template <int D, int KV, int NT, int KG, int MINB>
+using CfgFor = Cfg<D, KV, NT, KG, ring_stages<D, KV, NT, KG, MINB>(), MINB>;
 
 template <class Cfg>
 bool shape_of(KernelShape* out) {

@@ -14,16 +14,25 @@
 
 namespace pd {
 
-bool kernel_shape(int D, bool fp8, int nt, KernelShape* out) {
-  if (D == 128) return fp8 ? shape_fp8_d128(nt, out) : shape_f16_d128(nt, out);
-  if (D == 256) return fp8 ? shape_fp8_d256(nt, out) : shape_f16_d256(nt, out);
+bool kernel_shape(int D, int kv, int nt, KernelShape* out) {
+  if (D == 128)
+    return kv == kKvFp8 ? shape_fp8_d128(nt, out) : kv == kKvInt8 ? shape_i8_d128(nt, out)
+                                                                  : shape_f16_d128(nt, out);
+  if (D == 256)
+    return kv == kKvFp8 ? shape_fp8_d256(nt, out) : kv == kKvInt8 ? shape_i8_d256(nt, out)
+                                                                  : shape_f16_d256(nt, out);
   return false;
 }
 
-cudaError_t launch_decode(int D, bool fp8, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_decode(int D, int kv, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
                           const DecodeParams& p, int grid, cudaStream_t s) {
-  if (D == 128) return fp8 ? launch_fp8_d128(nt, tk, tv, p, grid, s) : launch_f16_d128(nt, tk, tv, p, grid, s);
-  return fp8 ? launch_fp8_d256(nt, tk, tv, p, grid, s) : launch_f16_d256(nt, tk, tv, p, grid, s);
+  if (D == 128)
+    return kv == kKvFp8 ? launch_fp8_d128(nt, tk, tv, p, grid, s)
+           : kv == kKvInt8 ? launch_i8_d128(nt, tk, tv, p, grid, s)
+                           : launch_f16_d128(nt, tk, tv, p, grid, s);
+  return kv == kKvFp8 ? launch_fp8_d256(nt, tk, tv, p, grid, s)
+         : kv == kKvInt8 ? launch_i8_d256(nt, tk, tv, p, grid, s)
+                         : launch_f16_d256(nt, tk, tv, p, grid, s);
 }
 
 namespace {
@@ -50,8 +59,9 @@ pd_status check_dims(const pd_dims* d, int qlen) {
       d->max_blocks_per_seq < 0 || qlen < 1)
     return PD_ERR_SHAPE;
   if (d->Hq % d->Hkv != 0) return PD_ERR_SHAPE;
-  if (d->kv_dtype != PD_KV_F16 && d->kv_dtype != PD_KV_FP8_E4M3) return PD_ERR_DTYPE;
-  if (d->kv_dtype == PD_KV_FP8_E4M3 &&
+  if (d->kv_dtype != PD_KV_F16 && d->kv_dtype != PD_KV_FP8_E4M3 && d->kv_dtype != PD_KV_INT8)
+    return PD_ERR_DTYPE;
+  if (d->kv_dtype != PD_KV_F16 &&
       (!std::isfinite(d->k_scale) || !std::isfinite(d->v_scale)))
     return PD_ERR_SHAPE;
   if (d->D != 128 && d->D != 256) return PD_ERR_UNSUPPORTED;
@@ -86,7 +96,7 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
   const int R = d->Hq / d->Hkv * qlen;
   pl->nt = (R + 7) / 8;
   KernelShape ks;
-  if (!kernel_shape(d->D, d->kv_dtype == PD_KV_FP8_E4M3, pl->nt, &ks)) return PD_ERR_UNSUPPORTED;
+  if (!kernel_shape(d->D, d->kv_dtype, pl->nt, &ks)) return PD_ERR_UNSUPPORTED;
   pl->rows_padded = ks.rows_padded;
   pl->units = static_cast<long long>(d->B) * d->Hkv;
   int splits = num_splits;
@@ -137,15 +147,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 bool encode_cache_map(CUtensorMap* m, const void* base, const pd_dims* d) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const bool fp8 = d->kv_dtype == PD_KV_FP8_E4M3;
-  const cuuint64_t elem = fp8 ? 1 : 2;
+  const bool byte = d->kv_dtype != PD_KV_F16;
+  const cuuint64_t elem = byte ? 1 : 2;
   const cuuint64_t rows = static_cast<cuuint64_t>(d->num_blocks) * d->block_size;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d->D), static_cast<cuuint64_t>(d->Hkv),
                         rows > 0 ? rows : 1};
   cuuint64_t strides[2] = {d->D * elem, static_cast<cuuint64_t>(d->Hkv) * d->D * elem};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem), 1, static_cast<cuuint32_t>(kTileKeys)};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+  CUresult r = fn(m, byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -211,7 +221,7 @@ pd_status decode_paged(const void* q, const void* k_cache, const void* v_cache,
   CUtensorMap tk, tv;
   if (!encode_cache_map(&tk, k_cache, dims) || !encode_cache_map(&tv, v_cache, dims)) return PD_ERR_CUDA;
 
-  const bool fp8 = dims->kv_dtype == PD_KV_FP8_E4M3;
+  const bool fp8 = dims->kv_dtype != PD_KV_F16;  // a one-byte kind with scales
   DecodeParams p;
   p.q = static_cast<const __half*>(q);
   p.out = static_cast<__half*>(out);
@@ -241,7 +251,7 @@ pd_status decode_paged(const void* q, const void* k_cache, const void* v_cache,
   p.out_scale = fp8 ? dims->v_scale : 1.0f;
   p.timeout_ns = kTimeoutNs;
 
-  cudaError_t e = launch_decode(dims->D, fp8, pl.nt, tk, tv, p, pl.grid,
+  cudaError_t e = launch_decode(dims->D, dims->kv_dtype, pl.nt, tk, tv, p, pl.grid,
                                 static_cast<cudaStream_t>(stream));
   if (e == cudaSuccess && pl.n_desc > 0)
     e = launch_split_combine(dims->D, p, static_cast<int>(pl.n_desc), static_cast<cudaStream_t>(stream));

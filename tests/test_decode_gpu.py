@@ -35,9 +35,17 @@ def pd():
 DEV = "cuda:0"
 
 
+def kv_on_device(w):
+    k, v = w.k_cache.to(DEV), w.v_cache.to(DEV)
+    if w.kv_int8:
+        k, v = k.view(torch.int8), v.view(torch.int8)
+    return k, v
+
+
 def gpu_run(pd, w, num_splits=None, out=None, flag=None, workspace=None):
     S = w.num_splits if num_splits is None else num_splits
-    res = pd.decode_paged(w.q.to(DEV), w.k_cache.to(DEV), w.v_cache.to(DEV), w.block_table.to(DEV),
+    k, v = kv_on_device(w)
+    res = pd.decode_paged(w.q.to(DEV), k, v, w.block_table.to(DEV),
                           w.seq_lens.to(DEV), w.scale, w.window, w.qlen, S, out=out,
                           k_scale=w.k_scale, v_scale=w.v_scale, error_flag=flag, workspace=workspace)
     torch.cuda.synchronize()
@@ -47,7 +55,7 @@ def gpu_run(pd, w, num_splits=None, out=None, flag=None, workspace=None):
 def ref_run(w):
     return oracle.decode_paged(w.q.numpy(), w.k_cache.numpy(), w.v_cache.numpy(),
                                w.block_table.numpy(), w.seq_lens.numpy(), w.scale, w.window, w.qlen,
-                               w.k_scale, w.v_scale, w.kv_fp8)
+                               w.k_scale, w.v_scale, w.kv_fp8, kv_int8=w.kv_int8)
 
 
 def empty_rows(w):
@@ -104,6 +112,15 @@ def test_long_context_window_across_splits(pd, B, window):
         assert torch.max(torch.abs(o - outs[0])).item() <= TOL
 
 
+def test_speculative_verify_int8(pd):
+    """The int8 decode wrapper: the verify shape over int8 KV codes."""
+    w = inputs.make_workload(B=8, Hq=24, Hkv=4, D=256, qlen=3, seq_lens=[8192] * 8, kv="int8",
+                             seed=1240, name="verify3_int8_d256_L8192_b8")
+    ref = ref_run(w)
+    for S in (0, 1, 4):
+        check(w, gpu_run(pd, w, S), ref)
+
+
 def test_speculative_verify_fp8(pd):
     w = inputs.verify_fp8()
     ref = ref_run(w)
@@ -127,6 +144,10 @@ EDGE = [
     ("fp8_d128_rows_24", dict(B=3, Hq=8, Hkv=1, D=128, kv="fp8", qlen=3, seq_lens=[5, 300, 1500])),
     ("fp8_d256_rows_6", dict(B=2, Hq=24, Hkv=4, D=256, kv="fp8", seq_lens=[4000, 17])),
     ("many_sequences", dict(B=300, Hq=8, Hkv=2, D=128, seq_lens=list(range(0, 3000, 10)))),
+    ("int8_d256_rows_6", dict(B=3, Hq=24, Hkv=4, D=256, kv="int8", seq_lens=[4000, 17, 0])),
+    ("int8_d128_rows_24_window", dict(B=2, Hq=8, Hkv=1, D=128, kv="int8", qlen=3, window=300,
+                                      seq_lens=[1500, 40])),
+    ("int8_d256_rows_32", dict(B=2, Hq=8, Hkv=1, D=256, kv="int8", qlen=4, seq_lens=[700, 90])),
 ]
 
 
@@ -161,6 +182,36 @@ def test_split_tree_with_many_pieces(pd, S):
     8) then has up to three levels."""
     w = inputs.make_workload(B=1, Hq=8, Hkv=1, D=128, seq_lens=[20000], seed=41, qlen=2)
     check(w, gpu_run(pd, w, S), ref_run(w))
+
+
+@pytest.mark.parametrize("S", [0, 1, 3])
+def test_cuda_graph_capture_and_replay(pd, S):
+    """A call captured once into a CUDA graph (no host sync, no allocation, the
+    split plan fixed by host-known shapes) replays correctly after new values
+    are written into the same input buffers."""
+    shape = dict(B=4, Hq=24, Hkv=4, D=256, pool_blocks=600, max_blocks_per_seq=256)
+    w1 = inputs.make_workload(seq_lens=[3000, 17, 900, 0], seed=51, **shape)
+    w2 = inputs.make_workload(seq_lens=[2999, 1, 4000, 64], seed=52, **shape)
+    q, bt, sl = w1.q.to(DEV), w1.block_table.to(DEV), w1.seq_lens.to(DEV)
+    k, v = kv_on_device(w1)
+    out = torch.empty_like(q)
+    dims = pd.dims_of(q, k, bt, 1)
+    ws = torch.empty(max(pd.workspace_bytes(dims, 1, S), 1), dtype=torch.uint8, device=DEV)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        pd.decode_paged(q, k, v, bt, sl, w1.scale, 0, 1, S, out=out, workspace=ws)  # warm up
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        pd.decode_paged(q, k, v, bt, sl, w1.scale, 0, 1, S, out=out, workspace=ws)
+    for w in (w1, w2):
+        q.copy_(w.q.to(DEV)); bt.copy_(w.block_table.to(DEV)); sl.copy_(w.seq_lens.to(DEV))
+        k2, v2 = kv_on_device(w)
+        k.copy_(k2); v.copy_(v2)
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        check(w, out, ref_run(w))
 
 
 def test_custom_scale_writes_into_out_only(pd):

@@ -95,6 +95,9 @@ def test_decode_paged_validates_before_touching_the_device(lib):
     bad = _dims()
     bad.kv_dtype = 7
     assert _call(lib, bad) == 3                  # dtype
+    i8 = _dims()
+    i8.kv_dtype = 2                              # int8 is a known kind
+    assert binding.workspace_bytes(i8, 1, 0, sm_count=152) > 0
     assert _call(lib, d, q=None) == 1            # null pointer
     assert _call(lib, d, out=None) == 1
     assert _call(lib, d, q=0x1008) == 5          # misaligned (not 16 B)

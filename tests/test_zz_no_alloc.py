@@ -38,13 +38,15 @@ def lib():
 
 
 def _device(w):
-    return (w.q.to(DEV), w.k_cache.to(DEV), w.v_cache.to(DEV), w.block_table.to(DEV),
-            w.seq_lens.to(DEV))
+    k, v = w.k_cache.to(DEV), w.v_cache.to(DEV)
+    if w.kv_int8:
+        k, v = k.view(torch.int8), v.view(torch.int8)
+    return (w.q.to(DEV), k, v, w.block_table.to(DEV), w.seq_lens.to(DEV))
 
 
 def _call_static(lib, w, t, num_splits, out, flag):
     q, k, v, bt, sl = t
-    dims = binding.dims_of(q, k, bt, w.qlen, w.kv_fp8, w.k_scale, w.v_scale)
+    dims = binding.dims_of(q, k, bt, w.qlen, None, w.k_scale, w.v_scale)
     stream = torch.cuda.current_stream().cuda_stream
     return lib.decode_paged_static_scratch(q.data_ptr(), k.data_ptr(), v.data_ptr(), bt.data_ptr(),
                                            sl.data_ptr(), w.scale, w.window, w.qlen, num_splits,
