@@ -153,6 +153,19 @@ PD_API pd_status decode_paged(const void* q, const void* k_cache, const void* v_
 PD_API pd_status decode_paged_combine(const float* part_m, const float* part_l, const float* part_o,
                                int rows, int num_splits, int D, void* out, void* stream);
 
+/* Failure-detection controls (process-wide, read at each launch; for tests of
+ * the error path, not for production use).
+ *   pd_set_wait_limit_ns: wall-time limit of every pipeline wait inside the
+ *     decode kernel (0 restores the default, 2 s). A wait that runs past it
+ *     sets PD_DEVERR_TIMEOUT; the kernel then skips its remaining waits and
+ *     work, keeps its barrier sequence, lets every issued copy land and exits,
+ *     so the CUDA context stays usable.
+ *   pd_set_fault_injection: 1 makes the decode kernel's producer issue no
+ *     loads, so the consumers' waits can only run out (a wait that nothing
+ *     completes); 0 turns it off. The outputs of such calls are unspecified. */
+PD_API void pd_set_wait_limit_ns(unsigned long long ns);
+PD_API void pd_set_fault_injection(int mode);
+
 /* Size of the scratch array built into the library for
  * decode_paged_static_scratch (32 MiB). Every GPU that loads the library
  * keeps this much device memory until the process exits. */

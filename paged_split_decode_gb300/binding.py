@@ -25,7 +25,8 @@ DEVERR_SEQ_LEN = 2
 DEVERR_TIMEOUT = 4
 
 EXPORTS = ("decode_paged", "decode_paged_combine", "decode_paged_static_scratch",
-           "pd_workspace_bytes", "pd_grid_ctas", "pd_status_str")
+           "pd_workspace_bytes", "pd_grid_ctas", "pd_status_str", "pd_set_wait_limit_ns",
+           "pd_set_fault_injection")
 
 
 class PdDims(ctypes.Structure):
@@ -69,8 +70,22 @@ def load():
             lib.decode_paged_combine.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                  P, P]
             lib.decode_paged_combine.restype = ctypes.c_int
+            lib.pd_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+            lib.pd_set_wait_limit_ns.restype = None
+            lib.pd_set_fault_injection.argtypes = [ctypes.c_int]
+            lib.pd_set_fault_injection.restype = None
             _lib = lib
     return _lib
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Wall-time limit of the decode kernel's pipeline waits (0: default 2 s)."""
+    load().pd_set_wait_limit_ns(int(ns))
+
+
+def set_fault_injection(mode: int) -> None:
+    """1: the decode kernel's producer issues no loads (waits run out); 0: off."""
+    load().pd_set_fault_injection(int(mode))
 
 
 def status_str(code: int) -> str:

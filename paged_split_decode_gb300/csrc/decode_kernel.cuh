@@ -47,6 +47,9 @@ constexpr int kMaxAutoB = 1024;    // sequences handled by the balanced split
 // descriptor per entry (balanced mode: per CTA range, fixed mode: per unit)
 // naming the split unit whose first piece it holds, then the partials.
 constexpr uint32_t kErrBlockId = 1u, kErrSeqLen = 2u, kErrTimeout = 4u;
+// Limit of the producer's final drain: every load it issued lands before the
+// CTA exits, whatever the (possibly short) pipeline wait limit.
+constexpr unsigned long long kDrainLimitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeParams {
@@ -66,7 +69,8 @@ struct DecodeParams {
   int num_splits;             // 0: balanced
   float sl2;                  // scale * log2(e) * k_scale
   float out_scale;            // v_scale (1 for fp16)
-  unsigned long long timeout_ns;
+  unsigned long long timeout_ns;  // limit of every pipeline wait
+  int inject;                     // fault injection: 1 = the producer issues no load
 };
 
 // KV element kinds: fp16, or one byte per element (OCP e4m3fn or int8 codes).
@@ -412,6 +416,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           const uint32_t fb = full0 + 8 * stage;
           if (lane == 0) {
             if (ok && q >= NS) ok = mbar_wait(empty0 + 8 * stage, ((q / NS) - 1) & 1, p.timeout_ns);
+            if (ok && p.inject == 1) ok = false;  // injected fault: the ring stays empty
             if (ok) mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -438,7 +443,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
       // run; after a timeout, wait (bounded) for whatever is still in flight.
       const uint32_t first = issued > NS ? issued - NS : 0;
       for (uint32_t k = first; k < issued; ++k) {
-        if (!mbar_wait(full0 + 8 * (k % NS), (k / NS) & 1, p.timeout_ns)) break;
+        if (!mbar_wait(full0 + 8 * (k % NS), (k / NS) & 1, kDrainLimitNs)) break;
       }
     }
     return;
@@ -515,7 +520,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
       const uint32_t qq = q + k;
       const int stage = qq % NS;
       if (ok) ok = mbar_wait(full0 + 8 * stage, (qq / NS) & 1, p.timeout_ns);
-      if (!ok) continue;
+      if (!ok) {
+        // gave up: skip the work but keep the pair's barrier sequence, so the
+        // partner warp (whose own wait may have succeeded) is never stranded
+        if constexpr (DS == 2) named_bar_sync(2 + pair, 64);
+        continue;
+      }
       const uint32_t kb = smem_u32(smem + stage * Cfg::kStageBytes);
       const uint32_t vb = kb + Cfg::kTileBytes;
       const int key0 = (pc.first_tile + k) * kTileKeys;

@@ -7,6 +7,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 
 #include "launch.h"
@@ -37,7 +38,9 @@ cudaError_t launch_decode(int D, int kv, int nt, const CUtensorMap& tk, const CU
 
 namespace {
 
-constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait
+constexpr unsigned long long kTimeoutNs = 2000000000ull;  // 2 s per pipeline wait (default)
+std::atomic<unsigned long long> g_wait_limit_ns{kTimeoutNs};
+std::atomic<int> g_inject{0};
 
 // Resolved work decomposition of one call.
 struct Plan {
@@ -169,6 +172,12 @@ using namespace pd;
 
 extern "C" {
 
+void pd_set_wait_limit_ns(unsigned long long ns) {
+  g_wait_limit_ns.store(ns ? ns : kTimeoutNs, std::memory_order_relaxed);
+}
+
+void pd_set_fault_injection(int mode) { g_inject.store(mode == 1 ? 1 : 0, std::memory_order_relaxed); }
+
 const char* pd_status_str(pd_status s) {
   switch (s) {
     case PD_OK: return "ok";
@@ -249,7 +258,8 @@ pd_status decode_paged(const void* q, const void* k_cache, const void* v_cache,
   const double ks = fp8 ? static_cast<double>(dims->k_scale) : 1.0;
   p.sl2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 * ks);
   p.out_scale = fp8 ? dims->v_scale : 1.0f;
-  p.timeout_ns = kTimeoutNs;
+  p.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  p.inject = g_inject.load(std::memory_order_relaxed);
 
   cudaError_t e = launch_decode(dims->D, dims->kv_dtype, pl.nt, tk, tv, p, pl.grid,
                                 static_cast<cudaStream_t>(stream));

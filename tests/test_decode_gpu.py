@@ -280,6 +280,29 @@ def test_device_errors_are_flagged_not_trapped(pd):
     check(w, out, ref_run(w))
 
 
+@pytest.mark.parametrize("shape", [dict(B=4, Hq=24, Hkv=4, D=256, qlen=1),
+                                   dict(B=3, Hq=24, Hkv=4, D=256, qlen=3, kv="fp8")],
+                         ids=["rows_6", "rows_18_pairs"])
+def test_wait_that_nothing_completes_times_out_cleanly(pd, shape):
+    """Failure detection without a GPU fault: with loads suppressed the ring's
+    barriers never complete, every wait runs out after a short limit, the call
+    sets PD_DEVERR_TIMEOUT and returns; the next normal call is correct."""
+    from paged_split_decode_gb300 import binding
+    w = inputs.make_workload(seq_lens=[700, 3000, 16, 0][:shape["B"]], seed=61, **shape)
+    flag = torch.zeros(1, dtype=torch.int32, device=DEV)
+    binding.set_wait_limit_ns(20_000_000)   # 20 ms
+    binding.set_fault_injection(1)
+    try:
+        gpu_run(pd, w, 0, flag=flag)
+    finally:
+        binding.set_fault_injection(0)
+        binding.set_wait_limit_ns(0)
+    assert int(flag.item()) & 4, "the timeout bit must be set"
+    flag.zero_()
+    check(w, gpu_run(pd, w, 0, flag=flag), ref_run(w))
+    assert int(flag.item()) == 0
+
+
 def test_combine_entry_point_matches_oracle(pd):
     w = inputs.make_workload(B=3, Hq=8, Hkv=2, D=128, seq_lens=[500, 0, 77], qlen=2, seed=10)
     _, m, l, O = oracle.decode_paged_split(w.q.numpy(), w.k_cache.numpy(), w.v_cache.numpy(),
