@@ -15,7 +15,11 @@ the source, and wraps its three entry points for numpy arrays:
 * :func:`decode_paged_split` -- the same result reached through contiguous
   block chunks, online softmax inside each chunk and a split-K combine (the
   schedule model of the same section);
-* :func:`combine` -- that combine on its own.
+* :func:`combine` -- that combine on its own;
+* :func:`write_kv_cache` -- the paged KV-cache writer (new tokens into their
+  slots, fp16 copied, fp8 / int8 quantised with the per-cache scale) whose
+  layout the decode reads back, with its quantisers :func:`e4m3fn_encode` and
+  :func:`i8_encode`.
 
 Row ranges are spread over a thread pool; the C code runs without the GIL.
 """
@@ -83,6 +87,12 @@ def _load():
         lib.pdo_decode_paged_split.restype = ctypes.c_int
         lib.pdo_combine.argtypes = [ctypes.c_long, ctypes.c_int, ctypes.c_int, P, P, P, P]
         lib.pdo_combine.restype = ctypes.c_int
+        lib.pdo_e4m3fn_encode.argtypes = [ctypes.c_float]
+        lib.pdo_e4m3fn_encode.restype = ctypes.c_uint8
+        lib.pdo_i8_encode.argtypes = [ctypes.c_float]
+        lib.pdo_i8_encode.restype = ctypes.c_int8
+        lib.pdo_write_kv_cache.argtypes = [ctypes.POINTER(Dims), P, P, P, ctypes.c_long, P, P]
+        lib.pdo_write_kv_cache.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -97,6 +107,16 @@ def e4m3fn_to_f64(code: int) -> float:
 
 def i8_to_f64(code: int) -> float:
     return _load().pdo_i8_to_f64(code)
+
+
+def e4m3fn_encode(t: float) -> int:
+    """e4m3fn code nearest to the fp32 value t (ties to even, saturating)."""
+    return int(_load().pdo_e4m3fn_encode(float(np.float32(t))))
+
+
+def i8_encode(t: float) -> int:
+    """Nearest integer to the fp32 value t (ties to even), clamped to +-127."""
+    return int(_load().pdo_i8_encode(float(np.float32(t))))
 
 
 def default_threads() -> int:
@@ -211,8 +231,41 @@ def combine(m, l, O):
     return out
 
 
-__all__ = ["build", "decode_paged", "decode_paged_split", "combine", "f16_to_f64",
-           "e4m3fn_to_f64", "i8_to_f64", "default_threads"]
+def write_kv_cache(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale=1.0, v_scale=1.0,
+                   kv_fp8=False, kv_int8=False, allow_bad_slots=False):
+    """Paged KV-cache writer, in place on the numpy caches.
+
+    k_new/v_new: fp16 [T, Hkv, D]; slot_mapping: int64 [T] (negative = padding
+    token, skipped); caches [num_blocks, block_size, Hkv, D] fp16, or uint8
+    holding e4m3fn codes (kv_fp8) or int8 codes (kv_int8). A slot beyond the
+    cache raises ValueError, or with ``allow_bad_slots`` is skipped and the
+    call returns False. Returns True when every slot was in range."""
+    lib = _load()
+    kdt = np.uint8 if (kv_fp8 or kv_int8) else np.uint16
+    if not (k_cache.flags.c_contiguous and v_cache.flags.c_contiguous):
+        raise ValueError("caches must be C-contiguous (they are written in place)")
+    kc = k_cache.view(kdt) if k_cache.dtype != kdt else k_cache
+    vc = v_cache.view(kdt) if v_cache.dtype != kdt else v_cache
+    kn = _as_bits(k_new, np.uint16)
+    vn = _as_bits(v_new, np.uint16)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    num_blocks, bs, Hkv, D = kc.shape
+    T = sm.shape[0]
+    assert kn.shape == (T, Hkv, D) and vn.shape == kn.shape and vc.shape == kc.shape
+    dims = Dims(0, 1, Hkv, Hkv, D, bs, num_blocks, 0, 2 if kv_int8 else int(bool(kv_fp8)),
+                float(np.float32(k_scale)), float(np.float32(v_scale)))
+    rc = lib.pdo_write_kv_cache(ctypes.byref(dims), _ptr(kn), _ptr(vn), _ptr(sm), T, _ptr(kc),
+                                _ptr(vc))
+    if rc == -2 and allow_bad_slots:
+        return False
+    if rc != 0:
+        raise ValueError(f"oracle: {_ERRORS.get(rc, rc)}")
+    return True
+
+
+__all__ = ["build", "decode_paged", "decode_paged_split", "combine", "write_kv_cache",
+           "f16_to_f64", "e4m3fn_to_f64", "i8_to_f64", "e4m3fn_encode", "i8_encode",
+           "default_threads"]
 
 if __name__ == "__main__":  # pragma: no cover
     print(build(force="--force" in sys.argv))

@@ -314,3 +314,98 @@ int pdo_decode_paged_split(const pdo_dims* d, const uint16_t* q, const void* k_c
   free(pO);
   return rc;
 }
+
+/*
+ * Quantisers of the paged KV-cache writer. The test plan of the pull request
+ * ("Test Plan": the writer-layout cell) checks that the decode reads back what
+ * the cache writer stored; the writer's arithmetic is not spelled out there,
+ * so these follow the plain reading: a new value x (fp16) is divided by the
+ * cache's scale in IEEE single precision, and the quotient t is stored as the
+ * nearest code.
+ */
+
+/* e4m3fn code nearest to t, found by trying every finite code: ties go to the
+ * even code, anything beyond 448 in magnitude (infinities included) saturates
+ * to +-448, the sign of t (zero included) is kept, NaN gives 0x7F. */
+uint8_t pdo_e4m3fn_encode(float t) {
+  if (isnan(t)) return 0x7f;
+  uint8_t sign = signbit(t) ? 0x80 : 0x00;
+  double a = fabs((double)t);
+  if (isinf(t)) return sign | 0x7e;
+  int best = 0;
+  double best_d = INFINITY;
+  for (int c = 0; c <= 0x7e; ++c) {
+    double d = fabs(pdo_e4m3fn_to_f64((uint8_t)c) - a);
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return sign | (uint8_t)best;
+}
+
+/* Nearest integer to t, ties to even, clamped to [-127, 127]; NaN gives 0. */
+int8_t pdo_i8_encode(float t) {
+  if (isnan(t)) return 0;
+  double v = (double)t;
+  if (v >= 127.0) return 127;
+  if (v <= -127.0) return -127;
+  double f = floor(v);
+  double frac = v - f;
+  double r;
+  if (frac > 0.5)
+    r = f + 1.0;
+  else if (frac < 0.5)
+    r = f;
+  else
+    r = (fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+  return (int8_t)r;
+}
+
+/*
+ * Paged KV-cache writer. New token t in [0, T) carries k_new[t] and v_new[t]
+ * ([T, Hkv, D] fp16 bit patterns) and a slot slot_mapping[t] in the cache:
+ * block slot / block_size, offset slot % block_size. A negative slot marks a
+ * padding token and writes nothing. For every KV head h and dim x of a token:
+ *   fp16 cache:  K[block][offset][h][x] = k_new[t][h][x]        (bit copy)
+ *   fp8 cache:   pdo_e4m3fn_encode(fp32(k_new) / fp32(k_scale))
+ *   int8 cache:  pdo_i8_encode(fp32(k_new) / fp32(k_scale))
+ * and likewise V with v_scale. A slot at or beyond num_blocks * block_size
+ * writes nothing and makes the call return PDO_ERR_BLOCK_ID once every other
+ * token has been written.
+ */
+int pdo_write_kv_cache(const pdo_dims* d, const uint16_t* k_new, const uint16_t* v_new,
+                       const int64_t* slot_mapping, long T, void* k_cache, void* v_cache) {
+  if (!d || T < 0 || d->Hkv < 1 || d->D < 1 || d->block_size < 1 || d->num_blocks < 0 ||
+      d->kv_kind < 0 || d->kv_kind > 2)
+    return PDO_ERR_ARGS;
+  const long row = (long)d->Hkv * d->D;
+  const int64_t cap = (int64_t)d->num_blocks * d->block_size;
+  const float ks = (float)d->k_scale, vs = (float)d->v_scale;
+  int rc = PDO_OK;
+  for (long t = 0; t < T; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= cap) { rc = PDO_ERR_BLOCK_ID; continue; }
+    long blk = (long)(slot / d->block_size), off = (long)(slot % d->block_size);
+    long dst = (blk * d->block_size + off) * row;
+    for (long e = 0; e < row; ++e) {
+      uint16_t kx = k_new[t * row + e], vx = v_new[t * row + e];
+      if (d->kv_kind == 0) {
+        ((uint16_t*)k_cache)[dst + e] = kx;
+        ((uint16_t*)v_cache)[dst + e] = vx;
+      } else {
+        float kq = (float)pdo_f16_to_f64(kx) / ks;
+        float vq = (float)pdo_f16_to_f64(vx) / vs;
+        if (d->kv_kind == 1) {
+          ((uint8_t*)k_cache)[dst + e] = pdo_e4m3fn_encode(kq);
+          ((uint8_t*)v_cache)[dst + e] = pdo_e4m3fn_encode(vq);
+        } else {
+          ((uint8_t*)k_cache)[dst + e] = (uint8_t)pdo_i8_encode(kq);
+          ((uint8_t*)v_cache)[dst + e] = (uint8_t)pdo_i8_encode(vq);
+        }
+      }
+    }
+  }
+  return rc;
+}

@@ -9,6 +9,7 @@ import sys
 import pytest
 
 import test_oracle as pins
+import test_oracle_writer as writer_pins
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -31,6 +32,15 @@ MUTANTS = [
      "double pdo_i8_to_f64(uint8_t c) { return (double)c; }"),
     ("split_chunk_bound", "if (cb1 > first_block + n_blocks) cb1 = first_block + n_blocks;",
      "if (cb1 > first_block + n_blocks - 1) cb1 = first_block + n_blocks - 1;"),
+    ("writer_scale_multiplies", "float kq = (float)pdo_f16_to_f64(kx) / ks;",
+     "float kq = (float)pdo_f16_to_f64(kx) * ks;"),
+    ("e4m3_ties_away", "if (d < best_d || (d == best_d && (c & 1) == 0)) {",
+     "if (d <= best_d) {"),
+    ("i8_ties_up", "r = (fmod(f, 2.0) == 0.0) ? f : f + 1.0;", "r = f + 1.0;"),
+    ("i8_clamp_asymmetric", "if (v <= -127.0) return -127;", "if (v <= -128.0) return -128;"),
+    ("writer_offset_transposed", "long dst = (blk * d->block_size + off) * row;",
+     "long dst = (off * d->num_blocks + blk) * row;"),
+    ("writer_padding_written", "if (slot < 0) continue;", "if (slot < 0) slot = -slot;"),
 ]
 
 
@@ -60,6 +70,11 @@ def _pin_calls():
               for ci in range(len(pins.TINY)) for kv in ("f16", "fp8", "int8")]
     calls += [(pins.test_split_mode_matches_one_shot, {"ci": ci, "kv": "f16"}) for ci in (2, 5)]
     calls += [(pins.test_combine_edge_cases, {}), (pins.test_split_partials_recombine, {})]
+    calls += [(writer_pins.test_e4m3fn_encoder_golden_points, {}),
+              (writer_pins.test_i8_encoder_golden_points, {}),
+              (writer_pins.test_e4m3fn_encoder_matches_torch_cast, {}),
+              (writer_pins.test_i8_encoder_matches_numpy, {})]
+    calls += [(writer_pins.test_writer_layout_and_codes, {"kind": k}) for k in writer_pins.KINDS]
     return calls
 
 
