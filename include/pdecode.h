@@ -78,6 +78,8 @@ typedef enum {
 #define PD_DEVERR_BLOCK_ID 1u /* a block_table entry used by the call is outside [0, num_blocks) */
 #define PD_DEVERR_SEQ_LEN 2u  /* a seq_len is negative or above max_blocks_per_seq*block_size */
 #define PD_DEVERR_TIMEOUT 4u  /* a pipeline wait ran past its limit; the call gave up */
+#define PD_DEVERR_SLOT 8u     /* write_kv_cache: a slot at or beyond num_blocks*block_size */
+#define PD_DEVERR_QUERY_START 16u /* decode_paged_varlen: a sequence's query range is malformed */
 
 /* Shapes of one call.
  *   B                  number of sequences (rows of block_table / seq_lens)
@@ -140,6 +142,29 @@ PD_API pd_status decode_paged(const void* q, const void* k_cache, const void* v_
                        void* workspace, size_t workspace_bytes, uint32_t* error_flag,
                        void* stream);
 
+/* decode_paged with a different number of query tokens per sequence (the
+ * multi-token verify cell of "Test Plan" generalised: a batch mixing plain
+ * decode with speculative verify of varying depth).
+ *   query_start_loc  device int32 [B+1], non-decreasing: sequence b owns rows
+ *                    query_start_loc[b] .. query_start_loc[b+1]-1 of q and
+ *                    out, its qlen_b = query_start_loc[b+1] - query_start_loc[b]
+ *                    tokens at positions seq_lens[b] - qlen_b + i (i < qlen_b)
+ *   num_query_tokens rows of q and out (total over the batch)
+ *   max_qlen         an upper bound of every qlen_b, 1..8; it sizes the
+ *                    kernel (G * max_qlen <= 32) and the workspace:
+ *                    pd_workspace_bytes(dims, max_qlen, num_splits, 0)
+ * Every other argument is decode_paged's. A sequence with qlen_b = 0 writes
+ * nothing; rows of out outside [query_start_loc[0], query_start_loc[B]) are
+ * not written. A range that decreases, exceeds max_qlen or leaves
+ * [0, num_query_tokens) sets PD_DEVERR_QUERY_START and that sequence is
+ * skipped. */
+PD_API pd_status decode_paged_varlen(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_table, const int32_t* seq_lens,
+                                     const int32_t* query_start_loc, int num_query_tokens,
+                                     int max_qlen, float scale, int window, int num_splits,
+                                     void* out, const pd_dims* dims, void* workspace,
+                                     size_t workspace_bytes, uint32_t* error_flag, void* stream);
+
 /* Split-K combine on its own (the combine step of "Purpose" and of the
  * schedule model in "Test Result"). For each of `rows` rows and S partials:
  *   part_m  fp32 [rows, S]     largest score of the chunk, natural-log units
@@ -152,6 +177,28 @@ PD_API pd_status decode_paged(const void* q, const void* k_cache, const void* v_
  * D is 1..1024 and a multiple of 8. */
 PD_API pd_status decode_paged_combine(const float* part_m, const float* part_l, const float* part_o,
                                int rows, int num_splits, int D, void* out, void* stream);
+
+/* Paged KV-cache writer: stores the K and V rows of new tokens where the
+ * decode reads them (opengfx1030/vllm-rdna pull request #33, "Test Plan": the
+ * decode is checked against the paged writer's layout).
+ *   k_new, v_new  fp16 [num_tokens, Hkv, D], 16-byte aligned
+ *   slot_mapping  int64 [num_tokens], device; token t goes to block
+ *                 slot / block_size, offset slot % block_size of both caches;
+ *                 a negative slot is a padding token and writes nothing
+ *   k_cache,      [num_blocks, block_size, Hkv, D] of dims->kv_dtype (16-byte
+ *   v_cache       aligned for fp16, 8-byte for one-byte codes), updated in place
+ *   dims          Hkv, D (a multiple of 8), block_size, num_blocks, kv_dtype,
+ *                 k_scale, v_scale are read; B, Hq, max_blocks_per_seq are not
+ *   error_flag    device uint32 or NULL
+ * fp16 caches receive the input bits unchanged. fp8 / int8 caches receive the
+ * code nearest to the IEEE fp32 quotient x / k_scale (V: v_scale): e4m3fn
+ * with ties to even, saturating at +-448, NaN -> 0x7F; int8 with ties to even,
+ * clamped to [-127, 127], NaN -> 0. A slot at or beyond num_blocks*block_size
+ * writes nothing and sets PD_DEVERR_SLOT. Two tokens with the same slot race
+ * (one of them wins). One launch on `stream`; nothing is allocated. */
+PD_API pd_status write_kv_cache(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                                int num_tokens, void* k_cache, void* v_cache, const pd_dims* dims,
+                                uint32_t* error_flag, void* stream);
 
 /* Failure-detection controls (process-wide, read at each launch; for tests of
  * the error path, not for production use).

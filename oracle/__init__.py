@@ -16,6 +16,8 @@ the source, and wraps its three entry points for numpy arrays:
   block chunks, online softmax inside each chunk and a split-K combine (the
   schedule model of the same section);
 * :func:`combine` -- that combine on its own;
+* :func:`decode_paged_varlen` -- a different query count per sequence, each
+  sequence being the one-shot decode of itself alone;
 * :func:`write_kv_cache` -- the paged KV-cache writer (new tokens into their
   slots, fp16 copied, fp8 / int8 quantised with the per-cache scale) whose
   layout the decode reads back, with its quantisers :func:`e4m3fn_encode` and
@@ -217,6 +219,28 @@ def decode_paged_split(q, k_cache, v_cache, block_table, seq_lens, scale, num_sp
     return (out, m, l, O) if return_partials else out
 
 
+def decode_paged_varlen(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, scale,
+                        window=0, k_scale=1.0, v_scale=1.0, kv_fp8=False, kv_int8=False,
+                        threads=None):
+    """fp64 paged decode with a query count per sequence: sequence b owns rows
+    query_start_loc[b] .. query_start_loc[b+1]-1 of q, and is the one-shot
+    decode of that single sequence with qlen = the row count. Rows outside
+    every sequence stay 0. Returns float64 [T, Hq, D]."""
+    qs = np.asarray(query_start_loc, dtype=np.int64)
+    q = np.asarray(q)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    out = np.zeros(q.shape, dtype=np.float64)
+    for b in range(sl.shape[0]):
+        a, e = int(qs[b]), int(qs[b + 1])
+        if e <= a:
+            continue
+        out[a:e] = decode_paged(q[a:e], k_cache, v_cache, bt[b:b + 1], sl[b:b + 1], scale,
+                                window=window, qlen=e - a, k_scale=k_scale, v_scale=v_scale,
+                                kv_fp8=kv_fp8, kv_int8=kv_int8, threads=threads)
+    return out
+
+
 def combine(m, l, O):
     """fp64 split-K combine: m, l [rows, S] (natural-log m), O [rows, S, D] -> [rows, D]."""
     lib = _load()
@@ -263,7 +287,8 @@ def write_kv_cache(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale=1.0, v_
     return True
 
 
-__all__ = ["build", "decode_paged", "decode_paged_split", "combine", "write_kv_cache",
+__all__ = ["build", "decode_paged", "decode_paged_split", "decode_paged_varlen", "combine",
+           "write_kv_cache",
            "f16_to_f64", "e4m3fn_to_f64", "i8_to_f64", "e4m3fn_encode", "i8_encode",
            "default_threads"]
 

@@ -23,9 +23,11 @@ PD_KV_INT8 = 2
 DEVERR_BLOCK_ID = 1
 DEVERR_SEQ_LEN = 2
 DEVERR_TIMEOUT = 4
+DEVERR_SLOT = 8
+DEVERR_QUERY_START = 16
 
-EXPORTS = ("decode_paged", "decode_paged_combine", "decode_paged_static_scratch",
-           "pd_workspace_bytes", "pd_grid_ctas", "pd_status_str", "pd_set_wait_limit_ns",
+EXPORTS = ("decode_paged", "decode_paged_varlen", "decode_paged_combine", "decode_paged_static_scratch",
+           "write_kv_cache", "pd_workspace_bytes", "pd_grid_ctas", "pd_status_str", "pd_set_wait_limit_ns",
            "pd_set_fault_injection")
 
 
@@ -67,9 +69,15 @@ def load():
                                          ctypes.c_int, P, ctypes.POINTER(PdDims), P,
                                          ctypes.c_size_t, P, P]
             lib.decode_paged.restype = ctypes.c_int
+            lib.decode_paged_varlen.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_float, ctypes.c_int, ctypes.c_int, P,
+                                                ctypes.POINTER(PdDims), P, ctypes.c_size_t, P, P]
+            lib.decode_paged_varlen.restype = ctypes.c_int
             lib.decode_paged_combine.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                  P, P]
             lib.decode_paged_combine.restype = ctypes.c_int
+            lib.write_kv_cache.argtypes = [P, P, P, ctypes.c_int, P, P, ctypes.POINTER(PdDims), P, P]
+            lib.write_kv_cache.restype = ctypes.c_int
             lib.pd_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
             lib.pd_set_wait_limit_ns.restype = None
             lib.pd_set_fault_injection.argtypes = [ctypes.c_int]
@@ -202,6 +210,47 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, ql
     return out
 
 
+def decode_paged_varlen(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, max_qlen,
+                        scale, window=0, num_splits=0, out=None, *, k_scale=1.0, v_scale=1.0,
+                        workspace=None, error_flag=None, stream=None):
+    """Paged decode with qlen_b = query_start_loc[b+1] - query_start_loc[b]
+    query tokens for sequence b (rows query_start_loc[b].. of q and out);
+    returns ``out`` (fp16 [T, Hq, D]; rows outside every sequence's range are
+    left as they were)."""
+    lib = load()
+    kind = kv_kind_of(k_cache)
+    kv_dt = {PD_KV_F16: torch.float16, PD_KV_INT8: torch.int8,
+             PD_KV_FP8_E4M3: (torch.uint8, torch.float8_e4m3fn)}[kind]
+    dims = dims_of(q, k_cache, block_table, max_qlen, None, k_scale, v_scale)
+    if out is None:
+        out = torch.zeros_like(q)
+    if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype:
+        raise ValueError("v_cache must match k_cache in shape and dtype")
+    B = block_table.shape[0]
+    if q.dim() != 3 or seq_lens.numel() != B or query_start_loc.numel() != B + 1:
+        raise ValueError("q must be [T, Hq, D]; seq_lens [B]; query_start_loc [B+1]")
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    need = workspace_bytes(dims, max_qlen, num_splits)
+    if workspace is None:
+        workspace = get_workspace(q.device, need)
+    ws_ptr = 0 if workspace is None else _dev_ptr(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    flag_ptr = None if error_flag is None else _dev_ptr(error_flag, "error_flag", (torch.int32, torch.uint32))
+    rc = lib.decode_paged_varlen(_dev_ptr(q, "q", torch.float16), _dev_ptr(k_cache, "k_cache", kv_dt),
+                                 _dev_ptr(v_cache, "v_cache", kv_dt),
+                                 _dev_ptr(block_table, "block_table", torch.int32),
+                                 _dev_ptr(seq_lens, "seq_lens", torch.int32),
+                                 _dev_ptr(query_start_loc, "query_start_loc", torch.int32),
+                                 int(q.shape[0]), int(max_qlen), float(scale), int(window),
+                                 int(num_splits), _dev_ptr(out, "out", torch.float16),
+                                 ctypes.byref(dims), ws_ptr or None, ws_bytes, flag_ptr, stream)
+    _check(rc, "decode_paged_varlen")
+    return out
+
+
 def decode_paged_combine(part_m, part_l, part_o, out=None, *, stream=None):
     """Split-K combine: part_m/part_l fp32 [rows, S] (natural-log m), part_o fp32
     [rows, S, D] -> fp16 [rows, D]."""
@@ -217,3 +266,34 @@ def decode_paged_combine(part_m, part_l, part_o, out=None, *, stream=None):
                                   int(D), _dev_ptr(out, "out", torch.float16), stream)
     _check(rc, "decode_paged_combine")
     return out
+
+
+def write_kv_cache(k_new, v_new, slot_mapping, k_cache, v_cache, *, k_scale=1.0, v_scale=1.0,
+                   error_flag=None, stream=None):
+    """Store new tokens' K/V rows in the paged caches, in place.
+
+    k_new/v_new: fp16 [T, Hkv, D]; slot_mapping: int64 [T] (negative =
+    padding); caches [num_blocks, block_size, Hkv, D] fp16, uint8 /
+    float8_e4m3fn (e4m3fn codes) or int8 (codes), quantised with
+    ``k_scale``/``v_scale``."""
+    lib = load()
+    kind = kv_kind_of(k_cache)
+    kv_dt = {PD_KV_F16: torch.float16, PD_KV_INT8: torch.int8,
+             PD_KV_FP8_E4M3: (torch.uint8, torch.float8_e4m3fn)}[kind]
+    if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype:
+        raise ValueError("v_cache must match k_cache in shape and dtype")
+    num_blocks, bs, Hkv, D = k_cache.shape
+    T = slot_mapping.numel()
+    if k_new.shape != (T, Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [T, Hkv, D] with T = len(slot_mapping)")
+    dims = make_dims(0, Hkv, Hkv, D, bs, num_blocks, 0, kind == PD_KV_FP8_E4M3, k_scale, v_scale,
+                     kind == PD_KV_INT8)
+    if stream is None:
+        stream = torch.cuda.current_stream(k_cache.device).cuda_stream
+    flag_ptr = None if error_flag is None else _dev_ptr(error_flag, "error_flag", (torch.int32, torch.uint32))
+    rc = lib.write_kv_cache(_dev_ptr(k_new, "k_new", torch.float16),
+                            _dev_ptr(v_new, "v_new", torch.float16),
+                            _dev_ptr(slot_mapping, "slot_mapping", torch.int64), int(T),
+                            _dev_ptr(k_cache, "k_cache", kv_dt), _dev_ptr(v_cache, "v_cache", kv_dt),
+                            ctypes.byref(dims), flag_ptr, stream)
+    _check(rc, "write_kv_cache")

@@ -46,24 +46,26 @@ constexpr int kMaxAutoB = 1024;    // sequences handled by the balanced split
 // Split units are merged by a second kernel: the workspace opens with one
 // descriptor per entry (balanced mode: per CTA range, fixed mode: per unit)
 // naming the split unit whose first piece it holds, then the partials.
-constexpr uint32_t kErrBlockId = 1u, kErrSeqLen = 2u, kErrTimeout = 4u;
+constexpr uint32_t kErrBlockId = 1u, kErrSeqLen = 2u, kErrTimeout = 4u, kErrQueryStart = 16u;
 // Limit of the producer's final drain: every load it issued lands before the
 // CTA exits, whatever the (possibly short) pipeline wait limit.
 constexpr unsigned long long kDrainLimitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeParams {
-  const __half* q;            // [B*qlen, Hq, D]
-  __half* out;                // [B*qlen, Hq, D]
+  const __half* q;            // [total_q, Hq, D]
+  __half* out;                // [total_q, Hq, D]
   const int32_t* block_table; // [B, max_blocks]
   const int32_t* seq_lens;    // [B]
+  const int32_t* q_start;     // [B+1] query rows of each sequence; null: b*qlen, qlen each
+  int total_q;                // rows of q and out
   float* ws_o;                // [slots, RP, D]   partial O (log2-domain weights)
   float* ws_ml;               // [slots, RP, 2]   partial (m, l), m in log2 units
   int4* ws_desc;              // [n_desc] {unit, pieces, slot of piece 0, slot base} or unit -1
   int n_desc;
   int rows_padded;            // RP: rows per partial slot
   uint32_t* error_flag;       // may be null
-  int B, qlen, Hq, Hkv, G, R;
+  int B, qlen, Hq, Hkv, G, R;  // qlen, R: the largest per sequence (R = G*qlen rows per unit)
   int max_blocks, block_size, num_blocks, tiles_per_block;
   int window;                 // <= 0: none
   int num_splits;             // 0: balanced
@@ -99,7 +101,7 @@ __device__ __forceinline__ uint32_t byte_word_prep(uint32_t w) {
   else return w;
 }
 
-template <int D_, int KV_, int NT_, int KG_, int NS_, int MINB_>
+template <int D_, int KV_, int NT_, int KG_, int NS_, int MINB_, int DS_ = (NT_ == 1 ? 1 : 2)>
 struct Cfg {
   static constexpr int D = D_, NT = NT_, KG = KG_, NS = NS_;
   static constexpr int kMinBlocks = MINB_;              // resident CTAs per SM the plan targets
@@ -111,13 +113,15 @@ struct Cfg {
   static constexpr int kSlabBytes = kTileKeys * 128;    // 2 KB, 1024-aligned
   static constexpr int kTileBytes = kSlabs * kSlabBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;    // K tile then V tile
-  // NT == 1: each consumer warp covers all of D for the 8 rows (DS = 1).
-  // NT >= 2: consumer warps come in pairs splitting D in halves; each warp of
-  // a pair covers all NT row tiles and converts only its half of every tile,
-  // and the pair adds their partial scores through shared memory (DS = 2).
-  // NT == 4: two row groups of two row tiles each, so a warp's fragments fit.
-  static constexpr int DS = NT == 1 ? 1 : 2;
-  static constexpr int RG = NT == 4 ? 2 : 1;
+  // DS = 1: each consumer warp covers all of D for its 8-row tiles.
+  // DS = 2 or 4: consumer warps come in groups splitting D into DS parts; each
+  // warp of a group covers every row tile of its row group for its part of D,
+  // widens only its part of a one-byte tile, and the group sums the partial
+  // scores through shared memory in a fixed order (bitwise identical in every
+  // warp of the group). NT == 4 with DS == 2: two row groups of two row tiles,
+  // so a warp's fragments fit.
+  static constexpr int DS = DS_;
+  static constexpr int RG = (NT == 4 && DS == 2) ? 2 : 1;
   static constexpr int NTW = NT / RG;                    // row tiles per warp
   static constexpr int kConsumerWarps = KG * RG * DS;
   static constexpr int kConsumerThreads = kConsumerWarps * 32;
@@ -127,7 +131,9 @@ struct Cfg {
   static constexpr int kMergeOBytes = NT * 8 * kDP * 4;        // one buffer per row tile
   static constexpr int kMergeMLBytes = KG * NT * 8 * 2 * 4;
   static constexpr int kXchgFloats = 32 * 4 * NTW;       // one warp's partial S^T, lane-major
-  static constexpr int kXchgBytes = DS == 2 ? KG * RG * 2 * 2 * kXchgFloats * 4 : 0;
+  static constexpr int kXchgBytes = DS > 1 ? KG * RG * 2 * DS * kXchgFloats * 4 : 0;
+  static_assert(DS == 1 || DS == 2 || DS == 4, "D splits into 1, 2 or 4 parts");
+  static_assert(!FP8 || (D / 16 / DS) % 4 == 0, "one-byte tiles need 64-dim parts");
   static constexpr int kOffMergeO = NS * kStageBytes;
   static constexpr int kOffMergeML = kOffMergeO + kMergeOBytes;
   static constexpr int kOffXchg = (kOffMergeML + kMergeMLBytes + 15) / 16 * 16;
@@ -155,12 +161,34 @@ struct Piece {
   long long unit_start;  // balanced mode: global tile index where the unit begins
   int tile_lo_all;     // keys [tile_lo_all, tile_hi_all] are visible to every query
   int tile_hi_all;     // token of the unit (empty range when hi < lo)
+  int qlen;            // query tokens of sequence b (0: nothing to compute or write)
+  int R;               // G * qlen rows of the unit
+  int q0;              // row of q / out holding the sequence's first query token
 };
+
+// Query tokens of sequence b: rows [q0, q0 + qn) of q and out. With
+// per-sequence starts, a malformed range (decreasing, longer than qlen, or
+// outside [0, total_q)) is reported and the sequence is skipped.
+__device__ __forceinline__ void seq_queries(const DecodeParams& p, int b, bool report, int& q0,
+                                            int& qn) {
+  if (p.q_start == nullptr) {
+    q0 = b * p.qlen;
+    qn = p.qlen;
+    return;
+  }
+  q0 = __ldg(p.q_start + b);
+  qn = __ldg(p.q_start + b + 1) - q0;
+  if (q0 < 0 || qn < 0 || qn > p.qlen || q0 > p.total_q - qn) {
+    if (report && p.error_flag) atomicOr(p.error_flag, kErrQueryStart);
+    q0 = 0;
+    qn = 0;
+  }
+}
 
 // Keys every query token of a sequence of length L sees: token 0 limits the
 // top (position L - qlen), token qlen-1 the window's start.
 __device__ __forceinline__ void common_range(const DecodeParams& p, int L, Piece& pc) {
-  const int hi = L - p.qlen;
+  const int hi = L - pc.qlen;
   const int last = L - 1;
   int lo = 0;
   if (p.window > 0) lo = max(0, last - p.window + 1);
@@ -172,19 +200,21 @@ __device__ __forceinline__ void raise_error(uint32_t* flag, uint32_t bit) {
   if (flag) atomicOr(flag, bit);
 }
 
-// Visible tile span of sequence b: tiles [t0, t0 + n). Validates seq_len.
+// Visible tile span of sequence b: tiles [t0, t0 + n), and its query rows
+// [q0, q0 + qn). Validates seq_len and the query range.
 __device__ __forceinline__ void seq_span(const DecodeParams& p, int b, bool report, int& L, int& t0,
-                                         int& n) {
+                                         int& n, int& q0, int& qn) {
   L = p.seq_lens[b];
   const int cap = p.max_blocks * p.block_size;
   if (L < 0 || L > cap) {
     if (report) raise_error(p.error_flag, kErrSeqLen);
     L = L < 0 ? 0 : cap;
   }
-  if (L == 0) { t0 = 0; n = 0; return; }
+  seq_queries(p, b, report, q0, qn);
+  if (L == 0 || qn == 0) { t0 = 0; n = 0; return; }
   int lo = 0;
   if (p.window > 0) {
-    const int first = L - p.qlen - p.window + 1;  // token 0's first visible key
+    const int first = L - qn - p.window + 1;  // token 0's first visible key
     lo = first > 0 ? first : 0;
   }
   t0 = lo / kTileKeys;
@@ -262,9 +292,10 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
       const long long us = s_pre[b] + static_cast<long long>(kh) * n;
       const long long ue = us + n;
       const long long pe = ue < it.g_end ? ue : it.g_end;
-      int L, t0, nn;
-      seq_span(p, b, false, L, t0, nn);
+      int L, t0, nn, q0, qn;
+      seq_span(p, b, false, L, t0, nn, q0, qn);
       pc.b = b; pc.kh = kh; pc.L = L; pc.unit_t0 = t0; pc.unit = b * p.Hkv + kh;
+      pc.qlen = qn; pc.R = p.G * qn; pc.q0 = q0;
       pc.first_tile = t0 + static_cast<int>(it.g - us);
       pc.ntiles = static_cast<int>(pe - it.g);
       const int cf = it.cp.owner(us), cl = it.cp.owner(ue - 1);
@@ -281,6 +312,9 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
     while (it.zero_b < p.B) {
       const int b = it.zero_b;
       if (s_pre[b + 1] == s_pre[b]) {
+        int q0, qn;
+        seq_queries(p, b, false, q0, qn);
+        pc.qlen = qn; pc.R = p.G * qn; pc.q0 = q0;
         pc.b = b; pc.kh = it.zero_kh; pc.L = 0; pc.unit_t0 = 0; pc.unit = b * p.Hkv + it.zero_kh;
         pc.first_tile = 0; pc.ntiles = 0; pc.npieces = 1; pc.slot = 0; pc.chunk = 0;
         pc.first_slot_cta = 0; pc.unit_start = 0;
@@ -298,8 +332,9 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
     it.piece += C;
     const int u = static_cast<int>(pi / S), s = static_cast<int>(pi % S);
     const int b = u / p.Hkv, kh = u % p.Hkv;
-    int L, t0, n;
-    seq_span(p, b, s == 0 && kh == 0, L, t0, n);
+    int L, t0, n, q0, qn;
+    seq_span(p, b, s == 0 && kh == 0, L, t0, n, q0, qn);
+    pc.qlen = qn; pc.R = p.G * qn; pc.q0 = q0;
     const int chunk = (n + S - 1) / S;
     const int c0 = s * chunk;
     const int c1 = (c0 + chunk < n) ? c0 + chunk : n;
@@ -361,8 +396,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
       const int b = base + lane;
       int v = 0;
       if (b < p.B) {
-        int L, t0, n;
-        seq_span(p, b, blockIdx.x == 0, L, t0, n);
+        int L, t0, n, q0, qn;
+        seq_span(p, b, blockIdx.x == 0, L, t0, n, q0, qn);
         v = n * p.Hkv;
       }
 #pragma unroll
@@ -451,10 +486,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
 
   // -------------------------------------------------------------- consumers
   constexpr int DS = Cfg::DS, NTW = Cfg::NTW, RG = Cfg::RG;
-  const int dh = warp % DS;                   // half of D (DS = 2)
+  const int dh = warp % DS;                   // part of D
   const int rg = (warp / DS) % RG;            // row group: row tiles rg*NTW .. rg*NTW+NTW-1
   const int kg = warp / (DS * RG);            // key group
-  const int pair = kg * RG + rg;              // the D pair this warp belongs to
+  const int pair = kg * RG + rg;              // the D group this warp belongs to
   const int g = lane >> 2, t4 = lane & 3;
   constexpr int KSTEPS = D / 16;
   constexpr int KSW = KSTEPS / DS;             // k-steps of this warp's part of D
@@ -471,9 +506,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
     for (int n = 0; n < NTW; ++n) {
       const int r = (rg * NTW + n) * 8 + g;
       const __half* qrow = nullptr;
-      if (r < p.R && pc.ntiles > 0) {
+      if (r < pc.R && pc.ntiles > 0) {
         const int i = r / p.G, hl = r % p.G;
-        qrow = p.q + (static_cast<long long>(pc.b * p.qlen + i) * p.Hq + pc.kh * p.G + hl) * D;
+        qrow = p.q + (static_cast<long long>(pc.q0 + i) * p.Hq + pc.kh * p.G + hl) * D;
       }
 #pragma unroll
       for (int ksl = 0; ksl < KSW; ++ksl) {
@@ -499,8 +534,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         const int r = (rg * NTW + n) * 8 + 2 * t4 + c;
-        if (r < p.R) {
-          const int pos = pc.L - p.qlen + r / p.G;
+        if (r < pc.R) {
+          const int pos = pc.L - pc.qlen + r / p.G;
           hi_r[n][c] = pos;
           lo_r[n][c] = (p.window > 0) ? max(0, pos - p.window + 1) : 0;
         } else {
@@ -523,7 +558,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
       if (!ok) {
         // gave up: skip the work but keep the pair's barrier sequence, so the
         // partner warp (whose own wait may have succeeded) is never stranded
-        if constexpr (DS == 2) named_bar_sync(2 + pair, 64);
+        if constexpr (DS > 1) named_bar_sync(2 + pair, DS * 32);
         continue;
       }
       const uint32_t kb = smem_u32(smem + stage * Cfg::kStageBytes);
@@ -590,19 +625,24 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
       for (int n = 0; n < NTW; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sc[n][e] = sa[n][e] + sb[n][e];
-      if constexpr (DS == 2) {
-        // add the other half's partial scores (a + b == b + a: both warps of the
-        // pair end up with bitwise identical scores)
-        float* mine = xchg + ((pair * 2 + (qq & 1)) * 2 + dh) * Cfg::kXchgFloats + lane * 4 * NTW;
-        float* other = xchg + ((pair * 2 + (qq & 1)) * 2 + (dh ^ 1)) * Cfg::kXchgFloats + lane * 4 * NTW;
+      if constexpr (DS > 1) {
+        // sum the group's partial scores in part order (every warp of the group
+        // evaluates the same expression, so all hold identical scores)
+        float* grp = xchg + (pair * 2 + (qq & 1)) * DS * Cfg::kXchgFloats + lane * 4 * NTW;
 #pragma unroll
         for (int n = 0; n < NTW; ++n)
-          *reinterpret_cast<float4*>(mine + 4 * n) = make_float4(sc[n][0], sc[n][1], sc[n][2], sc[n][3]);
-        named_bar_sync(2 + pair, 64);
+          *reinterpret_cast<float4*>(grp + dh * Cfg::kXchgFloats + 4 * n) =
+              make_float4(sc[n][0], sc[n][1], sc[n][2], sc[n][3]);
+        named_bar_sync(2 + pair, DS * 32);
 #pragma unroll
         for (int n = 0; n < NTW; ++n) {
-          const float4 v = *reinterpret_cast<const float4*>(other + 4 * n);
-          sc[n][0] += v.x; sc[n][1] += v.y; sc[n][2] += v.z; sc[n][3] += v.w;
+          float4 t = *reinterpret_cast<const float4*>(grp + 4 * n);
+#pragma unroll
+          for (int part = 1; part < DS; ++part) {
+            const float4 v = *reinterpret_cast<const float4*>(grp + part * Cfg::kXchgFloats + 4 * n);
+            t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
+          }
+          sc[n][0] = t.x; sc[n][1] = t.y; sc[n][2] = t.z; sc[n][3] = t.w;
         }
       }
       // per row tile: mask, online softmax, P^T fragments; C layout of S^T:
@@ -660,16 +700,29 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           }
       }
 
-      // O^T += V^T P^T over this warp's m-tiles
+      // O^T += V^T P^T over this warp's m-tiles. Keys at or past the sequence
+      // end (the unwritten tail of its last block) may hold any bits, NaN
+      // included: their V is zeroed so that P = 0 there never meets 0 * NaN.
+      const bool tail = key0 + kTileKeys > pc.L;
       if constexpr (!FP8) {
         const int key = (lane & 7) + (lane >> 4) * 8;
         const uint32_t rowb = vb + key * 128;
+        // A = V^T fragment: a[0], a[1] hold keys 2t4, 2t4+1; a[2], a[3] keys 2t4+8, 2t4+9
+        uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
+        if (tail) {
+          const int k0 = key0 + 2 * t4;
+          vm01 = (k0 < pc.L ? 0x0000ffffu : 0u) | (k0 + 1 < pc.L ? 0xffff0000u : 0u);
+          vm23 = (k0 + 8 < pc.L ? 0x0000ffffu : 0u) | (k0 + 9 < pc.L ? 0xffff0000u : 0u);
+        }
 #pragma unroll
         for (int mtl = 0; mtl < MTW; ++mtl) {
           const int mt = dh * MTW + mtl;
           const int slab = mt >> 2, chunk = (mt & 3) * 2 + ((lane >> 3) & 1);
           uint32_t a[4];
           ldsm_x4_trans(rowb + slab * Cfg::kSlabBytes + ((chunk ^ (key & 7)) << 4), a);
+          if (tail) {
+            a[0] &= vm01; a[1] &= vm01; a[2] &= vm23; a[3] &= vm23;
+          }
 #pragma unroll
           for (int n = 0; n < NTW; ++n) mma_16816(o[mtl][n], a, pb0[n], pb1[n]);
         }
@@ -690,6 +743,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wB) : "r"(sb0 + kB * 128 + ((chunk ^ (kB & 7)) << 4)));
           asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wC) : "r"(sb0 + kC * 128 + ((chunk ^ (kC & 7)) << 4)));
           asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wD) : "r"(sb0 + kD * 128 + ((chunk ^ (kD & 7)) << 4)));
+          if (tail) {  // code 0 is the value 0 in both byte formats
+            if (key0 + kA >= pc.L) wA = 0u;
+            if (key0 + kB >= pc.L) wB = 0u;
+            if (key0 + kC >= pc.L) wC = 0u;
+            if (key0 + kD >= pc.L) wD = 0u;
+          }
           wA = byte_word_prep<Cfg::KV>(wA); wB = byte_word_prep<Cfg::KV>(wB);
           wC = byte_word_prep<Cfg::KV>(wC); wD = byte_word_prep<Cfg::KV>(wD);
           const uint32_t ab01 = prmt(wA, wB, 0x5140u), ab23 = prmt(wA, wB, 0x7362u);
@@ -787,7 +846,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
     const int tid = threadIdx.x;
     constexpr int DCH = D / 8;  // 8-dim chunks per row
     const bool direct = pc.npieces == 1;
-    for (int item = tid; item < p.R * DCH; item += Cfg::kConsumerThreads) {
+    for (int item = tid; item < pc.R * DCH; item += Cfg::kConsumerThreads) {
       const int r = item / DCH, dc = item % DCH;
       const int rnt = r >> 3, rr = r & 7;
       float M = -INFINITY;
@@ -804,7 +863,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
       const float4 v1 = *reinterpret_cast<const float4*>(src + 4);
       if (direct) {
         const int i = r / p.G, hl = r % p.G;
-        __half* dst = p.out + (static_cast<long long>(pc.b * p.qlen + i) * p.Hq + pc.kh * p.G + hl) * D + dc * 8;
+        __half* dst = p.out + (static_cast<long long>(pc.q0 + i) * p.Hq + pc.kh * p.G + hl) * D + dc * 8;
         const float inv = (Ls > 0.f) ? p.out_scale / Ls : 0.f;
         uint4 v;
         v.x = pack_half2(v0.x * inv, v0.y * inv);
@@ -863,14 +922,18 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
   if (u < 0 || P <= 1) return;
   const int step = p.num_splits == 0 ? 2 : 1;
   const int R = p.R, RP = p.rows_padded;
+  const int b = u / p.Hkv, kh = u % p.Hkv;
+  int q0, qn;
+  seq_queries(p, b, false, q0, qn);
   const int items = R * 8;
   const int PG = 256 / items > 0 ? 256 / items : 1;
   const int t = threadIdx.x;
   const int item = t % items, pg = t / items;
   const int r = item >> 3, dim0 = blockIdx.y * 32 + (item & 7) * 4;
+  const bool live = r < p.G * qn;  // rows of the sequence's query tokens
   float m_run = -INFINITY, l_run = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (pg < PG) {
+  if (pg < PG && live) {
     for (int k0 = pg; k0 < P; k0 += 4 * PG) {
       float2 ml[4];
       float4 v[4];
@@ -906,7 +969,7 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
   s_l[t] = l_run;
   s_o[t] = acc;
   __syncthreads();
-  if (pg != 0 || t >= items) return;
+  if (pg != 0 || t >= items || !live) return;
   float M = -INFINITY;
   for (int g2 = 0; g2 < PG; ++g2) M = fmaxf(M, s_m[g2 * items + item]);
   float L = 0.f;
@@ -920,9 +983,8 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
     o.x += w * a.x; o.y += w * a.y; o.z += w * a.z; o.w += w * a.w;
   }
   const float inv = (L > 0.f) ? p.out_scale / L : 0.f;
-  const int b = u / p.Hkv, kh = u % p.Hkv;
   const int i = r / p.G, hl = r % p.G;
-  __half* dst = p.out + (static_cast<long long>(b * p.qlen + i) * p.Hq + kh * p.G + hl) * D + dim0;
+  __half* dst = p.out + (static_cast<long long>(q0 + i) * p.Hq + kh * p.G + hl) * D + dim0;
   uint2 o2;
   o2.x = pack_half2(o.x * inv, o.y * inv);
   o2.y = pack_half2(o.z * inv, o.w * inv);

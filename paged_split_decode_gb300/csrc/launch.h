@@ -69,15 +69,15 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
 // MINB CTAs share one SM's 228 KiB (1 KiB of it reserved per CTA; at most
 // 227 KiB for one CTA).
 constexpr int smem_limit(int minb) { return minb == 1 ? 227 * 1024 : 228 * 1024 / minb - 1024; }
-template <int D, int KV, int NT, int KG, int MINB, int NS = 32>
+template <int D, int KV, int NT, int KG, int MINB, int DS, int NS = 32>
 constexpr int ring_stages() {
-  if constexpr (NS <= 2 || Cfg<D, KV, NT, KG, NS, MINB>::kSmemBytes <= smem_limit(MINB))
+  if constexpr (NS <= 2 || Cfg<D, KV, NT, KG, NS, MINB, DS>::kSmemBytes <= smem_limit(MINB))
     return NS;
   else
-    return ring_stages<D, KV, NT, KG, MINB, NS - 1>();
+    return ring_stages<D, KV, NT, KG, MINB, DS, NS - 1>();
 }
-template <int D, int KV, int NT, int KG, int MINB>
-using CfgFor = Cfg<D, KV, NT, KG, ring_stages<D, KV, NT, KG, MINB>(), MINB>;
+template <int D, int KV, int NT, int KG, int MINB, int DS = (NT == 1 ? 1 : 2)>
+using CfgFor = Cfg<D, KV, NT, KG, ring_stages<D, KV, NT, KG, MINB, DS>(), MINB, DS>;
 
 template <class Cfg>
 bool shape_of(KernelShape* out) {

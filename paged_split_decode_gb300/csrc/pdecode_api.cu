@@ -204,19 +204,28 @@ int pd_grid_ctas(const pd_dims* dims, int qlen, int num_splits, int sm_count) {
   return pl.grid;
 }
 
-pd_status decode_paged(const void* q, const void* k_cache, const void* v_cache,
-                       const int32_t* block_table, const int32_t* seq_lens, float scale,
-                       int window, int qlen, int num_splits, void* out, const pd_dims* dims,
-                       void* workspace, size_t workspace_bytes, uint32_t* error_flag,
-                       void* stream) {
+}  // extern "C"
+
+namespace {
+
+// decode_paged and decode_paged_varlen: q_start null means B sequences of qlen
+// query tokens each (total_q = B * qlen); otherwise sequence b owns rows
+// [q_start[b], q_start[b+1]) of q and out, at most qlen of them.
+pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_table, const int32_t* seq_lens, const int32_t* q_start,
+                      int total_q, float scale, int window, int qlen, int num_splits, void* out,
+                      const pd_dims* dims, void* workspace, size_t workspace_bytes,
+                      uint32_t* error_flag, void* stream) {
   pd_status st = check_dims(dims, qlen);
   if (st != PD_OK) return st;
   if (num_splits < 0 || !std::isfinite(scale)) return PD_ERR_SHAPE;
-  if (dims->B == 0) return PD_OK;
+  if (total_q < 0 || static_cast<long long>(total_q) * dims->Hq > (1ll << 31) - 1)
+    return q_start ? PD_ERR_SHAPE : PD_ERR_UNSUPPORTED;
+  if (dims->B == 0 || total_q == 0) return PD_OK;
   if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return PD_ERR_NULL;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
-      (reinterpret_cast<uintptr_t>(error_flag) & 3u))
+      (reinterpret_cast<uintptr_t>(q_start) & 3u) || (reinterpret_cast<uintptr_t>(error_flag) & 3u))
     return PD_ERR_ALIGN;
   if (dims->num_blocks == 0) return PD_ERR_SHAPE;
   Plan pl;
@@ -236,6 +245,8 @@ pd_status decode_paged(const void* q, const void* k_cache, const void* v_cache,
   p.out = static_cast<__half*>(out);
   p.block_table = block_table;
   p.seq_lens = seq_lens;
+  p.q_start = q_start;
+  p.total_q = total_q;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   p.ws_desc = pl.bytes ? reinterpret_cast<int4*>(ws) : nullptr;
   p.n_desc = static_cast<int>(pl.n_desc);
@@ -266,6 +277,36 @@ pd_status decode_paged(const void* q, const void* k_cache, const void* v_cache,
   if (e == cudaSuccess && pl.n_desc > 0)
     e = launch_split_combine(dims->D, p, static_cast<int>(pl.n_desc), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PD_OK : PD_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+pd_status decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_table, const int32_t* seq_lens, float scale,
+                       int window, int qlen, int num_splits, void* out, const pd_dims* dims,
+                       void* workspace, size_t workspace_bytes, uint32_t* error_flag,
+                       void* stream) {
+  if (!dims) return PD_ERR_NULL;
+  const long long total = static_cast<long long>(dims->B) * (qlen > 0 ? qlen : 0);
+  if (total > (1ll << 31) - 1) return PD_ERR_UNSUPPORTED;
+  return decode_impl(q, k_cache, v_cache, block_table, seq_lens, nullptr, static_cast<int>(total),
+                     scale, window, qlen, num_splits, out, dims, workspace, workspace_bytes,
+                     error_flag, stream);
+}
+
+pd_status decode_paged_varlen(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_table, const int32_t* seq_lens,
+                              const int32_t* query_start_loc, int num_query_tokens, int max_qlen,
+                              float scale, int window, int num_splits, void* out,
+                              const pd_dims* dims, void* workspace, size_t workspace_bytes,
+                              uint32_t* error_flag, void* stream) {
+  if (!dims) return PD_ERR_NULL;
+  if (dims->B > 0 && num_query_tokens > 0 && !query_start_loc) return PD_ERR_NULL;
+  return decode_impl(q, k_cache, v_cache, block_table, seq_lens, query_start_loc,
+                     num_query_tokens, scale, window, max_qlen, num_splits, out, dims, workspace,
+                     workspace_bytes, error_flag, stream);
 }
 
 }  // extern "C"

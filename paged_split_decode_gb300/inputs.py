@@ -20,7 +20,13 @@ request #33, "Test Plan" step 3, and the geometry of its results comment):
   contiguous run of blocks after sequence b-1's. Table entries past a
   sequence's last block are -1, so reading one is an error the kernel reports.
 * Every slot of every pool block holds a drawn value, including the slots
-  after a sequence's last key (the stale tail of a partly filled block).
+  after a sequence's last key (the stale tail of a partly filled block);
+  optionally that tail holds NaN patterns instead.
+* KV-cache writer inputs: new K/V rows N(0, sigma) in fp16 for T tokens, a
+  slot per token drawn without repetition from the cache's slots (a random
+  permutation), every ``pad_every``-th token a padding token (slot -1), and
+  optionally a sprinkle of special fp16 values (zeros of both signs,
+  infinities, NaN, the largest finite and subnormal values).
 """
 from __future__ import annotations
 
@@ -50,6 +56,9 @@ class Workload:
     k_scale: float = 1.0
     v_scale: float = 1.0
     meta: dict = field(default_factory=dict)
+    # per-sequence query counts: sequence b owns rows q_start[b]..q_start[b+1]-1
+    # of q (int32 [B+1]); None = qlen rows each. qlen is then the largest count.
+    q_start: torch.Tensor | None = None
 
     @property
     def B(self):
@@ -120,7 +129,10 @@ def make_block_table(gen, seq_lens, max_blocks_per_seq, layout="permuted", pool_
 
 def make_workload(*, B, Hq, Hkv, D, seq_lens, qlen=1, block_size=BLOCK_SIZE, layout="permuted",
                   window=0, kv="f16", seed=0, scale=None, num_splits=0, max_blocks_per_seq=None,
-                  pool_blocks=None, name="custom") -> Workload:
+                  pool_blocks=None, name="custom", stale="drawn") -> Workload:
+    """``stale="nan"`` overwrites, in each sequence's last block, the slots past
+    its last key with NaN bit patterns (the unwritten tail of a block may hold
+    anything); int8 codes have no NaN, so they get -128 there."""
     gen = torch.Generator().manual_seed(int(seed))
     seq_lens = [int(x) for x in seq_lens]
     if max_blocks_per_seq is None:
@@ -143,6 +155,20 @@ def make_workload(*, B, Hq, Hkv, D, seq_lens, qlen=1, block_size=BLOCK_SIZE, lay
         k_scale = v_scale = 1.0
     else:
         raise ValueError(kv)
+    if stale == "nan":
+        for b, L in enumerate(seq_lens):
+            if L % block_size == 0 or L == 0:
+                continue
+            blk = int(table[b, (L - 1) // block_size])
+            for c in (k_cache, v_cache):
+                if c.dtype == torch.float16:
+                    c.view(torch.int16)[blk, L % block_size:] = 0x7E00
+                elif kv == "fp8":
+                    c[blk, L % block_size:] = 0x7F
+                else:
+                    c[blk, L % block_size:] = 0x80
+    elif stale != "drawn":
+        raise ValueError(stale)
     return Workload(name=name, q=q, k_cache=k_cache, v_cache=v_cache, block_table=table,
                     seq_lens=torch.tensor(seq_lens, dtype=torch.int32),
                     scale=float(scale if scale is not None else 1.0 / math.sqrt(D)),
@@ -150,6 +176,24 @@ def make_workload(*, B, Hq, Hkv, D, seq_lens, qlen=1, block_size=BLOCK_SIZE, lay
                     kv_int8=kv_int8,
                     k_scale=k_scale, v_scale=v_scale,
                     meta=dict(layout=layout, seed=int(seed), kv=kv))
+
+
+def make_varlen_workload(*, qlens, seed=0, name="varlen", **kw) -> Workload:
+    """A batch whose sequences carry different numbers of query tokens: the
+    caches and tables as make_workload draws them, Q redrawn as
+    [sum(qlens), Hq, D] with sequence b owning the rows after sequence b-1's."""
+    qlens = [int(x) for x in qlens]
+    w = make_workload(seed=seed, name=name, qlen=1, **kw)
+    assert len(qlens) == w.B
+    gen = torch.Generator().manual_seed(int(seed) + 7919)
+    starts = [0]
+    for n in qlens:
+        starts.append(starts[-1] + n)
+    w.q = _normal(gen, (starts[-1], w.Hq, w.D)).to(torch.float16)
+    w.q_start = torch.tensor(starts, dtype=torch.int32)
+    w.qlen = max(qlens + [1])
+    w.meta["qlens"] = qlens
+    return w
 
 
 # ---- the five named workloads ------------------------------------------------
@@ -190,3 +234,41 @@ def verify_fp8(B=8, seed=1239, seq_len=8192) -> Workload:
     """B=8, Hq=24, Hkv=4, D=256, qlen=3 causal, L=8192, e4m3fn KV with per-cache scales."""
     return make_workload(B=B, Hq=24, Hkv=4, D=256, seq_lens=[seq_len] * B, qlen=3, kv="fp8",
                          seed=seed, name=f"verify3_fp8_d256_L{seq_len}_b{B}")
+
+
+@dataclass
+class WriterInputs:
+    k_new: torch.Tensor        # fp16 [T, Hkv, D]
+    v_new: torch.Tensor        # fp16 [T, Hkv, D]
+    slot_mapping: torch.Tensor  # int64 [T]; -1 = padding token
+    num_blocks: int
+    block_size: int
+
+
+_SPECIAL_F16 = (0x0000, 0x8000, 0x7C00, 0xFC00, 0x7E00, 0x7BFF, 0xFBFF, 0x0001, 0x8001, 0x03FF,
+                0x0400, 0x3C00, 0xBC00)
+
+
+def make_writer_inputs(T, Hkv, D, num_blocks, block_size=BLOCK_SIZE, seed=0, sigma=1.0,
+                       pad_every=0, specials=False) -> WriterInputs:
+    """New tokens for the paged KV-cache writer (see the module recipe)."""
+    g = torch.Generator().manual_seed(seed)
+    k = (torch.randn((T, Hkv, D), generator=g) * sigma).half()
+    v = (torch.randn((T, Hkv, D), generator=g) * sigma).half()
+    if specials and T > 0:
+        sp = torch.tensor(_SPECIAL_F16, dtype=torch.int32).to(torch.int16).view(torch.float16)
+        for x in (k, v):
+            flat = x.view(-1)
+            idx = torch.randint(0, flat.numel(), (4 * len(_SPECIAL_F16),), generator=g)
+            flat[idx] = sp.repeat(4)
+    slots = torch.randperm(num_blocks * block_size, generator=g)[:T].to(torch.int64)
+    assert slots.numel() == T, "more tokens than cache slots"
+    if pad_every > 0:
+        slots[::pad_every] = -1
+    return WriterInputs(k, v, slots, num_blocks, block_size)
+
+
+def all_f16_patterns(Hkv=1, D=256) -> torch.Tensor:
+    """Every fp16 bit pattern once, as [65536 / (Hkv*D), Hkv, D] fp16."""
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    return bits.view(torch.float16).reshape(-1, Hkv, D).clone()

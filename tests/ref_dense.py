@@ -39,7 +39,9 @@ def visibility(L, qlen, window):
 
 
 def attention(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, qlen=1,
-              kv_fp8=False, k_scale=1.0, v_scale=1.0, kv_int8=False):
+              kv_fp8=False, k_scale=1.0, v_scale=1.0, kv_int8=False, q_start=None):
+    """q_start (optional, [B+1]): sequence b owns rows q_start[b]..q_start[b+1]-1
+    and has that many query tokens; otherwise every sequence has qlen."""
     qf = np.asarray(q).astype(np.float16).astype(np.float64)
     Kc = decode_cache(k_cache, kv_fp8, k_scale, kv_int8)
     Vc = decode_cache(v_cache, kv_fp8, v_scale, kv_int8)
@@ -50,14 +52,15 @@ def attention(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, qlen=
     out = np.zeros_like(qf)
     for b in range(B):
         L = int(seq_lens[b])
-        if L <= 0:
+        r0, n = (b * qlen, qlen) if q_start is None else (int(q_start[b]), int(q_start[b + 1]) - int(q_start[b]))
+        if L <= 0 or n <= 0:
             continue
         Kd = dense_kv(Kc, block_table, b, L)  # [L, Hkv, D]
         Vd = dense_kv(Vc, block_table, b, L)
         Kh = np.repeat(Kd, G, axis=1)           # [L, Hq, D]
         Vh = np.repeat(Vd, G, axis=1)
-        vis = visibility(L, qlen, window)       # [qlen, L]
-        qb = qf[b * qlen:(b + 1) * qlen]        # [qlen, Hq, D]
+        vis = visibility(L, n, window)          # [n, L]
+        qb = qf[r0:r0 + n]                      # [n, Hq, D]
         s = scale * np.einsum("ihd,jhd->ihj", qb, Kh)
         s = np.where(vis[:, None, :], s, -np.inf)
         m = s.max(axis=-1, keepdims=True)
@@ -65,5 +68,5 @@ def attention(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, qlen=
         w = np.where(seen, np.exp(s - np.where(seen, m, 0.0)), 0.0)
         den = w.sum(axis=-1, keepdims=True)
         o = np.einsum("ihj,jhd->ihd", w, Vh) / np.where(den > 0, den, 1.0)
-        out[b * qlen:(b + 1) * qlen] = np.where(seen, o, 0.0)
+        out[r0:r0 + n] = np.where(seen, o, 0.0)
     return out

@@ -158,6 +158,28 @@ def test_edge_cases(pd, name, kw, S):
     check(w, gpu_run(pd, w, S), ref_run(w))
 
 
+STALE = [
+    ("f16_rows_6", dict(B=4, Hq=24, Hkv=4, D=256, seq_lens=[1, 17, 4001, 250])),
+    ("f16_rows_18_window", dict(B=3, Hq=24, Hkv=4, D=256, qlen=3, window=100,
+                                seq_lens=[2, 333, 1029])),
+    ("f16_d128_rows_8", dict(B=3, Hq=32, Hkv=8, D=128, seq_lens=[7, 90, 700])),
+    ("fp8_rows_6", dict(B=3, Hq=24, Hkv=4, D=256, kv="fp8", seq_lens=[3, 4001, 250])),
+    ("fp8_d128_rows_24", dict(B=2, Hq=8, Hkv=1, D=128, kv="fp8", qlen=3, seq_lens=[5, 301])),
+    ("int8_rows_32", dict(B=2, Hq=8, Hkv=1, D=256, kv="int8", qlen=4, seq_lens=[700, 91])),
+]
+
+
+@pytest.mark.parametrize("S", [0, 1, 5])
+@pytest.mark.parametrize("name,kw", STALE, ids=[e[0] for e in STALE])
+def test_stale_block_tail_is_never_read(pd, name, kw, S):
+    """The slots past each sequence's last key in its last block hold NaN
+    patterns (the unwritten tail of a block may hold anything): the output
+    must equal the oracle, which never reads them."""
+    w = inputs.make_workload(seed=zlib.crc32(name.encode()) % 10000 + 7, name=name, stale="nan",
+                             **kw)
+    check(w, gpu_run(pd, w, S), ref_run(w))
+
+
 def test_one_workspace_across_changing_shapes(pd):
     """One workspace buffer serves calls of different shapes back to back: every
     call writes the descriptors and partials it reads."""
