@@ -220,7 +220,7 @@ class DeviceWorkload:
     device from a seeded generator; the timed path does not look at them."""
 
     def __init__(self, device, l2_bytes, seed, B, Hq, Hkv, Dh, seq_lens, qlen=1, window=0,
-                 kv="f16", layout="permuted", bs=BS, max_blocks=None):
+                 kv="f16", layout="permuted", bs=BS, max_blocks=None, qlens=None):
         gen = torch.Generator().manual_seed(seed)
         need = [(L + bs - 1) // bs for L in seq_lens]
         self.max_blocks = max_blocks or max(need + [1])
@@ -258,7 +258,17 @@ class DeviceWorkload:
             self.k = torch.randn(shape, generator=dg, device=device, dtype=torch.float32).to(torch.float16)
             self.v = torch.randn(shape, generator=dg, device=device, dtype=torch.float32).to(torch.float16)
             self.k_scale = self.v_scale = 1.0
-        self.q = torch.randn((B * qlen, Hq, Dh), generator=dg, device=device,
+        self.q_start = None
+        if qlens is not None:  # a query count per sequence (rows q_start[b]..q_start[b+1]-1)
+            starts = [0]
+            for n in qlens:
+                starts.append(starts[-1] + n)
+            self.q_start = torch.tensor(starts, dtype=torch.int32, device=device)
+            qlen = max(qlens)
+            rows = starts[-1]
+        else:
+            rows = B * qlen
+        self.q = torch.randn((rows, Hq, Dh), generator=dg, device=device,
                              dtype=torch.float32).to(torch.float16)
         self.seq_lens = torch.tensor(seq_lens, dtype=torch.int32, device=device)
         self.out = torch.empty_like(self.q)
@@ -278,6 +288,12 @@ def time_workload(wl, num_splits, steps, warmup, device, world, sample_clocks=Fa
     flag = torch.zeros(1, dtype=torch.int32, device=device)
 
     def call(r):
+        if wl.q_start is not None:
+            pd.decode_paged_varlen(wl.q, wl.k, wl.v, wl.tables[r % wl.n_rot], wl.seq_lens,
+                                   wl.q_start, wl.qlen, wl.scale, wl.window, num_splits, out=wl.out,
+                                   k_scale=wl.k_scale, v_scale=wl.v_scale, workspace=ws,
+                                   error_flag=flag)
+            return
         pd.decode_paged(wl.q, wl.k, wl.v, wl.tables[r % wl.n_rot], wl.seq_lens, wl.scale, wl.window,
                         wl.qlen, num_splits, out=wl.out, k_scale=wl.k_scale, v_scale=wl.v_scale,
                         workspace=ws, error_flag=flag)
@@ -361,10 +377,79 @@ def other_workloads(device, l2, seed, only=None):
         lambda: DeviceWorkload(device, l2, seed + 96, 32, 24, 4, 256, [4096] * 32, kv="fp8"), 0)
     add("gqa6_d256_L4096_b32_int8",
         lambda: DeviceWorkload(device, l2, seed + 95, 32, 24, 4, 256, [4096] * 32, kv="int8"), 0)
+    gq = torch.Generator().manual_seed(seed + 94)
+    qlens = torch.randint(1, 5, (32,), generator=gq).tolist()
+    add("varlen_q1to4_d256_L4096_b32",
+        lambda: DeviceWorkload(device, l2, seed + 94, 32, 24, 4, 256, [4096] * 32, qlens=qlens), 0)
     for name, make, S in full:
         if only is None or name == only:
             yield name, make(), S
 
+
+
+class WriterWorkload:
+    """The paged KV-cache writer storing T new tokens (fp16 [T, Hkv, D] K and
+    V) into a cache pool at least 4x L2; each step takes the next of n_rot
+    disjoint slot mappings and the next of two input sets, so the written
+    lines and the read inputs are cold in L2."""
+
+    def __init__(self, device, l2_bytes, seed, T, Hkv, Dh, kv="f16", bs=BS):
+        gen = torch.Generator(device=device).manual_seed(seed)
+        elem = 1 if kv in ("fp8", "int8") else 2
+        row = Hkv * Dh
+        self.n_rot = max(2, -(-4 * l2_bytes // (T * row * elem * 2)))
+        slots = self.n_rot * T
+        self.num_blocks = -(-slots // bs)
+        shape = (self.num_blocks, bs, Hkv, Dh)
+        dt = {"f16": torch.float16, "fp8": torch.uint8, "int8": torch.int8}[kv]
+        self.k = torch.empty(shape, dtype=dt, device=device)
+        self.v = torch.empty(shape, dtype=dt, device=device)
+        perm = torch.randperm(self.num_blocks * bs, generator=gen, device=device)[:slots]
+        self.maps = [perm[r * T:(r + 1) * T].to(torch.int64).contiguous() for r in range(self.n_rot)]
+        self.inputs = [(torch.randn((T, Hkv, Dh), generator=gen, device=device).half(),
+                        torch.randn((T, Hkv, Dh), generator=gen, device=device).half())
+                       for _ in range(2)]
+        self.scale = 1.0 if kv == "f16" else 1.0 / 64
+        self.bytes = T * row * (2 * 2 + elem * 2)  # read K and V fp16, write both caches
+
+
+def time_writer(wl, steps, warmup, device, world):
+    import paged_split_decode_gb300 as pd
+    stream = torch.cuda.Stream(device)
+    flag = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def call(r):
+        kn, vn = wl.inputs[r % 2]
+        pd.write_kv_cache(kn, vn, wl.maps[r % wl.n_rot], wl.k, wl.v, k_scale=wl.scale,
+                          v_scale=wl.scale, error_flag=flag)
+
+    with torch.cuda.stream(stream):
+        for r in range(warmup):
+            call(r)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for r in range(steps):
+            call(warmup + r)
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        graph.replay()
+        end.record(stream)
+        end.synchronize()
+    barrier(world)
+    if int(flag.item()) != 0:
+        raise RuntimeError(f"writer error flag {int(flag.item())}")
+    del graph
+    return start.elapsed_time(end)
+
+
+def writer_workloads(device, l2, seed):
+    """Prefill-sized writes: 32768 tokens of the D=256 GQA 6:1 geometry (Hkv=4)."""
+    for kv in ("f16", "fp8", "int8"):
+        yield f"kv_writer_{kv}_T32768_h4_d256", WriterWorkload(device, l2, seed, 32768, 4, 256, kv)
 
 
 def time_e2e(B, steps, warmup, device, seed, world):
@@ -557,7 +642,19 @@ def main():
                             "us_per_call": round(cper * 1e3, 3), "kv_gbs": round(cg, 1),
                             "frac_of_peak": round(cg / peak, 4), "kv_bytes": wl.kv_bytes,
                             "grid_ctas": grid, "steps": small_steps})
-        torch.cuda.empty_cache()
+            del wl
+            torch.cuda.empty_cache()
+        for name, wwl in writer_workloads(device, l2, 7000 + 17 * rank):
+            wms = max_over_ranks(time_writer(wwl, small_steps, args.warmup, device, world), world,
+                                 device)
+            wper = wms / small_steps
+            wg = wwl.bytes / (wper * 1e-3) / 1e9
+            configs.append({"workload": name, "us_per_call": round(wper * 1e3, 3),
+                            "hbm_gbs": round(wg, 1), "frac_of_peak": round(wg / peak, 4),
+                            "bytes": wwl.bytes, "steps": small_steps,
+                            "bytes_are": "K and V fp16 read + both caches written"})
+            del wwl
+            torch.cuda.empty_cache()
 
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 10))
     e_ms, h2d, d2h = time_e2e(HEADLINE_B, e2e_steps, 2, device, 99 + rank, world)
@@ -581,7 +678,8 @@ def main():
                          "frac": round(gbs / peak, 4), "peak_kind": peak_kind,
                          "traffic": traffic,
                          "algorithmic_bytes_per_launch": kvb,
-                         "kernel": "decode_paged_kernel<D=256,f16,NT=1>"},
+                         "kernel": "decode_paged_kernel<D=256,f16,NT=1,HG=2,DS=2>",
+                         "timed": "decode kernel + split-combine kernel per step (CUDA events around the graph of K steps)"},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_val, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},

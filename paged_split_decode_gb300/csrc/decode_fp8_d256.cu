@@ -1,8 +1,13 @@
-// decode_fp8_d256.cu -- instantiations of the decode kernel for fp8 KV, D=256.
-// NT = row tiles of 8 query rows (rows per unit = Hq/Hkv * qlen <= 8*NT);
-// KG = key groups (consumer warps per row tile); two CTAs share each SM, so
-// two producers keep the SM's TMA traffic flowing; the ring takes as many
-// stages as half an SM's shared memory allows.
+// decode_fp8_d256.cu -- instantiations of the decode kernel for fp8 (e4m3fn) KV, D=256.
+// NT = row tiles of 8 query rows per KV head (rows per head = Hq/Hkv * qlen
+// <= 8*NT); KG = key groups (consumer warps per row tile). Per-head tiles
+// (HG = 1): two CTAs share each SM, so two producers keep the SM's TMA
+// traffic flowing. Head-group tiles (C1H, NT = 1, Hkv a multiple of 4): a
+// tile holds 16 keys of HG consecutive KV heads -- one contiguous run of the
+// cache per key -- and one CTA per SM holds a deep ring of them; each head has
+// its own consumer warps (DS of them splitting D). The ring takes as many
+// stages as the shared memory allows. The head-group shapes are the ones that
+// measured fastest on GB300.
 #include "launch.h"
 
 namespace pd {
@@ -13,9 +18,11 @@ using C1 = CfgFor<kD, kKv, 1, 2, 2>;
 using C2 = CfgFor<kD, kKv, 2, 1, 2>;
 using C3 = CfgFor<kD, kKv, 3, 1, 2>;
 using C4 = CfgFor<kD, kKv, 4, 1, 2>;
+using C1H = CfgFor<kD, kKv, 1, 1, 1, 1, 4>;
 }  // namespace
 
-bool shape_fp8_d256(int nt, KernelShape* out) {
+bool shape_fp8_d256(int nt, int grouped, KernelShape* out) {
+  if (grouped) return nt == 1 && shape_of<C1H>(out);
   switch (nt) {
     case 1: return shape_of<C1>(out);
     case 2: return shape_of<C2>(out);
@@ -25,8 +32,9 @@ bool shape_fp8_d256(int nt, KernelShape* out) {
   }
 }
 
-cudaError_t launch_fp8_d256(int nt, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const DecodeParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_fp8_d256(int nt, int grouped, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const DecodeParams& p, int grid, cudaStream_t s) {
+  if (grouped) return nt == 1 ? launch_cfg<C1H>(tk, tv, p, grid, s) : cudaErrorInvalidValue;
   switch (nt) {
     case 1: return launch_cfg<C1>(tk, tv, p, grid, s);
     case 2: return launch_cfg<C2>(tk, tv, p, grid, s);

@@ -7,32 +7,36 @@
 // [num_blocks, block_size, Hkv, D].
 //
 // GB300 design (the pull request's RDNA2 schedule is prior art only):
-//  * Work unit = (sequence b, KV head kh). All G*qlen query rows that read kh
-//    are packed into one CTA, so each K/V byte crosses HBM once.
-//  * Persistent grid, one CTA per SM. The visible key tiles (16 keys each) of
-//    all units are laid end to end and cut into equal contiguous ranges, one
-//    per CTA (balanced split-K). A fixed num_splits instead cuts each unit
-//    into num_splits chunks handed out round robin.
+//  * Work unit = (sequence b, group of HG consecutive KV heads). All G*qlen
+//    query rows of every head in the group are packed into one CTA, so each
+//    K/V byte crosses HBM once. A tile is 16 keys of the HG heads: with HG > 1
+//    one TMA box reads HG*128 contiguous bytes per key, which is what lets the
+//    HBM stream run near the copy rate (one head per tile reads 256-512 B at
+//    an Hkv-fold stride and tops out lower).
+//  * Persistent grid (one or two CTAs per SM). The visible key tiles of all
+//    units are laid end to end and cut into equal contiguous ranges, one per
+//    CTA (balanced split-K). A fixed num_splits instead cuts each unit into
+//    num_splits chunks handed out round robin.
 //  * One producer warp walks the CTA's tiles, reads block-table entries 32 at
 //    a time (the next group is prefetched while the current one is issued)
 //    and issues TMA bulk-tensor loads of the K and V tiles into an NS-stage
 //    ring of 128B-swizzled shared-memory slabs, completed on mbarriers.
-//  * Consumer warps are (row tile nt, key group kg): warp (nt, kg) takes the
-//    ring's tiles kg, kg+KG, ... for query rows 8nt..8nt+7. Per tile it forms
-//    S^T = K Q^T with mma.sync m16n8k16 (keys on M, query rows on N, Q held in
-//    registers), masks, runs the online softmax with warp shuffles, turns P
-//    into the B operand with movmatrix and accumulates O^T = V^T P^T.
-//    fp8 e4m3 tiles are widened to fp16 in registers (cvt.f16x2.e4m3x2), int8
-//    tiles by an exact magic-number conversion; the K scale is folded into the
-//    score scale and the V scale into the output.
-//  * At the end of a unit piece the KG key groups merge (m, l, O) through
-//    shared memory. A unit covered by one piece is normalised and written as
-//    fp16; otherwise the piece writes an fp32 partial and bumps the unit's
-//    ticket; the piece that arrives last merges all partials in a fixed
-//    order (deterministic) and writes the row, then resets the ticket.
+//  * Consumer warps are (tile head th, key group kg, row group, D part): per
+//    tile a warp forms S^T = K Q^T with mma.sync m16n8k16 (keys on M, query
+//    rows on N, Q held in registers), masks, runs the online softmax with warp
+//    shuffles, turns P into the B operand with movmatrix and accumulates
+//    O^T = V^T P^T. fp8 e4m3 tiles are widened to fp16 in registers
+//    (cvt.f16x2.e4m3x2), int8 tiles by an exact magic-number conversion; the K
+//    scale is folded into the score scale and the V scale into the output.
+//  * At the end of a unit piece the key groups of a head merge (m, l, O)
+//    through shared memory (or, with one key group per head, each warp writes
+//    its rows from registers). A unit covered by one piece is normalised and
+//    written as fp16; otherwise the piece writes an fp32 partial and the
+//    split-combine kernel, launched behind this one with programmatic
+//    dependent launch, merges every split unit's partials in a fixed order.
 //  * Every mbarrier wait is bounded in wall time; on expiry the kernel raises
 //    an error bit and runs the rest of its control flow without waiting, so
-//    named barriers and tickets stay consistent and the CTA always exits.
+//    named barriers stay consistent and the CTA always exits.
 #pragma once
 #include <cuda.h>
 #include <cstdint>
@@ -65,7 +69,9 @@ struct DecodeParams {
   int n_desc;
   int rows_padded;            // RP: rows per partial slot
   uint32_t* error_flag;       // may be null
-  int B, qlen, Hq, Hkv, G, R;  // qlen, R: the largest per sequence (R = G*qlen rows per unit)
+  int B, qlen, Hq, Hkv, G, R;  // qlen, R: the largest per sequence (R = G*qlen rows per head)
+  int hg, hgn;                 // KV heads per tile; head groups per sequence (Hkv / hg)
+  int rows_head;               // partial rows reserved per head of a unit (row tiles * 8)
   int max_blocks, block_size, num_blocks, tiles_per_block;
   int window;                 // <= 0: none
   int num_splits;             // 0: balanced
@@ -101,16 +107,25 @@ __device__ __forceinline__ uint32_t byte_word_prep(uint32_t w) {
   else return w;
 }
 
-template <int D_, int KV_, int NT_, int KG_, int NS_, int MINB_, int DS_ = (NT_ == 1 ? 1 : 2)>
+template <int D_, int KV_, int NT_, int KG_, int NS_, int MINB_, int DS_ = (NT_ == 1 ? 1 : 2),
+          int HG_ = 1>
 struct Cfg {
   static constexpr int D = D_, NT = NT_, KG = KG_, NS = NS_;
+  // HG KV heads per tile: a tile is 16 keys of HG consecutive heads, which sit
+  // next to each other in the cache; one TMA box per 128-byte slab covers all
+  // HG heads (measured: boxes of one head each read the same bytes markedly
+  // slower). The smem rows are (key, head) pairs, so the 16 rows of one head
+  // meet only 8/HG of the eight 128B-swizzle phases: a 2- or 4-way bank
+  // conflict on the consumers' reads, the smaller cost of the two. Each head
+  // has its own consumer warps.
+  static constexpr int HG = HG_;
   static constexpr int kMinBlocks = MINB_;              // resident CTAs per SM the plan targets
   static constexpr int KV = KV_;
   static constexpr bool FP8 = KV_ != kKvF16;   // one-byte elements (e4m3fn or int8)
   static constexpr int kElem = FP8 ? 1 : 2;
   static constexpr int kSlabElems = 128 / kElem;        // one 128-byte swizzle row
   static constexpr int kSlabs = D / kSlabElems;
-  static constexpr int kSlabBytes = kTileKeys * 128;    // 2 KB, 1024-aligned
+  static constexpr int kSlabBytes = kTileKeys * HG * 128;  // [key][head][128 B], 1024-aligned
   static constexpr int kTileBytes = kSlabs * kSlabBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;    // K tile then V tile
   // DS = 1: each consumer warp covers all of D for its 8-row tiles.
@@ -123,15 +138,27 @@ struct Cfg {
   static constexpr int DS = DS_;
   static constexpr int RG = (NT == 4 && DS == 2) ? 2 : 1;
   static constexpr int NTW = NT / RG;                    // row tiles per warp
-  static constexpr int kConsumerWarps = KG * RG * DS;
+  static constexpr int kConsumerWarps = HG * KG * RG * DS;
   static constexpr int kConsumerThreads = kConsumerWarps * 32;
   static constexpr int kThreads = kConsumerThreads + 32;
-  static constexpr int RP = NT * 8;
+  static constexpr int RP = HG * NT * 8;                // partial rows per unit
+  // Key groups merge through shared memory, which also stages the epilogue.
+  // With one key group per head and several heads per tile, each warp's
+  // (m, l, O) is final and is written straight from registers instead.
+  static constexpr bool kSmemMerge = !(KG == 1 && HG > 1);
   static constexpr int kDP = D + 4;                     // merge row pitch (floats)
-  static constexpr int kMergeOBytes = NT * 8 * kDP * 4;        // one buffer per row tile
-  static constexpr int kMergeMLBytes = KG * NT * 8 * 2 * 4;
+  static constexpr int kMergeOBytes = kSmemMerge ? HG * NT * 8 * kDP * 4 : 0;
+  static constexpr int kMergeMLBytes = kSmemMerge ? HG * KG * NT * 8 * 2 * 4 : 0;
   static constexpr int kXchgFloats = 32 * 4 * NTW;       // one warp's partial S^T, lane-major
-  static constexpr int kXchgBytes = DS > 1 ? KG * RG * 2 * DS * kXchgFloats * 4 : 0;
+  static constexpr int kXchgBytes = DS > 1 ? HG * KG * RG * 2 * DS * kXchgFloats * 4 : 0;
+  static_assert(HG == 1 || HG == 2 || HG == 4, "1, 2 or 4 heads per tile");
+  // Key group kg takes the ring's tiles kg, kg+KG, ... With NS a multiple of
+  // KG every use of a stage belongs to the same key group, which consumes its
+  // tiles in order; so when it waits on a stage's full barrier, the stage's
+  // previous phase is its own, already consumed, and a parity wait can never
+  // be satisfied by a phase that is one round old.
+  static_assert(NS % KG == 0, "ring stages must be a multiple of the key groups");
+  static_assert(HG * KG * RG <= 14, "named barriers 2.. cover every D group");
   static_assert(DS == 1 || DS == 2 || DS == 4, "D splits into 1, 2 or 4 parts");
   static_assert(!FP8 || (D / 16 / DS) % 4 == 0, "one-byte tiles need 64-dim parts");
   static constexpr int kOffMergeO = NS * kStageBytes;
@@ -149,14 +176,14 @@ struct Cfg {
 // Work decomposition shared by the producer and the consumers. Both walk the
 // same sequence of pieces, so the ring's tile order matches on both sides.
 struct Piece {
-  int b, kh, L;
+  int b, kh, L;     // kh: first KV head of the unit's head group
   int first_tile;   // tile index (within the sequence) of the piece's first tile
   int ntiles;       // tiles in this piece (0: a zero-fill piece for an empty unit)
   int npieces;      // pieces the unit was cut into (1: write the output directly)
   int slot;         // workspace slot of this piece's partial (npieces > 1)
   int chunk;        // balanced mode: chunk the piece belongs to; fixed mode: split index
   int unit_t0;      // first visible tile of the unit (within the sequence)
-  int unit;         // b * Hkv + kh
+  int unit;         // b * hgn + head group
   int first_slot_cta;  // balanced mode: the first chunk covering the unit
   long long unit_start;  // balanced mode: global tile index where the unit begins
   int tile_lo_all;     // keys [tile_lo_all, tile_hi_all] are visible to every query
@@ -249,7 +276,7 @@ struct WorkIter {
   int chunk;        // the CTA's range (balanced mode)
   int b;
   int zero_b;       // next sequence to test for zero-fill, stepping by gridDim.x
-  int zero_kh;
+  int zero_kh;      // head group of the next zero-fill piece
   long long piece;  // fixed-split mode
 };
 
@@ -286,15 +313,15 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
     if (it.g < it.g_end) {
       while (s_pre[it.b + 1] <= it.g) ++it.b;
       const int b = it.b;
-      const int n = (s_pre[b + 1] - s_pre[b]) / p.Hkv;
+      const int n = (s_pre[b + 1] - s_pre[b]) / p.hgn;
       const long long off = it.g - s_pre[b];
-      const int kh = static_cast<int>(off / n);
-      const long long us = s_pre[b] + static_cast<long long>(kh) * n;
+      const int grp = static_cast<int>(off / n);
+      const long long us = s_pre[b] + static_cast<long long>(grp) * n;
       const long long ue = us + n;
       const long long pe = ue < it.g_end ? ue : it.g_end;
       int L, t0, nn, q0, qn;
       seq_span(p, b, false, L, t0, nn, q0, qn);
-      pc.b = b; pc.kh = kh; pc.L = L; pc.unit_t0 = t0; pc.unit = b * p.Hkv + kh;
+      pc.b = b; pc.kh = grp * p.hg; pc.L = L; pc.unit_t0 = t0; pc.unit = b * p.hgn + grp;
       pc.qlen = qn; pc.R = p.G * qn; pc.q0 = q0;
       pc.first_tile = t0 + static_cast<int>(it.g - us);
       pc.ntiles = static_cast<int>(pe - it.g);
@@ -315,10 +342,11 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
         int q0, qn;
         seq_queries(p, b, false, q0, qn);
         pc.qlen = qn; pc.R = p.G * qn; pc.q0 = q0;
-        pc.b = b; pc.kh = it.zero_kh; pc.L = 0; pc.unit_t0 = 0; pc.unit = b * p.Hkv + it.zero_kh;
+        pc.b = b; pc.kh = it.zero_kh * p.hg; pc.L = 0; pc.unit_t0 = 0;
+        pc.unit = b * p.hgn + it.zero_kh;
         pc.first_tile = 0; pc.ntiles = 0; pc.npieces = 1; pc.slot = 0; pc.chunk = 0;
         pc.first_slot_cta = 0; pc.unit_start = 0;
-        if (++it.zero_kh == p.Hkv) { it.zero_kh = 0; it.zero_b += C; }
+        if (++it.zero_kh == p.hgn) { it.zero_kh = 0; it.zero_b += C; }
         return true;
       }
       it.zero_b += C;
@@ -326,12 +354,12 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
     return false;
   }
   const int S = p.num_splits;
-  const long long total = static_cast<long long>(p.B) * p.Hkv * S;
+  const long long total = static_cast<long long>(p.B) * p.hgn * S;
   while (it.piece < total) {
     const long long pi = it.piece;
     it.piece += C;
     const int u = static_cast<int>(pi / S), s = static_cast<int>(pi % S);
-    const int b = u / p.Hkv, kh = u % p.Hkv;
+    const int b = u / p.hgn, kh = (u % p.hgn) * p.hg;
     int L, t0, n, q0, qn;
     seq_span(p, b, s == 0 && kh == 0, L, t0, n, q0, qn);
     pc.qlen = qn; pc.R = p.G * qn; pc.q0 = q0;
@@ -380,7 +408,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, Cfg::RG * Cfg::DS);
+      mbar_init(empty0 + 8 * s, Cfg::HG * Cfg::RG * Cfg::DS);  // the warps of one key group
     }
     fence_mbar_init();
   }
@@ -398,7 +426,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
       if (b < p.B) {
         int L, t0, n, q0, qn;
         seq_span(p, b, blockIdx.x == 0, L, t0, n, q0, qn);
-        v = n * p.Hkv;
+        v = n * p.hgn;
       }
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -456,7 +484,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) continue;
-          // lanes 0..kSlabs-1 load the K slabs, the next kSlabs lanes the V slabs
+          // lanes 0..kSlabs-1 load the K slabs, the next kSlabs lanes the V
+          // slabs; one box covers 16 keys x HG heads x 128 bytes
           if (lane < 2 * Cfg::kSlabs) {
             const int tile = pc.first_tile + t + i;
             const int z = blk * p.block_size + (tile % p.tiles_per_block) * kTileKeys;
@@ -485,11 +514,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
   }
 
   // -------------------------------------------------------------- consumers
-  constexpr int DS = Cfg::DS, NTW = Cfg::NTW, RG = Cfg::RG;
+  constexpr int DS = Cfg::DS, NTW = Cfg::NTW, RG = Cfg::RG, HG = Cfg::HG;
   const int dh = warp % DS;                   // part of D
   const int rg = (warp / DS) % RG;            // row group: row tiles rg*NTW .. rg*NTW+NTW-1
-  const int kg = warp / (DS * RG);            // key group
-  const int pair = kg * RG + rg;              // the D group this warp belongs to
+  const int kg = (warp / (DS * RG)) % KG;     // key group
+  const int th = warp / (DS * RG * KG);       // head of the tile (KV head pc.kh + th)
+  const int pair = (th * KG + kg) * RG + rg;  // the D group this warp belongs to
   const int g = lane >> 2, t4 = lane & 3;
   constexpr int KSTEPS = D / 16;
   constexpr int KSW = KSTEPS / DS;             // k-steps of this warp's part of D
@@ -508,7 +538,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
       const __half* qrow = nullptr;
       if (r < pc.R && pc.ntiles > 0) {
         const int i = r / p.G, hl = r % p.G;
-        qrow = p.q + (static_cast<long long>(pc.q0 + i) * p.Hq + pc.kh * p.G + hl) * D;
+        qrow = p.q + (static_cast<long long>(pc.q0 + i) * p.Hq + (pc.kh + th) * p.G + hl) * D;
       }
 #pragma unroll
       for (int ksl = 0; ksl < KSW; ++ksl) {
@@ -573,13 +603,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
         for (int e = 0; e < 4; ++e) sa[n][e] = sb[n][e] = 0.f;
       if constexpr (!FP8) {
         const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
-        const uint32_t rowb = kb + key * 128;
+        const int srow = key * HG + th;  // 128-byte row of (key, head) in a slab
+        const uint32_t rowb = kb + srow * 128;
 #pragma unroll
         for (int ksl = 0; ksl < KSW; ++ksl) {
           const int ks = dh * KSW + ksl;
           const int slab = ks >> 2, chunk = (ks & 3) * 2 + (lane >> 4);
           uint32_t a[4];
-          ldsm_x4(rowb + slab * Cfg::kSlabBytes + ((chunk ^ (key & 7)) << 4), a);
+          ldsm_x4(rowb + slab * Cfg::kSlabBytes + ((chunk ^ (srow & 7)) << 4), a);
 #pragma unroll
           for (int n = 0; n < NTW; ++n) {
             if (ksl & 1) mma_16816(sb[n], a, qf[ksl][n][0], qf[ksl][n][1]);
@@ -587,13 +618,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           }
         }
       } else {
-        const uint32_t r0 = kb + g * 128, r8 = kb + (g + 8) * 128;
+        // rows (key g, head th) and (key g+8, head th); both have swizzle phase srow & 7
+        const int srow = g * HG + th;
+        const uint32_t r0 = kb + srow * 128, r8 = kb + (srow + 8 * HG) * 128;
         // super-steps of 4 k-steps: (slab, ss) = ks / 4
 #pragma unroll
         for (int sup = 0; sup < KSW / 4; ++sup) {
           const int gsup = dh * (KSW / 4) + sup;
           const int slab = gsup >> 1, ss = gsup & 1;
-          const int chunk = (2 * t4 + ss) ^ (g & 7);
+          const int chunk = (2 * t4 + ss) ^ (srow & 7);
           uint4 w0, w8;
           asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                        : "=r"(w0.x), "=r"(w0.y), "=r"(w0.z), "=r"(w0.w)
@@ -706,7 +739,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
       const bool tail = key0 + kTileKeys > pc.L;
       if constexpr (!FP8) {
         const int key = (lane & 7) + (lane >> 4) * 8;
-        const uint32_t rowb = vb + key * 128;
+        const int srow = key * HG + th;
+        const uint32_t rowb = vb + srow * 128;
         // A = V^T fragment: a[0], a[1] hold keys 2t4, 2t4+1; a[2], a[3] keys 2t4+8, 2t4+9
         uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
         if (tail) {
@@ -719,7 +753,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           const int mt = dh * MTW + mtl;
           const int slab = mt >> 2, chunk = (mt & 3) * 2 + ((lane >> 3) & 1);
           uint32_t a[4];
-          ldsm_x4_trans(rowb + slab * Cfg::kSlabBytes + ((chunk ^ (key & 7)) << 4), a);
+          ldsm_x4_trans(rowb + slab * Cfg::kSlabBytes + ((chunk ^ (srow & 7)) << 4), a);
           if (tail) {
             a[0] &= vm01; a[1] &= vm01; a[2] &= vm23; a[3] &= vm23;
           }
@@ -739,10 +773,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           const int byte = (4 * g) & 15;
           const uint32_t sb0 = vb + slab * Cfg::kSlabBytes + byte;
           uint32_t wA, wB, wC, wD;
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wA) : "r"(sb0 + kA * 128 + ((chunk ^ (kA & 7)) << 4)));
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wB) : "r"(sb0 + kB * 128 + ((chunk ^ (kB & 7)) << 4)));
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wC) : "r"(sb0 + kC * 128 + ((chunk ^ (kC & 7)) << 4)));
-          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wD) : "r"(sb0 + kD * 128 + ((chunk ^ (kD & 7)) << 4)));
+          const int rA = kA * HG + th, rB = kB * HG + th, rC = kC * HG + th, rD = kD * HG + th;
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wA) : "r"(sb0 + rA * 128 + ((chunk ^ (rA & 7)) << 4)));
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wB) : "r"(sb0 + rB * 128 + ((chunk ^ (rB & 7)) << 4)));
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wC) : "r"(sb0 + rC * 128 + ((chunk ^ (rC & 7)) << 4)));
+          asm volatile("ld.shared.b32 %0, [%1];" : "=r"(wD) : "r"(sb0 + rD * 128 + ((chunk ^ (rD & 7)) << 4)));
           if (tail) {  // code 0 is the value 0 in both byte formats
             if (key0 + kA >= pc.L) wA = 0u;
             if (key0 + kB >= pc.L) wB = 0u;
@@ -773,8 +808,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
     }
     q += pc.ntiles;
 
-    // ---- merge the KG key groups of each row tile through shared memory
-    // (m and l are identical in the two warps of a D pair; warp dh = 0 posts them)
+    // ---- row sums over the lanes of each row (m is already warp-uniform per row)
 #pragma unroll
     for (int n = 0; n < NTW; ++n)
 #pragma unroll
@@ -782,103 +816,155 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
         l_r[n][0] += __shfl_xor_sync(0xffffffffu, l_r[n][0], off);
         l_r[n][1] += __shfl_xor_sync(0xffffffffu, l_r[n][1], off);
       }
-    if (g == 0 && dh == 0) {
+    const int tid = threadIdx.x;
+    const bool direct = pc.npieces == 1;
+    constexpr int NT = Cfg::NT, RH = NT * 8;  // partial rows per head of a unit
+    if constexpr (Cfg::kSmemMerge) {
+      // ---- merge the KG key groups of each row tile through shared memory
+      // (m and l are identical in the warps of a D group; warp dh = 0 posts them)
+      if (g == 0 && dh == 0) {
 #pragma unroll
-      for (int n = 0; n < NTW; ++n) {
-        float* ml = merge_ml + ((rg * NTW + n) * KG + kg) * 16;
-        ml[(2 * t4) * 2 + 0] = m_r[n][0];
-        ml[(2 * t4) * 2 + 1] = l_r[n][0];
-        ml[(2 * t4 + 1) * 2 + 0] = m_r[n][1];
-        ml[(2 * t4 + 1) * 2 + 1] = l_r[n][1];
+        for (int n = 0; n < NTW; ++n) {
+          float* ml = merge_ml + ((th * NT + rg * NTW + n) * KG + kg) * 16;
+          ml[(2 * t4) * 2 + 0] = m_r[n][0];
+          ml[(2 * t4) * 2 + 1] = l_r[n][0];
+          ml[(2 * t4 + 1) * 2 + 0] = m_r[n][1];
+          ml[(2 * t4 + 1) * 2 + 1] = l_r[n][1];
+        }
       }
-    }
-    named_bar_sync(1, Cfg::kConsumerThreads);
-    {
-      // this warp's weight per row: exp2(m_own - max over the key groups)
-      float f_r[NTW][2];
+      named_bar_sync(1, Cfg::kConsumerThreads);
+      {
+        // this warp's weight per row: exp2(m_own - max over the key groups)
+        float f_r[NTW][2];
+#pragma unroll
+        for (int n = 0; n < NTW; ++n)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int row = 2 * t4 + c;
+            float M = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < KG; ++k)
+              M = fmaxf(M, merge_ml[(((th * NT + rg * NTW + n) * KG + k) * 8 + row) * 2]);
+            f_r[n][c] = (m_r[n][c] == -INFINITY) ? 0.f : ex2(m_r[n][c] - M);
+          }
+        // each row tile's buffer accumulates f * O one key group at a time
+        const int r0 = 2 * t4, r1 = r0 + 1;
+#pragma unroll 1
+        for (int k = 0; k < KG; ++k) {
+          if (kg == k) {
+#pragma unroll
+            for (int n = 0; n < NTW; ++n) {
+              float* mo = merge_o + (th * NT + rg * NTW + n) * 8 * Cfg::kDP;
+#pragma unroll
+              for (int mtl = 0; mtl < MTW; ++mtl) {
+                const int mt = dh * MTW + mtl;
+                int d0, d1;  // output dims of C rows g and g+8 of m-tile mt
+                if constexpr (FP8) {
+                  d0 = (mt >> 1) * 32 + 4 * g + 2 * (mt & 1);
+                  d1 = d0 + 1;
+                } else {
+                  d0 = mt * 16 + g;
+                  d1 = d0 + 8;
+                }
+                float* a00 = mo + r0 * Cfg::kDP + d0;
+                float* a10 = mo + r1 * Cfg::kDP + d0;
+                float* a01 = mo + r0 * Cfg::kDP + d1;
+                float* a11 = mo + r1 * Cfg::kDP + d1;
+                if (k == 0) {
+                  *a00 = f_r[n][0] * o[mtl][n][0]; *a10 = f_r[n][1] * o[mtl][n][1];
+                  *a01 = f_r[n][0] * o[mtl][n][2]; *a11 = f_r[n][1] * o[mtl][n][3];
+                } else {
+                  *a00 += f_r[n][0] * o[mtl][n][0]; *a10 += f_r[n][1] * o[mtl][n][1];
+                  *a01 += f_r[n][0] * o[mtl][n][2]; *a11 += f_r[n][1] * o[mtl][n][3];
+                }
+              }
+            }
+          }
+          named_bar_sync(1, Cfg::kConsumerThreads);
+        }
+      }
+
+      constexpr int DCH = D / 8;  // 8-dim chunks per row
+      const int per_head = pc.R * DCH;
+      for (int item = tid; item < HG * per_head; item += Cfg::kConsumerThreads) {
+        const int hh = item / per_head, rem = item - hh * per_head;
+        const int r = rem / DCH, dc = rem % DCH;
+        const int rnt = hh * NT + (r >> 3), rr = r & 7;
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < KG; ++k) M = fmaxf(M, merge_ml[((rnt * KG + k) * 8 + rr) * 2]);
+        float Ls = 0.f;
+#pragma unroll
+        for (int k = 0; k < KG; ++k) {
+          const float mk = merge_ml[((rnt * KG + k) * 8 + rr) * 2];
+          if (mk != -INFINITY) Ls += ex2(mk - M) * merge_ml[((rnt * KG + k) * 8 + rr) * 2 + 1];
+        }
+        const float* src = merge_o + (rnt * 8 + rr) * Cfg::kDP + dc * 8;
+        const float4 v0 = *reinterpret_cast<const float4*>(src);
+        const float4 v1 = *reinterpret_cast<const float4*>(src + 4);
+        if (direct) {
+          const int i = r / p.G, hl = r % p.G;
+          __half* dst = p.out + (static_cast<long long>(pc.q0 + i) * p.Hq + (pc.kh + hh) * p.G + hl) * D + dc * 8;
+          const float inv = (Ls > 0.f) ? p.out_scale / Ls : 0.f;
+          uint4 v;
+          v.x = pack_half2(v0.x * inv, v0.y * inv);
+          v.y = pack_half2(v0.z * inv, v0.w * inv);
+          v.z = pack_half2(v1.x * inv, v1.y * inv);
+          v.w = pack_half2(v1.z * inv, v1.w * inv);
+          *reinterpret_cast<uint4*>(dst) = v;
+        } else {
+          const long long prow = static_cast<long long>(pc.slot) * Cfg::RP + hh * RH + r;
+          float* dst = p.ws_o + prow * D + dc * 8;
+          __stcg(reinterpret_cast<float4*>(dst), v0);
+          __stcg(reinterpret_cast<float4*>(dst + 4), v1);
+          if (dc == 0) __stcg(reinterpret_cast<float2*>(p.ws_ml + prow * 2), make_float2(M, Ls));
+        }
+      }
+    } else {
+      // ---- one key group per head: this warp's (m, l, O) are final for its
+      // rows and dims, written straight from the accumulator fragments
 #pragma unroll
       for (int n = 0; n < NTW; ++n)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const int row = 2 * t4 + c;
-          float M = -INFINITY;
-#pragma unroll
-          for (int k = 0; k < KG; ++k) M = fmaxf(M, merge_ml[(((rg * NTW + n) * KG + k) * 8 + row) * 2]);
-          f_r[n][c] = (m_r[n][c] == -INFINITY) ? 0.f : ex2(m_r[n][c] - M);
-        }
-      // each row tile's buffer accumulates f * O one key group at a time
-      const int r0 = 2 * t4, r1 = r0 + 1;
-#pragma unroll 1
-      for (int k = 0; k < KG; ++k) {
-        if (kg == k) {
-#pragma unroll
-          for (int n = 0; n < NTW; ++n) {
-            float* mo = merge_o + (rg * NTW + n) * 8 * Cfg::kDP;
+          const int r = (rg * NTW + n) * 8 + 2 * t4 + c;
+          if (r >= pc.R) continue;
+          const float Ls = l_r[n][c];
+          if (direct) {
+            const int i = r / p.G, hl = r % p.G;
+            __half* dst = p.out + (static_cast<long long>(pc.q0 + i) * p.Hq + (pc.kh + th) * p.G + hl) * D;
+            const float inv = (Ls > 0.f) ? p.out_scale / Ls : 0.f;
 #pragma unroll
             for (int mtl = 0; mtl < MTW; ++mtl) {
               const int mt = dh * MTW + mtl;
-              int d0, d1;  // output dims of C rows g and g+8 of m-tile mt
               if constexpr (FP8) {
-                d0 = (mt >> 1) * 32 + 4 * g + 2 * (mt & 1);
-                d1 = d0 + 1;
+                const int d0 = (mt >> 1) * 32 + 4 * g + 2 * (mt & 1);  // dims d0, d0 + 1
+                *reinterpret_cast<uint32_t*>(dst + d0) =
+                    pack_half2(o[mtl][n][c] * inv, o[mtl][n][2 + c] * inv);
               } else {
-                d0 = mt * 16 + g;
-                d1 = d0 + 8;
-              }
-              float* a00 = mo + r0 * Cfg::kDP + d0;
-              float* a10 = mo + r1 * Cfg::kDP + d0;
-              float* a01 = mo + r0 * Cfg::kDP + d1;
-              float* a11 = mo + r1 * Cfg::kDP + d1;
-              if (k == 0) {
-                *a00 = f_r[n][0] * o[mtl][n][0]; *a10 = f_r[n][1] * o[mtl][n][1];
-                *a01 = f_r[n][0] * o[mtl][n][2]; *a11 = f_r[n][1] * o[mtl][n][3];
-              } else {
-                *a00 += f_r[n][0] * o[mtl][n][0]; *a10 += f_r[n][1] * o[mtl][n][1];
-                *a01 += f_r[n][0] * o[mtl][n][2]; *a11 += f_r[n][1] * o[mtl][n][3];
+                const int d0 = mt * 16 + g;                           // dims d0, d0 + 8
+                dst[d0] = __float2half_rn(o[mtl][n][c] * inv);
+                dst[d0 + 8] = __float2half_rn(o[mtl][n][2 + c] * inv);
               }
             }
+          } else {
+            const long long prow = static_cast<long long>(pc.slot) * Cfg::RP + th * RH + r;
+            float* dst = p.ws_o + prow * D;
+#pragma unroll
+            for (int mtl = 0; mtl < MTW; ++mtl) {
+              const int mt = dh * MTW + mtl;
+              if constexpr (FP8) {
+                const int d0 = (mt >> 1) * 32 + 4 * g + 2 * (mt & 1);
+                __stcg(reinterpret_cast<float2*>(dst + d0), make_float2(o[mtl][n][c], o[mtl][n][2 + c]));
+              } else {
+                const int d0 = mt * 16 + g;
+                __stcg(dst + d0, o[mtl][n][c]);
+                __stcg(dst + d0 + 8, o[mtl][n][2 + c]);
+              }
+            }
+            if (g == 0 && dh == 0) __stcg(reinterpret_cast<float2*>(p.ws_ml + prow * 2), make_float2(m_r[n][c], Ls));
           }
         }
-        named_bar_sync(1, Cfg::kConsumerThreads);
-      }
-    }
-
-    const int tid = threadIdx.x;
-    constexpr int DCH = D / 8;  // 8-dim chunks per row
-    const bool direct = pc.npieces == 1;
-    for (int item = tid; item < pc.R * DCH; item += Cfg::kConsumerThreads) {
-      const int r = item / DCH, dc = item % DCH;
-      const int rnt = r >> 3, rr = r & 7;
-      float M = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < KG; ++k) M = fmaxf(M, merge_ml[((rnt * KG + k) * 8 + rr) * 2]);
-      float Ls = 0.f;
-#pragma unroll
-      for (int k = 0; k < KG; ++k) {
-        const float mk = merge_ml[((rnt * KG + k) * 8 + rr) * 2];
-        if (mk != -INFINITY) Ls += ex2(mk - M) * merge_ml[((rnt * KG + k) * 8 + rr) * 2 + 1];
-      }
-      const float* src = merge_o + (rnt * 8 + rr) * Cfg::kDP + dc * 8;
-      const float4 v0 = *reinterpret_cast<const float4*>(src);
-      const float4 v1 = *reinterpret_cast<const float4*>(src + 4);
-      if (direct) {
-        const int i = r / p.G, hl = r % p.G;
-        __half* dst = p.out + (static_cast<long long>(pc.q0 + i) * p.Hq + pc.kh * p.G + hl) * D + dc * 8;
-        const float inv = (Ls > 0.f) ? p.out_scale / Ls : 0.f;
-        uint4 v;
-        v.x = pack_half2(v0.x * inv, v0.y * inv);
-        v.y = pack_half2(v0.z * inv, v0.w * inv);
-        v.z = pack_half2(v1.x * inv, v1.y * inv);
-        v.w = pack_half2(v1.z * inv, v1.w * inv);
-        *reinterpret_cast<uint4*>(dst) = v;
-      } else {
-        float* dst = p.ws_o + (static_cast<long long>(pc.slot) * Cfg::RP + r) * D + dc * 8;
-        __stcg(reinterpret_cast<float4*>(dst), v0);
-        __stcg(reinterpret_cast<float4*>(dst + 4), v1);
-        if (dc == 0)
-          __stcg(reinterpret_cast<float2*>(p.ws_ml + (static_cast<long long>(pc.slot) * Cfg::RP + r) * 2),
-                 make_float2(M, Ls));
-      }
     }
     if (tid == 0 && p.n_desc > 0) {
       // the first piece of a unit posts its descriptor for the split combine
@@ -896,7 +982,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
         p.ws_desc[p.num_splits == 0 ? pc.chunk : pc.unit] = d;
       }
     }
-    named_bar_sync(1, Cfg::kConsumerThreads);  // merge buffers free again
+    if constexpr (Cfg::kSmemMerge) named_bar_sync(1, Cfg::kConsumerThreads);  // merge buffers free again
   }
   if (!ok && lane == 0) raise_error(p.error_flag, kErrTimeout);
 }
@@ -907,8 +993,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
 // the decode kernel with programmatic dependent launch: its CTAs may start
 // while the decode grid drains and wait in griddepcontrol.wait until that grid
 // has completed and its writes are visible.
-//   grid (n_desc, D/32), 256 threads: CTA (e, c) merges descriptor e's unit
-//   for output dims [32c, 32c+32). Thread t covers item t % items (row r,
+//   grid (n_desc, D/32, heads per tile), 256 threads: CTA (e, c, z) merges
+//   head z of descriptor e's unit for output dims [32c, 32c+32). Thread t covers item t % items (row r,
 //   4-dim slice) for pieces pg, pg+PG, ... (pg = t / items, PG = 256 / items)
 //   with a running max; the PG partial states are then merged in pg order, so
 //   the result does not depend on scheduling.
@@ -922,7 +1008,9 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
   if (u < 0 || P <= 1) return;
   const int step = p.num_splits == 0 ? 2 : 1;
   const int R = p.R, RP = p.rows_padded;
-  const int b = u / p.Hkv, kh = u % p.Hkv;
+  // blockIdx.z: head of the unit's head group; its rows start at z * rows_head
+  const int b = u / p.hgn, kh = (u % p.hgn) * p.hg + blockIdx.z;
+  const int rbase = blockIdx.z * p.rows_head;
   int q0, qn;
   seq_queries(p, b, false, q0, qn);
   const int items = R * 8;
@@ -942,8 +1030,8 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
         const int k = k0 + j * PG;
         if (k < P) {
           const long long sl = k == 0 ? d.z : d.w + static_cast<long long>(step) * k;
-          ml[j] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (sl * RP + r) * 2));
-          v[j] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sl * RP + r) * D + dim0));
+          ml[j] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (sl * RP + rbase + r) * 2));
+          v[j] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sl * RP + rbase + r) * D + dim0));
         } else {
           ml[j] = make_float2(-INFINITY, 0.f);
           v[j] = make_float4(0.f, 0.f, 0.f, 0.f);

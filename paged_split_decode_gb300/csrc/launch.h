@@ -14,36 +14,40 @@ struct KernelShape {
   int smem_bytes;   // dynamic shared memory per CTA
   int rows_padded;  // RP: query rows per unit rounded up to the row-tile size
   int ctas_per_sm;  // resident CTAs per SM the configuration is sized for
+  int heads;        // KV heads per tile (the TMA box's head extent)
 };
 
-// Returns false when no instantiation covers (D, kv kind, nt).
-bool kernel_shape(int D, int kv, int nt, KernelShape* out);
+// Returns false when no instantiation covers (D, kv kind, nt, grouped):
+// grouped = 1 asks for the head-group tiles (KernelShape::heads KV heads per
+// tile, Hkv a multiple of four), grouped = 0 for per-head tiles.
+bool kernel_shape(int D, int kv, int nt, int grouped, KernelShape* out);
 
-// Launch the instantiation for (D, kv kind, nt) on `grid` CTAs.
-cudaError_t launch_decode(int D, int kv, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const DecodeParams& p, int grid, cudaStream_t stream);
+// Launch the instantiation for (D, kv kind, nt, grouped) on `grid` CTAs.
+cudaError_t launch_decode(int D, int kv, int nt, int grouped, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const DecodeParams& p, int grid,
+                          cudaStream_t stream);
 
 // Split combine behind a decode launch (split_combine.cu).
 cudaError_t launch_split_combine(int D, const DecodeParams& p, int n_desc, cudaStream_t stream);
 
 // Per-dtype/head-size entry points defined in decode_*.cu.
-bool shape_f16_d128(int nt, KernelShape* out);
-bool shape_f16_d256(int nt, KernelShape* out);
-bool shape_fp8_d128(int nt, KernelShape* out);
-bool shape_fp8_d256(int nt, KernelShape* out);
-bool shape_i8_d128(int nt, KernelShape* out);
-bool shape_i8_d256(int nt, KernelShape* out);
-cudaError_t launch_f16_d128(int nt, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
+bool shape_f16_d128(int nt, int grouped, KernelShape* out);
+bool shape_f16_d256(int nt, int grouped, KernelShape* out);
+bool shape_fp8_d128(int nt, int grouped, KernelShape* out);
+bool shape_fp8_d256(int nt, int grouped, KernelShape* out);
+bool shape_i8_d128(int nt, int grouped, KernelShape* out);
+bool shape_i8_d256(int nt, int grouped, KernelShape* out);
+cudaError_t launch_f16_d128(int nt, int grouped, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
                             cudaStream_t);
-cudaError_t launch_f16_d256(int nt, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
+cudaError_t launch_f16_d256(int nt, int grouped, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
                             cudaStream_t);
-cudaError_t launch_fp8_d128(int nt, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
+cudaError_t launch_fp8_d128(int nt, int grouped, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
                             cudaStream_t);
-cudaError_t launch_fp8_d256(int nt, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
+cudaError_t launch_fp8_d256(int nt, int grouped, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
                             cudaStream_t);
-cudaError_t launch_i8_d128(int nt, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
+cudaError_t launch_i8_d128(int nt, int grouped, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
                            cudaStream_t);
-cudaError_t launch_i8_d256(int nt, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
+cudaError_t launch_i8_d256(int nt, int grouped, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
                            cudaStream_t);
 
 // Launch one configuration; sets the shared-memory opt-in once per device.
@@ -69,15 +73,20 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
 // MINB CTAs share one SM's 228 KiB (1 KiB of it reserved per CTA; at most
 // 227 KiB for one CTA).
 constexpr int smem_limit(int minb) { return minb == 1 ? 227 * 1024 : 228 * 1024 / minb - 1024; }
-template <int D, int KV, int NT, int KG, int MINB, int DS, int NS = 32>
+// The stage count is a multiple of KG (see Cfg).
+template <int D, int KV, int NT, int KG, int MINB, int DS, int HG, int NS = 32>
 constexpr int ring_stages() {
-  if constexpr (NS <= 2 || Cfg<D, KV, NT, KG, NS, MINB, DS>::kSmemBytes <= smem_limit(MINB))
+  if constexpr (NS <= KG)
+    return KG;
+  else if constexpr (NS % KG != 0)
+    return ring_stages<D, KV, NT, KG, MINB, DS, HG, NS - 1>();
+  else if constexpr (Cfg<D, KV, NT, KG, NS, MINB, DS, HG>::kSmemBytes <= smem_limit(MINB))
     return NS;
   else
-    return ring_stages<D, KV, NT, KG, MINB, DS, NS - 1>();
+    return ring_stages<D, KV, NT, KG, MINB, DS, HG, NS - 1>();
 }
-template <int D, int KV, int NT, int KG, int MINB, int DS = (NT == 1 ? 1 : 2)>
-using CfgFor = Cfg<D, KV, NT, KG, ring_stages<D, KV, NT, KG, MINB, DS>(), MINB, DS>;
+template <int D, int KV, int NT, int KG, int MINB, int DS = (NT == 1 ? 1 : 2), int HG = 1>
+using CfgFor = Cfg<D, KV, NT, KG, ring_stages<D, KV, NT, KG, MINB, DS, HG>(), MINB, DS, HG>;
 
 template <class Cfg>
 bool shape_of(KernelShape* out) {
@@ -85,6 +94,7 @@ bool shape_of(KernelShape* out) {
   out->smem_bytes = Cfg::kSmemBytes;
   out->rows_padded = Cfg::RP;
   out->ctas_per_sm = Cfg::kMinBlocks;
+  out->heads = Cfg::HG;
   return true;
 }
 

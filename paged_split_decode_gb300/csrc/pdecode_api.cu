@@ -15,25 +15,25 @@
 
 namespace pd {
 
-bool kernel_shape(int D, int kv, int nt, KernelShape* out) {
+bool kernel_shape(int D, int kv, int nt, int grouped, KernelShape* out) {
   if (D == 128)
-    return kv == kKvFp8 ? shape_fp8_d128(nt, out) : kv == kKvInt8 ? shape_i8_d128(nt, out)
-                                                                  : shape_f16_d128(nt, out);
+    return kv == kKvFp8 ? shape_fp8_d128(nt, grouped, out) : kv == kKvInt8 ? shape_i8_d128(nt, grouped, out)
+                                                                      : shape_f16_d128(nt, grouped, out);
   if (D == 256)
-    return kv == kKvFp8 ? shape_fp8_d256(nt, out) : kv == kKvInt8 ? shape_i8_d256(nt, out)
-                                                                  : shape_f16_d256(nt, out);
+    return kv == kKvFp8 ? shape_fp8_d256(nt, grouped, out) : kv == kKvInt8 ? shape_i8_d256(nt, grouped, out)
+                                                                      : shape_f16_d256(nt, grouped, out);
   return false;
 }
 
-cudaError_t launch_decode(int D, int kv, int nt, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const DecodeParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_decode(int D, int kv, int nt, int grouped, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const DecodeParams& p, int grid, cudaStream_t s) {
   if (D == 128)
-    return kv == kKvFp8 ? launch_fp8_d128(nt, tk, tv, p, grid, s)
-           : kv == kKvInt8 ? launch_i8_d128(nt, tk, tv, p, grid, s)
-                           : launch_f16_d128(nt, tk, tv, p, grid, s);
-  return kv == kKvFp8 ? launch_fp8_d256(nt, tk, tv, p, grid, s)
-         : kv == kKvInt8 ? launch_i8_d256(nt, tk, tv, p, grid, s)
-                         : launch_f16_d256(nt, tk, tv, p, grid, s);
+    return kv == kKvFp8 ? launch_fp8_d128(nt, grouped, tk, tv, p, grid, s)
+           : kv == kKvInt8 ? launch_i8_d128(nt, grouped, tk, tv, p, grid, s)
+                           : launch_f16_d128(nt, grouped, tk, tv, p, grid, s);
+  return kv == kKvFp8 ? launch_fp8_d256(nt, grouped, tk, tv, p, grid, s)
+         : kv == kKvInt8 ? launch_i8_d256(nt, grouped, tk, tv, p, grid, s)
+                         : launch_f16_d256(nt, grouped, tk, tv, p, grid, s);
 }
 
 namespace {
@@ -46,10 +46,11 @@ std::atomic<int> g_inject{0};
 struct Plan {
   int splits;       // 0 = balanced, >= 1 fixed
   int grid;         // CTAs launched
-  int nt;           // row tiles
+  int nt;           // row tiles per head
+  int hg;           // KV heads per tile
   long long slots;  // partial slots in the workspace
   long long n_desc; // split-combine descriptors
-  long long units;  // B * Hkv tickets
+  long long units;  // B * Hkv / hg work units
   int rows_padded;
   size_t off_ml, off_o, bytes;  // workspace layout
 };
@@ -99,9 +100,16 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
   const int R = d->Hq / d->Hkv * qlen;
   pl->nt = (R + 7) / 8;
   KernelShape ks;
-  if (!kernel_shape(d->D, d->kv_dtype, pl->nt, &ks)) return PD_ERR_UNSUPPORTED;
+  // tiles of several KV heads read the cache contiguously; they serve the
+  // single-row-tile shapes whose head count is a multiple of four (the
+  // instantiation chooses how many heads a tile holds: 2 or 4)
+  const bool grouped = pl->nt == 1 && d->Hkv % 4 == 0;
+  if (!(grouped && kernel_shape(d->D, d->kv_dtype, pl->nt, 1, &ks)) &&
+      !kernel_shape(d->D, d->kv_dtype, pl->nt, 0, &ks))
+    return PD_ERR_UNSUPPORTED;
+  pl->hg = ks.heads;
   pl->rows_padded = ks.rows_padded;
-  pl->units = static_cast<long long>(d->B) * d->Hkv;
+  pl->units = static_cast<long long>(d->B) * (d->Hkv / pl->hg);
   int splits = num_splits;
   if (splits == 0 && d->B > kMaxAutoB) splits = 1;  // plenty of units: one piece each
   pl->splits = splits;
@@ -147,7 +155,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 3-D map over a paged cache viewed as [num_blocks*block_size][Hkv][D]:
 // box = one 128-byte row slab x one head x 16 keys, 128B swizzle.
-bool encode_cache_map(CUtensorMap* m, const void* base, const pd_dims* d) {
+// Box: 128 bytes of D x hg heads x 16 keys, 128-byte swizzled.
+bool encode_cache_map(CUtensorMap* m, const void* base, const pd_dims* d, int hg) {
   auto fn = encode_fn();
   if (!fn) return false;
   const bool byte = d->kv_dtype != PD_KV_F16;
@@ -156,7 +165,8 @@ bool encode_cache_map(CUtensorMap* m, const void* base, const pd_dims* d) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d->D), static_cast<cuuint64_t>(d->Hkv),
                         rows > 0 ? rows : 1};
   cuuint64_t strides[2] = {d->D * elem, static_cast<cuuint64_t>(d->Hkv) * d->D * elem};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem), 1, static_cast<cuuint32_t>(kTileKeys)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem), static_cast<cuuint32_t>(hg),
+                       static_cast<cuuint32_t>(kTileKeys)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -237,7 +247,8 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   }
 
   CUtensorMap tk, tv;
-  if (!encode_cache_map(&tk, k_cache, dims) || !encode_cache_map(&tv, v_cache, dims)) return PD_ERR_CUDA;
+  if (!encode_cache_map(&tk, k_cache, dims, pl.hg) || !encode_cache_map(&tv, v_cache, dims, pl.hg))
+    return PD_ERR_CUDA;
 
   const bool fp8 = dims->kv_dtype != PD_KV_F16;  // a one-byte kind with scales
   DecodeParams p;
@@ -260,6 +271,9 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   p.Hkv = dims->Hkv;
   p.G = dims->Hq / dims->Hkv;
   p.R = p.G * qlen;
+  p.hg = pl.hg;
+  p.hgn = dims->Hkv / pl.hg;
+  p.rows_head = pl.rows_padded / pl.hg;
   p.max_blocks = dims->max_blocks_per_seq;
   p.block_size = dims->block_size;
   p.num_blocks = dims->num_blocks;
@@ -272,7 +286,7 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   p.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   p.inject = g_inject.load(std::memory_order_relaxed);
 
-  cudaError_t e = launch_decode(dims->D, dims->kv_dtype, pl.nt, tk, tv, p, pl.grid,
+  cudaError_t e = launch_decode(dims->D, dims->kv_dtype, pl.nt, pl.hg > 1 ? 1 : 0, tk, tv, p, pl.grid,
                                 static_cast<cudaStream_t>(stream));
   if (e == cudaSuccess && pl.n_desc > 0)
     e = launch_split_combine(dims->D, p, static_cast<int>(pl.n_desc), static_cast<cudaStream_t>(stream));

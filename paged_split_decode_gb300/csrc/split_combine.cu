@@ -7,7 +7,8 @@ namespace pd {
 
 cudaError_t launch_split_combine(int D, const DecodeParams& p, int n_desc, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(n_desc), static_cast<unsigned>(D / 32), 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(n_desc), static_cast<unsigned>(D / 32),
+                     static_cast<unsigned>(p.hg));
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

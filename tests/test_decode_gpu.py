@@ -148,6 +148,14 @@ EDGE = [
     ("int8_d128_rows_24_window", dict(B=2, Hq=8, Hkv=1, D=128, kv="int8", qlen=3, window=300,
                                       seq_lens=[1500, 40])),
     ("int8_d256_rows_32", dict(B=2, Hq=8, Hkv=1, D=256, kv="int8", qlen=4, seq_lens=[700, 90])),
+    # per-head tiles with two key groups over long rings (Hkv not a multiple of 4)
+    ("fp8_d128_per_head_kg2", dict(B=4, Hq=16, Hkv=2, D=128, kv="fp8",
+                                   seq_lens=[5000, 3001, 17, 4096])),
+    ("int8_d128_per_head_kg2", dict(B=3, Hq=8, Hkv=1, D=128, kv="int8", seq_lens=[6000, 2500, 1])),
+    ("f16_d256_per_head_kg2", dict(B=3, Hq=12, Hkv=2, D=256, seq_lens=[4100, 900, 33])),
+    # head-group tiles with two head groups per sequence (Hkv = 8)
+    ("fp8_d128_two_head_groups", dict(B=3, Hq=32, Hkv=8, D=128, kv="fp8", seq_lens=[3000, 47, 800])),
+    ("f16_d256_two_head_groups", dict(B=2, Hq=16, Hkv=8, D=256, seq_lens=[2049, 700])),
 ]
 
 
