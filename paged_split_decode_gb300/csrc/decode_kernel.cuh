@@ -993,11 +993,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
 // the decode kernel with programmatic dependent launch: its CTAs may start
 // while the decode grid drains and wait in griddepcontrol.wait until that grid
 // has completed and its writes are visible.
-//   grid (n_desc, D/32, heads per tile), 256 threads: CTA (e, c, z) merges
-//   head z of descriptor e's unit for output dims [32c, 32c+32). Thread t covers item t % items (row r,
-//   4-dim slice) for pieces pg, pg+PG, ... (pg = t / items, PG = 256 / items)
-//   with a running max; the PG partial states are then merged in pg order, so
-//   the result does not depend on scheduling.
+//   grid (n_desc, C, heads per tile), 256 threads: CTA (e, c, z) merges
+//   head z of descriptor e's unit for output dims [c*D/C, (c+1)*D/C); the
+//   host picks C = D/32 when units are few and split into many pieces, and
+//   C = 1 otherwise. An item is (row, 4 dims). With more than 256 items a
+//   thread merges its items' pieces in order with a running max; with fewer,
+//   thread t covers item t % items for pieces pg, pg+PG, ... (pg = t / items,
+//   PG = 256 / items) and the PG partial states are then merged in pg order.
+//   Either way the result does not depend on scheduling.
 template <int D>
 __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1013,23 +1016,25 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
   const int rbase = blockIdx.z * p.rows_head;
   int q0, qn;
   seq_queries(p, b, false, q0, qn);
-  const int items = R * 8;
-  const int PG = 256 / items > 0 ? 256 / items : 1;
+  const int live_rows = p.G * qn;  // rows of the sequence's query tokens
+  // blockIdx.y: which D / gridDim.y output dims; an item is (row, 4 dims)
+  const int dims_cta = D / gridDim.y, slices = dims_cta / 4;
+  const int items = R * slices;
   const int t = threadIdx.x;
-  const int item = t % items, pg = t / items;
-  const int r = item >> 3, dim0 = blockIdx.y * 32 + (item & 7) * 4;
-  const bool live = r < p.G * qn;  // rows of the sequence's query tokens
-  float m_run = -INFINITY, l_run = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (pg < PG && live) {
-    for (int k0 = pg; k0 < P; k0 += 4 * PG) {
+  const long long slot0 = d.z, slot_base = d.w;
+  auto slot_of = [&](int k) -> long long {
+    return k == 0 ? slot0 : slot_base + static_cast<long long>(step) * k;
+  };
+  // running merge of pieces k0, k0 + stride, ... of one item into (m, l, acc)
+  auto merge = [&](int r, int dim0, int k0, int stride, float& m_run, float& l_run, float4& acc) {
+    for (; k0 < P; k0 += 4 * stride) {
       float2 ml[4];
       float4 v[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int k = k0 + j * PG;
+        const int k = k0 + j * stride;
         if (k < P) {
-          const long long sl = k == 0 ? d.z : d.w + static_cast<long long>(step) * k;
+          const long long sl = slot_of(k);
           ml[j] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (sl * RP + rbase + r) * 2));
           v[j] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sl * RP + rbase + r) * D + dim0));
         } else {
@@ -1052,7 +1057,38 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
         acc.x += w * v[j].x; acc.y += w * v[j].y; acc.z += w * v[j].z; acc.w += w * v[j].w;
       }
     }
+  };
+  auto store = [&](int r, int dim0, float L, float4 o) {
+    const float inv = (L > 0.f) ? p.out_scale / L : 0.f;
+    const int i = r / p.G, hl = r % p.G;
+    __half* dst = p.out + (static_cast<long long>(q0 + i) * p.Hq + kh * p.G + hl) * D + dim0;
+    uint2 o2;
+    o2.x = pack_half2(o.x * inv, o.y * inv);
+    o2.y = pack_half2(o.z * inv, o.w * inv);
+    *reinterpret_cast<uint2*>(dst) = o2;
+  };
+
+  if (items > 256) {
+    // many items, few pieces each: one thread per item, all pieces in order
+    for (int item = t; item < items; item += 256) {
+      const int r = item / slices, dim0 = blockIdx.y * dims_cta + (item % slices) * 4;
+      if (r >= live_rows) continue;
+      float m_run = -INFINITY, l_run = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      merge(r, dim0, 0, 1, m_run, l_run, acc);
+      store(r, dim0, l_run, acc);
+    }
+    return;
   }
+  // few items, possibly many pieces: PG thread groups take interleaved
+  // pieces, then the groups merge in group order (deterministic)
+  const int PG = 256 / items;
+  const int item = t % items, pg = t / items;
+  const int r = item / slices, dim0 = blockIdx.y * dims_cta + (item % slices) * 4;
+  const bool live = r < live_rows;
+  float m_run = -INFINITY, l_run = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (pg < PG && live) merge(r, dim0, pg, PG, m_run, l_run, acc);
   s_m[t] = m_run;
   s_l[t] = l_run;
   s_o[t] = acc;
@@ -1070,13 +1106,7 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
     const float4 a = s_o[g2 * items + item];
     o.x += w * a.x; o.y += w * a.y; o.z += w * a.z; o.w += w * a.w;
   }
-  const float inv = (L > 0.f) ? p.out_scale / L : 0.f;
-  const int i = r / p.G, hl = r % p.G;
-  __half* dst = p.out + (static_cast<long long>(q0 + i) * p.Hq + kh * p.G + hl) * D + dim0;
-  uint2 o2;
-  o2.x = pack_half2(o.x * inv, o.y * inv);
-  o2.y = pack_half2(o.z * inv, o.w * inv);
-  *reinterpret_cast<uint2*>(dst) = o2;
+  store(r, dim0, L, o);
 }
 
 }  // namespace pd

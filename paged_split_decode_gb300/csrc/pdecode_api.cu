@@ -288,8 +288,14 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
 
   cudaError_t e = launch_decode(dims->D, dims->kv_dtype, pl.nt, pl.hg > 1 ? 1 : 0, tk, tv, p, pl.grid,
                                 static_cast<cudaStream_t>(stream));
-  if (e == cudaSuccess && pl.n_desc > 0)
-    e = launch_split_combine(dims->D, p, static_cast<int>(pl.n_desc), static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess && pl.n_desc > 0) {
+    // pieces per split unit: about grid / units + 1 (balanced) or S (fixed);
+    // many pieces -> spread a unit's dims over CTAs so threads can share pieces
+    const long long per_unit = pl.splits == 0 ? pl.grid / (pl.units > 0 ? pl.units : 1) + 1 : pl.splits;
+    const int chunks = per_unit >= 4 ? dims->D / 32 : 1;
+    e = launch_split_combine(dims->D, p, static_cast<int>(pl.n_desc), chunks,
+                             static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? PD_OK : PD_ERR_CUDA;
 }
 

@@ -5,9 +5,10 @@
 
 namespace pd {
 
-cudaError_t launch_split_combine(int D, const DecodeParams& p, int n_desc, cudaStream_t stream) {
+cudaError_t launch_split_combine(int D, const DecodeParams& p, int n_desc, int dim_chunks,
+                                 cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(n_desc), static_cast<unsigned>(D / 32),
+  cfg.gridDim = dim3(static_cast<unsigned>(n_desc), static_cast<unsigned>(dim_chunks),
                      static_cast<unsigned>(p.hg));
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = 0;
