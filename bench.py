@@ -51,7 +51,8 @@ KERNEL_SOURCES = ["paged_split_decode_gb300/csrc/decode_kernel.cuh",
                   "paged_split_decode_gb300/csrc/ptx.cuh",
                   "paged_split_decode_gb300/csrc/decode_f16_d256.cu",
                   "paged_split_decode_gb300/csrc/launch.h",
-                  "paged_split_decode_gb300/csrc/pdecode_api.cu"]
+                  "paged_split_decode_gb300/csrc/pdecode_api.cu",
+                  "paged_split_decode_gb300/csrc/split_combine.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_f16_d256_gqa6_b32_traffic.md")
 
 
