@@ -78,6 +78,8 @@ def _load():
         lib.pdo_f16_to_f64.restype = ctypes.c_double
         lib.pdo_e4m3fn_to_f64.argtypes = [ctypes.c_uint8]
         lib.pdo_e4m3fn_to_f64.restype = ctypes.c_double
+        lib.pdo_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.pdo_bf16_to_f64.restype = ctypes.c_double
         lib.pdo_i8_to_f64.argtypes = [ctypes.c_uint8]
         lib.pdo_i8_to_f64.restype = ctypes.c_double
         lib.pdo_decode_paged.argtypes = [ctypes.POINTER(Dims), P, P, P, P, P, ctypes.c_double,
@@ -105,6 +107,10 @@ def f16_to_f64(bits: int) -> float:
 
 def e4m3fn_to_f64(code: int) -> float:
     return _load().pdo_e4m3fn_to_f64(code)
+
+
+def bf16_to_f64(bits: int) -> float:
+    return _load().pdo_bf16_to_f64(bits)
 
 
 def i8_to_f64(code: int) -> float:
@@ -141,8 +147,12 @@ def _as_bits(a, dtype):
     return a
 
 
+def _kv_kind(kv_fp8, kv_int8, bf16):
+    return 3 if bf16 else (2 if kv_int8 else int(bool(kv_fp8)))
+
+
 def _prepare(q, k_cache, v_cache, block_table, seq_lens, qlen, k_scale, v_scale, kv_fp8,
-             kv_int8=False):
+             kv_int8=False, bf16=False):
     q = _as_bits(q, np.uint16)
     kdt = np.uint8 if (kv_fp8 or kv_int8) else np.uint16
     k = _as_bits(k_cache, kdt)
@@ -155,7 +165,7 @@ def _prepare(q, k_cache, v_cache, block_table, seq_lens, qlen, k_scale, v_scale,
     assert bt.ndim == 2 and bt.shape[0] == B
     assert q.shape[0] == B * qlen and q.shape[2] == D
     Hq = q.shape[1]
-    dims = Dims(B, qlen, Hq, Hkv, D, bs, num_blocks, bt.shape[1], 2 if kv_int8 else int(bool(kv_fp8)),
+    dims = Dims(B, qlen, Hq, Hkv, D, bs, num_blocks, bt.shape[1], _kv_kind(kv_fp8, kv_int8, bf16),
                 float(k_scale), float(v_scale))
     return dims, q, k, v, bt, sl
 
@@ -174,18 +184,20 @@ def _run_rows(n_rows, threads, fn):
 
 
 def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, qlen=1,
-                 k_scale=1.0, v_scale=1.0, kv_fp8=False, threads=None, rows=None, kv_int8=False):
+                 k_scale=1.0, v_scale=1.0, kv_fp8=False, threads=None, rows=None, kv_int8=False,
+                 bf16=False):
     """One-shot fp64 paged decode. Returns float64 [B*qlen, Hq, D].
 
     q: fp16 [B*qlen, Hq, D]; caches: fp16 (or uint8 e4m3fn codes with
     kv_fp8=True, or int8 codes as uint8 with kv_int8=True)
-    [num_blocks, block_size, Hkv, D]; block_table int32
-    [B, max_blocks]; seq_lens int32 [B]. ``rows`` = (begin, end) restricts the
-    computed output rows (flattened (token, head) index); the others stay 0.
+    [num_blocks, block_size, Hkv, D]; with bf16=True q and both caches hold
+    bfloat16 bit patterns (uint16). block_table int32 [B, max_blocks];
+    seq_lens int32 [B]. ``rows`` = (begin, end) restricts the computed output
+    rows (flattened (token, head) index); the others stay 0.
     """
     lib = _load()
     dims, q, k, v, bt, sl = _prepare(q, k_cache, v_cache, block_table, seq_lens, qlen,
-                                     k_scale, v_scale, kv_fp8, kv_int8)
+                                     k_scale, v_scale, kv_fp8, kv_int8, bf16)
     out = np.zeros((q.shape[0], q.shape[1], q.shape[2]), dtype=np.float64)
     r0, r1 = rows if rows is not None else (0, q.shape[0] * q.shape[1])
     fn = lambda a, b: lib.pdo_decode_paged(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(bt),
@@ -197,14 +209,14 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, ql
 
 def decode_paged_split(q, k_cache, v_cache, block_table, seq_lens, scale, num_splits, window=0,
                        qlen=1, k_scale=1.0, v_scale=1.0, kv_fp8=False, threads=None,
-                       return_partials=False, kv_int8=False):
+                       return_partials=False, kv_int8=False, bf16=False):
     """Split-mode fp64 paged decode (chunks + online softmax + combine).
 
     Returns out, or (out, m, l, O) with m/l [rows, S] and O [rows, S, D] when
     ``return_partials`` (rows = B*qlen*Hq, m in natural-log units)."""
     lib = _load()
     dims, q, k, v, bt, sl = _prepare(q, k_cache, v_cache, block_table, seq_lens, qlen,
-                                     k_scale, v_scale, kv_fp8, kv_int8)
+                                     k_scale, v_scale, kv_fp8, kv_int8, bf16)
     S = int(num_splits)
     n_rows = q.shape[0] * q.shape[1]
     D = q.shape[2]
@@ -221,7 +233,7 @@ def decode_paged_split(q, k_cache, v_cache, block_table, seq_lens, scale, num_sp
 
 def decode_paged_varlen(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, scale,
                         window=0, k_scale=1.0, v_scale=1.0, kv_fp8=False, kv_int8=False,
-                        threads=None):
+                        threads=None, bf16=False):
     """fp64 paged decode with a query count per sequence: sequence b owns rows
     query_start_loc[b] .. query_start_loc[b+1]-1 of q, and is the one-shot
     decode of that single sequence with qlen = the row count. Rows outside
@@ -237,7 +249,7 @@ def decode_paged_varlen(q, k_cache, v_cache, block_table, seq_lens, query_start_
             continue
         out[a:e] = decode_paged(q[a:e], k_cache, v_cache, bt[b:b + 1], sl[b:b + 1], scale,
                                 window=window, qlen=e - a, k_scale=k_scale, v_scale=v_scale,
-                                kv_fp8=kv_fp8, kv_int8=kv_int8, threads=threads)
+                                kv_fp8=kv_fp8, kv_int8=kv_int8, threads=threads, bf16=bf16)
     return out
 
 
@@ -289,7 +301,7 @@ def write_kv_cache(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale=1.0, v_
 
 __all__ = ["build", "decode_paged", "decode_paged_split", "decode_paged_varlen", "combine",
            "write_kv_cache",
-           "f16_to_f64", "e4m3fn_to_f64", "i8_to_f64", "e4m3fn_encode", "i8_encode",
+           "f16_to_f64", "bf16_to_f64", "e4m3fn_to_f64", "i8_to_f64", "e4m3fn_encode", "i8_encode",
            "default_threads"]
 
 if __name__ == "__main__":  # pragma: no cover

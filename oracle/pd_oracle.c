@@ -32,7 +32,10 @@
  *     a code c is decode(c) * k_scale (or v_scale); int8 KV holds signed
  *     two's-complement codes with the same per-cache scales ("Purpose": the
  *     fp8 and int8 decode wrappers share the body);
- *   - a row with no visible key is all zeros.
+ *   - a row with no visible key is all zeros;
+ *   - bfloat16 (not on the pages): a bfloat16 model keeps q and both caches
+ *     in bfloat16 (kv_kind 3); every value is still converted to fp64
+ *     exactly and the arithmetic is the same.
  *
  * Every value is converted to fp64 exactly and all arithmetic is fp64, in
  * key order, with no blocking beyond what each function states.
@@ -51,7 +54,8 @@
 typedef struct {
   int B, qlen, Hq, Hkv, D;
   int block_size, num_blocks, max_blocks_per_seq;
-  int kv_kind;      /* 0: IEEE binary16 bit patterns; 1: e4m3fn bytes; 2: int8 codes */
+  int kv_kind;      /* 0: IEEE binary16 bit patterns; 1: e4m3fn bytes; 2: int8 codes;
+                       3: bfloat16 bit patterns (q is then bfloat16 as well) */
   double k_scale;   /* fp8 / int8: value = decode(code) * k_scale */
   double v_scale;
 } pdo_dims;
@@ -87,6 +91,22 @@ double pdo_e4m3fn_to_f64(uint8_t c) {
   return sign ? -v : v;
 }
 
+/* bfloat16: 1 sign, 8 exponent (bias 127), 7 fraction bits -- the upper half
+ * of an IEEE binary32. */
+double pdo_bf16_to_f64(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 7) & 0xff;
+  int f = h & 0x7f;
+  double v;
+  if (e == 0)
+    v = ldexp((double)f, -133); /* subnormal: f/128 * 2^-126 */
+  else if (e == 255)
+    v = f ? NAN : INFINITY;
+  else
+    v = ldexp((double)(128 + f), e - 134); /* (1 + f/128) * 2^(e-127) */
+  return sign ? -v : v;
+}
+
 /* Signed 8-bit two's-complement code. */
 double pdo_i8_to_f64(uint8_t c) { return (double)(int8_t)c; }
 
@@ -96,7 +116,14 @@ static double cache_at(const pdo_dims* d, const void* cache, double fp8_scale, l
   long idx = ((blk * d->block_size + slot) * (long)d->Hkv + kh) * d->D + x;
   if (d->kv_kind == 1) return pdo_e4m3fn_to_f64(((const uint8_t*)cache)[idx]) * fp8_scale;
   if (d->kv_kind == 2) return pdo_i8_to_f64(((const uint8_t*)cache)[idx]) * fp8_scale;
+  if (d->kv_kind == 3) return pdo_bf16_to_f64(((const uint16_t*)cache)[idx]);
   return pdo_f16_to_f64(((const uint16_t*)cache)[idx]);
+}
+
+/* Element x of a query row (fp16, or bfloat16 with bfloat16 caches). */
+static double q_at(const pdo_dims* d, const uint16_t* q, long rho, int x) {
+  uint16_t bits = q[rho * d->D + x];
+  return d->kv_kind == 3 ? pdo_bf16_to_f64(bits) : pdo_f16_to_f64(bits);
 }
 
 /* Visible key range [*lo, *hi] of query token i of a sequence of length L.
@@ -158,7 +185,7 @@ int pdo_decode_paged(const pdo_dims* d, const uint16_t* q, const void* k_cache,
     long n = hi - lo + 1;
     s = (double*)realloc(s, sizeof(double) * n);
     if (!s) { rc = PDO_ERR_NOMEM; break; }
-    for (int x = 0; x < D; ++x) qv[x] = pdo_f16_to_f64(q[rho * D + x]);
+    for (int x = 0; x < D; ++x) qv[x] = q_at(d, q, rho, x);
     double M = -INFINITY;
     for (long j = lo; j <= hi; ++j) {
       long blk = phys_block(d, block_table, b, j);
@@ -269,7 +296,7 @@ int pdo_decode_paged_split(const pdo_dims* d, const uint16_t* q, const void* k_c
       n_blocks = hi0 / bs - first_block + 1;
     }
     long chunk = (n_blocks + S - 1) / S;
-    for (int x = 0; x < D; ++x) qv[x] = pdo_f16_to_f64(q[rho * D + x]);
+    for (int x = 0; x < D; ++x) qv[x] = q_at(d, q, rho, x);
     for (int s = 0; s < S && any; ++s) {
       long cb0 = first_block + (long)s * chunk;
       long cb1 = cb0 + chunk;

@@ -8,7 +8,8 @@ and returned as CPU tensors.
 Recipe (shapes follow the benchmark commands of opengfx1030/vllm-rdna pull
 request #33, "Test Plan" step 3, and the geometry of its results comment):
 
-* Q, K, V values are i.i.d. N(0, 1) drawn in fp32 and rounded to fp16.
+* Q, K, V values are i.i.d. N(0, 1) drawn in fp32 and rounded to fp16 (or,
+  for the bfloat16 kind, to bfloat16 -- q and both caches).
 * fp8 KV: the N(0, 1) fp32 draw is divided by one per-cache scale
   ``amax / 448`` (448 is the largest finite e4m3fn value), clamped to
   [-448, 448] and rounded to e4m3fn by torch's CPU cast; the cache holds the
@@ -53,6 +54,7 @@ class Workload:
     num_splits: int = 0
     kv_fp8: bool = False
     kv_int8: bool = False
+    bf16: bool = False         # q, caches (and the output) in bfloat16
     k_scale: float = 1.0
     v_scale: float = 1.0
     meta: dict = field(default_factory=dict)
@@ -138,7 +140,8 @@ def make_workload(*, B, Hq, Hkv, D, seq_lens, qlen=1, block_size=BLOCK_SIZE, lay
     if max_blocks_per_seq is None:
         max_blocks_per_seq = max([blocks_needed(L, block_size) for L in seq_lens] + [1])
     table, pool = make_block_table(gen, seq_lens, max_blocks_per_seq, layout, pool_blocks, block_size)
-    q = _normal(gen, (B * qlen, Hq, D)).to(torch.float16)
+    qf = _normal(gen, (B * qlen, Hq, D))
+    q = qf.to(torch.bfloat16) if kv == "bf16" else qf.to(torch.float16)
     kf = _normal(gen, (pool, block_size, Hkv, D))
     vf = _normal(gen, (pool, block_size, Hkv, D))
     kv_fp8 = kv_int8 = False
@@ -153,6 +156,9 @@ def make_workload(*, B, Hq, Hkv, D, seq_lens, qlen=1, block_size=BLOCK_SIZE, lay
     elif kv == "f16":
         k_cache, v_cache = kf.to(torch.float16), vf.to(torch.float16)
         k_scale = v_scale = 1.0
+    elif kv == "bf16":
+        k_cache, v_cache = kf.to(torch.bfloat16), vf.to(torch.bfloat16)
+        k_scale = v_scale = 1.0
     else:
         raise ValueError(kv)
     if stale == "nan":
@@ -163,6 +169,8 @@ def make_workload(*, B, Hq, Hkv, D, seq_lens, qlen=1, block_size=BLOCK_SIZE, lay
             for c in (k_cache, v_cache):
                 if c.dtype == torch.float16:
                     c.view(torch.int16)[blk, L % block_size:] = 0x7E00
+                elif c.dtype == torch.bfloat16:
+                    c.view(torch.int16)[blk, L % block_size:] = 0x7FC0
                 elif kv == "fp8":
                     c[blk, L % block_size:] = 0x7F
                 else:
@@ -173,7 +181,7 @@ def make_workload(*, B, Hq, Hkv, D, seq_lens, qlen=1, block_size=BLOCK_SIZE, lay
                     seq_lens=torch.tensor(seq_lens, dtype=torch.int32),
                     scale=float(scale if scale is not None else 1.0 / math.sqrt(D)),
                     window=int(window), qlen=int(qlen), num_splits=int(num_splits), kv_fp8=kv_fp8,
-                    kv_int8=kv_int8,
+                    kv_int8=kv_int8, bf16=kv == "bf16",
                     k_scale=k_scale, v_scale=v_scale,
                     meta=dict(layout=layout, seed=int(seed), kv=kv))
 

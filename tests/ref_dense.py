@@ -11,7 +11,14 @@ import numpy as np
 import torch
 
 
-def decode_cache(cache, fp8, scale, int8=False):
+def _bf16_to_f64(x):
+    t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def decode_cache(cache, fp8, scale, int8=False, bf16=False):
+    if bf16:
+        return _bf16_to_f64(cache)
     if int8:
         return np.ascontiguousarray(cache).view(np.int8).astype(np.float64) * float(scale)
     if fp8:
@@ -39,12 +46,12 @@ def visibility(L, qlen, window):
 
 
 def attention(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, qlen=1,
-              kv_fp8=False, k_scale=1.0, v_scale=1.0, kv_int8=False, q_start=None):
+              kv_fp8=False, k_scale=1.0, v_scale=1.0, kv_int8=False, q_start=None, bf16=False):
     """q_start (optional, [B+1]): sequence b owns rows q_start[b]..q_start[b+1]-1
     and has that many query tokens; otherwise every sequence has qlen."""
-    qf = np.asarray(q).astype(np.float16).astype(np.float64)
-    Kc = decode_cache(k_cache, kv_fp8, k_scale, kv_int8)
-    Vc = decode_cache(v_cache, kv_fp8, v_scale, kv_int8)
+    qf = _bf16_to_f64(q) if bf16 else np.asarray(q).astype(np.float16).astype(np.float64)
+    Kc = decode_cache(k_cache, kv_fp8, k_scale, kv_int8, bf16)
+    Vc = decode_cache(v_cache, kv_fp8, v_scale, kv_int8, bf16)
     B = len(seq_lens)
     Hq, D = qf.shape[1], qf.shape[2]
     Hkv = Kc.shape[2]

@@ -23,12 +23,16 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
 def _np(t):
-    return t.numpy() if isinstance(t, torch.Tensor) else t
+    if isinstance(t, torch.Tensor):
+        if t.dtype == torch.bfloat16:  # numpy has no bfloat16: hand over the bit patterns
+            return t.view(torch.int16).numpy().view(np.uint16)
+        return t.numpy()
+    return t
 
 
 def run_oracle(oracle, w, split=None, **kw):
     args = dict(scale=w.scale, window=w.window, qlen=w.qlen, k_scale=w.k_scale,
-                v_scale=w.v_scale, kv_fp8=w.kv_fp8, kv_int8=w.kv_int8)
+                v_scale=w.v_scale, kv_fp8=w.kv_fp8, kv_int8=w.kv_int8, bf16=w.bf16)
     args.update(kw)
     if split is None:
         return oracle.decode_paged(_np(w.q), _np(w.k_cache), _np(w.v_cache), _np(w.block_table),
@@ -40,7 +44,7 @@ def run_oracle(oracle, w, split=None, **kw):
 def run_dense(w):
     return ref_dense.attention(_np(w.q), _np(w.k_cache), _np(w.v_cache), _np(w.block_table),
                                _np(w.seq_lens), w.scale, w.window, w.qlen, w.kv_fp8, w.k_scale,
-                               w.v_scale, w.kv_int8)
+                               w.v_scale, w.kv_int8, bf16=w.bf16)
 
 
 # ---- element decoders ----------------------------------------------------------
@@ -62,6 +66,16 @@ def test_e4m3fn_decoder_every_code(oracle_lib):
     nan = np.isnan(want)
     assert np.array_equal(np.isnan(got), nan)
     assert np.array_equal(got[~nan], want[~nan])
+
+
+def test_bf16_decoder_every_pattern(oracle_lib):
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    want = bits.view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle_lib.bf16_to_f64(b) for b in range(65536)])
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
 
 
 def test_int8_decoder_every_code(oracle_lib):
@@ -152,7 +166,7 @@ def _tiny(c, kv="f16", seed=7, layout="permuted", scale=None):
                                 pool_blocks=sum((L + c["bs"] - 1) // c["bs"] for L in c["lens"]) + 3)
 
 
-@pytest.mark.parametrize("kv", ["f16", "fp8", "int8"])
+@pytest.mark.parametrize("kv", ["f16", "fp8", "int8", "bf16"])
 @pytest.mark.parametrize("ci", range(len(TINY)))
 def test_oracle_matches_dense_bruteforce(oracle_lib, ci, kv):
     w = _tiny(TINY[ci], kv=kv, seed=100 + ci)
@@ -161,10 +175,11 @@ def test_oracle_matches_dense_bruteforce(oracle_lib, ci, kv):
     assert np.max(np.abs(got - want)) <= 1e-12
 
 
+@pytest.mark.parametrize("kv", ["f16", "bf16"])
 @pytest.mark.parametrize("ci", [1, 2, 4, 5])
-def test_oracle_matches_torch_sdpa(oracle_lib, ci):
+def test_oracle_matches_torch_sdpa(oracle_lib, ci, kv):
     """Dense fp64 torch scaled_dot_product_attention with a boolean mask per token."""
-    w = _tiny(TINY[ci], seed=200 + ci)
+    w = _tiny(TINY[ci], kv=kv, seed=200 + ci)
     got = run_oracle(oracle_lib, w)
     Kc = w.k_cache.to(torch.float64)
     Vc = w.v_cache.to(torch.float64)
@@ -242,7 +257,7 @@ def test_empty_rows_are_exact_zero(oracle_lib):
 
 # ---- invariants ------------------------------------------------------------------------
 
-@pytest.mark.parametrize("kv", ["f16", "fp8", "int8"])
+@pytest.mark.parametrize("kv", ["f16", "fp8", "int8", "bf16"])
 @pytest.mark.parametrize("ci", [1, 2, 3, 4, 5, 7])
 def test_split_mode_matches_one_shot(oracle_lib, ci, kv):
     w = _tiny(TINY[ci], kv=kv, seed=300 + ci)

@@ -41,6 +41,9 @@ MUTANTS = [
     ("writer_offset_transposed", "long dst = (blk * d->block_size + off) * row;",
      "long dst = (off * d->num_blocks + blk) * row;"),
     ("writer_padding_written", "if (slot < 0) continue;", "if (slot < 0) slot = -slot;"),
+    ("bf16_exponent_bias", "v = ldexp((double)(128 + f), e - 134);", "v = ldexp((double)(128 + f), e - 133);"),
+    ("bf16_q_read_as_f16", "return d->kv_kind == 3 ? pdo_bf16_to_f64(bits) : pdo_f16_to_f64(bits);",
+     "return pdo_f16_to_f64(bits);"),
 ]
 
 
@@ -64,10 +67,11 @@ def _pin_calls():
     import json
     cases = json.load(open(os.path.join(pins.GOLDEN, "closed_forms.json")))["cases"]
     calls = [(pins.test_f16_decoder_every_pattern, {}), (pins.test_e4m3fn_decoder_every_code, {}),
-             (pins.test_e4m3fn_spec_points, {}), (pins.test_int8_decoder_every_code, {})]
+             (pins.test_e4m3fn_spec_points, {}), (pins.test_int8_decoder_every_code, {}),
+             (pins.test_bf16_decoder_every_pattern, {})]
     calls += [(pins.test_golden_closed_forms, {"case": c}) for c in cases]
     calls += [(pins.test_oracle_matches_dense_bruteforce, {"ci": ci, "kv": kv})
-              for ci in range(len(pins.TINY)) for kv in ("f16", "fp8", "int8")]
+              for ci in range(len(pins.TINY)) for kv in ("f16", "fp8", "int8", "bf16")]
     calls += [(pins.test_split_mode_matches_one_shot, {"ci": ci, "kv": "f16"}) for ci in (2, 5)]
     calls += [(pins.test_combine_edge_cases, {}), (pins.test_split_partials_recombine, {})]
     calls += [(writer_pins.test_e4m3fn_encoder_golden_points, {}),
