@@ -256,8 +256,9 @@ class DeviceWorkload:
             self.k, self.v = codes(), codes()
             self.k_scale = self.v_scale = 1.0 / 64
         else:
-            self.k = torch.randn(shape, generator=dg, device=device, dtype=torch.float32).to(torch.float16)
-            self.v = torch.randn(shape, generator=dg, device=device, dtype=torch.float32).to(torch.float16)
+            dt = torch.bfloat16 if kv == "bf16" else torch.float16
+            self.k = torch.randn(shape, generator=dg, device=device, dtype=torch.float32).to(dt)
+            self.v = torch.randn(shape, generator=dg, device=device, dtype=torch.float32).to(dt)
             self.k_scale = self.v_scale = 1.0
         self.q_start = None
         if qlens is not None:  # a query count per sequence (rows q_start[b]..q_start[b+1]-1)
@@ -270,7 +271,7 @@ class DeviceWorkload:
         else:
             rows = B * qlen
         self.q = torch.randn((rows, Hq, Dh), generator=dg, device=device,
-                             dtype=torch.float32).to(torch.float16)
+                             dtype=torch.float32).to(torch.bfloat16 if kv == "bf16" else torch.float16)
         self.seq_lens = torch.tensor(seq_lens, dtype=torch.int32, device=device)
         self.out = torch.empty_like(self.q)
         self.B, self.qlen, self.window, self.Dh = B, qlen, window, Dh
@@ -378,6 +379,8 @@ def other_workloads(device, l2, seed, only=None):
         lambda: DeviceWorkload(device, l2, seed + 96, 32, 24, 4, 256, [4096] * 32, kv="fp8"), 0)
     add("gqa6_d256_L4096_b32_int8",
         lambda: DeviceWorkload(device, l2, seed + 95, 32, 24, 4, 256, [4096] * 32, kv="int8"), 0)
+    add("gqa6_d256_L4096_b32_bf16",
+        lambda: DeviceWorkload(device, l2, seed + 93, 32, 24, 4, 256, [4096] * 32, kv="bf16"), 0)
     gq = torch.Generator().manual_seed(seed + 94)
     qlens = torch.randint(1, 5, (32,), generator=gq).tolist()
     add("varlen_q1to4_d256_L4096_b32",

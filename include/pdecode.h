@@ -71,7 +71,9 @@ typedef enum {
 typedef enum {
   PD_KV_F16 = 0,       /* K and V caches hold IEEE binary16 */
   PD_KV_FP8_E4M3 = 1,  /* K and V caches hold OCP e4m3fn codes; value = decode(code) * scale */
-  PD_KV_INT8 = 2       /* K and V caches hold int8 two's-complement codes; value = code * scale */
+  PD_KV_INT8 = 2,      /* K and V caches hold int8 two's-complement codes; value = code * scale */
+  PD_KV_BF16 = 3       /* K and V caches, q and out hold bfloat16 (scales ignored); the products
+                          run on bfloat16 tensor-core operands (P rounded to bfloat16) */
 } pd_kv_dtype;
 
 /* Bits written into *error_flag by the device. */
@@ -89,7 +91,8 @@ typedef enum {
  *   num_blocks         blocks in each of the K and V caches
  *   max_blocks_per_seq columns of block_table
  *   kv_dtype           pd_kv_dtype
- *   k_scale, v_scale   fp8 / int8: per-cache dequantisation scales (ignored for fp16) */
+ *   k_scale, v_scale   fp8 / int8: per-cache dequantisation scales (ignored for fp16 and
+ *                      bfloat16) */
 typedef struct {
   int32_t B, Hq, Hkv, D;
   int32_t block_size, num_blocks, max_blocks_per_seq;
@@ -116,7 +119,8 @@ PD_API int pd_grid_ctas(const pd_dims* dims, int qlen, int num_splits, int sm_co
  * decode kernel, then a split-combine kernel launched with programmatic
  * dependent launch that merges the partials of units cut into pieces.
  *
- *   q            fp16 [B*qlen, Hq, D]; row b*qlen + i is query token i of sequence b
+ *   q            fp16 [B*qlen, Hq, D] (bfloat16 with PD_KV_BF16 caches); row
+ *                b*qlen + i is query token i of sequence b
  *   k_cache      [num_blocks, block_size, Hkv, D] fp16, e4m3fn or int8 (dims->kv_dtype)
  *   v_cache      same layout and dtype as k_cache
  *   block_table  int32 [B, max_blocks_per_seq]; entry [b][n] is the physical
@@ -129,7 +133,7 @@ PD_API int pd_grid_ctas(const pd_dims* dims, int qlen, int num_splits, int sm_co
  *   num_splits   0: balanced split of all visible key tiles over the SMs;
  *                >= 1: each sequence's visible tiles cut into num_splits
  *                contiguous chunks (1 = no split)
- *   out          fp16 [B*qlen, Hq, D], written in full (rows without a visible
+ *   out          q's type, [B*qlen, Hq, D], written in full (rows without a visible
  *                key are zeros); must not overlap the inputs
  *   workspace    device buffer of >= pd_workspace_bytes(...) bytes (contents need
  *                no initialisation; see pd_workspace_bytes)
@@ -181,16 +185,17 @@ PD_API pd_status decode_paged_combine(const float* part_m, const float* part_l, 
 /* Paged KV-cache writer: stores the K and V rows of new tokens where the
  * decode reads them (opengfx1030/vllm-rdna pull request #33, "Test Plan": the
  * decode is checked against the paged writer's layout).
- *   k_new, v_new  fp16 [num_tokens, Hkv, D], 16-byte aligned
+ *   k_new, v_new  fp16 [num_tokens, Hkv, D] (bfloat16 for a PD_KV_BF16 cache),
+ *                 16-byte aligned
  *   slot_mapping  int64 [num_tokens], device; token t goes to block
  *                 slot / block_size, offset slot % block_size of both caches;
  *                 a negative slot is a padding token and writes nothing
  *   k_cache,      [num_blocks, block_size, Hkv, D] of dims->kv_dtype (16-byte
- *   v_cache       aligned for fp16, 8-byte for one-byte codes), updated in place
+ *   v_cache       aligned for 16-bit kinds, 8-byte for one-byte codes), updated in place
  *   dims          Hkv, D (a multiple of 8), block_size, num_blocks, kv_dtype,
  *                 k_scale, v_scale are read; B, Hq, max_blocks_per_seq are not
  *   error_flag    device uint32 or NULL
- * fp16 caches receive the input bits unchanged. fp8 / int8 caches receive the
+ * fp16 and bfloat16 caches receive the input bits unchanged. fp8 / int8 caches receive the
  * code nearest to the IEEE fp32 quotient x / k_scale (V: v_scale): e4m3fn
  * with ties to even, saturating at +-448, NaN -> 0x7F; int8 with ties to even,
  * clamped to [-127, 127], NaN -> 0. A slot at or beyond num_blocks*block_size

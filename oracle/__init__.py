@@ -268,10 +268,11 @@ def combine(m, l, O):
 
 
 def write_kv_cache(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale=1.0, v_scale=1.0,
-                   kv_fp8=False, kv_int8=False, allow_bad_slots=False):
+                   kv_fp8=False, kv_int8=False, allow_bad_slots=False, bf16=False):
     """Paged KV-cache writer, in place on the numpy caches.
 
-    k_new/v_new: fp16 [T, Hkv, D]; slot_mapping: int64 [T] (negative = padding
+    k_new/v_new: fp16 [T, Hkv, D] (bfloat16 bits with bf16=True, written to
+    bfloat16 caches as they are); slot_mapping: int64 [T] (negative = padding
     token, skipped); caches [num_blocks, block_size, Hkv, D] fp16, or uint8
     holding e4m3fn codes (kv_fp8) or int8 codes (kv_int8). A slot beyond the
     cache raises ValueError, or with ``allow_bad_slots`` is skipped and the
@@ -288,7 +289,7 @@ def write_kv_cache(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale=1.0, v_
     num_blocks, bs, Hkv, D = kc.shape
     T = sm.shape[0]
     assert kn.shape == (T, Hkv, D) and vn.shape == kn.shape and vc.shape == kc.shape
-    dims = Dims(0, 1, Hkv, Hkv, D, bs, num_blocks, 0, 2 if kv_int8 else int(bool(kv_fp8)),
+    dims = Dims(0, 1, Hkv, Hkv, D, bs, num_blocks, 0, _kv_kind(kv_fp8, kv_int8, bf16),
                 float(np.float32(k_scale)), float(np.float32(v_scale)))
     rc = lib.pdo_write_kv_cache(ctypes.byref(dims), _ptr(kn), _ptr(vn), _ptr(sm), T, _ptr(kc),
                                 _ptr(vc))

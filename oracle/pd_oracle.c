@@ -394,7 +394,8 @@ int8_t pdo_i8_encode(float t) {
  * ([T, Hkv, D] fp16 bit patterns) and a slot slot_mapping[t] in the cache:
  * block slot / block_size, offset slot % block_size. A negative slot marks a
  * padding token and writes nothing. For every KV head h and dim x of a token:
- *   fp16 cache:  K[block][offset][h][x] = k_new[t][h][x]        (bit copy)
+ *   fp16 cache:  K[block][offset][h][x] = k_new[t][h][x]        (bit copy;
+ *                likewise a bfloat16 cache from bfloat16 input)
  *   fp8 cache:   pdo_e4m3fn_encode(fp32(k_new) / fp32(k_scale))
  *   int8 cache:  pdo_i8_encode(fp32(k_new) / fp32(k_scale))
  * and likewise V with v_scale. A slot at or beyond num_blocks * block_size
@@ -404,7 +405,7 @@ int8_t pdo_i8_encode(float t) {
 int pdo_write_kv_cache(const pdo_dims* d, const uint16_t* k_new, const uint16_t* v_new,
                        const int64_t* slot_mapping, long T, void* k_cache, void* v_cache) {
   if (!d || T < 0 || d->Hkv < 1 || d->D < 1 || d->block_size < 1 || d->num_blocks < 0 ||
-      d->kv_kind < 0 || d->kv_kind > 2)
+      d->kv_kind < 0 || d->kv_kind > 3)
     return PDO_ERR_ARGS;
   const long row = (long)d->Hkv * d->D;
   const int64_t cap = (int64_t)d->num_blocks * d->block_size;
@@ -418,7 +419,7 @@ int pdo_write_kv_cache(const pdo_dims* d, const uint16_t* k_new, const uint16_t*
     long dst = (blk * d->block_size + off) * row;
     for (long e = 0; e < row; ++e) {
       uint16_t kx = k_new[t * row + e], vx = v_new[t * row + e];
-      if (d->kv_kind == 0) {
+      if (d->kv_kind == 0 || d->kv_kind == 3) {  /* 16-bit caches: the input's bits */
         ((uint16_t*)k_cache)[dst + e] = kx;
         ((uint16_t*)v_cache)[dst + e] = vx;
       } else {

@@ -20,6 +20,7 @@ _lock = threading.Lock()
 PD_KV_F16 = 0
 PD_KV_FP8_E4M3 = 1
 PD_KV_INT8 = 2
+PD_KV_BF16 = 3
 DEVERR_BLOCK_ID = 1
 DEVERR_SEQ_LEN = 2
 DEVERR_TIMEOUT = 4
@@ -106,17 +107,20 @@ def _check(code: int, what: str):
 
 
 def make_dims(B, Hq, Hkv, D, block_size, num_blocks, max_blocks_per_seq, kv_fp8=False,
-              k_scale=1.0, v_scale=1.0, kv_int8=False) -> PdDims:
-    kind = PD_KV_INT8 if kv_int8 else (PD_KV_FP8_E4M3 if kv_fp8 else PD_KV_F16)
+              k_scale=1.0, v_scale=1.0, kv_int8=False, kv_bf16=False) -> PdDims:
+    kind = (PD_KV_BF16 if kv_bf16 else PD_KV_INT8 if kv_int8
+            else PD_KV_FP8_E4M3 if kv_fp8 else PD_KV_F16)
     return PdDims(int(B), int(Hq), int(Hkv), int(D), int(block_size), int(num_blocks),
                   int(max_blocks_per_seq), kind, float(k_scale), float(v_scale))
 
 
 def kv_kind_of(k_cache) -> int:
-    """fp16 caches -> PD_KV_F16; torch.int8 -> PD_KV_INT8; uint8 or float8_e4m3fn
-    -> PD_KV_FP8_E4M3."""
+    """fp16 caches -> PD_KV_F16; bfloat16 -> PD_KV_BF16; torch.int8 ->
+    PD_KV_INT8; uint8 or float8_e4m3fn -> PD_KV_FP8_E4M3."""
     if k_cache.dtype == torch.float16:
         return PD_KV_F16
+    if k_cache.dtype == torch.bfloat16:
+        return PD_KV_BF16
     if k_cache.dtype == torch.int8:
         return PD_KV_INT8
     if k_cache.dtype in (torch.uint8, torch.float8_e4m3fn):
@@ -129,7 +133,7 @@ def dims_of(q, k_cache, block_table, qlen, kv_fp8=None, k_scale=1.0, v_scale=1.0
     kind = kv_kind_of(k_cache)
     return make_dims(block_table.shape[0], q.shape[1], Hkv, D, bs, num_blocks,
                      block_table.shape[1], kind == PD_KV_FP8_E4M3, k_scale, v_scale,
-                     kind == PD_KV_INT8)
+                     kind == PD_KV_INT8, kind == PD_KV_BF16)
 
 
 def workspace_bytes(dims: PdDims, qlen: int, num_splits: int, sm_count: int = 0) -> int:
@@ -181,8 +185,9 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, ql
     """
     lib = load()
     kind = kv_kind_of(k_cache)
-    kv_dt = {PD_KV_F16: torch.float16, PD_KV_INT8: torch.int8,
+    kv_dt = {PD_KV_F16: torch.float16, PD_KV_INT8: torch.int8, PD_KV_BF16: torch.bfloat16,
              PD_KV_FP8_E4M3: (torch.uint8, torch.float8_e4m3fn)}[kind]
+    q_dt = torch.bfloat16 if kind == PD_KV_BF16 else torch.float16
     dims = dims_of(q, k_cache, block_table, qlen, None, k_scale, v_scale)
     if out is None:
         out = torch.empty_like(q)
@@ -200,11 +205,11 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, ql
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
     flag_ptr = None if error_flag is None else _dev_ptr(error_flag, "error_flag", (torch.int32, torch.uint32))
-    rc = lib.decode_paged(_dev_ptr(q, "q", torch.float16), _dev_ptr(k_cache, "k_cache", kv_dt),
+    rc = lib.decode_paged(_dev_ptr(q, "q", q_dt), _dev_ptr(k_cache, "k_cache", kv_dt),
                           _dev_ptr(v_cache, "v_cache", kv_dt),
                           _dev_ptr(block_table, "block_table", torch.int32),
                           _dev_ptr(seq_lens, "seq_lens", torch.int32), float(scale), int(window),
-                          int(qlen), int(num_splits), _dev_ptr(out, "out", torch.float16),
+                          int(qlen), int(num_splits), _dev_ptr(out, "out", q_dt),
                           ctypes.byref(dims), ws_ptr or None, ws_bytes, flag_ptr, stream)
     _check(rc, "decode_paged")
     return out
@@ -219,8 +224,9 @@ def decode_paged_varlen(q, k_cache, v_cache, block_table, seq_lens, query_start_
     left as they were)."""
     lib = load()
     kind = kv_kind_of(k_cache)
-    kv_dt = {PD_KV_F16: torch.float16, PD_KV_INT8: torch.int8,
+    kv_dt = {PD_KV_F16: torch.float16, PD_KV_INT8: torch.int8, PD_KV_BF16: torch.bfloat16,
              PD_KV_FP8_E4M3: (torch.uint8, torch.float8_e4m3fn)}[kind]
+    q_dt = torch.bfloat16 if kind == PD_KV_BF16 else torch.float16
     dims = dims_of(q, k_cache, block_table, max_qlen, None, k_scale, v_scale)
     if out is None:
         out = torch.zeros_like(q)
@@ -239,13 +245,13 @@ def decode_paged_varlen(q, k_cache, v_cache, block_table, seq_lens, query_start_
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
     flag_ptr = None if error_flag is None else _dev_ptr(error_flag, "error_flag", (torch.int32, torch.uint32))
-    rc = lib.decode_paged_varlen(_dev_ptr(q, "q", torch.float16), _dev_ptr(k_cache, "k_cache", kv_dt),
+    rc = lib.decode_paged_varlen(_dev_ptr(q, "q", q_dt), _dev_ptr(k_cache, "k_cache", kv_dt),
                                  _dev_ptr(v_cache, "v_cache", kv_dt),
                                  _dev_ptr(block_table, "block_table", torch.int32),
                                  _dev_ptr(seq_lens, "seq_lens", torch.int32),
                                  _dev_ptr(query_start_loc, "query_start_loc", torch.int32),
                                  int(q.shape[0]), int(max_qlen), float(scale), int(window),
-                                 int(num_splits), _dev_ptr(out, "out", torch.float16),
+                                 int(num_splits), _dev_ptr(out, "out", q_dt),
                                  ctypes.byref(dims), ws_ptr or None, ws_bytes, flag_ptr, stream)
     _check(rc, "decode_paged_varlen")
     return out
@@ -278,8 +284,9 @@ def write_kv_cache(k_new, v_new, slot_mapping, k_cache, v_cache, *, k_scale=1.0,
     ``k_scale``/``v_scale``."""
     lib = load()
     kind = kv_kind_of(k_cache)
-    kv_dt = {PD_KV_F16: torch.float16, PD_KV_INT8: torch.int8,
+    kv_dt = {PD_KV_F16: torch.float16, PD_KV_INT8: torch.int8, PD_KV_BF16: torch.bfloat16,
              PD_KV_FP8_E4M3: (torch.uint8, torch.float8_e4m3fn)}[kind]
+    q_dt = torch.bfloat16 if kind == PD_KV_BF16 else torch.float16
     if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype:
         raise ValueError("v_cache must match k_cache in shape and dtype")
     num_blocks, bs, Hkv, D = k_cache.shape
@@ -287,12 +294,12 @@ def write_kv_cache(k_new, v_new, slot_mapping, k_cache, v_cache, *, k_scale=1.0,
     if k_new.shape != (T, Hkv, D) or v_new.shape != k_new.shape:
         raise ValueError("k_new/v_new must be [T, Hkv, D] with T = len(slot_mapping)")
     dims = make_dims(0, Hkv, Hkv, D, bs, num_blocks, 0, kind == PD_KV_FP8_E4M3, k_scale, v_scale,
-                     kind == PD_KV_INT8)
+                     kind == PD_KV_INT8, kind == PD_KV_BF16)
     if stream is None:
         stream = torch.cuda.current_stream(k_cache.device).cuda_stream
     flag_ptr = None if error_flag is None else _dev_ptr(error_flag, "error_flag", (torch.int32, torch.uint32))
-    rc = lib.write_kv_cache(_dev_ptr(k_new, "k_new", torch.float16),
-                            _dev_ptr(v_new, "v_new", torch.float16),
+    rc = lib.write_kv_cache(_dev_ptr(k_new, "k_new", q_dt),
+                            _dev_ptr(v_new, "v_new", q_dt),
                             _dev_ptr(slot_mapping, "slot_mapping", torch.int64), int(T),
                             _dev_ptr(k_cache, "k_cache", kv_dt), _dev_ptr(v_cache, "v_cache", kv_dt),
                             ctypes.byref(dims), flag_ptr, stream)

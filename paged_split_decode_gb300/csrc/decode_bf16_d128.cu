@@ -1,0 +1,47 @@
+// decode_bf16_d128.cu -- instantiations of the decode kernel for bfloat16 q, KV and output, D=128.
+// NT = row tiles of 8 query rows per KV head (rows per head = Hq/Hkv * qlen
+// <= 8*NT); KG = key groups (consumer warps per row tile). Per-head tiles
+// (HG = 1): two CTAs share each SM, so two producers keep the SM's TMA
+// traffic flowing. Head-group tiles (C1H, NT = 1, Hkv a multiple of 4): a
+// tile holds 16 keys of HG consecutive KV heads -- one contiguous run of the
+// cache per key -- and one CTA per SM holds a deep ring of them; each head has
+// its own consumer warps (DS of them splitting D). The ring takes as many
+// stages as the shared memory allows. The head-group shapes are the ones that
+// measured fastest on GB300.
+#include "launch.h"
+
+namespace pd {
+namespace {
+constexpr int kKv = kKvBf16;
+constexpr int kD = 128;
+using C1 = CfgFor<kD, kKv, 1, 2, 2>;
+using C2 = CfgFor<kD, kKv, 2, 1, 2>;
+using C3 = CfgFor<kD, kKv, 3, 1, 2>;
+using C4 = CfgFor<kD, kKv, 4, 1, 2>;
+using C1H = CfgFor<kD, kKv, 1, 1, 1, 1, 4>;
+}  // namespace
+
+bool shape_bf16_d128(int nt, int grouped, KernelShape* out) {
+  if (grouped) return nt == 1 && shape_of<C1H>(out);
+  switch (nt) {
+    case 1: return shape_of<C1>(out);
+    case 2: return shape_of<C2>(out);
+    case 3: return shape_of<C3>(out);
+    case 4: return shape_of<C4>(out);
+    default: return false;
+  }
+}
+
+cudaError_t launch_bf16_d128(int nt, int grouped, const CUtensorMap& tk, const CUtensorMap& tv,
+                        const DecodeParams& p, int grid, cudaStream_t s) {
+  if (grouped) return nt == 1 ? launch_cfg<C1H>(tk, tv, p, grid, s) : cudaErrorInvalidValue;
+  switch (nt) {
+    case 1: return launch_cfg<C1>(tk, tv, p, grid, s);
+    case 2: return launch_cfg<C2>(tk, tv, p, grid, s);
+    case 3: return launch_cfg<C3>(tk, tv, p, grid, s);
+    case 4: return launch_cfg<C4>(tk, tv, p, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pd

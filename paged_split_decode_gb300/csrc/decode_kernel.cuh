@@ -57,8 +57,8 @@ constexpr unsigned long long kDrainLimitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeParams {
-  const __half* q;            // [total_q, Hq, D]
-  __half* out;                // [total_q, Hq, D]
+  const __half* q;            // [total_q, Hq, D] fp16 (bfloat16 bits for bfloat16 caches)
+  __half* out;                // [total_q, Hq, D] same type as q
   const int32_t* block_table; // [B, max_blocks]
   const int32_t* seq_lens;    // [B]
   const int32_t* q_start;     // [B+1] query rows of each sequence; null: b*qlen, qlen each
@@ -77,12 +77,31 @@ struct DecodeParams {
   int num_splits;             // 0: balanced
   float sl2;                  // scale * log2(e) * k_scale
   float out_scale;            // v_scale (1 for fp16)
+  int out_bf16;               // q and out hold bfloat16 (bfloat16 caches)
   unsigned long long timeout_ns;  // limit of every pipeline wait
   int inject;                     // fault injection: 1 = the producer issues no load
 };
 
-// KV element kinds: fp16, or one byte per element (OCP e4m3fn or int8 codes).
-constexpr int kKvF16 = 0, kKvFp8 = 1, kKvInt8 = 2;
+// KV element kinds: fp16, one byte per element (OCP e4m3fn or int8 codes), or
+// bfloat16 (then q and out are bfloat16 too and the products run in bfloat16).
+constexpr int kKvF16 = 0, kKvFp8 = 1, kKvInt8 = 2, kKvBf16 = 3;
+
+// Tensor-core product and output packing for the 16-bit operand type.
+template <bool BF16>
+__device__ __forceinline__ void mma_op(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                       uint32_t b1) {
+  if constexpr (BF16) mma_16816_bf16(d, a, b0, b1);
+  else mma_16816(d, a, b0, b1);
+}
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) return pack_bf162(lo, hi);
+  else return pack_half2(lo, hi);
+}
+template <bool BF16>
+__device__ __forceinline__ uint16_t pack1(float x) {
+  return static_cast<uint16_t>(pack2<BF16>(x, 0.f) & 0xffffu);
+}
 
 // Two byte codes of `w` (its low or high 16 bits, byte 0 / 2 the lower index)
 // widened to an fp16 pair, exactly. e4m3fn: the hardware conversion. int8:
@@ -121,7 +140,8 @@ struct Cfg {
   static constexpr int HG = HG_;
   static constexpr int kMinBlocks = MINB_;              // resident CTAs per SM the plan targets
   static constexpr int KV = KV_;
-  static constexpr bool FP8 = KV_ != kKvF16;   // one-byte elements (e4m3fn or int8)
+  static constexpr bool FP8 = KV_ == kKvFp8 || KV_ == kKvInt8;  // one-byte elements
+  static constexpr bool BF16 = KV_ == kKvBf16;  // bfloat16 operands, q and out
   static constexpr int kElem = FP8 ? 1 : 2;
   static constexpr int kSlabElems = 128 / kElem;        // one 128-byte swizzle row
   static constexpr int kSlabs = D / kSlabElems;
@@ -392,7 +412,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
     decode_paged_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
   constexpr int D = Cfg::D, KG = Cfg::KG, NS = Cfg::NS;
-  constexpr bool FP8 = Cfg::FP8;
+  constexpr bool FP8 = Cfg::FP8, BF16 = Cfg::BF16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -613,8 +633,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           ldsm_x4(rowb + slab * Cfg::kSlabBytes + ((chunk ^ (srow & 7)) << 4), a);
 #pragma unroll
           for (int n = 0; n < NTW; ++n) {
-            if (ksl & 1) mma_16816(sb[n], a, qf[ksl][n][0], qf[ksl][n][1]);
-            else mma_16816(sa[n], a, qf[ksl][n][0], qf[ksl][n][1]);
+            if (ksl & 1) mma_op<BF16>(sb[n], a, qf[ksl][n][0], qf[ksl][n][1]);
+            else mma_op<BF16>(sa[n], a, qf[ksl][n][0], qf[ksl][n][1]);
           }
         }
       } else {
@@ -647,8 +667,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
             a[3] = byte_pair_to_half2<Cfg::KV>(xb, true);
 #pragma unroll
             for (int n = 0; n < NTW; ++n) {
-              if (j & 1) mma_16816(sb[n], a, qf[ksl][n][0], qf[ksl][n][1]);
-              else mma_16816(sa[n], a, qf[ksl][n][0], qf[ksl][n][1]);
+              if (j & 1) mma_op<BF16>(sb[n], a, qf[ksl][n][0], qf[ksl][n][1]);
+              else mma_op<BF16>(sa[n], a, qf[ksl][n][0], qf[ksl][n][1]);
             }
           }
         }
@@ -720,8 +740,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
         l_r[n][0] = l_r[n][0] * al[n][0] + (p00 + p10);
         l_r[n][1] = l_r[n][1] * al[n][1] + (p01 + p11);
         rescale |= (al[n][0] != 1.f || al[n][1] != 1.f);
-        pb0[n] = movmatrix_trans(pack_half2(p00, p01));
-        pb1[n] = movmatrix_trans(pack_half2(p10, p11));
+        pb0[n] = movmatrix_trans(pack2<BF16>(p00, p01));
+        pb1[n] = movmatrix_trans(pack2<BF16>(p10, p11));
       }
       if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
@@ -758,7 +778,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
             a[0] &= vm01; a[1] &= vm01; a[2] &= vm23; a[3] &= vm23;
           }
 #pragma unroll
-          for (int n = 0; n < NTW; ++n) mma_16816(o[mtl][n], a, pb0[n], pb1[n]);
+          for (int n = 0; n < NTW; ++n) mma_op<BF16>(o[mtl][n], a, pb0[n], pb1[n]);
         }
       } else {
         // 32-dim group P32: lane reads 4 codes at dims 32*P32 + 4g .. +3 of keys
@@ -794,13 +814,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           a[2] = byte_pair_to_half2<Cfg::KV>(cd01, false);
           a[3] = byte_pair_to_half2<Cfg::KV>(cd01, true);
 #pragma unroll
-          for (int n = 0; n < NTW; ++n) mma_16816(o[2 * pl][n], a, pb0[n], pb1[n]);
+          for (int n = 0; n < NTW; ++n) mma_op<BF16>(o[2 * pl][n], a, pb0[n], pb1[n]);
           a[0] = byte_pair_to_half2<Cfg::KV>(ab23, false);
           a[1] = byte_pair_to_half2<Cfg::KV>(ab23, true);
           a[2] = byte_pair_to_half2<Cfg::KV>(cd23, false);
           a[3] = byte_pair_to_half2<Cfg::KV>(cd23, true);
 #pragma unroll
-          for (int n = 0; n < NTW; ++n) mma_16816(o[2 * pl + 1][n], a, pb0[n], pb1[n]);
+          for (int n = 0; n < NTW; ++n) mma_op<BF16>(o[2 * pl + 1][n], a, pb0[n], pb1[n]);
         }
       }
       __syncwarp();
@@ -907,10 +927,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           __half* dst = p.out + (static_cast<long long>(pc.q0 + i) * p.Hq + (pc.kh + hh) * p.G + hl) * D + dc * 8;
           const float inv = (Ls > 0.f) ? p.out_scale / Ls : 0.f;
           uint4 v;
-          v.x = pack_half2(v0.x * inv, v0.y * inv);
-          v.y = pack_half2(v0.z * inv, v0.w * inv);
-          v.z = pack_half2(v1.x * inv, v1.y * inv);
-          v.w = pack_half2(v1.z * inv, v1.w * inv);
+          v.x = pack2<BF16>(v0.x * inv, v0.y * inv);
+          v.y = pack2<BF16>(v0.z * inv, v0.w * inv);
+          v.z = pack2<BF16>(v1.x * inv, v1.y * inv);
+          v.w = pack2<BF16>(v1.z * inv, v1.w * inv);
           *reinterpret_cast<uint4*>(dst) = v;
         } else {
           const long long prow = static_cast<long long>(pc.slot) * Cfg::RP + hh * RH + r;
@@ -940,11 +960,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
               if constexpr (FP8) {
                 const int d0 = (mt >> 1) * 32 + 4 * g + 2 * (mt & 1);  // dims d0, d0 + 1
                 *reinterpret_cast<uint32_t*>(dst + d0) =
-                    pack_half2(o[mtl][n][c] * inv, o[mtl][n][2 + c] * inv);
+                    pack2<BF16>(o[mtl][n][c] * inv, o[mtl][n][2 + c] * inv);
               } else {
                 const int d0 = mt * 16 + g;                           // dims d0, d0 + 8
-                dst[d0] = __float2half_rn(o[mtl][n][c] * inv);
-                dst[d0 + 8] = __float2half_rn(o[mtl][n][2 + c] * inv);
+                reinterpret_cast<uint16_t*>(dst)[d0] = pack1<BF16>(o[mtl][n][c] * inv);
+                reinterpret_cast<uint16_t*>(dst)[d0 + 8] = pack1<BF16>(o[mtl][n][2 + c] * inv);
               }
             }
           } else {
@@ -1063,8 +1083,13 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
     const int i = r / p.G, hl = r % p.G;
     __half* dst = p.out + (static_cast<long long>(q0 + i) * p.Hq + kh * p.G + hl) * D + dim0;
     uint2 o2;
-    o2.x = pack_half2(o.x * inv, o.y * inv);
-    o2.y = pack_half2(o.z * inv, o.w * inv);
+    if (p.out_bf16) {
+      o2.x = pack_bf162(o.x * inv, o.y * inv);
+      o2.y = pack_bf162(o.z * inv, o.w * inv);
+    } else {
+      o2.x = pack_half2(o.x * inv, o.y * inv);
+      o2.y = pack_half2(o.z * inv, o.w * inv);
+    }
     *reinterpret_cast<uint2*>(dst) = o2;
   };
 

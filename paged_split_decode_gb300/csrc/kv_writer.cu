@@ -5,8 +5,9 @@
 // Token t goes to block slot / block_size, offset slot % block_size of
 // [num_blocks, block_size, Hkv, D]; its Hkv*D elements are contiguous in both
 // the input [T, Hkv, D] and the cache, so the copy is a stream of 16-byte
-// input vectors (8 fp16 values) per token. fp16 caches get the bits as they
-// are; fp8 and int8 caches get the code nearest to the IEEE fp32 quotient
+// input vectors (8 values) per token. fp16 and bfloat16 caches get the input
+// bits as they are (the input has the cache's type); fp8 and int8 caches get
+// the code nearest to the IEEE fp32 quotient
 // x / scale: cvt.rn.satfinite to e4m3 (ties to even, +-448 at most, NaN ->
 // 0x7F), or round-to-nearest-even to an integer clamped to [-127, 127]
 // (NaN -> 0).
@@ -102,13 +103,15 @@ extern "C" pd_status write_kv_cache(const void* k_new, const void* v_new,
   if (num_tokens < 0 || d.Hkv < 1 || d.D < 8 || d.D % 8 != 0 || d.block_size < 1 ||
       d.num_blocks < 0)
     return PD_ERR_SHAPE;
-  if (d.kv_dtype != PD_KV_F16 && d.kv_dtype != PD_KV_FP8_E4M3 && d.kv_dtype != PD_KV_INT8)
+  if (d.kv_dtype != PD_KV_F16 && d.kv_dtype != PD_KV_FP8_E4M3 && d.kv_dtype != PD_KV_INT8 &&
+      d.kv_dtype != PD_KV_BF16)
     return PD_ERR_DTYPE;
   const long long row = static_cast<long long>(d.Hkv) * d.D;
   if (row / 8 > 0x7fffffffll) return PD_ERR_SHAPE;
   if (num_tokens == 0) return PD_OK;
   if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PD_ERR_NULL;
-  const uintptr_t cache_align = d.kv_dtype == PD_KV_F16 ? 15u : 7u;
+  const bool two_byte = d.kv_dtype == PD_KV_F16 || d.kv_dtype == PD_KV_BF16;
+  const uintptr_t cache_align = two_byte ? 15u : 7u;
   if ((reinterpret_cast<uintptr_t>(k_new) & 15u) || (reinterpret_cast<uintptr_t>(v_new) & 15u) ||
       (reinterpret_cast<uintptr_t>(k_cache) & cache_align) ||
       (reinterpret_cast<uintptr_t>(v_cache) & cache_align) ||
@@ -129,6 +132,7 @@ extern "C" pd_status write_kv_cache(const void* k_new, const void* v_new,
   const auto* vn = static_cast<const uint4*>(v_new);
   switch (d.kv_dtype) {
     case PD_KV_F16:
+    case PD_KV_BF16:  // 16-bit caches: the input bits as they are
       pd::kv_writer_kernel<PD_KV_F16><<<grid, pd::kWriterThreads, 0, s>>>(
           kn, vn, slot_mapping, items, vecs, slots, d.block_size, k_cache, v_cache, 1.f, 1.f,
           error_flag);

@@ -39,6 +39,8 @@ bool shape_fp8_d128(int nt, int grouped, KernelShape* out);
 bool shape_fp8_d256(int nt, int grouped, KernelShape* out);
 bool shape_i8_d128(int nt, int grouped, KernelShape* out);
 bool shape_i8_d256(int nt, int grouped, KernelShape* out);
+bool shape_bf16_d128(int nt, int grouped, KernelShape* out);
+bool shape_bf16_d256(int nt, int grouped, KernelShape* out);
 cudaError_t launch_f16_d128(int nt, int grouped, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
                             cudaStream_t);
 cudaError_t launch_f16_d256(int nt, int grouped, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
@@ -51,6 +53,10 @@ cudaError_t launch_i8_d128(int nt, int grouped, const CUtensorMap&, const CUtens
                            cudaStream_t);
 cudaError_t launch_i8_d256(int nt, int grouped, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
                            cudaStream_t);
+cudaError_t launch_bf16_d128(int nt, int grouped, const CUtensorMap&, const CUtensorMap&,
+                             const DecodeParams&, int, cudaStream_t);
+cudaError_t launch_bf16_d256(int nt, int grouped, const CUtensorMap&, const CUtensorMap&,
+                             const DecodeParams&, int, cudaStream_t);
 
 // Launch one configuration; sets the shared-memory opt-in once per device.
 template <class Cfg>

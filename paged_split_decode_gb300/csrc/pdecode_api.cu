@@ -16,6 +16,9 @@
 namespace pd {
 
 bool kernel_shape(int D, int kv, int nt, int grouped, KernelShape* out) {
+  if (kv == kKvBf16)
+    return D == 128 ? shape_bf16_d128(nt, grouped, out)
+                    : D == 256 && shape_bf16_d256(nt, grouped, out);
   if (D == 128)
     return kv == kKvFp8 ? shape_fp8_d128(nt, grouped, out) : kv == kKvInt8 ? shape_i8_d128(nt, grouped, out)
                                                                       : shape_f16_d128(nt, grouped, out);
@@ -27,6 +30,9 @@ bool kernel_shape(int D, int kv, int nt, int grouped, KernelShape* out) {
 
 cudaError_t launch_decode(int D, int kv, int nt, int grouped, const CUtensorMap& tk,
                           const CUtensorMap& tv, const DecodeParams& p, int grid, cudaStream_t s) {
+  if (kv == kKvBf16)
+    return D == 128 ? launch_bf16_d128(nt, grouped, tk, tv, p, grid, s)
+                    : launch_bf16_d256(nt, grouped, tk, tv, p, grid, s);
   if (D == 128)
     return kv == kKvFp8 ? launch_fp8_d128(nt, grouped, tk, tv, p, grid, s)
            : kv == kKvInt8 ? launch_i8_d128(nt, grouped, tk, tv, p, grid, s)
@@ -63,9 +69,10 @@ pd_status check_dims(const pd_dims* d, int qlen) {
       d->max_blocks_per_seq < 0 || qlen < 1)
     return PD_ERR_SHAPE;
   if (d->Hq % d->Hkv != 0) return PD_ERR_SHAPE;
-  if (d->kv_dtype != PD_KV_F16 && d->kv_dtype != PD_KV_FP8_E4M3 && d->kv_dtype != PD_KV_INT8)
+  if (d->kv_dtype != PD_KV_F16 && d->kv_dtype != PD_KV_FP8_E4M3 && d->kv_dtype != PD_KV_INT8 &&
+      d->kv_dtype != PD_KV_BF16)
     return PD_ERR_DTYPE;
-  if (d->kv_dtype != PD_KV_F16 &&
+  if ((d->kv_dtype == PD_KV_FP8_E4M3 || d->kv_dtype == PD_KV_INT8) &&
       (!std::isfinite(d->k_scale) || !std::isfinite(d->v_scale)))
     return PD_ERR_SHAPE;
   if (d->D != 128 && d->D != 256) return PD_ERR_UNSUPPORTED;
@@ -159,7 +166,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 bool encode_cache_map(CUtensorMap* m, const void* base, const pd_dims* d, int hg) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const bool byte = d->kv_dtype != PD_KV_F16;
+  const bool byte = d->kv_dtype == PD_KV_FP8_E4M3 || d->kv_dtype == PD_KV_INT8;
   const cuuint64_t elem = byte ? 1 : 2;
   const cuuint64_t rows = static_cast<cuuint64_t>(d->num_blocks) * d->block_size;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d->D), static_cast<cuuint64_t>(d->Hkv),
@@ -168,7 +175,10 @@ bool encode_cache_map(CUtensorMap* m, const void* base, const pd_dims* d, int hg
   cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elem), static_cast<cuuint32_t>(hg),
                        static_cast<cuuint32_t>(kTileKeys)};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+  const CUtensorMapDataType type = byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : d->kv_dtype == PD_KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(m, type, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -250,7 +260,7 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   if (!encode_cache_map(&tk, k_cache, dims, pl.hg) || !encode_cache_map(&tv, v_cache, dims, pl.hg))
     return PD_ERR_CUDA;
 
-  const bool fp8 = dims->kv_dtype != PD_KV_F16;  // a one-byte kind with scales
+  const bool fp8 = dims->kv_dtype == PD_KV_FP8_E4M3 || dims->kv_dtype == PD_KV_INT8;  // scaled codes
   DecodeParams p;
   p.q = static_cast<const __half*>(q);
   p.out = static_cast<__half*>(out);
@@ -283,6 +293,7 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   const double ks = fp8 ? static_cast<double>(dims->k_scale) : 1.0;
   p.sl2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 * ks);
   p.out_scale = fp8 ? dims->v_scale : 1.0f;
+  p.out_bf16 = dims->kv_dtype == PD_KV_BF16 ? 1 : 0;
   p.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   p.inject = g_inject.load(std::memory_order_relaxed);
 

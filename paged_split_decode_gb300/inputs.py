@@ -197,7 +197,7 @@ def make_varlen_workload(*, qlens, seed=0, name="varlen", **kw) -> Workload:
     starts = [0]
     for n in qlens:
         starts.append(starts[-1] + n)
-    w.q = _normal(gen, (starts[-1], w.Hq, w.D)).to(torch.float16)
+    w.q = _normal(gen, (starts[-1], w.Hq, w.D)).to(torch.bfloat16 if w.bf16 else torch.float16)
     w.q_start = torch.tensor(starts, dtype=torch.int32)
     w.qlen = max(qlens + [1])
     w.meta["qlens"] = qlens
