@@ -15,9 +15,9 @@ namespace {
 constexpr int kKv = kKvFp8;
 constexpr int kD = 128;
 using C1 = CfgFor<kD, kKv, 1, 2, 2>;
-using C2 = CfgFor<kD, kKv, 2, 1, 2>;
-using C3 = CfgFor<kD, kKv, 3, 1, 2>;
-using C4 = CfgFor<kD, kKv, 4, 1, 2>;
+using C2 = CfgFor<kD, kKv, 2, 1, 2, 1, 1, 2>;
+using C3 = CfgFor<kD, kKv, 3, 1, 2, 1, 1, 3>;
+using C4 = CfgFor<kD, kKv, 4, 1, 2, 1, 1, 4>;
 using C1H = CfgFor<kD, kKv, 1, 1, 1, 2, 4>;
 }  // namespace
 

@@ -127,7 +127,7 @@ __device__ __forceinline__ uint32_t byte_word_prep(uint32_t w) {
 }
 
 template <int D_, int KV_, int NT_, int KG_, int NS_, int MINB_, int DS_ = (NT_ == 1 ? 1 : 2),
-          int HG_ = 1>
+          int HG_ = 1, int RG_ = ((NT_ == 4 && DS_ == 2) ? 2 : 1)>
 struct Cfg {
   static constexpr int D = D_, NT = NT_, KG = KG_, NS = NS_;
   // HG KV heads per tile: a tile is 16 keys of HG consecutive heads, which sit
@@ -153,10 +153,13 @@ struct Cfg {
   // warp of a group covers every row tile of its row group for its part of D,
   // widens only its part of a one-byte tile, and the group sums the partial
   // scores through shared memory in a fixed order (bitwise identical in every
-  // warp of the group). NT == 4 with DS == 2: two row groups of two row tiles,
-  // so a warp's fragments fit.
+  // warp of the group). RG row groups split a head's NT row tiles between
+  // warps (NT == 4 with DS == 2: two groups of two, so a warp's fragments
+  // fit; RG == NT: one row tile per warp, which keeps each warp's softmax to
+  // its own rows at the price of every warp reading the whole tile).
   static constexpr int DS = DS_;
-  static constexpr int RG = (NT == 4 && DS == 2) ? 2 : 1;
+  static constexpr int RG = RG_;
+  static_assert(NT % RG == 0, "row groups take equal shares of the row tiles");
   static constexpr int NTW = NT / RG;                    // row tiles per warp
   static constexpr int kConsumerWarps = HG * KG * RG * DS;
   static constexpr int kConsumerThreads = kConsumerWarps * 32;

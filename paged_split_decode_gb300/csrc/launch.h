@@ -82,19 +82,21 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
 // 227 KiB for one CTA).
 constexpr int smem_limit(int minb) { return minb == 1 ? 227 * 1024 : 228 * 1024 / minb - 1024; }
 // The stage count is a multiple of KG (see Cfg).
-template <int D, int KV, int NT, int KG, int MINB, int DS, int HG, int NS = 32>
+template <int D, int KV, int NT, int KG, int MINB, int DS, int HG, int RG, int NS = 32>
 constexpr int ring_stages() {
   if constexpr (NS <= KG)
     return KG;
   else if constexpr (NS % KG != 0)
-    return ring_stages<D, KV, NT, KG, MINB, DS, HG, NS - 1>();
-  else if constexpr (Cfg<D, KV, NT, KG, NS, MINB, DS, HG>::kSmemBytes <= smem_limit(MINB))
+    return ring_stages<D, KV, NT, KG, MINB, DS, HG, RG, NS - 1>();
+  else if constexpr (Cfg<D, KV, NT, KG, NS, MINB, DS, HG, RG>::kSmemBytes <= smem_limit(MINB))
     return NS;
   else
-    return ring_stages<D, KV, NT, KG, MINB, DS, HG, NS - 1>();
+    return ring_stages<D, KV, NT, KG, MINB, DS, HG, RG, NS - 1>();
 }
-template <int D, int KV, int NT, int KG, int MINB, int DS = (NT == 1 ? 1 : 2), int HG = 1>
-using CfgFor = Cfg<D, KV, NT, KG, ring_stages<D, KV, NT, KG, MINB, DS, HG>(), MINB, DS, HG>;
+template <int D, int KV, int NT, int KG, int MINB, int DS = (NT == 1 ? 1 : 2), int HG = 1,
+          int RG = ((NT == 4 && DS == 2) ? 2 : 1)>
+using CfgFor =
+    Cfg<D, KV, NT, KG, ring_stages<D, KV, NT, KG, MINB, DS, HG, RG>(), MINB, DS, HG, RG>;
 
 template <class Cfg>
 bool shape_of(KernelShape* out) {
