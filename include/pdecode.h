@@ -103,8 +103,8 @@ typedef struct {
 /* Workspace bytes that decode_paged needs for these shapes, qlen and
  * num_splits (0 = balanced automatic split) on a device with sm_count SMs
  * (sm_count <= 0: the current device's). 0 means no workspace is needed (the
- * pointer may then be NULL). Layout: one 16-byte split descriptor per CTA range
- * (balanced) or per unit (fixed split), then the fp32 split partials. Every
+ * pointer may then be NULL). Layout: one 16-byte split descriptor per work
+ * unit (a sequence and a group of KV heads), then the fp32 split partials. Every
  * call writes what it later reads, so the buffer needs no initialisation and
  * one buffer serves any sequence of calls on one stream; calls that may run
  * at the same time must not share a workspace. Returns 0 for invalid dims. */

@@ -48,8 +48,8 @@ namespace pd {
 constexpr int kTileKeys = 16;      // keys per pipeline tile
 constexpr int kMaxAutoB = 1024;    // sequences handled by the balanced split
 // Split units are merged by a second kernel: the workspace opens with one
-// descriptor per entry (balanced mode: per CTA range, fixed mode: per unit)
-// naming the split unit whose first piece it holds, then the partials.
+// descriptor per unit (its pieces and their slots, or -1 when the unit was not
+// split), written by the unit's first piece, then the partials.
 constexpr uint32_t kErrBlockId = 1u, kErrSeqLen = 2u, kErrTimeout = 4u, kErrQueryStart = 16u;
 // Limit of the producer's final drain: every load it issued lands before the
 // CTA exits, whatever the (possibly short) pipeline wait limit.
@@ -65,7 +65,7 @@ struct DecodeParams {
   int total_q;                // rows of q and out
   float* ws_o;                // [slots, RP, D]   partial O (log2-domain weights)
   float* ws_ml;               // [slots, RP, 2]   partial (m, l), m in log2 units
-  int4* ws_desc;              // [n_desc] {unit, pieces, slot of piece 0, slot base} or unit -1
+  int4* ws_desc;              // [units] {unit, pieces, slot of piece 0, slot base} or unit -1
   int n_desc;
   int rows_padded;            // RP: rows per partial slot
   uint32_t* error_flag;       // may be null
@@ -466,8 +466,6 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
   work_init(p, s_pre, it);
   // the split-combine kernel may be scheduled now; it waits for this grid
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0 && p.num_splits == 0 && blockIdx.x < p.n_desc)
-    p.ws_desc[blockIdx.x] = make_int4(-1, 0, 0, 0);  // no split unit starts here (yet)
   Piece pc;
 
   if (is_producer) {
@@ -990,10 +988,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
         }
     }
     if (tid == 0 && p.n_desc > 0) {
-      // the first piece of a unit posts its descriptor for the split combine
-      // (no descriptors -- and no workspace -- without a split)
-      const bool first = p.num_splits == 0 ? (pc.npieces > 1 && pc.chunk == pc.first_slot_cta)
-                                            : (pc.chunk == 0);
+      // the first piece of every unit posts the unit's descriptor for the
+      // split combine: its pieces, or -1 when the unit was not split (no
+      // descriptors -- and no workspace -- without a split)
+      const bool first = p.num_splits == 0 ? pc.chunk == pc.first_slot_cta : pc.chunk == 0;
       if (first) {
         int4 d = make_int4(-1, 0, 0, 0);
         if (pc.npieces > 1) {
@@ -1002,7 +1000,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           d.z = pc.slot;
           d.w = p.num_splits == 0 ? 2 * pc.first_slot_cta : pc.slot;
         }
-        p.ws_desc[p.num_splits == 0 ? pc.chunk : pc.unit] = d;
+        p.ws_desc[pc.unit] = d;
       }
     }
     if constexpr (Cfg::kSmemMerge) named_bar_sync(1, Cfg::kConsumerThreads);  // merge buffers free again

@@ -124,7 +124,7 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
   if (splits == 0) {
     pl->grid = ctas;
     pl->slots = 2ll * ctas;  // a CTA's range holds at most two split pieces
-    pl->n_desc = ctas;       // at most one split unit starts in a CTA's range
+    pl->n_desc = pl->units;  // one descriptor per unit
   } else {
     const long long pieces = pl->units * splits;
     pl->grid = static_cast<int>(pieces < ctas ? (pieces > 0 ? pieces : 1) : ctas);
@@ -303,7 +303,7 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     // pieces per split unit: about grid / units + 1 (balanced) or S (fixed);
     // many pieces -> spread a unit's dims over CTAs so threads can share pieces
     const long long per_unit = pl.splits == 0 ? pl.grid / (pl.units > 0 ? pl.units : 1) + 1 : pl.splits;
-    const int chunks = per_unit >= 4 ? dims->D / 32 : 1;
+    const int chunks = per_unit >= 16 ? dims->D / 8 : per_unit >= 4 ? dims->D / 32 : 1;
     e = launch_split_combine(dims->D, p, static_cast<int>(pl.n_desc), chunks,
                              static_cast<cudaStream_t>(stream));
   }

@@ -59,11 +59,11 @@ def test_workspace_and_grid_plans(lib):
     up = lambda x: (x + 255) // 256 * 256
     # one row tile per head and Hkv % 4 == 0: head-group tiles (fp16 D=256:
     # two KV heads per tile), one persistent CTA per SM; balanced: one 16-byte
-    # split descriptor per CTA, two partial slots per CTA, 2 heads x 8 padded
-    # rows of D floats per slot
+    # split descriptor per unit (B * Hkv / 2), two partial slots per CTA,
+    # 2 heads x 8 padded rows of D floats per slot
     assert binding.grid_ctas(d, 1, 0, sm_count=152) == 152
     ws = binding.workspace_bytes(d, 1, 0, sm_count=152)
-    assert ws == up(152 * 16) + up(304 * 16 * 2 * 4) + 304 * 16 * 256 * 4
+    assert ws == up(64 * 16) + up(304 * 16 * 2 * 4) + 304 * 16 * 256 * 4
     # no split: no workspace at all; one CTA per unit (B * Hkv / 2 units)
     assert binding.workspace_bytes(d, 1, 1, sm_count=152) == 0
     assert binding.grid_ctas(d, 1, 1, sm_count=152) == 64
@@ -74,17 +74,17 @@ def test_workspace_and_grid_plans(lib):
     # fp8 D=256: four KV heads per tile, 32 rows per slot, B * Hkv / 4 units
     d8 = _dims(kv_fp8=True)
     assert binding.workspace_bytes(d8, 1, 0, sm_count=152) == \
-        up(152 * 16) + up(304 * 32 * 2 * 4) + 304 * 32 * 256 * 4
+        up(32 * 16) + up(304 * 32 * 2 * 4) + 304 * 32 * 256 * 4
     assert binding.grid_ctas(d8, 1, 1, sm_count=152) == 32
     # per-head tiles (Hkv = 2): two CTAs per SM, 8 padded rows per slot
     d2 = _dims(Hq=12, Hkv=2)
     assert binding.grid_ctas(d2, 1, 0, sm_count=152) == 304
     assert binding.workspace_bytes(d2, 1, 0, sm_count=152) == \
-        up(304 * 16) + up(608 * 8 * 2 * 4) + 608 * 8 * 256 * 4
+        up(64 * 16) + up(608 * 8 * 2 * 4) + 608 * 8 * 256 * 4
     assert binding.grid_ctas(d2, 1, 1, sm_count=152) == 64
     # qlen 3 x G 6 = 18 rows -> three row tiles of 8, per-head tiles
     ws3 = binding.workspace_bytes(_dims(B=8), 3, 0, sm_count=152)
-    assert ws3 == up(304 * 16) + up(608 * 24 * 2 * 4) + 608 * 24 * 256 * 4
+    assert ws3 == up(32 * 16) + up(608 * 24 * 2 * 4) + 608 * 24 * 256 * 4
 
 
 @pytest.mark.parametrize("kw,qlen", [
