@@ -143,3 +143,67 @@ def test_varlen_gqa6_batch32_full_size(pd):
     w = inputs.make_varlen_workload(qlens=qlens, B=32, Hq=24, Hkv=4, D=256, seq_lens=[4096] * 32,
                                     seed=12)
     check(gpu_varlen(pd, w, 0), ref_varlen(w))
+
+
+def test_writer_and_varlen_decode_in_one_cuda_graph(pd):
+    """The serving step -- write the new tokens' K/V, then decode a batch with a
+    query count per sequence -- captured once into a CUDA graph and replayed
+    after new values are written into the same buffers."""
+    Hq, Hkv, D, bs = 24, 4, 256, 16
+    qlens = [1, 3, 2]
+    lens = [700, 45, 1300]
+    B = len(lens)
+    nb = sum((L + bs - 1) // bs for L in lens) + 4
+    g = torch.Generator().manual_seed(90)
+    perm = torch.randperm(nb, generator=g).to(torch.int32)
+    mb = max((L + bs - 1) // bs for L in lens)
+    table = torch.full((B, mb), -1, dtype=torch.int32)
+    used = 0
+    for b, L in enumerate(lens):
+        n = (L + bs - 1) // bs
+        table[b, :n] = perm[used:used + n]
+        used += n
+    # the new tokens are the last qlen_b keys of each sequence
+    slots = torch.tensor([int(table[b, j // bs]) * bs + j % bs
+                          for b, L in enumerate(lens) for j in range(L - qlens[b], L)],
+                         dtype=torch.int64)
+    starts = torch.tensor([0, 1, 4, 6], dtype=torch.int32)
+    T = int(starts[-1])
+    kc = (torch.randn((nb, bs, Hkv, D), generator=g)).half().to(DEV)
+    vc = (torch.randn((nb, bs, Hkv, D), generator=g)).half().to(DEV)
+    q = torch.empty((T, Hq, D), dtype=torch.float16, device=DEV)
+    kn = torch.empty((T, Hkv, D), dtype=torch.float16, device=DEV)
+    vn = torch.empty_like(kn)
+    out = torch.empty_like(q)
+    bt, sl, qs, sm = table.to(DEV), torch.tensor(lens, dtype=torch.int32, device=DEV), \
+        starts.to(DEV), slots.to(DEV)
+    dims = pd.dims_of(q, kc, bt, max(qlens))
+    ws = torch.empty(max(pd.workspace_bytes(dims, max(qlens), 0), 1), dtype=torch.uint8, device=DEV)
+    stream = torch.cuda.Stream()
+
+    def step():
+        pd.write_kv_cache(kn, vn, sm, kc, vc)
+        pd.decode_paged_varlen(q, kc, vc, bt, sl, qs, max(qlens), 0.0625, out=out, workspace=ws)
+
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for seed in (1, 2):
+        gg = torch.Generator().manual_seed(seed)
+        q.copy_(torch.randn((T, Hq, D), generator=gg).half())
+        kn.copy_(torch.randn((T, Hkv, D), generator=gg).half())
+        vn.copy_(torch.randn((T, Hkv, D), generator=gg).half())
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        ko, vo = kc.cpu().numpy(), vc.cpu().numpy()
+        # the new tokens landed where the table says
+        for t, s_ in enumerate(slots.tolist()):
+            assert np.array_equal(ko[s_ // bs, s_ % bs], kn[t].cpu().numpy())
+        ref = oracle.decode_paged_varlen(q.cpu().numpy(), ko, vo, table.numpy(),
+                                         np.array(lens, np.int32), starts.numpy(), 0.0625)
+        g_ = out.float().cpu().numpy()
+        assert float(np.max(np.abs(g_ - ref))) <= TOL
