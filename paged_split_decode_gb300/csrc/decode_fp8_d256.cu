@@ -7,17 +7,17 @@
 // cache per key -- and one CTA per SM holds a deep ring of them; each head has
 // its own consumer warps (DS of them splitting D). The ring takes as many
 // stages as the shared memory allows. The head-group shapes are the ones that
-// measured fastest on GB300.
-#include "launch.h"
+// measured fastest on GB300. Units of 9 to 32 query rows per KV head (two to
+// four row tiles) run on the tensor-memory kernel of decode_tc8.cuh instead:
+// its products use the e4m3 codes themselves (tcgen05.mma kind::f8f6f4).
+#include "decode_tc8.cuh"
 
 namespace pd {
 namespace {
 constexpr int kKv = kKvFp8;
 constexpr int kD = 256;
 using C1 = CfgFor<kD, kKv, 1, 2, 2>;
-using C2 = CfgFor<kD, kKv, 2, 1, 2, 1, 1, 2>;
-using C3 = CfgFor<kD, kKv, 3, 1, 2, 1, 1, 3>;
-using C4 = CfgFor<kD, kKv, 4, 1, 2, 1, 1, 4>;
+using TC = Tc8<kD>;  // two to four row tiles: the tensor-core (tcgen05) kernel
 using C1H = CfgFor<kD, kKv, 1, 1, 1, 1, 4>;
 }  // namespace
 
@@ -25,9 +25,9 @@ bool shape_fp8_d256(int nt, int grouped, KernelShape* out) {
   if (grouped) return nt == 1 && shape_of<C1H>(out);
   switch (nt) {
     case 1: return shape_of<C1>(out);
-    case 2: return shape_of<C2>(out);
-    case 3: return shape_of<C3>(out);
-    case 4: return shape_of<C4>(out);
+    case 2:
+    case 3:
+    case 4: return shape_tc8<TC>(nt, out);
     default: return false;
   }
 }
@@ -37,9 +37,9 @@ cudaError_t launch_fp8_d256(int nt, int grouped, const CUtensorMap& tk, const CU
   if (grouped) return nt == 1 ? launch_cfg<C1H>(tk, tv, p, grid, s) : cudaErrorInvalidValue;
   switch (nt) {
     case 1: return launch_cfg<C1>(tk, tv, p, grid, s);
-    case 2: return launch_cfg<C2>(tk, tv, p, grid, s);
-    case 3: return launch_cfg<C3>(tk, tv, p, grid, s);
-    case 4: return launch_cfg<C4>(tk, tv, p, grid, s);
+    case 2:
+    case 3:
+    case 4: return launch_tc8<TC>(tk, tv, p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,0 +1,728 @@
+// decode_tc8.cuh -- paged decode attention for e4m3 caches on the 5th-generation
+// tensor cores (tcgen05, accumulators in tensor memory), for units with many
+// query rows per KV head (G * qlen up to 32: speculative verify, wide GQA).
+//
+// Same method and work split as decode_kernel.cuh (the per-head paged decode
+// of opengfx1030/vllm-rdna pull request #33, "Purpose"; split-K pieces merged
+// by the split-combine kernel), different engine:
+//  * A unit is (sequence, KV head); its visible 16-key tiles are cut into
+//    pieces by the balanced split (work_next). Within a piece, 8 consecutive
+//    tiles form a 128-key block. One producer warp TMA-loads each tile's K and
+//    V rows (128-byte swizzled, the layout the tensor cores read) into a ring
+//    of block stages.
+//  * One thread issues tcgen05.mma kind::f8f6f4 on the e4m3 codes themselves:
+//    S^T[128 keys x 96] = K Q^T into tensor memory, and later O^T[D x 96] +=
+//    V^T P^T. The K and V codes are never widened.
+//  * q (fp16) is scaled per row by a power of two and split exactly into three
+//    e4m3 terms, q = t1 + t2 + t3 (see split3_e4m3); the terms are stacked on
+//    the N side (3 x 32 rows) and their products summed when S^T is read. The
+//    softmax weights are split the same way and stacked on N for P.V; the
+//    three O^T accumulators are summed at the end of a piece.
+//  * Four softmax warps own the 128 keys of a block (one TMEM lane each): they
+//    read S^T, mask, take the per-row block maximum (warp transpose-reduce and
+//    a shared exchange), form the weights against a running maximum that is
+//    only raised when the block maximum exceeds it by more than 2^4 (then the
+//    O^T accumulator is rescaled in tensor memory), and write P^T: each key's
+//    thread stores its 32 row weights as one 32-byte row of an MN-major
+//    operand (32-byte swizzle). V^T is read by
+//    the product straight from the ring as an MN-major operand (each 128-byte
+//    key row is 128 consecutive dims). Keys past the sequence end or outside
+//    the piece get -inf scores and their V rows are zeroed in the ring.
+//  * K and V have rings of their own: a K stage is released when S^T is
+//    computed, a V stage when the P.V product that reads it completes.
+//  * At the end of a piece the warps read O^T (one output dim per thread) and
+//    write fp16 rows (unit done in one piece) or the fp32 (m, l, O) partial.
+//  * Every wait is bounded; after a timeout each role stops waiting and
+//    issuing but keeps the softmax warps' named-barrier sequence, so the CTA
+//    always reaches its exit, where the tensor memory is freed.
+#pragma once
+#include "launch.h"
+#include "tc5.cuh"
+
+namespace pd {
+
+template <int D_>
+struct Tc8 {
+  static constexpr int D = D_;
+  static constexpr int kSlabs = D / 128;            // 128-byte slabs of one e4m3 key row
+  static constexpr int kBlkTiles = 8;               // 16-key tiles per 128-key block
+  static constexpr int kSlabBlk = 128 * 128;        // one slab of a block: [128 keys][128 B]
+  static constexpr int kKBlk = kSlabs * kSlabBlk;   // K (or V) of one block
+  static constexpr int NBK = D == 256 ? 2 : 4;      // K ring stages
+  static constexpr int NBV = D == 256 ? 3 : 5;      // V ring stages (held until P.V completes)
+  static constexpr int kTileBox = 16 * 128;         // one TMA box: 16 keys x 128 bytes
+  static constexpr int kN = 32;                     // query rows per unit on the N side
+  static constexpr int kNT = 3 * kN;                // N of both products: three terms x 32 rows
+  static constexpr int kQSlab = kNT * 128;          // q operand, one slab: [term][32 rows][128 B]
+  static constexpr int kQBytes = kSlabs * kQSlab;
+  static constexpr int kPtTerm = 128 * kN;          // one P^T term: [128 keys][32 rows], MN-major
+  static constexpr int kThreads = 192;              // warps 0-3 softmax, 4 producer, 5 MMA
+  static constexpr int kProducerWarp = 4, kMmaWarp = 5;
+  static constexpr int kTmemCols = 512;             // S^T x2 (2 x 96), O^T (kSlabs x 96)
+  static constexpr int kColS = 0, kColO = 2 * kNT;
+  static constexpr uint32_t kIdescS = idesc_e4m3(128, kNT);               // K-major A and B
+  static constexpr uint32_t kIdescO = idesc_e4m3(128, kNT) | (3u << 15);  // A (V^T), B (P^T) MN-major
+  static constexpr float kRaise = 4.f;              // running max raised past this gap (log2)
+  static constexpr float kBias = 4.f;               // weights are 2^(x - m + kBias) <= 2^8
+
+  static constexpr int kOffV = NBK * kKBlk;
+  static constexpr int kOffQ = kOffV + NBV * kKBlk;
+  static constexpr int kOffPt = kOffQ + kQBytes;
+  static constexpr int kOffRed = kOffPt + 3 * kPtTerm;     // float [4 warps][32 rows]
+  static constexpr int kRowWords = 7 * 32;                 // row state: 7 arrays of 32 words
+  static constexpr int kOffRow = kOffRed + 4 * 32 * 4;
+  static constexpr int kOffBars = kOffRow + kRowWords * 4;
+  static constexpr int kBars = 2 * NBK + 2 * NBV + 8;
+  static constexpr int kOffTmem = kOffBars + kBars * 8;
+  static constexpr int kOffPre = kOffTmem + 16;
+  static constexpr int kSmemBytes = kOffPre + (kMaxAutoB + 1) * 4 + 1024;  // + alignment slack
+  static_assert(D == 128 || D == 256, "head size 128 or 256");
+  static_assert(kOffV % 1024 == 0 && kOffQ % 1024 == 0 && kOffPt % 1024 == 0 && kQSlab % 1024 == 0 &&
+                    kPtTerm % 1024 == 0,
+                "tensor-core operands start on 1024-byte swizzle atoms");
+  static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
+};
+
+// An fp16 pair to two e4m3fn codes (low half -> low byte), round to nearest
+// even, saturating at +-448.
+__device__ __forceinline__ uint32_t half2_to_e4m3x2(uint32_t h) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(d) : "r"(h));
+  return d;
+}
+// An fp16 pair x as three e4m3 code pairs whose values add up to x: t1 =
+// e4m3(x), t2 = e4m3(x - t1), t3 = e4m3(x - t1 - t2) (codes in the low 16
+// bits). Each difference is exact in fp16 (a multiple of x's last place, at
+// most half of t1's step), and three 4-bit significands cover fp16's 11 bits,
+// so the sum is x exactly unless a remainder falls below e4m3's subnormal
+// step 2^-9 (then the error is at most 2^-10). |x| <= 448.
+__device__ __forceinline__ void split3_e4m3(uint32_t x, uint32_t& t1, uint32_t& t2, uint32_t& t3) {
+  t1 = half2_to_e4m3x2(x);
+  const uint32_t f1 = e4m3x2_to_half2(static_cast<uint16_t>(t1));
+  const __half2 r1 = __hsub2(*reinterpret_cast<const __half2*>(&x), *reinterpret_cast<const __half2*>(&f1));
+  const uint32_t r1u = *reinterpret_cast<const uint32_t*>(&r1);
+  t2 = half2_to_e4m3x2(r1u);
+  const uint32_t f2 = e4m3x2_to_half2(static_cast<uint16_t>(t2));
+  const __half2 r2 = __hsub2(r1, *reinterpret_cast<const __half2*>(&f2));
+  t3 = half2_to_e4m3x2(*reinterpret_cast<const uint32_t*>(&r2));
+}
+
+// Row state arrays in shared memory (32 entries each).
+enum { kRowFsl = 0, kRowMu = 1, kRowAl = 2, kRowLo = 3, kRowHi = 4, kRowL = 5, kRowFlag = 6 };
+// Barriers: fullK[NBK], emptyK[NBK], fullV[NBV], emptyV[NBV], then these.
+enum { kBarSFull = 0, kBarSEmpty = 2, kBarPFull = 4, kBarPvDone = 5, kBarQFull = 6, kBarFinal = 7 };
+
+// 32 values, one per row, held by every lane of a warp -> lane l holds the
+// reduction of row l over the 32 lanes (5 butterfly rounds, 31 shuffles).
+template <bool MAX>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool up = (lane & w) != 0;
+#pragma unroll
+    for (int k = 0; k < w; ++k) {
+      const float send = up ? v[k] : v[k + w];
+      const float keep = up ? v[k + w] : v[k];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, w);
+      v[k] = MAX ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  return v[0];
+}
+
+// Posts a unit's split descriptor from its first piece (as decode_kernel).
+__device__ __forceinline__ void post_unit_descriptor(const DecodeParams& p, const Piece& pc) {
+  if (p.n_desc <= 0) return;
+  const bool first = p.num_splits == 0 ? pc.chunk == pc.first_slot_cta : pc.chunk == 0;
+  if (!first) return;
+  int4 d = make_int4(-1, 0, 0, 0);
+  if (pc.npieces > 1) {
+    d.x = pc.unit;
+    d.y = pc.npieces;
+    d.z = pc.slot;
+    d.w = p.num_splits == 0 ? 2 * pc.first_slot_cta : pc.slot;
+  }
+  p.ws_desc[pc.unit] = d;
+}
+
+// The four softmax warps (threads 0..127; thread i owns TMEM lane i: key i of
+// a block for S^T, output dim i (+128) for O^T).
+template <class T>
+__device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s_pre, WorkIter& it, Piece& pc,
+                                             uint8_t* smem, uint32_t sbase, uint32_t tmem, bool& ok) {
+  constexpr int D = T::D, NBK = T::NBK, NBV = T::NBV, S = T::kSlabs;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  float* rf = reinterpret_cast<float*>(smem + T::kOffRow);
+  int* ri = reinterpret_cast<int*>(smem + T::kOffRow);
+  float* red = reinterpret_cast<float*>(smem + T::kOffRed);
+  const uint32_t fullv0 = sbase + T::kOffBars + 16 * NBK, bx = fullv0 + 16 * NBV;
+  auto bar = [&](int i) -> uint32_t { return bx + 8 * i; };
+  const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's TMEM lanes
+  const uint32_t qs = sbase + T::kOffQ, pt = sbase + T::kOffPt;
+  uint32_t bq = 0;
+  // Pieces with nothing visible are finished on the spot (zero rows; such a
+  // unit is never split); returns the next piece that has tiles.
+  auto next_piece = [&](Piece& out) -> bool {
+    while (work_next(p, s_pre, it, out)) {
+      if (out.ntiles > 0) return true;
+      for (int item = tid; item < out.R * (D / 8); item += 128) {
+        const int r = item / (D / 8), dc = item % (D / 8);
+        const int i = r / p.G, hl = r % p.G;
+        *reinterpret_cast<uint4*>(p.out + (static_cast<long long>(out.q0 + i) * p.Hq + out.kh * p.G + hl) * D +
+                                  dc * 8) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (tid == 0) post_unit_descriptor(p, out);
+    }
+    return false;
+  };
+  // A piece's q terms and row state (the previous piece's S^T products are
+  // complete: its softmax has read all of them).
+  auto q_setup = [&](const Piece& pq) {
+    // ---- q rows as three e4m3 terms (the B operand of S^T, K-major, 128-byte
+    // swizzle), row score factors and visible key limits. Thread t: row t / 4,
+    // dims [(t % 4) D / 4, (t % 4 + 1) D / 4).
+    {
+      const int r = tid >> 2, part = tid & 3;
+      constexpr int NCH = D / 64;  // 16-dim chunks per thread
+      const __half* qrow = nullptr;
+      if (r < pq.R) {
+        const int i = r / p.G, hl = r % p.G;
+        qrow = p.q + (static_cast<long long>(pq.q0 + i) * p.Hq + pq.kh * p.G + hl) * D;
+      }
+      uint4 qv[NCH][2];
+      float mx = 0.f;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        const int d0 = part * (D / 4) + 16 * c;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          qv[c][hh] = qrow ? __ldg(reinterpret_cast<const uint4*>(qrow + d0 + 8 * hh)) : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t w[4] = {qv[c][hh].x, qv[c][hh].y, qv[c][hh].z, qv[c][hh].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+            mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+          }
+        }
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      // 2^e with the row's largest |q| * 2^e in [128, 256); |q| is an fp16
+      // value, so e lies in [-8, 31] and 2^e, 2^-e are normal floats
+      const int e = mx > 0.f ? 134 - static_cast<int>((__float_as_uint(mx) >> 23) & 255u) : 0;
+      const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        const int d0 = part * (D / 4) + 16 * c;
+        uint32_t tw[3][4];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t w[4] = {qv[c][hh].x, qv[c][hh].y, qv[c][hh].z, qv[c][hh].w};
+#pragma unroll
+          for (int k = 0; k < 4; k += 2) {
+            uint32_t a[3], b[3];
+            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&w[k + 1]));
+            split3_e4m3(pack_half2(fa.x * up, fa.y * up), a[0], a[1], a[2]);
+            split3_e4m3(pack_half2(fb.x * up, fb.y * up), b[0], b[1], b[2]);
+#pragma unroll
+            for (int t = 0; t < 3; ++t) tw[t][2 * hh + k / 2] = a[t] | (b[t] << 16);
+          }
+        }
+        const uint32_t off = (d0 >> 7) * T::kQSlab + r * 128 + ((((d0 & 127) >> 4) ^ (r & 7)) << 4);
+#pragma unroll
+        for (int t = 0; t < 3; ++t)
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(qs + t * T::kN * 128 + off), "r"(tw[t][0]),
+                       "r"(tw[t][1]), "r"(tw[t][2]), "r"(tw[t][3])
+                       : "memory");
+      }
+      if (part == 0) {
+        int lo = 0, hi = -1;
+        if (r < pq.R) {
+          hi = pq.L - pq.qlen + r / p.G;
+          lo = p.window > 0 ? max(0, hi - p.window + 1) : 0;
+        }
+        rf[kRowFsl * 32 + r] = r < pq.R ? p.sl2 * __uint_as_float(static_cast<uint32_t>(127 - e) << 23) : 0.f;
+        rf[kRowMu * 32 + r] = -INFINITY;
+        ri[kRowLo * 32 + r] = lo;
+        ri[kRowHi * 32 + r] = hi;
+      }
+      fence_proxy_async_smem();
+    }
+  };
+
+  while (next_piece(pc)) {
+    const bool direct = pc.npieces == 1;
+    const int nblk = (pc.ntiles + T::kBlkTiles - 1) / T::kBlkTiles;
+    q_setup(pc);
+    named_bar_sync(1, 128);
+    if (tid == 0) mbar_arrive(bar(kBarQFull));
+    float fs[32];  // score factor of each row
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float4 f = reinterpret_cast<const float4*>(rf + kRowFsl * 32)[k];
+      fs[4 * k] = f.x; fs[4 * k + 1] = f.y; fs[4 * k + 2] = f.z; fs[4 * k + 3] = f.w;
+    }
+
+    float lp[32];  // this key lane's share of each row's weight sum
+#pragma unroll
+    for (int r = 0; r < 32; ++r) lp[r] = 0.f;
+
+    for (int i = 0; i < nblk; ++i) {
+      const uint32_t b = bq + i;
+      const int sv = b % NBV, sb = b & 1;
+      const int key0 = (pc.first_tile + T::kBlkTiles * i) * kTileKeys;
+      const int nvalid = min(128, kTileKeys * (pc.ntiles - T::kBlkTiles * i));  // keys loaded
+      // ---- this key's scores for the 32 rows
+      float x[32];
+      if (ok) ok = mbar_wait(bar(kBarSFull + sb), (b >> 1) & 1, p.timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
+      tc_fence_after();
+      if (ok) {
+        float y[32], z[32];
+        tmem_ld32(tl + T::kColS + T::kNT * sb, x);
+        tmem_ld32(tl + T::kColS + T::kNT * sb + 32, y);
+        tmem_ld32(tl + T::kColS + T::kNT * sb + 64, z);
+        tmem_wait_ld();
+#pragma unroll
+        for (int r = 0; r < 32; ++r) x[r] = (x[r] + y[r]) + z[r];
+      } else {
+#pragma unroll
+        for (int r = 0; r < 32; ++r) x[r] = 0.f;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(bar(kBarSEmpty + sb));
+      const int j = key0 + tid;
+      const bool interior = nvalid == 128 && key0 >= pc.tile_lo_all && key0 + 127 <= pc.tile_hi_all;
+      if (interior) {
+#pragma unroll
+        for (int r = 0; r < 32; ++r) x[r] *= fs[r];
+      } else {
+        const bool loaded = tid < nvalid;
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+          x[r] = (loaded && j >= ri[kRowLo * 32 + r] && j <= ri[kRowHi * 32 + r])
+                     ? x[r] * fs[r]
+                     : -INFINITY;
+      }
+      // ---- running maximum per row, raised to the block maximum only where
+      // that exceeds it by more than 2^kRaise. Most blocks raise nothing: one
+      // OR-barrier tells, and only then are the block maxima reduced.
+      float mu[32];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float4 m4 = reinterpret_cast<const float4*>(rf + kRowMu * 32)[k];
+        mu[4 * k] = m4.x; mu[4 * k + 1] = m4.y; mu[4 * k + 2] = m4.z; mu[4 * k + 3] = m4.w;
+      }
+      bool up = false;
+#pragma unroll
+      for (int r = 0; r < 32; ++r) up |= x[r] > mu[r] + T::kRaise;
+      bool rescale = false;
+      if (bar_red_or(1, 128, up)) {
+        {
+          float v[32];
+#pragma unroll
+          for (int r = 0; r < 32; ++r) v[r] = x[r];
+          red[warp * 32 + lane] = warp_transpose_reduce<true>(v, lane);
+        }
+        named_bar_sync(1, 128);
+        if (warp == 0) {
+          const float mx = fmaxf(fmaxf(red[lane], red[32 + lane]), fmaxf(red[64 + lane], red[96 + lane]));
+          const float m0 = rf[kRowMu * 32 + lane];
+          float nmu = m0, al = 1.f;
+          if (mx > m0 + T::kRaise) {
+            nmu = mx;
+            al = (m0 == -INFINITY) ? 0.f : ex2(m0 - mx);
+          }
+          rf[kRowMu * 32 + lane] = nmu;
+          rf[kRowAl * 32 + lane] = al;
+          const bool any = __any_sync(0xffffffffu, al != 1.f);
+          if (lane == 0) ri[kRowFlag * 32] = any ? 1 : 0;
+        }
+        named_bar_sync(1, 128);
+        rescale = ri[kRowFlag * 32] != 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float4 m4 = reinterpret_cast<const float4*>(rf + kRowMu * 32)[k];
+          mu[4 * k] = m4.x; mu[4 * k + 1] = m4.y; mu[4 * k + 2] = m4.z; mu[4 * k + 3] = m4.w;
+        }
+      }
+      // ---- weights 2^(x - mu + kBias) (<= 2^8) and the row sums
+#pragma unroll
+      for (int r = 0; r < 32; ++r) x[r] = ex2(x[r] - (mu[r] == -INFINITY ? 0.f : mu[r] - T::kBias));
+      if (rescale) {
+#pragma unroll
+        for (int r = 0; r < 32; ++r) lp[r] = lp[r] * rf[kRowAl * 32 + r] + x[r];
+      } else {
+#pragma unroll
+        for (int r = 0; r < 32; ++r) lp[r] += x[r];
+      }
+      // ---- the P.V operands are free once the previous block's product is done
+      if (ok && b >= 1) ok = mbar_wait(bar(kBarPvDone), (b - 1) & 1, p.timeout_ns);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+      if (rescale && i > 0 && ok) {
+        // O^T columns of rows whose running maximum was raised
+#pragma unroll 1
+        for (int c = 0; c < 3 * S; ++c) {
+          float o[32];
+          tmem_ld32(tl + T::kColO + 32 * c, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int r = 0; r < 32; ++r) o[r] *= rf[kRowAl * 32 + r];
+          tmem_st32(tl + T::kColO + 32 * c, o);
+        }
+        tmem_wait_st();
+      }
+      // ---- P^T, three e4m3 terms: this key's 32 row weights are one 32-byte
+      // row (k = key) of an MN-major operand in the 32-byte swizzle layout
+      // (8-key atoms of 256 bytes; the two 16-byte halves swap in rows 4-7)
+      {
+        uint32_t tt[3][16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) split3_e4m3(pack_half2(x[2 * k], x[2 * k + 1]), tt[0][k], tt[1][k], tt[2][k]);
+        const uint32_t row = pt + (tid >> 3) * 256 + (tid & 7) * 32;
+        const uint32_t flip = ((tid & 7) >> 2) << 4;
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+          uint32_t w[8];
+#pragma unroll
+          for (int m = 0; m < 8; ++m) w[m] = tt[t][2 * m] | (tt[t][2 * m + 1] << 16);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(row + t * T::kPtTerm + flip), "r"(w[0]),
+                       "r"(w[1]), "r"(w[2]), "r"(w[3])
+                       : "memory");
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(row + t * T::kPtTerm + (16 ^ flip)),
+                       "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                       : "memory");
+        }
+      }
+      // ---- V rows of keys past the sequence end or not loaded (stale or
+      // unwritten bytes, NaN codes included) are zeroed in the ring: the P.V
+      // product reads V there, and a zero weight must not meet a NaN
+      const int lim = min(nvalid, pc.L - key0);
+      if (lim < 128) {
+        if (ok) ok = mbar_wait(fullv0 + 8 * sv, (b / NBV) & 1, p.timeout_ns);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok && tid >= lim) {
+          const uint32_t vrow = sbase + T::kOffV + sv * T::kKBlk + tid * 128;
+#pragma unroll
+          for (int sl = 0; sl < S; ++sl)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(vrow + sl * T::kSlabBlk + 16 * c), "r"(0u)
+                           : "memory");
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (ok && lane == 0) mbar_arrive(bar(kBarPFull));
+    }
+    bq += nblk;
+
+    // ---- epilogue: O^T (this thread: dims tid, tid + 128), row sums, output
+    if (ok) ok = mbar_wait(bar(kBarPvDone), (bq - 1) & 1, p.timeout_ns);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    float o[S][32];
+#pragma unroll
+    for (int h = 0; h < S; ++h) {
+      if (ok) {
+        float y[32], z[32];
+        tmem_ld32(tl + T::kColO + T::kNT * h, o[h]);
+        tmem_ld32(tl + T::kColO + T::kNT * h + 32, y);
+        tmem_ld32(tl + T::kColO + T::kNT * h + 64, z);
+        tmem_wait_ld();
+#pragma unroll
+        for (int r = 0; r < 32; ++r) o[h][r] = (o[h][r] + y[r]) + z[r];
+      } else {
+#pragma unroll
+        for (int r = 0; r < 32; ++r) o[h][r] = 0.f;
+      }
+    }
+    tc_fence_before();
+    {
+      float v[32];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) v[r] = lp[r];
+      red[warp * 32 + lane] = warp_transpose_reduce<false>(v, lane);
+    }
+    named_bar_sync(1, 128);
+    if (warp == 0) rf[kRowL * 32 + lane] = (red[lane] + red[32 + lane]) + (red[64 + lane] + red[96 + lane]);
+    named_bar_sync(1, 128);
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      if (r >= pc.R) break;
+      const float L = rf[kRowL * 32 + r];
+      if (direct) {
+        const int i = r / p.G, hl = r % p.G;
+        __half* dst = p.out + (static_cast<long long>(pc.q0 + i) * p.Hq + pc.kh * p.G + hl) * D;
+        const float inv = L > 0.f ? p.out_scale / L : 0.f;
+#pragma unroll
+        for (int h = 0; h < S; ++h) dst[128 * h + tid] = __float2half_rn(o[h][r] * inv);
+      } else {
+        float* dst = p.ws_o + (static_cast<long long>(pc.slot) * p.rows_padded + r) * D;
+#pragma unroll
+        for (int h = 0; h < S; ++h) __stcg(dst + 128 * h + tid, o[h][r]);
+      }
+    }
+    if (!direct && tid < pc.R) {
+      const float mu = rf[kRowMu * 32 + tid];
+      __stcg(reinterpret_cast<float2*>(p.ws_ml + (static_cast<long long>(pc.slot) * p.rows_padded + tid) * 2),
+             make_float2(mu == -INFINITY ? -INFINITY : mu - T::kBias, rf[kRowL * 32 + tid]));
+    }
+    if (tid == 0) post_unit_descriptor(p, pc);
+    named_bar_sync(1, 128);  // red[] and the row state are reused by the next piece
+  }
+  if (!ok && lane == 0) raise_error(p.error_flag, kErrTimeout);
+}
+
+template <class T>
+__global__ void __launch_bounds__(T::kThreads, 1)
+    decode_tc8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                      const DecodeParams p) {
+  constexpr int D = T::D, NBK = T::NBK, NBV = T::NBV, KS = D / 32;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t fullk0 = sbase + T::kOffBars, emptyk0 = fullk0 + 8 * NBK;
+  const uint32_t fullv0 = emptyk0 + 8 * NBK, emptyv0 = fullv0 + 8 * NBV, bx = emptyv0 + 8 * NBV;
+  auto bar = [&](int i) -> uint32_t { return bx + 8 * i; };
+  int* s_pre = reinterpret_cast<int*>(smem + T::kOffPre);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffTmem);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NBK; ++s) {
+      mbar_init(fullk0 + 8 * s, 1);
+      mbar_init(emptyk0 + 8 * s, 1);  // the S^T commit
+    }
+    for (int s = 0; s < NBV; ++s) {
+      mbar_init(fullv0 + 8 * s, 1);
+      mbar_init(emptyv0 + 8 * s, 1);  // the P.V commit
+    }
+    mbar_init(bar(kBarSFull), 1);
+    mbar_init(bar(kBarSFull + 1), 1);
+    mbar_init(bar(kBarSEmpty), 4);
+    mbar_init(bar(kBarSEmpty + 1), 4);
+    mbar_init(bar(kBarPFull), 4);
+    mbar_init(bar(kBarPvDone), 1);
+    mbar_init(bar(kBarQFull), 1);
+    mbar_init(bar(kBarFinal), 1);
+    fence_mbar_init();
+  }
+  if (warp == T::kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), T::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == T::kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  // balanced mode: prefix over sequences of visible tiles (as decode_kernel)
+  if (p.num_splits == 0 && warp == 0) {
+    int carry = 0;
+    if (lane == 0) s_pre[0] = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int b = base + lane;
+      int v = 0;
+      if (b < p.B) {
+        int L, t0, n, q0, qn;
+        seq_span(p, b, blockIdx.x == 0, L, t0, n, q0, qn);
+        v = n * p.hgn;
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      if (b < p.B) s_pre[b + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  WorkIter it;
+  work_init(p, s_pre, it);
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  Piece pc;
+  bool ok = true;
+
+  if (warp == T::kProducerWarp) {
+    // ---------------------------------------------------------------- producer
+    const uint64_t pol = l2_policy_evict_first();
+    uint32_t bq = 0, posted = 0;  // blocks walked; blocks whose loads were all issued
+    while (work_next(p, s_pre, it, pc)) {
+      if (pc.ntiles == 0) continue;
+      const int nblk = (pc.ntiles + T::kBlkTiles - 1) / T::kBlkTiles;
+      const int32_t* row = p.block_table + static_cast<long long>(pc.b) * p.max_blocks;
+      auto load_group = [&](int t) -> int {
+        int blk = 0;
+        if (t + lane < pc.ntiles) blk = __ldg(row + (pc.first_tile + t + lane) / p.tiles_per_block);
+        return blk;
+      };
+      // block table entries 32 tiles (4 blocks) at a time, the next group in flight
+      int cur = load_group(0), nxt = pc.ntiles > 32 ? load_group(32) : 0;
+      constexpr int kBoxes = 2 * T::kSlabs;  // boxes per tile: K slabs, then V slabs
+      for (int i = 0; i < nblk; ++i) {
+        const int t0 = i * T::kBlkTiles;
+        if (t0 > 0 && t0 % 32 == 0) {
+          cur = nxt;
+          nxt = t0 + 32 < pc.ntiles ? load_group(t0 + 32) : 0;
+        }
+        const uint32_t b = bq + i;
+        const int sk = b % NBK, sv = b % NBV;
+        const int ntb = min(T::kBlkTiles, pc.ntiles - t0);
+        if (lane == 0) {
+          const uint32_t bytes = ntb * T::kSlabs * T::kTileBox;
+          if (ok && b >= NBK) ok = mbar_wait(emptyk0 + 8 * sk, ((b / NBK) - 1) & 1, p.timeout_ns);
+          if (ok && b >= NBV) ok = mbar_wait(emptyv0 + 8 * sv, ((b / NBV) - 1) & 1, p.timeout_ns);
+          if (ok && p.inject == 1) ok = false;  // injected fault: the rings stay empty
+          if (ok) {
+            mbar_arrive_expect_tx(fullk0 + 8 * sk, bytes);
+            mbar_arrive_expect_tx(fullv0 + 8 * sv, bytes);
+            posted = b + 1;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        // lane l: tile l / kBoxes of the block, box l % kBoxes (all boxes at once)
+        const int j = min(lane / kBoxes, T::kBlkTiles - 1);
+        int blk = __shfl_sync(0xffffffffu, cur, (t0 % 32) + j);
+        if (!ok) continue;
+        if (lane < kBoxes * ntb) {
+          if (blk < 0 || blk >= p.num_blocks) {
+            raise_error(p.error_flag, kErrBlockId);
+            blk = 0;
+          }
+          const int gt = pc.first_tile + t0 + j;
+          const int z = blk * p.block_size + (gt % p.tiles_per_block) * kTileKeys;
+          const int bx2 = lane % kBoxes, sl = bx2 % T::kSlabs;
+          const bool is_v = bx2 >= T::kSlabs;
+          const uint32_t dst = sbase + (is_v ? T::kOffV + sv * T::kKBlk : sk * T::kKBlk) + sl * T::kSlabBlk +
+                               j * T::kTileBox;
+          tma_load_3d(dst, is_v ? &tm_v : &tm_k, is_v ? fullv0 + 8 * sv : fullk0 + 8 * sk, sl * 128, pc.kh, z,
+                      pol);
+        }
+      }
+      bq += nblk;
+    }
+    if (lane == 0) {
+      if (!ok) raise_error(p.error_flag, kErrTimeout);
+      // every load issued lands before the CTA exits: a block's loads are all
+      // issued once its transaction counts are posted, so wait for the last
+      // posted blocks of each ring
+      for (uint32_t k = posted > NBK ? posted - NBK : 0; k < posted; ++k)
+        if (!mbar_wait(fullk0 + 8 * (k % NBK), (k / NBK) & 1, kDrainLimitNs)) break;
+      for (uint32_t k = posted > NBV ? posted - NBV : 0; k < posted; ++k)
+        if (!mbar_wait(fullv0 + 8 * (k % NBV), (k / NBV) & 1, kDrainLimitNs)) break;
+    }
+  } else if (warp == T::kMmaWarp) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t bq = 0, pq = 0;
+      bool any = false;
+      const uint32_t qb = sbase + T::kOffQ, pt = sbase + T::kOffPt;
+      while (work_next(p, s_pre, it, pc)) {
+        if (pc.ntiles == 0) continue;
+        const int nblk = (pc.ntiles + T::kBlkTiles - 1) / T::kBlkTiles;
+        if (ok) ok = mbar_wait(bar(kBarQFull), pq & 1, p.timeout_ns);
+        ++pq;
+        tc_fence_after();
+        for (int i = 0; i <= nblk; ++i) {
+          if (i < nblk) {  // S^T of block i
+            const uint32_t b = bq + i;
+            const int sk = b % NBK, sb = b & 1;
+            if (ok) ok = mbar_wait(fullk0 + 8 * sk, (b / NBK) & 1, p.timeout_ns);
+            if (ok && b >= 2) ok = mbar_wait(bar(kBarSEmpty + sb), ((b >> 1) - 1) & 1, p.timeout_ns);
+            tc_fence_after();
+            if (ok) {
+              const uint32_t kbase = sbase + sk * T::kKBlk;
+#pragma unroll
+              for (int ks = 0; ks < KS; ++ks) {
+                const uint32_t koff = (ks >> 2) * T::kSlabBlk + (ks & 3) * 32;
+                const uint32_t qoff = (ks >> 2) * T::kQSlab + (ks & 3) * 32;
+                mma_e4m3(tmem + T::kColS + T::kNT * sb, sdesc_sw128(kbase + koff), sdesc_sw128(qb + qoff),
+                         T::kIdescS, ks != 0);
+              }
+              mma_commit(bar(kBarSFull + sb));
+              mma_commit(emptyk0 + 8 * sk);
+              any = true;
+            }
+          }
+          if (i >= 1) {  // O^T += V^T P^T of block i - 1, V^T read in place (MN-major)
+            const uint32_t b = bq + i - 1;
+            const int sv = b % NBV;
+            if (ok) ok = mbar_wait(fullv0 + 8 * sv, (b / NBV) & 1, p.timeout_ns);
+            if (ok) ok = mbar_wait(bar(kBarPFull), b & 1, p.timeout_ns);
+            tc_fence_after();
+            if (ok) {
+              const uint32_t vbase = sbase + T::kOffV + sv * T::kKBlk;
+#pragma unroll
+              for (int h = 0; h < T::kSlabs; ++h)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_e4m3(tmem + T::kColO + T::kNT * h, sdesc_sw128_mn(vbase + h * T::kSlabBlk + kk * 4096),
+                           sdesc_sw32_mn(pt + kk * 1024, T::kPtTerm), T::kIdescO, (i > 1 || kk > 0) ? 1u : 0u);
+              mma_commit(bar(kBarPvDone));
+              mma_commit(emptyv0 + 8 * sv);
+              any = true;
+            }
+          }
+        }
+        bq += nblk;
+      }
+      if (!ok) raise_error(p.error_flag, kErrTimeout);
+      // every issued product completes before the tensor memory is freed
+      if (any) {
+        mma_commit(bar(kBarFinal));
+        mbar_wait(bar(kBarFinal), 0, kDrainLimitNs);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------- softmax warps
+    softmax_role<T>(p, s_pre, it, pc, smem, sbase, tmem, ok);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == T::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, T::kTmemCols);
+  }
+}
+
+// Host launch of the e4m3 tensor-core decode (one CTA per SM); sets the
+// shared-memory opt-in once per device.
+template <class T>
+cudaError_t launch_tc8(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
+                       cudaStream_t stream) {
+  static unsigned long long attr_done = 0;  // bit per device ordinal (< 64)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
+    e = cudaFuncSetAttribute(decode_tc8_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);
+  }
+  decode_tc8_kernel<T><<<grid, T::kThreads, T::kSmemBytes, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+template <class T>
+bool shape_tc8(int nt, KernelShape* out) {
+  out->threads = T::kThreads;
+  out->smem_bytes = T::kSmemBytes;
+  out->rows_padded = 8 * nt;
+  out->ctas_per_sm = 1;
+  out->heads = 1;
+  return true;
+}
+
+}  // namespace pd

@@ -1,0 +1,152 @@
+// tc5.cuh -- inline-PTX wrappers for the 5th-generation tensor cores on sm_103a
+// (PTX ISA: tcgen05.alloc / dealloc / mma / commit / ld / st / wait / fence,
+// shared-memory matrix descriptors, ldmatrix with 8-bit elements).
+#pragma once
+#include <cstdint>
+
+namespace pd {
+
+// ---- tensor memory (TMEM) ------------------------------------------------------
+// Warp-wide: allocates `ncols` columns (a power of two >= 32) of this SM's
+// tensor memory for the CTA and writes the TMEM address to shared `dst`.
+__device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Shared-memory writes of this thread become visible to the tensor cores'
+// (async proxy) reads that are ordered after the next synchronisation.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of the TMEM lane (32 * (warp % 4) + lane):
+// taddr = TMEM address (lane in bits 31:16, column in 15:0) of the warp's lane 0.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---- tcgen05.mma ------------------------------------------------------------------
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte swizzle
+// layout: rows of 128 bytes, 8-row (1024-byte) swizzle atoms stacked at a
+// 1024-byte stride along M/N (the stride byte offset); `addr` is the operand's
+// first row plus the byte offset of the k step inside the 128-byte row, and
+// the atom it starts in is 1024-byte aligned. Fields: start >> 4 (bits 0-13),
+// leading byte offset >> 4 (16-29, unused by this layout), stride byte offset
+// >> 4 (32-45), descriptor version 1 (46-47), base offset 0 (49-51), layout
+// type 2 = 128-byte swizzle (61-63).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+// Descriptor of an MN-major operand in the 128-byte swizzle layout with 8-bit
+// elements: each 128-byte row holds 128 consecutive M (or N) elements of one k,
+// 8 rows (consecutive k) form a 1024-byte swizzle atom, atoms follow each other
+// along K every 1024 bytes. The operand is one atom wide along M/N, so only the
+// K-direction atom stride is used; both offset fields hold 1024 bytes.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t addr) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (64ull << 16) | (64ull << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+// Descriptor of an MN-major 8-bit operand in the 32-byte swizzle layout: each
+// 32-byte row holds 32 consecutive M/N elements of one k, 8 rows (consecutive
+// k) form a 256-byte atom whose two 16-byte halves are swapped in rows 4-7
+// (address bit 4 ^= bit 7); atoms follow each other along K every 256 bytes
+// (stride byte offset) and along M/N every `mn_stride` bytes (leading byte
+// offset).
+__device__ __forceinline__ uint64_t sdesc_sw32_mn(uint32_t addr, uint32_t mn_stride) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(mn_stride >> 4) << 16) |
+         (16ull << 32) | (1ull << 46) | (6ull << 61);
+}
+// Instruction descriptor of kind::f8f6f4 with e4m3 A and B, fp32 D, both
+// operands K-major: D format (bits 4-5) = 1 (f32), A and B formats (7-9,
+// 10-12) = 0 (e4m3), N >> 3 (17-22), M >> 4 (24-28). Bit 15 (16) set makes A
+// (B) MN-major.
+constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, one CTA; `acc` = 0 overwrites D.
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// Arrives (once) on the mbarrier when every tcgen05.mma this thread issued
+// before has completed.
+__device__ __forceinline__ void mma_commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+               : "memory");
+}
+
+// ---- barrier with an OR reduction ----------------------------------------------
+// Named barrier `id` over `nthreads` threads that also returns whether any of
+// them passed a true predicate.
+__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\tbar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// ---- 8-bit ldmatrix ----------------------------------------------------------------
+// Two 16x16 byte matrices, each from 16 rows of 16 bytes (lanes 0-15 address
+// the rows of the first, lanes 16-31 those of the second), transposed:
+// r0 = T[g][4t..4t+3], r1 = T[g+8][4t..4t+3] of the first (T = stored^T,
+// g = lane / 4, t = lane % 4), r2, r3 the same of the second.
+__device__ __forceinline__ void ldsm_b8_x2_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+}  // namespace pd

@@ -156,6 +156,14 @@ EDGE = [
     # head-group tiles with two head groups per sequence (Hkv = 8)
     ("fp8_d128_two_head_groups", dict(B=3, Hq=32, Hkv=8, D=128, kv="fp8", seq_lens=[3000, 47, 800])),
     ("f16_d256_two_head_groups", dict(B=2, Hq=16, Hkv=8, D=256, seq_lens=[2049, 700])),
+    # e4m3 units of 9..32 rows run on the tensor-memory kernel: 128-key blocks,
+    # partial blocks at piece ends, windows across blocks, block sizes > 16
+    ("fp8_d256_rows_32_window", dict(B=3, Hq=8, Hkv=1, D=256, kv="fp8", qlen=4, window=200,
+                                     seq_lens=[1000, 129, 3])),
+    ("fp8_d256_rows_16_bs64", dict(B=2, Hq=16, Hkv=2, D=256, kv="fp8", qlen=2, block_size=64,
+                                   seq_lens=[2000, 65])),
+    ("fp8_d128_rows_9_block_edges", dict(B=4, Hq=9, Hkv=1, D=128, kv="fp8",
+                                         seq_lens=[1, 128, 129, 5000])),
 ]
 
 
@@ -173,6 +181,7 @@ STALE = [
     ("f16_d128_rows_8", dict(B=3, Hq=32, Hkv=8, D=128, seq_lens=[7, 90, 700])),
     ("fp8_rows_6", dict(B=3, Hq=24, Hkv=4, D=256, kv="fp8", seq_lens=[3, 4001, 250])),
     ("fp8_d128_rows_24", dict(B=2, Hq=8, Hkv=1, D=128, kv="fp8", qlen=3, seq_lens=[5, 301])),
+    ("fp8_d256_rows_18", dict(B=3, Hq=24, Hkv=4, D=256, kv="fp8", qlen=3, seq_lens=[3, 4001, 250])),
     ("int8_rows_32", dict(B=2, Hq=8, Hkv=1, D=256, kv="int8", qlen=4, seq_lens=[700, 91])),
 ]
 
