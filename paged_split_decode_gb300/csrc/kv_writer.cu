@@ -12,8 +12,14 @@
 // 0x7F), or round-to-nearest-even to an integer clamped to [-127, 127]
 // (NaN -> 0).
 //
-// Memory-bound: a grid-stride loop over (token, vector) items, K and V of an
-// item together, sized to a few resident blocks per SM.
+// Memory-bound: one warp per token in a grid-stride loop, lanes over the
+// token's 16-byte vectors (K and V together), a few resident blocks per SM. The quotient is the
+// correctly rounded fp32 x / scale, formed from the reciprocal r = RN(1/scale)
+// by one residual correction (Markstein's theorem: with r the correctly
+// rounded reciprocal and q0 = RN(x r) within an ulp of x / scale, the residual
+// e = x - q0 scale is exact under FMA and RN(q0 + e r) is the correctly
+// rounded quotient, for quotients away from the underflow range); the host
+// takes the plain division when the scale is outside [2^-100, 2^100].
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -34,14 +40,28 @@ __device__ __forceinline__ uint32_t e4m3x2_of(float lo, float hi) {
   return r;
 }
 
-__device__ __forceinline__ uint32_t i8_of(float t) {
-  int c = __float2int_rn(t);  // NaN -> 0; beyond int range saturates
-  c = max(-127, min(127, c));
-  return static_cast<uint32_t>(c) & 0xffu;
+// Code of an int8 cache: the quotient clamped to [-127, 127] (NaN -> 0) and
+// rounded to the nearest integer, ties to even, by adding 1.5 * 2^23: the sum's
+// low mantissa bits then hold the integer in two's complement. Returns the
+// float whose low byte is the code.
+__device__ __forceinline__ uint32_t i8_bits(float t) {
+  t = (t == t) ? fminf(fmaxf(t, -127.f), 127.f) : 0.f;
+  return __float_as_uint(t + 12582912.f);
+}
+
+// Correctly rounded x / s (see the header); `fast` selects the residual form.
+__device__ __forceinline__ float quot(float x, float s, float r, bool fast) {
+  if (!fast) return __fdiv_rn(x, s);
+  const float q0 = x * r;
+  const float e = fmaf(-q0, s, x);
+  // q0 is kept when it is exact (e == 0: also keeps the sign of a zero
+  // quotient) or infinite (an infinite x; the residual is then NaN)
+  return (e == 0.f || !(fabsf(q0) < INFINITY)) ? q0 : fmaf(e, r, q0);
 }
 
 template <int KV>
-__device__ __forceinline__ void store_row8(void* cache, long long elem, uint4 x, float scale) {
+__device__ __forceinline__ void store_row8(void* cache, long long elem, uint4 x, float scale, float rcp,
+                                           bool fast) {
   if constexpr (KV == PD_KV_F16) {
     *reinterpret_cast<uint4*>(static_cast<__half*>(cache) + elem) = x;
   } else {
@@ -50,16 +70,19 @@ __device__ __forceinline__ void store_row8(void* cache, long long elem, uint4 x,
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-      f[2 * i] = __fdiv_rn(p.x, scale);
-      f[2 * i + 1] = __fdiv_rn(p.y, scale);
+      f[2 * i] = quot(p.x, scale, rcp, fast);
+      f[2 * i + 1] = quot(p.y, scale, rcp, fast);
     }
     uint2 o;
     if constexpr (KV == PD_KV_FP8_E4M3) {
       o.x = e4m3x2_of(f[0], f[1]) | (e4m3x2_of(f[2], f[3]) << 16);
       o.y = e4m3x2_of(f[4], f[5]) | (e4m3x2_of(f[6], f[7]) << 16);
     } else {
-      o.x = i8_of(f[0]) | (i8_of(f[1]) << 8) | (i8_of(f[2]) << 16) | (i8_of(f[3]) << 24);
-      o.y = i8_of(f[4]) | (i8_of(f[5]) << 8) | (i8_of(f[6]) << 16) | (i8_of(f[7]) << 24);
+      // low bytes of four sums -> one word (prmt selects bytes 0 of each)
+      o.x = __byte_perm(__byte_perm(i8_bits(f[0]), i8_bits(f[1]), 0x0040),
+                        __byte_perm(i8_bits(f[2]), i8_bits(f[3]), 0x0040), 0x5410);
+      o.y = __byte_perm(__byte_perm(i8_bits(f[4]), i8_bits(f[5]), 0x0040),
+                        __byte_perm(i8_bits(f[6]), i8_bits(f[7]), 0x0040), 0x5410);
     }
     *reinterpret_cast<uint2*>(static_cast<uint8_t*>(cache) + elem) = o;
   }
@@ -68,26 +91,31 @@ __device__ __forceinline__ void store_row8(void* cache, long long elem, uint4 x,
 template <int KV>
 __global__ void __launch_bounds__(kWriterThreads) kv_writer_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
-    const int64_t* __restrict__ slot_mapping, long long items, int vecs_per_token,
-    long long slots, int block_size, void* __restrict__ k_cache, void* __restrict__ v_cache,
-    float k_scale, float v_scale, uint32_t* error_flag) {
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long it = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; it < items;
-       it += stride) {
-    const long long t = it / vecs_per_token;
-    const int vec = static_cast<int>(it - t * vecs_per_token);
+    const int64_t* __restrict__ slot_mapping, long long num_tokens, int vecs_per_token,
+    long long slots, void* __restrict__ k_cache, void* __restrict__ v_cache, float k_scale,
+    float v_scale, float k_rcp, float v_rcp, int fast, uint32_t* error_flag) {
+  // one warp per token (grid-stride over tokens), lanes over its 16-byte input
+  // vectors; cache row = slot (block slot / bs, offset slot % bs of the
+  // [num_blocks, bs, Hkv, D] cache is row slot of [num_blocks * bs, Hkv, D])
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (kWriterThreads / 32);
+  for (long long t = static_cast<long long>(blockIdx.x) * (kWriterThreads / 32) + (threadIdx.x >> 5);
+       t < num_tokens; t += warps) {
     const int64_t slot = __ldg(slot_mapping + t);
     if (slot < 0) continue;  // padding token
     if (slot >= slots) {
-      if (error_flag && vec == 0) atomicOr(error_flag, PD_DEVERR_SLOT);
+      if (error_flag && lane == 0) atomicOr(error_flag, PD_DEVERR_SLOT);
       continue;
     }
-    const long long blk = slot / block_size, off = slot - blk * block_size;
-    const long long elem =
-        ((blk * block_size + off) * vecs_per_token + vec) * 8;  // first element of the vector
-    const uint4 kx = __ldcs(k_new + it), vx = __ldcs(v_new + it);
-    store_row8<KV>(k_cache, elem, kx, k_scale);
-    store_row8<KV>(v_cache, elem, vx, v_scale);
+    const uint4* kin = k_new + t * vecs_per_token;
+    const uint4* vin = v_new + t * vecs_per_token;
+    const long long base = static_cast<long long>(slot) * vecs_per_token;
+#pragma unroll 4
+    for (int v = lane; v < vecs_per_token; v += 32) {
+      const uint4 kx = __ldcs(kin + v), vx = __ldcs(vin + v);
+      store_row8<KV>(k_cache, (base + v) * 8, kx, k_scale, k_rcp, fast != 0);
+      store_row8<KV>(v_cache, (base + v) * 8, vx, v_scale, v_rcp, fast != 0);
+    }
   }
 }
 
@@ -118,34 +146,38 @@ extern "C" pd_status write_kv_cache(const void* k_new, const void* v_new,
       (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
     return PD_ERR_ALIGN;
   const int vecs = static_cast<int>(row / 8);
-  const long long items = static_cast<long long>(num_tokens) * vecs;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
     return PD_ERR_CUDA;
-  const long long want = (items + pd::kWriterThreads - 1) / pd::kWriterThreads;
+  const long long want = (static_cast<long long>(num_tokens) + pd::kWriterThreads / 32 - 1) / (pd::kWriterThreads / 32);
   const long long cap = static_cast<long long>(sms) * pd::kWriterBlocksPerSm;
   const unsigned grid = static_cast<unsigned>(want < cap ? want : cap);
   const long long slots = static_cast<long long>(d.num_blocks) * d.block_size;
   auto s = static_cast<cudaStream_t>(stream);
+  // residual-corrected division for scales whose reciprocal and quotients stay
+  // in the normal range; the plain correctly rounded division otherwise
+  auto moderate = [](float x) { const float a = x < 0 ? -x : x; return a >= 0x1p-100f && a <= 0x1p100f; };
+  const int fast = moderate(d.k_scale) && moderate(d.v_scale) ? 1 : 0;
+  const float k_rcp = fast ? 1.f / d.k_scale : 0.f, v_rcp = fast ? 1.f / d.v_scale : 0.f;
   const auto* kn = static_cast<const uint4*>(k_new);
   const auto* vn = static_cast<const uint4*>(v_new);
   switch (d.kv_dtype) {
     case PD_KV_F16:
     case PD_KV_BF16:  // 16-bit caches: the input bits as they are
       pd::kv_writer_kernel<PD_KV_F16><<<grid, pd::kWriterThreads, 0, s>>>(
-          kn, vn, slot_mapping, items, vecs, slots, d.block_size, k_cache, v_cache, 1.f, 1.f,
+          kn, vn, slot_mapping, static_cast<long long>(num_tokens), vecs, slots, k_cache, v_cache, 1.f, 1.f, 1.f, 1.f, 0,
           error_flag);
       break;
     case PD_KV_FP8_E4M3:
       pd::kv_writer_kernel<PD_KV_FP8_E4M3><<<grid, pd::kWriterThreads, 0, s>>>(
-          kn, vn, slot_mapping, items, vecs, slots, d.block_size, k_cache, v_cache, d.k_scale,
-          d.v_scale, error_flag);
+          kn, vn, slot_mapping, static_cast<long long>(num_tokens), vecs, slots, k_cache, v_cache, d.k_scale,
+          d.v_scale, k_rcp, v_rcp, fast, error_flag);
       break;
     default:
       pd::kv_writer_kernel<PD_KV_INT8><<<grid, pd::kWriterThreads, 0, s>>>(
-          kn, vn, slot_mapping, items, vecs, slots, d.block_size, k_cache, v_cache, d.k_scale,
-          d.v_scale, error_flag);
+          kn, vn, slot_mapping, static_cast<long long>(num_tokens), vecs, slots, k_cache, v_cache, d.k_scale,
+          d.v_scale, k_rcp, v_rcp, fast, error_flag);
       break;
   }
   return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
