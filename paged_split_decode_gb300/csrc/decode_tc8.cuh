@@ -7,9 +7,9 @@
 // by the split-combine kernel), different engine:
 //  * A unit is (sequence, KV head); its visible 16-key tiles are cut into
 //    pieces by the balanced split (work_next). Within a piece, 8 consecutive
-//    tiles form a 128-key block. One producer warp TMA-loads each tile's K and
-//    V rows (128-byte swizzled, the layout the tensor cores read) into a ring
-//    of block stages.
+//    tiles form a 128-key block. Two producer warps TMA-load the K and the V
+//    rows of each block (128-byte swizzled, the layout the tensor cores read)
+//    into rings of block stages, all boxes of a block at once.
 //  * One thread issues tcgen05.mma kind::f8f6f4 on the e4m3 codes themselves:
 //    S^T[128 keys x 96] = K Q^T into tensor memory, and later O^T[D x 96] +=
 //    V^T P^T. The K and V codes are never widened.
@@ -18,9 +18,11 @@
 //    the N side (3 x 32 rows) and their products summed when S^T is read. The
 //    softmax weights are split the same way and stacked on N for P.V; the
 //    three O^T accumulators are summed at the end of a piece.
-//  * Four softmax warps own the 128 keys of a block (one TMEM lane each): they
-//    read S^T, mask, take the per-row block maximum (warp transpose-reduce and
-//    a shared exchange), form the weights against a running maximum that is
+//  * Eight softmax warps in two groups: thread i of a group owns TMEM lane i
+//    (key i of a block), and group w owns query rows 16 w .. 16 w + 15 (their
+//    maxima, sums and O^T columns), so the groups never wait on each other.
+//    They read S^T, mask, take the per-row block maximum (warp transpose-reduce
+//    and a shared exchange), form the weights against a running maximum that is
 //    only raised when the block maximum exceeds it by more than 2^4 (then the
 //    O^T accumulator is rescaled in tensor memory), and write P^T: each key's
 //    thread stores its 32 row weights as one 32-byte row of an MN-major
@@ -56,8 +58,8 @@ struct Tc8 {
   static constexpr int kQSlab = kNT * 128;          // q operand, one slab: [term][32 rows][128 B]
   static constexpr int kQBytes = kSlabs * kQSlab;
   static constexpr int kPtTerm = 128 * kN;          // one P^T term: [128 keys][32 rows], MN-major
-  static constexpr int kThreads = 192;              // warps 0-3 softmax, 4 producer, 5 MMA
-  static constexpr int kProducerWarp = 4, kMmaWarp = 5;
+  static constexpr int kThreads = 352;              // warps 0-7 softmax, 8-9 producers (K, V), 10 MMA
+  static constexpr int kProducerWarp = 8, kMmaWarp = 10;
   static constexpr int kTmemCols = 512;             // S^T x2 (2 x 96), O^T (kSlabs x 96)
   static constexpr int kColS = 0, kColO = 2 * kNT;
   static constexpr uint32_t kIdescS = idesc_e4m3(128, kNT);               // K-major A and B
@@ -68,7 +70,7 @@ struct Tc8 {
   static constexpr int kOffV = NBK * kKBlk;
   static constexpr int kOffQ = kOffV + NBV * kKBlk;
   static constexpr int kOffPt = kOffQ + kQBytes;
-  static constexpr int kOffRed = kOffPt + 3 * kPtTerm;     // float [4 warps][32 rows]
+  static constexpr int kOffRed = kOffPt + 3 * kPtTerm;     // float [2 groups][4 warps][16 rows]
   static constexpr int kRowWords = 7 * 32;                 // row state: 7 arrays of 32 words
   static constexpr int kOffRow = kOffRed + 4 * 32 * 4;
   static constexpr int kOffBars = kOffRow + kRowWords * 4;
@@ -129,6 +131,24 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane)
   }
   return v[0];
 }
+// 16 values, one per row -> lanes l and l + 16 hold the reduction of row l
+// (l < 16) over the 32 lanes (4 butterfly rounds, then the two halves).
+template <bool MAX>
+__device__ __forceinline__ float warp_transpose_reduce16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {
+    const bool up = (lane & w) != 0;
+#pragma unroll
+    for (int k = 0; k < w; ++k) {
+      const float send = up ? v[k] : v[k + w];
+      const float keep = up ? v[k + w] : v[k];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, w);
+      v[k] = MAX ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  const float other = __shfl_xor_sync(0xffffffffu, v[0], 16);
+  return MAX ? fmaxf(v[0], other) : v[0] + other;
+}
 
 // Posts a unit's split descriptor from its first piece (as decode_kernel).
 __device__ __forceinline__ void post_unit_descriptor(const DecodeParams& p, const Piece& pc) {
@@ -145,20 +165,26 @@ __device__ __forceinline__ void post_unit_descriptor(const DecodeParams& p, cons
   p.ws_desc[pc.unit] = d;
 }
 
-// The four softmax warps (threads 0..127; thread i owns TMEM lane i: key i of
-// a block for S^T, output dim i (+128) for O^T).
+// The softmax warps: two warpgroups (threads 0-127 and 128-255) share the
+// keys of a block -- thread i of a group owns TMEM lane i (key i of a block for
+// S^T, output dims i and i + 128 for O^T) -- and split the 32 query rows:
+// group w takes rows 16 w .. 16 w + 15, with their running maxima, sums and
+// O^T columns, so the groups never wait on each other inside a block.
 template <class T>
 __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s_pre, WorkIter& it, Piece& pc,
                                              uint8_t* smem, uint32_t sbase, uint32_t tmem, bool& ok) {
   constexpr int D = T::D, NBK = T::NBK, NBV = T::NBV, S = T::kSlabs;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t4 = lane & 3;
+  const int wg = warp >> 2;             // row half
+  const int key = tid & 127;            // TMEM lane of this thread
+  const int rb = 16 * wg;               // first row of this half
+  const int bid = 1 + wg;               // the group's named barrier (128 threads)
   float* rf = reinterpret_cast<float*>(smem + T::kOffRow);
   int* ri = reinterpret_cast<int*>(smem + T::kOffRow);
-  float* red = reinterpret_cast<float*>(smem + T::kOffRed);
+  float* red = reinterpret_cast<float*>(smem + T::kOffRed) + 64 * wg;  // [4 warps][16 rows]
   const uint32_t fullv0 = sbase + T::kOffBars + 16 * NBK, bx = fullv0 + 16 * NBV;
   auto bar = [&](int i) -> uint32_t { return bx + 8 * i; };
-  const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);  // this warp's TMEM lanes
+  const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);  // this warp's TMEM lanes
   const uint32_t qs = sbase + T::kOffQ, pt = sbase + T::kOffPt;
   uint32_t bq = 0;
   // Pieces with nothing visible are finished on the spot (zero rows; such a
@@ -166,7 +192,7 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
   auto next_piece = [&](Piece& out) -> bool {
     while (work_next(p, s_pre, it, out)) {
       if (out.ntiles > 0) return true;
-      for (int item = tid; item < out.R * (D / 8); item += 128) {
+      for (int item = tid; item < out.R * (D / 8); item += 256) {
         const int r = item / (D / 8), dc = item % (D / 8);
         const int i = r / p.G, hl = r % p.G;
         *reinterpret_cast<uint4*>(p.out + (static_cast<long long>(out.q0 + i) * p.Hq + out.kh * p.G + hl) * D +
@@ -176,237 +202,227 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
     }
     return false;
   };
-  // A piece's q terms and row state (the previous piece's S^T products are
-  // complete: its softmax has read all of them).
+  // A piece's q terms (the B operand of S^T: K-major, 128-byte swizzle, the
+  // three terms stacked on N), row score factors and visible key limits; the
+  // previous piece's S^T products are complete (its softmax read them all).
+  // Thread t: row t / 8, dims [(t % 8) D / 8, (t % 8 + 1) D / 8).
   auto q_setup = [&](const Piece& pq) {
-    // ---- q rows as three e4m3 terms (the B operand of S^T, K-major, 128-byte
-    // swizzle), row score factors and visible key limits. Thread t: row t / 4,
-    // dims [(t % 4) D / 4, (t % 4 + 1) D / 4).
-    {
-      const int r = tid >> 2, part = tid & 3;
-      constexpr int NCH = D / 64;  // 16-dim chunks per thread
-      const __half* qrow = nullptr;
-      if (r < pq.R) {
-        const int i = r / p.G, hl = r % p.G;
-        qrow = p.q + (static_cast<long long>(pq.q0 + i) * p.Hq + pq.kh * p.G + hl) * D;
-      }
-      uint4 qv[NCH][2];
-      float mx = 0.f;
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        const int d0 = part * (D / 4) + 16 * c;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          qv[c][hh] = qrow ? __ldg(reinterpret_cast<const uint4*>(qrow + d0 + 8 * hh)) : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t w[4] = {qv[c][hh].x, qv[c][hh].y, qv[c][hh].z, qv[c][hh].w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
-            mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
-          }
-        }
-      }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      // 2^e with the row's largest |q| * 2^e in [128, 256); |q| is an fp16
-      // value, so e lies in [-8, 31] and 2^e, 2^-e are normal floats
-      const int e = mx > 0.f ? 134 - static_cast<int>((__float_as_uint(mx) >> 23) & 255u) : 0;
-      const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        const int d0 = part * (D / 4) + 16 * c;
-        uint32_t tw[3][4];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const uint32_t w[4] = {qv[c][hh].x, qv[c][hh].y, qv[c][hh].z, qv[c][hh].w};
-#pragma unroll
-          for (int k = 0; k < 4; k += 2) {
-            uint32_t a[3], b[3];
-            const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
-            const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&w[k + 1]));
-            split3_e4m3(pack_half2(fa.x * up, fa.y * up), a[0], a[1], a[2]);
-            split3_e4m3(pack_half2(fb.x * up, fb.y * up), b[0], b[1], b[2]);
-#pragma unroll
-            for (int t = 0; t < 3; ++t) tw[t][2 * hh + k / 2] = a[t] | (b[t] << 16);
-          }
-        }
-        const uint32_t off = (d0 >> 7) * T::kQSlab + r * 128 + ((((d0 & 127) >> 4) ^ (r & 7)) << 4);
-#pragma unroll
-        for (int t = 0; t < 3; ++t)
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(qs + t * T::kN * 128 + off), "r"(tw[t][0]),
-                       "r"(tw[t][1]), "r"(tw[t][2]), "r"(tw[t][3])
-                       : "memory");
-      }
-      if (part == 0) {
-        int lo = 0, hi = -1;
-        if (r < pq.R) {
-          hi = pq.L - pq.qlen + r / p.G;
-          lo = p.window > 0 ? max(0, hi - p.window + 1) : 0;
-        }
-        rf[kRowFsl * 32 + r] = r < pq.R ? p.sl2 * __uint_as_float(static_cast<uint32_t>(127 - e) << 23) : 0.f;
-        rf[kRowMu * 32 + r] = -INFINITY;
-        ri[kRowLo * 32 + r] = lo;
-        ri[kRowHi * 32 + r] = hi;
-      }
-      fence_proxy_async_smem();
+    const int r = tid >> 3, part = tid & 7;
+    constexpr int NCH = D / 128;  // 16-dim chunks per thread
+    const __half* qrow = nullptr;
+    if (r < pq.R) {
+      const int i = r / p.G, hl = r % p.G;
+      qrow = p.q + (static_cast<long long>(pq.q0 + i) * p.Hq + pq.kh * p.G + hl) * D;
     }
+    uint4 qv[NCH][2];
+    float mx = 0.f;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      const int d0 = part * (D / 8) + 16 * c;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        qv[c][hh] = qrow ? __ldg(reinterpret_cast<const uint4*>(qrow + d0 + 8 * hh)) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t w[4] = {qv[c][hh].x, qv[c][hh].y, qv[c][hh].z, qv[c][hh].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+          mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    // 2^e with the row's largest |q| * 2^e in [128, 256); |q| is an fp16
+    // value, so e lies in [-8, 31] and 2^e, 2^-e are normal floats
+    const int e = mx > 0.f ? 134 - static_cast<int>((__float_as_uint(mx) >> 23) & 255u) : 0;
+    const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      const int d0 = part * (D / 8) + 16 * c;
+      uint32_t tw[3][4];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t w[4] = {qv[c][hh].x, qv[c][hh].y, qv[c][hh].z, qv[c][hh].w};
+#pragma unroll
+        for (int k = 0; k < 4; k += 2) {
+          uint32_t a[3], b[3];
+          const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+          const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&w[k + 1]));
+          split3_e4m3(pack_half2(fa.x * up, fa.y * up), a[0], a[1], a[2]);
+          split3_e4m3(pack_half2(fb.x * up, fb.y * up), b[0], b[1], b[2]);
+#pragma unroll
+          for (int t = 0; t < 3; ++t) tw[t][2 * hh + k / 2] = a[t] | (b[t] << 16);
+        }
+      }
+      const uint32_t off = (d0 >> 7) * T::kQSlab + r * 128 + ((((d0 & 127) >> 4) ^ (r & 7)) << 4);
+#pragma unroll
+      for (int t = 0; t < 3; ++t)
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(qs + t * T::kN * 128 + off), "r"(tw[t][0]),
+                     "r"(tw[t][1]), "r"(tw[t][2]), "r"(tw[t][3])
+                     : "memory");
+    }
+    if (part == 0) {
+      int lo = 0, hi = -1;
+      if (r < pq.R) {
+        hi = pq.L - pq.qlen + r / p.G;
+        lo = p.window > 0 ? max(0, hi - p.window + 1) : 0;
+      }
+      rf[kRowFsl * 32 + r] = r < pq.R ? p.sl2 * __uint_as_float(static_cast<uint32_t>(127 - e) << 23) : 0.f;
+      rf[kRowMu * 32 + r] = -INFINITY;
+      ri[kRowLo * 32 + r] = lo;
+      ri[kRowHi * 32 + r] = hi;
+    }
+    fence_proxy_async_smem();
   };
 
   while (next_piece(pc)) {
     const bool direct = pc.npieces == 1;
     const int nblk = (pc.ntiles + T::kBlkTiles - 1) / T::kBlkTiles;
     q_setup(pc);
-    named_bar_sync(1, 128);
+    named_bar_sync(3, 256);
     if (tid == 0) mbar_arrive(bar(kBarQFull));
-    float fs[32];  // score factor of each row
+    float fs[16];  // score factor of each row of this half
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float4 f = reinterpret_cast<const float4*>(rf + kRowFsl * 32)[k];
+    for (int k = 0; k < 4; ++k) {
+      const float4 f = reinterpret_cast<const float4*>(rf + kRowFsl * 32 + rb)[k];
       fs[4 * k] = f.x; fs[4 * k + 1] = f.y; fs[4 * k + 2] = f.z; fs[4 * k + 3] = f.w;
     }
-
-    float lp[32];  // this key lane's share of each row's weight sum
+    float lp[16];  // this key lane's share of each row's weight sum
 #pragma unroll
-    for (int r = 0; r < 32; ++r) lp[r] = 0.f;
+    for (int r = 0; r < 16; ++r) lp[r] = 0.f;
 
     for (int i = 0; i < nblk; ++i) {
       const uint32_t b = bq + i;
       const int sv = b % NBV, sb = b & 1;
       const int key0 = (pc.first_tile + T::kBlkTiles * i) * kTileKeys;
       const int nvalid = min(128, kTileKeys * (pc.ntiles - T::kBlkTiles * i));  // keys loaded
-      // ---- this key's scores for the 32 rows
-      float x[32];
+      // ---- this key's scores for the half's 16 rows (three term slices)
+      float x[16];
       if (ok) ok = mbar_wait(bar(kBarSFull + sb), (b >> 1) & 1, p.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
       tc_fence_after();
       if (ok) {
-        float y[32], z[32];
-        tmem_ld32(tl + T::kColS + T::kNT * sb, x);
-        tmem_ld32(tl + T::kColS + T::kNT * sb + 32, y);
-        tmem_ld32(tl + T::kColS + T::kNT * sb + 64, z);
+        float y[16], z[16];
+        const uint32_t sc = tl + T::kColS + T::kNT * sb + rb;
+        tmem_ld16(sc, x);
+        tmem_ld16(sc + 32, y);
+        tmem_ld16(sc + 64, z);
         tmem_wait_ld();
 #pragma unroll
-        for (int r = 0; r < 32; ++r) x[r] = (x[r] + y[r]) + z[r];
+        for (int r = 0; r < 16; ++r) x[r] = (x[r] + y[r]) + z[r];
       } else {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) x[r] = 0.f;
+        for (int r = 0; r < 16; ++r) x[r] = 0.f;
       }
       tc_fence_before();
       __syncwarp();
       if (ok && lane == 0) mbar_arrive(bar(kBarSEmpty + sb));
-      const int j = key0 + tid;
+      const int j = key0 + key;
       const bool interior = nvalid == 128 && key0 >= pc.tile_lo_all && key0 + 127 <= pc.tile_hi_all;
       if (interior) {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) x[r] *= fs[r];
+        for (int r = 0; r < 16; ++r) x[r] *= fs[r];
       } else {
-        const bool loaded = tid < nvalid;
+        const bool loaded = key < nvalid;
 #pragma unroll
-        for (int r = 0; r < 32; ++r)
-          x[r] = (loaded && j >= ri[kRowLo * 32 + r] && j <= ri[kRowHi * 32 + r])
-                     ? x[r] * fs[r]
-                     : -INFINITY;
+        for (int r = 0; r < 16; ++r)
+          x[r] = (loaded && j >= ri[kRowLo * 32 + rb + r] && j <= ri[kRowHi * 32 + rb + r]) ? x[r] * fs[r]
+                                                                                         : -INFINITY;
       }
       // ---- running maximum per row, raised to the block maximum only where
       // that exceeds it by more than 2^kRaise. Most blocks raise nothing: one
       // OR-barrier tells, and only then are the block maxima reduced.
-      float mu[32];
+      float mu[16];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float4 m4 = reinterpret_cast<const float4*>(rf + kRowMu * 32)[k];
+      for (int k = 0; k < 4; ++k) {
+        const float4 m4 = reinterpret_cast<const float4*>(rf + kRowMu * 32 + rb)[k];
         mu[4 * k] = m4.x; mu[4 * k + 1] = m4.y; mu[4 * k + 2] = m4.z; mu[4 * k + 3] = m4.w;
       }
-      bool up = false;
+      bool upd = false;
 #pragma unroll
-      for (int r = 0; r < 32; ++r) up |= x[r] > mu[r] + T::kRaise;
+      for (int r = 0; r < 16; ++r) upd |= x[r] > mu[r] + T::kRaise;
       bool rescale = false;
-      if (bar_red_or(1, 128, up)) {
+      if (bar_red_or(bid, 128, upd)) {
         {
-          float v[32];
+          float v[16];
 #pragma unroll
-          for (int r = 0; r < 32; ++r) v[r] = x[r];
-          red[warp * 32 + lane] = warp_transpose_reduce<true>(v, lane);
+          for (int r = 0; r < 16; ++r) v[r] = x[r];
+          const float m = warp_transpose_reduce16<true>(v, lane);
+          if (lane < 16) red[(warp & 3) * 16 + lane] = m;
         }
-        named_bar_sync(1, 128);
-        if (warp == 0) {
-          const float mx = fmaxf(fmaxf(red[lane], red[32 + lane]), fmaxf(red[64 + lane], red[96 + lane]));
-          const float m0 = rf[kRowMu * 32 + lane];
+        named_bar_sync(bid, 128);
+        if ((warp & 3) == 0 && lane < 16) {
+          const float mx = fmaxf(fmaxf(red[lane], red[16 + lane]), fmaxf(red[32 + lane], red[48 + lane]));
+          const float m0 = rf[kRowMu * 32 + rb + lane];
           float nmu = m0, al = 1.f;
           if (mx > m0 + T::kRaise) {
             nmu = mx;
             al = (m0 == -INFINITY) ? 0.f : ex2(m0 - mx);
           }
-          rf[kRowMu * 32 + lane] = nmu;
-          rf[kRowAl * 32 + lane] = al;
-          const bool any = __any_sync(0xffffffffu, al != 1.f);
-          if (lane == 0) ri[kRowFlag * 32] = any ? 1 : 0;
+          rf[kRowMu * 32 + rb + lane] = nmu;
+          rf[kRowAl * 32 + rb + lane] = al;
+          const bool any = __any_sync(0x0000ffffu, al != 1.f);
+          if (lane == 0) ri[kRowFlag * 32 + wg] = any ? 1 : 0;
         }
-        named_bar_sync(1, 128);
-        rescale = ri[kRowFlag * 32] != 0;
+        named_bar_sync(bid, 128);
+        rescale = ri[kRowFlag * 32 + wg] != 0;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float4 m4 = reinterpret_cast<const float4*>(rf + kRowMu * 32)[k];
+        for (int k = 0; k < 4; ++k) {
+          const float4 m4 = reinterpret_cast<const float4*>(rf + kRowMu * 32 + rb)[k];
           mu[4 * k] = m4.x; mu[4 * k + 1] = m4.y; mu[4 * k + 2] = m4.z; mu[4 * k + 3] = m4.w;
         }
       }
       // ---- weights 2^(x - mu + kBias) (<= 2^8) and the row sums
 #pragma unroll
-      for (int r = 0; r < 32; ++r) x[r] = ex2(x[r] - (mu[r] == -INFINITY ? 0.f : mu[r] - T::kBias));
+      for (int r = 0; r < 16; ++r) x[r] = ex2(x[r] - (mu[r] == -INFINITY ? 0.f : mu[r] - T::kBias));
       if (rescale) {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) lp[r] = lp[r] * rf[kRowAl * 32 + r] + x[r];
+        for (int r = 0; r < 16; ++r) lp[r] = lp[r] * rf[kRowAl * 32 + rb + r] + x[r];
       } else {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) lp[r] += x[r];
+        for (int r = 0; r < 16; ++r) lp[r] += x[r];
       }
       // ---- the P.V operands are free once the previous block's product is done
       if (ok && b >= 1) ok = mbar_wait(bar(kBarPvDone), (b - 1) & 1, p.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after();
       if (rescale && i > 0 && ok) {
-        // O^T columns of rows whose running maximum was raised
+        // O^T columns of this half's rows whose running maximum was raised
 #pragma unroll 1
         for (int c = 0; c < 3 * S; ++c) {
-          float o[32];
-          tmem_ld32(tl + T::kColO + 32 * c, o);
+          float o[16];
+          tmem_ld16(tl + T::kColO + 32 * c + rb, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int r = 0; r < 32; ++r) o[r] *= rf[kRowAl * 32 + r];
-          tmem_st32(tl + T::kColO + 32 * c, o);
+          for (int r = 0; r < 16; ++r) o[r] *= rf[kRowAl * 32 + rb + r];
+          tmem_st16(tl + T::kColO + 32 * c + rb, o);
         }
         tmem_wait_st();
       }
-      // ---- P^T, three e4m3 terms: this key's 32 row weights are one 32-byte
-      // row (k = key) of an MN-major operand in the 32-byte swizzle layout
-      // (8-key atoms of 256 bytes; the two 16-byte halves swap in rows 4-7)
+      // ---- P^T, three e4m3 terms: this key's 16 row weights are one 16-byte
+      // half of a 32-byte row (k = key) of an MN-major operand in the 32-byte
+      // swizzle layout (8-key atoms of 256 bytes; the halves swap in rows 4-7)
       {
-        uint32_t tt[3][16];
+        uint32_t tt[3][8];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) split3_e4m3(pack_half2(x[2 * k], x[2 * k + 1]), tt[0][k], tt[1][k], tt[2][k]);
-        const uint32_t row = pt + (tid >> 3) * 256 + (tid & 7) * 32;
-        const uint32_t flip = ((tid & 7) >> 2) << 4;
+        for (int k = 0; k < 8; ++k) split3_e4m3(pack_half2(x[2 * k], x[2 * k + 1]), tt[0][k], tt[1][k], tt[2][k]);
+        const uint32_t row = pt + (key >> 3) * 256 + (key & 7) * 32 + ((wg ^ ((key & 7) >> 2)) << 4);
 #pragma unroll
-        for (int t = 0; t < 3; ++t) {
-          uint32_t w[8];
-#pragma unroll
-          for (int m = 0; m < 8; ++m) w[m] = tt[t][2 * m] | (tt[t][2 * m + 1] << 16);
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(row + t * T::kPtTerm + flip), "r"(w[0]),
-                       "r"(w[1]), "r"(w[2]), "r"(w[3])
+        for (int t = 0; t < 3; ++t)
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(row + t * T::kPtTerm),
+                       "r"(tt[t][0] | (tt[t][1] << 16)), "r"(tt[t][2] | (tt[t][3] << 16)),
+                       "r"(tt[t][4] | (tt[t][5] << 16)), "r"(tt[t][6] | (tt[t][7] << 16))
                        : "memory");
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(row + t * T::kPtTerm + (16 ^ flip)),
-                       "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                       : "memory");
-        }
       }
       // ---- V rows of keys past the sequence end or not loaded (stale or
-      // unwritten bytes, NaN codes included) are zeroed in the ring: the P.V
-      // product reads V there, and a zero weight must not meet a NaN
+      // unwritten bytes, NaN codes included) are zeroed in the ring by the first
+      // group: the P.V product reads V there, and a zero weight must not meet a NaN
       const int lim = min(nvalid, pc.L - key0);
-      if (lim < 128) {
+      if (wg == 0 && lim < 128) {
         if (ok) ok = mbar_wait(fullv0 + 8 * sv, (b / NBV) & 1, p.timeout_ns);
         ok = __all_sync(0xffffffffu, ok);
-        if (ok && tid >= lim) {
-          const uint32_t vrow = sbase + T::kOffV + sv * T::kKBlk + tid * 128;
+        if (ok && key >= lim) {
+          const uint32_t vrow = sbase + T::kOffV + sv * T::kKBlk + key * 128;
 #pragma unroll
           for (int sl = 0; sl < S; ++sl)
 #pragma unroll
@@ -422,38 +438,43 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
     }
     bq += nblk;
 
-    // ---- epilogue: O^T (this thread: dims tid, tid + 128), row sums, output
+    // ---- epilogue: O^T (this thread: dims key, key + 128) of the half's rows,
+    // row sums, output
     if (ok) ok = mbar_wait(bar(kBarPvDone), (bq - 1) & 1, p.timeout_ns);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
-    float o[S][32];
+    float o[S][16];
 #pragma unroll
     for (int h = 0; h < S; ++h) {
       if (ok) {
-        float y[32], z[32];
-        tmem_ld32(tl + T::kColO + T::kNT * h, o[h]);
-        tmem_ld32(tl + T::kColO + T::kNT * h + 32, y);
-        tmem_ld32(tl + T::kColO + T::kNT * h + 64, z);
+        float y[16], z[16];
+        const uint32_t oc = tl + T::kColO + T::kNT * h + rb;
+        tmem_ld16(oc, o[h]);
+        tmem_ld16(oc + 32, y);
+        tmem_ld16(oc + 64, z);
         tmem_wait_ld();
 #pragma unroll
-        for (int r = 0; r < 32; ++r) o[h][r] = (o[h][r] + y[r]) + z[r];
+        for (int r = 0; r < 16; ++r) o[h][r] = (o[h][r] + y[r]) + z[r];
       } else {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) o[h][r] = 0.f;
+        for (int r = 0; r < 16; ++r) o[h][r] = 0.f;
       }
     }
     tc_fence_before();
     {
-      float v[32];
+      float v[16];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) v[r] = lp[r];
-      red[warp * 32 + lane] = warp_transpose_reduce<false>(v, lane);
+      for (int r = 0; r < 16; ++r) v[r] = lp[r];
+      const float sum = warp_transpose_reduce16<false>(v, lane);
+      if (lane < 16) red[(warp & 3) * 16 + lane] = sum;
     }
-    named_bar_sync(1, 128);
-    if (warp == 0) rf[kRowL * 32 + lane] = (red[lane] + red[32 + lane]) + (red[64 + lane] + red[96 + lane]);
-    named_bar_sync(1, 128);
+    named_bar_sync(bid, 128);
+    if ((warp & 3) == 0 && lane < 16)
+      rf[kRowL * 32 + rb + lane] = (red[lane] + red[16 + lane]) + (red[32 + lane] + red[48 + lane]);
+    named_bar_sync(bid, 128);
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
+    for (int k = 0; k < 16; ++k) {
+      const int r = rb + k;
       if (r >= pc.R) break;
       const float L = rf[kRowL * 32 + r];
       if (direct) {
@@ -461,20 +482,21 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
         __half* dst = p.out + (static_cast<long long>(pc.q0 + i) * p.Hq + pc.kh * p.G + hl) * D;
         const float inv = L > 0.f ? p.out_scale / L : 0.f;
 #pragma unroll
-        for (int h = 0; h < S; ++h) dst[128 * h + tid] = __float2half_rn(o[h][r] * inv);
+        for (int h = 0; h < S; ++h) dst[128 * h + key] = __float2half_rn(o[h][k] * inv);
       } else {
         float* dst = p.ws_o + (static_cast<long long>(pc.slot) * p.rows_padded + r) * D;
 #pragma unroll
-        for (int h = 0; h < S; ++h) __stcg(dst + 128 * h + tid, o[h][r]);
+        for (int h = 0; h < S; ++h) __stcg(dst + 128 * h + key, o[h][k]);
       }
     }
-    if (!direct && tid < pc.R) {
-      const float mu = rf[kRowMu * 32 + tid];
-      __stcg(reinterpret_cast<float2*>(p.ws_ml + (static_cast<long long>(pc.slot) * p.rows_padded + tid) * 2),
-             make_float2(mu == -INFINITY ? -INFINITY : mu - T::kBias, rf[kRowL * 32 + tid]));
+    if (!direct && key < 16 && rb + key < pc.R) {
+      const int r = rb + key;
+      const float mu = rf[kRowMu * 32 + r];
+      __stcg(reinterpret_cast<float2*>(p.ws_ml + (static_cast<long long>(pc.slot) * p.rows_padded + r) * 2),
+             make_float2(mu == -INFINITY ? -INFINITY : mu - T::kBias, rf[kRowL * 32 + r]));
     }
     if (tid == 0) post_unit_descriptor(p, pc);
-    named_bar_sync(1, 128);  // red[] and the row state are reused by the next piece
+    named_bar_sync(3, 256);  // the row state and red[] are rewritten by the next piece
   }
   if (!ok && lane == 0) raise_error(p.error_flag, kErrTimeout);
 }
@@ -506,9 +528,9 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     }
     mbar_init(bar(kBarSFull), 1);
     mbar_init(bar(kBarSFull + 1), 1);
-    mbar_init(bar(kBarSEmpty), 4);
-    mbar_init(bar(kBarSEmpty + 1), 4);
-    mbar_init(bar(kBarPFull), 4);
+    mbar_init(bar(kBarSEmpty), 8);  // the eight softmax warps
+    mbar_init(bar(kBarSEmpty + 1), 8);
+    mbar_init(bar(kBarPFull), 8);
     mbar_init(bar(kBarPvDone), 1);
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarFinal), 1);
@@ -554,8 +576,16 @@ __global__ void __launch_bounds__(T::kThreads, 1)
   Piece pc;
   bool ok = true;
 
-  if (warp == T::kProducerWarp) {
-    // ---------------------------------------------------------------- producer
+  if (warp == T::kProducerWarp || warp == T::kProducerWarp + 1) {
+    // --------------------------------------------------------------- producers
+    // warp kProducerWarp fills the K ring, the next warp the V ring: each waits
+    // only for its own ring's empty stages, so K runs ahead of V (a V stage is
+    // held until the P.V product that reads it completes)
+    const bool is_v = warp != T::kProducerWarp;
+    const int nb = is_v ? NBV : NBK;
+    const uint32_t fullb = is_v ? fullv0 : fullk0, emptyb = is_v ? emptyv0 : emptyk0;
+    const uint32_t ringb = sbase + (is_v ? T::kOffV : 0);
+    const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
     const uint64_t pol = l2_policy_evict_first();
     uint32_t bq = 0, posted = 0;  // blocks walked; blocks whose loads were all issued
     while (work_next(p, s_pre, it, pc)) {
@@ -569,7 +599,6 @@ __global__ void __launch_bounds__(T::kThreads, 1)
       };
       // block table entries 32 tiles (4 blocks) at a time, the next group in flight
       int cur = load_group(0), nxt = pc.ntiles > 32 ? load_group(32) : 0;
-      constexpr int kBoxes = 2 * T::kSlabs;  // boxes per tile: K slabs, then V slabs
       for (int i = 0; i < nblk; ++i) {
         const int t0 = i * T::kBlkTiles;
         if (t0 > 0 && t0 % 32 == 0) {
@@ -577,37 +606,31 @@ __global__ void __launch_bounds__(T::kThreads, 1)
           nxt = t0 + 32 < pc.ntiles ? load_group(t0 + 32) : 0;
         }
         const uint32_t b = bq + i;
-        const int sk = b % NBK, sv = b % NBV;
+        const int st = b % nb;
         const int ntb = min(T::kBlkTiles, pc.ntiles - t0);
         if (lane == 0) {
-          const uint32_t bytes = ntb * T::kSlabs * T::kTileBox;
-          if (ok && b >= NBK) ok = mbar_wait(emptyk0 + 8 * sk, ((b / NBK) - 1) & 1, p.timeout_ns);
-          if (ok && b >= NBV) ok = mbar_wait(emptyv0 + 8 * sv, ((b / NBV) - 1) & 1, p.timeout_ns);
+          if (ok && b >= static_cast<uint32_t>(nb)) ok = mbar_wait(emptyb + 8 * st, ((b / nb) - 1) & 1, p.timeout_ns);
           if (ok && p.inject == 1) ok = false;  // injected fault: the rings stay empty
           if (ok) {
-            mbar_arrive_expect_tx(fullk0 + 8 * sk, bytes);
-            mbar_arrive_expect_tx(fullv0 + 8 * sv, bytes);
+            mbar_arrive_expect_tx(fullb + 8 * st, ntb * T::kSlabs * T::kTileBox);
             posted = b + 1;
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        // lane l: tile l / kBoxes of the block, box l % kBoxes (all boxes at once)
-        const int j = min(lane / kBoxes, T::kBlkTiles - 1);
+        // lane l: tile l / kSlabs of the block, slab l % kSlabs (all boxes at once)
+        const int j = min(lane / T::kSlabs, T::kBlkTiles - 1);
         int blk = __shfl_sync(0xffffffffu, cur, (t0 % 32) + j);
         if (!ok) continue;
-        if (lane < kBoxes * ntb) {
+        if (lane < T::kSlabs * ntb) {
           if (blk < 0 || blk >= p.num_blocks) {
-            raise_error(p.error_flag, kErrBlockId);
+            if (!is_v) raise_error(p.error_flag, kErrBlockId);
             blk = 0;
           }
           const int gt = pc.first_tile + t0 + j;
           const int z = blk * p.block_size + (gt % p.tiles_per_block) * kTileKeys;
-          const int bx2 = lane % kBoxes, sl = bx2 % T::kSlabs;
-          const bool is_v = bx2 >= T::kSlabs;
-          const uint32_t dst = sbase + (is_v ? T::kOffV + sv * T::kKBlk : sk * T::kKBlk) + sl * T::kSlabBlk +
-                               j * T::kTileBox;
-          tma_load_3d(dst, is_v ? &tm_v : &tm_k, is_v ? fullv0 + 8 * sv : fullk0 + 8 * sk, sl * 128, pc.kh, z,
-                      pol);
+          const int sl = lane % T::kSlabs;
+          tma_load_3d(ringb + st * T::kKBlk + sl * T::kSlabBlk + j * T::kTileBox, tm, fullb + 8 * st, sl * 128,
+                      pc.kh, z, pol);
         }
       }
       bq += nblk;
@@ -615,12 +638,9 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     if (lane == 0) {
       if (!ok) raise_error(p.error_flag, kErrTimeout);
       // every load issued lands before the CTA exits: a block's loads are all
-      // issued once its transaction counts are posted, so wait for the last
-      // posted blocks of each ring
-      for (uint32_t k = posted > NBK ? posted - NBK : 0; k < posted; ++k)
-        if (!mbar_wait(fullk0 + 8 * (k % NBK), (k / NBK) & 1, kDrainLimitNs)) break;
-      for (uint32_t k = posted > NBV ? posted - NBV : 0; k < posted; ++k)
-        if (!mbar_wait(fullv0 + 8 * (k % NBV), (k / NBV) & 1, kDrainLimitNs)) break;
+      // issued once its transaction count is posted
+      for (uint32_t k = posted > static_cast<uint32_t>(nb) ? posted - nb : 0; k < posted; ++k)
+        if (!mbar_wait(fullb + 8 * (k % nb), (k / nb) & 1, kDrainLimitNs)) break;
     }
   } else if (warp == T::kMmaWarp) {
     // ------------------------------------------------------------- MMA issuer
