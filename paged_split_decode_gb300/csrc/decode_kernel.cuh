@@ -75,6 +75,7 @@ struct DecodeParams {
   int max_blocks, block_size, num_blocks, tiles_per_block;
   int window;                 // <= 0: none
   int num_splits;             // 0: balanced
+  int unit_cost;              // balanced: virtual tiles charged to the start of every unit
   float sl2;                  // scale * log2(e) * k_scale
   float out_scale;            // v_scale (1 for fp16)
   int out_bf16;               // q and out hold bfloat16 (bfloat16 caches)
@@ -208,7 +209,7 @@ struct Piece {
   int unit_t0;      // first visible tile of the unit (within the sequence)
   int unit;         // b * hgn + head group
   int first_slot_cta;  // balanced mode: the first chunk covering the unit
-  long long unit_start;  // balanced mode: global tile index where the unit begins
+  long long unit_start;  // balanced mode: global index of the unit's first real tile
   int tile_lo_all;     // keys [tile_lo_all, tile_hi_all] are visible to every query
   int tile_hi_all;     // token of the unit (empty range when hi < lo)
   int qlen;            // query tokens of sequence b (0: nothing to compute or write)
@@ -273,7 +274,10 @@ __device__ __forceinline__ void seq_span(const DecodeParams& p, int b, bool repo
 
 // Balanced mode: the visible 16-key tiles of all units, laid end to end (T of
 // them), are cut into Ce = min(grid, T) contiguous ranges of equal size (to
-// one tile), one per CTA; chunk k is CTA k's range. (A dynamic tail -- small
+// one tile), one per CTA; chunk k is CTA k's range. A kernel whose pieces have
+// a fixed cost (set-up, epilogue) charges unit_cost virtual tiles before the
+// tiles of every unit, so a range that takes on a second unit gets fewer real
+// tiles; a range's virtual tiles do no work. (A dynamic tail -- small
 // chunks taken from a global counter -- was measured and lost: every chunk
 // costs a key-group merge, a partial and a deeper combine tree.)
 struct ChunkPlan {
@@ -333,27 +337,32 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
                                           Piece& pc) {
   const int C = gridDim.x;
   if (p.num_splits == 0) {
-    if (it.g < it.g_end) {
+    while (it.g < it.g_end) {
       while (s_pre[it.b + 1] <= it.g) ++it.b;
       const int b = it.b;
-      const int n = (s_pre[b + 1] - s_pre[b]) / p.hgn;
+      const int span = (s_pre[b + 1] - s_pre[b]) / p.hgn;  // unit_cost + visible tiles
       const long long off = it.g - s_pre[b];
-      const int grp = static_cast<int>(off / n);
-      const long long us = s_pre[b] + static_cast<long long>(grp) * n;
-      const long long ue = us + n;
+      const int grp = static_cast<int>(off / span);
+      const long long us = s_pre[b] + static_cast<long long>(grp) * span;
+      const long long rs = us + p.unit_cost;  // the unit's first real tile
+      const long long ue = us + span;
+      if (it.g < rs) {  // the range starts in the unit's virtual tiles
+        it.g = rs;
+        if (it.g >= it.g_end) break;
+      }
       const long long pe = ue < it.g_end ? ue : it.g_end;
       int L, t0, nn, q0, qn;
       seq_span(p, b, false, L, t0, nn, q0, qn);
       pc.b = b; pc.kh = grp * p.hg; pc.L = L; pc.unit_t0 = t0; pc.unit = b * p.hgn + grp;
       pc.qlen = qn; pc.R = p.G * qn; pc.q0 = q0;
-      pc.first_tile = t0 + static_cast<int>(it.g - us);
+      pc.first_tile = t0 + static_cast<int>(it.g - rs);
       pc.ntiles = static_cast<int>(pe - it.g);
-      const int cf = it.cp.owner(us), cl = it.cp.owner(ue - 1);
+      const int cf = it.cp.owner(rs), cl = it.cp.owner(ue - 1);
       pc.npieces = cl - cf + 1;
-      pc.slot = 2 * it.chunk + (it.chunk_start < us ? 1 : 0);
+      pc.slot = 2 * it.chunk + (it.chunk_start < rs ? 1 : 0);
       pc.chunk = it.chunk;
       pc.first_slot_cta = cf;
-      pc.unit_start = us;
+      pc.unit_start = rs;
       common_range(p, L, pc);
       it.g = pe;
       return true;
@@ -449,7 +458,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
       if (b < p.B) {
         int L, t0, n, q0, qn;
         seq_span(p, b, blockIdx.x == 0, L, t0, n, q0, qn);
-        v = n * p.hgn;
+        v = n > 0 ? (n + p.unit_cost) * p.hgn : 0;
       }
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {

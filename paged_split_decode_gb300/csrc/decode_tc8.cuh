@@ -65,6 +65,11 @@ struct Tc8 {
   static constexpr uint32_t kIdescS = idesc_e4m3(128, kNT);               // K-major A and B
   static constexpr uint32_t kIdescO = idesc_e4m3(128, kNT) | (3u << 15);  // A (V^T), B (P^T) MN-major
   static constexpr float kRaise = 4.f;              // running max raised past this gap (log2)
+  // Balanced split: a piece's fixed cost (q set-up, pipeline refill, epilogue)
+  // is charged as this many 16-key tiles to the start of every unit (measured
+  // on the qlen=3 verify shape: 0 / 8 / 16 / 24 / 32 tiles -> 44.5 / 43.3 /
+  // 41.7 / 40.2 / 40.2 us per step).
+  static constexpr int kUnitCost = 24;
   static constexpr float kBias = 4.f;               // weights are 2^(x - m + kBias) <= 2^8
 
   static constexpr int kOffV = NBK * kKBlk;
@@ -554,7 +559,7 @@ __global__ void __launch_bounds__(T::kThreads, 1)
       if (b < p.B) {
         int L, t0, n, q0, qn;
         seq_span(p, b, blockIdx.x == 0, L, t0, n, q0, qn);
-        v = n * p.hgn;
+        v = n > 0 ? (n + p.unit_cost) * p.hgn : 0;
       }
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -742,6 +747,7 @@ bool shape_tc8(int nt, KernelShape* out) {
   out->rows_padded = 8 * nt;
   out->ctas_per_sm = 1;
   out->heads = 1;
+  out->unit_cost = T::kUnitCost;
   return true;
 }
 

@@ -15,6 +15,7 @@ struct KernelShape {
   int rows_padded;  // RP: query rows per unit rounded up to the row-tile size
   int ctas_per_sm;  // resident CTAs per SM the configuration is sized for
   int heads;        // KV heads per tile (the TMA box's head extent)
+  int unit_cost;    // balanced split: virtual tiles charged to every unit start
 };
 
 // Returns false when no instantiation covers (D, kv kind, nt, grouped):
@@ -105,6 +106,7 @@ bool shape_of(KernelShape* out) {
   out->rows_padded = Cfg::RP;
   out->ctas_per_sm = Cfg::kMinBlocks;
   out->heads = Cfg::HG;
+  out->unit_cost = 0;
   return true;
 }
 

@@ -58,6 +58,7 @@ struct Plan {
   long long n_desc; // split-combine descriptors
   long long units;  // B * Hkv / hg work units
   int rows_padded;
+  int unit_cost;    // balanced split: virtual tiles per unit start
   size_t off_ml, off_o, bytes;  // workspace layout
 };
 
@@ -83,7 +84,7 @@ pd_status check_dims(const pd_dims* d, int qlen) {
   // 32-bit index headroom: tiles, keys and cache rows
   const long long cap_keys = static_cast<long long>(d->max_blocks_per_seq) * d->block_size;
   if (cap_keys > (1ll << 30)) return PD_ERR_UNSUPPORTED;
-  if (static_cast<long long>(d->B) * d->Hkv * (cap_keys / kTileKeys + 1) > (1ll << 31) - 1)
+  if (static_cast<long long>(d->B) * d->Hkv * (cap_keys / kTileKeys + 1 + 64) > (1ll << 31) - 1)
     return PD_ERR_UNSUPPORTED;
   if (static_cast<long long>(d->num_blocks) * d->block_size > (1ll << 31) - 1) return PD_ERR_UNSUPPORTED;
   if (static_cast<long long>(d->B) * qlen * d->Hq > (1ll << 31) - 1) return PD_ERR_UNSUPPORTED;
@@ -116,6 +117,7 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
     return PD_ERR_UNSUPPORTED;
   pl->hg = ks.heads;
   pl->rows_padded = ks.rows_padded;
+  pl->unit_cost = ks.unit_cost;
   pl->units = static_cast<long long>(d->B) * (d->Hkv / pl->hg);
   int splits = num_splits;
   if (splits == 0 && d->B > kMaxAutoB) splits = 1;  // plenty of units: one piece each
@@ -290,6 +292,7 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   p.tiles_per_block = dims->block_size / kTileKeys;
   p.window = window > 0 ? window : 0;
   p.num_splits = pl.splits;
+  p.unit_cost = pl.unit_cost;
   const double ks = fp8 ? static_cast<double>(dims->k_scale) : 1.0;
   p.sl2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 * ks);
   p.out_scale = fp8 ? dims->v_scale : 1.0f;

@@ -44,32 +44,39 @@ def owner(cp, x):
     return ((x + 1) * cp["Ce"] - 1) // cp["T"]
 
 
-def all_pieces(grid, B, Hkv, lens, qlen, window, cap, S, rng):
-    """Every CTA's pieces."""
+def all_pieces(grid, B, Hkv, lens, qlen, window, cap, S, rng, cost=0):
+    """Every CTA's pieces. In balanced mode each unit with visible tiles is
+    preceded by `cost` virtual tiles (a piece's fixed cost), which count when
+    the ranges are cut but are not processed."""
     spans = [seq_span(L, qlen, window, cap) for L in lens]
     per_cta = {c: [] for c in range(grid)}
     if S == 0:
         pre = [0]
         for _, _, n in spans:
-            pre.append(pre[-1] + n * Hkv)
+            pre.append(pre[-1] + ((n + cost) * Hkv if n > 0 else 0))
         cp = chunk_plan(pre[B], grid)
         for k in range(cp["Ce"]):
             cta = k
             g, ge = chunk_start(cp, k), chunk_end(cp, k)
             while g < ge:
                 b = max(i for i in range(B) if pre[i] <= g)
-                n = (pre[b + 1] - pre[b]) // Hkv
-                kh = (g - pre[b]) // n
-                us = pre[b] + kh * n
-                ue = us + n
+                span = (pre[b + 1] - pre[b]) // Hkv
+                kh = (g - pre[b]) // span
+                us = pre[b] + kh * span
+                rs = us + cost  # first real tile of the unit
+                ue = us + span
+                if g < rs:
+                    g = rs
+                    if g >= ge:
+                        break
                 pe = min(ue, ge)
                 L, t0, _ = spans[b]
-                cf, cl = owner(cp, us), owner(cp, ue - 1)
+                cf, cl = owner(cp, rs), owner(cp, ue - 1)
                 npieces = cl - cf + 1
-                slots = [2 * cf + (1 if chunk_start(cp, cf) < us else 0)] + \
+                slots = [2 * cf + (1 if chunk_start(cp, cf) < rs else 0)] + \
                         [2 * (cf + q) for q in range(1, npieces)]
-                per_cta[cta].append(dict(unit=b * Hkv + kh, tiles=list(range(t0 + g - us, t0 + pe - us)),
-                                         npieces=npieces, slot=2 * k + (1 if chunk_start(cp, k) < us else 0),
+                per_cta[cta].append(dict(unit=b * Hkv + kh, tiles=list(range(t0 + g - rs, t0 + pe - rs)),
+                                         npieces=npieces, slot=2 * k + (1 if chunk_start(cp, k) < rs else 0),
                                          all_slots=slots))
                 g = pe
         for c in range(grid):
@@ -99,11 +106,11 @@ def all_pieces(grid, B, Hkv, lens, qlen, window, cap, S, rng):
     return per_cta, (B * Hkv * S if S > 1 else 0)
 
 
-def check(B, Hkv, lens, qlen, window, cap, S, grid, seed=0):
+def check(B, Hkv, lens, qlen, window, cap, S, grid, seed=0, cost=0):
     seen = {}
     slots_used = []
     units_pieces = {}
-    per_cta, nslots = all_pieces(grid, B, Hkv, lens, qlen, window, cap, S, random.Random(seed))
+    per_cta, nslots = all_pieces(grid, B, Hkv, lens, qlen, window, cap, S, random.Random(seed), cost)
     for c in range(grid):
         for pc in per_cta[c]:
             u = pc["unit"]
@@ -159,6 +166,33 @@ def test_schedule_covers_each_tile_once(case, S, grid):
     check(B, Hkv, lens, qlen, window, cap, S, grid)
 
 
+@pytest.mark.parametrize("grid", [1, 3, 7, 152])
+@pytest.mark.parametrize("cost", [1, 16, 1000])
+@pytest.mark.parametrize("case", CASES)
+def test_balanced_schedule_with_unit_cost(case, cost, grid):
+    """The tensor-memory kernel's split: every unit start charged `cost`
+    virtual tiles (ranges that fall inside them do nothing)."""
+    B, Hkv, lens, qlen, window = case
+    check(B, Hkv, lens, qlen, window, 1 << 20, 0, grid, cost=cost)
+
+
+def test_unit_cost_unloads_ranges_that_take_a_second_unit():
+    # 32 units of 512 tiles over 152 ranges: without a cost every range gets
+    # 107-108 real tiles whether it spans one unit or two; with a cost, a range
+    # holding a unit's start gets up to `cost` fewer, and a range that takes on
+    # a second unit always holds one
+    B, Hkv, lens = 8, 4, [8192] * 8
+    for cost in (0, 16):
+        per_cta, _ = all_pieces(152, B, Hkv, lens, 3, 0, 1 << 20, 0, random.Random(0), cost=cost)
+        real = [sum(len(pc["tiles"]) for pc in per_cta[c]) for c in range(152)]
+        two = [r for c, r in enumerate(real) if len(per_cta[c]) == 2]
+        one = [r for c, r in enumerate(real) if len(per_cta[c]) == 1]
+        assert sum(real) == B * Hkv * 512 and two and one
+        assert max(real) - min(real) <= cost + 1
+        if cost:
+            assert max(two) <= max(one) - cost
+
+
 def test_schedule_random():
     rng = random.Random(0)
     for _ in range(200):
@@ -169,4 +203,5 @@ def test_schedule_random():
         window = rng.choice([0, 0, rng.randint(1, 500)])
         S = rng.choice([0, 0, 1, 2, 5, 9])
         grid = rng.choice([1, 2, 5, 16, 152])
-        check(B, Hkv, lens, qlen, window, 1 << 20, S, grid, seed=rng.randrange(1 << 30))
+        cost = rng.choice([0, 0, 16, rng.randint(1, 200)]) if S == 0 else 0
+        check(B, Hkv, lens, qlen, window, 1 << 20, S, grid, seed=rng.randrange(1 << 30), cost=cost)
