@@ -448,6 +448,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
+  // Launched with programmatic dependent launch: everything above touches no
+  // global memory; wait here until the preceding grid in the stream has
+  // completed and its writes are visible (a no-op without one).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // Balanced mode: prefix over sequences of Hkv * (visible tiles), by warp 0.
   if (p.num_splits == 0 && warp == 0) {
     int carry = 0;

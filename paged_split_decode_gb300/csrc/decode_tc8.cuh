@@ -549,6 +549,8 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
+  // programmatic dependent launch: no global memory was touched above
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // balanced mode: prefix over sequences of visible tiles (as decode_kernel)
   if (p.num_splits == 0 && warp == 0) {
     int carry = 0;
@@ -737,8 +739,7 @@ cudaError_t launch_tc8(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);
   }
-  decode_tc8_kernel<T><<<grid, T::kThreads, T::kSmemBytes, stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  return launch_pdl(decode_tc8_kernel<T>, grid, T::kThreads, T::kSmemBytes, stream, tk, tv, p);
 }
 template <class T>
 bool shape_tc8(int nt, KernelShape* out) {

@@ -59,6 +59,26 @@ cudaError_t launch_bf16_d128(int nt, int grouped, const CUtensorMap&, const CUte
 cudaError_t launch_bf16_d256(int nt, int grouped, const CUtensorMap&, const CUtensorMap&,
                              const DecodeParams&, int, cudaStream_t);
 
+// Launch with programmatic dependent launch: the kernel's CTAs may be
+// scheduled while the preceding grid in the stream drains; the kernel waits
+// (griddepcontrol.wait) before its first global memory access.
+template <class Kern, class... Args>
+cudaError_t launch_pdl(Kern kernel, int grid, int threads, int smem, cudaStream_t stream, const Args&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 // Launch one configuration; sets the shared-memory opt-in once per device.
 template <class Cfg>
 cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
@@ -74,8 +94,7 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);
   }
-  decode_paged_kernel<Cfg><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  return launch_pdl(decode_paged_kernel<Cfg>, grid, Cfg::kThreads, Cfg::kSmemBytes, stream, tk, tv, p);
 }
 
 // Largest ring (stage count, capped at 32) whose shared-memory plan lets
