@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <atomic>
@@ -99,7 +100,22 @@ int device_sm_count(int sm_count) {
   return n;
 }
 
-pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Plan* pl) {
+// Automatic split (num_splits = 0): balanced over every resident CTA slot,
+// except when the units are few (<= a quarter of the CTA slots) and either
+// their work is small (at most 24 visible tiles per CTA slot, from the table
+// capacity and the window: latency-bound, where each piece's fixed cost and
+// the combine's fan-in dominate) or the kernel's pieces carry a fixed cost
+// (the tensor-memory kernel): then a fixed split of each unit into
+// floor(0.84 CTA slots / units) chunks, one per CTA, which leaves about a
+// sixth of the SMs idle but gives every CTA one piece. Measured on GB300
+// (D=256 GQA 6:1, L=4096): B = 1 / 2 / 3 12.9 / 16.1 / 19.2 -> 12.0 / 15.0 /
+// 18.0 us; windowed L=32768 B = 1 / 2 12.8 / 15.8 -> 12.0 / 14.9 us; qlen=3
+// e4m3 verify B=8 39.8 -> 36.0 us; shapes with more work per CTA (B >= 8 at
+// L=4096, L=32768 without a window) stay balanced: there the two splits are
+// within ~2 % or the fixed one loses (B=16: +1.0 us, 2 x 2048 tiles: +0.5). The
+// workspace is sized for the balanced split in either case (the fixed split
+// needs fewer slots), so pd_workspace_bytes does not depend on the window.
+pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Plan* pl, int window = 0) {
   pd_status st = check_dims(d, qlen);
   if (st != PD_OK) return st;
   if (num_splits < 0) return PD_ERR_SHAPE;
@@ -121,8 +137,16 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
   pl->units = static_cast<long long>(d->B) * (d->Hkv / pl->hg);
   int splits = num_splits;
   if (splits == 0 && d->B > kMaxAutoB) splits = 1;  // plenty of units: one piece each
-  pl->splits = splits;
   const int ctas = sms * ks.ctas_per_sm;  // persistent grid: every resident CTA slot
+  const bool automatic = splits == 0;
+  if (automatic && pl->units > 0 && pl->units <= ctas / 4) {
+    const long long cap_keys = static_cast<long long>(d->max_blocks_per_seq) * d->block_size;
+    const long long vis_keys = window > 0 ? std::min<long long>(cap_keys, window + qlen + kTileKeys) : cap_keys;
+    const long long tiles = pl->units * (vis_keys / kTileKeys + 1);
+    if (tiles <= 24ll * ctas || ks.unit_cost > 0)
+      splits = static_cast<int>(std::max<long long>(1, (ctas * 27 / 32) / pl->units));
+  }
+  pl->splits = splits;
   if (splits == 0) {
     pl->grid = ctas;
     pl->slots = 2ll * ctas;  // a CTA's range holds at most two split pieces
@@ -133,13 +157,17 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
     pl->slots = splits > 1 ? pieces : 0;
     pl->n_desc = splits > 1 ? pl->units : 0;
   }
-  if (pl->slots == 0) {
+  // an automatic plan sizes its workspace for the balanced split, whichever
+  // split it chose (so the size does not depend on the window)
+  const long long ws_slots = automatic && d->B <= kMaxAutoB ? 2ll * ctas : pl->slots;
+  const long long ws_desc = automatic && d->B <= kMaxAutoB ? pl->units : pl->n_desc;
+  if (pl->slots == 0 && ws_slots == 0) {
     pl->off_ml = pl->off_o = pl->bytes = 0;
   } else {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-    const size_t cnt = up(static_cast<size_t>(pl->n_desc) * 16);
-    const size_t ml = up(static_cast<size_t>(pl->slots) * pl->rows_padded * 2 * 4);
-    const size_t o = static_cast<size_t>(pl->slots) * pl->rows_padded * d->D * 4;
+    const size_t cnt = up(static_cast<size_t>(ws_desc) * 16);
+    const size_t ml = up(static_cast<size_t>(ws_slots) * pl->rows_padded * 2 * 4);
+    const size_t o = static_cast<size_t>(ws_slots) * pl->rows_padded * d->D * 4;
     pl->off_ml = cnt;
     pl->off_o = cnt + ml;
     pl->bytes = cnt + ml + o;
@@ -251,7 +279,7 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     return PD_ERR_ALIGN;
   if (dims->num_blocks == 0) return PD_ERR_SHAPE;
   Plan pl;
-  st = make_plan(dims, qlen, num_splits, 0, &pl);
+  st = make_plan(dims, qlen, num_splits, 0, &pl, window);
   if (st != PD_OK) return st;
   if (pl.bytes > 0) {
     if (!workspace || workspace_bytes < pl.bytes) return PD_ERR_WORKSPACE;

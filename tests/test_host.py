@@ -87,6 +87,22 @@ def test_workspace_and_grid_plans(lib):
     assert ws3 == up(32 * 16) + up(608 * 24 * 2 * 4) + 608 * 24 * 256 * 4
 
 
+def test_automatic_split_for_few_units(lib):
+    up = lambda x: (x + 255) // 256 * 256
+    # B=1..3 at L <= 4096 (2..6 units of at most 257 tiles, <= 24 tiles per
+    # CTA slot): each unit is cut into floor(128 / units) pieces, one per CTA
+    for B, units in ((1, 2), (2, 4), (3, 6)):
+        assert binding.grid_ctas(_dims(B=B), 1, 0, sm_count=152) == units * (128 // units)
+        # the workspace stays the balanced split's (two slots per CTA slot)
+        assert binding.workspace_bytes(_dims(B=B), 1, 0, sm_count=152) == \
+            up(units * 16) + up(304 * 16 * 2 * 4) + 304 * 16 * 256 * 4
+    # long tables (bandwidth-bound): balanced over every CTA slot
+    assert binding.grid_ctas(_dims(B=1, max_blocks_per_seq=2048), 1, 0, sm_count=152) == 152
+    assert binding.grid_ctas(_dims(B=8), 1, 0, sm_count=152) == 152
+    # e4m3 verify (tensor-memory kernel, 32 per-head units): fixed, 4 pieces each
+    assert binding.grid_ctas(_dims(B=8, kv_fp8=True, max_blocks_per_seq=512), 3, 0, sm_count=152) == 128
+
+
 @pytest.mark.parametrize("kw,qlen", [
     (dict(D=64), 1), (dict(D=96), 1), (dict(block_size=8), 1), (dict(Hq=24, Hkv=5), 1),
     (dict(Hq=40, Hkv=1), 1), (dict(), 9), (dict(Hq=24, Hkv=4), 6),
