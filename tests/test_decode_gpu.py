@@ -300,6 +300,74 @@ def test_block_permutation_invariance_and_determinism(pd):
     assert torch.equal(a, c), "a physical block permutation must not change the result"
 
 
+def test_tensor_memory_kernel_determinism_and_permutation(pd):
+    """The e4m3 units of 9..32 rows (tcgen05 kernel): run twice bitwise equal,
+    and unchanged by a physical permutation of the cache blocks."""
+    w = inputs.make_workload(B=3, Hq=24, Hkv=4, D=256, qlen=3, kv="fp8", seq_lens=[3000, 777, 40], seed=61,
+                             name="tc8_det")
+    for S in (0, 5):
+        a = gpu_run(pd, w, S).clone()
+        b = gpu_run(pd, w, S).clone()
+        assert torch.equal(a, b), "same inputs, same workspace: results must be bitwise equal"
+        pool = w.k_cache.shape[0]
+        perm = torch.randperm(pool, generator=torch.Generator().manual_seed(4))
+        inv = torch.empty_like(perm)
+        inv[perm] = torch.arange(pool)
+        w2 = inputs.Workload(**{**w.__dict__})
+        w2.k_cache = w.k_cache[perm].contiguous()
+        w2.v_cache = w.v_cache[perm].contiguous()
+        t = w.block_table.clone()
+        ok = t >= 0
+        t[ok] = inv[t[ok].long()].to(torch.int32)
+        w2.block_table = t
+        assert torch.equal(a, gpu_run(pd, w2, S)), "a physical block permutation must not change the result"
+        check(w, a, ref_run(w))
+
+
+@pytest.mark.parametrize("S", [0, 3])
+def test_tensor_memory_kernel_graph_replay(pd, S):
+    """The tcgen05 e4m3 kernel captured once into a CUDA graph replays
+    correctly on new inputs written into the same buffers."""
+    shape = dict(B=3, Hq=16, Hkv=2, D=128, qlen=2, kv="fp8", pool_blocks=700, max_blocks_per_seq=300)
+    w1 = inputs.make_workload(seq_lens=[4000, 33, 1500], seed=71, **shape)
+    w2 = inputs.make_workload(seq_lens=[129, 4700, 0], seed=72, **shape)
+    q, bt, sl = w1.q.to(DEV), w1.block_table.to(DEV), w1.seq_lens.to(DEV)
+    k, v = kv_on_device(w1)
+    out = torch.empty_like(q)
+    dims = pd.dims_of(q, k, bt, 2, None)
+    ws = torch.empty(max(pd.workspace_bytes(dims, 2, S), 1), dtype=torch.uint8, device=DEV)
+    kw = dict(k_scale=w1.k_scale, v_scale=w1.v_scale, out=out, workspace=ws)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        pd.decode_paged(q, k, v, bt, sl, w1.scale, 0, 2, S, **kw)  # warm up
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        pd.decode_paged(q, k, v, bt, sl, w1.scale, 0, 2, S, **kw)
+    for w in (w1, w2):
+        # the scales are arguments of the captured call (w1's): the codes of w2
+        # are read with them, and the reference does the same
+        q.copy_(w.q.to(DEV)); bt.copy_(w.block_table.to(DEV)); sl.copy_(w.seq_lens.to(DEV))
+        k2, v2 = kv_on_device(w)
+        k.copy_(k2); v.copy_(v2)
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        wref = inputs.Workload(**{**w.__dict__})
+        wref.k_scale, wref.v_scale = w1.k_scale, w1.v_scale
+        check(w, out, ref_run(wref))
+
+
+def test_tensor_memory_kernel_long_pieces(pd):
+    """Long sequences through the tcgen05 kernel: many 128-key blocks per
+    piece, windows that start inside blocks, a sequence shorter than qlen."""
+    w = inputs.make_workload(B=3, Hq=12, Hkv=1, D=256, qlen=2, kv="fp8", window=5000,
+                             seq_lens=[20000, 1, 7777], seed=81, name="tc8_long")
+    ref = ref_run(w)
+    for S in (0, 1, 2, 9):
+        check(w, gpu_run(pd, w, S), ref)
+
+
 def test_device_errors_are_flagged_not_trapped(pd):
     w = inputs.make_workload(B=2, Hq=8, Hkv=2, D=128, seq_lens=[100, 50], seed=9)
     flag = torch.zeros(1, dtype=torch.int32, device=DEV)
