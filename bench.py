@@ -592,6 +592,18 @@ def main():
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
     peak, peak_kind = measured_peaks()
 
+    if args.workload and args.workload.startswith("kv_writer_"):
+        for name, wwl in writer_workloads(device, l2, 7000):
+            if name != args.workload:
+                continue
+            ms = time_writer(wwl, args.steps, args.warmup, device, world)
+            per = ms / args.steps
+            if rank == 0:
+                print(json.dumps({"workload": name, "us_per_call": round(per * 1e3, 3),
+                                  "hbm_gbs": round(wwl.bytes / (per * 1e-3) / 1e9, 1),
+                                  "bytes": wwl.bytes, "steps": args.steps}), flush=True)
+            return
+        raise SystemExit(f"unknown workload {args.workload}")
     if args.workload:
         cands = [(f"gqa6_d256_L{SEQ_LEN}_b{B}", (lambda B=B: gqa6_workload(B, device, l2, 1000 + B)), 0)
                  for B in SWEEP_B]
