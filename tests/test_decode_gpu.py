@@ -148,6 +148,10 @@ EDGE = [
     ("int8_d128_rows_24_window", dict(B=2, Hq=8, Hkv=1, D=128, kv="int8", qlen=3, window=300,
                                       seq_lens=[1500, 40])),
     ("int8_d256_rows_32", dict(B=2, Hq=8, Hkv=1, D=256, kv="int8", qlen=4, seq_lens=[700, 90])),
+    # int8 with two and three row tiles per head (the latter windowed)
+    ("int8_d256_rows_12", dict(B=3, Hq=12, Hkv=2, D=256, kv="int8", qlen=2, seq_lens=[5, 1000, 64])),
+    ("int8_d256_rows_18_window", dict(B=3, Hq=24, Hkv=4, D=256, kv="int8", qlen=3, window=100,
+                                      seq_lens=[2, 333, 1029])),
     # per-head tiles with two key groups over long rings (Hkv not a multiple of 4)
     ("fp8_d128_per_head_kg2", dict(B=4, Hq=16, Hkv=2, D=128, kv="fp8",
                                    seq_lens=[5000, 3001, 17, 4096])),
@@ -183,6 +187,7 @@ STALE = [
     ("fp8_d128_rows_24", dict(B=2, Hq=8, Hkv=1, D=128, kv="fp8", qlen=3, seq_lens=[5, 301])),
     ("fp8_d256_rows_18", dict(B=3, Hq=24, Hkv=4, D=256, kv="fp8", qlen=3, seq_lens=[3, 4001, 250])),
     ("int8_rows_32", dict(B=2, Hq=8, Hkv=1, D=256, kv="int8", qlen=4, seq_lens=[700, 91])),
+    ("int8_rows_18", dict(B=3, Hq=24, Hkv=4, D=256, kv="int8", qlen=3, seq_lens=[3, 4001, 250])),
 ]
 
 
@@ -388,8 +393,9 @@ def test_device_errors_are_flagged_not_trapped(pd):
 
 
 @pytest.mark.parametrize("shape", [dict(B=4, Hq=24, Hkv=4, D=256, qlen=1),
-                                   dict(B=3, Hq=24, Hkv=4, D=256, qlen=3, kv="fp8")],
-                         ids=["rows_6", "rows_18_pairs"])
+                                   dict(B=3, Hq=24, Hkv=4, D=256, qlen=3, kv="fp8"),
+                                   dict(B=3, Hq=24, Hkv=4, D=256, qlen=3, kv="int8")],
+                         ids=["rows_6", "rows_18_pairs", "rows_18_int8"])
 def test_wait_that_nothing_completes_times_out_cleanly(pd, shape):
     """Failure detection without a GPU fault: with loads suppressed the ring's
     barriers never complete, every wait runs out after a short limit, the call
