@@ -496,15 +496,16 @@ def time_e2e(B, steps, warmup, device, seed, world):
     return s.elapsed_time(e), h2d, d2h
 
 
-def cpu_oracle_rate(B, budget_s=10.0, seed=777, max_seqs=None):
-    """Time the fp64 oracle on the host cores over whole sequences of the
-    workload; returns (GB/s of KV, cores, sample description, seconds/step)."""
+def cpu_oracle_rate(B, budget_s=10.0, seed=777, max_seqs=None, threads=None):
+    """Time the fp64 oracle on the host cores (all of them, or `threads`) over
+    whole sequences of the workload; returns (GB/s of KV, cores, sample
+    description, seconds/step)."""
     import oracle
     n = B if max_seqs is None else min(B, max_seqs)
     w = inputs.gqa_d256(n, seed=seed)
     args = (w.q.numpy(), w.k_cache.numpy(), w.v_cache.numpy(), w.block_table.numpy(),
             w.seq_lens.numpy(), w.scale)
-    cores = oracle.default_threads()
+    cores = threads or oracle.default_threads()
     oracle.decode_paged(*args, threads=cores)  # warm (builds if needed)
     t0 = time.perf_counter()
     reps = 0
@@ -680,8 +681,10 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu:
         rate, cores, sample, _ = cpu_oracle_rate(HEADLINE_B, budget_s=10.0, max_seqs=4)
+        rate1, _, sample1, _ = cpu_oracle_rate(HEADLINE_B, budget_s=5.0, max_seqs=1, threads=1)
         cpu = {"value": round(rate, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": sample + " (D=256 GQA 6:1, L=4096)"}
+               "sample": sample + " (D=256 GQA 6:1, L=4096)",
+               "one_core": {"value": round(rate1, 4), "unit": UNIT, "sample": sample1}}
     traffic = traffic_per_launch()
     if rank == 0:
         line = {
