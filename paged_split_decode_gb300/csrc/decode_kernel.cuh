@@ -613,9 +613,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
       for (int mt = 0; mt < MTW; ++mt) o[mt][n][0] = o[mt][n][1] = o[mt][n][2] = o[mt][n][3] = 0.f;
     }
 
-    // ---- this key group's tiles of the piece: k % KG == kg (piece-local, so
-    // the split of a piece over the key groups does not depend on the ring)
-    for (int k = kg; k < pc.ntiles; k += KG) {
+    // ---- this key group's tiles of the piece: those whose ring sequence
+    // number q + k is kg modulo KG. The assignment follows the ring, not the
+    // piece: with a piece-local one, a piece whose length is not a multiple of
+    // KG hands the following stages to the other group, and a group that
+    // skips a stage's phase could pass its next wait there on a phase two
+    // rounds old while that stage's load is still in flight.
+    for (int k = (kg - static_cast<int>(q % KG) + KG) % KG; k < pc.ntiles; k += KG) {
       const uint32_t qq = q + k;
       const int stage = qq % NS;
       if (ok) ok = mbar_wait(full0 + 8 * stage, (qq / NS) & 1, p.timeout_ns);
@@ -695,7 +699,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
       if constexpr (DS > 1) {
         // sum the group's partial scores in part order (every warp of the group
         // evaluates the same expression, so all hold identical scores)
-        float* grp = xchg + (pair * 2 + (qq & 1)) * DS * Cfg::kXchgFloats + lane * 4 * NTW;
+        // (double-buffered by the group's own tile count, so that a fast warp's
+        // next tile never writes the buffer its partner is still reading)
+        float* grp = xchg + (pair * 2 + ((qq / KG) & 1)) * DS * Cfg::kXchgFloats + lane * 4 * NTW;
 #pragma unroll
         for (int n = 0; n < NTW; ++n)
           *reinterpret_cast<float4*>(grp + dh * Cfg::kXchgFloats + 4 * n) =
