@@ -386,3 +386,49 @@ def test_tensor_memory_kernel_protocol_is_safe(NBK, NBV):
 def test_tensor_memory_kernel_planted_mistakes_are_caught(mutate):
     msg = find_violation(lambda rng: tc8_case(rng, 2, 3, mutate), range(400))
     assert msg is not None
+
+
+# ---------------------------------------------------------------------------
+# The D-split score exchange of the mma.sync kernel: the DS warps of a pair
+# split D; for each of the key group's tiles each warp writes its partial
+# scores to its part of buffer (t / KG) % 2 (t = the tile's ring sequence
+# number), meets its partners at a named barrier, and reads every part.
+# mutate="parity_index" restates an earlier buffer index, t % 2, which does
+# not alternate when KG is even.
+
+def exchange_roles(DS, KG, kg, ntiles, mutate=None):
+    tiles = [t for t in range(ntiles) if t % KG == kg]
+    part = [[None] * DS, [None] * DS]
+    reading = [0, 0]
+    arrived = {"n": 0}
+
+    def warp(dh):
+        for i, t in enumerate(tiles):
+            buf = t % 2 if mutate == "parity_index" else (t // KG) % 2
+            if reading[buf]:
+                raise Violation(f"part {dh} of tile {t} written while buffer {buf} is read")
+            part[buf][dh] = t
+            arrived["n"] += 1
+            yield (lambda target=DS * (i + 1): arrived["n"] >= target)
+            if part[buf] != [t] * DS:
+                raise Violation(f"tile {t}: buffer {buf} holds {part[buf]}")
+            reading[buf] += 1
+            yield always
+            if part[buf] != [t] * DS:
+                raise Violation(f"buffer {buf} changed under tile {t}")
+            reading[buf] -= 1
+
+    return {f"warp{dh}": warp(dh) for dh in range(DS)}
+
+
+@pytest.mark.parametrize("DS,KG", [(2, 1), (4, 1), (2, 2), (2, 3), (4, 2)])
+def test_score_exchange_is_safe(DS, KG):
+    for seed in range(200):
+        rng = random.Random(seed)
+        for kg in range(KG):
+            run(exchange_roles(DS, KG, kg, 40), rng)
+
+
+def test_score_exchange_indexed_by_tile_parity_fails_for_two_groups():
+    msg = find_violation(lambda rng: exchange_roles(2, 2, 1, 40, "parity_index"), range(200))
+    assert msg is not None
