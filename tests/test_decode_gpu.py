@@ -144,6 +144,12 @@ EDGE = [
     ("fp8_d128_rows_24", dict(B=3, Hq=8, Hkv=1, D=128, kv="fp8", qlen=3, seq_lens=[5, 300, 1500])),
     ("fp8_d256_rows_6", dict(B=2, Hq=24, Hkv=4, D=256, kv="fp8", seq_lens=[4000, 17])),
     ("many_sequences", dict(B=300, Hq=8, Hkv=2, D=128, seq_lens=list(range(0, 3000, 10)))),
+    # more sequences than the balanced split's shared-memory prefix holds
+    # (1024): the automatic split falls back to one piece per unit
+    ("beyond_balanced_split_batch", dict(B=1100, Hq=8, Hkv=2, D=128,
+                                         seq_lens=[(17 * i) % 211 for i in range(1100)])),
+    ("beyond_balanced_split_batch_fp8_verify", dict(B=1030, Hq=24, Hkv=4, D=256, kv="fp8", qlen=3,
+                                                    seq_lens=[(13 * i) % 97 for i in range(1030)])),
     ("int8_d256_rows_6", dict(B=3, Hq=24, Hkv=4, D=256, kv="int8", seq_lens=[4000, 17, 0])),
     ("int8_d128_rows_24_window", dict(B=2, Hq=8, Hkv=1, D=128, kv="int8", qlen=3, window=300,
                                       seq_lens=[1500, 40])),
