@@ -72,6 +72,9 @@ CASES = [
                        seq_lens=[900, 64, 3000, 3])),
     ("mha_many", dict(qlens=[(i % 4) for i in range(40)], Hq=4, Hkv=4, D=128,
                       seq_lens=[17 * i + 1 for i in range(40)])),
+    # more sequences than the balanced split's prefix holds (1024)
+    ("beyond_balanced_split_batch", dict(qlens=[(i % 3) + 1 for i in range(1050)], Hq=8, Hkv=2, D=128,
+                                         seq_lens=[(11 * i) % 151 + 3 for i in range(1050)])),
 ]
 
 
