@@ -176,11 +176,12 @@ struct Cfg {
   static constexpr int kXchgFloats = 32 * 4 * NTW;       // one warp's partial S^T, lane-major
   static constexpr int kXchgBytes = DS > 1 ? HG * KG * RG * 2 * DS * kXchgFloats * 4 : 0;
   static_assert(HG == 1 || HG == 2 || HG == 4, "1, 2 or 4 heads per tile");
-  // Key group kg takes the ring's tiles kg, kg+KG, ... With NS a multiple of
-  // KG every use of a stage belongs to the same key group, which consumes its
-  // tiles in order; so when it waits on a stage's full barrier, the stage's
-  // previous phase is its own, already consumed, and a parity wait can never
-  // be satisfied by a phase that is one round old.
+  // Key group kg takes the tiles whose ring sequence number is kg modulo KG
+  // (across pieces, not within each). With NS a multiple of KG every use of a
+  // stage belongs to the same key group, which consumes its tiles in order;
+  // so when it waits on a stage's full barrier, the stage's previous phase is
+  // its own, already consumed, and a parity wait can never be satisfied by a
+  // phase two rounds old.
   static_assert(NS % KG == 0, "ring stages must be a multiple of the key groups");
   static_assert(HG * KG * RG <= 14, "named barriers 2.. cover every D group");
   static_assert(DS == 1 || DS == 2 || DS == 4, "D splits into 1, 2 or 4 parts");
