@@ -148,7 +148,11 @@ def _as_bits(a, dtype):
 
 
 def _kv_kind(kv_fp8, kv_int8, bf16):
-    return 3 if bf16 else (2 if kv_int8 else int(bool(kv_fp8)))
+    """0 fp16, 1 e4m3fn, 2 int8 caches with fp16 q; with bf16: 3 bfloat16
+    caches, 4 e4m3fn and 5 int8 caches, q (and new tokens) in bfloat16."""
+    if bf16:
+        return 4 if kv_fp8 else (5 if kv_int8 else 3)
+    return 2 if kv_int8 else int(bool(kv_fp8))
 
 
 def _prepare(q, k_cache, v_cache, block_table, seq_lens, qlen, k_scale, v_scale, kv_fp8,
@@ -190,8 +194,9 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, ql
 
     q: fp16 [B*qlen, Hq, D]; caches: fp16 (or uint8 e4m3fn codes with
     kv_fp8=True, or int8 codes as uint8 with kv_int8=True)
-    [num_blocks, block_size, Hkv, D]; with bf16=True q and both caches hold
-    bfloat16 bit patterns (uint16). block_table int32 [B, max_blocks];
+    [num_blocks, block_size, Hkv, D]; with bf16=True q holds bfloat16 bit
+    patterns (uint16), over byte caches as given or else over caches of
+    bfloat16 bit patterns. block_table int32 [B, max_blocks];
     seq_lens int32 [B]. ``rows`` = (begin, end) restricts the computed output
     rows (flattened (token, head) index); the others stay 0.
     """
@@ -271,8 +276,8 @@ def write_kv_cache(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale=1.0, v_
                    kv_fp8=False, kv_int8=False, allow_bad_slots=False, bf16=False):
     """Paged KV-cache writer, in place on the numpy caches.
 
-    k_new/v_new: fp16 [T, Hkv, D] (bfloat16 bits with bf16=True, written to
-    bfloat16 caches as they are); slot_mapping: int64 [T] (negative = padding
+    k_new/v_new: fp16 [T, Hkv, D] (bfloat16 bits with bf16=True: written to
+    bfloat16 caches as they are, quantised into byte caches); slot_mapping: int64 [T] (negative = padding
     token, skipped); caches [num_blocks, block_size, Hkv, D] fp16, or uint8
     holding e4m3fn codes (kv_fp8) or int8 codes (kv_int8). A slot beyond the
     cache raises ValueError, or with ``allow_bad_slots`` is skipped and the

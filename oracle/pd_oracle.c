@@ -34,8 +34,9 @@
  *     fp8 and int8 decode wrappers share the body);
  *   - a row with no visible key is all zeros;
  *   - bfloat16 (not on the pages): a bfloat16 model keeps q and both caches
- *     in bfloat16 (kv_kind 3); every value is still converted to fp64
- *     exactly and the arithmetic is the same.
+ *     in bfloat16 (kv_kind 3), or q in bfloat16 over e4m3fn or int8 caches
+ *     (kv_kind 4 and 5); every value is still converted to fp64 exactly and
+ *     the arithmetic is the same.
  *
  * Every value is converted to fp64 exactly and all arithmetic is fp64, in
  * key order, with no blocking beyond what each function states.
@@ -55,7 +56,8 @@ typedef struct {
   int B, qlen, Hq, Hkv, D;
   int block_size, num_blocks, max_blocks_per_seq;
   int kv_kind;      /* 0: IEEE binary16 bit patterns; 1: e4m3fn bytes; 2: int8 codes;
-                       3: bfloat16 bit patterns (q is then bfloat16 as well) */
+                       3: bfloat16 bit patterns (q is then bfloat16 as well);
+                       4, 5: e4m3fn bytes, int8 codes with bfloat16 q */
   double k_scale;   /* fp8 / int8: value = decode(code) * k_scale */
   double v_scale;
 } pdo_dims;
@@ -114,16 +116,17 @@ double pdo_i8_to_f64(uint8_t c) { return (double)(int8_t)c; }
 static double cache_at(const pdo_dims* d, const void* cache, double fp8_scale, long blk,
                        int slot, int kh, int x) {
   long idx = ((blk * d->block_size + slot) * (long)d->Hkv + kh) * d->D + x;
-  if (d->kv_kind == 1) return pdo_e4m3fn_to_f64(((const uint8_t*)cache)[idx]) * fp8_scale;
-  if (d->kv_kind == 2) return pdo_i8_to_f64(((const uint8_t*)cache)[idx]) * fp8_scale;
+  if (d->kv_kind == 1 || d->kv_kind == 4)
+    return pdo_e4m3fn_to_f64(((const uint8_t*)cache)[idx]) * fp8_scale;
+  if (d->kv_kind == 2 || d->kv_kind == 5) return pdo_i8_to_f64(((const uint8_t*)cache)[idx]) * fp8_scale;
   if (d->kv_kind == 3) return pdo_bf16_to_f64(((const uint16_t*)cache)[idx]);
   return pdo_f16_to_f64(((const uint16_t*)cache)[idx]);
 }
 
-/* Element x of a query row (fp16, or bfloat16 with bfloat16 caches). */
+/* Element x of a query row (fp16, or bfloat16 for kv_kind 3, 4 and 5). */
 static double q_at(const pdo_dims* d, const uint16_t* q, long rho, int x) {
   uint16_t bits = q[rho * d->D + x];
-  return d->kv_kind == 3 ? pdo_bf16_to_f64(bits) : pdo_f16_to_f64(bits);
+  return d->kv_kind >= 3 ? pdo_bf16_to_f64(bits) : pdo_f16_to_f64(bits);
 }
 
 /* Visible key range [*lo, *hi] of query token i of a sequence of length L.
@@ -405,7 +408,7 @@ int8_t pdo_i8_encode(float t) {
 int pdo_write_kv_cache(const pdo_dims* d, const uint16_t* k_new, const uint16_t* v_new,
                        const int64_t* slot_mapping, long T, void* k_cache, void* v_cache) {
   if (!d || T < 0 || d->Hkv < 1 || d->D < 1 || d->block_size < 1 || d->num_blocks < 0 ||
-      d->kv_kind < 0 || d->kv_kind > 3)
+      d->kv_kind < 0 || d->kv_kind > 5)
     return PDO_ERR_ARGS;
   const long row = (long)d->Hkv * d->D;
   const int64_t cap = (int64_t)d->num_blocks * d->block_size;
@@ -423,9 +426,11 @@ int pdo_write_kv_cache(const pdo_dims* d, const uint16_t* k_new, const uint16_t*
         ((uint16_t*)k_cache)[dst + e] = kx;
         ((uint16_t*)v_cache)[dst + e] = vx;
       } else {
-        float kq = (float)pdo_f16_to_f64(kx) / ks;
-        float vq = (float)pdo_f16_to_f64(vx) / vs;
-        if (d->kv_kind == 1) {
+        /* new tokens in fp16, or bfloat16 for the bfloat16-q kinds 4 and 5 */
+        const int b16 = d->kv_kind >= 4;
+        float kq = (float)(b16 ? pdo_bf16_to_f64(kx) : pdo_f16_to_f64(kx)) / ks;
+        float vq = (float)(b16 ? pdo_bf16_to_f64(vx) : pdo_f16_to_f64(vx)) / vs;
+        if (d->kv_kind == 1 || d->kv_kind == 4) {
           ((uint8_t*)k_cache)[dst + e] = pdo_e4m3fn_encode(kq);
           ((uint8_t*)v_cache)[dst + e] = pdo_e4m3fn_encode(vq);
         } else {

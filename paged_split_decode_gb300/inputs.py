@@ -54,7 +54,7 @@ class Workload:
     num_splits: int = 0
     kv_fp8: bool = False
     kv_int8: bool = False
-    bf16: bool = False         # q, caches (and the output) in bfloat16
+    bf16: bool = False         # q and the output in bfloat16 (the caches too, unless byte codes)
     k_scale: float = 1.0
     v_scale: float = 1.0
     meta: dict = field(default_factory=dict)
@@ -132,16 +132,21 @@ def make_block_table(gen, seq_lens, max_blocks_per_seq, layout="permuted", pool_
 def make_workload(*, B, Hq, Hkv, D, seq_lens, qlen=1, block_size=BLOCK_SIZE, layout="permuted",
                   window=0, kv="f16", seed=0, scale=None, num_splits=0, max_blocks_per_seq=None,
                   pool_blocks=None, name="custom", stale="drawn") -> Workload:
-    """``stale="nan"`` overwrites, in each sequence's last block, the slots past
-    its last key with NaN bit patterns (the unwritten tail of a block may hold
-    anything); int8 codes have no NaN, so they get -128 there."""
+    """``kv``: "f16", "bf16", "fp8", "int8", or "fp8_bf16q" / "int8_bf16q"
+    (byte caches under a bfloat16 q). ``stale="nan"`` overwrites, in each
+    sequence's last block, the slots past its last key with NaN bit patterns
+    (the unwritten tail of a block may hold anything); int8 codes have no NaN,
+    so they get -128 there."""
+    kv_name = kv
+    bq = kv in ("bf16", "fp8_bf16q", "int8_bf16q")
+    kv = {"fp8_bf16q": "fp8", "int8_bf16q": "int8"}.get(kv, kv)
     gen = torch.Generator().manual_seed(int(seed))
     seq_lens = [int(x) for x in seq_lens]
     if max_blocks_per_seq is None:
         max_blocks_per_seq = max([blocks_needed(L, block_size) for L in seq_lens] + [1])
     table, pool = make_block_table(gen, seq_lens, max_blocks_per_seq, layout, pool_blocks, block_size)
     qf = _normal(gen, (B * qlen, Hq, D))
-    q = qf.to(torch.bfloat16) if kv == "bf16" else qf.to(torch.float16)
+    q = qf.to(torch.bfloat16) if bq else qf.to(torch.float16)
     kf = _normal(gen, (pool, block_size, Hkv, D))
     vf = _normal(gen, (pool, block_size, Hkv, D))
     kv_fp8 = kv_int8 = False
@@ -181,9 +186,9 @@ def make_workload(*, B, Hq, Hkv, D, seq_lens, qlen=1, block_size=BLOCK_SIZE, lay
                     seq_lens=torch.tensor(seq_lens, dtype=torch.int32),
                     scale=float(scale if scale is not None else 1.0 / math.sqrt(D)),
                     window=int(window), qlen=int(qlen), num_splits=int(num_splits), kv_fp8=kv_fp8,
-                    kv_int8=kv_int8, bf16=kv == "bf16",
+                    kv_int8=kv_int8, bf16=bq,
                     k_scale=k_scale, v_scale=v_scale,
-                    meta=dict(layout=layout, seed=int(seed), kv=kv))
+                    meta=dict(layout=layout, seed=int(seed), kv=kv_name))
 
 
 def make_varlen_workload(*, qlens, seed=0, name="varlen", **kw) -> Workload:

@@ -17,13 +17,14 @@ def _bf16_to_f64(x):
 
 
 def decode_cache(cache, fp8, scale, int8=False, bf16=False):
-    if bf16:
-        return _bf16_to_f64(cache)
+    """Byte codes (with a bfloat16 q or not), else bfloat16 or fp16 values."""
     if int8:
         return np.ascontiguousarray(cache).view(np.int8).astype(np.float64) * float(scale)
     if fp8:
         t = torch.from_numpy(np.ascontiguousarray(cache)).view(torch.float8_e4m3fn)
         return t.to(torch.float64).numpy() * float(scale)
+    if bf16:
+        return _bf16_to_f64(cache)
     return np.asarray(cache).astype(np.float16).astype(np.float64)
 
 

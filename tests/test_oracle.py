@@ -166,13 +166,36 @@ def _tiny(c, kv="f16", seed=7, layout="permuted", scale=None):
                                 pool_blocks=sum((L + c["bs"] - 1) // c["bs"] for L in c["lens"]) + 3)
 
 
-@pytest.mark.parametrize("kv", ["f16", "fp8", "int8", "bf16"])
+KV_KINDS = ["f16", "fp8", "int8", "bf16", "fp8_bf16q", "int8_bf16q"]
+
+
+@pytest.mark.parametrize("kv", KV_KINDS)
 @pytest.mark.parametrize("ci", range(len(TINY)))
 def test_oracle_matches_dense_bruteforce(oracle_lib, ci, kv):
     w = _tiny(TINY[ci], kv=kv, seed=100 + ci)
     got = run_oracle(oracle_lib, w)
     want = run_dense(w)
     assert np.max(np.abs(got - want)) <= 1e-12
+
+
+@pytest.mark.parametrize("kv", ["fp8", "int8"])
+@pytest.mark.parametrize("ci", [1, 4, 5])
+def test_bf16_q_over_byte_caches_equals_f16_q(oracle_lib, ci, kv):
+    """A q whose values are exact in both fp16 and bfloat16 gives the same
+    fp64 output, bit for bit, over the same byte caches whichever type it
+    arrives in."""
+    w = _tiny(TINY[ci], kv=kv, seed=300 + ci)
+    g = torch.Generator().manual_seed(ci)
+    # 8 significant bits and a modest exponent: exact in both types
+    qv = (torch.randint(-255, 256, w.q.shape, generator=g).to(torch.float64) *
+          torch.pow(2.0, torch.randint(-9, -3, w.q.shape, generator=g).to(torch.float64)))
+    w.q = qv.to(torch.float16)
+    assert torch.equal(w.q.to(torch.float64), qv)
+    f16 = run_oracle(oracle_lib, w)
+    w.q, w.bf16 = qv.to(torch.bfloat16), True
+    assert torch.equal(w.q.to(torch.float64), qv)
+    b16 = run_oracle(oracle_lib, w)
+    assert np.array_equal(f16, b16)
 
 
 @pytest.mark.parametrize("kv", ["f16", "bf16"])

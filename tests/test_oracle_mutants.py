@@ -32,8 +32,8 @@ MUTANTS = [
      "double pdo_i8_to_f64(uint8_t c) { return (double)c; }"),
     ("split_chunk_bound", "if (cb1 > first_block + n_blocks) cb1 = first_block + n_blocks;",
      "if (cb1 > first_block + n_blocks - 1) cb1 = first_block + n_blocks - 1;"),
-    ("writer_scale_multiplies", "float kq = (float)pdo_f16_to_f64(kx) / ks;",
-     "float kq = (float)pdo_f16_to_f64(kx) * ks;"),
+    ("writer_scale_multiplies", "float kq = (float)(b16 ? pdo_bf16_to_f64(kx) : pdo_f16_to_f64(kx)) / ks;",
+     "float kq = (float)(b16 ? pdo_bf16_to_f64(kx) : pdo_f16_to_f64(kx)) * ks;"),
     ("e4m3_ties_away", "if (d < best_d || (d == best_d && (c & 1) == 0)) {",
      "if (d <= best_d) {"),
     ("i8_ties_up", "r = (fmod(f, 2.0) == 0.0) ? f : f + 1.0;", "r = f + 1.0;"),
@@ -42,8 +42,11 @@ MUTANTS = [
      "long dst = (off * d->num_blocks + blk) * row;"),
     ("writer_padding_written", "if (slot < 0) continue;", "if (slot < 0) slot = -slot;"),
     ("bf16_exponent_bias", "v = ldexp((double)(128 + f), e - 134);", "v = ldexp((double)(128 + f), e - 133);"),
-    ("bf16_q_read_as_f16", "return d->kv_kind == 3 ? pdo_bf16_to_f64(bits) : pdo_f16_to_f64(bits);",
+    ("bf16_q_read_as_f16", "return d->kv_kind >= 3 ? pdo_bf16_to_f64(bits) : pdo_f16_to_f64(bits);",
      "return pdo_f16_to_f64(bits);"),
+    ("bf16q_e4m3_cache_read_as_f16", "if (d->kv_kind == 1 || d->kv_kind == 4)\n",
+     "if (d->kv_kind == 1)\n"),
+    ("writer_bf16_tokens_read_as_f16", "const int b16 = d->kv_kind >= 4;", "const int b16 = 0;"),
 ]
 
 
@@ -71,7 +74,7 @@ def _pin_calls():
              (pins.test_bf16_decoder_every_pattern, {})]
     calls += [(pins.test_golden_closed_forms, {"case": c}) for c in cases]
     calls += [(pins.test_oracle_matches_dense_bruteforce, {"ci": ci, "kv": kv})
-              for ci in range(len(pins.TINY)) for kv in ("f16", "fp8", "int8", "bf16")]
+              for ci in range(len(pins.TINY)) for kv in pins.KV_KINDS]
     calls += [(pins.test_split_mode_matches_one_shot, {"ci": ci, "kv": "f16"}) for ci in (2, 5)]
     calls += [(pins.test_combine_edge_cases, {}), (pins.test_split_partials_recombine, {})]
     calls += [(writer_pins.test_e4m3fn_encoder_golden_points, {}),

@@ -87,13 +87,27 @@ def test_i8_encoder_matches_numpy(oracle_lib):
 
 # ---- writer ------------------------------------------------------------------
 
-KINDS = ("f16", "fp8", "int8")
+# byte caches take fp16 new tokens, or bfloat16 ones under a bfloat16 model
+KINDS = ("f16", "fp8", "int8", "fp8_bf16q", "int8_bf16q")
+
+
+def _bf16_bits(x):
+    return torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _tokens_f32(x, kind):
+    """The new tokens' values (fp16 arrays, or bfloat16 bit patterns)."""
+    if kind.endswith("bf16q"):
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float32).numpy()
+    return x.astype(np.float32)
 
 
 def _writer_case(kind, seed=0, T=37, num_blocks=11, bs=16, Hkv=3, D=40):
     g = np.random.default_rng(seed)
     k_new = (g.standard_normal((T, Hkv, D)) * 2).astype(np.float16)
     v_new = (g.standard_normal((T, Hkv, D)) * 3).astype(np.float16)
+    if kind.endswith("bf16q"):
+        k_new, v_new = _bf16_bits(k_new), _bf16_bits(v_new)
     slots = g.permutation(num_blocks * bs)[:T].astype(np.int64)
     slots[::7] = -1  # padding tokens
     if kind == "f16":
@@ -105,12 +119,13 @@ def _writer_case(kind, seed=0, T=37, num_blocks=11, bs=16, Hkv=3, D=40):
 
 
 def _flags(kind):
-    return dict(kv_fp8=kind == "fp8", kv_int8=kind == "int8")
+    return dict(kv_fp8=kind.startswith("fp8"), kv_int8=kind.startswith("int8"),
+                bf16=kind.endswith("bf16q"))
 
 
 def _quantise_lib(x, scale, kind):
-    t = torch.from_numpy(x.astype(np.float32)) / torch.tensor(np.float32(scale))
-    if kind == "fp8":
+    t = torch.from_numpy(_tokens_f32(x, kind)) / torch.tensor(np.float32(scale))
+    if kind.startswith("fp8"):
         return t.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     return np.clip(np.rint(t.numpy().astype(np.float64)), -127, 127).astype(np.int8).view(np.uint8)
 
