@@ -72,8 +72,12 @@ typedef enum {
   PD_KV_F16 = 0,       /* K and V caches hold IEEE binary16 */
   PD_KV_FP8_E4M3 = 1,  /* K and V caches hold OCP e4m3fn codes; value = decode(code) * scale */
   PD_KV_INT8 = 2,      /* K and V caches hold int8 two's-complement codes; value = code * scale */
-  PD_KV_BF16 = 3       /* K and V caches, q and out hold bfloat16 (scales ignored); the products
+  PD_KV_BF16 = 3,      /* K and V caches, q and out hold bfloat16 (scales ignored); the products
                           run on bfloat16 tensor-core operands (P rounded to bfloat16) */
+  PD_KV_FP8_E4M3_BF16 = 4, /* e4m3fn caches as PD_KV_FP8_E4M3, q and out (and the writer's new
+                              tokens) in bfloat16: each q row is scaled by a power of two into
+                              fp16 exactly and the products run as for an fp16 q */
+  PD_KV_INT8_BF16 = 5  /* int8 caches as PD_KV_INT8, q and out (and new tokens) in bfloat16 */
 } pd_kv_dtype;
 
 /* Bits written into *error_flag by the device. */
@@ -91,8 +95,8 @@ typedef enum {
  *   num_blocks         blocks in each of the K and V caches
  *   max_blocks_per_seq columns of block_table
  *   kv_dtype           pd_kv_dtype
- *   k_scale, v_scale   fp8 / int8: per-cache dequantisation scales (ignored for fp16 and
- *                      bfloat16) */
+ *   k_scale, v_scale   fp8 / int8 (either q type): per-cache dequantisation scales
+ *                      (ignored for fp16 and bfloat16 caches) */
 typedef struct {
   int32_t B, Hq, Hkv, D;
   int32_t block_size, num_blocks, max_blocks_per_seq;
@@ -119,9 +123,10 @@ PD_API int pd_grid_ctas(const pd_dims* dims, int qlen, int num_splits, int sm_co
  * decode kernel, then a split-combine kernel launched with programmatic
  * dependent launch that merges the partials of units cut into pieces.
  *
- *   q            fp16 [B*qlen, Hq, D] (bfloat16 with PD_KV_BF16 caches); row
- *                b*qlen + i is query token i of sequence b
- *   k_cache      [num_blocks, block_size, Hkv, D] fp16, e4m3fn or int8 (dims->kv_dtype)
+ *   q            fp16 [B*qlen, Hq, D] (bfloat16 for PD_KV_BF16, PD_KV_FP8_E4M3_BF16 and
+ *                PD_KV_INT8_BF16); row b*qlen + i is query token i of sequence b
+ *   k_cache      [num_blocks, block_size, Hkv, D] fp16, bfloat16, e4m3fn or int8
+ *                (dims->kv_dtype)
  *   v_cache      same layout and dtype as k_cache
  *   block_table  int32 [B, max_blocks_per_seq]; entry [b][n] is the physical
  *                block holding keys n*block_size .. n*block_size+block_size-1 of
@@ -185,8 +190,8 @@ PD_API pd_status decode_paged_combine(const float* part_m, const float* part_l, 
 /* Paged KV-cache writer: stores the K and V rows of new tokens where the
  * decode reads them (opengfx1030/vllm-rdna pull request #33, "Test Plan": the
  * decode is checked against the paged writer's layout).
- *   k_new, v_new  fp16 [num_tokens, Hkv, D] (bfloat16 for a PD_KV_BF16 cache),
- *                 16-byte aligned
+ *   k_new, v_new  fp16 [num_tokens, Hkv, D] (bfloat16 for PD_KV_BF16, PD_KV_FP8_E4M3_BF16
+ *                 and PD_KV_INT8_BF16), 16-byte aligned
  *   slot_mapping  int64 [num_tokens], device; token t goes to block
  *                 slot / block_size, offset slot % block_size of both caches;
  *                 a negative slot is a padding token and writes nothing

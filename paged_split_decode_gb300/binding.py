@@ -21,6 +21,9 @@ PD_KV_F16 = 0
 PD_KV_FP8_E4M3 = 1
 PD_KV_INT8 = 2
 PD_KV_BF16 = 3
+PD_KV_FP8_E4M3_BF16 = 4  # e4m3fn caches under a bfloat16 q and out
+PD_KV_INT8_BF16 = 5      # int8 caches under a bfloat16 q and out
+_BF16_IO = (PD_KV_BF16, PD_KV_FP8_E4M3_BF16, PD_KV_INT8_BF16)
 DEVERR_BLOCK_ID = 1
 DEVERR_SEQ_LEN = 2
 DEVERR_TIMEOUT = 4
@@ -107,33 +110,55 @@ def _check(code: int, what: str):
 
 
 def make_dims(B, Hq, Hkv, D, block_size, num_blocks, max_blocks_per_seq, kv_fp8=False,
-              k_scale=1.0, v_scale=1.0, kv_int8=False, kv_bf16=False) -> PdDims:
+              k_scale=1.0, v_scale=1.0, kv_int8=False, kv_bf16=False, q_bf16=False) -> PdDims:
+    """``q_bf16``: a bfloat16 q (and out, and new tokens) over fp8 / int8 caches."""
     kind = (PD_KV_BF16 if kv_bf16 else PD_KV_INT8 if kv_int8
             else PD_KV_FP8_E4M3 if kv_fp8 else PD_KV_F16)
+    if q_bf16 and kind in (PD_KV_FP8_E4M3, PD_KV_INT8):
+        kind += 3
+    elif q_bf16 and kind == PD_KV_F16:
+        raise TypeError("a bfloat16 q needs bfloat16, fp8 or int8 caches")
     return PdDims(int(B), int(Hq), int(Hkv), int(D), int(block_size), int(num_blocks),
                   int(max_blocks_per_seq), kind, float(k_scale), float(v_scale))
 
 
-def kv_kind_of(k_cache) -> int:
+def kv_kind_of(k_cache, act_dtype=None) -> int:
     """fp16 caches -> PD_KV_F16; bfloat16 -> PD_KV_BF16; torch.int8 ->
-    PD_KV_INT8; uint8 or float8_e4m3fn -> PD_KV_FP8_E4M3."""
+    PD_KV_INT8; uint8 or float8_e4m3fn -> PD_KV_FP8_E4M3; the byte kinds with
+    a bfloat16 ``act_dtype`` (q, or a writer's new tokens) -> PD_KV_INT8_BF16,
+    PD_KV_FP8_E4M3_BF16."""
     if k_cache.dtype == torch.float16:
-        return PD_KV_F16
-    if k_cache.dtype == torch.bfloat16:
-        return PD_KV_BF16
-    if k_cache.dtype == torch.int8:
-        return PD_KV_INT8
-    if k_cache.dtype in (torch.uint8, torch.float8_e4m3fn):
-        return PD_KV_FP8_E4M3
-    raise TypeError(f"unsupported KV cache dtype {k_cache.dtype}")
+        kind = PD_KV_F16
+    elif k_cache.dtype == torch.bfloat16:
+        kind = PD_KV_BF16
+    elif k_cache.dtype == torch.int8:
+        kind = PD_KV_INT8
+    elif k_cache.dtype in (torch.uint8, torch.float8_e4m3fn):
+        kind = PD_KV_FP8_E4M3
+    else:
+        raise TypeError(f"unsupported KV cache dtype {k_cache.dtype}")
+    if act_dtype == torch.bfloat16 and kind in (PD_KV_FP8_E4M3, PD_KV_INT8):
+        kind += 3
+    return kind
+
+
+def _dtypes(kind):
+    """(cache dtype(s), q / out / new-token dtype) of a kind."""
+    base = {PD_KV_FP8_E4M3_BF16: PD_KV_FP8_E4M3, PD_KV_INT8_BF16: PD_KV_INT8}.get(kind, kind)
+    kv_dt = {PD_KV_F16: torch.float16, PD_KV_INT8: torch.int8, PD_KV_BF16: torch.bfloat16,
+             PD_KV_FP8_E4M3: (torch.uint8, torch.float8_e4m3fn)}[base]
+    return kv_dt, torch.bfloat16 if kind in _BF16_IO else torch.float16
+
+
+def _dims_for(kind, B, Hq, Hkv, D, bs, num_blocks, max_blocks, k_scale, v_scale) -> PdDims:
+    return PdDims(int(B), int(Hq), int(Hkv), int(D), int(bs), int(num_blocks), int(max_blocks), int(kind),
+                  float(k_scale), float(v_scale))
 
 
 def dims_of(q, k_cache, block_table, qlen, kv_fp8=None, k_scale=1.0, v_scale=1.0) -> PdDims:
     num_blocks, bs, Hkv, D = k_cache.shape
-    kind = kv_kind_of(k_cache)
-    return make_dims(block_table.shape[0], q.shape[1], Hkv, D, bs, num_blocks,
-                     block_table.shape[1], kind == PD_KV_FP8_E4M3, k_scale, v_scale,
-                     kind == PD_KV_INT8, kind == PD_KV_BF16)
+    return _dims_for(kv_kind_of(k_cache, q.dtype), block_table.shape[0], q.shape[1], Hkv, D, bs,
+                     num_blocks, block_table.shape[1], k_scale, v_scale)
 
 
 def workspace_bytes(dims: PdDims, qlen: int, num_splits: int, sm_count: int = 0) -> int:
@@ -184,10 +209,8 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, ql
     0 = balanced.
     """
     lib = load()
-    kind = kv_kind_of(k_cache)
-    kv_dt = {PD_KV_F16: torch.float16, PD_KV_INT8: torch.int8, PD_KV_BF16: torch.bfloat16,
-             PD_KV_FP8_E4M3: (torch.uint8, torch.float8_e4m3fn)}[kind]
-    q_dt = torch.bfloat16 if kind == PD_KV_BF16 else torch.float16
+    kind = kv_kind_of(k_cache, q.dtype)
+    kv_dt, q_dt = _dtypes(kind)
     dims = dims_of(q, k_cache, block_table, qlen, None, k_scale, v_scale)
     if out is None:
         out = torch.empty_like(q)
@@ -223,10 +246,8 @@ def decode_paged_varlen(q, k_cache, v_cache, block_table, seq_lens, query_start_
     returns ``out`` (fp16 [T, Hq, D]; rows outside every sequence's range are
     left as they were)."""
     lib = load()
-    kind = kv_kind_of(k_cache)
-    kv_dt = {PD_KV_F16: torch.float16, PD_KV_INT8: torch.int8, PD_KV_BF16: torch.bfloat16,
-             PD_KV_FP8_E4M3: (torch.uint8, torch.float8_e4m3fn)}[kind]
-    q_dt = torch.bfloat16 if kind == PD_KV_BF16 else torch.float16
+    kind = kv_kind_of(k_cache, q.dtype)
+    kv_dt, q_dt = _dtypes(kind)
     dims = dims_of(q, k_cache, block_table, max_qlen, None, k_scale, v_scale)
     if out is None:
         out = torch.zeros_like(q)
@@ -278,23 +299,20 @@ def write_kv_cache(k_new, v_new, slot_mapping, k_cache, v_cache, *, k_scale=1.0,
                    error_flag=None, stream=None):
     """Store new tokens' K/V rows in the paged caches, in place.
 
-    k_new/v_new: fp16 [T, Hkv, D]; slot_mapping: int64 [T] (negative =
-    padding); caches [num_blocks, block_size, Hkv, D] fp16, uint8 /
-    float8_e4m3fn (e4m3fn codes) or int8 (codes), quantised with
-    ``k_scale``/``v_scale``."""
+    k_new/v_new: fp16 or bfloat16 [T, Hkv, D]; slot_mapping: int64 [T]
+    (negative = padding); caches [num_blocks, block_size, Hkv, D] of the
+    tokens' type, or uint8 / float8_e4m3fn (e4m3fn codes) or int8 (codes),
+    quantised with ``k_scale``/``v_scale``."""
     lib = load()
-    kind = kv_kind_of(k_cache)
-    kv_dt = {PD_KV_F16: torch.float16, PD_KV_INT8: torch.int8, PD_KV_BF16: torch.bfloat16,
-             PD_KV_FP8_E4M3: (torch.uint8, torch.float8_e4m3fn)}[kind]
-    q_dt = torch.bfloat16 if kind == PD_KV_BF16 else torch.float16
+    kind = kv_kind_of(k_cache, k_new.dtype)
+    kv_dt, q_dt = _dtypes(kind)
     if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype:
         raise ValueError("v_cache must match k_cache in shape and dtype")
     num_blocks, bs, Hkv, D = k_cache.shape
     T = slot_mapping.numel()
     if k_new.shape != (T, Hkv, D) or v_new.shape != k_new.shape:
         raise ValueError("k_new/v_new must be [T, Hkv, D] with T = len(slot_mapping)")
-    dims = make_dims(0, Hkv, Hkv, D, bs, num_blocks, 0, kind == PD_KV_FP8_E4M3, k_scale, v_scale,
-                     kind == PD_KV_INT8, kind == PD_KV_BF16)
+    dims = _dims_for(kind, 0, Hkv, Hkv, D, bs, num_blocks, 0, k_scale, v_scale)
     if stream is None:
         stream = torch.cuda.current_stream(k_cache.device).cuda_stream
     flag_ptr = None if error_flag is None else _dev_ptr(error_flag, "error_flag", (torch.int32, torch.uint32))

@@ -14,34 +14,53 @@
 
 namespace pd {
 namespace {
-constexpr int kKv = kKvFp8;
 constexpr int kD = 128;
-using C1 = CfgFor<kD, kKv, 1, 2, 2>;
-using TC = Tc8<kD>;  // two to four row tiles: the tensor-core (tcgen05) kernel
-using C1H = CfgFor<kD, kKv, 1, 1, 1, 2, 4>;
+// The shapes for caches of this kind, with an fp16 q (kKv = kKvFp8) or a
+// bfloat16 q and out (kKvFp8Bq).
+template <int kKv>
+struct Shapes {
+  using C1 = CfgFor<kD, kKv, 1, 2, 2>;
+  using TC = Tc8<kD, q_is_bf16(kKv)>;  // two to four row tiles: the tensor-core (tcgen05) kernel
+  using C1H = CfgFor<kD, kKv, 1, 1, 1, 2, 4>;
+
+  static bool shape(int nt, int grouped, KernelShape* out) {
+    if (grouped) return nt == 1 && shape_of<C1H>(out);
+    switch (nt) {
+      case 1: return shape_of<C1>(out);
+      case 2:
+      case 3:
+      case 4: return shape_tc8<TC>(nt, out);
+      default: return false;
+    }
+  }
+
+  static cudaError_t launch(int nt, int grouped, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const DecodeParams& p, int grid, cudaStream_t s) {
+    if (grouped) return nt == 1 ? launch_cfg<C1H>(tk, tv, p, grid, s) : cudaErrorInvalidValue;
+    switch (nt) {
+      case 1: return launch_cfg<C1>(tk, tv, p, grid, s);
+      case 2:
+      case 3:
+      case 4: return launch_tc8<TC>(tk, tv, p, grid, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+};
 }  // namespace
 
 bool shape_fp8_d128(int nt, int grouped, KernelShape* out) {
-  if (grouped) return nt == 1 && shape_of<C1H>(out);
-  switch (nt) {
-    case 1: return shape_of<C1>(out);
-    case 2:
-    case 3:
-    case 4: return shape_tc8<TC>(nt, out);
-    default: return false;
-  }
+  return Shapes<kKvFp8>::shape(nt, grouped, out);
 }
-
+bool shape_fp8q_d128(int nt, int grouped, KernelShape* out) {
+  return Shapes<kKvFp8Bq>::shape(nt, grouped, out);
+}
 cudaError_t launch_fp8_d128(int nt, int grouped, const CUtensorMap& tk, const CUtensorMap& tv,
-                        const DecodeParams& p, int grid, cudaStream_t s) {
-  if (grouped) return nt == 1 ? launch_cfg<C1H>(tk, tv, p, grid, s) : cudaErrorInvalidValue;
-  switch (nt) {
-    case 1: return launch_cfg<C1>(tk, tv, p, grid, s);
-    case 2:
-    case 3:
-    case 4: return launch_tc8<TC>(tk, tv, p, grid, s);
-    default: return cudaErrorInvalidValue;
-  }
+                          const DecodeParams& p, int grid, cudaStream_t s) {
+  return Shapes<kKvFp8>::launch(nt, grouped, tk, tv, p, grid, s);
+}
+cudaError_t launch_fp8q_d128(int nt, int grouped, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const DecodeParams& p, int grid, cudaStream_t s) {
+  return Shapes<kKvFp8Bq>::launch(nt, grouped, tk, tv, p, grid, s);
 }
 
 }  // namespace pd

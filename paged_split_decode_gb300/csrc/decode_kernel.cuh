@@ -85,7 +85,28 @@ struct DecodeParams {
 
 // KV element kinds: fp16, one byte per element (OCP e4m3fn or int8 codes), or
 // bfloat16 (then q and out are bfloat16 too and the products run in bfloat16).
-constexpr int kKvF16 = 0, kKvFp8 = 1, kKvInt8 = 2, kKvBf16 = 3;
+// The byte kinds also come with a bfloat16 q and out (kKvFp8Bq, kKvInt8Bq):
+// the products still run in fp16 on the exactly widened codes, with each q row
+// scaled by a power of two into fp16 (exact) and the factor taken back out of
+// the row's scores.
+constexpr int kKvF16 = 0, kKvFp8 = 1, kKvInt8 = 2, kKvBf16 = 3, kKvFp8Bq = 4, kKvInt8Bq = 5;
+
+// The cache element kind of a kind, and whether q and out are bfloat16.
+constexpr int cache_kind(int kv) { return kv == kKvFp8Bq ? kKvFp8 : kv == kKvInt8Bq ? kKvInt8 : kv; }
+constexpr bool q_is_bf16(int kv) { return kv == kKvBf16 || kv == kKvFp8Bq || kv == kKvInt8Bq; }
+
+// Row scale of a q row whose largest |value| is m (a float, >= 0): 2^e with
+// m * 2^e in [2^14, 2^15) where that keeps 2^e and 2^-e normal floats, so the
+// scaled bfloat16 values are exact fp16 values (8 significant bits, within
+// fp16's range); e = 0 for an all-zero row.
+__device__ __forceinline__ int q_row_exponent(float m) {
+  if (!(m > 0.f)) return 0;
+  const int eb = static_cast<int>((__float_as_uint(m) >> 23) & 255u);
+  return max(-113, min(126, 141 - eb));
+}
+__device__ __forceinline__ float pow2f(int e) {  // 2^e for e in [-126, 127]
+  return __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+}
 
 // Tensor-core product and output packing for the 16-bit operand type.
 template <bool BF16>
@@ -140,9 +161,11 @@ struct Cfg {
   // has its own consumer warps.
   static constexpr int HG = HG_;
   static constexpr int kMinBlocks = MINB_;              // resident CTAs per SM the plan targets
-  static constexpr int KV = KV_;
-  static constexpr bool FP8 = KV_ == kKvFp8 || KV_ == kKvInt8;  // one-byte elements
-  static constexpr bool BF16 = KV_ == kKvBf16;  // bfloat16 operands, q and out
+  static constexpr int KV = cache_kind(KV_);     // the cache's element kind
+  static constexpr bool FP8 = KV == kKvFp8 || KV == kKvInt8;  // one-byte elements
+  static constexpr bool BF16 = KV_ == kKvBf16;  // bfloat16 tensor-core operands
+  static constexpr bool QB = q_is_bf16(KV_);     // q and out in bfloat16
+  static constexpr bool kQScale = QB && !BF16;   // q rows scaled into fp16
   static constexpr int kElem = FP8 ? 1 : 2;
   static constexpr int kSlabElems = 128 / kElem;        // one 128-byte swizzle row
   static constexpr int kSlabs = D / kSlabElems;
@@ -567,6 +590,48 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
 
   while (work_next(p, s_pre, it, pc)) {
     // ---- per-piece setup: Q fragments (B operand) and per-row visible key limits
+    // bfloat16 q over byte caches: every lane takes part in each row's maximum
+    // over all of D (so the warps sharing a row agree), then keeps the exponent
+    // of row g (its q fragments) and the score factors of rows 2t4, 2t4 + 1
+    int eq[NTW];          // exponent of q row g of row tile n
+    float sl2r[NTW][2];   // score factor of rows 2t4 + c: p.sl2 / 2^e
+#pragma unroll
+    for (int n = 0; n < NTW; ++n) {
+      eq[n] = 0;
+      sl2r[n][0] = sl2r[n][1] = p.sl2;
+    }
+    if constexpr (Cfg::kQScale) {
+#pragma unroll
+      for (int n = 0; n < NTW; ++n) {
+#pragma unroll 1
+        for (int j = 0; j < 8; ++j) {
+          const int r = (rg * NTW + n) * 8 + j;
+          float m = 0.f;
+          if (r < pc.R && pc.ntiles > 0) {  // uniform over the warp
+            const int i = r / p.G, hl = r % p.G;
+            const __half* row = p.q + (static_cast<long long>(pc.q0 + i) * p.Hq + (pc.kh + th) * p.G + hl) * D;
+            constexpr int W = D / 64;  // 32-bit words (bfloat16 pairs) per lane
+            uint32_t w[W];
+            if constexpr (W == 4) {
+              const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + lane);
+              w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+            } else {
+              const uint2 v = __ldg(reinterpret_cast<const uint2*>(row) + lane);
+              w[0] = v.x; w[1] = v.y;
+            }
+#pragma unroll
+            for (int k = 0; k < W; ++k)
+              m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xffff0000u))));
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          }
+          const int e = q_row_exponent(m);
+          if (g == j) eq[n] = e;
+          if (2 * t4 == j) sl2r[n][0] = p.sl2 * pow2f(-e);
+          if (2 * t4 + 1 == j) sl2r[n][1] = p.sl2 * pow2f(-e);
+        }
+      }
+    }
 #pragma unroll
     for (int n = 0; n < NTW; ++n) {
       const int r = (rg * NTW + n) * 8 + g;
@@ -590,6 +655,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
         }
         qf[ksl][n][0] = qrow ? __ldg(reinterpret_cast<const uint32_t*>(qrow + d0)) : 0u;
         qf[ksl][n][1] = qrow ? __ldg(reinterpret_cast<const uint32_t*>(qrow + d1)) : 0u;
+        if constexpr (Cfg::kQScale) {  // bfloat16 pair * 2^e -> fp16 pair, exact
+          const float up = pow2f(eq[n]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t w = qf[ksl][n][h];
+            qf[ksl][n][h] = pack_half2(__uint_as_float(w << 16) * up, __uint_as_float(w & 0xffff0000u) * up);
+          }
+        }
       }
     }
     int lo_r[NTW][2], hi_r[NTW][2];
@@ -732,15 +805,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
         float x[4];
         if (interior) {
           // padded rows (hi = -1) stay masked
-          x[0] = hi_r[n][0] >= 0 ? sc[n][0] * p.sl2 : -INFINITY;
-          x[1] = hi_r[n][1] >= 0 ? sc[n][1] * p.sl2 : -INFINITY;
-          x[2] = hi_r[n][0] >= 0 ? sc[n][2] * p.sl2 : -INFINITY;
-          x[3] = hi_r[n][1] >= 0 ? sc[n][3] * p.sl2 : -INFINITY;
+          x[0] = hi_r[n][0] >= 0 ? sc[n][0] * sl2r[n][0] : -INFINITY;
+          x[1] = hi_r[n][1] >= 0 ? sc[n][1] * sl2r[n][1] : -INFINITY;
+          x[2] = hi_r[n][0] >= 0 ? sc[n][2] * sl2r[n][0] : -INFINITY;
+          x[3] = hi_r[n][1] >= 0 ? sc[n][3] * sl2r[n][1] : -INFINITY;
         } else {
-          x[0] = (j0 >= lo_r[n][0] && j0 <= hi_r[n][0]) ? sc[n][0] * p.sl2 : -INFINITY;
-          x[1] = (j0 >= lo_r[n][1] && j0 <= hi_r[n][1]) ? sc[n][1] * p.sl2 : -INFINITY;
-          x[2] = (j1 >= lo_r[n][0] && j1 <= hi_r[n][0]) ? sc[n][2] * p.sl2 : -INFINITY;
-          x[3] = (j1 >= lo_r[n][1] && j1 <= hi_r[n][1]) ? sc[n][3] * p.sl2 : -INFINITY;
+          x[0] = (j0 >= lo_r[n][0] && j0 <= hi_r[n][0]) ? sc[n][0] * sl2r[n][0] : -INFINITY;
+          x[1] = (j0 >= lo_r[n][1] && j0 <= hi_r[n][1]) ? sc[n][1] * sl2r[n][1] : -INFINITY;
+          x[2] = (j1 >= lo_r[n][0] && j1 <= hi_r[n][0]) ? sc[n][2] * sl2r[n][0] : -INFINITY;
+          x[3] = (j1 >= lo_r[n][1] && j1 <= hi_r[n][1]) ? sc[n][3] * sl2r[n][1] : -INFINITY;
         }
         float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
@@ -948,10 +1021,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           __half* dst = p.out + (static_cast<long long>(pc.q0 + i) * p.Hq + (pc.kh + hh) * p.G + hl) * D + dc * 8;
           const float inv = (Ls > 0.f) ? p.out_scale / Ls : 0.f;
           uint4 v;
-          v.x = pack2<BF16>(v0.x * inv, v0.y * inv);
-          v.y = pack2<BF16>(v0.z * inv, v0.w * inv);
-          v.z = pack2<BF16>(v1.x * inv, v1.y * inv);
-          v.w = pack2<BF16>(v1.z * inv, v1.w * inv);
+          v.x = pack2<Cfg::QB>(v0.x * inv, v0.y * inv);
+          v.y = pack2<Cfg::QB>(v0.z * inv, v0.w * inv);
+          v.z = pack2<Cfg::QB>(v1.x * inv, v1.y * inv);
+          v.w = pack2<Cfg::QB>(v1.z * inv, v1.w * inv);
           *reinterpret_cast<uint4*>(dst) = v;
         } else {
           const long long prow = static_cast<long long>(pc.slot) * Cfg::RP + hh * RH + r;
@@ -981,11 +1054,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
               if constexpr (FP8) {
                 const int d0 = (mt >> 1) * 32 + 4 * g + 2 * (mt & 1);  // dims d0, d0 + 1
                 *reinterpret_cast<uint32_t*>(dst + d0) =
-                    pack2<BF16>(o[mtl][n][c] * inv, o[mtl][n][2 + c] * inv);
+                    pack2<Cfg::QB>(o[mtl][n][c] * inv, o[mtl][n][2 + c] * inv);
               } else {
                 const int d0 = mt * 16 + g;                           // dims d0, d0 + 8
-                reinterpret_cast<uint16_t*>(dst)[d0] = pack1<BF16>(o[mtl][n][c] * inv);
-                reinterpret_cast<uint16_t*>(dst)[d0 + 8] = pack1<BF16>(o[mtl][n][2 + c] * inv);
+                reinterpret_cast<uint16_t*>(dst)[d0] = pack1<Cfg::QB>(o[mtl][n][c] * inv);
+                reinterpret_cast<uint16_t*>(dst)[d0 + 8] = pack1<Cfg::QB>(o[mtl][n][2 + c] * inv);
               }
             }
           } else {

@@ -43,9 +43,10 @@
 
 namespace pd {
 
-template <int D_>
+template <int D_, bool QB_ = false>
 struct Tc8 {
   static constexpr int D = D_;
+  static constexpr bool QB = QB_;                   // q and out in bfloat16 (else fp16)
   static constexpr int kSlabs = D / 128;            // 128-byte slabs of one e4m3 key row
   static constexpr int kBlkTiles = 8;               // 16-key tiles per 128-key block
   static constexpr int kSlabBlk = 128 * 128;        // one slab of a block: [128 keys][128 B]
@@ -89,6 +90,13 @@ struct Tc8 {
                 "tensor-core operands start on 1024-byte swizzle atoms");
   static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
 };
+
+// A 16-bit pair (fp16, or bfloat16 with QB) as two floats, exactly.
+template <bool QB>
+__device__ __forceinline__ float2 pair_to_float2(uint32_t w) {
+  if constexpr (QB) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  else return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
 
 // An fp16 pair to two e4m3fn codes (low half -> low byte), round to nearest
 // even, saturating at +-448.
@@ -230,16 +238,19 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
         const uint32_t w[4] = {qv[c][hh].x, qv[c][hh].y, qv[c][hh].z, qv[c][hh].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+          const float2 f = pair_to_float2<T::QB>(w[k]);
           mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
         }
       }
     }
 #pragma unroll
     for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    // 2^e with the row's largest |q| * 2^e in [128, 256); |q| is an fp16
-    // value, so e lies in [-8, 31] and 2^e, 2^-e are normal floats
-    const int e = mx > 0.f ? 134 - static_cast<int>((__float_as_uint(mx) >> 23) & 255u) : 0;
+    // 2^e with the row's largest |q| * 2^e in [128, 256); for an fp16 q, e
+    // lies in [-8, 31]; a bfloat16 q reaches further, and e is held to
+    // [-126, 126] so that 2^e and 2^-e stay normal floats (only rows whose
+    // largest |q| is below 2^-119 then keep fewer than 11 bits)
+    const int e = mx > 0.f ? max(-126, min(126, 134 - static_cast<int>((__float_as_uint(mx) >> 23) & 255u)))
+                           : 0;
     const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
@@ -251,8 +262,8 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
 #pragma unroll
         for (int k = 0; k < 4; k += 2) {
           uint32_t a[3], b[3];
-          const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
-          const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&w[k + 1]));
+          const float2 fa = pair_to_float2<T::QB>(w[k]);
+          const float2 fb = pair_to_float2<T::QB>(w[k + 1]);
           split3_e4m3(pack_half2(fa.x * up, fa.y * up), a[0], a[1], a[2]);
           split3_e4m3(pack_half2(fb.x * up, fb.y * up), b[0], b[1], b[2]);
 #pragma unroll
@@ -487,7 +498,8 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
         __half* dst = p.out + (static_cast<long long>(pc.q0 + i) * p.Hq + pc.kh * p.G + hl) * D;
         const float inv = L > 0.f ? p.out_scale / L : 0.f;
 #pragma unroll
-        for (int h = 0; h < S; ++h) dst[128 * h + key] = __float2half_rn(o[h][k] * inv);
+        for (int h = 0; h < S; ++h)
+          reinterpret_cast<uint16_t*>(dst)[128 * h + key] = pack1<T::QB>(o[h][k] * inv);
       } else {
         float* dst = p.ws_o + (static_cast<long long>(pc.slot) * p.rows_padded + r) * D;
 #pragma unroll

@@ -59,7 +59,8 @@ __device__ __forceinline__ float quot(float x, float s, float r, bool fast) {
   return (e == 0.f || !(fabsf(q0) < INFINITY)) ? q0 : fmaf(e, r, q0);
 }
 
-template <int KV>
+// BIN: the new tokens are bfloat16 (fp16 otherwise); both widen to fp32 exactly.
+template <int KV, bool BIN>
 __device__ __forceinline__ void store_row8(void* cache, long long elem, uint4 x, float scale, float rcp,
                                            bool fast) {
   if constexpr (KV == PD_KV_F16) {
@@ -69,7 +70,8 @@ __device__ __forceinline__ void store_row8(void* cache, long long elem, uint4 x,
     float f[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      const float2 p = BIN ? make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u))
+                           : __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
       f[2 * i] = quot(p.x, scale, rcp, fast);
       f[2 * i + 1] = quot(p.y, scale, rcp, fast);
     }
@@ -88,7 +90,7 @@ __device__ __forceinline__ void store_row8(void* cache, long long elem, uint4 x,
   }
 }
 
-template <int KV>
+template <int KV, bool BIN>
 __global__ void __launch_bounds__(kWriterThreads) kv_writer_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
     const int64_t* __restrict__ slot_mapping, long long num_tokens, int vecs_per_token,
@@ -113,8 +115,8 @@ __global__ void __launch_bounds__(kWriterThreads) kv_writer_kernel(
 #pragma unroll 4
     for (int v = lane; v < vecs_per_token; v += 32) {
       const uint4 kx = __ldcs(kin + v), vx = __ldcs(vin + v);
-      store_row8<KV>(k_cache, (base + v) * 8, kx, k_scale, k_rcp, fast != 0);
-      store_row8<KV>(v_cache, (base + v) * 8, vx, v_scale, v_rcp, fast != 0);
+      store_row8<KV, BIN>(k_cache, (base + v) * 8, kx, k_scale, k_rcp, fast != 0);
+      store_row8<KV, BIN>(v_cache, (base + v) * 8, vx, v_scale, v_rcp, fast != 0);
     }
   }
 }
@@ -132,7 +134,7 @@ extern "C" pd_status write_kv_cache(const void* k_new, const void* v_new,
       d.num_blocks < 0)
     return PD_ERR_SHAPE;
   if (d.kv_dtype != PD_KV_F16 && d.kv_dtype != PD_KV_FP8_E4M3 && d.kv_dtype != PD_KV_INT8 &&
-      d.kv_dtype != PD_KV_BF16)
+      d.kv_dtype != PD_KV_BF16 && d.kv_dtype != PD_KV_FP8_E4M3_BF16 && d.kv_dtype != PD_KV_INT8_BF16)
     return PD_ERR_DTYPE;
   const long long row = static_cast<long long>(d.Hkv) * d.D;
   if (row / 8 > 0x7fffffffll) return PD_ERR_SHAPE;
@@ -165,17 +167,27 @@ extern "C" pd_status write_kv_cache(const void* k_new, const void* v_new,
   switch (d.kv_dtype) {
     case PD_KV_F16:
     case PD_KV_BF16:  // 16-bit caches: the input bits as they are
-      pd::kv_writer_kernel<PD_KV_F16><<<grid, pd::kWriterThreads, 0, s>>>(
+      pd::kv_writer_kernel<PD_KV_F16, false><<<grid, pd::kWriterThreads, 0, s>>>(
           kn, vn, slot_mapping, static_cast<long long>(num_tokens), vecs, slots, k_cache, v_cache, 1.f, 1.f, 1.f, 1.f, 0,
           error_flag);
       break;
     case PD_KV_FP8_E4M3:
-      pd::kv_writer_kernel<PD_KV_FP8_E4M3><<<grid, pd::kWriterThreads, 0, s>>>(
+      pd::kv_writer_kernel<PD_KV_FP8_E4M3, false><<<grid, pd::kWriterThreads, 0, s>>>(
+          kn, vn, slot_mapping, static_cast<long long>(num_tokens), vecs, slots, k_cache, v_cache, d.k_scale,
+          d.v_scale, k_rcp, v_rcp, fast, error_flag);
+      break;
+    case PD_KV_FP8_E4M3_BF16:
+      pd::kv_writer_kernel<PD_KV_FP8_E4M3, true><<<grid, pd::kWriterThreads, 0, s>>>(
+          kn, vn, slot_mapping, static_cast<long long>(num_tokens), vecs, slots, k_cache, v_cache, d.k_scale,
+          d.v_scale, k_rcp, v_rcp, fast, error_flag);
+      break;
+    case PD_KV_INT8_BF16:
+      pd::kv_writer_kernel<PD_KV_INT8, true><<<grid, pd::kWriterThreads, 0, s>>>(
           kn, vn, slot_mapping, static_cast<long long>(num_tokens), vecs, slots, k_cache, v_cache, d.k_scale,
           d.v_scale, k_rcp, v_rcp, fast, error_flag);
       break;
     default:
-      pd::kv_writer_kernel<PD_KV_INT8><<<grid, pd::kWriterThreads, 0, s>>>(
+      pd::kv_writer_kernel<PD_KV_INT8, false><<<grid, pd::kWriterThreads, 0, s>>>(
           kn, vn, slot_mapping, static_cast<long long>(num_tokens), vecs, slots, k_cache, v_cache, d.k_scale,
           d.v_scale, k_rcp, v_rcp, fast, error_flag);
       break;

@@ -40,6 +40,10 @@ bool shape_fp8_d128(int nt, int grouped, KernelShape* out);
 bool shape_fp8_d256(int nt, int grouped, KernelShape* out);
 bool shape_i8_d128(int nt, int grouped, KernelShape* out);
 bool shape_i8_d256(int nt, int grouped, KernelShape* out);
+bool shape_fp8q_d128(int nt, int grouped, KernelShape* out);  // bfloat16 q and out
+bool shape_fp8q_d256(int nt, int grouped, KernelShape* out);
+bool shape_i8q_d128(int nt, int grouped, KernelShape* out);
+bool shape_i8q_d256(int nt, int grouped, KernelShape* out);
 bool shape_bf16_d128(int nt, int grouped, KernelShape* out);
 bool shape_bf16_d256(int nt, int grouped, KernelShape* out);
 cudaError_t launch_f16_d128(int nt, int grouped, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
@@ -54,6 +58,14 @@ cudaError_t launch_i8_d128(int nt, int grouped, const CUtensorMap&, const CUtens
                            cudaStream_t);
 cudaError_t launch_i8_d256(int nt, int grouped, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
                            cudaStream_t);
+cudaError_t launch_fp8q_d128(int nt, int grouped, const CUtensorMap&, const CUtensorMap&, const DecodeParams&,
+                             int, cudaStream_t);
+cudaError_t launch_fp8q_d256(int nt, int grouped, const CUtensorMap&, const CUtensorMap&, const DecodeParams&,
+                             int, cudaStream_t);
+cudaError_t launch_i8q_d128(int nt, int grouped, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
+                            cudaStream_t);
+cudaError_t launch_i8q_d256(int nt, int grouped, const CUtensorMap&, const CUtensorMap&, const DecodeParams&, int,
+                            cudaStream_t);
 cudaError_t launch_bf16_d128(int nt, int grouped, const CUtensorMap&, const CUtensorMap&,
                              const DecodeParams&, int, cudaStream_t);
 cudaError_t launch_bf16_d256(int nt, int grouped, const CUtensorMap&, const CUtensorMap&,

@@ -20,6 +20,10 @@ bool kernel_shape(int D, int kv, int nt, int grouped, KernelShape* out) {
   if (kv == kKvBf16)
     return D == 128 ? shape_bf16_d128(nt, grouped, out)
                     : D == 256 && shape_bf16_d256(nt, grouped, out);
+  if (kv == kKvFp8Bq)
+    return D == 128 ? shape_fp8q_d128(nt, grouped, out) : D == 256 && shape_fp8q_d256(nt, grouped, out);
+  if (kv == kKvInt8Bq)
+    return D == 128 ? shape_i8q_d128(nt, grouped, out) : D == 256 && shape_i8q_d256(nt, grouped, out);
   if (D == 128)
     return kv == kKvFp8 ? shape_fp8_d128(nt, grouped, out) : kv == kKvInt8 ? shape_i8_d128(nt, grouped, out)
                                                                       : shape_f16_d128(nt, grouped, out);
@@ -34,6 +38,12 @@ cudaError_t launch_decode(int D, int kv, int nt, int grouped, const CUtensorMap&
   if (kv == kKvBf16)
     return D == 128 ? launch_bf16_d128(nt, grouped, tk, tv, p, grid, s)
                     : launch_bf16_d256(nt, grouped, tk, tv, p, grid, s);
+  if (kv == kKvFp8Bq)
+    return D == 128 ? launch_fp8q_d128(nt, grouped, tk, tv, p, grid, s)
+                    : launch_fp8q_d256(nt, grouped, tk, tv, p, grid, s);
+  if (kv == kKvInt8Bq)
+    return D == 128 ? launch_i8q_d128(nt, grouped, tk, tv, p, grid, s)
+                    : launch_i8q_d256(nt, grouped, tk, tv, p, grid, s);
   if (D == 128)
     return kv == kKvFp8 ? launch_fp8_d128(nt, grouped, tk, tv, p, grid, s)
            : kv == kKvInt8 ? launch_i8_d128(nt, grouped, tk, tv, p, grid, s)
@@ -65,17 +75,22 @@ struct Plan {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Caches of one-byte codes (e4m3fn or int8, with an fp16 or a bfloat16 q).
+bool byte_kind(int kv) {
+  return kv == PD_KV_FP8_E4M3 || kv == PD_KV_INT8 || kv == PD_KV_FP8_E4M3_BF16 || kv == PD_KV_INT8_BF16;
+}
+// q and out (and a writer's new tokens) in bfloat16.
+bool bf16_io(int kv) { return kv == PD_KV_BF16 || kv == PD_KV_FP8_E4M3_BF16 || kv == PD_KV_INT8_BF16; }
+
 pd_status check_dims(const pd_dims* d, int qlen) {
   if (!d) return PD_ERR_NULL;
   if (d->B < 0 || d->Hq < 1 || d->Hkv < 1 || d->D < 1 || d->block_size < 1 || d->num_blocks < 0 ||
       d->max_blocks_per_seq < 0 || qlen < 1)
     return PD_ERR_SHAPE;
   if (d->Hq % d->Hkv != 0) return PD_ERR_SHAPE;
-  if (d->kv_dtype != PD_KV_F16 && d->kv_dtype != PD_KV_FP8_E4M3 && d->kv_dtype != PD_KV_INT8 &&
-      d->kv_dtype != PD_KV_BF16)
+  if (d->kv_dtype != PD_KV_F16 && d->kv_dtype != PD_KV_BF16 && !byte_kind(d->kv_dtype))
     return PD_ERR_DTYPE;
-  if ((d->kv_dtype == PD_KV_FP8_E4M3 || d->kv_dtype == PD_KV_INT8) &&
-      (!std::isfinite(d->k_scale) || !std::isfinite(d->v_scale)))
+  if (byte_kind(d->kv_dtype) && (!std::isfinite(d->k_scale) || !std::isfinite(d->v_scale)))
     return PD_ERR_SHAPE;
   if (d->D != 128 && d->D != 256) return PD_ERR_UNSUPPORTED;
   if (d->block_size % kTileKeys != 0) return PD_ERR_UNSUPPORTED;
@@ -196,7 +211,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 bool encode_cache_map(CUtensorMap* m, const void* base, const pd_dims* d, int hg) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const bool byte = d->kv_dtype == PD_KV_FP8_E4M3 || d->kv_dtype == PD_KV_INT8;
+  const bool byte = byte_kind(d->kv_dtype);
   const cuuint64_t elem = byte ? 1 : 2;
   const cuuint64_t rows = static_cast<cuuint64_t>(d->num_blocks) * d->block_size;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d->D), static_cast<cuuint64_t>(d->Hkv),
@@ -290,7 +305,7 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   if (!encode_cache_map(&tk, k_cache, dims, pl.hg) || !encode_cache_map(&tv, v_cache, dims, pl.hg))
     return PD_ERR_CUDA;
 
-  const bool fp8 = dims->kv_dtype == PD_KV_FP8_E4M3 || dims->kv_dtype == PD_KV_INT8;  // scaled codes
+  const bool fp8 = byte_kind(dims->kv_dtype);  // scaled codes
   DecodeParams p;
   p.q = static_cast<const __half*>(q);
   p.out = static_cast<__half*>(out);
@@ -324,7 +339,7 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   const double ks = fp8 ? static_cast<double>(dims->k_scale) : 1.0;
   p.sl2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 * ks);
   p.out_scale = fp8 ? dims->v_scale : 1.0f;
-  p.out_bf16 = dims->kv_dtype == PD_KV_BF16 ? 1 : 0;
+  p.out_bf16 = bf16_io(dims->kv_dtype) ? 1 : 0;
   p.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   p.inject = g_inject.load(std::memory_order_relaxed);
 
