@@ -222,6 +222,9 @@ class DeviceWorkload:
 
     def __init__(self, device, l2_bytes, seed, B, Hq, Hkv, Dh, seq_lens, qlen=1, window=0,
                  kv="f16", layout="permuted", bs=BS, max_blocks=None, qlens=None):
+        # "fp8_bf16q" / "int8_bf16q": byte caches under a bfloat16 q and out
+        q_bf16 = kv in ("bf16", "fp8_bf16q", "int8_bf16q")
+        kv = {"fp8_bf16q": "fp8", "int8_bf16q": "int8"}.get(kv, kv)
         gen = torch.Generator().manual_seed(seed)
         need = [(L + bs - 1) // bs for L in seq_lens]
         self.max_blocks = max_blocks or max(need + [1])
@@ -271,7 +274,7 @@ class DeviceWorkload:
         else:
             rows = B * qlen
         self.q = torch.randn((rows, Hq, Dh), generator=dg, device=device,
-                             dtype=torch.float32).to(torch.bfloat16 if kv == "bf16" else torch.float16)
+                             dtype=torch.float32).to(torch.bfloat16 if q_bf16 else torch.float16)
         self.seq_lens = torch.tensor(seq_lens, dtype=torch.int32, device=device)
         self.out = torch.empty_like(self.q)
         self.B, self.qlen, self.window, self.Dh = B, qlen, window, Dh
@@ -381,6 +384,10 @@ def other_workloads(device, l2, seed, only=None):
         lambda: DeviceWorkload(device, l2, seed + 95, 32, 24, 4, 256, [4096] * 32, kv="int8"), 0)
     add("gqa6_d256_L4096_b32_bf16",
         lambda: DeviceWorkload(device, l2, seed + 93, 32, 24, 4, 256, [4096] * 32, kv="bf16"), 0)
+    add("gqa6_d256_L4096_b32_fp8_bf16q",
+        lambda: DeviceWorkload(device, l2, seed + 92, 32, 24, 4, 256, [4096] * 32, kv="fp8_bf16q"), 0)
+    add("verify_q3_fp8_bf16q_d256_L8192_b8",
+        lambda: DeviceWorkload(device, l2, seed + 91, 8, 24, 4, 256, [8192] * 8, qlen=3, kv="fp8_bf16q"), 0)
     gq = torch.Generator().manual_seed(seed + 94)
     qlens = torch.randint(1, 5, (32,), generator=gq).tolist()
     add("varlen_q1to4_d256_L4096_b32",
