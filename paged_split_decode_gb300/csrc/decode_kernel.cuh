@@ -590,9 +590,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
 
   while (work_next(p, s_pre, it, pc)) {
     // ---- per-piece setup: Q fragments (B operand) and per-row visible key limits
-    // bfloat16 q over byte caches: every lane takes part in each row's maximum
-    // over all of D (so the warps sharing a row agree), then keeps the exponent
-    // of row g (its q fragments) and the score factors of rows 2t4, 2t4 + 1
+    // bfloat16 q over byte caches: each row's exponent from its largest |q|
+    // over all of D (a warp that holds only part of D loads its rows whole,
+    // all at once, so the warps sharing a row agree); each lane keeps the
+    // exponent of row g (its q fragments) and the score factors of rows 2t4,
+    // 2t4 + 1 (lane = 4 g + t4)
     int eq[NTW];          // exponent of q row g of row tile n
     float sl2r[NTW][2];   // score factor of rows 2t4 + c: p.sl2 / 2^e
 #pragma unroll
@@ -600,36 +602,34 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
       eq[n] = 0;
       sl2r[n][0] = sl2r[n][1] = p.sl2;
     }
-    if constexpr (Cfg::kQScale) {
+    if constexpr (Cfg::kQScale && DS > 1) {
+      constexpr int W = D / 64;  // 32-bit words (bfloat16 pairs) per lane and row
+      uint32_t wv[NTW * 8][W];
 #pragma unroll
-      for (int n = 0; n < NTW; ++n) {
-#pragma unroll 1
-        for (int j = 0; j < 8; ++j) {
-          const int r = (rg * NTW + n) * 8 + j;
-          float m = 0.f;
-          if (r < pc.R && pc.ntiles > 0) {  // uniform over the warp
-            const int i = r / p.G, hl = r % p.G;
-            const __half* row = p.q + (static_cast<long long>(pc.q0 + i) * p.Hq + (pc.kh + th) * p.G + hl) * D;
-            constexpr int W = D / 64;  // 32-bit words (bfloat16 pairs) per lane
-            uint32_t w[W];
-            if constexpr (W == 4) {
-              const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + lane);
-              w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-            } else {
-              const uint2 v = __ldg(reinterpret_cast<const uint2*>(row) + lane);
-              w[0] = v.x; w[1] = v.y;
-            }
+      for (int rr = 0; rr < NTW * 8; ++rr) {
+        const int r = (rg * NTW + rr / 8) * 8 + rr % 8;
 #pragma unroll
-            for (int k = 0; k < W; ++k)
-              m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xffff0000u))));
+        for (int k = 0; k < W; ++k) wv[rr][k] = 0u;
+        if (r < pc.R && pc.ntiles > 0) {
+          const int i = r / p.G, hl = r % p.G;
+          const uint32_t* row = reinterpret_cast<const uint32_t*>(
+              p.q + (static_cast<long long>(pc.q0 + i) * p.Hq + (pc.kh + th) * p.G + hl) * D);
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          }
-          const int e = q_row_exponent(m);
-          if (g == j) eq[n] = e;
-          if (2 * t4 == j) sl2r[n][0] = p.sl2 * pow2f(-e);
-          if (2 * t4 + 1 == j) sl2r[n][1] = p.sl2 * pow2f(-e);
+          for (int k = 0; k < W; ++k) wv[rr][k] = __ldg(row + W * lane + k);
         }
+      }
+#pragma unroll
+      for (int rr = 0; rr < NTW * 8; ++rr) {
+        float m = 0.f;
+#pragma unroll
+        for (int k = 0; k < W; ++k)
+          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(wv[rr][k] << 16)), fabsf(__uint_as_float(wv[rr][k] & 0xffff0000u))));
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const int e = q_row_exponent(m), n = rr / 8, j = rr % 8;
+        if (g == j) eq[n] = e;
+        if (2 * t4 == j) sl2r[n][0] = p.sl2 * pow2f(-e);
+        if (2 * t4 + 1 == j) sl2r[n][1] = p.sl2 * pow2f(-e);
       }
     }
 #pragma unroll
@@ -655,14 +655,36 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
         }
         qf[ksl][n][0] = qrow ? __ldg(reinterpret_cast<const uint32_t*>(qrow + d0)) : 0u;
         qf[ksl][n][1] = qrow ? __ldg(reinterpret_cast<const uint32_t*>(qrow + d1)) : 0u;
-        if constexpr (Cfg::kQScale) {  // bfloat16 pair * 2^e -> fp16 pair, exact
-          const float up = pow2f(eq[n]);
+      }
+    }
+    if constexpr (Cfg::kQScale) {
+#pragma unroll
+      for (int n = 0; n < NTW; ++n) {
+        if constexpr (DS == 1) {
+          // the four lanes of row g hold all of its D: their fragments' maximum
+          float m = 0.f;
+#pragma unroll
+          for (int ksl = 0; ksl < KSW; ++ksl)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t w = qf[ksl][n][h];
+              m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w << 16)), fabsf(__uint_as_float(w & 0xffff0000u))));
+            }
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+          eq[n] = q_row_exponent(m);
+          sl2r[n][0] = p.sl2 * pow2f(-__shfl_sync(0xffffffffu, eq[n], 8 * t4));
+          sl2r[n][1] = p.sl2 * pow2f(-__shfl_sync(0xffffffffu, eq[n], 8 * t4 + 4));
+        }
+        // bfloat16 pair * 2^e -> fp16 pair, exact
+        const float up = pow2f(eq[n]);
+#pragma unroll
+        for (int ksl = 0; ksl < KSW; ++ksl)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint32_t w = qf[ksl][n][h];
             qf[ksl][n][h] = pack_half2(__uint_as_float(w << 16) * up, __uint_as_float(w & 0xffff0000u) * up);
           }
-        }
       }
     }
     int lo_r[NTW][2], hi_r[NTW][2];
