@@ -141,3 +141,26 @@ def test_combine_validates(lib):
     assert lib.decode_paged_combine(None, 16, 16, 4, 2, 256, 16, None) == 1
     assert lib.decode_paged_combine(16, 16, 0x1004, 4, 2, 256, 16, None) == 5
     assert lib.decode_paged_combine(16, 16, 16, 0, 2, 256, 16, None) == 0   # no rows
+
+
+@pytest.mark.parametrize("byte", ["fp8", "int8"])
+@pytest.mark.parametrize("qlen,kw", [(1, {}), (1, dict(Hq=12, Hkv=2)), (3, dict(B=8)), (2, dict(D=128))])
+def test_bf16_q_byte_kinds_plan_like_their_fp16_q_kinds(lib, byte, qlen, kw):
+    """A bfloat16 q over fp8 / int8 caches runs the same shapes as an fp16 q:
+    the same grids and workspaces, for every split mode."""
+    flag = {"kv_fp8": True} if byte == "fp8" else {"kv_int8": True}
+    f16q = _dims(**flag, **kw)
+    bq = _dims(**flag, q_bf16=True, **kw)
+    assert bq.kv_dtype == f16q.kv_dtype + 3
+    for S in (0, 1, 3):
+        assert binding.grid_ctas(bq, qlen, S, sm_count=152) == binding.grid_ctas(f16q, qlen, S, sm_count=152) > 0
+        assert binding.workspace_bytes(bq, qlen, S, sm_count=152) == \
+            binding.workspace_bytes(f16q, qlen, S, sm_count=152)
+
+
+def test_bf16_q_needs_a_bf16_or_byte_cache():
+    with pytest.raises(TypeError):
+        _dims(q_bf16=True)
+    bad = _dims(kv_fp8=True, q_bf16=True)
+    bad.kv_dtype = 6
+    assert binding.workspace_bytes(bad, 1, 0, sm_count=152) == 0
