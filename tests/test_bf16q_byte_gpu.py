@@ -119,3 +119,24 @@ def test_writer_takes_bf16_tokens(pd, kind):
                                  kv_fp8=kind == "fp8", kv_int8=kind == "int8", bf16=True)
     assert np.array_equal(kd.view(torch.uint8).cpu().numpy(), ko)
     assert np.array_equal(vd.view(torch.uint8).cpu().numpy(), vo)
+
+
+@pytest.mark.parametrize("kv", KINDS)
+def test_varlen_under_bf16_q_matches_oracle(pd, kv):
+    """A query count per sequence (decode_paged_varlen) over byte caches with
+    a bfloat16 q: rows outside every sequence's range are left as they were."""
+    qlens = [1, 3, 0, 2, 4, 1]
+    w = inputs.make_varlen_workload(qlens=qlens, B=len(qlens), Hq=16, Hkv=4, D=256, kv=kv,
+                                    seq_lens=[500, 2000, 7, 1, 900, 0], seed=31)
+    k, v = w.k_cache.to(DEV), w.v_cache.to(DEV)
+    if w.kv_int8:
+        k, v = k.view(torch.int8), v.view(torch.int8)
+    got = pd.decode_paged_varlen(w.q.to(DEV), k, v, w.block_table.to(DEV), w.seq_lens.to(DEV),
+                                 w.q_start.to(DEV), w.qlen, w.scale, w.window, 0, k_scale=w.k_scale,
+                                 v_scale=w.v_scale)
+    torch.cuda.synchronize()
+    ref = oracle.decode_paged_varlen(bits(w.q), w.k_cache.numpy(), w.v_cache.numpy(),
+                                     w.block_table.numpy(), w.seq_lens.numpy(), w.q_start.numpy(),
+                                     w.scale, w.window, w.k_scale, w.v_scale, w.kv_fp8, w.kv_int8,
+                                     bf16=True)
+    check(w, got, ref)
