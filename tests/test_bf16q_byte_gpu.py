@@ -71,6 +71,9 @@ def check(w, got, ref):
 CASES = [
     ("gqa6_d256_head_groups", dict(B=3, Hq=24, Hkv=4, D=256, seq_lens=[4096, 1000, 17])),
     ("gqa6_d128_per_head_kg2", dict(B=3, Hq=12, Hkv=2, D=128, seq_lens=[2500, 300, 1])),
+    # four heads per tile with D split over two warps: each warp loads its q
+    # rows whole for the row exponents
+    ("gqa4_d128_head_groups_dsplit", dict(B=3, Hq=16, Hkv=4, D=128, seq_lens=[3000, 200, 1])),
     ("rows_12_d256", dict(B=3, Hq=12, Hkv=2, D=256, qlen=2, seq_lens=[5, 1000, 64])),
     ("verify_q3_d256", dict(B=3, Hq=24, Hkv=4, D=256, qlen=3, seq_lens=[2, 2000, 800])),
     ("rows_32_window_d128", dict(B=2, Hq=16, Hkv=2, D=128, qlen=4, window=300, seq_lens=[1500, 40])),
