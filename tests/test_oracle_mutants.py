@@ -47,6 +47,9 @@ MUTANTS = [
     ("bf16q_e4m3_cache_read_as_f16", "if (d->kv_kind == 1 || d->kv_kind == 4)\n",
      "if (d->kv_kind == 1)\n"),
     ("writer_bf16_tokens_read_as_f16", "const int b16 = d->kv_kind >= 4;", "const int b16 = 0;"),
+    ("writer_bf16_cache_quantised", "if (d->kv_kind == 0 || d->kv_kind == 3) {", "if (d->kv_kind == 0) {"),
+    ("writer_bf16_cache_byte_stores", "((uint16_t*)k_cache)[dst + e] = kx;",
+     "if (d->kv_kind == 3) ((uint8_t*)k_cache)[dst + e] = (uint8_t)kx; else ((uint16_t*)k_cache)[dst + e] = kx;"),
 ]
 
 

@@ -87,8 +87,14 @@ def test_i8_encoder_matches_numpy(oracle_lib):
 
 # ---- writer ------------------------------------------------------------------
 
-# byte caches take fp16 new tokens, or bfloat16 ones under a bfloat16 model
-KINDS = ("f16", "fp8", "int8", "fp8_bf16q", "int8_bf16q")
+# 16-bit caches take the new tokens' bits (fp16, or bfloat16 for a bfloat16
+# model); byte caches quantise fp16 new tokens, or bfloat16 ones under a
+# bfloat16 model
+KINDS = ("f16", "bf16", "fp8", "int8", "fp8_bf16q", "int8_bf16q")
+
+
+def _bf16_tokens(kind):
+    return kind == "bf16" or kind.endswith("bf16q")
 
 
 def _bf16_bits(x):
@@ -97,7 +103,7 @@ def _bf16_bits(x):
 
 def _tokens_f32(x, kind):
     """The new tokens' values (fp16 arrays, or bfloat16 bit patterns)."""
-    if kind.endswith("bf16q"):
+    if _bf16_tokens(kind):
         return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(torch.float32).numpy()
     return x.astype(np.float32)
 
@@ -106,12 +112,14 @@ def _writer_case(kind, seed=0, T=37, num_blocks=11, bs=16, Hkv=3, D=40):
     g = np.random.default_rng(seed)
     k_new = (g.standard_normal((T, Hkv, D)) * 2).astype(np.float16)
     v_new = (g.standard_normal((T, Hkv, D)) * 3).astype(np.float16)
-    if kind.endswith("bf16q"):
+    if _bf16_tokens(kind):
         k_new, v_new = _bf16_bits(k_new), _bf16_bits(v_new)
     slots = g.permutation(num_blocks * bs)[:T].astype(np.int64)
     slots[::7] = -1  # padding tokens
     if kind == "f16":
         kc = np.full((num_blocks, bs, Hkv, D), 0x7E01, dtype=np.uint16).view(np.float16)
+    elif kind == "bf16":
+        kc = np.full((num_blocks, bs, Hkv, D), 0x7FC1, dtype=np.uint16)
     else:
         kc = np.full((num_blocks, bs, Hkv, D), 0x5A, dtype=np.uint8)
     vc = kc.copy()
@@ -120,7 +128,7 @@ def _writer_case(kind, seed=0, T=37, num_blocks=11, bs=16, Hkv=3, D=40):
 
 def _flags(kind):
     return dict(kv_fp8=kind.startswith("fp8"), kv_int8=kind.startswith("int8"),
-                bf16=kind.endswith("bf16q"))
+                bf16=_bf16_tokens(kind))
 
 
 def _quantise_lib(x, scale, kind):
@@ -140,7 +148,9 @@ def test_writer_layout_and_codes(oracle_lib, kind):
     bs = kc.shape[1]
     live = slots >= 0
     blk, off = slots[live] // bs, slots[live] % bs
-    if kind == "f16":
+    if kind in ("f16", "bf16"):
+        # a 16-bit cache holds the new tokens' bit patterns, two bytes each
+        assert kc.dtype.itemsize == 2
         want_k, want_v = k_new[live], v_new[live]
         assert np.array_equal(kc[blk, off].view(np.uint16), want_k.view(np.uint16))
         assert np.array_equal(vc[blk, off].view(np.uint16), want_v.view(np.uint16))
