@@ -53,7 +53,13 @@ KERNEL_SOURCES = ["paged_split_decode_gb300/csrc/decode_kernel.cuh",
                   "paged_split_decode_gb300/csrc/launch.h",
                   "paged_split_decode_gb300/csrc/pdecode_api.cu",
                   "paged_split_decode_gb300/csrc/split_combine.cu"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_f16_d256_gqa6_b32_traffic.md")
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
+# the headline decode kernel, from one ncu capture of
+#   bench.py --workload gqa6_d256_L4096_b32 --steps 5 --warmup 3
+# (-k regex:decode_paged_kernel -s 3 -c 1), with the hash of KERNEL_SOURCES
+# it was taken on; reported as roofline.traffic only while the sources hash
+# the same (null otherwise).
+HEADLINE_TRAFFIC = {"kernel_source_hash": None, "bytes_per_launch": None}
 
 
 def kv_bytes_of(seq_lens, qlen, window, Hkv, Dh, elem):
@@ -85,16 +91,11 @@ def measured_peaks():
 
 
 def traffic_per_launch():
-    """dram read+write bytes per launch from the committed ncu summary, or None
-    when the summary is missing or was taken on other kernel sources."""
-    if not os.path.exists(TRAFFIC_FILE):
+    """ncu's DRAM read+write bytes per headline decode launch, or None when no
+    capture was taken on the current kernel sources."""
+    if HEADLINE_TRAFFIC["bytes_per_launch"] is None or HEADLINE_TRAFFIC["kernel_source_hash"] != kernel_hash():
         return None
-    txt = open(TRAFFIC_FILE).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", txt)
-    hsh = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
-    if not m or not hsh or hsh.group(1) != kernel_hash():
-        return None
-    return int(m.group(1))
+    return int(HEADLINE_TRAFFIC["bytes_per_launch"])
 
 
 class ClockSampler:
@@ -560,6 +561,18 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def short_name(name):
+    """A workload's name in the compact per-workload summary."""
+    for pat, rep in ((r"^gqa6_d256_L4096_b(\d+)$", r"b\1"), (r"^tiny_.*", "tiny"),
+                     (r"^gqa(\d)_d128_b32_ragged_(dense|permuted)$", r"d128g\1_\2"),
+                     (r"^long_d256_L32768_", "L32k_"), (r"_w4096_", "_w4k_"),
+                     (r"^verify_q3_(\w+?)_d256_L8192_b8$", r"q3_\1"),
+                     (r"^gqa6_d256_L4096_b32_", "b32_"), (r"^varlen_q1to4_.*", "varlen"),
+                     (r"^kv_writer_(\w+?)_T32768_h4_d256$", r"wr_\1")):
+        name = re.sub(pat, rep, name)
+    return name
+
+
 def workload_config(B):
     return {"workload": f"gqa6_d256_L{SEQ_LEN}_b{B}", "B": B, "Hq": HQ, "Hkv": HKV, "D": D,
             "qlen": 1, "seq_len": SEQ_LEN, "block_size": BS, "block_table": "random-permuted",
@@ -713,6 +726,12 @@ def main():
             "clocks": clk,
             "sweep": sweep,
             "configs": configs,
+            # last, so that it ends the line: every workload as [us per call,
+            # fraction of the measured copy peak]
+            "workloads_fmt": "short name: [us_per_call, frac_of_peak]",
+            "workloads": {short_name(f"gqa6_d256_L{SEQ_LEN}_b{r['B']}"): [r["us_per_call"], r["frac_of_peak"]]
+                          for r in sweep} | {short_name(c["workload"]): [c["us_per_call"], c["frac_of_peak"]]
+                                             for c in configs},
         }
         print(json.dumps(line), flush=True)
     if world > 1:

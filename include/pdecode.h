@@ -31,7 +31,8 @@
  *     (a cudaStream_t; NULL = the legacy default stream) and returns at once.
  *   - Host-checkable problems are reported through the return value before
  *     anything is launched. PD_ERR_CUDA means a launch or runtime call failed;
- *     cudaGetLastError() then holds the CUDA error.
+ *     the library only peeks at the runtime's last error, so the caller's
+ *     cudaGetLastError() still returns the CUDA error.
  *   - Data errors that only the device can see (a block id outside
  *     [0, num_blocks), a seq_len outside [0, max_blocks_per_seq*block_size],
  *     a pipeline wait that ran past its time limit) never trap: the kernel
@@ -224,8 +225,8 @@ PD_API void pd_set_wait_limit_ns(unsigned long long ns);
 PD_API void pd_set_fault_injection(int mode);
 
 /* Size of the scratch array built into the library for
- * decode_paged_static_scratch (32 MiB). Every GPU that loads the library
- * keeps this much device memory until the process exits. */
+ * decode_paged_static_scratch (32 MiB). Every GPU on which that entry point
+ * has been called keeps this much device memory until the process exits. */
 #define PD_STATIC_SCRATCH_BYTES (32u << 20)
 
 /* decode_paged for callers that cannot allocate device memory (no counterpart
@@ -242,8 +243,15 @@ PD_API void pd_set_fault_injection(int mode);
  *     PD_STATIC_SCRATCH_BYTES return PD_ERR_WORKSPACE before anything runs.
  *   - Each call launches exactly as decode_paged does, on `stream`.
  *   - The first call on a device looks up the scratch's device address on
- *     that device (cudaGetSymbolAddress, the device being current); make
- *     that first call before any stream capture.
+ *     that device (cudaGetSymbolAddress, the device being current). Under
+ *     CUDA's lazy module loading (the default) that lookup is also when the
+ *     driver loads the module holding the array and takes its
+ *     PD_STATIC_SCRATCH_BYTES of device memory. So make the first call on
+ *     each device at start-up: outside any allocator callback, while the
+ *     process may still grow its footprint, and before any stream capture.
+ *     Later calls take no device memory.
+ *   - After a cudaDeviceReset the next call on that device is a first call
+ *     again (the address is looked up in the new context).
  *   - All calls on a device share the one scratch array, which keeps the
  *     last call's contents: calls that may overlap on the GPU (different
  *     streams without ordering between them) race and give wrong results. */

@@ -173,18 +173,28 @@ def grid_ctas(dims: PdDims, qlen: int, num_splits: int, sm_count: int = 0) -> in
 _workspaces: dict = {}
 
 
-def get_workspace(device: torch.device, nbytes: int) -> torch.Tensor | None:
-    """A reusable workspace per device, grown on demand.
+def get_workspace(device: torch.device, nbytes: int, stream: int | None = None) -> torch.Tensor | None:
+    """A reusable workspace per (device, stream), grown on demand.
 
     Every call writes what it reads, so one buffer serves every call made on
-    one stream. Pass your own buffer to decode_paged for calls that may
-    overlap on different streams."""
+    one stream in turn; calls on different streams (which may overlap on the
+    GPU) get different buffers. ``stream`` is the raw cudaStream_t handle the
+    call launches on (default: torch's current stream on ``device``); the
+    buffer is allocated on that stream, so torch's allocator reuses it, once
+    it is outgrown, only in that stream's order."""
     if nbytes == 0:
         return None
-    key = (device.type, device.index)
+    cur = torch.cuda.current_stream(device)
+    handle = cur.cuda_stream if stream is None else int(stream)
+    key = (device.type, device.index, handle)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        size = max(nbytes, 1 << 20)
+        if handle == cur.cuda_stream:
+            ws = torch.empty(size, dtype=torch.uint8, device=device)
+        else:
+            with torch.cuda.stream(torch.cuda.ExternalStream(handle, device=device)):
+                ws = torch.empty(size, dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
 
@@ -220,13 +230,13 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale, window=0, ql
         raise ValueError("q must be [B*qlen, Hq, D] with B = rows of block_table and seq_lens")
     if out.shape != q.shape:
         raise ValueError("out must have q's shape")
-    need = workspace_bytes(dims, qlen, num_splits)
-    if workspace is None:
-        workspace = get_workspace(q.device, need)
-    ws_ptr = 0 if workspace is None else _dev_ptr(workspace, "workspace")
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
+    need = workspace_bytes(dims, qlen, num_splits)
+    if workspace is None:
+        workspace = get_workspace(q.device, need, stream)
+    ws_ptr = 0 if workspace is None else _dev_ptr(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     flag_ptr = None if error_flag is None else _dev_ptr(error_flag, "error_flag", (torch.int32, torch.uint32))
     rc = lib.decode_paged(_dev_ptr(q, "q", q_dt), _dev_ptr(k_cache, "k_cache", kv_dt),
                           _dev_ptr(v_cache, "v_cache", kv_dt),
@@ -258,13 +268,13 @@ def decode_paged_varlen(q, k_cache, v_cache, block_table, seq_lens, query_start_
         raise ValueError("q must be [T, Hq, D]; seq_lens [B]; query_start_loc [B+1]")
     if out.shape != q.shape:
         raise ValueError("out must have q's shape")
-    need = workspace_bytes(dims, max_qlen, num_splits)
-    if workspace is None:
-        workspace = get_workspace(q.device, need)
-    ws_ptr = 0 if workspace is None else _dev_ptr(workspace, "workspace")
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
+    need = workspace_bytes(dims, max_qlen, num_splits)
+    if workspace is None:
+        workspace = get_workspace(q.device, need, stream)
+    ws_ptr = 0 if workspace is None else _dev_ptr(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     flag_ptr = None if error_flag is None else _dev_ptr(error_flag, "error_flag", (torch.int32, torch.uint32))
     rc = lib.decode_paged_varlen(_dev_ptr(q, "q", q_dt), _dev_ptr(k_cache, "k_cache", kv_dt),
                                  _dev_ptr(v_cache, "v_cache", kv_dt),

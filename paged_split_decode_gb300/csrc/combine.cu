@@ -71,5 +71,5 @@ extern "C" pd_status decode_paged_combine(const float* part_m, const float* part
   if (blocks > 0x7fffffffll) return PD_ERR_UNSUPPORTED;
   pd::combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, static_cast<cudaStream_t>(stream)>>>(
       part_m, part_l, part_o, rows, num_splits, D, static_cast<__half*>(out));
-  return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
+  return cudaPeekAtLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
 }

@@ -1,8 +1,8 @@
 // decode_static_scratch.cu -- decode_paged for callers that cannot allocate
 // device memory.
 //
-// decode_paged needs a workspace for its split-K partials and tickets, which
-// the caller normally allocates. Some callers cannot: code that runs where
+// decode_paged needs a workspace for its split descriptors and split-K
+// partials, which the caller normally allocates. Some callers cannot: code that runs where
 // cudaMalloc is not allowed (inside a custom allocator's own callbacks, a
 // plugin host that hands out no device buffers, or a process that must not
 // grow its device footprint after start-up). This file gives them one entry
@@ -12,12 +12,15 @@
 #include <cstdint>
 #include <mutex>
 
+#include "launch.h"
 #include "pdecode.h"
 
 namespace {
 
-// Size of the built-in scratch. Every GPU that loads the library holds this
-// array until the process exits.
+// Size of the built-in scratch. Every GPU on which this entry point has been
+// called holds this array until the process exits (under CUDA's lazy module
+// loading the driver takes the memory at the first call, not when the
+// library is loaded).
 constexpr size_t kStaticScratchBytes = PD_STATIC_SCRATCH_BYTES;
 
 // File-scope device array. In host code its name is only a host-side stand-in
@@ -27,22 +30,25 @@ static __device__ __align__(256) uint8_t g_scratch[kStaticScratchBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
-bool g_ready[kMaxDevices] = {};
+unsigned long long g_ctx[kMaxDevices] = {};  // context the address belongs to (0: none yet)
 
-// Device address of g_scratch on the current device; looked up once per
-// device, with that device current.
+// Device address of g_scratch on the current device: looked up with that
+// device current, once per device and context (a cudaDeviceReset makes a new
+// context, whose module may place the array elsewhere, so it is looked up
+// again there).
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const unsigned long long ctx = pd::current_context_id();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_ready[dev]) {
+  if (ctx == 0 || g_ctx[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess) return e;
     g_addr[dev] = p;
-    g_ready[dev] = true;
+    g_ctx[dev] = ctx;
   }
   *out = g_addr[dev];
   return cudaSuccess;

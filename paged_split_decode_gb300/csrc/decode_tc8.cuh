@@ -737,20 +737,15 @@ __global__ void __launch_bounds__(T::kThreads, 1)
 }
 
 // Host launch of the e4m3 tensor-core decode (one CTA per SM); sets the
-// shared-memory opt-in once per device.
+// shared-memory opt-in once per context.
 template <class T>
 cudaError_t launch_tc8(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
                        cudaStream_t stream) {
-  static unsigned long long attr_done = 0;  // bit per device ordinal (< 64)
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static unsigned long long attr_ctx[64] = {};
+  const cudaError_t e = once_per_context(attr_ctx, [] {
+    return cudaFuncSetAttribute(decode_tc8_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
+  });
   if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
-    e = cudaFuncSetAttribute(decode_tc8_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);
-  }
   return launch_pdl(decode_tc8_kernel<T>, grid, T::kThreads, T::kSmemBytes, stream, tk, tv, p);
 }
 template <class T>

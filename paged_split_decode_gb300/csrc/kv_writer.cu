@@ -192,5 +192,5 @@ extern "C" pd_status write_kv_cache(const void* k_new, const void* v_new,
           d.v_scale, k_rcp, v_rcp, fast, error_flag);
       break;
   }
-  return cudaGetLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
+  return cudaPeekAtLastError() == cudaSuccess ? PD_OK : PD_ERR_CUDA;
 }

@@ -71,6 +71,30 @@ cudaError_t launch_bf16_d128(int nt, int grouped, const CUtensorMap&, const CUte
 cudaError_t launch_bf16_d256(int nt, int grouped, const CUtensorMap&, const CUtensorMap&,
                              const DecodeParams&, int, cudaStream_t);
 
+// Identity of the CUDA context current on the calling thread: a number the
+// driver never hands out twice in one process (the primary context made after
+// a cudaDeviceReset gets a new one), or 0 when no context is current or the
+// driver cannot tell. Per-device set-up (a kernel's shared-memory opt-in, a
+// device symbol's address) is keyed on it, so it is redone after a reset.
+unsigned long long current_context_id();
+
+// Runs `setup` once per CUDA context for the calling thread's current device:
+// `done` holds, per device ordinal (< 64), the id of the context that last
+// completed it. Returns setup's error, or cudaSuccess.
+template <class F>
+cudaError_t once_per_context(unsigned long long (&done)[64], F setup) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const unsigned long long ctx = current_context_id();
+  if (ctx != 0 && __atomic_load_n(&done[dev], __ATOMIC_ACQUIRE) == ctx) return cudaSuccess;
+  e = setup();
+  if (e != cudaSuccess) return e;
+  __atomic_store_n(&done[dev], ctx, __ATOMIC_RELEASE);
+  return cudaSuccess;
+}
+
 // Launch with programmatic dependent launch: the kernel's CTAs may be
 // scheduled while the preceding grid in the stream drains; the kernel waits
 // (griddepcontrol.wait) before its first global memory access.
@@ -88,24 +112,19 @@ cudaError_t launch_pdl(Kern kernel, int grid, int threads, int smem, cudaStream_
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
   if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return cudaPeekAtLastError();  // the error stays visible to the caller
 }
 
-// Launch one configuration; sets the shared-memory opt-in once per device.
+// Launch one configuration; sets the shared-memory opt-in once per context.
 template <class Cfg>
 cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
                        cudaStream_t stream) {
-  static unsigned long long attr_done = 0;  // bit per device ordinal (< 64)
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static unsigned long long attr_ctx[64] = {};
+  cudaError_t e = once_per_context(attr_ctx, [] {
+    return cudaFuncSetAttribute(decode_paged_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg::kSmemBytes);
+  });
   if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
-    e = cudaFuncSetAttribute(decode_paged_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);
-  }
   return launch_pdl(decode_paged_kernel<Cfg>, grid, Cfg::kThreads, Cfg::kSmemBytes, stream, tk, tv, p);
 }
 

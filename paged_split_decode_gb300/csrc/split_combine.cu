@@ -24,7 +24,7 @@ cudaError_t launch_split_combine(int D, const DecodeParams& p, int n_desc, int d
   else
     e = cudaLaunchKernelEx(&cfg, split_combine_kernel<256>, p);
   if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return cudaPeekAtLastError();
 }
 
 }  // namespace pd

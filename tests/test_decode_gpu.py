@@ -436,3 +436,27 @@ def test_combine_entry_point_matches_oracle(pd):
     g = got.float().cpu().numpy()
     assert np.max(np.abs(g - want)) <= TOL
     assert np.all(g[np.all(want == 0, axis=1)] == 0)
+
+
+def test_default_workspace_is_per_stream(pd):
+    """Decodes on two streams with no workspace argument each get their own
+    default buffer (their split partials would race in a shared one): every
+    result matches the oracle."""
+    ws = [inputs.gqa_d256(2),
+          inputs.make_workload(B=2, Hq=24, Hkv=4, D=256, qlen=1, seq_lens=[4096, 3000], seed=77)]
+    refs = [ref_run(w) for w in ws]
+    dev_in = []
+    for w in ws:
+        k, v = kv_on_device(w)
+        dev_in.append((w.q.to(DEV), k, v, w.block_table.to(DEV), w.seq_lens.to(DEV)))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in ws]
+    outs = []
+    for _ in range(4):  # back to back, so that the two streams' calls overlap
+        for w, s, (q, k, v, bt, sl) in zip(ws, streams, dev_in):
+            with torch.cuda.stream(s):
+                outs.append((w, pd.decode_paged(q, k, v, bt, sl, w.scale, w.window, w.qlen, 0,
+                                                k_scale=w.k_scale, v_scale=w.v_scale)))
+    torch.cuda.synchronize()
+    for w, got in outs:
+        check(w, got, refs[ws.index(w)])

@@ -5,9 +5,10 @@ visible 16-key tiles of all (sequence, KV head) units are laid end to end and
 cut into equal contiguous ranges; with a fixed split count each unit is cut
 into that many chunks, dealt round robin. This model restates those index
 rules and checks the properties the kernel relies on: every visible tile is
-processed exactly once, each unit's piece count equals the number of pieces
-that bump its ticket, partial slots are distinct and inside the workspace the
-host sizes, and each empty unit gets exactly one zero-fill piece.
+processed exactly once, the piece count each piece carries (what the unit's
+split descriptor tells the combine) equals the number of pieces the unit is
+cut into, partial slots are distinct and inside the workspace the host sizes,
+and each empty unit gets exactly one zero-fill piece.
 """
 import itertools
 import random
@@ -141,7 +142,7 @@ def check(B, Hkv, lens, qlen, window, cap, S, grid, seed=0, cost=0):
             if n == 0:
                 assert len(pcs) == 1 and pcs[0]["tiles"] == [], "empty unit needs one zero piece"
                 continue
-            assert all(pc["npieces"] == len(pcs) for pc in pcs), "ticket count mismatch"
+            assert all(pc["npieces"] == len(pcs) for pc in pcs), "piece count mismatch"
             if len(pcs) > 1:
                 assert sorted(pcs[0]["all_slots"]) == sorted(pc["slot"] for pc in pcs)
                 # the combiner visits partials in key order
