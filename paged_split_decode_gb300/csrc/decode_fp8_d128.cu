@@ -20,16 +20,19 @@ constexpr int kD = 128;
 template <int kKv>
 struct Shapes {
   using C1 = CfgFor<kD, kKv, 1, 2, 2>;
-  using TC = Tc8<kD, q_is_bf16(kKv)>;  // two to four row tiles: the tensor-core (tcgen05) kernel
+  // two to four row tiles: the tensor-core (tcgen05) kernel, one softmax
+  // warpgroup per row tile
+  template <int NG>
+  using TC = Tc8<kD, q_is_bf16(kKv), NG>;
   using C1H = CfgFor<kD, kKv, 1, 1, 1, 2, 4>;
 
   static bool shape(int nt, int grouped, KernelShape* out) {
     if (grouped) return nt == 1 && shape_of<C1H>(out);
     switch (nt) {
       case 1: return shape_of<C1>(out);
-      case 2:
-      case 3:
-      case 4: return shape_tc8<TC>(nt, out);
+      case 2: return shape_tc8<TC<2>>(nt, out);
+      case 3: return shape_tc8<TC<3>>(nt, out);
+      case 4: return shape_tc8<TC<4>>(nt, out);
       default: return false;
     }
   }
@@ -39,9 +42,9 @@ struct Shapes {
     if (grouped) return nt == 1 ? launch_cfg<C1H>(tk, tv, p, grid, s) : cudaErrorInvalidValue;
     switch (nt) {
       case 1: return launch_cfg<C1>(tk, tv, p, grid, s);
-      case 2:
-      case 3:
-      case 4: return launch_tc8<TC>(tk, tv, p, grid, s);
+      case 2: return launch_tc8<TC<2>>(tk, tv, p, grid, s);
+      case 3: return launch_tc8<TC<3>>(tk, tv, p, grid, s);
+      case 4: return launch_tc8<TC<4>>(tk, tv, p, grid, s);
       default: return cudaErrorInvalidValue;
     }
   }

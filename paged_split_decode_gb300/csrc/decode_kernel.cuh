@@ -81,6 +81,8 @@ struct DecodeParams {
   int out_bf16;               // q and out hold bfloat16 (bfloat16 caches)
   unsigned long long timeout_ns;  // limit of every pipeline wait
   int inject;                     // fault injection: 1 = the producer issues no load
+  int cluster;                    // > 1: fixed split of this many pieces per unit, one CTA each, launched as
+                                  // thread-block clusters that merge a unit's partials in shared memory
 };
 
 // KV element kinds: fp16, one byte per element (OCP e4m3fn or int8 codes), or

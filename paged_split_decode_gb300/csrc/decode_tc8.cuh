@@ -18,18 +18,20 @@
 //    the N side (3 x 32 rows) and their products summed when S^T is read. The
 //    softmax weights are split the same way and stacked on N for P.V; the
 //    three O^T accumulators are summed at the end of a piece.
-//  * Eight softmax warps in two groups: thread i of a group owns TMEM lane i
-//    (key i of a block), and group w owns query rows 16 w .. 16 w + 15 (their
-//    maxima, sums and O^T columns), so the groups never wait on each other.
-//    They read S^T, mask, take the per-row block maximum (warp transpose-reduce
-//    and a shared exchange), form the weights against a running maximum that is
-//    only raised when the block maximum exceeds it by more than 2^4 (then the
-//    O^T accumulator is rescaled in tensor memory), and write P^T: each key's
-//    thread stores its 32 row weights as one 32-byte row of an MN-major
-//    operand (32-byte swizzle). V^T is read by
-//    the product straight from the ring as an MN-major operand (each 128-byte
-//    key row is 128 consecutive dims). Keys past the sequence end or outside
-//    the piece get -inf scores and their V rows are zeroed in the ring.
+//  * Softmax warps in NG groups of four (NG = the unit's 8-row tiles, 2 to
+//    4): thread i of a group owns TMEM lane i (key i of a block), and group g
+//    owns query rows 8 g .. 8 g + 7 (their maxima, sums and O^T columns), so
+//    the groups never wait on each other and no group works on padding rows
+//    beyond its tile. They read S^T, mask, take the per-row block maximum
+//    (warp transpose-reduce and a shared exchange), form the weights against a
+//    running maximum that is only raised when the block maximum exceeds it by
+//    more than 2^4 (then the O^T accumulator is rescaled in tensor memory), and
+//    write P^T: each key's thread stores its 8 row weights per term as one
+//    8-byte piece of a 32-byte row of an MN-major operand (32-byte swizzle).
+//    V^T is read by the product straight from the ring as an MN-major operand
+//    (each 128-byte key row is 128 consecutive dims). Keys past the sequence
+//    end or outside the piece get -inf scores and their V rows are zeroed in
+//    the ring.
 //  * K and V have rings of their own: a K stage is released when S^T is
 //    computed, a V stage when the P.V product that reads it completes.
 //  * At the end of a piece the warps read O^T (one output dim per thread) and
@@ -43,10 +45,11 @@
 
 namespace pd {
 
-template <int D_, bool QB_ = false>
+template <int D_, bool QB_ = false, int NG_ = 4>
 struct Tc8 {
   static constexpr int D = D_;
   static constexpr bool QB = QB_;                   // q and out in bfloat16 (else fp16)
+  static constexpr int NG = NG_;                    // softmax groups = 8-row tiles of a unit (1 to 4)
   static constexpr int kSlabs = D / 128;            // 128-byte slabs of one e4m3 key row
   static constexpr int kBlkTiles = 8;               // 16-key tiles per 128-key block
   static constexpr int kSlabBlk = 128 * 128;        // one slab of a block: [128 keys][128 B]
@@ -59,8 +62,11 @@ struct Tc8 {
   static constexpr int kQSlab = kNT * 128;          // q operand, one slab: [term][32 rows][128 B]
   static constexpr int kQBytes = kSlabs * kQSlab;
   static constexpr int kPtTerm = 128 * kN;          // one P^T term: [128 keys][32 rows], MN-major
-  static constexpr int kThreads = 352;              // warps 0-7 softmax, 8-9 producers (K, V), 10 MMA
-  static constexpr int kProducerWarp = 8, kMmaWarp = 10;
+  static constexpr int kGroupRows = 8;              // query rows per softmax group
+  static constexpr int kSoftThreads = 128 * NG;     // softmax warps 0 .. 4 NG - 1
+  static constexpr int kThreads = kSoftThreads + 96;  // then the K and V producers and the MMA warp
+  static constexpr int kProducerWarp = 4 * NG, kMmaWarp = 4 * NG + 2;
+  static constexpr int kBarAll = NG + 1;            // named barrier of every softmax thread (1..NG: groups)
   static constexpr int kTmemCols = 512;             // S^T x2 (2 x 96), O^T (kSlabs x 96)
   static constexpr int kColS = 0, kColO = 2 * kNT;
   static constexpr uint32_t kIdescS = idesc_e4m3(128, kNT);               // K-major A and B
@@ -76,19 +82,26 @@ struct Tc8 {
   static constexpr int kOffV = NBK * kKBlk;
   static constexpr int kOffQ = kOffV + NBV * kKBlk;
   static constexpr int kOffPt = kOffQ + kQBytes;
-  static constexpr int kOffRed = kOffPt + 3 * kPtTerm;     // float [2 groups][4 warps][16 rows]
+  static constexpr int kOffRed = kOffPt + 3 * kPtTerm;     // float [NG groups][4 warps][8 rows]
   static constexpr int kRowWords = 7 * 32;                 // row state: 7 arrays of 32 words
-  static constexpr int kOffRow = kOffRed + 4 * 32 * 4;
-  static constexpr int kOffBars = kOffRow + kRowWords * 4;
+  static constexpr int kOffRow = kOffRed + NG * 4 * kGroupRows * 4;
+  // Cluster merge (a fixed split whose pieces are the CTAs of one cluster):
+  // each CTA stages its partial (m, l) here and its partial O rows [32][D]
+  // fp32 at offset 0, over the K ring, which is idle once the piece is done.
+  static constexpr int kOffStageMl = kOffRow + kRowWords * 4;  // float2 [32 rows]
+  static constexpr int kOffBars = kOffStageMl + 32 * 8;
   static constexpr int kBars = 2 * NBK + 2 * NBV + 8;
   static constexpr int kOffTmem = kOffBars + kBars * 8;
   static constexpr int kOffPre = kOffTmem + 16;
   static constexpr int kSmemBytes = kOffPre + (kMaxAutoB + 1) * 4 + 1024;  // + alignment slack
   static_assert(D == 128 || D == 256, "head size 128 or 256");
+  static_assert(NG >= 1 && NG <= 4, "one to four 8-row tiles per unit");
+  static_assert(kGroupRows * NG <= kN, "rows of every group on the N side");
   static_assert(kOffV % 1024 == 0 && kOffQ % 1024 == 0 && kOffPt % 1024 == 0 && kQSlab % 1024 == 0 &&
                     kPtTerm % 1024 == 0,
                 "tensor-core operands start on 1024-byte swizzle atoms");
   static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
+  static_assert(kN * D * 4 <= NBK * kKBlk, "the staged O rows fit over the K ring");
 };
 
 // A 16-bit pair (fp16, or bfloat16 with QB) as two floats, exactly.
@@ -127,12 +140,14 @@ enum { kRowFsl = 0, kRowMu = 1, kRowAl = 2, kRowLo = 3, kRowHi = 4, kRowL = 5, k
 // Barriers: fullK[NBK], emptyK[NBK], fullV[NBV], emptyV[NBV], then these.
 enum { kBarSFull = 0, kBarSEmpty = 2, kBarPFull = 4, kBarPvDone = 5, kBarQFull = 6, kBarFinal = 7 };
 
-// 32 values, one per row, held by every lane of a warp -> lane l holds the
-// reduction of row l over the 32 lanes (5 butterfly rounds, 31 shuffles).
-template <bool MAX>
-__device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane) {
+// N values (8, 16 or 32), one per row, held by every lane of a warp -> lane
+// l holds the reduction of row l % N over the 32 lanes (log2 N butterfly
+// rounds exchanging half of the remaining values, then the lane groups).
+template <bool MAX, int N>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) {
+  static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 rows");
 #pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
+  for (int w = N / 2; w >= 1; w >>= 1) {
     const bool up = (lane & w) != 0;
 #pragma unroll
     for (int k = 0; k < w; ++k) {
@@ -142,25 +157,13 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[32], int lane)
       v[k] = MAX ? fmaxf(keep, recv) : keep + recv;
     }
   }
-  return v[0];
-}
-// 16 values, one per row -> lanes l and l + 16 hold the reduction of row l
-// (l < 16) over the 32 lanes (4 butterfly rounds, then the two halves).
-template <bool MAX>
-__device__ __forceinline__ float warp_transpose_reduce16(float (&v)[16], int lane) {
+  float r = v[0];
 #pragma unroll
-  for (int w = 8; w >= 1; w >>= 1) {
-    const bool up = (lane & w) != 0;
-#pragma unroll
-    for (int k = 0; k < w; ++k) {
-      const float send = up ? v[k] : v[k + w];
-      const float keep = up ? v[k + w] : v[k];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, w);
-      v[k] = MAX ? fmaxf(keep, recv) : keep + recv;
-    }
+  for (int o = N; o < 32; o <<= 1) {
+    const float other = __shfl_xor_sync(0xffffffffu, r, o);
+    r = MAX ? fmaxf(r, other) : r + other;
   }
-  const float other = __shfl_xor_sync(0xffffffffu, v[0], 16);
-  return MAX ? fmaxf(v[0], other) : v[0] + other;
+  return r;
 }
 
 // Posts a unit's split descriptor from its first piece (as decode_kernel).
@@ -178,23 +181,25 @@ __device__ __forceinline__ void post_unit_descriptor(const DecodeParams& p, cons
   p.ws_desc[pc.unit] = d;
 }
 
-// The softmax warps: two warpgroups (threads 0-127 and 128-255) share the
-// keys of a block -- thread i of a group owns TMEM lane i (key i of a block for
-// S^T, output dims i and i + 128 for O^T) -- and split the 32 query rows:
-// group w takes rows 16 w .. 16 w + 15, with their running maxima, sums and
-// O^T columns, so the groups never wait on each other inside a block.
+// The softmax warps: NG warpgroups share the keys of a block -- thread i of a
+// group owns TMEM lane i (key i of a block for S^T, output dims i and i + 128
+// for O^T) -- and split the query rows: group g takes rows 8 g .. 8 g + 7,
+// with their running maxima, sums and O^T columns, so the groups never wait on
+// each other inside a block.
 template <class T>
 __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s_pre, WorkIter& it, Piece& pc,
                                              uint8_t* smem, uint32_t sbase, uint32_t tmem, bool& ok) {
-  constexpr int D = T::D, NBK = T::NBK, NBV = T::NBV, S = T::kSlabs;
+  constexpr int D = T::D, NBK = T::NBK, NBV = T::NBV, S = T::kSlabs, NR = T::kGroupRows;
+  constexpr int NST = T::kSoftThreads;
+  (void)NBK;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int wg = warp >> 2;             // row half
+  const int g = warp >> 2;              // row group
   const int key = tid & 127;            // TMEM lane of this thread
-  const int rb = 16 * wg;               // first row of this half
-  const int bid = 1 + wg;               // the group's named barrier (128 threads)
+  const int rb = NR * g;                // first row of this group
+  const int bid = 1 + g;                // the group's named barrier (128 threads)
   float* rf = reinterpret_cast<float*>(smem + T::kOffRow);
   int* ri = reinterpret_cast<int*>(smem + T::kOffRow);
-  float* red = reinterpret_cast<float*>(smem + T::kOffRed) + 64 * wg;  // [4 warps][16 rows]
+  float* red = reinterpret_cast<float*>(smem + T::kOffRed) + 4 * NR * g;  // [4 warps][8 rows]
   const uint32_t fullv0 = sbase + T::kOffBars + 16 * NBK, bx = fullv0 + 16 * NBV;
   auto bar = [&](int i) -> uint32_t { return bx + 8 * i; };
   const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);  // this warp's TMEM lanes
@@ -205,7 +210,7 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
   auto next_piece = [&](Piece& out) -> bool {
     while (work_next(p, s_pre, it, out)) {
       if (out.ntiles > 0) return true;
-      for (int item = tid; item < out.R * (D / 8); item += 256) {
+      for (int item = tid; item < out.R * (D / 8); item += NST) {
         const int r = item / (D / 8), dc = item % (D / 8);
         const int i = r / p.G, hl = r % p.G;
         *reinterpret_cast<uint4*>(p.out + (static_cast<long long>(out.q0 + i) * p.Hq + out.kh * p.G + hl) * D +
@@ -218,117 +223,123 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
   // A piece's q terms (the B operand of S^T: K-major, 128-byte swizzle, the
   // three terms stacked on N), row score factors and visible key limits; the
   // previous piece's S^T products are complete (its softmax read them all).
-  // Thread t: row t / 8, dims [(t % 8) D / 8, (t % 8 + 1) D / 8).
+  // Item t < 256 (thread t, and t + 128 with a single group): row t / 8,
+  // dims [(t % 8) D / 8, (t % 8 + 1) D / 8).
   auto q_setup = [&](const Piece& pq) {
-    const int r = tid >> 3, part = tid & 7;
-    constexpr int NCH = D / 128;  // 16-dim chunks per thread
-    const __half* qrow = nullptr;
-    if (r < pq.R) {
-      const int i = r / p.G, hl = r % p.G;
-      qrow = p.q + (static_cast<long long>(pq.q0 + i) * p.Hq + pq.kh * p.G + hl) * D;
-    }
-    uint4 qv[NCH][2];
-    float mx = 0.f;
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      const int d0 = part * (D / 8) + 16 * c;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        qv[c][hh] = qrow ? __ldg(reinterpret_cast<const uint4*>(qrow + d0 + 8 * hh)) : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t w[4] = {qv[c][hh].x, qv[c][hh].y, qv[c][hh].z, qv[c][hh].w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 f = pair_to_float2<T::QB>(w[k]);
-          mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    // 2^e with the row's largest |q| * 2^e in [128, 256); for an fp16 q, e
-    // lies in [-8, 31]; a bfloat16 q reaches further, and e is held to
-    // [-126, 126] so that 2^e and 2^-e stay normal floats (only rows whose
-    // largest |q| is below 2^-119 then keep fewer than 11 bits)
-    const int e = mx > 0.f ? max(-126, min(126, 134 - static_cast<int>((__float_as_uint(mx) >> 23) & 255u)))
-                           : 0;
-    const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
-#pragma unroll
-    for (int c = 0; c < NCH; ++c) {
-      const int d0 = part * (D / 8) + 16 * c;
-      uint32_t tw[3][4];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const uint32_t w[4] = {qv[c][hh].x, qv[c][hh].y, qv[c][hh].z, qv[c][hh].w};
-#pragma unroll
-        for (int k = 0; k < 4; k += 2) {
-          uint32_t a[3], b[3];
-          const float2 fa = pair_to_float2<T::QB>(w[k]);
-          const float2 fb = pair_to_float2<T::QB>(w[k + 1]);
-          split3_e4m3(pack_half2(fa.x * up, fa.y * up), a[0], a[1], a[2]);
-          split3_e4m3(pack_half2(fb.x * up, fb.y * up), b[0], b[1], b[2]);
-#pragma unroll
-          for (int t = 0; t < 3; ++t) tw[t][2 * hh + k / 2] = a[t] | (b[t] << 16);
-        }
-      }
-      const uint32_t off = (d0 >> 7) * T::kQSlab + r * 128 + ((((d0 & 127) >> 4) ^ (r & 7)) << 4);
-#pragma unroll
-      for (int t = 0; t < 3; ++t)
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(qs + t * T::kN * 128 + off), "r"(tw[t][0]),
-                     "r"(tw[t][1]), "r"(tw[t][2]), "r"(tw[t][3])
-                     : "memory");
-    }
-    if (part == 0) {
-      int lo = 0, hi = -1;
+    for (int item = tid; item < 256; item += NST) {
+      const int r = item >> 3, part = item & 7;
+      constexpr int NCH = D / 128;  // 16-dim chunks per thread
+      const __half* qrow = nullptr;
       if (r < pq.R) {
-        hi = pq.L - pq.qlen + r / p.G;
-        lo = p.window > 0 ? max(0, hi - p.window + 1) : 0;
+        const int i = r / p.G, hl = r % p.G;
+        qrow = p.q + (static_cast<long long>(pq.q0 + i) * p.Hq + pq.kh * p.G + hl) * D;
       }
-      rf[kRowFsl * 32 + r] = r < pq.R ? p.sl2 * __uint_as_float(static_cast<uint32_t>(127 - e) << 23) : 0.f;
-      rf[kRowMu * 32 + r] = -INFINITY;
-      ri[kRowLo * 32 + r] = lo;
-      ri[kRowHi * 32 + r] = hi;
+      uint4 qv[NCH][2];
+      float mx = 0.f;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        const int d0 = part * (D / 8) + 16 * c;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          qv[c][hh] = qrow ? __ldg(reinterpret_cast<const uint4*>(qrow + d0 + 8 * hh)) : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t w[4] = {qv[c][hh].x, qv[c][hh].y, qv[c][hh].z, qv[c][hh].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = pair_to_float2<T::QB>(w[k]);
+            mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      // 2^e with the row's largest |q| * 2^e in [128, 256); for an fp16 q, e
+      // lies in [-8, 31]; a bfloat16 q reaches further, and e is held to
+      // [-126, 126] so that 2^e and 2^-e stay normal floats (only rows whose
+      // largest |q| is below 2^-119 then keep fewer than 11 bits)
+      const int e = mx > 0.f ? max(-126, min(126, 134 - static_cast<int>((__float_as_uint(mx) >> 23) & 255u)))
+                             : 0;
+      const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        const int d0 = part * (D / 8) + 16 * c;
+        uint32_t tw[3][4];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t w[4] = {qv[c][hh].x, qv[c][hh].y, qv[c][hh].z, qv[c][hh].w};
+#pragma unroll
+          for (int k = 0; k < 4; k += 2) {
+            uint32_t a[3], b[3];
+            const float2 fa = pair_to_float2<T::QB>(w[k]);
+            const float2 fb = pair_to_float2<T::QB>(w[k + 1]);
+            split3_e4m3(pack_half2(fa.x * up, fa.y * up), a[0], a[1], a[2]);
+            split3_e4m3(pack_half2(fb.x * up, fb.y * up), b[0], b[1], b[2]);
+#pragma unroll
+            for (int t = 0; t < 3; ++t) tw[t][2 * hh + k / 2] = a[t] | (b[t] << 16);
+          }
+        }
+        const uint32_t off = (d0 >> 7) * T::kQSlab + r * 128 + ((((d0 & 127) >> 4) ^ (r & 7)) << 4);
+#pragma unroll
+        for (int t = 0; t < 3; ++t)
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(qs + t * T::kN * 128 + off), "r"(tw[t][0]),
+                       "r"(tw[t][1]), "r"(tw[t][2]), "r"(tw[t][3])
+                       : "memory");
+      }
+      if (part == 0) {
+        int lo = 0, hi = -1;
+        if (r < pq.R) {
+          hi = pq.L - pq.qlen + r / p.G;
+          lo = p.window > 0 ? max(0, hi - p.window + 1) : 0;
+        }
+        rf[kRowFsl * 32 + r] = r < pq.R ? p.sl2 * __uint_as_float(static_cast<uint32_t>(127 - e) << 23) : 0.f;
+        rf[kRowMu * 32 + r] = -INFINITY;
+        ri[kRowLo * 32 + r] = lo;
+        ri[kRowHi * 32 + r] = hi;
+      }
     }
     fence_proxy_async_smem();
+  };
+  auto load8 = [&](const float* src, float (&dst)[NR]) {
+#pragma unroll
+    for (int k = 0; k < NR / 4; ++k) {
+      const float4 f = reinterpret_cast<const float4*>(src)[k];
+      dst[4 * k] = f.x; dst[4 * k + 1] = f.y; dst[4 * k + 2] = f.z; dst[4 * k + 3] = f.w;
+    }
   };
 
   while (next_piece(pc)) {
     const bool direct = pc.npieces == 1;
     const int nblk = (pc.ntiles + T::kBlkTiles - 1) / T::kBlkTiles;
     q_setup(pc);
-    named_bar_sync(3, 256);
+    named_bar_sync(T::kBarAll, NST);
     if (tid == 0) mbar_arrive(bar(kBarQFull));
-    float fs[16];  // score factor of each row of this half
+    float fs[NR];  // score factor of each row of this group
+    load8(rf + kRowFsl * 32 + rb, fs);
+    float lp[NR];  // this key lane's share of each row's weight sum
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float4 f = reinterpret_cast<const float4*>(rf + kRowFsl * 32 + rb)[k];
-      fs[4 * k] = f.x; fs[4 * k + 1] = f.y; fs[4 * k + 2] = f.z; fs[4 * k + 3] = f.w;
-    }
-    float lp[16];  // this key lane's share of each row's weight sum
-#pragma unroll
-    for (int r = 0; r < 16; ++r) lp[r] = 0.f;
+    for (int r = 0; r < NR; ++r) lp[r] = 0.f;
 
     for (int i = 0; i < nblk; ++i) {
       const uint32_t b = bq + i;
       const int sv = b % NBV, sb = b & 1;
       const int key0 = (pc.first_tile + T::kBlkTiles * i) * kTileKeys;
       const int nvalid = min(128, kTileKeys * (pc.ntiles - T::kBlkTiles * i));  // keys loaded
-      // ---- this key's scores for the half's 16 rows (three term slices)
-      float x[16];
+      // ---- this key's scores for the group's 8 rows (three term slices)
+      float x[NR];
       if (ok) ok = mbar_wait(bar(kBarSFull + sb), (b >> 1) & 1, p.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
       tc_fence_after();
       if (ok) {
-        float y[16], z[16];
+        float y[NR], z[NR];
         const uint32_t sc = tl + T::kColS + T::kNT * sb + rb;
-        tmem_ld16(sc, x);
-        tmem_ld16(sc + 32, y);
-        tmem_ld16(sc + 64, z);
+        tmem_ld8(sc, x);
+        tmem_ld8(sc + 32, y);
+        tmem_ld8(sc + 64, z);
         tmem_wait_ld();
 #pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = (x[r] + y[r]) + z[r];
+        for (int r = 0; r < NR; ++r) x[r] = (x[r] + y[r]) + z[r];
       } else {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = 0.f;
+        for (int r = 0; r < NR; ++r) x[r] = 0.f;
       }
       tc_fence_before();
       __syncwarp();
@@ -337,38 +348,34 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
       const bool interior = nvalid == 128 && key0 >= pc.tile_lo_all && key0 + 127 <= pc.tile_hi_all;
       if (interior) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] *= fs[r];
+        for (int r = 0; r < NR; ++r) x[r] *= fs[r];
       } else {
         const bool loaded = key < nvalid;
 #pragma unroll
-        for (int r = 0; r < 16; ++r)
+        for (int r = 0; r < NR; ++r)
           x[r] = (loaded && j >= ri[kRowLo * 32 + rb + r] && j <= ri[kRowHi * 32 + rb + r]) ? x[r] * fs[r]
                                                                                          : -INFINITY;
       }
       // ---- running maximum per row, raised to the block maximum only where
       // that exceeds it by more than 2^kRaise. Most blocks raise nothing: one
       // OR-barrier tells, and only then are the block maxima reduced.
-      float mu[16];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 m4 = reinterpret_cast<const float4*>(rf + kRowMu * 32 + rb)[k];
-        mu[4 * k] = m4.x; mu[4 * k + 1] = m4.y; mu[4 * k + 2] = m4.z; mu[4 * k + 3] = m4.w;
-      }
+      float mu[NR];
+      load8(rf + kRowMu * 32 + rb, mu);
       bool upd = false;
 #pragma unroll
-      for (int r = 0; r < 16; ++r) upd |= x[r] > mu[r] + T::kRaise;
+      for (int r = 0; r < NR; ++r) upd |= x[r] > mu[r] + T::kRaise;
       bool rescale = false;
       if (bar_red_or(bid, 128, upd)) {
         {
-          float v[16];
+          float v[NR];
 #pragma unroll
-          for (int r = 0; r < 16; ++r) v[r] = x[r];
-          const float m = warp_transpose_reduce16<true>(v, lane);
-          if (lane < 16) red[(warp & 3) * 16 + lane] = m;
+          for (int r = 0; r < NR; ++r) v[r] = x[r];
+          const float m = warp_transpose_reduce<true, NR>(v, lane);
+          if (lane < NR) red[(warp & 3) * NR + lane] = m;
         }
         named_bar_sync(bid, 128);
-        if ((warp & 3) == 0 && lane < 16) {
-          const float mx = fmaxf(fmaxf(red[lane], red[16 + lane]), fmaxf(red[32 + lane], red[48 + lane]));
+        if ((warp & 3) == 0 && lane < NR) {
+          const float mx = fmaxf(fmaxf(red[lane], red[NR + lane]), fmaxf(red[2 * NR + lane], red[3 * NR + lane]));
           const float m0 = rf[kRowMu * 32 + rb + lane];
           float nmu = m0, al = 1.f;
           if (mx > m0 + T::kRaise) {
@@ -377,64 +384,62 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
           }
           rf[kRowMu * 32 + rb + lane] = nmu;
           rf[kRowAl * 32 + rb + lane] = al;
-          const bool any = __any_sync(0x0000ffffu, al != 1.f);
-          if (lane == 0) ri[kRowFlag * 32 + wg] = any ? 1 : 0;
+          const bool any = __any_sync((1u << NR) - 1u, al != 1.f);
+          if (lane == 0) ri[kRowFlag * 32 + g] = any ? 1 : 0;
         }
         named_bar_sync(bid, 128);
-        rescale = ri[kRowFlag * 32 + wg] != 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float4 m4 = reinterpret_cast<const float4*>(rf + kRowMu * 32 + rb)[k];
-          mu[4 * k] = m4.x; mu[4 * k + 1] = m4.y; mu[4 * k + 2] = m4.z; mu[4 * k + 3] = m4.w;
-        }
+        rescale = ri[kRowFlag * 32 + g] != 0;
+        load8(rf + kRowMu * 32 + rb, mu);
       }
       // ---- weights 2^(x - mu + kBias) (<= 2^8) and the row sums
 #pragma unroll
-      for (int r = 0; r < 16; ++r) x[r] = ex2(x[r] - (mu[r] == -INFINITY ? 0.f : mu[r] - T::kBias));
+      for (int r = 0; r < NR; ++r) x[r] = ex2(x[r] - (mu[r] == -INFINITY ? 0.f : mu[r] - T::kBias));
       if (rescale) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) lp[r] = lp[r] * rf[kRowAl * 32 + rb + r] + x[r];
+        for (int r = 0; r < NR; ++r) lp[r] = lp[r] * rf[kRowAl * 32 + rb + r] + x[r];
       } else {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) lp[r] += x[r];
+        for (int r = 0; r < NR; ++r) lp[r] += x[r];
       }
       // ---- the P.V operands are free once the previous block's product is done
       if (ok && b >= 1) ok = mbar_wait(bar(kBarPvDone), (b - 1) & 1, p.timeout_ns);
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after();
       if (rescale && i > 0 && ok) {
-        // O^T columns of this half's rows whose running maximum was raised
+        // O^T columns of this group's rows whose running maximum was raised
 #pragma unroll 1
         for (int c = 0; c < 3 * S; ++c) {
-          float o[16];
-          tmem_ld16(tl + T::kColO + 32 * c + rb, o);
+          float o[NR];
+          tmem_ld8(tl + T::kColO + 32 * c + rb, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int r = 0; r < 16; ++r) o[r] *= rf[kRowAl * 32 + rb + r];
-          tmem_st16(tl + T::kColO + 32 * c + rb, o);
+          for (int r = 0; r < NR; ++r) o[r] *= rf[kRowAl * 32 + rb + r];
+          tmem_st8(tl + T::kColO + 32 * c + rb, o);
         }
         tmem_wait_st();
       }
-      // ---- P^T, three e4m3 terms: this key's 16 row weights are one 16-byte
-      // half of a 32-byte row (k = key) of an MN-major operand in the 32-byte
-      // swizzle layout (8-key atoms of 256 bytes; the halves swap in rows 4-7)
+      // ---- P^T, three e4m3 terms: this key's 8 row weights are the 8-byte
+      // piece 8 g of a 32-byte row (k = key) of an MN-major operand in the
+      // 32-byte swizzle layout (8-key atoms of 256 bytes; the 16-byte halves
+      // swap in rows 4-7)
       {
-        uint32_t tt[3][8];
+        uint32_t tt[3][NR / 2];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) split3_e4m3(pack_half2(x[2 * k], x[2 * k + 1]), tt[0][k], tt[1][k], tt[2][k]);
-        const uint32_t row = pt + (key >> 3) * 256 + (key & 7) * 32 + ((wg ^ ((key & 7) >> 2)) << 4);
+        for (int k = 0; k < NR / 2; ++k)
+          split3_e4m3(pack_half2(x[2 * k], x[2 * k + 1]), tt[0][k], tt[1][k], tt[2][k]);
+        const uint32_t row = pt + (key >> 3) * 256 + (key & 7) * 32 +
+                             ((((g >> 1) ^ ((key & 7) >> 2)) << 4) | ((g & 1) << 3));
 #pragma unroll
         for (int t = 0; t < 3; ++t)
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(row + t * T::kPtTerm),
-                       "r"(tt[t][0] | (tt[t][1] << 16)), "r"(tt[t][2] | (tt[t][3] << 16)),
-                       "r"(tt[t][4] | (tt[t][5] << 16)), "r"(tt[t][6] | (tt[t][7] << 16))
+          asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"(row + t * T::kPtTerm),
+                       "r"(tt[t][0] | (tt[t][1] << 16)), "r"(tt[t][2] | (tt[t][3] << 16))
                        : "memory");
       }
       // ---- V rows of keys past the sequence end or not loaded (stale or
       // unwritten bytes, NaN codes included) are zeroed in the ring by the first
       // group: the P.V product reads V there, and a zero weight must not meet a NaN
       const int lim = min(nvalid, pc.L - key0);
-      if (wg == 0 && lim < 128) {
+      if (g == 0 && lim < 128) {
         if (ok) ok = mbar_wait(fullv0 + 8 * sv, (b / NBV) & 1, p.timeout_ns);
         ok = __all_sync(0xffffffffu, ok);
         if (ok && key >= lim) {
@@ -454,42 +459,42 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
     }
     bq += nblk;
 
-    // ---- epilogue: O^T (this thread: dims key, key + 128) of the half's rows,
-    // row sums, output
+    // ---- epilogue: O^T (this thread: dims key, key + 128) of the group's
+    // rows, row sums, output
     if (ok) ok = mbar_wait(bar(kBarPvDone), (bq - 1) & 1, p.timeout_ns);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
-    float o[S][16];
+    float o[S][NR];
 #pragma unroll
     for (int h = 0; h < S; ++h) {
       if (ok) {
-        float y[16], z[16];
+        float y[NR], z[NR];
         const uint32_t oc = tl + T::kColO + T::kNT * h + rb;
-        tmem_ld16(oc, o[h]);
-        tmem_ld16(oc + 32, y);
-        tmem_ld16(oc + 64, z);
+        tmem_ld8(oc, o[h]);
+        tmem_ld8(oc + 32, y);
+        tmem_ld8(oc + 64, z);
         tmem_wait_ld();
 #pragma unroll
-        for (int r = 0; r < 16; ++r) o[h][r] = (o[h][r] + y[r]) + z[r];
+        for (int r = 0; r < NR; ++r) o[h][r] = (o[h][r] + y[r]) + z[r];
       } else {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) o[h][r] = 0.f;
+        for (int r = 0; r < NR; ++r) o[h][r] = 0.f;
       }
     }
     tc_fence_before();
     {
-      float v[16];
+      float v[NR];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) v[r] = lp[r];
-      const float sum = warp_transpose_reduce16<false>(v, lane);
-      if (lane < 16) red[(warp & 3) * 16 + lane] = sum;
+      for (int r = 0; r < NR; ++r) v[r] = lp[r];
+      const float sum = warp_transpose_reduce<false, NR>(v, lane);
+      if (lane < NR) red[(warp & 3) * NR + lane] = sum;
     }
     named_bar_sync(bid, 128);
-    if ((warp & 3) == 0 && lane < 16)
-      rf[kRowL * 32 + rb + lane] = (red[lane] + red[16 + lane]) + (red[32 + lane] + red[48 + lane]);
+    if ((warp & 3) == 0 && lane < NR)
+      rf[kRowL * 32 + rb + lane] = (red[lane] + red[NR + lane]) + (red[2 * NR + lane] + red[3 * NR + lane]);
     named_bar_sync(bid, 128);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < NR; ++k) {
       const int r = rb + k;
       if (r >= pc.R) break;
       const float L = rf[kRowL * 32 + r];
@@ -500,22 +505,88 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
 #pragma unroll
         for (int h = 0; h < S; ++h)
           reinterpret_cast<uint16_t*>(dst)[128 * h + key] = pack1<T::QB>(o[h][k] * inv);
+      } else if (p.cluster > 1) {
+        float* dst = reinterpret_cast<float*>(smem) + r * D;  // the staged rows, over the K ring
+#pragma unroll
+        for (int h = 0; h < S; ++h) dst[128 * h + key] = o[h][k];
       } else {
         float* dst = p.ws_o + (static_cast<long long>(pc.slot) * p.rows_padded + r) * D;
 #pragma unroll
         for (int h = 0; h < S; ++h) __stcg(dst + 128 * h + key, o[h][k]);
       }
     }
-    if (!direct && key < 16 && rb + key < pc.R) {
+    if (!direct && key < NR && rb + key < pc.R) {
       const int r = rb + key;
       const float mu = rf[kRowMu * 32 + r];
-      __stcg(reinterpret_cast<float2*>(p.ws_ml + (static_cast<long long>(pc.slot) * p.rows_padded + r) * 2),
-             make_float2(mu == -INFINITY ? -INFINITY : mu - T::kBias, rf[kRowL * 32 + r]));
+      const float2 ml = make_float2(mu == -INFINITY ? -INFINITY : mu - T::kBias, rf[kRowL * 32 + r]);
+      if (p.cluster > 1)
+        reinterpret_cast<float2*>(smem + T::kOffStageMl)[r] = ml;
+      else
+        __stcg(reinterpret_cast<float2*>(p.ws_ml + (static_cast<long long>(pc.slot) * p.rows_padded + r) * 2), ml);
     }
     if (tid == 0) post_unit_descriptor(p, pc);
-    named_bar_sync(3, 256);  // the row state and red[] are rewritten by the next piece
+    named_bar_sync(T::kBarAll, NST);  // the row state and red[] are rewritten by the next piece
   }
   if (!ok && lane == 0) raise_error(p.error_flag, kErrTimeout);
+}
+
+// Cluster merge of a fixed split (p.cluster = S pieces per unit, the S CTAs
+// of one cluster, cluster rank = split index): every CTA has staged its
+// partial (m, l) per row and its unnormalised O rows in its shared memory;
+// CTA s merges the float4 groups g of the unit's rows with g % S == s, reading
+// all S partials through distributed shared memory (all loads of an item in
+// flight at once), and writes them as the split combine would: M = max m,
+// w = 2^(m - M), out = sum w O / sum w l. A CTA that got no piece staged
+// m = -inf (weight 0; its O rows are never written and are not used). A unit
+// covered by one piece (or none) was written by its piece.
+template <class T>
+__device__ __forceinline__ void cluster_merge(const DecodeParams& p, uint32_t sbase) {
+  constexpr int D = T::D, Q4 = D / 4, SMAX = 8;
+  const int S = p.cluster;
+  const int rank = static_cast<int>(cluster_rank());
+  const int u = blockIdx.x / S;
+  const int b = u / p.hgn, kh = (u % p.hgn) * p.hg;
+  int L, t0, n, q0, qn;
+  seq_span(p, b, false, L, t0, n, q0, qn);
+  if (n == 0) return;
+  const int chunk = (n + S - 1) / S;
+  if ((n + chunk - 1) / chunk <= 1) return;
+  const int R = p.G * qn;
+  uint32_t peer[SMAX];  // each peer's shared memory base in the cluster window
+#pragma unroll
+  for (int s = 0; s < SMAX; ++s) peer[s] = s < S ? peer_smem(sbase, s) : 0u;
+  for (int item = rank + S * static_cast<int>(threadIdx.x); item < R * Q4; item += S * T::kThreads) {
+    const int r = item / Q4, c4 = item % Q4;
+    float2 ml[SMAX];
+    float4 o[SMAX];
+#pragma unroll
+    for (int s = 0; s < SMAX; ++s) {
+      if (s < S) {
+        ml[s] = ld_peer_f2(peer[s] + T::kOffStageMl + 8 * r);
+        o[s] = ld_peer_f4(peer[s] + (r * D + 4 * c4) * 4);
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < SMAX; ++s)
+      if (s < S) M = fmaxf(M, ml[s].x);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lsum = 0.f;
+#pragma unroll
+    for (int s = 0; s < SMAX; ++s) {
+      if (s < S && ml[s].x != -INFINITY) {  // an empty piece staged nothing
+        const float w = ex2(ml[s].x - M);
+        lsum += w * ml[s].y;
+        acc.x += w * o[s].x; acc.y += w * o[s].y; acc.z += w * o[s].z; acc.w += w * o[s].w;
+      }
+    }
+    const float inv = lsum > 0.f ? p.out_scale / lsum : 0.f;
+    const int i = r / p.G, hl = r % p.G;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) +
+                    (static_cast<long long>(q0 + i) * p.Hq + kh * p.G + hl) * D + 4 * c4;
+    const uint32_t lo = pack2<T::QB>(acc.x * inv, acc.y * inv), hi = pack2<T::QB>(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+  }
 }
 
 template <class T>
@@ -545,9 +616,9 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     }
     mbar_init(bar(kBarSFull), 1);
     mbar_init(bar(kBarSFull + 1), 1);
-    mbar_init(bar(kBarSEmpty), 8);  // the eight softmax warps
-    mbar_init(bar(kBarSEmpty + 1), 8);
-    mbar_init(bar(kBarPFull), 8);
+    mbar_init(bar(kBarSEmpty), 4 * T::NG);  // the softmax warps
+    mbar_init(bar(kBarSEmpty + 1), 4 * T::NG);
+    mbar_init(bar(kBarPFull), 4 * T::NG);
     mbar_init(bar(kBarPvDone), 1);
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarFinal), 1);
@@ -561,6 +632,15 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
+  // P^T starts as zeros: the columns of rows no group owns (a unit of fewer
+  // than four row tiles) are multiplied but never written or read
+  for (int i = threadIdx.x; i < 3 * T::kPtTerm / 16; i += T::kThreads)
+    asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(sbase + T::kOffPt + 16 * i), "r"(0u) : "memory");
+  fence_proxy_async_smem();
+  // a CTA of a cluster that gets no piece (a unit with fewer tiles than
+  // pieces) contributes nothing to the merge
+  if (threadIdx.x < 32)
+    reinterpret_cast<float2*>(smem + T::kOffStageMl)[threadIdx.x] = make_float2(-INFINITY, 0.f);
   // programmatic dependent launch: no global memory was touched above
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // balanced mode: prefix over sequences of visible tiles (as decode_kernel)
@@ -730,24 +810,89 @@ __global__ void __launch_bounds__(T::kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (p.cluster > 1) {
+    cluster_sync();  // every CTA of the cluster has staged its partial
+    cluster_merge<T>(p, sbase);
+    cluster_sync();  // no CTA leaves while a peer still reads its shared memory
+  }
   if (warp == T::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, T::kTmemCols);
   }
 }
 
-// Host launch of the e4m3 tensor-core decode (one CTA per SM); sets the
-// shared-memory opt-in once per context.
+// Host launch of the e4m3 tensor-core decode (one CTA per SM), with
+// programmatic dependent launch and, for a cluster-merged fixed split,
+// clusters of p.cluster CTAs; sets the shared-memory opt-in once per context.
 template <class T>
 cudaError_t launch_tc8(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
                        cudaStream_t stream) {
   static unsigned long long attr_ctx[64] = {};
-  const cudaError_t e = once_per_context(attr_ctx, [] {
+  cudaError_t e = once_per_context(attr_ctx, [] {
     return cudaFuncSetAttribute(decode_tc8_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
   });
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_tc8_kernel<T>, grid, T::kThreads, T::kSmemBytes, stream, tk, tv, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(T::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = T::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (p.cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+  e = cudaLaunchKernelEx(&cfg, decode_tc8_kernel<T>, tk, tv, p);
+  if (e != cudaSuccess) return e;
+  return cudaPeekAtLastError();
 }
+
+// Clusters of c CTAs (2 <= c <= 8) of this kernel that the device runs at
+// once (cudaOccupancyMaxActiveClusters), found once per context: counts[c]
+// (0 for c < 2, or when the query fails: then there is no cluster merge).
+template <class T>
+void tc8_max_clusters(int (&counts)[9]) {
+  static unsigned long long ctx_done[64] = {};
+  static int cache[64][9] = {};
+  for (int c = 0; c <= 8; ++c) counts[c] = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
+  const cudaError_t e = once_per_context(ctx_done, [dev] {
+    cudaError_t r = cudaFuncSetAttribute(decode_tc8_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         T::kSmemBytes);
+    if (r != cudaSuccess) return r;
+    for (int c = 2; c <= 8; ++c) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(c * 64), 1, 1);
+      cfg.blockDim = dim3(T::kThreads, 1, 1);
+      cfg.dynamicSmemBytes = T::kSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, decode_tc8_kernel<T>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();  // the query's own failure: no cluster merge
+        n = 0;
+      }
+      cache[dev][c] = n;
+    }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return;
+  for (int c = 0; c <= 8; ++c) counts[c] = cache[dev][c];
+}
+
 template <class T>
 bool shape_tc8(int nt, KernelShape* out) {
   out->threads = T::kThreads;
@@ -756,6 +901,7 @@ bool shape_tc8(int nt, KernelShape* out) {
   out->ctas_per_sm = 1;
   out->heads = 1;
   out->unit_cost = T::kUnitCost;
+  tc8_max_clusters<T>(out->max_clusters);
   return true;
 }
 

@@ -16,6 +16,7 @@ struct KernelShape {
   int ctas_per_sm;  // resident CTAs per SM the configuration is sized for
   int heads;        // KV heads per tile (the TMA box's head extent)
   int unit_cost;    // balanced split: virtual tiles charged to every unit start
+  int max_clusters[9];  // [S]: clusters of S CTAs the device runs at once (0: no cluster merge)
 };
 
 // Returns false when no instantiation covers (D, kv kind, nt, grouped):
@@ -157,6 +158,7 @@ bool shape_of(KernelShape* out) {
   out->ctas_per_sm = Cfg::kMinBlocks;
   out->heads = Cfg::HG;
   out->unit_cost = 0;
+  for (int c = 0; c <= 8; ++c) out->max_clusters[c] = 0;
   return true;
 }
 

@@ -70,6 +70,7 @@ struct Plan {
   long long units;  // B * Hkv / hg work units
   int rows_padded;
   int unit_cost;    // balanced split: virtual tiles per unit start
+  int cluster;      // > 1: the fixed split's pieces of a unit form a cluster that merges them
   size_t off_ml, off_o, bytes;  // workspace layout
 };
 
@@ -186,6 +187,16 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
     pl->off_ml = cnt;
     pl->off_o = cnt + ml;
     pl->bytes = cnt + ml + o;
+  }
+  // A fixed split of at most eight pieces per unit, one CTA each, on a kernel
+  // that merges a unit's pieces inside its thread-block cluster (distributed
+  // shared memory), when the device runs every unit's cluster at once: no
+  // split-combine launch. (The workspace keeps the size computed above, so it
+  // does not depend on the device's cluster occupancy.)
+  pl->cluster = 0;
+  if (splits >= 2 && splits <= 8 && pl->units * splits == pl->grid && ks.max_clusters[splits] >= pl->units) {
+    pl->cluster = splits;
+    pl->n_desc = 0;
   }
   return PD_OK;
 }
@@ -369,6 +380,7 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   p.out_bf16 = bf16_io(dims->kv_dtype) ? 1 : 0;
   p.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   p.inject = g_inject.load(std::memory_order_relaxed);
+  p.cluster = pl.cluster;
 
   cudaError_t e = launch_decode(dims->D, dims->kv_dtype, pl.nt, pl.hg > 1 ? 1 : 0, tk, tv, p, pl.grid,
                                 static_cast<cudaStream_t>(stream));

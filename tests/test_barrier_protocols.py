@@ -208,21 +208,22 @@ def test_decode_ring_planted_parity_mistakes_are_caught(mutate):
 # The tensor-memory kernel: per 128-key block b, a K producer and a V producer
 # fill rings of NBK and NBV stages; the MMA thread issues S^T = K Q^T into S
 # buffer b % 2 and, one block behind, O^T += V^T P^T, committing S-full,
-# K-empty, PV-done and V-empty; two softmax warpgroups (four warps each) read
-# S^T, arrive on S-empty, may rescale O^T, write their half of the single P^T
-# buffer after the previous product completed, zero V rows of tail blocks
-# (group 0), and arrive on P-full. Per piece the groups write the q operand
-# and arrive on Q-full, and read O^T at the end.
+# K-empty, PV-done and V-empty; NG softmax warpgroups (four warps each, one
+# per 8-row tile of the unit) read S^T, arrive on S-empty, may rescale O^T,
+# write their rows of the single P^T buffer after the previous product
+# completed, zero V rows of tail blocks (group 0), and arrive on P-full. Per
+# piece the groups write the q operand and arrive on Q-full, and read O^T at
+# the end.
 
-def tc8_roles(NBK, NBV, pieces, tails, rescales, rng, mutate=None):
+def tc8_roles(NBK, NBV, pieces, tails, rescales, rng, mutate=None, NG=2):
     fullk, emptyk = [Bar(1) for _ in range(NBK)], [Bar(1) for _ in range(NBK)]
     fullv, emptyv = [Bar(1) for _ in range(NBV)], [Bar(1) for _ in range(NBV)]
-    sfull, sempty = [Bar(1), Bar(1)], [Bar(8), Bar(8)]
-    pfull, pvdone, qfull = Bar(8), Bar(1), Bar(1)
-    st = {"K": [None] * NBK, "V": [None] * NBV, "S": [None, None], "P": [None, None], "Q": None,
+    sfull, sempty = [Bar(1), Bar(1)], [Bar(4 * NG), Bar(4 * NG)]
+    pfull, pvdone, qfull = Bar(4 * NG), Bar(1), Bar(1)
+    st = {"K": [None] * NBK, "V": [None] * NBV, "S": [None, None], "P": [None] * NG, "Q": None,
           "s_read": [0, 0], "o_busy": 0, "loading": 0}
     inflight, pipe = [], []
-    meet = {"n": 0}  # two-group rendezvous counter (the 256-thread named barrier)
+    meet = {"n": 0}  # rendezvous counter of the groups (the named barrier of every softmax thread)
     nblocks = sum(pieces)
 
     def producer(ring, nb, full, empty):
@@ -278,7 +279,7 @@ def tc8_roles(NBK, NBV, pieces, tails, rescales, rng, mutate=None):
                     yield (lambda par=b & 1: pfull.passed(par))
                     check(st["V"][sv] == ("zeroed", b) or st["V"][sv] == b,
                           f"P.V of block {b} issued on V stage holding {st['V'][sv]}")
-                    check(st["P"] == [b, b] and st["o_busy"] == 0,
+                    check(st["P"] == [b] * NG and st["o_busy"] == 0,
                           f"P.V of block {b} issued on P^T {st['P']} or a busy O^T")
                     if mutate == "early_v_release":
                         pipe.append(("commit", emptyv[sv]))
@@ -304,7 +305,7 @@ def tc8_roles(NBK, NBV, pieces, tails, rescales, rng, mutate=None):
                 st["S"][sb] = b
             else:
                 _, b, sv = op
-                check(st["V"][sv] in (b, ("zeroed", b)) and st["P"] == [b, b] and st["o_busy"] == 0,
+                check(st["V"][sv] in (b, ("zeroed", b)) and st["P"] == [b] * NG and st["o_busy"] == 0,
                       f"P.V of block {b} read a changed operand or a busy O^T")
 
     mma_done = {"v": False}
@@ -324,7 +325,7 @@ def tc8_roles(NBK, NBV, pieces, tails, rescales, rng, mutate=None):
             check(not any(op[0] == "QK" for op in pipe), f"q of piece {p} written under an S^T product")
             if g == 0:
                 st["Q"] = p
-            meets += 2
+            meets += NG
             yield from rendezvous(meets)
             if g == 0:
                 qfull.arrive()
@@ -360,26 +361,30 @@ def tc8_roles(NBK, NBV, pieces, tails, rescales, rng, mutate=None):
             st["o_busy"] += 1
             yield always
             st["o_busy"] -= 1
-            meets += 2
+            meets += NG
             yield from rendezvous(meets)
 
-    return {"K": producers_done(producer("K", NBK, fullk, emptyk)),
-            "V": producers_done(producer("V", NBV, fullv, emptyv)), "tma": tma(), "mma": mma_role(),
-            "pipe": tensor_pipe(), "softmax0": softmax(0), "softmax1": softmax(1)}
+    roles = {"K": producers_done(producer("K", NBK, fullk, emptyk)),
+             "V": producers_done(producer("V", NBV, fullv, emptyv)), "tma": tma(), "mma": mma_role(),
+             "pipe": tensor_pipe()}
+    for g in range(NG):
+        roles[f"softmax{g}"] = softmax(g)
+    return roles
 
 
-def tc8_case(rng, NBK, NBV, mutate=None):
+def tc8_case(rng, NBK, NBV, mutate=None, NG=2):
     pieces = [rng.randint(1, 6) for _ in range(rng.randint(1, 4))]
     n = sum(pieces)
     tails, rescales = [rng.random() < 0.3 for _ in range(n)], [rng.random() < 0.3 for _ in range(n)]
-    return tc8_roles(NBK, NBV, pieces, tails, rescales, rng, mutate)
+    return tc8_roles(NBK, NBV, pieces, tails, rescales, rng, mutate, NG)
 
 
+@pytest.mark.parametrize("NG", [2, 3, 4])  # softmax groups = 8-row tiles of a unit
 @pytest.mark.parametrize("NBK,NBV", [(2, 3), (4, 5)])  # D = 256, D = 128
-def test_tensor_memory_kernel_protocol_is_safe(NBK, NBV):
-    for seed in range(300):
-        rng = random.Random(7000 + 10 * NBK + seed)
-        run(tc8_case(rng, NBK, NBV), rng)
+def test_tensor_memory_kernel_protocol_is_safe(NBK, NBV, NG):
+    for seed in range(200):
+        rng = random.Random(7000 + 10 * NBK + 1000 * NG + seed)
+        run(tc8_case(rng, NBK, NBV, NG=NG), rng)
 
 
 @pytest.mark.parametrize("mutate", ["skip_pv_wait", "sempty_parity", "early_v_release"])

@@ -460,3 +460,25 @@ def test_default_workspace_is_per_stream(pd):
     torch.cuda.synchronize()
     for w, got in outs:
         check(w, got, refs[ws.index(w)])
+
+
+# Fixed splits of two to eight pieces on the tensor-memory kernel (e4m3 KV,
+# 9-32 query rows per KV head): a unit's pieces run as one thread-block
+# cluster and merge through distributed shared memory, with no split-combine
+# launch. Sequences with fewer tiles than pieces leave CTAs of a cluster
+# without a piece; empty sequences and tokens that see no key are zero rows.
+CLUSTER = [
+    ("rows18_d256", dict(B=4, Hq=24, Hkv=4, D=256, qlen=3, kv="fp8", seq_lens=[3000, 40, 0, 2])),
+    ("rows16_d128", dict(B=3, Hq=16, Hkv=2, D=128, qlen=2, kv="fp8", seq_lens=[900, 17, 2500])),
+    ("rows32_d256_window", dict(B=2, Hq=8, Hkv=1, D=256, qlen=4, kv="fp8", window=300,
+                                seq_lens=[2000, 33])),
+    ("rows24_d128_stale", dict(B=3, Hq=8, Hkv=1, D=128, qlen=3, kv="fp8", seq_lens=[5, 301, 4000],
+                               stale="nan")),
+]
+
+
+@pytest.mark.parametrize("S", [2, 3, 4, 5, 8])
+@pytest.mark.parametrize("name,kw", CLUSTER, ids=[c[0] for c in CLUSTER])
+def test_tensor_memory_kernel_cluster_merge(pd, name, kw, S):
+    w = inputs.make_workload(seed=zlib.crc32(name.encode()) % 10000 + 3, name=name, **kw)
+    check(w, gpu_run(pd, w, S), ref_run(w))
