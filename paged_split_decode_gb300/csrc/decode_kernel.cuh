@@ -445,6 +445,75 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
   return false;
 }
 
+// Cluster merge of a fixed split whose S pieces per unit (p.cluster = S) are
+// the S CTAs of one cluster (rank = split index). Every thread of the CTA
+// calls it once, after the CTA's piece wrote its partial to the workspace
+// (fp32 rows slot * RP + head * RH + r with slot = unit * S + split, O
+// relative to m, m in log2 units): one cluster barrier (release / acquire at
+// cluster scope, so every piece's partial is visible), then CTA s merges the
+// float4 groups g of the unit's rows with g % S == s, reading the partials of
+// the unit's pieces from L2 (all loads of an item in flight at once), and
+// writes them as the split combine would: M = max m, w = 2^(m - M),
+// out = sum w O / sum w l. A unit covered by one piece (or none) was written
+// by its piece.
+template <int D, int RP, int RH, int HG, int NTHREADS>
+__device__ __forceinline__ void cluster_merge_ws(const DecodeParams& p) {
+  constexpr int Q4 = D / 4, SMAX = 8;
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+  const int S = p.cluster;
+  int rank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const int u = blockIdx.x / S;
+  const int b = u / p.hgn, kh = (u % p.hgn) * p.hg;
+  int L, t0, n, q0, qn;
+  seq_span(p, b, false, L, t0, n, q0, qn);
+  if (n == 0) return;
+  const int chunk = (n + S - 1) / S;
+  const int np = (n + chunk - 1) / chunk;  // pieces that hold tiles (split indices 0 .. np - 1)
+  if (np <= 1) return;
+  const int R = p.G * qn;
+  const long long slot0 = static_cast<long long>(u) * S;
+  for (int item = rank + S * static_cast<int>(threadIdx.x); item < HG * R * Q4; item += S * NTHREADS) {
+    const int hh = item / (R * Q4), rem = item - hh * (R * Q4);
+    const int r = rem / Q4, c4 = rem % Q4;
+    float2 ml[SMAX];
+    float4 o[SMAX];
+#pragma unroll
+    for (int s = 0; s < SMAX; ++s) {
+      if (s < np) {
+        const long long prow = (slot0 + s) * RP + hh * RH + r;
+        ml[s] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + prow * 2));
+        o[s] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + prow * D + 4 * c4));
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < SMAX; ++s)
+      if (s < np) M = fmaxf(M, ml[s].x);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lsum = 0.f;
+#pragma unroll
+    for (int s = 0; s < SMAX; ++s) {
+      if (s < np && ml[s].x != -INFINITY) {
+        const float w = ex2(ml[s].x - M);
+        lsum += w * ml[s].y;
+        acc.x += w * o[s].x; acc.y += w * o[s].y; acc.z += w * o[s].z; acc.w += w * o[s].w;
+      }
+    }
+    const float inv = lsum > 0.f ? p.out_scale / lsum : 0.f;
+    const int i = r / p.G, hl = r % p.G;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(p.out) +
+                    (static_cast<long long>(q0 + i) * p.Hq + (kh + hh) * p.G + hl) * D + 4 * c4);
+    if (p.out_bf16) {
+      dst[0] = pack_bf162(acc.x * inv, acc.y * inv);
+      dst[1] = pack_bf162(acc.z * inv, acc.w * inv);
+    } else {
+      dst[0] = pack_half2(acc.x * inv, acc.y * inv);
+      dst[1] = pack_half2(acc.z * inv, acc.w * inv);
+    }
+  }
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
     decode_paged_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -570,6 +639,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
         if (!mbar_wait(full0 + 8 * (k % NS), (k / NS) & 1, kDrainLimitNs)) break;
       }
     }
+    __syncwarp();
+    if (p.cluster > 1) cluster_merge_ws<D, Cfg::RP, Cfg::NT * 8, Cfg::HG, Cfg::kThreads>(p);
     return;
   }
 
@@ -1123,6 +1194,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
     if constexpr (Cfg::kSmemMerge) named_bar_sync(1, Cfg::kConsumerThreads);  // merge buffers free again
   }
   if (!ok && lane == 0) raise_error(p.error_flag, kErrTimeout);
+  if (p.cluster > 1) cluster_merge_ws<D, Cfg::RP, Cfg::NT * 8, Cfg::HG, Cfg::kThreads>(p);
 }
 
 // ---------------------------------------------------------------------------

@@ -828,69 +828,11 @@ template <class T>
 cudaError_t launch_tc8(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int grid,
                        cudaStream_t stream) {
   static unsigned long long attr_ctx[64] = {};
-  cudaError_t e = once_per_context(attr_ctx, [] {
+  const cudaError_t e = once_per_context(attr_ctx, [] {
     return cudaFuncSetAttribute(decode_tc8_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
   });
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(T::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = T::kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (p.cluster > 1) {
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = static_cast<unsigned>(p.cluster);
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.numAttrs = 2;
-  }
-  e = cudaLaunchKernelEx(&cfg, decode_tc8_kernel<T>, tk, tv, p);
-  if (e != cudaSuccess) return e;
-  return cudaPeekAtLastError();
-}
-
-// Clusters of c CTAs (2 <= c <= 8) of this kernel that the device runs at
-// once (cudaOccupancyMaxActiveClusters), found once per context: counts[c]
-// (0 for c < 2, or when the query fails: then there is no cluster merge).
-template <class T>
-void tc8_max_clusters(int (&counts)[9]) {
-  static unsigned long long ctx_done[64] = {};
-  static int cache[64][9] = {};
-  for (int c = 0; c <= 8; ++c) counts[c] = 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
-  const cudaError_t e = once_per_context(ctx_done, [dev] {
-    cudaError_t r = cudaFuncSetAttribute(decode_tc8_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         T::kSmemBytes);
-    if (r != cudaSuccess) return r;
-    for (int c = 2; c <= 8; ++c) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(static_cast<unsigned>(c * 64), 1, 1);
-      cfg.blockDim = dim3(T::kThreads, 1, 1);
-      cfg.dynamicSmemBytes = T::kSmemBytes;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = static_cast<unsigned>(c);
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, decode_tc8_kernel<T>, &cfg) != cudaSuccess) {
-        (void)cudaGetLastError();  // the query's own failure: no cluster merge
-        n = 0;
-      }
-      cache[dev][c] = n;
-    }
-    return cudaSuccess;
-  });
-  if (e != cudaSuccess) return;
-  for (int c = 0; c <= 8; ++c) counts[c] = cache[dev][c];
+  return launch_pdl(decode_tc8_kernel<T>, grid, T::kThreads, T::kSmemBytes, stream, p.cluster, tk, tv, p);
 }
 
 template <class T>
@@ -901,7 +843,9 @@ bool shape_tc8(int nt, KernelShape* out) {
   out->ctas_per_sm = 1;
   out->heads = 1;
   out->unit_cost = T::kUnitCost;
-  tc8_max_clusters<T>(out->max_clusters);
+  static unsigned long long ctx_done[64] = {};
+  static int cache[64][9] = {};
+  max_active_clusters(decode_tc8_kernel<T>, T::kThreads, T::kSmemBytes, ctx_done, cache, out->max_clusters);
   return true;
 }
 

@@ -15,7 +15,8 @@
 // Memory-bound: one warp per token in a grid-stride loop, lanes over the
 // token's 16-byte vectors (K and V together), a few resident blocks per SM. The quotient is the
 // correctly rounded fp32 x / scale, formed from the reciprocal r = RN(1/scale)
-// by one residual correction (Markstein's theorem: with r the correctly
+// by one residual correction, two elements at a time with the packed f32x2
+// multiply and fused multiply-add (Markstein's theorem: with r the correctly
 // rounded reciprocal and q0 = RN(x r) within an ulp of x / scale, the residual
 // e = x - q0 scale is exact under FMA and RN(q0 + e r) is the correctly
 // rounded quotient, for quotients away from the underflow range); the host
@@ -49,14 +50,41 @@ __device__ __forceinline__ uint32_t i8_bits(float t) {
   return __float_as_uint(t + 12582912.f);
 }
 
-// Correctly rounded x / s (see the header); `fast` selects the residual form.
-__device__ __forceinline__ float quot(float x, float s, float r, bool fast) {
-  if (!fast) return __fdiv_rn(x, s);
-  const float q0 = x * r;
-  const float e = fmaf(-q0, s, x);
-  // q0 is kept when it is exact (e == 0: also keeps the sign of a zero
-  // quotient) or infinite (an infinite x; the residual is then NaN)
-  return (e == 0.f || !(fabsf(q0) < INFINITY)) ? q0 : fmaf(e, r, q0);
+// Two fp32 values in one 64-bit register (low word = first), for the packed
+// f32x2 arithmetic of sm_100-class GPUs.
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+  return static_cast<unsigned long long>(__float_as_uint(lo)) |
+         (static_cast<unsigned long long>(__float_as_uint(hi)) << 32);
+}
+__device__ __forceinline__ float f2_lo(unsigned long long v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f2_hi(unsigned long long v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// Correctly rounded quotients x / s of a pair (see the header): q0 = RN(x r),
+// e = x - q0 s (exact under FMA), q1 = RN(q0 + e r), as packed f32x2
+// operations; ns = -s. q1 is kept unless it is zero or NaN: then q0 is the
+// quotient (x = +-0, whose sign q1 can lose, or x infinite, where the
+// residual is NaN; a NaN x gives NaN either way). `fast` = 0 takes the plain
+// correctly rounded division (scales outside [2^-100, 2^100]).
+__device__ __forceinline__ float2 quot2(float2 x, float s, unsigned long long r2, unsigned long long ns2,
+                                        bool fast) {
+  if (!fast) return make_float2(__fdiv_rn(x.x, s), __fdiv_rn(x.y, s));
+  const unsigned long long xx = f2_pack(x.x, x.y);
+  const unsigned long long q0 = f2_mul(xx, r2);
+  const unsigned long long e = f2_fma(q0, ns2, xx);
+  const unsigned long long q1 = f2_fma(e, r2, q0);
+  const float a = f2_lo(q1), b = f2_hi(q1);
+  return make_float2(fabsf(a) > 0.f ? a : f2_lo(q0), fabsf(b) > 0.f ? b : f2_hi(q0));
 }
 
 // BIN: the new tokens are bfloat16 (fp16 otherwise); both widen to fp32 exactly.
@@ -67,13 +95,15 @@ __device__ __forceinline__ void store_row8(void* cache, long long elem, uint4 x,
     *reinterpret_cast<uint4*>(static_cast<__half*>(cache) + elem) = x;
   } else {
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    const unsigned long long r2 = f2_pack(rcp, rcp), ns2 = f2_pack(-scale, -scale);
     float f[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 p = BIN ? make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u))
                            : __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-      f[2 * i] = quot(p.x, scale, rcp, fast);
-      f[2 * i + 1] = quot(p.y, scale, rcp, fast);
+      const float2 q = quot2(p, scale, r2, ns2, fast);
+      f[2 * i] = q.x;
+      f[2 * i + 1] = q.y;
     }
     uint2 o;
     if constexpr (KV == PD_KV_FP8_E4M3) {

@@ -96,21 +96,69 @@ cudaError_t once_per_context(unsigned long long (&done)[64], F setup) {
   return cudaSuccess;
 }
 
+// Clusters of c CTAs (2 <= c <= 8) of `kernel` (threads and dynamic shared
+// memory per CTA as given) that the device runs at once
+// (cudaOccupancyMaxActiveClusters), found once per context: counts[c], 0 for
+// c < 2 or when the query fails (then no cluster merge is planned).
+template <class Kern>
+void max_active_clusters(Kern kernel, int threads, int smem, unsigned long long (&ctx_done)[64],
+                         int (&cache)[64][9], int (&counts)[9]) {
+  for (int c = 0; c <= 8; ++c) counts[c] = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
+  const cudaError_t e = once_per_context(ctx_done, [&] {
+    cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (r != cudaSuccess) return r;
+    for (int c = 2; c <= 8; ++c) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(c * 64), 1, 1);
+      cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+      cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();  // the query's own failure: no cluster merge
+        n = 0;
+      }
+      cache[dev][c] = n;
+    }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return;
+  for (int c = 0; c <= 8; ++c) counts[c] = cache[dev][c];
+}
+
 // Launch with programmatic dependent launch: the kernel's CTAs may be
 // scheduled while the preceding grid in the stream drains; the kernel waits
 // (griddepcontrol.wait) before its first global memory access.
+// With cluster > 1 the grid (a multiple of it) runs as clusters of that many
+// CTAs.
 template <class Kern, class... Args>
-cudaError_t launch_pdl(Kern kernel, int grid, int threads, int smem, cudaStream_t stream, const Args&... args) {
+cudaError_t launch_pdl(Kern kernel, int grid, int threads, int smem, cudaStream_t stream, int cluster,
+                       const Args&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
   if (e != cudaSuccess) return e;
   return cudaPeekAtLastError();  // the error stays visible to the caller
@@ -126,7 +174,7 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
                                 Cfg::kSmemBytes);
   });
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_paged_kernel<Cfg>, grid, Cfg::kThreads, Cfg::kSmemBytes, stream, tk, tv, p);
+  return launch_pdl(decode_paged_kernel<Cfg>, grid, Cfg::kThreads, Cfg::kSmemBytes, stream, p.cluster, tk, tv, p);
 }
 
 // Largest ring (stage count, capped at 32) whose shared-memory plan lets
@@ -158,7 +206,9 @@ bool shape_of(KernelShape* out) {
   out->ctas_per_sm = Cfg::kMinBlocks;
   out->heads = Cfg::HG;
   out->unit_cost = 0;
-  for (int c = 0; c <= 8; ++c) out->max_clusters[c] = 0;
+  static unsigned long long ctx_done[64] = {};
+  static int cache[64][9] = {};
+  max_active_clusters(decode_paged_kernel<Cfg>, Cfg::kThreads, Cfg::kSmemBytes, ctx_done, cache, out->max_clusters);
   return true;
 }
 
