@@ -87,6 +87,39 @@ __device__ __forceinline__ float2 quot2(float2 x, float s, unsigned long long r2
   return make_float2(fabsf(a) > 0.f ? a : f2_lo(q0), fabsf(b) > 0.f ? b : f2_hi(q0));
 }
 
+// Minimum / maximum that return NaN when either input is NaN.
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ float min_nan(float a, float b) {
+  float d;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+// int8 code of a quotient t: max(t, -127) (NaN kept), then the conversion's
+// own rounding to the nearest integer (ties to even), saturation at 127 and
+// NaN -> 0. The code is in the low byte.
+__device__ __forceinline__ uint32_t i8_code(float t) {
+  uint32_t d;
+  asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(d) : "f"(max_nan(t, -127.f)));
+  return d;
+}
+// int8 codes of a pair on the fast path: x is first held to [-b, b]
+// (b = 128 |scale|; NaN kept), which changes no code (every quotient beyond
+// +-127.5 saturates) and keeps the residual finite, so the plain residual
+// quotient q1 is the correctly rounded one (the sign of a zero quotient does
+// not matter for an integer code).
+__device__ __forceinline__ uint32_t i8_pair_fast(float2 x, float b, unsigned long long r2,
+                                                 unsigned long long ns2) {
+  const unsigned long long xx = f2_pack(min_nan(max_nan(x.x, -b), b), min_nan(max_nan(x.y, -b), b));
+  const unsigned long long q0 = f2_mul(xx, r2);
+  const unsigned long long e = f2_fma(q0, ns2, xx);
+  const unsigned long long q1 = f2_fma(e, r2, q0);
+  return __byte_perm(i8_code(f2_lo(q1)), i8_code(f2_hi(q1)), 0x0040);
+}
+
 // BIN: the new tokens are bfloat16 (fp16 otherwise); both widen to fp32 exactly.
 template <int KV, bool BIN>
 __device__ __forceinline__ void store_row8(void* cache, long long elem, uint4 x, float scale, float rcp,
@@ -96,6 +129,19 @@ __device__ __forceinline__ void store_row8(void* cache, long long elem, uint4 x,
   } else {
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};
     const unsigned long long r2 = f2_pack(rcp, rcp), ns2 = f2_pack(-scale, -scale);
+    if (KV == PD_KV_INT8 && fast) {
+      const float b = 128.f * fabsf(scale);
+      uint32_t c[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 p = BIN ? make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u))
+                             : __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        c[i] = i8_pair_fast(p, b, r2, ns2);
+      }
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(cache) + elem) =
+          make_uint2(__byte_perm(c[0], c[1], 0x5410), __byte_perm(c[2], c[3], 0x5410));
+      return;
+    }
     float f[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
