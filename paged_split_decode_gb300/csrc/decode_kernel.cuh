@@ -277,6 +277,19 @@ __device__ __forceinline__ void raise_error(uint32_t* flag, uint32_t bit) {
   if (flag) atomicOr(flag, bit);
 }
 
+// The visible tiles [t0, t0 + n) of a sequence of (validated) length L whose
+// query rows are [q0, q0 + qn).
+__device__ __forceinline__ void span_of(const DecodeParams& p, int L, int qn, int& t0, int& n) {
+  if (L == 0 || qn == 0) { t0 = 0; n = 0; return; }
+  int lo = 0;
+  if (p.window > 0) {
+    const int first = L - qn - p.window + 1;  // token 0's first visible key
+    lo = first > 0 ? first : 0;
+  }
+  t0 = lo / kTileKeys;
+  n = (L - 1) / kTileKeys - t0 + 1;
+}
+
 // Visible tile span of sequence b: tiles [t0, t0 + n), and its query rows
 // [q0, q0 + qn). Validates seq_len and the query range.
 __device__ __forceinline__ void seq_span(const DecodeParams& p, int b, bool report, int& L, int& t0,
@@ -288,14 +301,34 @@ __device__ __forceinline__ void seq_span(const DecodeParams& p, int b, bool repo
     L = L < 0 ? 0 : cap;
   }
   seq_queries(p, b, report, q0, qn);
-  if (L == 0 || qn == 0) { t0 = 0; n = 0; return; }
-  int lo = 0;
-  if (p.window > 0) {
-    const int first = L - qn - p.window + 1;  // token 0's first visible key
-    lo = first > 0 ? first : 0;
+  span_of(p, L, qn, t0, n);
+}
+
+// Balanced mode keeps, for batches of up to kSeqCacheB sequences, each
+// sequence's validated (L, q0, qn) in the unused tail of the prefix array
+// (read once from global memory while the prefix is formed), so that a CTA's
+// walk over its pieces issues no dependent global load before its first
+// block-table read.
+constexpr int kSeqCacheB = 256;
+constexpr int kCacheL = kSeqCacheB + 1, kCacheQ0 = 2 * kSeqCacheB + 1, kCacheQn = 3 * kSeqCacheB + 1;
+static_assert(kCacheQn + kSeqCacheB <= kMaxAutoB + 1, "the cache fits in the prefix array");
+__device__ __forceinline__ void seq_cache_put(const DecodeParams& p, int* s_pre, int b, int L, int q0, int qn) {
+  if (p.B <= kSeqCacheB) {
+    s_pre[kCacheL + b] = L;
+    s_pre[kCacheQ0 + b] = q0;
+    s_pre[kCacheQn + b] = qn;
   }
-  t0 = lo / kTileKeys;
-  n = (L - 1) / kTileKeys - t0 + 1;
+}
+__device__ __forceinline__ void seq_span_cached(const DecodeParams& p, const int* s_pre, int b, int& L, int& t0,
+                                                int& n, int& q0, int& qn) {
+  if (p.B > kSeqCacheB) {
+    seq_span(p, b, false, L, t0, n, q0, qn);
+    return;
+  }
+  L = s_pre[kCacheL + b];
+  q0 = s_pre[kCacheQ0 + b];
+  qn = s_pre[kCacheQn + b];
+  span_of(p, L, qn, t0, n);
 }
 
 // Balanced mode: the visible 16-key tiles of all units, laid end to end (T of
@@ -378,7 +411,7 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
       }
       const long long pe = ue < it.g_end ? ue : it.g_end;
       int L, t0, nn, q0, qn;
-      seq_span(p, b, false, L, t0, nn, q0, qn);
+      seq_span_cached(p, s_pre, b, L, t0, nn, q0, qn);
       pc.b = b; pc.kh = grp * p.hg; pc.L = L; pc.unit_t0 = t0; pc.unit = b * p.hgn + grp;
       pc.qlen = qn; pc.R = p.G * qn; pc.q0 = q0;
       pc.first_tile = t0 + static_cast<int>(it.g - rs);
@@ -557,6 +590,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
       if (b < p.B) {
         int L, t0, n, q0, qn;
         seq_span(p, b, blockIdx.x == 0, L, t0, n, q0, qn);
+        seq_cache_put(p, s_pre, b, L, q0, qn);
         v = n > 0 ? (n + p.unit_cost) * p.hgn : 0;
       }
 #pragma unroll

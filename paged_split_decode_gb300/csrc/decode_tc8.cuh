@@ -653,6 +653,7 @@ __global__ void __launch_bounds__(T::kThreads, 1)
       if (b < p.B) {
         int L, t0, n, q0, qn;
         seq_span(p, b, blockIdx.x == 0, L, t0, n, q0, qn);
+        seq_cache_put(p, s_pre, b, L, q0, qn);
         v = n > 0 ? (n + p.unit_cost) * p.hgn : 0;
       }
 #pragma unroll
