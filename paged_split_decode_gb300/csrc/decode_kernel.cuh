@@ -491,7 +491,7 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
 // by its piece.
 template <int D, int RP, int RH, int HG, int NTHREADS>
 __device__ __forceinline__ void cluster_merge_ws(const DecodeParams& p) {
-  constexpr int Q4 = D / 4, SMAX = 8;
+  constexpr int Q4 = D / 4, SMAX = 16;  // the largest cluster
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
   const int S = p.cluster;
   int rank;

@@ -541,7 +541,7 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
 // covered by one piece (or none) was written by its piece.
 template <class T>
 __device__ __forceinline__ void cluster_merge(const DecodeParams& p, uint32_t sbase) {
-  constexpr int D = T::D, Q4 = D / 4, SMAX = 8;
+  constexpr int D = T::D, Q4 = D / 4, SMAX = kMaxCluster;
   const int S = p.cluster;
   const int rank = static_cast<int>(cluster_rank());
   const int u = blockIdx.x / S;
@@ -830,7 +830,7 @@ cudaError_t launch_tc8(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
                        cudaStream_t stream) {
   static unsigned long long attr_ctx[64] = {};
   const cudaError_t e = once_per_context(attr_ctx, [] {
-    return cudaFuncSetAttribute(decode_tc8_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
+    return set_kernel_attributes(decode_tc8_kernel<T>, T::kSmemBytes);
   });
   if (e != cudaSuccess) return e;
   return launch_pdl(decode_tc8_kernel<T>, grid, T::kThreads, T::kSmemBytes, stream, p.cluster, tk, tv, p);
@@ -845,7 +845,7 @@ bool shape_tc8(int nt, KernelShape* out) {
   out->heads = 1;
   out->unit_cost = T::kUnitCost;
   static unsigned long long ctx_done[64] = {};
-  static int cache[64][9] = {};
+  static int cache[64][kMaxCluster + 1] = {};
   max_active_clusters(decode_tc8_kernel<T>, T::kThreads, T::kSmemBytes, ctx_done, cache, out->max_clusters);
   return true;
 }

@@ -16,7 +16,7 @@ struct KernelShape {
   int ctas_per_sm;  // resident CTAs per SM the configuration is sized for
   int heads;        // KV heads per tile (the TMA box's head extent)
   int unit_cost;    // balanced split: virtual tiles charged to every unit start
-  int max_clusters[9];  // [S]: clusters of S CTAs the device runs at once (0: no cluster merge)
+  int max_clusters[17];  // [S]: clusters of S CTAs the device runs at once (0: no cluster merge)
 };
 
 // Returns false when no instantiation covers (D, kv kind, nt, grouped):
@@ -96,20 +96,33 @@ cudaError_t once_per_context(unsigned long long (&done)[64], F setup) {
   return cudaSuccess;
 }
 
-// Clusters of c CTAs (2 <= c <= 8) of `kernel` (threads and dynamic shared
-// memory per CTA as given) that the device runs at once
+// Largest thread-block cluster of a cluster-merged split: 16 CTAs, beyond the
+// portable 8 (each kernel opts in with cudaFuncAttributeNonPortableClusterSizeAllowed).
+constexpr int kMaxCluster = 16;
+
+// A kernel's per-context attributes: its dynamic shared memory opt-in and
+// clusters of up to kMaxCluster CTAs.
+template <class Kern>
+cudaError_t set_kernel_attributes(Kern kernel, int smem) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+}
+
+// Clusters of c CTAs (2 <= c <= kMaxCluster) of `kernel` (threads and dynamic
+// shared memory per CTA as given) that the device runs at once
 // (cudaOccupancyMaxActiveClusters), found once per context: counts[c], 0 for
 // c < 2 or when the query fails (then no cluster merge is planned).
 template <class Kern>
 void max_active_clusters(Kern kernel, int threads, int smem, unsigned long long (&ctx_done)[64],
-                         int (&cache)[64][9], int (&counts)[9]) {
-  for (int c = 0; c <= 8; ++c) counts[c] = 0;
+                         int (&cache)[64][kMaxCluster + 1], int (&counts)[kMaxCluster + 1]) {
+  for (int c = 0; c <= kMaxCluster; ++c) counts[c] = 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
   const cudaError_t e = once_per_context(ctx_done, [&] {
-    cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t r = set_kernel_attributes(kernel, smem);
     if (r != cudaSuccess) return r;
-    for (int c = 2; c <= 8; ++c) {
+    for (int c = 2; c <= kMaxCluster; ++c) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(static_cast<unsigned>(c * 64), 1, 1);
       cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
@@ -131,7 +144,7 @@ void max_active_clusters(Kern kernel, int threads, int smem, unsigned long long 
     return cudaSuccess;
   });
   if (e != cudaSuccess) return;
-  for (int c = 0; c <= 8; ++c) counts[c] = cache[dev][c];
+  for (int c = 0; c <= kMaxCluster; ++c) counts[c] = cache[dev][c];
 }
 
 // Launch with programmatic dependent launch: the kernel's CTAs may be
@@ -170,8 +183,7 @@ cudaError_t launch_cfg(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
                        cudaStream_t stream) {
   static unsigned long long attr_ctx[64] = {};
   cudaError_t e = once_per_context(attr_ctx, [] {
-    return cudaFuncSetAttribute(decode_paged_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Cfg::kSmemBytes);
+    return set_kernel_attributes(decode_paged_kernel<Cfg>, Cfg::kSmemBytes);
   });
   if (e != cudaSuccess) return e;
   return launch_pdl(decode_paged_kernel<Cfg>, grid, Cfg::kThreads, Cfg::kSmemBytes, stream, p.cluster, tk, tv, p);
@@ -207,7 +219,7 @@ bool shape_of(KernelShape* out) {
   out->heads = Cfg::HG;
   out->unit_cost = 0;
   static unsigned long long ctx_done[64] = {};
-  static int cache[64][9] = {};
+  static int cache[64][kMaxCluster + 1] = {};
   max_active_clusters(decode_paged_kernel<Cfg>, Cfg::kThreads, Cfg::kSmemBytes, ctx_done, cache, out->max_clusters);
   return true;
 }

@@ -188,13 +188,14 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
     pl->off_o = cnt + ml;
     pl->bytes = cnt + ml + o;
   }
-  // A fixed split of at most eight pieces per unit, one CTA each, on a kernel
+  // A fixed split of at most kMaxCluster pieces per unit, one CTA each, on a kernel
   // that merges a unit's pieces inside its thread-block cluster (distributed
   // shared memory), when the device runs every unit's cluster at once: no
   // split-combine launch. (The workspace keeps the size computed above, so it
   // does not depend on the device's cluster occupancy.)
   pl->cluster = 0;
-  if (splits >= 2 && splits <= 8 && pl->units * splits == pl->grid && ks.max_clusters[splits] >= pl->units) {
+  if (splits >= 2 && splits <= kMaxCluster && pl->units * splits == pl->grid &&
+      ks.max_clusters[splits] >= pl->units) {
     pl->cluster = splits;
     pl->n_desc = 0;
   }

@@ -83,7 +83,7 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("S", [0, 1, 5])
+@pytest.mark.parametrize("S", [0, 1, 5, 12])
 @pytest.mark.parametrize("name,kw", CASES, ids=[c[0] for c in CASES])
 def test_bf16_matches_oracle(pd, name, kw, S):
     w = inputs.make_workload(kv="bf16", seed=zlib.crc32(name.encode()) % 10000, name=name, **kw)

@@ -482,3 +482,22 @@ CLUSTER = [
 def test_tensor_memory_kernel_cluster_merge(pd, name, kw, S):
     w = inputs.make_workload(seed=zlib.crc32(name.encode()) % 10000 + 3, name=name, **kw)
     check(w, gpu_run(pd, w, S), ref_run(w))
+
+
+# Fixed splits of 9 to 16 pieces on the mma.sync kernels: clusters beyond the
+# portable eight CTAs (the merge reads each unit's partials back from L2 after
+# one cluster barrier); units with fewer tiles than pieces, empty sequences,
+# windows and a bfloat16 cache included.
+WIDE_CLUSTER = [
+    ("f16_d256_gqa6", dict(B=3, Hq=24, Hkv=4, D=256, seq_lens=[4096, 70, 0])),
+    ("f16_d128_gqa4_window", dict(B=2, Hq=32, Hkv=8, D=128, window=900, seq_lens=[3000, 2200])),
+    ("fp8_d256_gqa6", dict(B=2, Hq=24, Hkv=4, D=256, kv="fp8", seq_lens=[5000, 33])),
+    ("int8_d256_q3", dict(B=2, Hq=24, Hkv=4, D=256, kv="int8", qlen=3, seq_lens=[2500, 3])),
+]
+
+
+@pytest.mark.parametrize("S", [9, 12, 16])
+@pytest.mark.parametrize("name,kw", WIDE_CLUSTER, ids=[c[0] for c in WIDE_CLUSTER])
+def test_wide_cluster_merge(pd, name, kw, S):
+    w = inputs.make_workload(seed=zlib.crc32(name.encode()) % 10000 + 5, name=name, **kw)
+    check(w, gpu_run(pd, w, S), ref_run(w))
