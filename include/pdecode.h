@@ -108,8 +108,9 @@ typedef struct {
 /* Workspace bytes that decode_paged needs for these shapes, qlen and
  * num_splits (0 = balanced automatic split) on a device with sm_count SMs
  * (sm_count <= 0: the current device's). 0 means no workspace is needed (the
- * pointer may then be NULL). Layout: one 16-byte split descriptor per work
- * unit (a sequence and a group of KV heads), then the fp32 split partials. Every
+ * pointer may then be NULL). Layout: the fp32 split partials (m and l of
+ * every partial row, then its O row); a split unit's pieces and their slots
+ * follow from the sequence lengths, so nothing else is stored. Every
  * call writes what it later reads, so the buffer needs no initialisation and
  * one buffer serves any sequence of calls on one stream; calls that may run
  * at the same time must not share a workspace. Returns 0 for invalid dims. */
@@ -122,7 +123,10 @@ PD_API int pd_grid_ctas(const pd_dims* dims, int qlen, int num_splits, int sm_co
 /* Paged decode attention, split-K over keys, GQA heads packed per CTA.
  * With a split (num_splits != 1) the call is two launches on `stream`: the
  * decode kernel, then a split-combine kernel launched with programmatic
- * dependent launch that merges the partials of units cut into pieces.
+ * dependent launch that merges the partials of units cut into pieces; a
+ * fixed split of 2 to 16 pieces per unit whose pieces get one CTA each is
+ * instead one launch of thread-block clusters (one per unit) that merge the
+ * pieces themselves, when the device runs all those clusters at once.
  *
  *   q            fp16 [B*qlen, Hq, D] (bfloat16 for PD_KV_BF16, PD_KV_FP8_E4M3_BF16 and
  *                PD_KV_INT8_BF16); row b*qlen + i is query token i of sequence b

@@ -47,9 +47,9 @@ namespace pd {
 
 constexpr int kTileKeys = 16;      // keys per pipeline tile
 constexpr int kMaxAutoB = 1024;    // sequences handled by the balanced split
-// Split units are merged by a second kernel: the workspace opens with one
-// descriptor per unit (its pieces and their slots, or -1 when the unit was not
-// split), written by the unit's first piece, then the partials.
+// Split units are merged by a second kernel, which derives each unit's pieces
+// and their workspace slots from the sequence lengths exactly as the decode
+// kernel's walk cuts them (unit_layout below).
 constexpr uint32_t kErrBlockId = 1u, kErrSeqLen = 2u, kErrTimeout = 4u, kErrQueryStart = 16u;
 // Limit of the producer's final drain: every load it issued lands before the
 // CTA exits, whatever the (possibly short) pipeline wait limit.
@@ -65,8 +65,8 @@ struct DecodeParams {
   int total_q;                // rows of q and out
   float* ws_o;                // [slots, RP, D]   partial O (log2-domain weights)
   float* ws_ml;               // [slots, RP, 2]   partial (m, l), m in log2 units
-  int4* ws_desc;              // [units] {unit, pieces, slot of piece 0, slot base} or unit -1
-  int n_desc;
+  int n_merge;                // units the split combine visits (its grid's x extent; 0: no combine)
+  int decode_grid;            // CTAs of the decode launch (the balanced split's cut)
   int rows_padded;            // RP: rows per partial slot
   uint32_t* error_flag;       // may be null
   int B, qlen, Hq, Hkv, G, R;  // qlen, R: the largest per sequence (R = G*qlen rows per head)
@@ -1209,26 +1209,68 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
           }
         }
     }
-    if (tid == 0 && p.n_desc > 0) {
-      // the first piece of every unit posts the unit's descriptor for the
-      // split combine: its pieces, or -1 when the unit was not split (no
-      // descriptors -- and no workspace -- without a split)
-      const bool first = p.num_splits == 0 ? pc.chunk == pc.first_slot_cta : pc.chunk == 0;
-      if (first) {
-        int4 d = make_int4(-1, 0, 0, 0);
-        if (pc.npieces > 1) {
-          d.x = pc.unit;
-          d.y = pc.npieces;
-          d.z = pc.slot;
-          d.w = p.num_splits == 0 ? 2 * pc.first_slot_cta : pc.slot;
-        }
-        p.ws_desc[pc.unit] = d;
-      }
-    }
     if constexpr (Cfg::kSmemMerge) named_bar_sync(1, Cfg::kConsumerThreads);  // merge buffers free again
   }
   if (!ok && lane == 0) raise_error(p.error_flag, kErrTimeout);
   if (p.cluster > 1) cluster_merge_ws<D, Cfg::RP, Cfg::NT * 8, Cfg::HG, Cfg::kThreads>(p);
+}
+
+// ---------------------------------------------------------------------------
+// The pieces of split unit u as the decode kernel's walk (work_next) cuts
+// them: P pieces, piece 0 in slot slot0, piece k > 0 in slot slot_base + step
+// * k (step 2 balanced, 1 fixed). Balanced mode restates the walk's prefix
+// over the sequences (a block-wide sum of every sequence's unit_cost-charged
+// span before b, and of all of them) and its chunk plan over the decode grid;
+// every thread of the CTA must call it. P <= 1: nothing to merge.
+__device__ __forceinline__ void unit_layout(const DecodeParams& p, int u, long long (&s_red)[2][8], int& P,
+                                            long long& slot0, long long& slot_base) {
+  const int b = u / p.hgn, grp = u % p.hgn;
+  int L, t0, n, q0, qn;
+  seq_span(p, b, false, L, t0, n, q0, qn);
+  if (p.num_splits > 0) {
+    const int S = p.num_splits;
+    const int chunk = (n + S - 1) / S;
+    P = n > 0 ? (n + chunk - 1) / chunk : 0;
+    slot0 = slot_base = static_cast<long long>(u) * S;
+    return;
+  }
+  long long before = 0, total = 0;
+  for (int bb = threadIdx.x; bb < p.B; bb += blockDim.x) {
+    int Lb, tb, nb, qb, qnb;
+    seq_span(p, bb, false, Lb, tb, nb, qb, qnb);
+    const long long v = nb > 0 ? static_cast<long long>(nb + p.unit_cost) * p.hgn : 0;
+    total += v;
+    if (bb < b) before += v;
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    total += __shfl_xor_sync(0xffffffffu, total, o);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    s_red[0][warp] = before;
+    s_red[1][warp] = total;
+  }
+  __syncthreads();
+  before = total = 0;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+    before += s_red[0][w];
+    total += s_red[1][w];
+  }
+  if (n == 0) {
+    P = 0;
+    slot0 = slot_base = 0;
+    return;
+  }
+  const ChunkPlan cp = make_chunk_plan(total, p.decode_grid);
+  const long long span = n + p.unit_cost;
+  const long long us = before + grp * span;
+  const long long rs = us + p.unit_cost, ue = us + span;
+  const int cf = cp.owner(rs), cl = cp.owner(ue - 1);
+  P = cl - cf + 1;
+  slot_base = 2ll * cf;
+  slot0 = slot_base + (cp.start(cf) < rs ? 1 : 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -1237,35 +1279,41 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
 // the decode kernel with programmatic dependent launch: its CTAs may start
 // while the decode grid drains and wait in griddepcontrol.wait until that grid
 // has completed and its writes are visible.
-//   grid (n_desc, C, heads per tile), 256 threads: CTA (e, c, z) merges
-//   head z of descriptor e's unit for output dims [c*D/C, (c+1)*D/C); the
-//   host picks C = D/32 when units are few and split into many pieces, and
-//   C = 1 otherwise. An item is (row, 4 dims). With more than 256 items a
+//   grid (units, C, heads per tile), 256 threads: CTA (u, c, z) merges
+//   head z of unit u for output dims [c*D/C, (c+1)*D/C); the host picks
+//   C = D/32 when units are few and split into many pieces, and C = 1
+//   otherwise. An item is (row, 4 dims). With more than 256 items a
 //   thread merges its items' pieces in order with a running max; with fewer,
 //   thread t covers item t % items for pieces pg, pg+PG, ... (pg = t / items,
 //   PG = 256 / items) and the PG partial states are then merged in pg order.
-//   Either way the result does not depend on scheduling.
+//   Either way the result does not depend on scheduling. The unit's pieces
+//   and their slots are derived from the sequence lengths (inputs the decode
+//   kernel does not write) before the wait, so that the first global read
+//   after it is already a partial.
 template <int D>
 __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float s_m[256], s_l[256];
   __shared__ float4 s_o[256];
-  const int4 d = __ldcg(p.ws_desc + blockIdx.x);
-  const int u = d.x, P = d.y;
-  if (u < 0 || P <= 1) return;
+  __shared__ long long s_red[2][8];
+  const int u = blockIdx.x;
+  int P;
+  long long slot0, slot_base;
+  unit_layout(p, u, s_red, P, slot0, slot_base);
+  const int b = u / p.hgn;
+  int q0, qn;
+  seq_queries(p, b, false, q0, qn);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (P <= 1) return;
   const int step = p.num_splits == 0 ? 2 : 1;
   const int R = p.R, RP = p.rows_padded;
   // blockIdx.z: head of the unit's head group; its rows start at z * rows_head
-  const int b = u / p.hgn, kh = (u % p.hgn) * p.hg + blockIdx.z;
+  const int kh = (u % p.hgn) * p.hg + blockIdx.z;
   const int rbase = blockIdx.z * p.rows_head;
-  int q0, qn;
-  seq_queries(p, b, false, q0, qn);
   const int live_rows = p.G * qn;  // rows of the sequence's query tokens
   // blockIdx.y: which D / gridDim.y output dims; an item is (row, 4 dims)
   const int dims_cta = D / gridDim.y, slices = dims_cta / 4;
   const int items = R * slices;
   const int t = threadIdx.x;
-  const long long slot0 = d.z, slot_base = d.w;
   auto slot_of = [&](int k) -> long long {
     return k == 0 ? slot0 : slot_base + static_cast<long long>(step) * k;
   };

@@ -1,8 +1,8 @@
 // decode_static_scratch.cu -- decode_paged for callers that cannot allocate
 // device memory.
 //
-// decode_paged needs a workspace for its split descriptors and split-K
-// partials, which the caller normally allocates. Some callers cannot: code that runs where
+// decode_paged needs a workspace for its split-K partials, which the caller
+// normally allocates. Some callers cannot: code that runs where
 // cudaMalloc is not allowed (inside a custom allocator's own callbacks, a
 // plugin host that hands out no device buffers, or a process that must not
 // grow its device footprint after start-up). This file gives them one entry

@@ -166,21 +166,6 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) 
   return r;
 }
 
-// Posts a unit's split descriptor from its first piece (as decode_kernel).
-__device__ __forceinline__ void post_unit_descriptor(const DecodeParams& p, const Piece& pc) {
-  if (p.n_desc <= 0) return;
-  const bool first = p.num_splits == 0 ? pc.chunk == pc.first_slot_cta : pc.chunk == 0;
-  if (!first) return;
-  int4 d = make_int4(-1, 0, 0, 0);
-  if (pc.npieces > 1) {
-    d.x = pc.unit;
-    d.y = pc.npieces;
-    d.z = pc.slot;
-    d.w = p.num_splits == 0 ? 2 * pc.first_slot_cta : pc.slot;
-  }
-  p.ws_desc[pc.unit] = d;
-}
-
 // The softmax warps: NG warpgroups share the keys of a block -- thread i of a
 // group owns TMEM lane i (key i of a block for S^T, output dims i and i + 128
 // for O^T) -- and split the query rows: group g takes rows 8 g .. 8 g + 7,
@@ -216,7 +201,6 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
         *reinterpret_cast<uint4*>(p.out + (static_cast<long long>(out.q0 + i) * p.Hq + out.kh * p.G + hl) * D +
                                   dc * 8) = make_uint4(0u, 0u, 0u, 0u);
       }
-      if (tid == 0) post_unit_descriptor(p, out);
     }
     return false;
   };
@@ -524,7 +508,6 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
       else
         __stcg(reinterpret_cast<float2*>(p.ws_ml + (static_cast<long long>(pc.slot) * p.rows_padded + r) * 2), ml);
     }
-    if (tid == 0) post_unit_descriptor(p, pc);
     named_bar_sync(T::kBarAll, NST);  // the row state and red[] are rewritten by the next piece
   }
   if (!ok && lane == 0) raise_error(p.error_flag, kErrTimeout);

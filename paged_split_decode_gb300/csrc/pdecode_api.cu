@@ -66,7 +66,7 @@ struct Plan {
   int nt;           // row tiles per head
   int hg;           // KV heads per tile
   long long slots;  // partial slots in the workspace
-  long long n_desc; // split-combine descriptors
+  long long n_merge; // units the split combine visits
   long long units;  // B * Hkv / hg work units
   int rows_padded;
   int unit_cost;    // balanced split: virtual tiles per unit start
@@ -166,27 +166,25 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
   if (splits == 0) {
     pl->grid = ctas;
     pl->slots = 2ll * ctas;  // a CTA's range holds at most two split pieces
-    pl->n_desc = pl->units;  // one descriptor per unit
+    pl->n_merge = pl->units;
   } else {
     const long long pieces = pl->units * splits;
     pl->grid = static_cast<int>(pieces < ctas ? (pieces > 0 ? pieces : 1) : ctas);
     pl->slots = splits > 1 ? pieces : 0;
-    pl->n_desc = splits > 1 ? pl->units : 0;
+    pl->n_merge = splits > 1 ? pl->units : 0;
   }
   // an automatic plan sizes its workspace for the balanced split, whichever
   // split it chose (so the size does not depend on the window)
   const long long ws_slots = automatic && d->B <= kMaxAutoB ? 2ll * ctas : pl->slots;
-  const long long ws_desc = automatic && d->B <= kMaxAutoB ? pl->units : pl->n_desc;
   if (pl->slots == 0 && ws_slots == 0) {
     pl->off_ml = pl->off_o = pl->bytes = 0;
   } else {
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-    const size_t cnt = up(static_cast<size_t>(ws_desc) * 16);
     const size_t ml = up(static_cast<size_t>(ws_slots) * pl->rows_padded * 2 * 4);
     const size_t o = static_cast<size_t>(ws_slots) * pl->rows_padded * d->D * 4;
-    pl->off_ml = cnt;
-    pl->off_o = cnt + ml;
-    pl->bytes = cnt + ml + o;
+    pl->off_ml = 0;
+    pl->off_o = ml;
+    pl->bytes = ml + o;
   }
   // A fixed split of at most kMaxCluster pieces per unit, one CTA each, on a kernel
   // that merges a unit's pieces inside its thread-block cluster (distributed
@@ -197,7 +195,7 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
   if (splits >= 2 && splits <= kMaxCluster && pl->units * splits == pl->grid &&
       ks.max_clusters[splits] >= pl->units) {
     pl->cluster = splits;
-    pl->n_desc = 0;
+    pl->n_merge = 0;
   }
   return PD_OK;
 }
@@ -353,8 +351,8 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
   p.q_start = q_start;
   p.total_q = total_q;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.ws_desc = pl.bytes ? reinterpret_cast<int4*>(ws) : nullptr;
-  p.n_desc = static_cast<int>(pl.n_desc);
+  p.n_merge = static_cast<int>(pl.n_merge);
+  p.decode_grid = pl.grid;
   p.rows_padded = pl.rows_padded;
   p.ws_ml = pl.bytes ? reinterpret_cast<float*>(ws + pl.off_ml) : nullptr;
   p.ws_o = pl.bytes ? reinterpret_cast<float*>(ws + pl.off_o) : nullptr;
@@ -385,12 +383,12 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
 
   cudaError_t e = launch_decode(dims->D, dims->kv_dtype, pl.nt, pl.hg > 1 ? 1 : 0, tk, tv, p, pl.grid,
                                 static_cast<cudaStream_t>(stream));
-  if (e == cudaSuccess && pl.n_desc > 0) {
+  if (e == cudaSuccess && pl.n_merge > 0) {
     // pieces per split unit: about grid / units + 1 (balanced) or S (fixed);
     // many pieces -> spread a unit's dims over CTAs so threads can share pieces
     const long long per_unit = pl.splits == 0 ? pl.grid / (pl.units > 0 ? pl.units : 1) + 1 : pl.splits;
     const int chunks = per_unit >= 16 ? dims->D / 8 : per_unit >= 4 ? dims->D / 32 : 1;
-    e = launch_split_combine(dims->D, p, static_cast<int>(pl.n_desc), chunks,
+    e = launch_split_combine(dims->D, p, static_cast<int>(pl.n_merge), chunks,
                              static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? PD_OK : PD_ERR_CUDA;

@@ -5,10 +5,10 @@
 
 namespace pd {
 
-cudaError_t launch_split_combine(int D, const DecodeParams& p, int n_desc, int dim_chunks,
+cudaError_t launch_split_combine(int D, const DecodeParams& p, int n_units, int dim_chunks,
                                  cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(n_desc), static_cast<unsigned>(dim_chunks),
+  cfg.gridDim = dim3(static_cast<unsigned>(n_units), static_cast<unsigned>(dim_chunks),
                      static_cast<unsigned>(p.hg));
   cfg.blockDim = dim3(256, 1, 1);
   cfg.dynamicSmemBytes = 0;

@@ -58,33 +58,34 @@ def test_workspace_and_grid_plans(lib):
     d = _dims()
     up = lambda x: (x + 255) // 256 * 256
     # one row tile per head and Hkv % 4 == 0: head-group tiles (fp16 D=256:
-    # two KV heads per tile), one persistent CTA per SM; balanced: one 16-byte
-    # split descriptor per unit (B * Hkv / 2), two partial slots per CTA,
-    # 2 heads x 8 padded rows of D floats per slot
+    # two KV heads per tile), one persistent CTA per SM; balanced: two
+    # partial slots per CTA, 2 heads x 8 padded rows of (m, l) and of D floats
+    # per slot (a unit's pieces follow from the sequence lengths: nothing else
+    # is stored)
     assert binding.grid_ctas(d, 1, 0, sm_count=152) == 152
     ws = binding.workspace_bytes(d, 1, 0, sm_count=152)
-    assert ws == up(64 * 16) + up(304 * 16 * 2 * 4) + 304 * 16 * 256 * 4
+    assert ws == up(304 * 16 * 2 * 4) + 304 * 16 * 256 * 4
     # no split: no workspace at all; one CTA per unit (B * Hkv / 2 units)
     assert binding.workspace_bytes(d, 1, 1, sm_count=152) == 0
     assert binding.grid_ctas(d, 1, 1, sm_count=152) == 64
-    # fixed split: one descriptor per unit, units * S slots
+    # fixed split: units * S slots
     assert binding.workspace_bytes(d, 1, 3, sm_count=152) == \
-        up(64 * 16) + up(192 * 16 * 2 * 4) + 192 * 16 * 256 * 4
+        up(192 * 16 * 2 * 4) + 192 * 16 * 256 * 4
     assert binding.grid_ctas(d, 1, 3, sm_count=152) == 152
     # fp8 D=256: four KV heads per tile, 32 rows per slot, B * Hkv / 4 units
     d8 = _dims(kv_fp8=True)
     assert binding.workspace_bytes(d8, 1, 0, sm_count=152) == \
-        up(32 * 16) + up(304 * 32 * 2 * 4) + 304 * 32 * 256 * 4
+        up(304 * 32 * 2 * 4) + 304 * 32 * 256 * 4
     assert binding.grid_ctas(d8, 1, 1, sm_count=152) == 32
     # per-head tiles (Hkv = 2): two CTAs per SM, 8 padded rows per slot
     d2 = _dims(Hq=12, Hkv=2)
     assert binding.grid_ctas(d2, 1, 0, sm_count=152) == 304
     assert binding.workspace_bytes(d2, 1, 0, sm_count=152) == \
-        up(64 * 16) + up(608 * 8 * 2 * 4) + 608 * 8 * 256 * 4
+        up(608 * 8 * 2 * 4) + 608 * 8 * 256 * 4
     assert binding.grid_ctas(d2, 1, 1, sm_count=152) == 64
     # qlen 3 x G 6 = 18 rows -> three row tiles of 8, per-head tiles
     ws3 = binding.workspace_bytes(_dims(B=8), 3, 0, sm_count=152)
-    assert ws3 == up(32 * 16) + up(608 * 24 * 2 * 4) + 608 * 24 * 256 * 4
+    assert ws3 == up(608 * 24 * 2 * 4) + 608 * 24 * 256 * 4
 
 
 def test_automatic_split_for_few_units(lib):
@@ -95,7 +96,7 @@ def test_automatic_split_for_few_units(lib):
         assert binding.grid_ctas(_dims(B=B), 1, 0, sm_count=152) == units * (128 // units)
         # the workspace stays the balanced split's (two slots per CTA slot)
         assert binding.workspace_bytes(_dims(B=B), 1, 0, sm_count=152) == \
-            up(units * 16) + up(304 * 16 * 2 * 4) + 304 * 16 * 256 * 4
+            up(304 * 16 * 2 * 4) + 304 * 16 * 256 * 4
     # long tables (bandwidth-bound): balanced over every CTA slot
     assert binding.grid_ctas(_dims(B=1, max_blocks_per_seq=2048), 1, 0, sm_count=152) == 152
     assert binding.grid_ctas(_dims(B=8), 1, 0, sm_count=152) == 152

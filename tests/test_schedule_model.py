@@ -5,10 +5,11 @@ visible 16-key tiles of all (sequence, KV head) units are laid end to end and
 cut into equal contiguous ranges; with a fixed split count each unit is cut
 into that many chunks, dealt round robin. This model restates those index
 rules and checks the properties the kernel relies on: every visible tile is
-processed exactly once, the piece count each piece carries (what the unit's
-split descriptor tells the combine) equals the number of pieces the unit is
-cut into, partial slots are distinct and inside the workspace the host sizes,
-and each empty unit gets exactly one zero-fill piece.
+processed exactly once, the piece count and slots that the split combine
+derives for a unit from the prefix alone (all_slots) are those of the pieces
+the walk cuts, in key order, partial slots are distinct and inside the
+workspace the host sizes, and each empty unit gets exactly one zero-fill
+piece.
 """
 import itertools
 import random
@@ -123,15 +124,6 @@ def check(B, Hkv, lens, qlen, window, cap, S, grid, seed=0, cost=0):
                 assert 0 <= pc["slot"] < nslots
                 slots_used.append(pc["slot"])
     assert len(slots_used) == len(set(slots_used)), "two pieces share a slot"
-    # the first piece of every split unit posts the unit's descriptor: one per
-    # CTA range (balanced) or per unit (fixed); no two split units share one
-    posts = {}
-    for u, pcs in units_pieces.items():
-        if pcs[0]["npieces"] > 1:
-            firsts = [pc for pc in pcs if pc["slot"] == pcs[0]["all_slots"][0]]
-            assert len(firsts) == 1, "a split unit needs exactly one first piece"
-            entry = firsts[0]["slot"] // 2 if S == 0 else u
-            assert posts.setdefault(entry, u) == u, "two split units share a descriptor"
     for b, L in enumerate(lens):
         _, t0, n = seq_span(L, qlen, window, cap)
         for kh in range(Hkv):
