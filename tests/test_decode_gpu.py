@@ -210,7 +210,7 @@ def test_stale_block_tail_is_never_read(pd, name, kw, S):
 
 def test_one_workspace_across_changing_shapes(pd):
     """One workspace buffer serves calls of different shapes back to back: every
-    call writes the descriptors and partials it reads."""
+    call writes the partials it reads."""
     import paged_split_decode_gb300 as P
     ws = torch.full((64 << 20,), 0xA5, dtype=torch.uint8, device=DEV)  # garbage start
     ws_list = [inputs.make_workload(B=2, Hq=8, Hkv=8, D=128, seq_lens=[5000, 16384], seed=21),

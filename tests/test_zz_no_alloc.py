@@ -3,9 +3,8 @@
 Callers that cannot allocate device memory (code inside an allocator's
 callbacks, plugin hosts that hand out no device buffers, processes whose
 device footprint is fixed after start-up) use this entry point: it runs the
-same decode as decode_paged but keeps its split descriptors and split-K
-partials in a scratch array built into the library instead of a
-caller-provided workspace.
+same decode as decode_paged but keeps its split-K partials in a scratch
+array built into the library instead of a caller-provided workspace.
 
 The test calls it through the C ABI (ctypes) twice in a row and compares each
 result with decode_paged's on the same inputs and with the fp64 oracle, within
@@ -66,9 +65,8 @@ def _oracle(w):
 
 
 def test_static_scratch_matches_decode_paged_and_the_oracle(lib):
-    # balanced split over every SM: the split descriptors and partials live in
-    # the scratch (fp16 KV; and e4m3 KV with three query tokens, the
-    # tensor-memory kernel)
+    # balanced split over every SM: the split-K partials live in the scratch
+    # (fp16 KV; and e4m3 KV with three query tokens, the tensor-memory kernel)
     cases = [inputs.gqa_d256(2),
              inputs.make_workload(B=5, Hq=32, Hkv=8, D=128, qlen=1,
                                   seq_lens=[3000, 0, 17, 900, 4096], seed=31),
@@ -102,7 +100,7 @@ def test_static_scratch_matches_decode_paged_and_the_oracle(lib):
 
 def test_static_scratch_rejects_plans_beyond_its_size(lib):
     # a fixed split of 8 over 64 sequences x 8 KV heads needs 4096 partial slots
-    # of 8 rows x 256 floats (32 MiB) plus the split descriptors: more than the
+    # of 8 rows x 256 floats (32 MiB) plus their (m, l) pairs: more than the
     # scratch
     w = inputs.make_workload(B=64, Hq=8, Hkv=8, D=256, qlen=1, seq_lens=[64] * 64, seed=32)
     t = _device(w)
