@@ -7,8 +7,11 @@
 // cache per key -- and one CTA per SM holds a deep ring of them; each head has
 // its own consumer warps (DS of them splitting D). The ring takes as many
 // stages as the shared memory allows. The head-group shapes are the ones that
-// measured fastest on GB300.
-#include "launch.h"
+// measured fastest on GB300. Units of 9 to 32 query rows per KV head (two to
+// four row tiles) run on the tensor-memory kernel of decode_tci8.cuh instead:
+// the int8 codes are widened exactly to fp16 operands of tcgen05.mma
+// kind::f16.
+#include "decode_tci8.cuh"
 
 namespace pd {
 namespace {
@@ -18,18 +21,19 @@ constexpr int kD = 256;
 template <int kKv>
 struct Shapes {
   using C1 = CfgFor<kD, kKv, 1, 2, 2>;
-  using C2 = CfgFor<kD, kKv, 2, 1, 2, 1, 1, 2>;
-  using C3 = CfgFor<kD, kKv, 3, 1, 2, 1, 1, 3>;
-  using C4 = CfgFor<kD, kKv, 4, 1, 2, 1, 1, 4>;
+  // two to four row tiles: the tensor-core (tcgen05) kernel, one softmax
+  // warpgroup per row tile
+  template <int NG>
+  using TC = Tci8<kD, q_is_bf16(kKv), NG>;
   using C1H = CfgFor<kD, kKv, 1, 1, 1, 1, 4>;
 
   static bool shape(int nt, int grouped, KernelShape* out) {
     if (grouped) return nt == 1 && shape_of<C1H>(out);
     switch (nt) {
       case 1: return shape_of<C1>(out);
-      case 2: return shape_of<C2>(out);
-      case 3: return shape_of<C3>(out);
-      case 4: return shape_of<C4>(out);
+      case 2: return shape_tci8<TC<2>>(nt, out);
+      case 3: return shape_tci8<TC<3>>(nt, out);
+      case 4: return shape_tci8<TC<4>>(nt, out);
       default: return false;
     }
   }
@@ -39,9 +43,9 @@ struct Shapes {
     if (grouped) return nt == 1 ? launch_cfg<C1H>(tk, tv, p, grid, s) : cudaErrorInvalidValue;
     switch (nt) {
       case 1: return launch_cfg<C1>(tk, tv, p, grid, s);
-      case 2: return launch_cfg<C2>(tk, tv, p, grid, s);
-      case 3: return launch_cfg<C3>(tk, tv, p, grid, s);
-      case 4: return launch_cfg<C4>(tk, tv, p, grid, s);
+      case 2: return launch_tci8<TC<2>>(tk, tv, p, grid, s);
+      case 3: return launch_tci8<TC<3>>(tk, tv, p, grid, s);
+      case 4: return launch_tci8<TC<4>>(tk, tv, p, grid, s);
       default: return cudaErrorInvalidValue;
     }
   }

@@ -166,6 +166,150 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) 
   return r;
 }
 
+// The next piece with visible tiles for the softmax warps (thread index < NST);
+// pieces with nothing visible are finished on the spot: their rows are written
+// as zeros (such a unit is never split).
+template <class T>
+__device__ __forceinline__ bool tc_next_piece(const DecodeParams& p, const int* s_pre, WorkIter& it, Piece& out) {
+  constexpr int D = T::D;
+  while (work_next(p, s_pre, it, out)) {
+    if (out.ntiles > 0) return true;
+    for (int item = threadIdx.x; item < out.R * (D / 8); item += T::kSoftThreads) {
+      const int r = item / (D / 8), dc = item % (D / 8);
+      const int i = r / p.G, hl = r % p.G;
+      *reinterpret_cast<uint4*>(p.out + (static_cast<long long>(out.q0 + i) * p.Hq + out.kh * p.G + hl) * D +
+                                dc * 8) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  return false;
+}
+
+// Scores of key key0 + key for the rows rb .. rb + 7 in the log2 domain: the
+// products times the row factors fs; -inf for keys not loaded (key >= nvalid)
+// or outside a row's visible range [lo, hi] (causal end and window). A block
+// whose keys all lie inside every row's range skips the per-row test.
+template <class T>
+__device__ __forceinline__ void tc_scale_mask(float (&x)[8], const float (&fs)[8], int key0, int nvalid,
+                                              const Piece& pc, const int* ri, int rb, int key) {
+  constexpr int NR = T::kGroupRows;
+  const bool interior = nvalid == 128 && key0 >= pc.tile_lo_all && key0 + 127 <= pc.tile_hi_all;
+  if (interior) {
+#pragma unroll
+    for (int r = 0; r < NR; ++r) x[r] *= fs[r];
+  } else {
+    const int j = key0 + key;
+    const bool loaded = key < nvalid;
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+      x[r] = (loaded && j >= ri[kRowLo * 32 + rb + r] && j <= ri[kRowHi * 32 + rb + r]) ? x[r] * fs[r] : -INFINITY;
+  }
+}
+
+// Running maximum of a softmax group's 8 rows (rows 8 g .. 8 g + 7, the
+// group's named barrier 1 + g), raised to the block maximum only where that
+// exceeds it by more than 2^kRaise. Most blocks raise nothing: one OR-barrier
+// tells, and only then are the block maxima reduced (warp transpose-reduce and
+// a shared exchange). On return mu holds the rows' maxima; the result says
+// whether any row was raised, its factor 2^(old - new) then in kRowAl.
+template <class T>
+__device__ __forceinline__ bool tc_raise_max(const float (&x)[8], float (&mu)[8], float* rf, int* ri, float* red,
+                                             int g, int warp, int lane) {
+  constexpr int NR = T::kGroupRows;
+  const int rb = NR * g, bid = 1 + g;
+  auto load8 = [&](const float* src) {
+#pragma unroll
+    for (int k = 0; k < NR / 4; ++k) {
+      const float4 f = reinterpret_cast<const float4*>(src)[k];
+      mu[4 * k] = f.x; mu[4 * k + 1] = f.y; mu[4 * k + 2] = f.z; mu[4 * k + 3] = f.w;
+    }
+  };
+  load8(rf + kRowMu * 32 + rb);
+  bool upd = false;
+#pragma unroll
+  for (int r = 0; r < NR; ++r) upd |= x[r] > mu[r] + T::kRaise;
+  if (!bar_red_or(bid, 128, upd)) return false;
+  {
+    float v[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) v[r] = x[r];
+    const float m = warp_transpose_reduce<true, NR>(v, lane);
+    if (lane < NR) red[(warp & 3) * NR + lane] = m;
+  }
+  named_bar_sync(bid, 128);
+  if ((warp & 3) == 0 && lane < NR) {
+    const float mx = fmaxf(fmaxf(red[lane], red[NR + lane]), fmaxf(red[2 * NR + lane], red[3 * NR + lane]));
+    const float m0 = rf[kRowMu * 32 + rb + lane];
+    float nmu = m0, al = 1.f;
+    if (mx > m0 + T::kRaise) {
+      nmu = mx;
+      al = (m0 == -INFINITY) ? 0.f : ex2(m0 - mx);
+    }
+    rf[kRowMu * 32 + rb + lane] = nmu;
+    rf[kRowAl * 32 + rb + lane] = al;
+    const bool any = __any_sync((1u << NR) - 1u, al != 1.f);
+    if (lane == 0) ri[kRowFlag * 32 + g] = any ? 1 : 0;
+  }
+  named_bar_sync(bid, 128);
+  load8(rf + kRowMu * 32 + rb);
+  return ri[kRowFlag * 32 + g] != 0;
+}
+
+// End of a piece for softmax group g: the rows' weight sums (this thread's key
+// lane shares lp, reduced over the group), then the output: fp16 / bfloat16
+// rows when the unit is one piece, else the unnormalised O rows and (m, l) --
+// staged in shared memory for a cluster merge, or written to the workspace
+// slot of the piece. o[h][k] is output dim 128 h + key of row 8 g + k.
+template <class T>
+__device__ __forceinline__ void tc_write_piece(const DecodeParams& p, const Piece& pc, const float (&o)[T::kSlabs][8],
+                                               const float (&lp)[8], uint8_t* smem, float* rf, float* red, int g,
+                                               int warp, int lane, int key) {
+  constexpr int D = T::D, S = T::kSlabs, NR = T::kGroupRows;
+  const int rb = NR * g, bid = 1 + g;
+  {
+    float v[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) v[r] = lp[r];
+    const float sum = warp_transpose_reduce<false, NR>(v, lane);
+    if (lane < NR) red[(warp & 3) * NR + lane] = sum;
+  }
+  named_bar_sync(bid, 128);
+  if ((warp & 3) == 0 && lane < NR)
+    rf[kRowL * 32 + rb + lane] = (red[lane] + red[NR + lane]) + (red[2 * NR + lane] + red[3 * NR + lane]);
+  named_bar_sync(bid, 128);
+  const bool direct = pc.npieces == 1;
+#pragma unroll
+  for (int k = 0; k < NR; ++k) {
+    const int r = rb + k;
+    if (r >= pc.R) break;
+    const float L = rf[kRowL * 32 + r];
+    if (direct) {
+      const int i = r / p.G, hl = r % p.G;
+      __half* dst = p.out + (static_cast<long long>(pc.q0 + i) * p.Hq + pc.kh * p.G + hl) * D;
+      const float inv = L > 0.f ? p.out_scale / L : 0.f;
+#pragma unroll
+      for (int h = 0; h < S; ++h)
+        reinterpret_cast<uint16_t*>(dst)[128 * h + key] = pack1<T::QB>(o[h][k] * inv);
+    } else if (p.cluster > 1) {
+      float* dst = reinterpret_cast<float*>(smem) + r * D;  // the staged rows, over the K ring
+#pragma unroll
+      for (int h = 0; h < S; ++h) dst[128 * h + key] = o[h][k];
+    } else {
+      float* dst = p.ws_o + (static_cast<long long>(pc.slot) * p.rows_padded + r) * D;
+#pragma unroll
+      for (int h = 0; h < S; ++h) __stcg(dst + 128 * h + key, o[h][k]);
+    }
+  }
+  if (!direct && key < NR && rb + key < pc.R) {
+    const int r = rb + key;
+    const float mu = rf[kRowMu * 32 + r];
+    const float2 ml = make_float2(mu == -INFINITY ? -INFINITY : mu - T::kBias, rf[kRowL * 32 + r]);
+    if (p.cluster > 1)
+      reinterpret_cast<float2*>(smem + T::kOffStageMl)[r] = ml;
+    else
+      __stcg(reinterpret_cast<float2*>(p.ws_ml + (static_cast<long long>(pc.slot) * p.rows_padded + r) * 2), ml);
+  }
+}
+
 // The softmax warps: NG warpgroups share the keys of a block -- thread i of a
 // group owns TMEM lane i (key i of a block for S^T, output dims i and i + 128
 // for O^T) -- and split the query rows: group g takes rows 8 g .. 8 g + 7,
@@ -181,7 +325,6 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
   const int g = warp >> 2;              // row group
   const int key = tid & 127;            // TMEM lane of this thread
   const int rb = NR * g;                // first row of this group
-  const int bid = 1 + g;                // the group's named barrier (128 threads)
   float* rf = reinterpret_cast<float*>(smem + T::kOffRow);
   int* ri = reinterpret_cast<int*>(smem + T::kOffRow);
   float* red = reinterpret_cast<float*>(smem + T::kOffRed) + 4 * NR * g;  // [4 warps][8 rows]
@@ -190,20 +333,6 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
   const uint32_t tl = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);  // this warp's TMEM lanes
   const uint32_t qs = sbase + T::kOffQ, pt = sbase + T::kOffPt;
   uint32_t bq = 0;
-  // Pieces with nothing visible are finished on the spot (zero rows; such a
-  // unit is never split); returns the next piece that has tiles.
-  auto next_piece = [&](Piece& out) -> bool {
-    while (work_next(p, s_pre, it, out)) {
-      if (out.ntiles > 0) return true;
-      for (int item = tid; item < out.R * (D / 8); item += NST) {
-        const int r = item / (D / 8), dc = item % (D / 8);
-        const int i = r / p.G, hl = r % p.G;
-        *reinterpret_cast<uint4*>(p.out + (static_cast<long long>(out.q0 + i) * p.Hq + out.kh * p.G + hl) * D +
-                                  dc * 8) = make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-    return false;
-  };
   // A piece's q terms (the B operand of S^T: K-major, 128-byte swizzle, the
   // three terms stacked on N), row score factors and visible key limits; the
   // previous piece's S^T products are complete (its softmax read them all).
@@ -290,8 +419,7 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
     }
   };
 
-  while (next_piece(pc)) {
-    const bool direct = pc.npieces == 1;
+  while (tc_next_piece<T>(p, s_pre, it, pc)) {
     const int nblk = (pc.ntiles + T::kBlkTiles - 1) / T::kBlkTiles;
     q_setup(pc);
     named_bar_sync(T::kBarAll, NST);
@@ -328,53 +456,10 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
       tc_fence_before();
       __syncwarp();
       if (ok && lane == 0) mbar_arrive(bar(kBarSEmpty + sb));
-      const int j = key0 + key;
-      const bool interior = nvalid == 128 && key0 >= pc.tile_lo_all && key0 + 127 <= pc.tile_hi_all;
-      if (interior) {
-#pragma unroll
-        for (int r = 0; r < NR; ++r) x[r] *= fs[r];
-      } else {
-        const bool loaded = key < nvalid;
-#pragma unroll
-        for (int r = 0; r < NR; ++r)
-          x[r] = (loaded && j >= ri[kRowLo * 32 + rb + r] && j <= ri[kRowHi * 32 + rb + r]) ? x[r] * fs[r]
-                                                                                         : -INFINITY;
-      }
-      // ---- running maximum per row, raised to the block maximum only where
-      // that exceeds it by more than 2^kRaise. Most blocks raise nothing: one
-      // OR-barrier tells, and only then are the block maxima reduced.
+      tc_scale_mask<T>(x, fs, key0, nvalid, pc, ri, rb, key);
+      // ---- running maximum per row (see tc_raise_max)
       float mu[NR];
-      load8(rf + kRowMu * 32 + rb, mu);
-      bool upd = false;
-#pragma unroll
-      for (int r = 0; r < NR; ++r) upd |= x[r] > mu[r] + T::kRaise;
-      bool rescale = false;
-      if (bar_red_or(bid, 128, upd)) {
-        {
-          float v[NR];
-#pragma unroll
-          for (int r = 0; r < NR; ++r) v[r] = x[r];
-          const float m = warp_transpose_reduce<true, NR>(v, lane);
-          if (lane < NR) red[(warp & 3) * NR + lane] = m;
-        }
-        named_bar_sync(bid, 128);
-        if ((warp & 3) == 0 && lane < NR) {
-          const float mx = fmaxf(fmaxf(red[lane], red[NR + lane]), fmaxf(red[2 * NR + lane], red[3 * NR + lane]));
-          const float m0 = rf[kRowMu * 32 + rb + lane];
-          float nmu = m0, al = 1.f;
-          if (mx > m0 + T::kRaise) {
-            nmu = mx;
-            al = (m0 == -INFINITY) ? 0.f : ex2(m0 - mx);
-          }
-          rf[kRowMu * 32 + rb + lane] = nmu;
-          rf[kRowAl * 32 + rb + lane] = al;
-          const bool any = __any_sync((1u << NR) - 1u, al != 1.f);
-          if (lane == 0) ri[kRowFlag * 32 + g] = any ? 1 : 0;
-        }
-        named_bar_sync(bid, 128);
-        rescale = ri[kRowFlag * 32 + g] != 0;
-        load8(rf + kRowMu * 32 + rb, mu);
-      }
+      const bool rescale = tc_raise_max<T>(x, mu, rf, ri, red, g, warp, lane);
       // ---- weights 2^(x - mu + kBias) (<= 2^8) and the row sums
 #pragma unroll
       for (int r = 0; r < NR; ++r) x[r] = ex2(x[r] - (mu[r] == -INFINITY ? 0.f : mu[r] - T::kBias));
@@ -466,48 +551,7 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
       }
     }
     tc_fence_before();
-    {
-      float v[NR];
-#pragma unroll
-      for (int r = 0; r < NR; ++r) v[r] = lp[r];
-      const float sum = warp_transpose_reduce<false, NR>(v, lane);
-      if (lane < NR) red[(warp & 3) * NR + lane] = sum;
-    }
-    named_bar_sync(bid, 128);
-    if ((warp & 3) == 0 && lane < NR)
-      rf[kRowL * 32 + rb + lane] = (red[lane] + red[NR + lane]) + (red[2 * NR + lane] + red[3 * NR + lane]);
-    named_bar_sync(bid, 128);
-#pragma unroll
-    for (int k = 0; k < NR; ++k) {
-      const int r = rb + k;
-      if (r >= pc.R) break;
-      const float L = rf[kRowL * 32 + r];
-      if (direct) {
-        const int i = r / p.G, hl = r % p.G;
-        __half* dst = p.out + (static_cast<long long>(pc.q0 + i) * p.Hq + pc.kh * p.G + hl) * D;
-        const float inv = L > 0.f ? p.out_scale / L : 0.f;
-#pragma unroll
-        for (int h = 0; h < S; ++h)
-          reinterpret_cast<uint16_t*>(dst)[128 * h + key] = pack1<T::QB>(o[h][k] * inv);
-      } else if (p.cluster > 1) {
-        float* dst = reinterpret_cast<float*>(smem) + r * D;  // the staged rows, over the K ring
-#pragma unroll
-        for (int h = 0; h < S; ++h) dst[128 * h + key] = o[h][k];
-      } else {
-        float* dst = p.ws_o + (static_cast<long long>(pc.slot) * p.rows_padded + r) * D;
-#pragma unroll
-        for (int h = 0; h < S; ++h) __stcg(dst + 128 * h + key, o[h][k]);
-      }
-    }
-    if (!direct && key < NR && rb + key < pc.R) {
-      const int r = rb + key;
-      const float mu = rf[kRowMu * 32 + r];
-      const float2 ml = make_float2(mu == -INFINITY ? -INFINITY : mu - T::kBias, rf[kRowL * 32 + r]);
-      if (p.cluster > 1)
-        reinterpret_cast<float2*>(smem + T::kOffStageMl)[r] = ml;
-      else
-        __stcg(reinterpret_cast<float2*>(p.ws_ml + (static_cast<long long>(pc.slot) * p.rows_padded + r) * 2), ml);
-    }
+    tc_write_piece<T>(p, pc, o, lp, smem, rf, red, g, warp, lane, key);
     named_bar_sync(T::kBarAll, NST);  // the row state and red[] are rewritten by the next piece
   }
   if (!ok && lane == 0) raise_error(p.error_flag, kErrTimeout);
@@ -572,6 +616,110 @@ __device__ __forceinline__ void cluster_merge(const DecodeParams& p, uint32_t sb
   }
 }
 
+// Balanced mode, warp 0: the prefix over sequences of their units' cost
+// (visible tiles plus the per-unit charge, times the head groups), s_pre[b]
+// for b = 0 .. B, and the per-sequence cache of lengths and query ranges.
+__device__ __forceinline__ void tc_balanced_prefix(const DecodeParams& p, int* s_pre, int lane) {
+  int carry = 0;
+  if (lane == 0) s_pre[0] = 0;
+  for (int base = 0; base < p.B; base += 32) {
+    const int b = base + lane;
+    int v = 0;
+    if (b < p.B) {
+      int L, t0, n, q0, qn;
+      seq_span(p, b, blockIdx.x == 0, L, t0, n, q0, qn);
+      seq_cache_put(p, s_pre, b, L, q0, qn);
+      v = n > 0 ? (n + p.unit_cost) * p.hgn : 0;
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (b < p.B) s_pre[b + 1] = carry + v;
+    carry += __shfl_sync(0xffffffffu, v, 31);
+  }
+}
+
+// The producer warps (kProducerWarp: K ring, the next warp: V ring): each
+// TMA-loads the rows of its operand for every block of its CTA's pieces, all
+// boxes of a block at once (lane l: tile l / kSlabs of the block, 128-byte
+// slab l % kSlabs), and waits only for its own ring's empty stages, so K runs
+// ahead of V. Block table entries are read 32 tiles (4 blocks) at a time, the
+// next group in flight. Rings and their barriers: K stages at offset 0, V
+// stages at kOffV; fullK[NBK], emptyK[NBK], fullV[NBV], emptyV[NBV] first in
+// the barrier area.
+template <class T>
+__device__ __forceinline__ void tc_producer_role(const DecodeParams& p, const int* s_pre, WorkIter& it, Piece& pc,
+                                                 const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint32_t sbase,
+                                                 bool& ok) {
+  constexpr int NBK = T::NBK, NBV = T::NBV;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t fullk0 = sbase + T::kOffBars, emptyk0 = fullk0 + 8 * NBK;
+  const uint32_t fullv0 = emptyk0 + 8 * NBK, emptyv0 = fullv0 + 8 * NBV;
+  const bool is_v = warp != T::kProducerWarp;
+  const int nb = is_v ? NBV : NBK;
+  const uint32_t fullb = is_v ? fullv0 : fullk0, emptyb = is_v ? emptyv0 : emptyk0;
+  const uint32_t ringb = sbase + (is_v ? T::kOffV : 0);
+  const CUtensorMap* tm = is_v ? tm_v : tm_k;
+  const uint64_t pol = l2_policy_evict_first();
+  uint32_t bq = 0, posted = 0;  // blocks walked; blocks whose loads were all issued
+  while (work_next(p, s_pre, it, pc)) {
+    if (pc.ntiles == 0) continue;
+    const int nblk = (pc.ntiles + T::kBlkTiles - 1) / T::kBlkTiles;
+    const int32_t* row = p.block_table + static_cast<long long>(pc.b) * p.max_blocks;
+    auto load_group = [&](int t) -> int {
+      int blk = 0;
+      if (t + lane < pc.ntiles) blk = __ldg(row + (pc.first_tile + t + lane) / p.tiles_per_block);
+      return blk;
+    };
+    // block table entries 32 tiles (4 blocks) at a time, the next group in flight
+    int cur = load_group(0), nxt = pc.ntiles > 32 ? load_group(32) : 0;
+    for (int i = 0; i < nblk; ++i) {
+      const int t0 = i * T::kBlkTiles;
+      if (t0 > 0 && t0 % 32 == 0) {
+        cur = nxt;
+        nxt = t0 + 32 < pc.ntiles ? load_group(t0 + 32) : 0;
+      }
+      const uint32_t b = bq + i;
+      const int st = b % nb;
+      const int ntb = min(T::kBlkTiles, pc.ntiles - t0);
+      if (lane == 0) {
+        if (ok && b >= static_cast<uint32_t>(nb)) ok = mbar_wait(emptyb + 8 * st, ((b / nb) - 1) & 1, p.timeout_ns);
+        if (ok && p.inject == 1) ok = false;  // injected fault: the rings stay empty
+        if (ok) {
+          mbar_arrive_expect_tx(fullb + 8 * st, ntb * T::kSlabs * T::kTileBox);
+          posted = b + 1;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      // lane l: tile l / kSlabs of the block, slab l % kSlabs (all boxes at once)
+      const int j = min(lane / T::kSlabs, T::kBlkTiles - 1);
+      int blk = __shfl_sync(0xffffffffu, cur, (t0 % 32) + j);
+      if (!ok) continue;
+      if (lane < T::kSlabs * ntb) {
+        if (blk < 0 || blk >= p.num_blocks) {
+          if (!is_v) raise_error(p.error_flag, kErrBlockId);
+          blk = 0;
+        }
+        const int gt = pc.first_tile + t0 + j;
+        const int z = blk * p.block_size + (gt % p.tiles_per_block) * kTileKeys;
+        const int sl = lane % T::kSlabs;
+        tma_load_3d(ringb + st * T::kKBlk + sl * T::kSlabBlk + j * T::kTileBox, tm, fullb + 8 * st, sl * 128,
+                    pc.kh, z, pol);
+      }
+    }
+    bq += nblk;
+  }
+  if (lane == 0) {
+    if (!ok) raise_error(p.error_flag, kErrTimeout);
+    // every load issued lands before the CTA exits: a block's loads are all
+    // issued once its transaction count is posted
+    for (uint32_t k = posted > static_cast<uint32_t>(nb) ? posted - nb : 0; k < posted; ++k)
+      if (!mbar_wait(fullb + 8 * (k % nb), (k / nb) & 1, kDrainLimitNs)) break;
+  }
+}
+
 template <class T>
 __global__ void __launch_bounds__(T::kThreads, 1)
     decode_tc8_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -626,28 +774,7 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     reinterpret_cast<float2*>(smem + T::kOffStageMl)[threadIdx.x] = make_float2(-INFINITY, 0.f);
   // programmatic dependent launch: no global memory was touched above
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // balanced mode: prefix over sequences of visible tiles (as decode_kernel)
-  if (p.num_splits == 0 && warp == 0) {
-    int carry = 0;
-    if (lane == 0) s_pre[0] = 0;
-    for (int base = 0; base < p.B; base += 32) {
-      const int b = base + lane;
-      int v = 0;
-      if (b < p.B) {
-        int L, t0, n, q0, qn;
-        seq_span(p, b, blockIdx.x == 0, L, t0, n, q0, qn);
-        seq_cache_put(p, s_pre, b, L, q0, qn);
-        v = n > 0 ? (n + p.unit_cost) * p.hgn : 0;
-      }
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += y;
-      }
-      if (b < p.B) s_pre[b + 1] = carry + v;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-  }
+  if (p.num_splits == 0 && warp == 0) tc_balanced_prefix(p, s_pre, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -660,71 +787,7 @@ __global__ void __launch_bounds__(T::kThreads, 1)
   bool ok = true;
 
   if (warp == T::kProducerWarp || warp == T::kProducerWarp + 1) {
-    // --------------------------------------------------------------- producers
-    // warp kProducerWarp fills the K ring, the next warp the V ring: each waits
-    // only for its own ring's empty stages, so K runs ahead of V (a V stage is
-    // held until the P.V product that reads it completes)
-    const bool is_v = warp != T::kProducerWarp;
-    const int nb = is_v ? NBV : NBK;
-    const uint32_t fullb = is_v ? fullv0 : fullk0, emptyb = is_v ? emptyv0 : emptyk0;
-    const uint32_t ringb = sbase + (is_v ? T::kOffV : 0);
-    const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
-    const uint64_t pol = l2_policy_evict_first();
-    uint32_t bq = 0, posted = 0;  // blocks walked; blocks whose loads were all issued
-    while (work_next(p, s_pre, it, pc)) {
-      if (pc.ntiles == 0) continue;
-      const int nblk = (pc.ntiles + T::kBlkTiles - 1) / T::kBlkTiles;
-      const int32_t* row = p.block_table + static_cast<long long>(pc.b) * p.max_blocks;
-      auto load_group = [&](int t) -> int {
-        int blk = 0;
-        if (t + lane < pc.ntiles) blk = __ldg(row + (pc.first_tile + t + lane) / p.tiles_per_block);
-        return blk;
-      };
-      // block table entries 32 tiles (4 blocks) at a time, the next group in flight
-      int cur = load_group(0), nxt = pc.ntiles > 32 ? load_group(32) : 0;
-      for (int i = 0; i < nblk; ++i) {
-        const int t0 = i * T::kBlkTiles;
-        if (t0 > 0 && t0 % 32 == 0) {
-          cur = nxt;
-          nxt = t0 + 32 < pc.ntiles ? load_group(t0 + 32) : 0;
-        }
-        const uint32_t b = bq + i;
-        const int st = b % nb;
-        const int ntb = min(T::kBlkTiles, pc.ntiles - t0);
-        if (lane == 0) {
-          if (ok && b >= static_cast<uint32_t>(nb)) ok = mbar_wait(emptyb + 8 * st, ((b / nb) - 1) & 1, p.timeout_ns);
-          if (ok && p.inject == 1) ok = false;  // injected fault: the rings stay empty
-          if (ok) {
-            mbar_arrive_expect_tx(fullb + 8 * st, ntb * T::kSlabs * T::kTileBox);
-            posted = b + 1;
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        // lane l: tile l / kSlabs of the block, slab l % kSlabs (all boxes at once)
-        const int j = min(lane / T::kSlabs, T::kBlkTiles - 1);
-        int blk = __shfl_sync(0xffffffffu, cur, (t0 % 32) + j);
-        if (!ok) continue;
-        if (lane < T::kSlabs * ntb) {
-          if (blk < 0 || blk >= p.num_blocks) {
-            if (!is_v) raise_error(p.error_flag, kErrBlockId);
-            blk = 0;
-          }
-          const int gt = pc.first_tile + t0 + j;
-          const int z = blk * p.block_size + (gt % p.tiles_per_block) * kTileKeys;
-          const int sl = lane % T::kSlabs;
-          tma_load_3d(ringb + st * T::kKBlk + sl * T::kSlabBlk + j * T::kTileBox, tm, fullb + 8 * st, sl * 128,
-                      pc.kh, z, pol);
-        }
-      }
-      bq += nblk;
-    }
-    if (lane == 0) {
-      if (!ok) raise_error(p.error_flag, kErrTimeout);
-      // every load issued lands before the CTA exits: a block's loads are all
-      // issued once its transaction count is posted
-      for (uint32_t k = posted > static_cast<uint32_t>(nb) ? posted - nb : 0; k < posted; ++k)
-        if (!mbar_wait(fullb + 8 * (k % nb), (k / nb) & 1, kDrainLimitNs)) break;
-    }
+    tc_producer_role<T>(p, s_pre, it, pc, &tm_k, &tm_v, sbase, ok);
   } else if (warp == T::kMmaWarp) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {

@@ -106,6 +106,12 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
                "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
                : "memory");
 }
+// 8 consecutive 32-bit columns of the warp's TMEM lanes from raw words.
+__device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -155,6 +161,50 @@ __device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// Descriptor of an MN-major 16-bit operand in the 128-byte swizzle layout
+// that spans several atoms along M/N: each 128-byte row holds 64 consecutive
+// M/N elements of one k, 8 rows (consecutive k) form a 1024-byte atom, atoms
+// follow each other along K every 1024 bytes (stride byte offset) and the next
+// 64 elements of M/N lie `mn_stride` bytes further (leading byte offset).
+__device__ __forceinline__ uint64_t sdesc_sw128_mn16(uint32_t addr, uint32_t mn_stride) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(mn_stride >> 4) << 16) |
+         (64ull << 32) | (1ull << 46) | (2ull << 61);
+}
+// Descriptor of an MN-major 16-bit operand in the 64-byte swizzle layout, one
+// atom wide: each 64-byte row holds 32 consecutive M/N elements of one k (its
+// 16-byte chunks permuted by chunk ^= (k >> 1) & 3), 8 rows form a 512-byte
+// atom, atoms follow each other along K every 512 bytes; both offset fields
+// hold 512 bytes. Layout type 4 = 64-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc_sw64_mn16(uint32_t addr) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (32ull << 16) | (32ull << 32) | (1ull << 46) |
+         (4ull << 61);
+}
+// Instruction descriptor of kind::f16 with fp16 A and B and fp32 D: D format
+// (bits 4-5) = 1 (f32), A and B formats (7-9, 10-12) = 0 (f16), A MN-major
+// (bit 15), B MN-major (bit 16), N >> 3 (17-22), M >> 4 (24-28).
+constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+// kind::f16: D[tmem] (+)= A[smem] * B[smem]^T (K = 16 per instruction).
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// kind::f16 with A in tensor memory: lane m holds row m of A, column c the
+// element pair (2c, 2c + 1) of its 16 k values (8 columns per instruction).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
 }
 // Arrives (once) on the mbarrier when every tcgen05.mma this thread issued

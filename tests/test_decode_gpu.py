@@ -462,8 +462,8 @@ def test_default_workspace_is_per_stream(pd):
         check(w, got, refs[ws.index(w)])
 
 
-# Fixed splits of two to eight pieces on the tensor-memory kernel (e4m3 KV,
-# 9-32 query rows per KV head): a unit's pieces run as one thread-block
+# Fixed splits of two to eight pieces on the tensor-memory kernels (e4m3 and
+# int8 KV, 9-32 query rows per KV head): a unit's pieces run as one thread-block
 # cluster and merge through distributed shared memory, with no split-combine
 # launch. Sequences with fewer tiles than pieces leave CTAs of a cluster
 # without a piece; empty sequences and tokens that see no key are zero rows.
@@ -474,6 +474,9 @@ CLUSTER = [
                                 seq_lens=[2000, 33])),
     ("rows24_d128_stale", dict(B=3, Hq=8, Hkv=1, D=128, qlen=3, kv="fp8", seq_lens=[5, 301, 4000],
                                stale="nan")),
+    ("rows18_d256_int8", dict(B=4, Hq=24, Hkv=4, D=256, qlen=3, kv="int8", seq_lens=[3000, 40, 0, 2])),
+    ("rows12_d128_int8_window", dict(B=3, Hq=8, Hkv=2, D=128, qlen=3, kv="int8", window=500,
+                                     seq_lens=[2000, 33, 700])),
 ]
 
 
