@@ -136,7 +136,8 @@ __device__ __forceinline__ void split3_e4m3(uint32_t x, uint32_t& t1, uint32_t& 
 }
 
 // Row state arrays in shared memory (32 entries each).
-enum { kRowFsl = 0, kRowMu = 1, kRowAl = 2, kRowLo = 3, kRowHi = 4, kRowL = 5, kRowFlag = 6 };
+// kRowCf (a per-row score offset) is used by the int8 kernel only.
+enum { kRowFsl = 0, kRowMu = 1, kRowAl = 2, kRowLo = 3, kRowHi = 4, kRowL = 5, kRowFlag = 6, kRowCf = 7 };
 // Barriers: fullK[NBK], emptyK[NBK], fullV[NBV], emptyV[NBV], then these.
 enum { kBarSFull = 0, kBarSEmpty = 2, kBarPFull = 4, kBarPvDone = 5, kBarQFull = 6, kBarFinal = 7 };
 
@@ -185,23 +186,25 @@ __device__ __forceinline__ bool tc_next_piece(const DecodeParams& p, const int* 
 }
 
 // Scores of key key0 + key for the rows rb .. rb + 7 in the log2 domain: the
-// products times the row factors fs; -inf for keys not loaded (key >= nvalid)
-// or outside a row's visible range [lo, hi] (causal end and window). A block
-// whose keys all lie inside every row's range skips the per-row test.
-template <class T>
-__device__ __forceinline__ void tc_scale_mask(float (&x)[8], const float (&fs)[8], int key0, int nvalid,
-                                              const Piece& pc, const int* ri, int rb, int key) {
+// products times the row factors fs (plus the row offsets cf with OFF); -inf
+// for keys not loaded (key >= nvalid) or outside a row's visible range [lo, hi]
+// (causal end and window). A block whose keys all lie inside every row's range
+// skips the per-row test.
+template <class T, bool OFF = false>
+__device__ __forceinline__ void tc_scale_mask(float (&x)[8], const float (&fs)[8], const float (&cf)[8], int key0,
+                                              int nvalid, const Piece& pc, const int* ri, int rb, int key) {
   constexpr int NR = T::kGroupRows;
+  auto scaled = [&](int r) { return OFF ? fmaf(x[r], fs[r], cf[r]) : x[r] * fs[r]; };
   const bool interior = nvalid == 128 && key0 >= pc.tile_lo_all && key0 + 127 <= pc.tile_hi_all;
   if (interior) {
 #pragma unroll
-    for (int r = 0; r < NR; ++r) x[r] *= fs[r];
+    for (int r = 0; r < NR; ++r) x[r] = scaled(r);
   } else {
     const int j = key0 + key;
     const bool loaded = key < nvalid;
 #pragma unroll
     for (int r = 0; r < NR; ++r)
-      x[r] = (loaded && j >= ri[kRowLo * 32 + rb + r] && j <= ri[kRowHi * 32 + rb + r]) ? x[r] * fs[r] : -INFINITY;
+      x[r] = (loaded && j >= ri[kRowLo * 32 + rb + r] && j <= ri[kRowHi * 32 + rb + r]) ? scaled(r) : -INFINITY;
   }
 }
 
@@ -456,7 +459,7 @@ __device__ __forceinline__ void softmax_role(const DecodeParams& p, const int* s
       tc_fence_before();
       __syncwarp();
       if (ok && lane == 0) mbar_arrive(bar(kBarSEmpty + sb));
-      tc_scale_mask<T>(x, fs, key0, nvalid, pc, ri, rb, key);
+      tc_scale_mask<T>(x, fs, fs, key0, nvalid, pc, ri, rb, key);
       // ---- running maximum per row (see tc_raise_max)
       float mu[NR];
       const bool rescale = tc_raise_max<T>(x, mu, rf, ri, red, g, warp, lane);

@@ -6,13 +6,16 @@
 // decode_tc8.cuh (the per-head paged decode of opengfx1030/vllm-rdna pull
 // request #33, "Purpose"); the products run on fp16 operands
 // (tcgen05.mma kind::f16, fp32 accumulation):
-//  * The softmax warps widen the int8 codes to fp16 exactly (widen_i8x16).
-//    K of a block goes into tensor memory as the A operand of S^T (lane =
-//    key, the packed fp16 pairs of its row in D / 2 columns, two buffers), one
-//    block ahead of its scores; V of a block goes into an fp16 shared-memory
-//    buffer laid out as the MN-major A operand of O^T += V^T P^T (128-byte
-//    swizzle, 64-dim slabs). An int8 ring stage is released as soon as it is
-//    widened.
+//  * The softmax warps widen the int8 codes to fp16 exactly. K of a block
+//    goes into tensor memory as the A operand of S^T (lane = key, the packed
+//    fp16 pairs of its row in D / 2 columns, two buffers), one block ahead of
+//    its scores, each code x as the integer x + 1152 (widen_i8x16_offset): the
+//    offset adds 1152 * sum(q) to every score of a row, a constant per row
+//    that the score step subtracts again (kRowCf) and to which the softmax is
+//    blind in any case. V of a block goes into an fp16 shared-memory buffer
+//    laid out as the MN-major A operand of O^T += V^T P^T (128-byte swizzle,
+//    64-dim slabs), each code as x itself (widen_i8x16). An int8 ring stage
+//    is released as soon as it is widened.
 //  * q is one fp16 term, scaled per row by a power of two so that its largest
 //    |q| lies in [2^14, 2^15) (exact for an fp16 q; a bfloat16 q keeps its 8
 //    significant bits), the factor folded into the row's score factor.
@@ -69,7 +72,7 @@ struct Tci8 {
   static constexpr int kOffQ = kOffV16 + kV16Bytes;
   static constexpr int kOffPt = kOffQ + kQBytes;
   static constexpr int kOffRed = kOffPt + kPtBytes;        // float [NG groups][4 warps][8 rows]
-  static constexpr int kRowWords = 7 * 32;                 // row state: 7 arrays of 32 words
+  static constexpr int kRowWords = 8 * 32;                 // row state: 8 arrays of 32 words
   static constexpr int kOffRow = kOffRed + NG * 4 * kGroupRows * 4;
   // Cluster merge: each CTA stages its partial (m, l) here and its partial O
   // rows [32][D] fp32 at offset 0, over the K ring, idle once the piece is done.
@@ -102,9 +105,19 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // Sixteen int8 codes (four words, lowest byte first) to sixteen fp16 values,
 // exactly (h[k] holds codes 2k and 2k + 1, the lower one in the low half).
 // The code x, offset to x + 128 in [0, 255] by flipping its sign bit, becomes
-// the low byte of an fp16 whose high byte is 0x64: that is 1024 + x + 128, an
-// integer below 2048 and so exact; subtracting 1152 leaves the integer x,
-// exactly (fp16 represents every integer of magnitude at most 2048).
+// the low byte of an fp16 whose high byte is 0x64: that is 1024 + x + 128 =
+// x + 1152, an integer below 2048 and so exact (widen_i8x16_offset stops
+// here); subtracting 1152 leaves the integer x, exactly (fp16 represents every
+// integer of magnitude at most 2048).
+__device__ __forceinline__ void widen_i8x16_offset(const uint4& w, uint32_t (&h)[8]) {
+  const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t u = in[k] ^ 0x80808080u;
+    h[2 * k] = prmt(u, 0x64646464u, 0x4140u);
+    h[2 * k + 1] = prmt(u, 0x64646464u, 0x4342u);
+  }
+}
 __device__ __forceinline__ void widen_i8x16(const uint4& w, uint32_t (&h)[8]) {
   const uint32_t in[4] = {w.x, w.y, w.z, w.w};
   const uint32_t off2 = 0x64806480u;  // 1152 in both fp16 halves
@@ -147,9 +160,10 @@ __device__ __forceinline__ void softmax_role_i8(const DecodeParams& p, const int
   uint32_t bq = 0;
 
   // K of block b (ring stage b % NBK): this key's chunks c = g, g + NG, ...
-  // widened into the block's tensor-memory buffer (b & 1), columns 8 c ..
-  // 8 c + 7; then the ring stage is released and the buffer marked ready. The
-  // buffer last held block b - 2, whose S^T this warp has already waited for.
+  // widened (offset by 1152) into the block's tensor-memory buffer (b & 1),
+  // columns 8 c .. 8 c + 7; then the ring stage is released and the buffer
+  // marked ready. The buffer last held block b - 2, whose S^T this warp has
+  // already waited for.
   auto widen_k = [&](uint32_t b) {
     const int st = b % NBK;
     if (ok) ok = mbar_wait(fullk0 + 8 * st, (b / NBK) & 1, p.timeout_ns);
@@ -162,7 +176,7 @@ __device__ __forceinline__ void softmax_role_i8(const DecodeParams& p, const int
         const int c = g + NG * k;
         if (c < NCH) {  // warp-uniform
           uint32_t h[8];
-          widen_i8x16(ld_shared_v4(src + (c >> 3) * T::kSlabBlk + (((c & 7) ^ swz) << 4)), h);
+          widen_i8x16_offset(ld_shared_v4(src + (c >> 3) * T::kSlabBlk + (((c & 7) ^ swz) << 4)), h);
           tmem_st8u(dst + 8 * c, h);
         }
       }
@@ -233,6 +247,7 @@ __device__ __forceinline__ void softmax_role_i8(const DecodeParams& p, const int
       const int e = mx > 0.f ? max(-126, min(126, 141 - static_cast<int>((__float_as_uint(mx) >> 23) & 255u)))
                              : 0;
       const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+      float qsum = 0.f;  // the row's sum of its fp16 q values (for the K offset)
 #pragma unroll
       for (int c = 0; c < NW; ++c) {
         const int d0 = part * (D / 8) + 8 * c;
@@ -242,17 +257,23 @@ __device__ __forceinline__ void softmax_role_i8(const DecodeParams& p, const int
         for (int k = 0; k < 4; ++k) {
           const float2 f = pair_to_float2<T::QB>(w[k]);
           h[k] = pack_half2(f.x * up, f.y * up);
+          const float2 hq = __half22float2(*reinterpret_cast<const __half2*>(&h[k]));
+          qsum += hq.x + hq.y;
         }
         st_shared_v4(qs + (d0 >> 6) * T::kQSlab + r * 128 + ((((d0 & 63) >> 3) ^ (r & 7)) << 4), h[0], h[1], h[2],
                      h[3]);
       }
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) qsum += __shfl_xor_sync(0xffffffffu, qsum, o);
       if (part == 0) {
         int lo = 0, hi = -1;
         if (r < pq.R) {
           hi = pq.L - pq.qlen + r / p.G;
           lo = p.window > 0 ? max(0, hi - p.window + 1) : 0;
         }
-        rf[kRowFsl * 32 + r] = r < pq.R ? p.sl2 * __uint_as_float(static_cast<uint32_t>(127 - e) << 23) : 0.f;
+        const float fsl = r < pq.R ? p.sl2 * __uint_as_float(static_cast<uint32_t>(127 - e) << 23) : 0.f;
+        rf[kRowFsl * 32 + r] = fsl;
+        rf[kRowCf * 32 + r] = -1152.f * qsum * fsl;  // minus the K offset's share of every score
         rf[kRowMu * 32 + r] = -INFINITY;
         ri[kRowLo * 32 + r] = lo;
         ri[kRowHi * 32 + r] = hi;
@@ -294,7 +315,10 @@ __device__ __forceinline__ void softmax_role_i8(const DecodeParams& p, const int
 #pragma unroll
         for (int r = 0; r < NR; ++r) x[r] = 0.f;
       }
-      tc_scale_mask<T>(x, fs, key0, nvalid, pc, ri, rb, key);
+      float cf[NR];  // score offset of each row (re-read: registers are scarce)
+#pragma unroll
+      for (int r = 0; r < NR; ++r) cf[r] = rf[kRowCf * 32 + rb + r];
+      tc_scale_mask<T, true>(x, fs, cf, key0, nvalid, pc, ri, rb, key);
       float mu[NR];
       const bool rescale = tc_raise_max<T>(x, mu, rf, ri, red, g, warp, lane);
       // ---- weights 2^(x - mu + kBias) (<= 2^8) rounded to fp16, and the row

@@ -18,10 +18,12 @@ passes while the current phase's parity differs from P, so a phase two
 rounds old is indistinguishable from the one awaited.
 
 Covered: the TMA ring of the mma.sync decode kernel (NS stages, KG key
-groups, W warps per group) and the tensor-memory kernel's K and V rings,
-double-buffered S^T, single P^T buffer, O^T accumulator and q operand. The
-checker must also find the known failure of an odd-depth ring shared by two
-key groups, and planted parity and ordering mistakes.
+groups, W warps per group); the e4m3 tensor-memory kernel's K and V rings,
+double-buffered S^T, single P^T buffer, O^T accumulator and q operand; and
+the int8 tensor-memory kernel, whose softmax groups also widen K into
+double-buffered tensor memory one block ahead and V into a single fp16
+buffer. The checker must also find the known failure of an odd-depth ring
+shared by two key groups, and planted parity and ordering mistakes.
 """
 import random
 
@@ -390,6 +392,202 @@ def test_tensor_memory_kernel_protocol_is_safe(NBK, NBV, NG):
 @pytest.mark.parametrize("mutate", ["skip_pv_wait", "sempty_parity", "early_v_release"])
 def test_tensor_memory_kernel_planted_mistakes_are_caught(mutate):
     msg = find_violation(lambda rng: tc8_case(rng, 2, 3, mutate), range(400))
+    assert msg is not None
+
+
+# ---------------------------------------------------------------------------
+# The int8 tensor-memory kernel: the same K and V producers; each of the NG
+# softmax groups widens its chunks of K block b + 1 into tensor-memory buffer
+# (b + 1) % 2 before reading the scores of block b (block 0 of a piece right
+# after the q set-up), then releases the K stage and arrives on K-ready (count
+# 4 NG per buffer); the MMA issuer computes S^T of block b once K-ready (b % 2)
+# completes -- no S-empty barrier: a group arrives on K-ready of block b + 2
+# only after reading S^T of block b -- and, one block behind, O^T += V16^T P^T.
+# After the previous product completed, each group writes its rows of P^T,
+# widens its chunks of V block b into the single fp16 buffer (releasing the V
+# stage), and arrives on P-full. mutate: "kready_parity" (the issuer waits on
+# the wrong phase), "skip_pv_wait" (P^T and V16 written without waiting for the
+# previous product), "k_two_ahead" (K widened two blocks ahead).
+
+def tci8_roles(NBK, NBV, pieces, rescales, rng, mutate=None, NG=2):
+    fullk, emptyk = [Bar(1) for _ in range(NBK)], [Bar(4 * NG) for _ in range(NBK)]
+    fullv, emptyv = [Bar(1) for _ in range(NBV)], [Bar(4 * NG) for _ in range(NBV)]
+    sfull, kready = [Bar(1), Bar(1)], [Bar(4 * NG), Bar(4 * NG)]
+    pfull, pvdone, qfull = Bar(4 * NG), Bar(1), Bar(1)
+    st = {"K": [None] * NBK, "V": [None] * NBV, "S": [None, None], "P": [None] * NG, "Q": None,
+          "KT": [[None] * NG, [None] * NG], "V16": [None] * NG, "s_read": [0, 0], "o_busy": 0,
+          "loading": 0}
+    inflight, pipe = [], []
+    meet = {"n": 0}
+    nblocks = sum(pieces)
+    mma_done = {"v": False}
+    ahead = 2 if mutate == "k_two_ahead" else 1
+
+    def check(cond, what):
+        if not cond:
+            raise Violation(what)
+
+    def producer(ring, nb, full, empty):
+        for b in range(nblocks):
+            s = b % nb
+            if b >= nb:
+                yield (lambda s=s, par=((b // nb) - 1) & 1: empty[s].passed(par))
+            st[ring][s] = ("loading", b)
+            inflight.append((ring, s, b))
+            yield always
+
+    def producers_done(gen):
+        yield from gen
+        st["loading"] += 1
+
+    def tma():
+        while True:
+            yield (lambda: bool(inflight) or st["loading"] == 2)
+            if not inflight:
+                return
+            ring, s, b = inflight.pop(rng.randrange(len(inflight)))
+            st[ring][s] = b
+            (fullk if ring == "K" else fullv)[s].arrive()
+
+    def mma():
+        bq = 0
+        for p, nblk in enumerate(pieces):
+            yield (lambda par=p & 1: qfull.passed(par))
+            for i in range(nblk + 1):
+                if i < nblk:
+                    b = bq + i
+                    sb = b & 1
+                    par = (b >> 1) & 1
+                    if mutate == "kready_parity":
+                        par ^= 1
+                    yield (lambda sb=sb, par=par: kready[sb].passed(par))
+                    check(st["KT"][sb] == [b] * NG and st["Q"] == p and st["s_read"][sb] == 0,
+                          f"S^T of block {b} issued on K buffer {st['KT'][sb]}, a wrong q or a busy S buffer")
+                    st["S"][sb] = ("computing", b)
+                    pipe.append(("QK", b, sb, p))
+                    pipe.append(("commit", sfull[sb]))
+                if i >= 1:
+                    b = bq + i - 1
+                    yield (lambda par=b & 1: pfull.passed(par))
+                    check(st["P"] == [b] * NG and st["V16"] == [b] * NG and st["o_busy"] == 0,
+                          f"P.V of block {b} issued on P^T {st['P']}, V16 {st['V16']} or a busy O^T")
+                    pipe.append(("PV", b))
+                    pipe.append(("commit", pvdone))
+                yield always
+            bq += nblk
+
+    def mma_role():
+        yield from mma()
+        mma_done["v"] = True
+
+    def tensor_pipe():
+        while True:
+            yield (lambda: bool(pipe) or mma_done["v"])
+            if not pipe:
+                return
+            op = pipe.pop(0)
+            if op[0] == "commit":
+                op[1].arrive()
+            elif op[0] == "QK":
+                _, b, sb, p = op
+                check(st["KT"][sb] == [b] * NG and st["Q"] == p, f"S^T of block {b} read a changed operand")
+                check(st["s_read"][sb] == 0, f"S^T of block {b} written while S buffer {sb} is read")
+                st["S"][sb] = b
+            else:
+                _, b = op
+                check(st["V16"] == [b] * NG and st["P"] == [b] * NG and st["o_busy"] == 0,
+                      f"P.V of block {b} read a changed operand or a busy O^T")
+
+    def rendezvous(target):
+        meet["n"] += 1
+        yield (lambda: meet["n"] >= target)
+
+    def softmax(g):
+        bq, meets = 0, 0
+
+        def widen_k(b):
+            sk = b % NBK
+            yield (lambda sk=sk, par=(b // NBK) & 1: fullk[sk].passed(par))
+            check(st["K"][sk] == b, f"group {g} widened K stage holding {st['K'][sk]} as block {b}")
+            check(not any(op[0] == "QK" and op[2] == (b & 1) for op in pipe),
+                  f"K buffer {b & 1} rewritten for block {b} under an S^T product")
+            st["KT"][b & 1][g] = b
+            yield always
+            emptyk[sk].arrive(4)
+            kready[b & 1].arrive(4)
+
+        for p, nblk in enumerate(pieces):
+            check(not any(op[0] == "QK" for op in pipe), f"q of piece {p} written under an S^T product")
+            if g == 0:
+                st["Q"] = p
+            meets += NG
+            yield from rendezvous(meets)
+            if g == 0:
+                qfull.arrive()
+            for k in range(min(ahead, nblk)):
+                yield from widen_k(bq + k)
+            for i in range(nblk):
+                b = bq + i
+                sb, sv = b & 1, b % NBV
+                if i + ahead < nblk:
+                    yield from widen_k(b + ahead)
+                yield (lambda sb=sb, par=(b >> 1) & 1: sfull[sb].passed(par))
+                check(st["S"][sb] == b, f"group {g} read S buffer {sb} for block {b}: {st['S'][sb]}")
+                st["s_read"][sb] += 1
+                yield always
+                check(st["S"][sb] == b, f"S buffer {sb} changed under block {b}")
+                st["s_read"][sb] -= 1
+                if b >= 1 and mutate != "skip_pv_wait":
+                    yield (lambda par=(b - 1) & 1: pvdone.passed(par))
+                if rescales[b] and i > 0:
+                    check(not any(op[0] == "PV" for op in pipe), "O^T rescaled under a P.V product")
+                    st["o_busy"] += 1
+                    yield always
+                    st["o_busy"] -= 1
+                check(not any(op[0] == "PV" for op in pipe), f"P^T of block {b} written under a P.V product")
+                st["P"][g] = b
+                yield (lambda sv=sv, par=(b // NBV) & 1: fullv[sv].passed(par))
+                check(st["V"][sv] == b, f"group {g} widened V stage holding {st['V'][sv]} as block {b}")
+                check(not any(op[0] == "PV" for op in pipe), f"V16 of block {b} written under a P.V product")
+                st["V16"][g] = b
+                yield always
+                emptyv[sv].arrive(4)
+                pfull.arrive(4)
+                yield always
+            bq += nblk
+            yield (lambda par=(bq - 1) & 1: pvdone.passed(par))
+            check(not any(op[0] == "PV" for op in pipe), "O^T read under a P.V product")
+            st["o_busy"] += 1
+            yield always
+            st["o_busy"] -= 1
+            meets += NG
+            yield from rendezvous(meets)
+
+    roles = {"K": producers_done(producer("K", NBK, fullk, emptyk)),
+             "V": producers_done(producer("V", NBV, fullv, emptyv)), "tma": tma(), "mma": mma_role(),
+             "pipe": tensor_pipe()}
+    for g in range(NG):
+        roles[f"softmax{g}"] = softmax(g)
+    return roles
+
+
+def tci8_case(rng, NBK, NBV, mutate=None, NG=2):
+    pieces = [rng.randint(1, 6) for _ in range(rng.randint(1, 4))]
+    rescales = [rng.random() < 0.3 for _ in range(sum(pieces))]
+    return tci8_roles(NBK, NBV, pieces, rescales, rng, mutate, NG)
+
+
+@pytest.mark.parametrize("NG", [2, 3, 4])
+@pytest.mark.parametrize("NBK,NBV", [(2, 2), (4, 4)])  # D = 256, D = 128
+def test_int8_tensor_memory_kernel_protocol_is_safe(NBK, NBV, NG):
+    for seed in range(200):
+        rng = random.Random(9000 + 10 * NBK + 1000 * NG + seed)
+        run(tci8_case(rng, NBK, NBV, NG=NG), rng)
+
+
+@pytest.mark.parametrize("mutate", ["kready_parity", "skip_pv_wait", "k_two_ahead"])
+def test_int8_tensor_memory_kernel_planted_mistakes_are_caught(mutate):
+    msg = find_violation(lambda rng: tci8_case(rng, 2, 2, mutate), range(400))
     assert msg is not None
 
 
