@@ -356,6 +356,31 @@ __device__ __forceinline__ ChunkPlan make_chunk_plan(long long T, int grid) {
   return cp;
 }
 
+// Balanced mode, warp 0: the prefix over sequences of their units' cost
+// (visible tiles plus the per-unit charge, times the head groups), s_pre[b]
+// for b = 0 .. B, and the per-sequence cache of lengths and query ranges.
+__device__ __forceinline__ void balanced_prefix(const DecodeParams& p, int* s_pre, int lane) {
+  int carry = 0;
+  if (lane == 0) s_pre[0] = 0;
+  for (int base = 0; base < p.B; base += 32) {
+    const int b = base + lane;
+    int v = 0;
+    if (b < p.B) {
+      int L, t0, n, q0, qn;
+      seq_span(p, b, blockIdx.x == 0, L, t0, n, q0, qn);
+      seq_cache_put(p, s_pre, b, L, q0, qn);
+      v = n > 0 ? (n + p.unit_cost) * p.hgn : 0;
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (b < p.B) s_pre[b + 1] = carry + v;
+    carry += __shfl_sync(0xffffffffu, v, 31);
+  }
+}
+
 struct WorkIter {
   ChunkPlan cp;
   long long g, g_end, chunk_start;
@@ -581,27 +606,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
   // completed and its writes are visible (a no-op without one).
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // Balanced mode: prefix over sequences of Hkv * (visible tiles), by warp 0.
-  if (p.num_splits == 0 && warp == 0) {
-    int carry = 0;
-    if (lane == 0) s_pre[0] = 0;
-    for (int base = 0; base < p.B; base += 32) {
-      const int b = base + lane;
-      int v = 0;
-      if (b < p.B) {
-        int L, t0, n, q0, qn;
-        seq_span(p, b, blockIdx.x == 0, L, t0, n, q0, qn);
-        seq_cache_put(p, s_pre, b, L, q0, qn);
-        v = n > 0 ? (n + p.unit_cost) * p.hgn : 0;
-      }
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += y;
-      }
-      if (b < p.B) s_pre[b + 1] = carry + v;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-  }
+  if (p.num_splits == 0 && warp == 0) balanced_prefix(p, s_pre, lane);
   __syncthreads();
 
   WorkIter it;
@@ -1223,7 +1228,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
 // span before b, and of all of them) and its chunk plan over the decode grid;
 // every thread of the CTA must call it. P <= 1: nothing to merge.
 __device__ __forceinline__ void unit_layout(const DecodeParams& p, int u, long long (&s_red)[2][8], int& P,
-                                            long long& slot0, long long& slot_base) {
+                                            long long& slot0, long long& slot_base, int& step) {
   const int b = u / p.hgn, grp = u % p.hgn;
   int L, t0, n, q0, qn;
   seq_span(p, b, false, L, t0, n, q0, qn);
@@ -1232,8 +1237,10 @@ __device__ __forceinline__ void unit_layout(const DecodeParams& p, int u, long l
     const int chunk = (n + S - 1) / S;
     P = n > 0 ? (n + chunk - 1) / chunk : 0;
     slot0 = slot_base = static_cast<long long>(u) * S;
+    step = 1;
     return;
   }
+  step = 2;
   long long before = 0, total = 0;
   for (int bb = threadIdx.x; bb < p.B; bb += blockDim.x) {
     int Lb, tb, nb, qb, qnb;
@@ -1296,15 +1303,14 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
   __shared__ float4 s_o[256];
   __shared__ long long s_red[2][8];
   const int u = blockIdx.x;
-  int P;
+  int P, step;
   long long slot0, slot_base;
-  unit_layout(p, u, s_red, P, slot0, slot_base);
+  unit_layout(p, u, s_red, P, slot0, slot_base, step);
   const int b = u / p.hgn;
   int q0, qn;
   seq_queries(p, b, false, q0, qn);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (P <= 1) return;
-  const int step = p.num_splits == 0 ? 2 : 1;
   const int R = p.R, RP = p.rows_padded;
   // blockIdx.z: head of the unit's head group; its rows start at z * rows_head
   const int kh = (u % p.hgn) * p.hg + blockIdx.z;

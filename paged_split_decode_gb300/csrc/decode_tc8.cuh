@@ -619,31 +619,6 @@ __device__ __forceinline__ void cluster_merge(const DecodeParams& p, uint32_t sb
   }
 }
 
-// Balanced mode, warp 0: the prefix over sequences of their units' cost
-// (visible tiles plus the per-unit charge, times the head groups), s_pre[b]
-// for b = 0 .. B, and the per-sequence cache of lengths and query ranges.
-__device__ __forceinline__ void tc_balanced_prefix(const DecodeParams& p, int* s_pre, int lane) {
-  int carry = 0;
-  if (lane == 0) s_pre[0] = 0;
-  for (int base = 0; base < p.B; base += 32) {
-    const int b = base + lane;
-    int v = 0;
-    if (b < p.B) {
-      int L, t0, n, q0, qn;
-      seq_span(p, b, blockIdx.x == 0, L, t0, n, q0, qn);
-      seq_cache_put(p, s_pre, b, L, q0, qn);
-      v = n > 0 ? (n + p.unit_cost) * p.hgn : 0;
-    }
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += y;
-    }
-    if (b < p.B) s_pre[b + 1] = carry + v;
-    carry += __shfl_sync(0xffffffffu, v, 31);
-  }
-}
-
 // The producer warps (kProducerWarp: K ring, the next warp: V ring): each
 // TMA-loads the rows of its operand for every block of its CTA's pieces, all
 // boxes of a block at once (lane l: tile l / kSlabs of the block, 128-byte
@@ -777,7 +752,7 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     reinterpret_cast<float2*>(smem + T::kOffStageMl)[threadIdx.x] = make_float2(-INFINITY, 0.f);
   // programmatic dependent launch: no global memory was touched above
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (p.num_splits == 0 && warp == 0) tc_balanced_prefix(p, s_pre, lane);
+  if (p.num_splits == 0 && warp == 0) balanced_prefix(p, s_pre, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -893,6 +868,7 @@ bool shape_tc8(int nt, KernelShape* out) {
   out->ctas_per_sm = 1;
   out->heads = 1;
   out->unit_cost = T::kUnitCost;
+  out->fixed_pieces = 1;
   static unsigned long long ctx_done[64] = {};
   static int cache[64][kMaxCluster + 1] = {};
   max_active_clusters(decode_tc8_kernel<T>, T::kThreads, T::kSmemBytes, ctx_done, cache, out->max_clusters);

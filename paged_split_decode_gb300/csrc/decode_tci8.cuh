@@ -317,7 +317,10 @@ __device__ __forceinline__ void softmax_role_i8(const DecodeParams& p, const int
       }
       float cf[NR];  // score offset of each row (re-read: registers are scarce)
 #pragma unroll
-      for (int r = 0; r < NR; ++r) cf[r] = rf[kRowCf * 32 + rb + r];
+      for (int k = 0; k < NR / 4; ++k) {
+        const float4 f = reinterpret_cast<const float4*>(rf + kRowCf * 32 + rb)[k];
+        cf[4 * k] = f.x; cf[4 * k + 1] = f.y; cf[4 * k + 2] = f.z; cf[4 * k + 3] = f.w;
+      }
       tc_scale_mask<T, true>(x, fs, cf, key0, nvalid, pc, ri, rb, key);
       float mu[NR];
       const bool rescale = tc_raise_max<T>(x, mu, rf, ri, red, g, warp, lane);
@@ -445,7 +448,7 @@ __global__ void __launch_bounds__(T::kThreads, 1)
     reinterpret_cast<float2*>(smem + T::kOffStageMl)[threadIdx.x] = make_float2(-INFINITY, 0.f);
   // programmatic dependent launch: no global memory was touched above
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (p.num_splits == 0 && warp == 0) tc_balanced_prefix(p, s_pre, lane);
+  if (p.num_splits == 0 && warp == 0) balanced_prefix(p, s_pre, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -552,6 +555,7 @@ bool shape_tci8(int nt, KernelShape* out) {
   out->ctas_per_sm = 1;
   out->heads = 1;
   out->unit_cost = T::kUnitCost;
+  out->fixed_pieces = 1;
   static unsigned long long ctx_done[64] = {};
   static int cache[64][kMaxCluster + 1] = {};
   max_active_clusters(decode_tci8_kernel<T>, T::kThreads, T::kSmemBytes, ctx_done, cache, out->max_clusters);

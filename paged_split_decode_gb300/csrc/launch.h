@@ -16,6 +16,8 @@ struct KernelShape {
   int ctas_per_sm;  // resident CTAs per SM the configuration is sized for
   int heads;        // KV heads per tile (the TMA box's head extent)
   int unit_cost;    // balanced split: virtual tiles charged to every unit start
+  int fixed_pieces; // 1: a piece has a large fixed cost (set-up, pipeline refill, epilogue), so
+                    // an automatic plan over few units takes the fixed split (one piece per CTA)
   int max_clusters[17];  // [S]: clusters of S CTAs the device runs at once (0: no cluster merge)
 };
 
@@ -217,7 +219,13 @@ bool shape_of(KernelShape* out) {
   out->rows_padded = Cfg::RP;
   out->ctas_per_sm = Cfg::kMinBlocks;
   out->heads = Cfg::HG;
-  out->unit_cost = 0;
+  // a piece's epilogue (partial rows) and the pipeline turn it causes, as
+  // 16-key tiles: ranges that take on a second unit get that many fewer
+  // (measured on GB300, D=256 GQA 6:1 L=4096, 0 -> 4 tiles: B=8 28.8 -> 28.5
+  // us, e4m3 B=32 54.9 -> 54.2 us, L=32768 B=1 30.2 -> 30.0 us, B=32 86.1 ->
+  // 86.0 us; 12 tiles slowed B=32 to 87.2 us)
+  out->unit_cost = 4;
+  out->fixed_pieces = 0;
   static unsigned long long ctx_done[64] = {};
   static int cache[64][kMaxCluster + 1] = {};
   max_active_clusters(decode_paged_kernel<Cfg>, Cfg::kThreads, Cfg::kSmemBytes, ctx_done, cache, out->max_clusters);

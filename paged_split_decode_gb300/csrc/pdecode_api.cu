@@ -120,8 +120,9 @@ int device_sm_count(int sm_count) {
 // except when the units are few (<= a quarter of the CTA slots) and either
 // their work is small (at most 24 visible tiles per CTA slot, from the table
 // capacity and the window: latency-bound, where each piece's fixed cost and
-// the combine's fan-in dominate) or the kernel's pieces carry a fixed cost
-// (the tensor-memory kernel): then a fixed split of each unit into
+// the combine's fan-in dominate) or the kernel's pieces carry a large fixed
+// cost (the tensor-memory kernels, KernelShape::fixed_pieces): then a fixed
+// split of each unit into
 // floor(0.84 CTA slots / units) chunks, one per CTA, which leaves about a
 // sixth of the SMs idle but gives every CTA one piece. Measured on GB300
 // (D=256 GQA 6:1, L=4096): B = 1 / 2 / 3 12.9 / 16.1 / 19.2 -> 12.0 / 15.0 /
@@ -159,7 +160,7 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
     const long long cap_keys = static_cast<long long>(d->max_blocks_per_seq) * d->block_size;
     const long long vis_keys = window > 0 ? std::min<long long>(cap_keys, window + qlen + kTileKeys) : cap_keys;
     const long long tiles = pl->units * (vis_keys / kTileKeys + 1);
-    if (tiles <= 24ll * ctas || ks.unit_cost > 0)
+    if (tiles <= 24ll * ctas || ks.fixed_pieces)
       splits = static_cast<int>(std::max<long long>(1, (ctas * 27 / 32) / pl->units));
   }
   pl->splits = splits;

@@ -80,6 +80,8 @@ CASES = [
                               seq_lens=[2, 2000, 800])),
     ("rows_32_d128", dict(B=2, Hq=16, Hkv=2, D=128, qlen=4, seq_lens=[900, 33])),
     ("stale_nan_tails", dict(B=3, Hq=24, Hkv=4, D=256, seq_lens=[17, 1001, 250], stale="nan")),
+    # two long sequences on a large table: many pieces per unit
+    ("two_long_sequences", dict(B=2, Hq=24, Hkv=4, D=256, seq_lens=[9000, 9000], max_blocks_per_seq=1024)),
 ]
 
 

@@ -184,6 +184,33 @@ def test_edge_cases(pd, name, kw, S):
     check(w, gpu_run(pd, w, S), ref_run(w))
 
 
+# Automatic plans with few units on large block tables (the balanced cut over
+# every CTA, several pieces per unit): equal lengths, equal tile counts with
+# unequal lengths, one longer sequence, windows, byte caches and two row tiles
+# per head (a bfloat16 cache: test_bf16_gpu.py).
+FEW_UNITS = [
+    ("f16_d256_gqa6_b8", dict(B=8, Hq=24, Hkv=4, D=256, seq_lens=[1000] * 8, max_blocks_per_seq=512)),
+    ("f16_d256_equal_tiles_unequal_lens", dict(B=8, Hq=24, Hkv=4, D=256, seq_lens=[1000] * 7 + [993],
+                                               max_blocks_per_seq=512)),
+    ("f16_d256_one_longer", dict(B=8, Hq=24, Hkv=4, D=256, seq_lens=[1000] * 7 + [1100],
+                                 max_blocks_per_seq=512)),
+    ("fp8_d256_gqa6_b16", dict(B=16, Hq=24, Hkv=4, D=256, kv="fp8", seq_lens=[600] * 16,
+                               max_blocks_per_seq=512)),
+    ("int8_d128_b8_window", dict(B=8, Hq=32, Hkv=8, D=128, kv="int8", window=4000, seq_lens=[6000] * 8,
+                                 max_blocks_per_seq=512)),
+    ("fp8_d256_gqa6_b32", dict(B=32, Hq=24, Hkv=4, D=256, kv="fp8", seq_lens=[600] * 32,
+                               max_blocks_per_seq=256)),
+    ("f16_d256_b2_long", dict(B=2, Hq=24, Hkv=4, D=256, seq_lens=[9000, 9000], max_blocks_per_seq=1024)),
+    ("f16_d256_qlen2_b4", dict(B=4, Hq=24, Hkv=4, D=256, qlen=2, seq_lens=[3000] * 4, max_blocks_per_seq=512)),
+]
+
+
+@pytest.mark.parametrize("name,kw", FEW_UNITS, ids=[e[0] for e in FEW_UNITS])
+def test_few_units_on_large_tables(pd, name, kw):
+    w = inputs.make_workload(seed=zlib.crc32(name.encode()) % 10000 + 11, name=name, **kw)
+    check(w, gpu_run(pd, w, 0), ref_run(w))
+
+
 STALE = [
     ("f16_rows_6", dict(B=4, Hq=24, Hkv=4, D=256, seq_lens=[1, 17, 4001, 250])),
     ("f16_rows_18_window", dict(B=3, Hq=24, Hkv=4, D=256, qlen=3, window=100,
