@@ -1,8 +1,8 @@
 """Caches larger than 4 GiB. The blocks a decode call reads, and the slots
 the writer stores, sit past the first 4 GiB of each cache tensor, so a 32-bit
 byte offset anywhere (kernels, tensor maps, writer) would touch the wrong
-place. The decode runs the head-group fp16 kernel, the per-head int8 kernel
-with three row tiles and the tensor-memory fp8 kernel. The oracle sees the
+place. The decode runs the head-group fp16 kernel and the tensor-memory int8
+and fp8 kernels (three row tiles). The oracle sees the
 same blocks gathered into a compact pool: the output does not depend on where
 the blocks sit (the oracle's block-permutation invariance)."""
 import numpy as np
