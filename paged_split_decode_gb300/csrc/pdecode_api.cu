@@ -71,6 +71,7 @@ struct Plan {
   int rows_padded;
   int unit_cost;    // balanced split: virtual tiles per unit start
   int cluster;      // > 1: the fixed split's pieces of a unit form a cluster that merges them
+  int sms;          // SMs of the device the plan was made for
   size_t off_ml, off_o, bytes;  // workspace layout
 };
 
@@ -138,6 +139,7 @@ pd_status make_plan(const pd_dims* d, int qlen, int num_splits, int sm_count, Pl
   if (num_splits < 0) return PD_ERR_SHAPE;
   const int sms = device_sm_count(sm_count);
   if (sms <= 0) return PD_ERR_CUDA;
+  pl->sms = sms;
   const int R = d->Hq / d->Hkv * qlen;
   pl->nt = (R + 7) / 8;
   KernelShape ks;
@@ -386,9 +388,17 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
                                 static_cast<cudaStream_t>(stream));
   if (e == cudaSuccess && pl.n_merge > 0) {
     // pieces per split unit: about grid / units + 1 (balanced) or S (fixed);
-    // many pieces -> spread a unit's dims over CTAs so threads can share pieces
+    // many pieces -> spread a unit's dims over CTAs so threads can share pieces,
+    // but keep the combine grid within one CTA per SM: those CTAs are resident
+    // beside the decode grid and do their pre-wait work (the unit's piece
+    // layout) while it runs, where CTAs beyond that start only as decode CTAs
+    // exit and add that work to the tail (measured on GB300, D=256 GQA 6:1:
+    // B = 2 / 3 / 8 15.0 / 17.6 / 28.9 -> 13.9 / 16.7 / 28.6 us, e4m3 B = 32
+    // 54.1 -> 52.5, L = 32768 B = 2 47.2 -> 45.8, windowed B = 2 14.7 ->
+    // 13.7; D=128 (28,4) ragged 86.5 -> 87.0; B = 1 and B = 32 unchanged)
     const long long per_unit = pl.splits == 0 ? pl.grid / (pl.units > 0 ? pl.units : 1) + 1 : pl.splits;
-    const int chunks = per_unit >= 16 ? dims->D / 8 : per_unit >= 4 ? dims->D / 32 : 1;
+    int chunks = per_unit >= 16 ? dims->D / 8 : per_unit >= 4 ? dims->D / 32 : 1;
+    while (chunks > 1 && pl.n_merge * chunks * pl.hg > pl.sms) chunks >>= 1;
     e = launch_split_combine(dims->D, p, static_cast<int>(pl.n_merge), chunks,
                              static_cast<cudaStream_t>(stream));
   }
