@@ -339,13 +339,28 @@ __device__ __forceinline__ void seq_span_cached(const DecodeParams& p, const int
 // tiles; a range's virtual tiles do no work. (A dynamic tail -- small
 // chunks taken from a global counter -- was measured and lost: every chunk
 // costs a key-group merge, a partial and a deeper combine tree.)
+// start(k) = floor(T k / Ce) and owner(x) = max{k : start(k) <= x} =
+// floor(((x + 1) Ce - 1) / T) in exact integer arithmetic, without 64-bit
+// divisions (slow on the GPU, and on the path to a CTA's first load): with
+// T = q Ce + r, floor(T k / Ce) = q k + floor(r k / Ce), and r k < Ce^2 fits
+// 32 bits; owner starts from a single-precision estimate of x Ce / T and
+// steps to the exact index along the monotone start().
 struct ChunkPlan {
   long long T;
   int Ce;
-  __device__ __forceinline__ long long start(int k) const { return T * k / Ce; }
-  __device__ __forceinline__ long long end(int k) const { return T * (k + 1) / Ce; }
+  long long q;  // T / Ce
+  int r;        // T % Ce
+  __device__ __forceinline__ long long start(int k) const {
+    return q * k + static_cast<long long>(static_cast<unsigned>(r) * static_cast<unsigned>(k) /
+                                          static_cast<unsigned>(Ce));
+  }
+  __device__ __forceinline__ long long end(int k) const { return start(k + 1); }
   __device__ __forceinline__ int owner(long long x) const {
-    return static_cast<int>(((x + 1) * Ce - 1) / T);
+    int k = static_cast<int>(static_cast<float>(x) * (static_cast<float>(Ce) / static_cast<float>(T)));
+    k = k < 0 ? 0 : (k > Ce - 1 ? Ce - 1 : k);
+    while (k > 0 && start(k) > x) --k;
+    while (k < Ce - 1 && start(k + 1) <= x) ++k;
+    return k;
   }
 };
 
@@ -353,6 +368,8 @@ __device__ __forceinline__ ChunkPlan make_chunk_plan(long long T, int grid) {
   ChunkPlan cp;
   cp.T = T;
   cp.Ce = T <= 0 ? 0 : static_cast<int>(T < grid ? T : grid);
+  cp.q = cp.Ce > 0 ? T / cp.Ce : 0;
+  cp.r = cp.Ce > 0 ? static_cast<int>(T - cp.q * cp.Ce) : 0;
   return cp;
 }
 
@@ -426,7 +443,7 @@ __device__ __forceinline__ bool work_next(const DecodeParams& p, const int* s_pr
       const int b = it.b;
       const int span = (s_pre[b + 1] - s_pre[b]) / p.hgn;  // unit_cost + visible tiles
       const long long off = it.g - s_pre[b];
-      const int grp = static_cast<int>(off / span);
+      const int grp = static_cast<int>(off) / span;        // the prefix is int: off < 2^31
       const long long us = s_pre[b] + static_cast<long long>(grp) * span;
       const long long rs = us + p.unit_cost;  // the unit's first real tile
       const long long ue = us + span;

@@ -198,3 +198,37 @@ def test_schedule_random():
         grid = rng.choice([1, 2, 5, 16, 152])
         cost = rng.choice([0, 0, 16, rng.randint(1, 200)]) if S == 0 else 0
         check(B, Hkv, lens, qlen, window, 1 << 20, S, grid, seed=rng.randrange(1 << 30), cost=cost)
+
+
+def chunk_start_qr(T, Ce, k):
+    """The kernel's start(k): floor(T k / Ce) as q k + floor(r k / Ce)."""
+    q, r = divmod(T, Ce)
+    return q * k + (r * k) // Ce
+
+
+def chunk_owner_stepped(T, Ce, x):
+    """The kernel's owner(x): a single-precision estimate of x Ce / T, then
+    steps along start() to the largest k with start(k) <= x."""
+    import numpy as np
+    k = int(np.float32(x) * (np.float32(Ce) / np.float32(T)))
+    k = min(max(k, 0), Ce - 1)
+    while k > 0 and chunk_start_qr(T, Ce, k) > x:
+        k -= 1
+    while k < Ce - 1 and chunk_start_qr(T, Ce, k + 1) <= x:
+        k += 1
+    return k
+
+
+def test_chunk_plan_arithmetic_matches_the_division_form():
+    rng = random.Random(5)
+    cases = [(1, 1), (7, 7), (152, 152), (153, 152), (2 ** 31 - 1, 152), (2 ** 31 - 1, 304),
+             (4112, 152), (4176, 152), (67_000_000, 304)]
+    cases += [(rng.randint(1, 2 ** 31 - 1), rng.randint(1, 304)) for _ in range(300)]
+    for T, grid in cases:
+        Ce = min(T, grid)
+        for k in set([0, 1, Ce - 1, Ce] + [rng.randint(0, Ce) for _ in range(20)]):
+            assert chunk_start_qr(T, Ce, k) == T * k // Ce
+        xs = [0, T - 1] + [rng.randint(0, T - 1) for _ in range(40)]
+        xs += [T * k // Ce + d for k in range(min(Ce, 8)) for d in (-1, 0, 1) if 0 <= T * k // Ce + d < T]
+        for x in xs:
+            assert chunk_owner_stepped(T, Ce, x) == ((x + 1) * Ce - 1) // T, (T, Ce, x)
