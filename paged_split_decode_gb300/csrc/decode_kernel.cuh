@@ -1297,6 +1297,48 @@ __device__ __forceinline__ void unit_layout(const DecodeParams& p, int u, long l
   slot0 = slot_base + (cp.start(cf) < rs ? 1 : 0);
 }
 
+// The split combine's running merge of pieces k0, k0 + stride, ... (< P) of
+// one item (row r of the head whose rows start at rbase, dims dim0 .. dim0 +
+// 3) into (m_run, l_run, acc), in piece order; the partials of NB pieces are
+// loaded at a time, all in flight at once. Piece k sits in slot slot0 (k = 0)
+// or slot_base + step * k.
+template <int D, int NB>
+__device__ __forceinline__ void merge_pieces(const DecodeParams& p, int P, long long slot0, long long slot_base,
+                                             int step, int rbase, int r, int dim0, int k0, int stride,
+                                             float& m_run, float& l_run, float4& acc) {
+  const int RP = p.rows_padded;
+  for (; k0 < P; k0 += NB * stride) {
+    float2 ml[NB];
+    float4 v[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const int k = k0 + j * stride;
+      if (k < P) {
+        const long long sl = k == 0 ? slot0 : slot_base + static_cast<long long>(step) * k;
+        ml[j] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (sl * RP + rbase + r) * 2));
+        v[j] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sl * RP + rbase + r) * D + dim0));
+      } else {
+        ml[j] = make_float2(-INFINITY, 0.f);
+        v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const float mk = ml[j].x;
+      if (mk == -INFINITY) continue;
+      if (mk > m_run) {
+        const float sc = (m_run == -INFINITY) ? 0.f : ex2(m_run - mk);
+        l_run *= sc;
+        acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+        m_run = mk;
+      }
+      const float w = ex2(mk - m_run);
+      l_run += w * ml[j].y;
+      acc.x += w * v[j].x; acc.y += w * v[j].y; acc.z += w * v[j].z; acc.w += w * v[j].w;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Split combine: merges the fp32 (m, l, O) partials of every unit the decode
 // kernel split into pieces (m in log2 units, O relative to m). Launched after
@@ -1310,11 +1352,13 @@ __device__ __forceinline__ void unit_layout(const DecodeParams& p, int u, long l
 //   thread merges its items' pieces in order with a running max; with fewer,
 //   thread t covers item t % items for pieces pg, pg+PG, ... (pg = t / items,
 //   PG = 256 / items) and the PG partial states are then merged in pg order.
-//   Either way the result does not depend on scheduling. The unit's pieces
+//   Either way the result does not depend on scheduling; NB pieces' partials
+//   are loaded at a time (the host takes NB = 8 when units have more than
+//   four pieces, else 4, whose kernel needs fewer registers). The unit's pieces
 //   and their slots are derived from the sequence lengths (inputs the decode
 //   kernel does not write) before the wait, so that the first global read
 //   after it is already a partial.
-template <int D>
+template <int D, int NB>
 __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p) {
   __shared__ float s_m[256], s_l[256];
   __shared__ float4 s_o[256];
@@ -1335,7 +1379,7 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
   seq_queries(p, b, false, q0, qn);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (P <= 1) return;
-  const int R = p.R, RP = p.rows_padded;
+  const int R = p.R;
   // blockIdx.z: head of the unit's head group; its rows start at z * rows_head
   const int kh = (u % p.hgn) * p.hg + blockIdx.z;
   const int rbase = blockIdx.z * p.rows_head;
@@ -1344,42 +1388,6 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
   const int dims_cta = D / gridDim.y, slices = dims_cta / 4;
   const int items = R * slices;
   const int t = threadIdx.x;
-  auto slot_of = [&](int k) -> long long {
-    return k == 0 ? slot0 : slot_base + static_cast<long long>(step) * k;
-  };
-  // running merge of pieces k0, k0 + stride, ... of one item into (m, l, acc)
-  auto merge = [&](int r, int dim0, int k0, int stride, float& m_run, float& l_run, float4& acc) {
-    for (; k0 < P; k0 += 4 * stride) {
-      float2 ml[4];
-      float4 v[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int k = k0 + j * stride;
-        if (k < P) {
-          const long long sl = slot_of(k);
-          ml[j] = __ldcg(reinterpret_cast<const float2*>(p.ws_ml + (sl * RP + rbase + r) * 2));
-          v[j] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sl * RP + rbase + r) * D + dim0));
-        } else {
-          ml[j] = make_float2(-INFINITY, 0.f);
-          v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float mk = ml[j].x;
-        if (mk == -INFINITY) continue;
-        if (mk > m_run) {
-          const float sc = (m_run == -INFINITY) ? 0.f : ex2(m_run - mk);
-          l_run *= sc;
-          acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
-          m_run = mk;
-        }
-        const float w = ex2(mk - m_run);
-        l_run += w * ml[j].y;
-        acc.x += w * v[j].x; acc.y += w * v[j].y; acc.z += w * v[j].z; acc.w += w * v[j].w;
-      }
-    }
-  };
   auto store = [&](int r, int dim0, float L, float4 o) {
     const float inv = (L > 0.f) ? p.out_scale / L : 0.f;
     const int i = r / p.G, hl = r % p.G;
@@ -1402,7 +1410,7 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
       if (r >= live_rows) continue;
       float m_run = -INFINITY, l_run = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      merge(r, dim0, 0, 1, m_run, l_run, acc);
+      merge_pieces<D, NB>(p, P, slot0, slot_base, step, rbase, r, dim0, 0, 1, m_run, l_run, acc);
       store(r, dim0, l_run, acc);
     }
     return;
@@ -1415,7 +1423,8 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
   const bool live = r < live_rows;
   float m_run = -INFINITY, l_run = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (pg < PG && live) merge(r, dim0, pg, PG, m_run, l_run, acc);
+  if (pg < PG && live)
+    merge_pieces<D, NB>(p, P, slot0, slot_base, step, rbase, r, dim0, pg, PG, m_run, l_run, acc);
   s_m[t] = m_run;
   s_l[t] = l_run;
   s_o[t] = acc;

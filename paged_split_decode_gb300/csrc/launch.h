@@ -32,8 +32,10 @@ cudaError_t launch_decode(int D, int kv, int nt, int grouped, const CUtensorMap&
                           cudaStream_t stream);
 
 // Split combine behind a decode launch (split_combine.cu); each split unit's
-// output dims are spread over dim_chunks CTAs per head (a divisor of D / 4).
-cudaError_t launch_split_combine(int D, const DecodeParams& p, int n_units, int dim_chunks,
+// output dims are spread over dim_chunks CTAs per head (a divisor of D / 4);
+// batch > 4 selects the kernel that loads eight pieces' partials at a time
+// (else four).
+cudaError_t launch_split_combine(int D, const DecodeParams& p, int n_units, int dim_chunks, int batch,
                                  cudaStream_t stream);
 
 // Per-dtype/head-size entry points defined in decode_*.cu.

@@ -5,7 +5,7 @@
 
 namespace pd {
 
-cudaError_t launch_split_combine(int D, const DecodeParams& p, int n_units, int dim_chunks,
+cudaError_t launch_split_combine(int D, const DecodeParams& p, int n_units, int dim_chunks, int batch,
                                  cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(n_units), static_cast<unsigned>(dim_chunks),
@@ -19,10 +19,13 @@ cudaError_t launch_split_combine(int D, const DecodeParams& p, int n_units, int 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
+  const bool wide = batch > 4;
   if (D == 128)
-    e = cudaLaunchKernelEx(&cfg, split_combine_kernel<128>, p);
+    e = wide ? cudaLaunchKernelEx(&cfg, split_combine_kernel<128, 8>, p)
+             : cudaLaunchKernelEx(&cfg, split_combine_kernel<128, 4>, p);
   else
-    e = cudaLaunchKernelEx(&cfg, split_combine_kernel<256>, p);
+    e = wide ? cudaLaunchKernelEx(&cfg, split_combine_kernel<256, 8>, p)
+             : cudaLaunchKernelEx(&cfg, split_combine_kernel<256, 4>, p);
   if (e != cudaSuccess) return e;
   return cudaPeekAtLastError();
 }
