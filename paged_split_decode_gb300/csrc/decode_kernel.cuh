@@ -1244,7 +1244,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, Cfg::kMinBlocks)
 // over the sequences (a block-wide sum of every sequence's unit_cost-charged
 // span before b, and of all of them) and its chunk plan over the decode grid;
 // every thread of the CTA must call it. P <= 1: nothing to merge.
-__device__ __forceinline__ void unit_layout(const DecodeParams& p, int u, long long (&s_red)[2][8], int& P,
+template <int NW>
+__device__ __forceinline__ void unit_layout(const DecodeParams& p, int u, long long (&s_red)[2][NW], int& P,
                                             long long& slot0, long long& slot_base, int& step) {
   const int b = u / p.hgn, grp = u % p.hgn;
   int L, t0, n, q0, qn;
@@ -1345,24 +1346,25 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams& p, int P, long 
 // the decode kernel with programmatic dependent launch: its CTAs may start
 // while the decode grid drains and wait in griddepcontrol.wait until that grid
 // has completed and its writes are visible.
-//   grid (units, C, heads per tile), 256 threads: CTA (u, c, z) merges
+//   grid (units, C, heads per tile), NT threads (256, or 512 for the
+//   batch-8 kernel when a CTA holds more than 256 items): CTA (u, c, z) merges
 //   head z of unit u for output dims [c*D/C, (c+1)*D/C); the host picks
 //   C = D/8 (16 or more pieces per unit), D/32 (4 or more) or 1, halved
-//   while the grid exceeds one CTA per SM. An item is (row, 4 dims). With more than 256 items a
+//   while the grid exceeds one CTA per SM. An item is (row, 4 dims). With more than NT items a
 //   thread merges its items' pieces in order with a running max; with fewer,
 //   thread t covers item t % items for pieces pg, pg+PG, ... (pg = t / items,
-//   PG = 256 / items) and the PG partial states are then merged in pg order.
+//   PG = NT / items) and the PG partial states are then merged in pg order.
 //   Either way the result does not depend on scheduling; NB pieces' partials
 //   are loaded at a time (the host takes NB = 8 when units have more than
 //   four pieces, else 4, whose kernel needs fewer registers). The unit's pieces
 //   and their slots are derived from the sequence lengths (inputs the decode
 //   kernel does not write) before the wait, so that the first global read
 //   after it is already a partial.
-template <int D, int NB>
-__global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p) {
-  __shared__ float s_m[256], s_l[256];
-  __shared__ float4 s_o[256];
-  __shared__ long long s_red[2][8];
+template <int D, int NB, int NT>
+__global__ void __launch_bounds__(NT) split_combine_kernel(const DecodeParams p) {
+  __shared__ float s_m[NT], s_l[NT];
+  __shared__ float4 s_o[NT];
+  __shared__ long long s_red[2][NT / 32];
   // the next launch in the stream may be scheduled now (it waits for this
   // grid in its own griddepcontrol.wait before touching global memory): its
   // CTAs take the SMs the decode grid leaves while this grid, resident beside
@@ -1403,9 +1405,9 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
     *reinterpret_cast<uint2*>(dst) = o2;
   };
 
-  if (items > 256) {
+  if (items > NT) {
     // many items, few pieces each: one thread per item, all pieces in order
-    for (int item = t; item < items; item += 256) {
+    for (int item = t; item < items; item += NT) {
       const int r = item / slices, dim0 = blockIdx.y * dims_cta + (item % slices) * 4;
       if (r >= live_rows) continue;
       float m_run = -INFINITY, l_run = 0.f;
@@ -1417,7 +1419,7 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const DecodeParams p
   }
   // few items, possibly many pieces: PG thread groups take interleaved
   // pieces, then the groups merge in group order (deterministic)
-  const int PG = 256 / items;
+  const int PG = NT / items;
   const int item = t % items, pg = t / items;
   const int r = item / slices, dim0 = blockIdx.y * dims_cta + (item % slices) * 4;
   const bool live = r < live_rows;

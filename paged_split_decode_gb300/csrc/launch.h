@@ -34,9 +34,9 @@ cudaError_t launch_decode(int D, int kv, int nt, int grouped, const CUtensorMap&
 // Split combine behind a decode launch (split_combine.cu); each split unit's
 // output dims are spread over dim_chunks CTAs per head (a divisor of D / 4);
 // batch > 4 selects the kernel that loads eight pieces' partials at a time
-// (else four).
+// (else four), and with it threads > 256 its 512-thread form.
 cudaError_t launch_split_combine(int D, const DecodeParams& p, int n_units, int dim_chunks, int batch,
-                                 cudaStream_t stream);
+                                 int threads, cudaStream_t stream);
 
 // Per-dtype/head-size entry points defined in decode_*.cu.
 bool shape_f16_d128(int nt, int grouped, KernelShape* out);

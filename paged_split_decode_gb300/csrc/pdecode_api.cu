@@ -405,7 +405,11 @@ pd_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     // e4m3 B = 32 52.3 -> 50.8 us, B = 8 28.2 -> 27.9, B = 3 16.6 -> 16.4 with
     // eight; the headline's ~3.4 pieces per unit 0.3 us slower with eight)
     const int batch = per_unit > 4 ? 8 : 4;
-    e = launch_split_combine(dims->D, p, static_cast<int>(pl.n_merge), chunks, batch,
+    // a CTA's items (row, 4 dims) beyond 256: the batch-8 kernel's 512-thread
+    // form gives each thread one item (e4m3 / int8 B = 32: 384 items)
+    const long long items = static_cast<long long>(p.R) * (dims->D / chunks / 4);
+    const int threads = items > 256 ? 512 : 256;
+    e = launch_split_combine(dims->D, p, static_cast<int>(pl.n_merge), chunks, batch, threads,
                              static_cast<cudaStream_t>(stream));
   }
   return e == cudaSuccess ? PD_OK : PD_ERR_CUDA;
